@@ -1,0 +1,366 @@
+#!/usr/bin/env python3
+"""Benchmark of the whole block-sparse attention hot path on GB300.
+
+One step = reorder Q, K, V into video tiles -> mean-pooled (or low-rank) block
+scores -> Top-p/Top-k selection into a per-head CSR -> KV demand of P query
+partitions with the gather -> block-sparse attention forward (and, for the
+training workload, the backward) -> outputs back to raster order.
+
+Default workload: the Wan-14B attention-layer shape (B=1, H=40, d=128,
+30,720 tokens in 2x8x8 tiles, Top-p 0.95, floor 8, P = 8), bf16, synthetic
+seeded inputs. Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload wan|skewed|training|medium|tiny]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores, same metric
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "block-sparse attn effective TFLOP/s at 32K video tokens; % of bf16 TC peak"
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def attn_flops(nnz: int, wl) -> float:
+    """Algorithmic forward flops over the selected blocks: QK^T and PV, 2 flops per MAC."""
+    return 4.0 * nnz * wl.Bt * wl.Bt * wl.d
+
+
+def bwd_flops(nnz: int, wl) -> float:
+    """FlashAttention convention for the backward: 2.5x the forward (recompute counted)."""
+    return 10.0 * nnz * wl.Bt * wl.Bt * wl.d
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={CLOCK_FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names[1:], parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def cpu_baseline(wl, data, budget_s: float = 12.0) -> dict:
+    """The oracle, as it stands, on a bounded sample of the same workload: the
+    whole forward chain for head 0 (reorder, scores, selection, demand) and
+    attention for that head's query blocks in longest-first order until the
+    time budget is spent. Value = attention flops done / total time."""
+    from oracle import sparsp_oracle as orc
+    g = orc.grid_of(wl)
+    g1 = orc.Grid(1, 1, g.T, g.Y, g.X, g.d, g.ta, g.tb, g.tc)
+    sub = {x: np.ascontiguousarray(data[x][:1, :, :1, :]) for x in ("q", "k", "v")}
+    t0 = time.perf_counter()
+    qb, kb, vb = (orc.reorder(sub[x], g1) for x in ("q", "k", "v"))
+    if wl.estimator == "lowrank":
+        S = orc.scores_lowrank(qb, kb, data["wq"][:1], data["wk"][:1], g.Bt)
+    else:
+        S = orc.scores_mean(qb, kb, g.Bt)
+    sel = orc.select(S.astype(np.float32).reshape(-1, g.nb), wl.top_p, wl.k_floor)
+    orc.kv_demand(sel.row_ptr, sel.col_idx, 1, 1, g.nb, wl.P, g.Bt, g.d, wl.elem_bytes, kb, vb)
+    order = orc.lpt_order(sel.row_ptr, 1, 1, g.nb)
+    flops = 0.0
+    done = 0
+    scale = 1.0 / math.sqrt(g.d)
+    for it in order:
+        orc.attn_fwd_row(qb, kb, vb, sel.row_ptr, sel.col_idx, g.Bt, scale, 0, 0, int(it))
+        flops += attn_flops(int(sel.row_ptr[it + 1] - sel.row_ptr[it]), wl)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    threads = os.cpu_count()
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        if info:
+            threads = max(int(x.get("num_threads", 1)) for x in info)
+    except Exception:
+        pass
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"head 0 of {wl.name}: reorder, scores, selection, demand+gather, then attention for "
+                      f"{done}/{g.nb} query blocks in longest-first order; {dt:.1f} s",
+            "seconds": dt}
+
+
+def run_reference(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    data = synth.make(wl)
+    per_step = []
+    cb = None
+    for _ in range(args.warmup + args.steps):
+        cb = cpu_baseline(wl, data, budget_s=max(2.0, min(20.0, 150.0 / max(1, args.warmup + args.steps))))
+        per_step.append(cb)
+    timed = per_step[args.warmup:]
+    val = statistics.median(x["value"] for x in timed)
+    secs = sum(x["seconds"] for x in timed)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / len(timed),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.name, "parallelism": "host cores"},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cb["cores"], "kind": "oracle",
+                             "sample": cb["sample"]},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="wan", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--flat", action="store_true", help="flat (cross-head) longest-first order")
+    ap.add_argument("--portable", action="store_true", help="mma.sync attention kernel")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+
+    import torch
+    import torch.distributed as dist
+
+    import block_sparse_attention_token_gb300 as sp
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    data = synth.make(wl)
+    shape = sp.shape_of(wl)
+    flags = (sp.SCHED_FLAT if args.flat else 0) | (sp.KERNEL_PORTABLE if args.portable else 0)
+    pipe = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P, backward=wl.backward, flags=flags)
+    tdt = shape.torch_dtype
+    host_in = {x: torch.from_numpy(data[x]).to(tdt).pin_memory() for x in ("q", "k", "v")}
+    dev_in = {x: host_in[x].cuda() for x in host_in}
+    kw = {}
+    if wl.estimator == "lowrank":
+        kw = {"wq": torch.from_numpy(data["wq"]).cuda(), "wk": torch.from_numpy(data["wk"]).cuda()}
+    dout = None
+    if wl.backward:
+        host_in["do"] = torch.from_numpy(data["do"]).to(tdt).pin_memory()
+        dout = host_in["do"].cuda()
+    stream = torch.cuda.current_stream()
+
+    def step(mark=None, prof=False):
+        pipe.forward(dev_in["q"], dev_in["k"], dev_in["v"], prof=prof, mark=mark, **kw)
+        if wl.backward:
+            pipe.backward(dout, prof=prof, mark=mark)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if pipe.status.item() != 0:
+        raise SystemExit(f"device status {sp.status_string(pipe.status.item())}")
+    nnz = int(pipe.row_ptr[-1].item())
+    demanded, all_bytes = (int(x) for x in pipe.demand.bytes[:2].tolist())
+
+    # ---- timed region: K steps, events around every stage
+    marks = []
+
+    def mark(name):
+        ev = torch.cuda.Event(enable_timing=True)
+        ev.record(stream)
+        marks.append((name, ev))
+
+    clocks = ClockSampler(local)
+    time.sleep(0.5)
+    barrier()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(args.steps):
+        mark("step_start")
+        step(mark=mark)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(end)
+    stage_ms = {}
+    prev = None
+    for name, ev in marks:
+        if prev is not None and name != "step_start":
+            stage_ms[name] = stage_ms.get(name, 0.0) + prev.elapsed_time(ev)
+        prev = ev
+    stage_ms = {k: v / args.steps for k, v in stage_ms.items()}
+    ms_step = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    pk = peaks()
+    f_fwd = attn_flops(nnz, wl)
+    f_step = f_fwd + (bwd_flops(nnz, wl) if wl.backward else 0.0)
+    value = world * f_step / (ms_step * 1e-3) / 1e12
+    attn_ms = stage_ms["attn_fwd"]
+    achieved = f_fwd / (attn_ms * 1e-3) / 1e12
+    peak = pk["bf16_tflops_sustained"]
+    roofline = {"bound": "tensor", "kernel": "attn_fwd", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_kind": f"bf16 sustained ({pk['source']})",
+                "frac_of_burst": achieved / pk["bf16_tflops"], "traffic": None,
+                "work": f"4*nnz*Bt^2*d = {f_fwd:.4g} flop per launch (nnz={nnz})"}
+    if wl.backward:
+        roofline["bwd_achieved"] = bwd_flops(nnz, wl) / (stage_ms["attn_bwd"] * 1e-3) / 1e12
+
+    # ---- end to end through the public API: pinned host -> device, step, O -> pinned host
+    e2e = None
+    if not args.no_e2e:
+        host_out = torch.empty(pipe.o.shape, dtype=tdt).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = host_out.numel() * host_out.element_size()
+        if wl.backward:
+            host_grads = [torch.empty(pipe.o.shape, dtype=tdt).pin_memory() for _ in range(3)]
+            d2h += 3 * host_out.numel() * host_out.element_size()
+
+        def e2e_step():
+            for x in ("q", "k", "v"):
+                dev_in[x].copy_(host_in[x], non_blocking=True)
+            if wl.backward:
+                dout.copy_(host_in["do"], non_blocking=True)
+            step()
+            host_out.copy_(pipe.o, non_blocking=True)
+            if wl.backward:
+                for hg, g in zip(host_grads, (pipe.dq, pipe.dk, pipe.dv)):
+                    hg.copy_(g, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / args.steps
+        if world > 1:
+            t = torch.tensor([e2e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * f_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    # per-SM busy imbalance of the attention kernel (one extra profiled step, untimed)
+    pipe.prof.zero_()
+    pipe.forward(dev_in["q"], dev_in["k"], dev_in["v"], prof=True, **kw)
+    torch.cuda.synchronize()
+    busy = pipe.prof.cpu().numpy().astype(np.float64)
+    busy = busy[busy > 0]
+    imbalance = float(busy.max() / busy.mean()) if len(busy) else None
+
+    launches = args.steps * (pipe.kernels_per_forward() + (pipe.kernels_per_backward() if wl.backward else 0))
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(wl, data)
+        cpu.pop("seconds", None)
+    counts = np.diff(pipe.row_ptr.cpu().numpy())
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
+        "pct_of_peak": 100.0 * value / world / peak,
+        "tokens_per_s": world * wl.B * wl.N / (ms_step * 1e-3),
+        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d, "tile": [wl.ta, wl.tb, wl.tc],
+                   "nb": shape.nb, "estimator": wl.estimator, "top_p": wl.top_p, "k_floor": wl.k_floor, "P": wl.P,
+                   "backward": wl.backward, "nnz_blocks": nnz, "density": nnz / (shape.rows * shape.nb),
+                   "row_len_min_max": [int(counts.min()), int(counts.max())],
+                   "schedule": "flat" if args.flat else "head-grouped longest-first",
+                   "kernel": "portable mma.sync" if args.portable else "default",
+                   "l2": f"inputs larger than L2 ({shape.B * shape.H * shape.N * shape.d * 2 / 1e6:.0f} MB per tensor)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "stages_ms": stage_ms,
+        "kv_bytes": {"demanded": demanded, "all": all_bytes},
+        "attn_sm_imbalance": imbalance,
+        "clocks": clk, "e2e": e2e, "gpu_launches": launches, "roofline": roofline, "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,301 @@
+"""Python binding of libsparsp (ctypes): dynamic per-head block-sparse attention
+for 3D video-DiT token sequences on one GB300.
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+PyTorch supplies device memory and the current CUDA stream. There is no CPU
+fallback: if the library cannot be loaded, every call raises.
+
+Calls mirror the C ABI in include/sparsp.h (same names, without the prefix).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libsparsp.so")
+
+OK, INVALID_ARG, UNSUPPORTED, SHAPE, ALIGN, WORKSPACE, CAPACITY, DATA, CUDA, TIMEOUT = range(10)
+F32, BF16 = 0, 1
+EST_MEAN, EST_LOWRANK = 0, 1
+SCHED_FLAT = 1
+KERNEL_PORTABLE = 2
+PROF_SLOTS = 1024
+
+
+class SparspError(RuntimeError):
+    def __init__(self, call: str, status: int):
+        self.status = status
+        super().__init__(f"{call} failed: {status_string(status)} ({status})")
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("B", "H", "T", "Y", "X", "d", "ta", "tb", "tc", "dtype")]
+
+    @property
+    def N(self):
+        return self.T * self.Y * self.X
+
+    @property
+    def Bt(self):
+        return self.ta * self.tb * self.tc
+
+    @property
+    def nb(self):
+        return self.N // self.Bt
+
+    @property
+    def rows(self):
+        return self.B * self.H * self.nb
+
+    @property
+    def torch_dtype(self):
+        return torch.float32 if self.dtype == F32 else torch.bfloat16
+
+
+def make_shape(B, H, T, Y, X, d, ta, tb, tc, dtype) -> Shape:
+    if isinstance(dtype, str):
+        dtype = F32 if dtype in ("f32", "float32") else BF16
+    return Shape(B, H, T, Y, X, d, ta, tb, tc, dtype)
+
+
+def shape_of(wl) -> Shape:
+    """Shape of a workload description with fields B, H, T, Y, X, d, ta, tb, tc, dtype."""
+    return make_shape(wl.B, wl.H, wl.T, wl.Y, wl.X, wl.d, wl.ta, wl.tb, wl.tc, wl.dtype)
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_SIG = {
+    "sparsp_status_string": (ctypes.c_char_p, [_I32]),
+    "sparsp_version": (_I32, []),
+    "sparsp_device_sm_count": (_I32, []),
+    "sparsp_reorder": (_I32, [_P, _P, _P, _I32, _P]),
+    "sparsp_block_scores_workspace_size": (ctypes.c_size_t, [_P, _I32, _I32]),
+    "sparsp_block_scores": (_I32, [_P, _I32, _P, _P, _P, _P, _I32, _P, _P, ctypes.c_size_t, _P]),
+    "sparsp_select_workspace_size": (ctypes.c_size_t, [_P]),
+    "sparsp_select": (_I32, [_P, _P, ctypes.c_float, _I32, _P, _P, _P, ctypes.c_size_t, _P, _P]),
+    "sparsp_kv_demand": (_I32, [_P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int64, _P, _P, _P]),
+    "sparsp_lpt_workspace_size": (ctypes.c_size_t, [_P]),
+    "sparsp_lpt_schedule": (_I32, [_P, _P, ctypes.c_uint32, _P, _P, ctypes.c_size_t, _P]),
+    "sparsp_attn_workspace_size": (ctypes.c_size_t, [_P, _I32]),
+    "sparsp_attn_fwd": (_I32, [_P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, ctypes.c_size_t,
+                               ctypes.c_uint32, _P, _P, _P]),
+    "sparsp_attn_bwd": (_I32, [_P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P,
+                               ctypes.c_size_t, ctypes.c_uint32, _P, _P, _P]),
+    "sparsp_csr_transpose": (_I32, [_P, _P, _P, _P, _P, _P, _P]),
+    "sparsp_diag_umma_tile": (_I32, [_P, _P, _P, _I32, _I32, _I32, _P]),
+}
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libsparsp.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+        h = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIG.items():
+            fn = getattr(h, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = h
+    return _lib
+
+
+def status_string(st: int) -> str:
+    return lib().sparsp_status_string(int(st)).decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _check(name, st):
+    if st != OK:
+        raise SparspError(name, st)
+
+
+def _sref(shape: Shape):
+    return ctypes.byref(shape)
+
+
+def _empty(n_bytes: int, device) -> torch.Tensor:
+    return torch.empty(max(int(n_bytes), 16), dtype=torch.uint8, device=device)
+
+
+# ----------------------------------------------------------------- step 1
+
+def reorder(shape: Shape, x: torch.Tensor, out: torch.Tensor | None = None, inverse: bool = False,
+            stream=None) -> torch.Tensor:
+    """Raster [B,N,H,d] -> blocked [B,H,N,d] (or back with inverse=True)."""
+    if out is None:
+        dims = (shape.B, shape.N, shape.H, shape.d) if inverse else (shape.B, shape.H, shape.N, shape.d)
+        out = torch.empty(dims, dtype=x.dtype, device=x.device)
+    _check("sparsp_reorder", lib().sparsp_reorder(_sref(shape), _ptr(x), _ptr(out), int(inverse), _stream(stream)))
+    return out
+
+
+# ----------------------------------------------------------------- step 2
+
+def block_scores_workspace_size(shape, estimator=EST_MEAN, rank=16) -> int:
+    return lib().sparsp_block_scores_workspace_size(_sref(shape), estimator, rank)
+
+
+def block_scores(shape: Shape, q, k, estimator=EST_MEAN, wq=None, wk=None, rank=16, out=None, ws=None,
+                 stream=None) -> torch.Tensor:
+    if out is None:
+        out = torch.empty((shape.B, shape.H, shape.nb, shape.nb), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = _empty(block_scores_workspace_size(shape, estimator, rank), q.device)
+    _check("sparsp_block_scores", lib().sparsp_block_scores(
+        _sref(shape), estimator, _ptr(q), _ptr(k), _ptr(wq), _ptr(wk), rank, _ptr(out), _ptr(ws),
+        ws.numel(), _stream(stream)))
+    return out
+
+
+# ----------------------------------------------------------------- step 3
+
+def select_workspace_size(shape) -> int:
+    return lib().sparsp_select_workspace_size(_sref(shape))
+
+
+def select(shape: Shape, scores, top_p: float, k_floor: int, row_ptr=None, col_idx=None, ws=None,
+           status=None, stream=None):
+    """Returns (row_ptr, col_idx); col_idx has capacity B*H*nb*nb, nnz = row_ptr[-1]."""
+    dev = scores.device
+    if row_ptr is None:
+        row_ptr = torch.empty(shape.rows + 1, dtype=torch.int32, device=dev)
+    if col_idx is None:
+        col_idx = torch.empty(shape.rows * shape.nb, dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = _empty(select_workspace_size(shape), dev)
+    _check("sparsp_select", lib().sparsp_select(
+        _sref(shape), _ptr(scores), float(top_p), int(k_floor), _ptr(row_ptr), _ptr(col_idx), _ptr(ws),
+        ws.numel(), _ptr(status), _stream(stream)))
+    return row_ptr, col_idx
+
+
+# ----------------------------------------------------------------- step 4
+
+@dataclass
+class DemandOut:
+    bitmap: torch.Tensor
+    dem_ptr: torch.Tensor
+    dem_idx: torch.Tensor
+    kg: torch.Tensor | None
+    vg: torch.Tensor | None
+    bytes: torch.Tensor
+
+
+def kv_demand(shape: Shape, P: int, row_ptr, col_idx, k=None, v=None, gather_cap: int | None = None,
+              out: DemandOut | None = None, status=None, stream=None) -> DemandOut:
+    dev = row_ptr.device
+    if out is None:
+        W = (shape.nb + 31) // 32
+        parts = shape.B * shape.H * P
+        kg = vg = None
+        if k is not None:
+            cap = parts * shape.nb if gather_cap is None else gather_cap
+            kg = torch.empty((max(cap, 1), shape.Bt, shape.d), dtype=k.dtype, device=dev)
+            vg = torch.empty_like(kg)
+        out = DemandOut(torch.empty((shape.B, shape.H, P, W), dtype=torch.int32, device=dev),
+                        torch.empty(parts + 1, dtype=torch.int32, device=dev),
+                        torch.empty(parts * shape.nb, dtype=torch.int32, device=dev), kg, vg,
+                        torch.empty(4, dtype=torch.int64, device=dev))
+    cap = 0 if out.kg is None else (out.kg.shape[0] if gather_cap is None else gather_cap)
+    _check("sparsp_kv_demand", lib().sparsp_kv_demand(
+        _sref(shape), int(P), _ptr(row_ptr), _ptr(col_idx), _ptr(out.bitmap), _ptr(out.dem_ptr),
+        _ptr(out.dem_idx), _ptr(k), _ptr(v), _ptr(out.kg), _ptr(out.vg), int(cap), _ptr(out.bytes),
+        _ptr(status), _stream(stream)))
+    return out
+
+
+# ----------------------------------------------------------------- step 5
+
+def lpt_schedule(shape: Shape, row_ptr, flags=0, items=None, stream=None) -> torch.Tensor:
+    dev = row_ptr.device
+    if items is None:
+        items = torch.empty(shape.rows, dtype=torch.int32, device=dev)
+    ws = _empty(lib().sparsp_lpt_workspace_size(_sref(shape)), dev)
+    _check("sparsp_lpt_schedule", lib().sparsp_lpt_schedule(
+        _sref(shape), _ptr(row_ptr), int(flags), _ptr(items), _ptr(ws), ws.numel(), _stream(stream)))
+    return items
+
+
+def csr_transpose(shape: Shape, row_ptr, col_idx, nnz_cap=None, status=None, stream=None):
+    dev = row_ptr.device
+    col_ptr = torch.empty(shape.rows + 1, dtype=torch.int32, device=dev)
+    cap = col_idx.numel() if nnz_cap is None else nnz_cap
+    row_idx = torch.empty(max(cap, 4), dtype=torch.int32, device=dev)
+    _check("sparsp_csr_transpose", lib().sparsp_csr_transpose(
+        _sref(shape), _ptr(row_ptr), _ptr(col_idx), _ptr(col_ptr), _ptr(row_idx), _ptr(status),
+        _stream(stream)))
+    return col_ptr, row_idx
+
+
+def attn_workspace_size(shape: Shape, backward: bool = False) -> int:
+    return lib().sparsp_attn_workspace_size(_sref(shape), int(backward))
+
+
+def attn_fwd(shape: Shape, q, k, v, row_ptr, col_idx, scale: float = 0.0, o=None, lse=None, ws=None,
+             flags: int = 0, prof=None, status=None, stream=None):
+    """Returns (O blocked [B,H,N,d], LSE [B,H,N] fp32)."""
+    dev = q.device
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((shape.B, shape.H, shape.N), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = _empty(attn_workspace_size(shape, False), dev)
+    _check("sparsp_attn_fwd", lib().sparsp_attn_fwd(
+        _sref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(row_ptr), _ptr(col_idx), float(scale), _ptr(o),
+        _ptr(lse), _ptr(ws), ws.numel(), int(flags), _ptr(prof), _ptr(status), _stream(stream)))
+    return o, lse
+
+
+def attn_bwd(shape: Shape, q, k, v, o, lse, dout, row_ptr, col_idx, scale: float = 0.0, dq=None, dk=None,
+             dv=None, ws=None, flags: int = 0, prof=None, status=None, stream=None):
+    """Returns (dQ, dK, dV), blocked [B,H,N,d] bf16."""
+    dev = q.device
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if ws is None:
+        ws = _empty(attn_workspace_size(shape, True), dev)
+    _check("sparsp_attn_bwd", lib().sparsp_attn_bwd(
+        _sref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(row_ptr),
+        _ptr(col_idx), float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), int(flags),
+        _ptr(prof), _ptr(status), _stream(stream)))
+    return dq, dk, dv
+
+
+def diag_umma_tile(a: torch.Tensor, b: torch.Tensor, mode: int, lbo: int = 16384, sbo: int = 1024,
+                   stream=None) -> torch.Tensor:
+    """One 128x128x128 bf16 tcgen05 tile product (layout diagnostic, include/sparsp_diag.h)."""
+    d = torch.empty((128, 128), dtype=torch.float32, device=a.device)
+    _check("sparsp_diag_umma_tile", lib().sparsp_diag_umma_tile(_ptr(a), _ptr(b), _ptr(d), int(mode), int(lbo),
+                                                                int(sbo), _stream(stream)))
+    return d
+
+
+def default_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)
+
+
+from .pipeline import Pipeline  # noqa: E402,F401

@@ -1,0 +1,448 @@
+// Step 5a, bf16, Bt = d = 128 on sm_103a: block-sparse flash-attention forward
+// on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// One persistent CTA per SM, 6 warps:
+//   warp 4     producer: pulls (b, h, query block) items longest-first through
+//              an atomic counter, validates the CSR row, publishes the item in
+//              a shared-memory ring, and TMA-loads Q_i and the selected K_j / V_j
+//              tiles (128 x 128 bf16, two 64-column boxes with 128-byte swizzle)
+//              into a 3-stage K ring and a 2-stage V ring, addressed through
+//              the CSR (row coordinate = bh*N + j*128).
+//   warp 5     MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM S
+//              buffers (M=N=128, K=16 per instruction, both operands K-major
+//              from shared memory), issued one block ahead of O += P_j V_j
+//              (A = P_j read from TMEM as packed bf16, B = V_j MN-major from
+//              shared memory). Completion is signalled with tcgen05.commit.
+//   warps 0-3  softmax and epilogue: thread t owns query row t = TMEM lane t.
+//              It reads its S row from TMEM, keeps a running max m and sum l in
+//              base 2, writes P = exp2(S*scale*log2e - m) as bf16 into TMEM, and
+//              rescales its O row in TMEM only when the row max grows by more
+//              than 8 (a factor 256); otherwise the stale max is kept, which
+//              leaves the result unchanged up to rounding because O and l use
+//              the same reference. At the end of the row: O / l to global
+//              memory, LSE = (m + log2 l) ln 2.
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256,384), P0 [384,448),
+// P1 [448,512). Every mbarrier wait is bounded (2 s); on expiry the CTA sets
+// SPARSP_ERR_TIMEOUT, all roles leave their loops, copies and MMAs in flight
+// are drained with a second bounded wait, and TMEM is released.
+#include "tc_helpers.cuh"
+
+namespace sparsp {
+namespace {
+
+using namespace tc;
+
+constexpr int BT = 128, D = 128;
+constexpr int kNK = 3, kNV = 2, kNI = 4;
+constexpr uint32_t kTile = BT * D * 2;      // 32 KB
+constexpr uint32_t kHalfTile = BT * 64 * 2; // one 64-column swizzled box: 16 KB
+constexpr int kThreads = 192;
+constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+constexpr uint32_t kOffK = kTile, kOffV = kOffK + kNK * kTile, kOffBar = kOffV + kNV * kTile;
+enum Bar {
+  Q_FULL = 0, Q_EMPTY, K_FULL, K_EMPTY = K_FULL + kNK, V_FULL = K_EMPTY + kNK, V_EMPTY = V_FULL + kNV,
+  S_FULL = V_EMPTY + kNV, S_FREE = S_FULL + 2, P_FULL = S_FREE + 2, PV_DONE = P_FULL + 2, O_FULL, O_EMPTY,
+  I_FULL, I_EMPTY = I_FULL + kNI, TEAR = I_EMPTY + kNI, NBAR
+};
+constexpr uint32_t kOffRing = kOffBar + 8 * NBAR;
+constexpr uint32_t kOffMisc = kOffRing + 8 * kNI;
+constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kDrainNs = 200000000ull;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+__device__ __forceinline__ bool wait_raw(uint32_t bar, uint32_t parity, uint64_t limit) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > limit) return false;
+  return true;
+}
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+struct Params {
+  const int32_t* row_ptr;
+  const int32_t* col_idx;
+  int64_t N;
+  int nb;
+  int64_t n_items;
+  float scale_log2;
+  __nv_bfloat16* o;
+  float* lse;
+  const int32_t* items;
+  int32_t* counter;
+  uint64_t* prof;
+  int32_t* d_status;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tv, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sQ = base, sK = base + kOffK, sV = base + kOffV;
+  auto bar = [&](int idx) -> uint32_t { return base + kOffBar + 8u * (uint32_t)idx; };
+  volatile int2* ring = reinterpret_cast<volatile int2*>(gbase + kOffRing);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kOffMisc);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + kOffMisc + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t t_start = globaltimer_ns();
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(Q_FULL), 1);
+    mbar_init(bar(Q_EMPTY), 1);
+    for (int s = 0; s < kNK; ++s) {
+      mbar_init(bar(K_FULL + s), 1);
+      mbar_init(bar(K_EMPTY + s), 1);
+    }
+    for (int s = 0; s < kNV; ++s) {
+      mbar_init(bar(V_FULL + s), 1);
+      mbar_init(bar(V_EMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(S_FULL + b), 1);
+      mbar_init(bar(S_FREE + b), 128);
+      mbar_init(bar(P_FULL + b), 128);
+    }
+    mbar_init(bar(PV_DONE), 1);
+    mbar_init(bar(O_FULL), 1);
+    mbar_init(bar(O_EMPTY), 128);
+    for (int r = 0; r < kNI; ++r) {
+      mbar_init(bar(I_FULL + r), 1);
+      mbar_init(bar(I_EMPTY + r), 5);
+    }
+    mbar_init(bar(TEAR), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 4 && lane == 0) {
+    prefetch_tmap(&tq);
+    prefetch_tmap(&tk);
+    prefetch_tmap(&tv);
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Guard g{abort_flag, p.d_status, kWaitNs};
+  const int nb = p.nb;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    uint32_t it_fill = 0, q_fill = 0, k_fill = 0, v_fill = 0;
+    for (;;) {
+      int32_t slot = 0;
+      if (lane == 0) slot = atomicAdd(p.counter, 1);
+      slot = __shfl_sync(0xffffffffu, slot, 0);
+      int32_t item = -1, len = -2;
+      if (slot < p.n_items) {
+        item = p.items[slot];
+        const int32_t a = p.row_ptr[item], b = p.row_ptr[item + 1];
+        bool bad = (b < a) || (b - a > nb);
+        if (!bad)
+          for (int32_t e = a + lane; e < b; e += 32) {
+            const int32_t j = p.col_idx[e];
+            if (j < 0 || j >= nb) bad = true;
+          }
+        bad = __any_sync(0xffffffffu, bad);
+        if (bad) {
+          if (lane == 0) report(p.d_status, SPARSP_ERR_DATA);
+          len = -1;
+        } else {
+          len = b - a;
+        }
+      }
+      const int ri = (int)(it_fill % kNI);
+      if (!wait_warp(bar(I_EMPTY + ri), ((it_fill / kNI) & 1u) ^ 1u, g)) break;
+      if (lane == 0) {
+        ring[ri].x = item;
+        ring[ri].y = len;
+        mbar_arrive(bar(I_FULL + ri));
+      }
+      __syncwarp();
+      ++it_fill;
+      if (len == -2) break;
+      if (len <= 0) continue;
+      const int64_t bh = item / nb;
+      const int i = item % nb;
+      const int32_t yq = (int32_t)(bh * p.N + (int64_t)i * BT);
+      if (!wait_warp(bar(Q_EMPTY), (q_fill & 1u) ^ 1u, g)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(Q_FULL), kTile);
+        tma_load_2d(sQ, &tq, bar(Q_FULL), 0, yq);
+        tma_load_2d(sQ + kHalfTile, &tq, bar(Q_FULL), 64, yq);
+      }
+      ++q_fill;
+      const int32_t e0 = p.row_ptr[item];
+      bool ok = true;
+      for (int e = 0; e < len && ok; ++e) {
+        const int32_t j = p.col_idx[e0 + e];
+        const int32_t yk = (int32_t)(bh * p.N + (int64_t)j * BT);
+        const uint32_t ks = k_fill % kNK;
+        if (!(ok = wait_warp(bar(K_EMPTY + ks), ((k_fill / kNK) & 1u) ^ 1u, g))) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(K_FULL + ks), kTile);
+          tma_load_2d(sK + ks * kTile, &tk, bar(K_FULL + ks), 0, yk);
+          tma_load_2d(sK + ks * kTile + kHalfTile, &tk, bar(K_FULL + ks), 64, yk);
+        }
+        ++k_fill;
+        const uint32_t vs = v_fill % kNV;
+        if (!(ok = wait_warp(bar(V_EMPTY + vs), ((v_fill / kNV) & 1u) ^ 1u, g))) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(V_FULL + vs), kTile);
+          tma_load_2d(sV + vs * kTile, &tv, bar(V_FULL + vs), 0, yk);
+          tma_load_2d(sV + vs * kTile + kHalfTile, &tv, bar(V_FULL + vs), 64, yk);
+        }
+        ++v_fill;
+      }
+      if (!ok) break;
+    }
+    if (*abort_flag && lane == 0) {
+      // drain copies still in flight before the shared memory goes away
+      if (q_fill) wait_raw(bar(Q_FULL), (q_fill - 1) & 1u, kDrainNs);
+      for (uint32_t s = 0; s < kNK; ++s)
+        if (k_fill > s) wait_raw(bar(K_FULL + s), ((k_fill - 1 - s) / kNK) & 1u, kDrainNs);
+      for (uint32_t s = 0; s < kNV; ++s)
+        if (v_fill > s) wait_raw(bar(V_FULL + s), ((v_fill - 1 - s) / kNV) & 1u, kDrainNs);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
+      constexpr uint32_t idO = idesc_bf16(128, 128, 0, 1);
+      uint32_t it_use = 0, q_use = 0, k_use = 0, v_use = 0, s_issue = 0, pv = 0, o_items = 0;
+      bool issued_any = false;
+      auto issue_s = [&]() -> bool {
+        const uint32_t b = s_issue & 1u, ks = k_use % kNK;
+        if (!wait(bar(S_FREE + b), ((s_issue >> 1) & 1u) ^ 1u, g)) return false;
+        if (!wait(bar(K_FULL + ks), (k_use / kNK) & 1u, g)) return false;
+        fence_after();
+        const uint32_t kb = sK + ks * kTile;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
+          mma_ss(tmem + kColS + b * 128u, smem_desc(sQ + off, 16, 1024, kSwizzle128B),
+                 smem_desc(kb + off, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
+        }
+        commit(bar(S_FULL + b));
+        commit(bar(K_EMPTY + ks));
+        ++s_issue;
+        ++k_use;
+        issued_any = true;
+        return true;
+      };
+      for (;;) {
+        const int ri = (int)(it_use % kNI);
+        if (!wait(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
+        const int2 ent = make_int2(ring[ri].x, ring[ri].y);
+        mbar_arrive(bar(I_EMPTY + ri));
+        ++it_use;
+        if (ent.y == -2) break;
+        if (ent.y <= 0) continue;
+        const int len = ent.y;
+        if (!wait(bar(Q_FULL), q_use & 1u, g)) break;
+        ++q_use;
+        bool ok = issue_s();
+        for (int e = 0; e < len && ok; ++e) {
+          if (e + 1 < len) {
+            if (!(ok = issue_s())) break;
+          } else {
+            commit(bar(Q_EMPTY));   // every S of this item is issued: Q may be replaced
+          }
+          const uint32_t b = pv & 1u, vs = v_use % kNV;
+          if (!(ok = wait(bar(V_FULL + vs), (v_use / kNV) & 1u, g))) break;
+          if (!(ok = wait(bar(P_FULL + b), (pv >> 1) & 1u, g))) break;
+          if (e == 0 && !(ok = wait(bar(O_EMPTY), (o_items & 1u) ^ 1u, g))) break;
+          fence_after();
+          const uint32_t vb = sV + vs * kTile;
+#pragma unroll
+          for (int kk = 0; kk < BT / 16; ++kk)
+            mma_ts(tmem + kColO, tmem + kColP + b * 64u + (uint32_t)kk * 8u,
+                   smem_desc(vb + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), idO,
+                   (e > 0 || kk > 0) ? 1u : 0u);
+          commit(bar(V_EMPTY + vs));
+          commit(bar(PV_DONE));
+          ++v_use;
+          ++pv;
+        }
+        if (!ok) break;
+        commit(bar(O_FULL));
+        ++o_items;
+      }
+      if (*abort_flag && issued_any) {
+        commit(bar(TEAR));
+        wait_raw(bar(TEAR), 0, kDrainNs);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t t_row = tmem + lane_base;
+    uint32_t it_use = 0, s_use = 0, o_items = 0;
+    uint64_t blocks_done = 0;
+    const float sl2 = p.scale_log2;
+    for (;;) {
+      const int ri = (int)(it_use % kNI);
+      if (!wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
+      const int2 ent = make_int2(ring[ri].x, ring[ri].y);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
+      ++it_use;
+      if (ent.y == -2) break;
+      if (ent.y == -1) continue;
+      const int64_t item = ent.x;
+      const int64_t bh = item / nb;
+      const int i = (int)(item % nb);
+      const int64_t row = bh * p.N + (int64_t)i * BT + threadIdx.x;
+      uint4* orow = reinterpret_cast<uint4*>(p.o + row * D);
+      const int len = ent.y;
+      if (len == 0) {
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
+        p.lse[row] = -INFINITY;
+        continue;
+      }
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int e = 0; e < len; ++e) {
+        const uint32_t b = s_use & 1u;
+        if (!(ok = wait_warp(bar(S_FULL + b), (s_use >> 1) & 1u, g))) break;
+        fence_after();
+        uint32_t s[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(t_row + kColS + b * 128u + c * 32u, s + 32 * c);
+        wait_ld();
+        fence_before();
+        mbar_arrive(bar(S_FREE + b));
+        ++s_use;
+        float mx = __uint_as_float(s[0]);
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+        const float m_new = fmaxf(m, mx * sl2);
+        bool waited = false;
+        if (e == 0) {
+          m = m_new;
+        } else if (__any_sync(0xffffffffu, m_new > m + kRescaleThreshold)) {
+          if (!(ok = wait_warp(bar(PV_DONE), (uint32_t)((blocks_done + e - 1) & 1u), g))) break;
+          waited = true;
+          fence_after();
+          const float f = ex2f(m - m_new);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(t_row + kColO + c * 32u, o);
+            wait_ld();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * f);
+            tmem_st32(t_row + kColO + c * 32u, o);
+          }
+          wait_st();
+          l *= f;
+          m = m_new;
+        }
+        uint32_t pk[64];
+        float rs = 0.f;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float p0 = ex2f(fmaf(__uint_as_float(s[2 * c]), sl2, -m));
+          const float p1 = ex2f(fmaf(__uint_as_float(s[2 * c + 1]), sl2, -m));
+          rs += p0 + p1;
+          pk[c] = pack2(p0, p1);
+        }
+        l += rs;
+        if (e > 0 && !waited) {
+          if (!(ok = wait_warp(bar(PV_DONE), (uint32_t)((blocks_done + e - 1) & 1u), g))) break;
+          fence_after();
+        }
+        tmem_st32(t_row + kColP + b * 64u, pk);
+        tmem_st32(t_row + kColP + b * 64u + 32u, pk + 32);
+        wait_st();
+        fence_before();
+        mbar_arrive(bar(P_FULL + b));
+      }
+      if (!ok) break;
+      blocks_done += (uint64_t)len;
+      if (!wait_warp(bar(O_FULL), o_items & 1u, g)) break;
+      ++o_items;
+      fence_after();
+      const float inv = 1.0f / l;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(t_row + kColO + c * 32u, o);
+        wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x)
+          w[x] = pack2(__uint_as_float(o[2 * x]) * inv, __uint_as_float(o[2 * x + 1]) * inv);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) orow[c * 4 + x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+      }
+      fence_before();
+      mbar_arrive(bar(O_EMPTY));
+      p.lse[row] = (m + log2f(l)) * 0.69314718055994531f;
+    }
+  }
+
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 5) tmem_dealloc(tmem, 512);
+  if (p.prof != nullptr && threadIdx.x == 0)
+    atomicAdd((unsigned long long*)&p.prof[smid() % SPARSP_PROF_SLOTS],
+              (unsigned long long)(globaltimer_ns() - t_start));
+}
+
+}  // namespace
+
+bool attn_fwd_tc_supported(const Dims& s) {
+  if (s.dtype != SPARSP_BF16 || s.Bt != 128 || s.d != 128) return false;
+  if ((int64_t)s.B * s.H * s.N >= (int64_t)1 << 31) return false;
+  int dev = 0, major = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return false;
+  return major == 10;
+}
+
+sparsp_status_t launch_attn_fwd_tc(const Dims& s, const __nv_bfloat16* q, const __nv_bfloat16* k,
+                                   const __nv_bfloat16* v, const int32_t* row_ptr,
+                                   const int32_t* col_idx, float scale, __nv_bfloat16* o,
+                                   float* lse, const int32_t* items, int32_t* counter,
+                                   uint64_t* prof, int32_t* d_status, cudaStream_t st) {
+  const uint64_t rows = (uint64_t)s.B * s.H * s.N;
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_bf16_rows(&tq, q, rows, D, BT) || !make_tmap_bf16_rows(&tk, k, rows, D, BT) ||
+      !make_tmap_bf16_rows(&tv, v, rows, D, BT))
+    return SPARSP_ERR_CUDA;
+  if (cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kSmemBytes) != cudaSuccess)
+    return SPARSP_ERR_CUDA;
+  const int sms = device_sm_count();
+  if (sms <= 0) return SPARSP_ERR_CUDA;
+  int64_t grid = sms;
+  if (grid > s.rows()) grid = s.rows();
+  if (grid < 1) grid = 1;
+  Params prm{row_ptr, col_idx, s.N, s.nb, s.rows(), scale * 1.4426950408889634f, o, lse, items,
+             counter, prof, d_status};
+  attn_fwd_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, prm);
+  SPARSP_LAUNCH_CHECK();
+  return SPARSP_OK;
+}
+
+}  // namespace sparsp

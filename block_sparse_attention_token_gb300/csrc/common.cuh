@@ -1,0 +1,118 @@
+// Shared internals of libsparsp: derived shape, status reporting, launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "sparsp.h"
+
+namespace sparsp {
+
+// Derived shape, validated by the API layer before any launcher sees it.
+struct Dims {
+  int B, H, T, Y, X, d, ta, tb, tc, dtype;
+  int64_t N;      // tokens per (b, h)
+  int Bt;         // tokens per tile
+  int nb;         // tiles per (b, h)
+  int nT, nY, nX; // tile lattice
+  int elem;       // bytes per element
+  int64_t rows() const { return (int64_t)B * H * nb; }  // CSR rows = work items
+};
+
+// First-error-wins device status word.
+__device__ __forceinline__ void report(int32_t* st, int32_t code) {
+  if (st != nullptr) atomicCAS(st, 0, code);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smid() {
+  uint32_t s;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(s));
+  return s;
+}
+
+// Launch-side helpers -------------------------------------------------------
+
+int device_sm_count();   // cached per device; -1 on error
+
+#define SPARSP_LAUNCH_CHECK()                                       \
+  do {                                                              \
+    cudaError_t e_ = cudaGetLastError();                            \
+    if (e_ != cudaSuccess) return SPARSP_ERR_CUDA;                  \
+  } while (0)
+
+// Launchers (each returns SPARSP_OK or SPARSP_ERR_CUDA). -------------------
+
+sparsp_status_t launch_reorder(const Dims& s, const void* in, void* out, bool inverse,
+                               cudaStream_t st);
+
+sparsp_status_t launch_block_scores(const Dims& s, int estimator, const void* q, const void* k,
+                                    const float* wq, const float* wk, int rank, float* scores,
+                                    void* ws, cudaStream_t st);
+size_t block_scores_ws(const Dims& s, int estimator, int rank);
+
+sparsp_status_t launch_select(const Dims& s, const float* scores, float top_p, int k_floor,
+                              int32_t* row_ptr, int32_t* col_idx, void* ws, int32_t* d_status,
+                              cudaStream_t st);
+size_t select_ws(const Dims& s);
+
+sparsp_status_t launch_kv_demand(const Dims& s, int P, const int32_t* row_ptr,
+                                 const int32_t* col_idx, uint32_t* bitmap, int32_t* dem_ptr,
+                                 int32_t* dem_idx, const void* k, const void* v, void* kg,
+                                 void* vg, int64_t cap, uint64_t* bytes, int32_t* d_status,
+                                 cudaStream_t st);
+
+size_t lpt_ws(const Dims& s);
+sparsp_status_t launch_lpt(const Dims& s, const int32_t* row_ptr, bool flat, int32_t* items,
+                           int32_t* counter, void* ws, cudaStream_t st);
+
+// Exclusive scan in place of n+1 int32 entries: a[0..n) counts -> offsets,
+// a[n] = total. `base` (may be null) is added to every output.
+sparsp_status_t launch_scan_counts(int32_t* a, int64_t n, cudaStream_t st);
+
+sparsp_status_t launch_csr_transpose(const Dims& s, const int32_t* row_ptr, const int32_t* col_idx,
+                                     int32_t* col_ptr, int32_t* row_idx, int32_t* d_status,
+                                     cudaStream_t st);
+
+// Attention forward variants. `items` is the work order, `counter` a zeroed
+// int32 that persistent CTAs pull from.
+sparsp_status_t launch_attn_fwd_f32(const Dims& s, const float* q, const float* k, const float* v,
+                                    const int32_t* row_ptr, const int32_t* col_idx, float scale,
+                                    float* o, float* lse, const int32_t* items, int32_t* counter,
+                                    uint64_t* prof, int32_t* d_status, cudaStream_t st);
+sparsp_status_t launch_attn_fwd_mma(const Dims& s, const __nv_bfloat16* q, const __nv_bfloat16* k,
+                                    const __nv_bfloat16* v, const int32_t* row_ptr,
+                                    const int32_t* col_idx, float scale, __nv_bfloat16* o,
+                                    float* lse, const int32_t* items, int32_t* counter,
+                                    uint64_t* prof, int32_t* d_status, cudaStream_t st);
+bool attn_fwd_tc_supported(const Dims& s);
+sparsp_status_t launch_attn_fwd_tc(const Dims& s, const __nv_bfloat16* q, const __nv_bfloat16* k,
+                                   const __nv_bfloat16* v, const int32_t* row_ptr,
+                                   const int32_t* col_idx, float scale, __nv_bfloat16* o,
+                                   float* lse, const int32_t* items, int32_t* counter,
+                                   uint64_t* prof, int32_t* d_status, cudaStream_t st);
+
+// Attention backward pieces.
+sparsp_status_t launch_bwd_rowdot(const Dims& s, const __nv_bfloat16* o, const __nv_bfloat16* dout,
+                                  float* delta, cudaStream_t st);
+sparsp_status_t launch_attn_bwd_dq(const Dims& s, const __nv_bfloat16* q, const __nv_bfloat16* k,
+                                   const __nv_bfloat16* v, const __nv_bfloat16* dout,
+                                   const float* lse, const float* delta, const int32_t* row_ptr,
+                                   const int32_t* col_idx, float scale, __nv_bfloat16* dq,
+                                   const int32_t* items, int32_t* counter, uint64_t* prof,
+                                   int32_t* d_status, cudaStream_t st);
+sparsp_status_t launch_attn_bwd_dkdv(const Dims& s, const __nv_bfloat16* q,
+                                     const __nv_bfloat16* k, const __nv_bfloat16* v,
+                                     const __nv_bfloat16* dout, const float* lse,
+                                     const float* delta, const int32_t* col_ptr,
+                                     const int32_t* row_idx, float scale, __nv_bfloat16* dk,
+                                     __nv_bfloat16* dv, const int32_t* items, int32_t* counter,
+                                     uint64_t* prof, int32_t* d_status, cudaStream_t st);
+
+}  // namespace sparsp

@@ -1,0 +1,170 @@
+// Step 4: KV demand of P contiguous virtual query partitions.
+//
+//  1. bitmap_kernel - one CTA per partition (b, h, r): the partition's rows
+//     are consecutive CSR rows, so its entries are one contiguous range of
+//     col_idx; each index is OR-ed into a shared bitmap. Writes the bitmap,
+//     its population into dem_ptr[part] and the byte counters.
+//  2. scan          - dem_ptr counts -> offsets.
+//  3. list_kernel   - one warp per partition writes the set bits ascending.
+//  4. gather_kernel - one CTA per demanded slot copies the K and V tiles
+//     (Bt x d, contiguous in the block-ordered layout) with 16-byte vectors;
+//     stores are streaming (the gathered copy is not re-read here), loads keep
+//     the default policy so the P-fold reuse of a source tile hits in L2.
+#include "common.cuh"
+
+namespace sparsp {
+namespace {
+
+constexpr int kMaxWords = 32;   // nb <= 1024
+
+__global__ void __launch_bounds__(256)
+bitmap_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ col_idx, int H,
+              int nb, int P, uint64_t tile2, uint32_t* __restrict__ bitmap,
+              int32_t* __restrict__ counts, uint64_t* __restrict__ bytes, int32_t* d_status) {
+  __shared__ uint32_t bits[kMaxWords];
+  const int part = blockIdx.x;           // (b*H + h)*P + r
+  const int bh = part / P, r = part % P;
+  const int lo = (int)(((int64_t)r * nb) / P), hi = (int)(((int64_t)(r + 1) * nb) / P);
+  const int W = (nb + 31) / 32;
+  if (threadIdx.x < kMaxWords) bits[threadIdx.x] = 0u;
+  __syncthreads();
+  const int64_t row0 = (int64_t)bh * nb + lo, row1 = (int64_t)bh * nb + hi;
+  const int32_t e0 = row_ptr[row0], e1 = row_ptr[row1];
+  if (e1 < e0) {
+    if (threadIdx.x == 0) report(d_status, SPARSP_ERR_DATA);
+  } else {
+    for (int32_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+      const int32_t j = col_idx[e];
+      if (j < 0 || j >= nb) {
+        report(d_status, SPARSP_ERR_DATA);
+        continue;
+      }
+      atomicOr(&bits[j >> 5], 1u << (j & 31));
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int w = threadIdx.x;
+    uint32_t word = w < W ? bits[w] : 0u;
+    if (w < W) bitmap[(int64_t)part * W + w] = word;
+    // blocks of this partition's own range [lo, hi)
+    uint32_t own = 0u;
+    for (int bit = 0; bit < 32; ++bit) {
+      const int j = w * 32 + bit;
+      if (j >= lo && j < hi) own |= 1u << bit;
+    }
+    int total = __popc(word), remote = __popc(word & ~own);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      total += __shfl_xor_sync(0xffffffffu, total, off);
+      remote += __shfl_xor_sync(0xffffffffu, remote, off);
+    }
+    if (w == 0) {
+      counts[part] = total;
+      atomicAdd((unsigned long long*)&bytes[0], (unsigned long long)total * tile2);
+      atomicAdd((unsigned long long*)&bytes[2], (unsigned long long)remote * tile2);
+      atomicAdd((unsigned long long*)&bytes[3], (unsigned long long)(nb - (hi - lo)) * tile2);
+      atomicAdd((unsigned long long*)&bytes[1], (unsigned long long)nb * tile2);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256)
+list_kernel(const uint32_t* __restrict__ bitmap, const int32_t* __restrict__ dem_ptr, int nparts,
+            int W, int32_t* __restrict__ dem_idx) {
+  const int lane = threadIdx.x & 31;
+  const int part = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (part >= nparts) return;
+  uint32_t word = lane < W ? bitmap[(int64_t)part * W + lane] : 0u;
+  int cnt = __popc(word);
+  int incl = cnt;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  int pos = dem_ptr[part] + incl - cnt;
+  while (word) {
+    const int bit = __ffs(word) - 1;
+    dem_idx[pos++] = lane * 32 + bit;
+    word &= word - 1;
+  }
+}
+
+// One CTA per slot < min(total, cap). The owning partition is found by binary
+// search in dem_ptr.
+__global__ void __launch_bounds__(256)
+gather_kernel(const int32_t* __restrict__ dem_ptr, const int32_t* __restrict__ dem_idx, int nparts,
+              int P, int64_t N, int Bt, int vec_per_row, const uint4* __restrict__ k,
+              const uint4* __restrict__ v, uint4* __restrict__ kg, uint4* __restrict__ vg,
+              int64_t cap, int32_t* d_status) {
+  const int64_t total = dem_ptr[nparts];
+  const int64_t slot = blockIdx.x;
+  if (slot == 0 && total > cap && threadIdx.x == 0) report(d_status, SPARSP_ERR_CAPACITY);
+  if (slot >= total || slot >= cap) return;
+  int lo = 0, hi = nparts - 1;   // last part with dem_ptr[part] <= slot
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (dem_ptr[mid] <= slot) lo = mid; else hi = mid - 1;
+  }
+  const int bh = lo / P;
+  const int j = dem_idx[slot];
+  const int64_t nvec = (int64_t)Bt * vec_per_row;
+  const uint4* ks = k + ((int64_t)bh * N + (int64_t)j * Bt) * vec_per_row;
+  const uint4* vs = v + ((int64_t)bh * N + (int64_t)j * Bt) * vec_per_row;
+  uint4* kd = kg + slot * nvec;
+  uint4* vd = vg + slot * nvec;
+  for (int64_t e = threadIdx.x; e < nvec; e += 4 * blockDim.x) {
+    uint4 a[4], b[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t idx = e + u * blockDim.x;
+      if (idx < nvec) {
+        a[u] = ks[idx];
+        b[u] = vs[idx];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t idx = e + u * blockDim.x;
+      if (idx < nvec) {
+        __stcs(kd + idx, a[u]);
+        __stcs(vd + idx, b[u]);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+sparsp_status_t launch_kv_demand(const Dims& s, int P, const int32_t* row_ptr,
+                                 const int32_t* col_idx, uint32_t* bitmap, int32_t* dem_ptr,
+                                 int32_t* dem_idx, const void* k, const void* v, void* kg,
+                                 void* vg, int64_t cap, uint64_t* bytes, int32_t* d_status,
+                                 cudaStream_t st) {
+  const int nparts = s.B * s.H * P;
+  const int W = (s.nb + 31) / 32;
+  const uint64_t tile2 = (uint64_t)s.Bt * s.d * s.elem * 2;
+  if (cudaMemsetAsync(bytes, 0, 4 * sizeof(uint64_t), st) != cudaSuccess) return SPARSP_ERR_CUDA;
+  bitmap_kernel<<<nparts, 256, 0, st>>>(row_ptr, col_idx, s.H, s.nb, P, tile2, bitmap, dem_ptr,
+                                        bytes, d_status);
+  SPARSP_LAUNCH_CHECK();
+  sparsp_status_t r = launch_scan_counts(dem_ptr, nparts, st);
+  if (r != SPARSP_OK) return r;
+  list_kernel<<<(nparts + 7) / 8, 256, 0, st>>>(bitmap, dem_ptr, nparts, W, dem_idx);
+  SPARSP_LAUNCH_CHECK();
+  if (kg != nullptr && vg != nullptr) {
+    // grid >= 1 so that slot 0 can report a capacity shortfall even when cap == 0
+    const int64_t upper = (int64_t)nparts * s.nb;
+    int64_t grid = upper < cap ? upper : cap;
+    if (grid < 1) grid = 1;
+    const int vec_per_row = s.d * s.elem / 16;
+    gather_kernel<<<(unsigned)grid, 256, 0, st>>>(dem_ptr, dem_idx, nparts, P, s.N, s.Bt,
+                                                   vec_per_row, (const uint4*)k, (const uint4*)v,
+                                                   (uint4*)kg, (uint4*)vg, cap, d_status);
+    SPARSP_LAUNCH_CHECK();
+  }
+  return SPARSP_OK;
+}
+
+}  // namespace sparsp

@@ -1,0 +1,198 @@
+// Step 5c: longest-first work order, and the CSR transpose used by the backward.
+//
+// Grouped order (default): heads by total cost descending, then each head's
+// query blocks by row cost descending, so that concurrently running CTAs work
+// on few heads and their K/V stays L2-resident. Flat order: every item by row
+// cost descending. Both break ties by index, so the order is deterministic.
+// Ranks are computed by counting (no sort, no atomics on the output).
+#include "common.cuh"
+
+namespace sparsp {
+namespace {
+
+constexpr int kThreads = 1024;
+
+__global__ void __launch_bounds__(kThreads)
+lpt_grouped_kernel(const int32_t* __restrict__ row_ptr, int BH, int nb, int32_t* __restrict__ items,
+                   int32_t* __restrict__ counter) {
+  __shared__ int32_t cost[1024];
+  __shared__ int32_t head_rank;
+  const int bh = blockIdx.x;
+  if (threadIdx.x == 0) head_rank = 0;
+  const int64_t r0 = (int64_t)bh * nb;
+  for (int i = threadIdx.x; i < nb; i += blockDim.x) cost[i] = row_ptr[r0 + i + 1] - row_ptr[r0 + i];
+  __syncthreads();
+  const int32_t mine = row_ptr[r0 + nb] - row_ptr[r0];
+  int cnt = 0;
+  for (int g = threadIdx.x; g < BH; g += blockDim.x) {
+    const int32_t c = row_ptr[(int64_t)(g + 1) * nb] - row_ptr[(int64_t)g * nb];
+    if (c > mine || (c == mine && g < bh)) ++cnt;
+  }
+  if (cnt) atomicAdd(&head_rank, cnt);
+  __syncthreads();
+  const int64_t slot0 = (int64_t)head_rank * nb;
+  for (int i = threadIdx.x; i < nb; i += blockDim.x) {
+    const int32_t c = cost[i];
+    int rank = 0;
+    for (int i2 = 0; i2 < nb; ++i2) {
+      const int32_t c2 = cost[i2];
+      rank += (c2 > c) || (c2 == c && i2 < i);
+    }
+    items[slot0 + rank] = (int32_t)(r0 + i);
+  }
+  if (bh == 0 && threadIdx.x == 0 && counter != nullptr) *counter = 0;
+}
+
+// Flat order, pass 1: per-head histogram of row costs (0..nb).
+__global__ void __launch_bounds__(kThreads)
+lpt_hist_kernel(const int32_t* __restrict__ row_ptr, int nb, int32_t* __restrict__ hist) {
+  __shared__ int32_t h[1025];
+  const int bh = blockIdx.x;
+  for (int c = threadIdx.x; c <= nb; c += blockDim.x) h[c] = 0;
+  __syncthreads();
+  const int64_t r0 = (int64_t)bh * nb;
+  for (int i = threadIdx.x; i < nb; i += blockDim.x) {
+    int32_t c = row_ptr[r0 + i + 1] - row_ptr[r0 + i];
+    c = c < 0 ? 0 : (c > nb ? nb : c);
+    atomicAdd(&h[c], 1);
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c <= nb; c += blockDim.x) hist[(int64_t)bh * (nb + 1) + c] = h[c];
+}
+
+// Flat order, pass 2: slot = #items with larger cost + #items of equal cost in
+// earlier heads + #rows of equal cost earlier in this head.
+__global__ void __launch_bounds__(kThreads)
+lpt_place_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ hist, int BH,
+                 int nb, int32_t* __restrict__ items, int32_t* __restrict__ counter) {
+  __shared__ int32_t greater[1026];
+  __shared__ int32_t before[1025];
+  __shared__ int32_t cost[1024];
+  const int bh = blockIdx.x;
+  const int64_t r0 = (int64_t)bh * nb;
+  for (int c = threadIdx.x; c <= nb; c += blockDim.x) {
+    int32_t tot = 0, bef = 0;
+    for (int g = 0; g < BH; ++g) {
+      const int32_t v = hist[(int64_t)g * (nb + 1) + c];
+      tot += v;
+      if (g < bh) bef += v;
+    }
+    greater[c] = tot;     // column totals for now
+    before[c] = bef;
+  }
+  for (int i = threadIdx.x; i < nb; i += blockDim.x) {
+    int32_t c = row_ptr[r0 + i + 1] - row_ptr[r0 + i];
+    cost[i] = c < 0 ? 0 : (c > nb ? nb : c);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {   // suffix sums: greater[c] = #items with cost > c
+    int32_t run = 0;
+    for (int c = nb; c >= 0; --c) {
+      const int32_t t = greater[c];
+      greater[c] = run;
+      run += t;
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < nb; i += blockDim.x) {
+    const int32_t c = cost[i];
+    int rank = 0;
+    for (int i2 = 0; i2 < i; ++i2) rank += cost[i2] == c;
+    items[(int64_t)greater[c] + before[c] + rank] = (int32_t)(r0 + i);
+  }
+  if (bh == 0 && threadIdx.x == 0 && counter != nullptr) *counter = 0;
+}
+
+// CSR -> CSC per head. Rows are visited in order, one row per step, so each
+// key block's list of query blocks comes out ascending.
+__global__ void __launch_bounds__(kThreads)
+csr_transpose_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ col_idx,
+                     int BH, int nb, int32_t* __restrict__ col_ptr, int32_t* __restrict__ row_idx,
+                     int32_t* d_status) {
+  __shared__ int32_t cnt[1024];
+  __shared__ int32_t cursor[1024];
+  __shared__ int32_t warp_tot[32];
+  const int bh = blockIdx.x;
+  const int64_t r0 = (int64_t)bh * nb;
+  for (int j = threadIdx.x; j < nb; j += blockDim.x) cnt[j] = 0;
+  __syncthreads();
+  const int32_t e0 = row_ptr[r0], e1 = row_ptr[r0 + nb];
+  for (int32_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+    const int32_t j = col_idx[e];
+    if (j >= 0 && j < nb) atomicAdd(&cnt[j], 1);
+    else report(d_status, SPARSP_ERR_DATA);
+  }
+  __syncthreads();
+  // exclusive scan of cnt[0..nb) (nb <= 1024 = blockDim)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int j = threadIdx.x;
+  const int32_t v = j < nb ? cnt[j] : 0;
+  int32_t incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t t = warp_tot[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t o = __shfl_up_sync(0xffffffffu, t, off);
+      if (lane >= off) t += o;
+    }
+    warp_tot[lane] = t;
+  }
+  __syncthreads();
+  const int32_t excl = (warp > 0 ? warp_tot[warp - 1] : 0) + incl - v;
+  if (j < nb) {
+    col_ptr[r0 + j] = e0 + excl;
+    cursor[j] = e0 + excl;
+  }
+  if (bh == BH - 1 && threadIdx.x == 0) col_ptr[(int64_t)BH * nb] = row_ptr[(int64_t)BH * nb];
+  __syncthreads();
+  for (int i = 0; i < nb; ++i) {
+    const int32_t a = row_ptr[r0 + i], b = row_ptr[r0 + i + 1];
+    for (int32_t e = a + threadIdx.x; e < b; e += blockDim.x) {
+      const int32_t jj = col_idx[e];
+      if (jj >= 0 && jj < nb) {
+        const int32_t pos = atomicAdd(&cursor[jj], 1);   // distinct jj within a row
+        row_idx[pos] = i;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+size_t lpt_ws(const Dims& s) { return (size_t)s.B * s.H * (s.nb + 1) * sizeof(int32_t); }
+
+sparsp_status_t launch_lpt(const Dims& s, const int32_t* row_ptr, bool flat, int32_t* items,
+                           int32_t* counter, void* ws, cudaStream_t st) {
+  const int BH = s.B * s.H;
+  if (!flat) {
+    lpt_grouped_kernel<<<BH, kThreads, 0, st>>>(row_ptr, BH, s.nb, items, counter);
+    SPARSP_LAUNCH_CHECK();
+  } else {
+    int32_t* hist = (int32_t*)ws;
+    lpt_hist_kernel<<<BH, kThreads, 0, st>>>(row_ptr, s.nb, hist);
+    SPARSP_LAUNCH_CHECK();
+    lpt_place_kernel<<<BH, kThreads, 0, st>>>(row_ptr, hist, BH, s.nb, items, counter);
+    SPARSP_LAUNCH_CHECK();
+  }
+  return SPARSP_OK;
+}
+
+sparsp_status_t launch_csr_transpose(const Dims& s, const int32_t* row_ptr, const int32_t* col_idx,
+                                     int32_t* col_ptr, int32_t* row_idx, int32_t* d_status,
+                                     cudaStream_t st) {
+  const int BH = s.B * s.H;
+  csr_transpose_kernel<<<BH, kThreads, 0, st>>>(row_ptr, col_idx, BH, s.nb, col_ptr, row_idx,
+                                                d_status);
+  SPARSP_LAUNCH_CHECK();
+  return SPARSP_OK;
+}
+
+}  // namespace sparsp

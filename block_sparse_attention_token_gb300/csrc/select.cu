@@ -1,0 +1,212 @@
+// Step 3: Top-p routing with a Top-k floor, compacted into a per-head CSR.
+//
+// Three launches, no atomics on data, deterministic:
+//  1. count_kernel  - one warp per row: bitonic sort of 64-bit keys
+//     (score descending as an order-preserving integer, then block index) held
+//     in registers and exchanged with shuffles; e_j = expf(S_j - max) in fp32;
+//     Z and the prefix masses in fp64; m = min(nb, max(m_p, k_floor, 1)).
+//     Writes m into row_ptr[row] and the key of the m-th kept block into ws.
+//  2. scan          - exclusive scan of the counts -> row_ptr.
+//  3. fill_kernel   - one warp per row: block j is kept iff its key <= the
+//     stored threshold key; kept indices are compacted in ascending j order
+//     with ballots.
+#include "common.cuh"
+
+namespace sparsp {
+namespace {
+
+constexpr int kWarpsPerCta = 8;
+
+// Order-preserving map of a finite float to uint32 (ascending), with -0 == +0.
+__device__ __forceinline__ uint32_t ordered_bits(float s) {
+  uint32_t u = __float_as_uint(s + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float from_ordered(uint32_t o) {
+  uint32_t u = (o & 0x80000000u) ? (o & 0x7fffffffu) : ~o;
+  return __uint_as_float(u);
+}
+
+// key: smaller = kept earlier. High word: descending score; low word: index.
+__device__ __forceinline__ uint64_t make_key(float s, int j) {
+  return ((uint64_t)(~ordered_bits(s)) << 32) | (uint32_t)j;
+}
+
+__device__ __forceinline__ float key_score(uint64_t key) {
+  return from_ordered(~(uint32_t)(key >> 32));
+}
+
+template <int E>   // elements per lane; padded row length = 32*E
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+count_kernel(const float* __restrict__ S, int64_t rows, int nb, double top_p, int k_floor,
+             int32_t* __restrict__ counts, uint64_t* __restrict__ thr, int32_t* d_status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const float* srow = S + row * nb;
+  uint64_t key[E];
+  bool bad = false;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int p = lane * E + e;
+    if (p < nb) {
+      const float s = srow[p];
+      if (!isfinite(s)) bad = true;
+      key[e] = make_key(s, p);
+    } else {
+      key[e] = ~0ull;
+    }
+  }
+  if (__any_sync(0xffffffffu, bad)) {
+    if (lane == 0) {
+      report(d_status, SPARSP_ERR_DATA);
+      counts[row] = 0;
+      thr[row] = 0;
+    }
+    return;
+  }
+  // bitonic sort, ascending key, positions p = lane*E + e
+  constexpr int NP = 32 * E;
+#pragma unroll
+  for (int size = 2; size <= NP; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride < E) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int e2 = e ^ stride;
+          if (e2 > e) {
+            const int p = lane * E + e;
+            const bool asc = (p & size) == 0;
+            const uint64_t a = key[e], b = key[e2];
+            const bool swap = asc ? (a > b) : (a < b);
+            key[e] = swap ? b : a;
+            key[e2] = swap ? a : b;
+          }
+        }
+      } else {
+        const int lmask = stride / E;
+        const bool lo = (lane & lmask) == 0;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int p = lane * E + e;
+          const bool asc = (p & size) == 0;
+          const uint64_t other = __shfl_xor_sync(0xffffffffu, key[e], lmask);
+          const uint64_t mn = key[e] < other ? key[e] : other;
+          const uint64_t mx = key[e] < other ? other : key[e];
+          key[e] = (lo == asc) ? mn : mx;
+        }
+      }
+    }
+  }
+  // softmax mass in sorted order
+  const float smax = __shfl_sync(0xffffffffu, key_score(key[0]), 0);
+  double ev[E];
+  double lane_sum = 0.0;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int p = lane * E + e;
+    ev[e] = 0.0;
+    if (p < nb) ev[e] = (double)expf(key_score(key[e]) - smax);
+    lane_sum += ev[e];
+  }
+  // inclusive scan of lane sums
+  double incl = lane_sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const double o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  const double Z = __shfl_sync(0xffffffffu, incl, 31);
+  int m_p;
+  if (top_p <= 0.0) {
+    m_p = 0;
+  } else if (top_p >= 1.0) {
+    m_p = nb;
+  } else {
+    const double target = top_p * Z;
+    double c = incl - lane_sum;   // exclusive prefix of this lane
+    int below = 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int p = lane * E + e;
+      c += ev[e];
+      if (p < nb && c < target) ++below;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) below += __shfl_xor_sync(0xffffffffu, below, off);
+    m_p = min(nb, below + 1);
+  }
+  const int m = min(nb, max(m_p, max(k_floor, 1)));
+  // threshold key = key at sorted position m-1
+  const int pos = m - 1;
+  const int src_lane = pos / E, src_e = pos % E;
+  uint64_t mine = 0;
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    if (e == src_e) mine = key[e];
+  const uint64_t tk = __shfl_sync(0xffffffffu, mine, src_lane);
+  if (lane == 0) {
+    counts[row] = m;
+    thr[row] = tk;
+  }
+}
+
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+fill_kernel(const float* __restrict__ S, int64_t rows, int nb, const int32_t* __restrict__ row_ptr,
+            const uint64_t* __restrict__ thr, int32_t* __restrict__ col_idx) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int32_t base = row_ptr[row];
+  const int32_t cnt = row_ptr[row + 1] - base;
+  if (cnt <= 0) return;
+  const uint64_t tk = thr[row];
+  const float* srow = S + row * nb;
+  int written = 0;
+  for (int j0 = 0; j0 < nb; j0 += 32) {
+    const int j = j0 + lane;
+    bool keep = false;
+    if (j < nb) keep = make_key(srow[j], j) <= tk;
+    const uint32_t ball = __ballot_sync(0xffffffffu, keep);
+    if (keep) col_idx[base + written + __popc(ball & ((1u << lane) - 1u))] = j;
+    written += __popc(ball);
+  }
+}
+
+template <int E>
+void count_go(const float* S, int64_t rows, int nb, double p, int kf, int32_t* counts,
+              uint64_t* thr, int32_t* st_word, cudaStream_t st) {
+  const int64_t ctas = (rows + kWarpsPerCta - 1) / kWarpsPerCta;
+  count_kernel<E><<<(unsigned)ctas, kWarpsPerCta * 32, 0, st>>>(S, rows, nb, p, kf, counts, thr,
+                                                               st_word);
+}
+
+}  // namespace
+
+size_t select_ws(const Dims& s) { return (size_t)s.rows() * sizeof(uint64_t); }
+
+sparsp_status_t launch_select(const Dims& s, const float* scores, float top_p, int k_floor,
+                              int32_t* row_ptr, int32_t* col_idx, void* ws, int32_t* d_status,
+                              cudaStream_t st) {
+  const int64_t rows = s.rows();
+  uint64_t* thr = (uint64_t*)ws;
+  const double p = (double)top_p;
+  const int nb = s.nb;
+  if (nb <= 32) count_go<1>(scores, rows, nb, p, k_floor, row_ptr, thr, d_status, st);
+  else if (nb <= 64) count_go<2>(scores, rows, nb, p, k_floor, row_ptr, thr, d_status, st);
+  else if (nb <= 128) count_go<4>(scores, rows, nb, p, k_floor, row_ptr, thr, d_status, st);
+  else if (nb <= 256) count_go<8>(scores, rows, nb, p, k_floor, row_ptr, thr, d_status, st);
+  else if (nb <= 512) count_go<16>(scores, rows, nb, p, k_floor, row_ptr, thr, d_status, st);
+  else count_go<32>(scores, rows, nb, p, k_floor, row_ptr, thr, d_status, st);
+  SPARSP_LAUNCH_CHECK();
+  sparsp_status_t r = launch_scan_counts(row_ptr, rows, st);
+  if (r != SPARSP_OK) return r;
+  const int64_t ctas = (rows + kWarpsPerCta - 1) / kWarpsPerCta;
+  fill_kernel<<<(unsigned)ctas, kWarpsPerCta * 32, 0, st>>>(scores, rows, nb, row_ptr, thr, col_idx);
+  SPARSP_LAUNCH_CHECK();
+  return SPARSP_OK;
+}
+
+}  // namespace sparsp

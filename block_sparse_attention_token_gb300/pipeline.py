@@ -1,0 +1,102 @@
+"""The whole hot path as one object with preallocated device buffers.
+
+forward(): reorder Q, K, V into tiles -> block scores -> Top-p/Top-k selection
+-> KV demand of P partitions (+ gather) -> block-sparse attention -> O back to
+raster order. backward(): dO into tiles -> attention backward -> dQ, dK, dV
+back to raster order. Every step is one or more libsparsp kernels on the
+current stream; nothing here allocates after construction.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (EST_LOWRANK, EST_MEAN, PROF_SLOTS, Shape, attn_bwd, attn_fwd, attn_workspace_size,
+               block_scores, block_scores_workspace_size, kv_demand, reorder, select,
+               select_workspace_size, DemandOut)
+
+
+class Pipeline:
+    def kernels_per_forward(self) -> int:
+        """Kernels forward() launches: reorder x3, pool + product, select x3 (count,
+        scan, fill), demand x4 (bitmap, scan, list, gather), schedule (1, or 2 in
+        flat order) + attention, inverse reorder."""
+        lpt = 2 if self.flags & 1 else 1
+        gather = 1 if self.demand.kg is not None else 0
+        return 3 + 2 + 3 + 3 + gather + lpt + 1 + 1
+
+    def kernels_per_backward(self) -> int:
+        """reorder dO, rowdot, CSR transpose, schedule, dQ, schedule, dK/dV, 3 inverse reorders."""
+        lpt = 2 if self.flags & 1 else 1
+        return 1 + 1 + 1 + lpt + 1 + lpt + 1 + 3
+
+    def __init__(self, shape: Shape, estimator: str, top_p: float, k_floor: int, P: int, rank: int = 16,
+                 gather: bool = True, flags: int = 0, backward: bool = False, device="cuda"):
+        self.shape, self.top_p, self.k_floor, self.P, self.rank, self.flags = shape, top_p, k_floor, P, rank, flags
+        self.est = EST_LOWRANK if estimator == "lowrank" else EST_MEAN
+        s = shape
+        dt = s.torch_dtype
+        dev = torch.device(device)
+        blocked = (s.B, s.H, s.N, s.d)
+        self.qb, self.kb, self.vb, self.ob = (torch.empty(blocked, dtype=dt, device=dev) for _ in range(4))
+        self.o = torch.empty((s.B, s.N, s.H, s.d), dtype=dt, device=dev)
+        self.lse = torch.empty((s.B, s.H, s.N), dtype=torch.float32, device=dev)
+        self.scores = torch.empty((s.B, s.H, s.nb, s.nb), dtype=torch.float32, device=dev)
+        self.ws_scores = torch.empty(max(block_scores_workspace_size(s, self.est, rank), 16), dtype=torch.uint8,
+                                     device=dev)
+        self.row_ptr = torch.empty(s.rows + 1, dtype=torch.int32, device=dev)
+        self.col_idx = torch.empty(s.rows * s.nb, dtype=torch.int32, device=dev)
+        self.ws_sel = torch.empty(max(select_workspace_size(s), 16), dtype=torch.uint8, device=dev)
+        W = (s.nb + 31) // 32
+        parts = s.B * s.H * P
+        kg = vg = None
+        if gather:
+            kg = torch.empty((parts * s.nb, s.Bt, s.d), dtype=dt, device=dev)
+            vg = torch.empty_like(kg)
+        self.demand = DemandOut(torch.empty((s.B, s.H, P, W), dtype=torch.int32, device=dev),
+                                torch.empty(parts + 1, dtype=torch.int32, device=dev),
+                                torch.empty(parts * s.nb, dtype=torch.int32, device=dev), kg, vg,
+                                torch.empty(4, dtype=torch.int64, device=dev))
+        self.ws_attn = torch.empty(max(attn_workspace_size(s, backward), 16), dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.prof = torch.zeros(PROF_SLOTS, dtype=torch.int64, device=dev)
+        if backward:
+            self.dob = torch.empty(blocked, dtype=dt, device=dev)
+            self.dqb, self.dkb, self.dvb = (torch.empty(blocked, dtype=dt, device=dev) for _ in range(3))
+            self.dq, self.dk, self.dv = (torch.empty((s.B, s.N, s.H, s.d), dtype=dt, device=dev)
+                                         for _ in range(3))
+
+    def forward(self, q, k, v, wq=None, wk=None, prof: bool = False, mark=None):
+        """mark: optional callable(stage_name) invoked after each stage is enqueued
+        (used to record CUDA events on the current stream)."""
+        s = self.shape
+        mark = mark or (lambda name: None)
+        reorder(s, q, self.qb)
+        reorder(s, k, self.kb)
+        reorder(s, v, self.vb)
+        mark("reorder")
+        block_scores(s, self.qb, self.kb, self.est, wq, wk, self.rank, out=self.scores, ws=self.ws_scores)
+        mark("scores")
+        select(s, self.scores, self.top_p, self.k_floor, self.row_ptr, self.col_idx, self.ws_sel, self.status)
+        mark("select")
+        kv_demand(s, self.P, self.row_ptr, self.col_idx, self.kb, self.vb, out=self.demand, status=self.status)
+        mark("kv_demand")
+        attn_fwd(s, self.qb, self.kb, self.vb, self.row_ptr, self.col_idx, 0.0, self.ob, self.lse, self.ws_attn,
+                 self.flags, self.prof if prof else None, self.status)
+        mark("attn_fwd")
+        reorder(s, self.ob, self.o, inverse=True)
+        mark("reorder_out")
+        return self.o, self.lse
+
+    def backward(self, dout, prof: bool = False, mark=None):
+        s = self.shape
+        mark = mark or (lambda name: None)
+        reorder(s, dout, self.dob)
+        mark("reorder_dout")
+        attn_bwd(s, self.qb, self.kb, self.vb, self.ob, self.lse, self.dob, self.row_ptr, self.col_idx, 0.0,
+                 self.dqb, self.dkb, self.dvb, self.ws_attn, self.flags, self.prof if prof else None, self.status)
+        mark("attn_bwd")
+        reorder(s, self.dqb, self.dq, inverse=True)
+        reorder(s, self.dkb, self.dk, inverse=True)
+        reorder(s, self.dvb, self.dv, inverse=True)
+        mark("reorder_grads")
+        return self.dq, self.dk, self.dv

@@ -1,0 +1,254 @@
+/*
+ * sparsp.h - C ABI of libsparsp: dynamic, per-head block-sparse attention over
+ * 3D video-DiT token sequences, on one NVIDIA GB300 (sm_103a).
+ *
+ * The method these calls implement is described, in words only, on the pages:
+ *
+ *  - "mlsift.com tag listing" (sequence parallelism), the Top-p video sparse-
+ *    attention entry, abstract: video-aware block organisation, Top-p routing
+ *    with a Top-k safety floor, per-head uneven workloads and their stragglers,
+ *    and sparse attention compared against FlashAttention;
+ *  - "Dynamic Sparsity in Large-Scale Video DiT Training", "How DSV works":
+ *    the per-head rank-16 low-rank Q.K predictor, sparse attention computed
+ *    only on the selected critical pairs without materialising the full score
+ *    matrix, query grouping, and rebalancing of lopsided per-head work;
+ *  - "SparSP: Exploiting Communication Sparsity for Sequence-Parallel Video
+ *    DiTs", abstract: demand-directed KV routing, which the KV-demand call
+ *    computes for P virtual query partitions on one GPU.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every call returns a sparsp_status_t. Errors that the host can see
+ *    (null or misaligned pointers, bad shapes, small workspace) are returned
+ *    synchronously BEFORE any work is enqueued; outputs are then untouched.
+ *  - Errors that depend on device data (an out-of-range block index, a
+ *    non-finite score, a full gather buffer, a wait that timed out) are
+ *    written to the optional device word *d_status (int32, caller-owned,
+ *    zero-initialised by the caller). The first error wins; the offending
+ *    work item is skipped. Kernels never trap and never spin without a bound.
+ *  - The caller owns every buffer. The library never allocates device
+ *    memory, never synchronises, and keeps no state apart from a per-device
+ *    cache of the SM count and of the tensor-map encoder entry point.
+ *    Calls are thread-safe.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default).
+ *  - All device pointers must be 16-byte aligned; tensors are contiguous.
+ *  - Shapes: d in {64, 128}; Bt = ta*tb*tc in {64, 128}; nb = N/Bt <= 1024;
+ *    dtype SPARSP_F32 or SPARSP_BF16 (bf16 inputs accumulate in fp32).
+ *
+ * Layouts
+ * -------
+ *  raster     [B, N, H, d]: N = T*Y*X tokens, t slowest, x fastest.
+ *  blocked    [B, H, N, d]: row j*Bt + o is token o of tile j. Tiles are
+ *             (ta, tb, tc) boxes numbered ((bt*nY)+by)*nX+bx (x tile fastest);
+ *             inside a tile tokens are numbered ((it*tb)+iy)*tc+ix.
+ *  scores     [B, H, nb, nb] float32; row (b, h, i) = query block i.
+ *  CSR        row_ptr [B*H*nb + 1] int32 (row r = (b*H + h)*nb + i),
+ *             col_idx [nnz] int32, key-block indices ascending within a row.
+ *  LSE        [B, H, N] float32, natural log.
+ */
+#ifndef SPARSP_H
+#define SPARSP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPARSP_VERSION 1
+
+#if defined(__GNUC__)
+#define SPARSP_API __attribute__((visibility("default")))
+#else
+#define SPARSP_API
+#endif
+
+/* A cudaStream_t, declared without CUDA headers. */
+typedef struct CUstream_st* sparsp_stream_t;
+
+typedef enum {
+  SPARSP_OK = 0,
+  SPARSP_ERR_INVALID_ARG = 1, /* null pointer, NaN parameter, bad enum      */
+  SPARSP_ERR_UNSUPPORTED = 2, /* dtype, d, Bt, nb or rank outside support    */
+  SPARSP_ERR_SHAPE = 3,       /* grid not divisible by tile, P out of range  */
+  SPARSP_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned            */
+  SPARSP_ERR_WORKSPACE = 5,   /* ws_bytes smaller than the size call returns */
+  SPARSP_ERR_CAPACITY = 6,    /* device: gather buffer too small             */
+  SPARSP_ERR_DATA = 7,        /* device: bad index, bad CSR row, NaN score   */
+  SPARSP_ERR_CUDA = 8,        /* a CUDA launch or runtime call failed        */
+  SPARSP_ERR_TIMEOUT = 9      /* device: a bounded wait expired              */
+} sparsp_status_t;
+
+typedef enum { SPARSP_F32 = 0, SPARSP_BF16 = 1 } sparsp_dtype_t;
+
+typedef enum { SPARSP_EST_MEAN = 0, SPARSP_EST_LOWRANK = 1 } sparsp_estimator_t;
+
+/* Attention options (bit flags). */
+enum {
+  /* Order work items purely by row cost across all heads instead of
+   * head-grouped longest-first (see sparsp_lpt_schedule). */
+  SPARSP_SCHED_FLAT = 1u << 0,
+  /* Use the portable mma.sync kernel even where the tcgen05 kernel applies. */
+  SPARSP_KERNEL_PORTABLE = 1u << 1
+};
+
+/* Per-SM profile slots that attention kernels accumulate into (see prof). */
+#define SPARSP_PROF_SLOTS 1024
+
+typedef struct {
+  int32_t B, H;        /* batch, heads                         */
+  int32_t T, Y, X;     /* latent grid (frames, height, width)  */
+  int32_t d;           /* head dimension                       */
+  int32_t ta, tb, tc;  /* tile (video-aware block) shape       */
+  int32_t dtype;       /* sparsp_dtype_t of Q, K, V, O, dO...  */
+} sparsp_shape_t;
+
+/* Name of a status code (static string). */
+SPARSP_API const char* sparsp_status_string(int32_t status);
+
+/* SPARSP_VERSION of the loaded library. */
+SPARSP_API int32_t sparsp_version(void);
+
+/*
+ * Step 1 - video-aware block organisation ("mlsift.com tag listing",
+ * Top-p video sparse-attention entry, abstract).
+ * inverse == 0: in = raster [B,N,H,d] -> out = blocked [B,H,N,d].
+ * inverse != 0: in = blocked -> out = raster. A pure permutation (bit-exact).
+ * in and out must not overlap. Element type = shape->dtype.
+ */
+SPARSP_API sparsp_status_t sparsp_reorder(const sparsp_shape_t* shape, const void* in, void* out,
+                               int32_t inverse, sparsp_stream_t stream);
+
+/*
+ * Step 2 - cheap block-score estimation.
+ * SPARSP_EST_MEAN:    S[b,h,i,j] = mean_{q in block i}(q) . mean_{k in block j}(k)
+ *                     (plain pooled dot product, no 1/sqrt(d)).
+ * SPARSP_EST_LOWRANK: S[b,h,i,j] = (mean_i(q) Wq[h]) . (mean_j(k) Wk[h]), which by
+ *                     bilinearity equals the block-pair mean of the token-level
+ *                     (q Wq)(k Wk)^T of the per-head low-rank predictor ("Dynamic
+ *                     Sparsity in Large-Scale Video DiT Training", "How DSV works").
+ * q, k: blocked [B,H,N,d] of shape->dtype. wq, wk: float32 [H, d, rank], NULL for
+ * MEAN; rank in [1, 64]. scores: float32 [B,H,nb,nb]. Means and projections are
+ * accumulated in float32 in a fixed order. ws: scratch of at least
+ * sparsp_block_scores_workspace_size() bytes.
+ */
+SPARSP_API size_t sparsp_block_scores_workspace_size(const sparsp_shape_t* shape, int32_t estimator,
+                                          int32_t rank);
+SPARSP_API sparsp_status_t sparsp_block_scores(const sparsp_shape_t* shape, int32_t estimator,
+                                    const void* q, const void* k, const float* wq,
+                                    const float* wk, int32_t rank, float* scores, void* ws,
+                                    size_t ws_bytes, sparsp_stream_t stream);
+
+/*
+ * Step 3 - Top-p routing with a Top-k safety floor ("mlsift.com tag listing",
+ * Top-p video sparse-attention entry, abstract), per (b, h, i) row of scores:
+ *   e_j = expf(S_j - max_j S_j) in float32; Z and prefix sums in float64;
+ *   blocks ordered by (S_j descending, j ascending);
+ *   m_p = smallest m whose prefix mass >= top_p * Z (0 if top_p <= 0, nb if >= 1);
+ *   m = min(nb, max(m_p, k_floor, 1)); the first m blocks, stored ascending.
+ * row_ptr [B*H*nb+1] and col_idx (capacity B*H*nb*nb) are written; nnz =
+ * row_ptr[B*H*nb] stays on the device. A row holding a NaN or infinite score
+ * sets SPARSP_ERR_DATA and is written as an empty row.
+ * ws: at least sparsp_select_workspace_size() bytes.
+ */
+SPARSP_API size_t sparsp_select_workspace_size(const sparsp_shape_t* shape);
+SPARSP_API sparsp_status_t sparsp_select(const sparsp_shape_t* shape, const float* scores, float top_p,
+                              int32_t k_floor, int32_t* row_ptr, int32_t* col_idx, void* ws,
+                              size_t ws_bytes, int32_t* d_status, sparsp_stream_t stream);
+
+/*
+ * Step 4 - KV demand of P contiguous virtual query partitions, the one-GPU
+ * analogue of Demand-Directed KV Routing ("SparSP: Exploiting Communication
+ * Sparsity for Sequence-Parallel Video DiTs", abstract). Partition r owns query
+ * blocks [floor(r*nb/P), floor((r+1)*nb/P)); its demand is the union of their
+ * CSR rows.
+ *   bitmap  uint32 [B,H,P,ceil(nb/32)]: bit j of partition (b,h,r).
+ *   dem_ptr int32 [B*H*P+1], dem_idx int32 (capacity B*H*P*nb): ascending set bits.
+ *   kg, vg  [gather_cap_blocks, Bt, d] of shape->dtype: slot s holds the K/V tile
+ *           of dem_idx[s] of its head, copied from blocked k, v. kg == vg == NULL
+ *           skips the gather (k, v may then be NULL). Slots beyond
+ *           gather_cap_blocks are not written and set SPARSP_ERR_CAPACITY.
+ *   bytes   uint64 [4]: demanded, all (every partition receives all KV),
+ *           remote_demanded, remote_all (blocks outside the partition's own
+ *           range); K and V both counted.
+ */
+SPARSP_API sparsp_status_t sparsp_kv_demand(const sparsp_shape_t* shape, int32_t P, const int32_t* row_ptr,
+                                 const int32_t* col_idx, uint32_t* bitmap, int32_t* dem_ptr,
+                                 int32_t* dem_idx, const void* k, const void* v, void* kg,
+                                 void* vg, int64_t gather_cap_blocks, uint64_t* bytes,
+                                 int32_t* d_status, sparsp_stream_t stream);
+
+/*
+ * Step 5c - longest-first work order for the attention kernels (the per-head
+ * straggler problem of the "mlsift.com tag listing" entry; the lopsided
+ * per-head work of "Dynamic Sparsity in Large-Scale Video DiT Training",
+ * "How DSV works"). Item (b,h,i) is encoded (b*H + h)*nb + i; its cost is its
+ * CSR row length.
+ *   flags & SPARSP_SCHED_FLAT == 0: heads by total cost descending (ties: lower
+ *     head first), rows inside a head by cost descending (ties: lower i first).
+ *   flags & SPARSP_SCHED_FLAT: all items by cost descending, ties by item.
+ * items: int32 [B*H*nb]. ws: at least sparsp_lpt_workspace_size() bytes.
+ */
+SPARSP_API size_t sparsp_lpt_workspace_size(const sparsp_shape_t* shape);
+SPARSP_API sparsp_status_t sparsp_lpt_schedule(const sparsp_shape_t* shape, const int32_t* row_ptr,
+                                    uint32_t flags, int32_t* items, void* ws, size_t ws_bytes,
+                                    sparsp_stream_t stream);
+
+/*
+ * Step 5a - block-sparse attention forward over the CSR ("Dynamic Sparsity in
+ * Large-Scale Video DiT Training", "How DSV works": attention only on the
+ * selected pairs, never materialising the full score matrix). For each query
+ * token q of block i, over the key tokens of the blocks in row (b,h,i):
+ *   O_q = sum_k softmax_k(scale q.k) v_k,   LSE_q = ln sum_k exp(scale q.k).
+ * q, k, v, o: blocked [B,H,N,d]; lse: float32 [B,H,N]. scale <= 0 means
+ * 1/sqrt(d). An empty row gives O = 0, LSE = -inf. A row with an index outside
+ * [0, nb) or more than nb entries sets SPARSP_ERR_DATA and is skipped.
+ * bf16 on sm_103a with Bt = d = 128 runs the tcgen05/TMEM/TMA kernel;
+ * otherwise (or with SPARSP_KERNEL_PORTABLE) an mma.sync kernel; float32 runs
+ * an fp32 FFMA kernel. Work items are pulled longest-first by persistent CTAs.
+ * prof: NULL or uint64 [SPARSP_PROF_SLOTS], caller-zeroed; receives per-SM busy
+ * nanoseconds (index = SM id).
+ * ws: at least sparsp_attn_workspace_size(shape, 0) bytes.
+ */
+SPARSP_API size_t sparsp_attn_workspace_size(const sparsp_shape_t* shape, int32_t backward);
+SPARSP_API sparsp_status_t sparsp_attn_fwd(const sparsp_shape_t* shape, const void* q, const void* k,
+                                const void* v, const int32_t* row_ptr, const int32_t* col_idx,
+                                float scale, void* o, float* lse, void* ws, size_t ws_bytes,
+                                uint32_t flags, uint64_t* prof, int32_t* d_status,
+                                sparsp_stream_t stream);
+
+/*
+ * Step 5b - block-sparse attention backward with the selection held fixed.
+ * Gradients of sum(dO * O) with O from sparsp_attn_fwd (its o and lse):
+ *   D = rowsum(dO * O); P = exp(scale QK^T - LSE) on the selected blocks;
+ *   dV = P^T dO; dS = P * (dO V^T - D); dQ = scale dS K; dK = scale dS^T Q.
+ * bf16 only. dq, dk, dv: blocked [B,H,N,d] bf16. dQ is accumulated per query
+ * block over its CSR row and dK/dV per key block over the transposed CSR, so
+ * the result is deterministic (no atomics on values).
+ * ws: at least sparsp_attn_workspace_size(shape, 1) bytes.
+ */
+SPARSP_API sparsp_status_t sparsp_attn_bwd(const sparsp_shape_t* shape, const void* q, const void* k,
+                                const void* v, const void* o, const float* lse, const void* dout,
+                                const int32_t* row_ptr, const int32_t* col_idx, float scale,
+                                void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                                uint32_t flags, uint64_t* prof, int32_t* d_status,
+                                sparsp_stream_t stream);
+
+/*
+ * Transpose of the per-head CSR (used by the backward): for each key block j
+ * of head (b,h), the query blocks that selected it, ascending.
+ * col_ptr int32 [B*H*nb+1]; row_idx int32 (capacity = nnz of the CSR).
+ */
+SPARSP_API sparsp_status_t sparsp_csr_transpose(const sparsp_shape_t* shape, const int32_t* row_ptr,
+                                     const int32_t* col_idx, int32_t* col_ptr, int32_t* row_idx,
+                                     int32_t* d_status, sparsp_stream_t stream);
+
+/* Number of SMs of the current device (cached), or -1 on error. */
+SPARSP_API int32_t sparsp_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSP_H */

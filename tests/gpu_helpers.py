@@ -1,0 +1,108 @@
+"""Shared pieces of the GPU parity tests: workload caching, device transfer,
+oracle chains and the comparison rules.
+
+Expected values always come from the oracle run on the generator's inputs
+(never from the CUDA path). The two paths meet only at the inputs.
+"""
+from __future__ import annotations
+
+import functools
+import math
+
+import numpy as np
+import torch
+
+import block_sparse_attention_token_gb300 as sp
+import synth
+from oracle import sparsp_oracle as orc
+
+BF16_MAX_ABS, BF16_MEAN_ABS = 1e-2, 1e-3
+F32_TOL = 1e-4
+
+
+@functools.lru_cache(maxsize=8)
+def workload(name: str):
+    wl = synth.WORKLOADS[name] if isinstance(name, str) and name in synth.WORKLOADS else name
+    return wl, synth.make(wl)
+
+
+def dev(x: np.ndarray, wl) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    return t.bfloat16() if wl.dtype == "bf16" else t.float()
+
+
+def i32(x) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(np.asarray(x, dtype=np.int32))).cuda()
+
+
+def host(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy() if t.dtype in (torch.bfloat16, torch.float16) else t.cpu().numpy()
+
+
+def status_word() -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+class OracleChain:
+    """The oracle's own forward chain on a workload's inputs (blocked tensors,
+    fp32-rounded scores, CSR)."""
+
+    def __init__(self, wl, data, blocked: bool = True):
+        self.wl, self.g = wl, orc.grid_of(wl)
+        g = self.g
+        self.qb, self.kb, self.vb = (orc.reorder(data[x], g) for x in ("q", "k", "v"))
+        if wl.estimator == "lowrank":
+            S = orc.scores_lowrank(self.qb, self.kb, data["wq"], data["wk"], g.Bt)
+        else:
+            S = orc.scores_mean(self.qb, self.kb, g.Bt)
+        self.S64 = S
+        self.S32 = S.astype(np.float32)
+        self.sel = orc.select(self.S32.reshape(-1, g.nb), wl.top_p, wl.k_floor)
+        self.scale = 1.0 / math.sqrt(g.d)
+
+
+def compare_values(got: np.ndarray, ref: np.ndarray, wl, what: str):
+    """Attention values: bf16 max-abs 1e-2 and mean-abs 1e-3; fp32 max-abs 1e-4."""
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err = np.abs(got.astype(np.float64) - ref)
+    if wl.dtype == "bf16":
+        assert err.max() <= BF16_MAX_ABS, f"{what}: max-abs {err.max():.3e}"
+        assert err.mean() <= BF16_MEAN_ABS, f"{what}: mean-abs {err.mean():.3e}"
+    else:
+        assert err.max() <= F32_TOL, f"{what}: max-abs {err.max():.3e}"
+    return float(err.max()), float(err.mean())
+
+
+def compare_csr(row_ptr: np.ndarray, col_idx: np.ndarray, sel: orc.Selection) -> int:
+    """Bit-exact CSR, except rows the oracle flags as within 1e-5 of the Top-p
+    threshold, where any count in its admissible range (and the corresponding
+    prefix of the score order) is accepted. Returns the number of such rows
+    whose count differed from the oracle's first choice."""
+    R = len(sel.row_ptr) - 1
+    assert row_ptr.shape == (R + 1,)
+    if np.array_equal(row_ptr, sel.row_ptr) and np.array_equal(col_idx[:row_ptr[-1]], sel.col_idx):
+        return 0
+    n_alt = 0
+    for r in range(R):
+        got = col_idx[row_ptr[r]:row_ptr[r + 1]]
+        want = sel.col_idx[sel.row_ptr[r]:sel.row_ptr[r + 1]]
+        if np.array_equal(got, want):
+            continue
+        m = len(got)
+        assert sel.m_lo[r] <= m <= sel.m_hi[r], f"row {r}: count {m} vs oracle {len(want)} (margin {sel.margin[r]:.2e})"
+        assert np.array_equal(got, np.sort(sel.order[r][:m])), f"row {r}: wrong block set"
+        n_alt += 1
+    return n_alt
+
+
+def jaccard_rows(rp_a, ci_a, rp_b, ci_b) -> float:
+    """Mean per-row Jaccard similarity of two CSRs' block sets."""
+    R = len(rp_a) - 1
+    tot = 0.0
+    for r in range(R):
+        a = set(ci_a[rp_a[r]:rp_a[r + 1]].tolist())
+        b = set(ci_b[rp_b[r]:rp_b[r + 1]].tolist())
+        u = len(a | b)
+        tot += 1.0 if u == 0 else len(a & b) / u
+    return tot / R

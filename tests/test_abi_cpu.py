@@ -1,0 +1,143 @@
+"""libsparsp loads, exports every symbol its header declares, and rejects bad
+arguments on the host before touching CUDA (no GPU needed: every call here
+fails validation, so nothing is launched)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import block_sparse_attention_token_gb300 as sp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_sparse_attention_token_gb300 import build
+    build.build()
+    return sp.lib()
+
+
+def declared_symbols():
+    text = "".join(open(h).read() for h in HEADERS)
+    return sorted(set(re.findall(r"SPARSP_API\s+[\w\s\*]+?\b(sparsp_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_six_calls():
+    names = declared_symbols()
+    for call in ("sparsp_reorder", "sparsp_block_scores", "sparsp_select", "sparsp_kv_demand",
+                 "sparsp_attn_fwd", "sparsp_attn_bwd"):
+        assert call in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    exported = subprocess.run(["nm", "-D", "--defined-only", sp.LIB_PATH], capture_output=True,
+                              text=True, check=True).stdout
+    names = set(re.findall(r"\s(sparsp_\w+)$", exported, flags=re.M))
+    missing = [n for n in declared_symbols() if n not in names]
+    assert not missing, missing
+    # the binding wires every declared call
+    assert set(declared_symbols()) <= set(sp._SIG)
+    # nothing else leaks out of the library
+    assert all(n.startswith("sparsp_") for n in names)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.sparsp_version() == 1
+    assert sp.status_string(0) == "SPARSP_OK"
+    assert sp.status_string(7) == "SPARSP_ERR_DATA"
+    assert sp.status_string(99) == "SPARSP_ERR_UNKNOWN"
+
+
+GOOD = dict(B=1, H=2, T=4, Y=16, X=16, d=64, ta=4, tb=4, tc=4, dtype=sp.BF16)
+FAKE = 1 << 20          # an aligned, never-dereferenced address
+
+
+def shape(**kw):
+    args = dict(GOOD)
+    args.update(kw)
+    return sp.make_shape(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=5), sp.SHAPE),              # grid not divisible by tile
+    (dict(B=0), sp.SHAPE),
+    (dict(d=96), sp.UNSUPPORTED),
+    (dict(ta=2), sp.UNSUPPORTED),       # Bt = 32
+    (dict(dtype=7), sp.UNSUPPORTED),
+    (dict(T=64, Y=64, X=64), sp.UNSUPPORTED),   # nb = 4096 > 1024
+])
+def test_shape_validation(lib, kw, code):
+    s = shape(**kw)
+    assert lib.sparsp_reorder(ctypes.byref(s), FAKE, FAKE * 2, 0, None) == code
+
+
+def test_null_and_misaligned_pointers(lib):
+    s = shape()
+    assert lib.sparsp_reorder(None, FAKE, FAKE * 2, 0, None) == sp.INVALID_ARG
+    assert lib.sparsp_reorder(ctypes.byref(s), None, FAKE, 0, None) == sp.INVALID_ARG
+    assert lib.sparsp_reorder(ctypes.byref(s), FAKE + 8, FAKE * 2, 0, None) == sp.ALIGN
+    # overlapping in/out
+    assert lib.sparsp_reorder(ctypes.byref(s), FAKE, FAKE + 4096, 0, None) == sp.INVALID_ARG
+
+
+def test_workspace_sizes(lib):
+    s = shape()
+    rows = s.B * s.H * s.nb
+    assert lib.sparsp_select_workspace_size(ctypes.byref(s)) == rows * 8
+    assert lib.sparsp_block_scores_workspace_size(ctypes.byref(s), sp.EST_MEAN, 16) == 2 * rows * s.d * 4
+    assert lib.sparsp_block_scores_workspace_size(ctypes.byref(s), sp.EST_LOWRANK, 16) == 2 * rows * 16 * 4
+    assert lib.sparsp_lpt_workspace_size(ctypes.byref(s)) == s.B * s.H * (s.nb + 1) * 4
+    fwd = lib.sparsp_attn_workspace_size(ctypes.byref(s), 0)
+    bwd = lib.sparsp_attn_workspace_size(ctypes.byref(s), 1)
+    assert fwd >= rows * 4 + 16 and bwd > fwd + s.B * s.H * s.N * 4
+    bad = shape(T=5)
+    assert lib.sparsp_attn_workspace_size(ctypes.byref(bad), 0) == 0
+
+
+def test_call_validation_codes(lib):
+    s = shape()
+    S = ctypes.byref(s)
+    f = ctypes.c_float
+    # select: NaN p, negative floor, small workspace
+    assert lib.sparsp_select(S, FAKE, f(float("nan")), 1, FAKE, FAKE, FAKE, 1 << 30, None, None) == sp.INVALID_ARG
+    assert lib.sparsp_select(S, FAKE, f(0.9), -1, FAKE, FAKE, FAKE, 1 << 30, None, None) == sp.INVALID_ARG
+    assert lib.sparsp_select(S, FAKE, f(0.9), 1, FAKE, FAKE, FAKE, 8, None, None) == sp.WORKSPACE
+    # scores: bad estimator, low-rank without weights, rank out of range, small workspace
+    assert lib.sparsp_block_scores(S, 5, FAKE, FAKE, None, None, 16, FAKE, FAKE, 1 << 30, None) == sp.INVALID_ARG
+    assert lib.sparsp_block_scores(S, sp.EST_LOWRANK, FAKE, FAKE, None, FAKE, 16, FAKE, FAKE, 1 << 30,
+                                   None) == sp.INVALID_ARG
+    assert lib.sparsp_block_scores(S, sp.EST_LOWRANK, FAKE, FAKE, FAKE, FAKE, 65, FAKE, FAKE, 1 << 30,
+                                   None) == sp.UNSUPPORTED
+    assert lib.sparsp_block_scores(S, sp.EST_MEAN, FAKE, FAKE, None, None, 16, FAKE, FAKE, 4, None) == sp.WORKSPACE
+    # demand: P out of range, kg without vg, negative capacity
+    args = (FAKE, FAKE, FAKE, FAKE, FAKE)
+    assert lib.sparsp_kv_demand(S, 0, *args, None, None, None, None, 0, FAKE, None, None) == sp.SHAPE
+    assert lib.sparsp_kv_demand(S, s.nb + 1, *args, None, None, None, None, 0, FAKE, None, None) == sp.SHAPE
+    assert lib.sparsp_kv_demand(S, 2, *args, FAKE, FAKE, FAKE, None, 4, FAKE, None, None) == sp.INVALID_ARG
+    assert lib.sparsp_kv_demand(S, 2, *args, FAKE, FAKE, FAKE, FAKE, -1, FAKE, None, None) == sp.INVALID_ARG
+    # attention: NaN scale, small workspace, misaligned optional pointer, fp32 backward
+    p7 = (FAKE,) * 5
+    assert lib.sparsp_attn_fwd(S, *p7, f(float("nan")), FAKE, FAKE, FAKE, 1 << 30, 0, None, None,
+                               None) == sp.INVALID_ARG
+    assert lib.sparsp_attn_fwd(S, *p7, f(0.0), FAKE, FAKE, FAKE, 8, 0, None, None, None) == sp.WORKSPACE
+    assert lib.sparsp_attn_fwd(S, *p7, f(0.0), FAKE, FAKE, FAKE, 1 << 30, 0, FAKE + 4, None,
+                               None) == sp.ALIGN
+    s32 = shape(dtype=sp.F32)
+    assert lib.sparsp_attn_bwd(ctypes.byref(s32), *((FAKE,) * 8), f(0.0), FAKE, FAKE, FAKE, FAKE, 1 << 30, 0,
+                               None, None, None) == sp.UNSUPPORTED
+    assert lib.sparsp_attn_bwd(S, *((FAKE,) * 8), f(0.0), FAKE, FAKE, FAKE, FAKE, 8, 0, None, None,
+                               None) == sp.WORKSPACE
+    assert lib.sparsp_lpt_schedule(S, FAKE, sp.SCHED_FLAT, FAKE, FAKE, 4, None) == sp.WORKSPACE
+    assert lib.sparsp_csr_transpose(S, FAKE, None, FAKE, FAKE, None, None) == sp.INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(sp, "_lib", None)
+    monkeypatch.setattr(sp, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        sp.lib()

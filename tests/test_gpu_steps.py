@@ -1,0 +1,295 @@
+"""GPU parity of every step against the oracle, element by element, on
+workloads the oracle finishes in seconds (several tiles, ragged item counts,
+both tile sizes, both head dimensions, fp32 and bf16), plus edge cases."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_attention_token_gb300 as sp
+import synth
+from oracle import sparsp_oracle as orc
+from tests.gpu_helpers import (OracleChain, compare_csr, compare_values, dev, host, i32, jaccard_rows,
+                               status_word, workload)
+
+pytestmark = [pytest.mark.gpu, pytest.mark.timeout(900)]
+
+W = synth.Workload
+SMALL = {
+    "tiny": synth.WORKLOADS["tiny"],
+    "medium": synth.WORKLOADS["medium"],
+    # 2 batches x 3 heads, Bt = 128, d = 128: 72 items (fewer than the SMs)
+    "r128": W("ragged-1.5k-bf16", 2, 3, 128, 4, 16, 24, 2, 8, 8, "bf16", "mean", 0.9, 2, 3, 2, False, True, 31),
+    # Bt = 64 with d = 128 and an odd tile lattice (3 x 2 x 3)
+    "r64": W("ragged-1.2k-bf16", 1, 5, 128, 6, 8, 24, 2, 4, 8, "bf16", "mean", 0.8, 3, 5, 3, False, True, 32),
+    # Bt = 128 with d = 64
+    "r128d64": W("ragged-2k-d64-bf16", 1, 4, 64, 4, 16, 32, 2, 8, 8, "bf16", "mean", 0.85, 2, 4, 2, False, True, 33),
+    # fp32, Bt = 128, d = 128
+    "f32big": W("f32-1k-d128", 1, 3, 128, 4, 8, 32, 2, 8, 8, "f32", "mean", 0.9, 1, 2, 1, False, False, 34),
+    # 640 items: more than one wave of persistent CTAs with a ragged tail; low-rank scores
+    "wave": W("wave-4k-lowrank-bf16", 1, 20, 128, 4, 32, 32, 2, 8, 8, "bf16", "lowrank", 0.0, 6, 4, 4, False, True, 35),
+}
+BWD = ["medium", "r128", "r64", "r128d64", "wave"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available()
+
+
+def _setup(name):
+    wl = SMALL[name]
+    _, data = workload(wl)
+    return wl, data, sp.shape_of(wl)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_reorder_bitexact(name):
+    wl, data, shape = _setup(name)
+    g = orc.grid_of(wl)
+    q = dev(data["q"], wl)
+    qb = sp.reorder(shape, q)
+    ref = orc.reorder(data["q"], g)
+    assert np.array_equal(host(qb), ref)
+    back = sp.reorder(shape, qb, inverse=True)
+    assert torch.equal(back, q)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_block_scores(name):
+    wl, data, shape = _setup(name)
+    ch = OracleChain(wl, data)
+    qb, kb = dev(ch.qb, wl), dev(ch.kb, wl)
+    if wl.estimator == "lowrank":
+        wq, wk = (torch.from_numpy(data[x]).cuda() for x in ("wq", "wk"))
+        S = sp.block_scores(shape, qb, kb, sp.EST_LOWRANK, wq, wk, 16)
+    else:
+        S = sp.block_scores(shape, qb, kb)
+    torch.cuda.synchronize()
+    got = host(S).astype(np.float64)
+    scale = np.abs(ch.S64).max()
+    np.testing.assert_allclose(got, ch.S64, rtol=2e-5, atol=2e-5 * scale)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_select_bitexact_on_oracle_scores(name):
+    wl, data, shape = _setup(name)
+    ch = OracleChain(wl, data)
+    st = status_word()
+    rp, ci = sp.select(shape, torch.from_numpy(ch.S32).cuda(), wl.top_p, wl.k_floor, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    n_alt = compare_csr(host(rp), host(ci), ch.sel)
+    assert n_alt <= max(1, len(ch.sel.margin) // 1000)
+
+
+@pytest.mark.parametrize("p,k", [(0.0, 0), (0.0, 3), (1.0, 0), (0.5, 999), (0.3, 1), (0.999, 2)])
+def test_select_extremes(p, k):
+    shape = sp.make_shape(1, 3, 4, 8, 16, 64, 2, 4, 4, "bf16")      # nb = 2*2*4 = 16
+    S = synth.random_scores(41, 3 * 16, 16, scale=3.0)
+    S[5, 3] = S[5, 7]          # exact ties
+    S[9, :] = 0.0              # a flat row
+    ref = orc.select(S, p, k)
+    rp, ci = sp.select(shape, torch.from_numpy(S).cuda(), p, k)
+    compare_csr(host(rp), host(ci), ref)
+
+
+def test_select_nan_row_is_empty_and_reported():
+    shape = sp.make_shape(1, 1, 4, 8, 16, 64, 2, 4, 4, "bf16")
+    S = synth.random_scores(42, 16, 16)
+    S[4, 2] = np.nan
+    S[11, 0] = np.inf
+    st = status_word()
+    rp, ci = sp.select(shape, torch.from_numpy(S).cuda(), 0.9, 2, status=st)
+    rp = host(rp)
+    assert st.item() == sp.DATA
+    assert rp[5] - rp[4] == 0 and rp[12] - rp[11] == 0
+    good = np.delete(np.arange(16), [4, 11])
+    ref = orc.select(S[good], 0.9, 2)
+    assert np.array_equal(np.diff(rp)[good], np.diff(ref.row_ptr))
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_kv_demand_bitexact(name):
+    wl, data, shape = _setup(name)
+    ch = OracleChain(wl, data)
+    g = ch.g
+    ref = orc.kv_demand(ch.sel.row_ptr, ch.sel.col_idx, g.B, g.H, g.nb, wl.P, g.Bt, g.d, wl.elem_bytes,
+                        ch.kb, ch.vb)
+    st = status_word()
+    out = sp.kv_demand(shape, wl.P, i32(ch.sel.row_ptr), i32(ch.sel.col_idx), dev(ch.kb, wl), dev(ch.vb, wl),
+                       status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert np.array_equal(host(out.bitmap).view(np.uint32).ravel(), ref.bitmap.ravel())
+    assert np.array_equal(host(out.dem_ptr), ref.dem_ptr)
+    total = int(ref.dem_ptr[-1])
+    assert np.array_equal(host(out.dem_idx)[:total], ref.dem_idx)
+    assert np.array_equal(host(out.kg)[:total], ref.kg)
+    assert np.array_equal(host(out.vg)[:total], ref.vg)
+    assert host(out.bytes).astype(np.uint64).tolist() == ref.bytes.tolist()
+
+
+def test_kv_demand_capacity_shortfall():
+    wl, data, shape = _setup("r64")
+    ch = OracleChain(wl, data)
+    g = ch.g
+    ref = orc.kv_demand(ch.sel.row_ptr, ch.sel.col_idx, g.B, g.H, g.nb, wl.P, g.Bt, g.d, 2, ch.kb, ch.vb)
+    cap = int(ref.dem_ptr[-1]) // 2
+    st = status_word()
+    out = sp.kv_demand(shape, wl.P, i32(ch.sel.row_ptr), i32(ch.sel.col_idx), dev(ch.kb, wl), dev(ch.vb, wl),
+                       gather_cap=cap, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == sp.CAPACITY
+    assert np.array_equal(host(out.kg)[:cap], ref.kg[:cap])
+    assert np.array_equal(host(out.dem_idx)[:int(ref.dem_ptr[-1])], ref.dem_idx)
+    # sets only (no gather), one partition and one partition per block
+    for P in (1, g.nb):
+        r2 = orc.kv_demand(ch.sel.row_ptr, ch.sel.col_idx, g.B, g.H, g.nb, P, g.Bt, g.d, 2)
+        o2 = sp.kv_demand(shape, P, i32(ch.sel.row_ptr), i32(ch.sel.col_idx))
+        assert np.array_equal(host(o2.dem_ptr), r2.dem_ptr)
+        assert np.array_equal(host(o2.dem_idx)[:int(r2.dem_ptr[-1])], r2.dem_idx)
+        assert host(o2.bytes).astype(np.uint64).tolist() == r2.bytes.tolist()
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("flat", [False, True])
+def test_lpt_schedule_bitexact(name, flat):
+    wl, data, shape = _setup(name)
+    ch = OracleChain(wl, data)
+    g = ch.g
+    items = sp.lpt_schedule(shape, i32(ch.sel.row_ptr), sp.SCHED_FLAT if flat else 0)
+    ref = orc.lpt_order(ch.sel.row_ptr, g.B, g.H, g.nb, grouped=not flat)
+    assert np.array_equal(host(items), ref)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_csr_transpose_bitexact(name):
+    wl, data, shape = _setup(name)
+    ch = OracleChain(wl, data)
+    g = ch.g
+    cp, ri = sp.csr_transpose(shape, i32(ch.sel.row_ptr), i32(ch.sel.col_idx))
+    rcp, rri = orc.csc_of(ch.sel.row_ptr, ch.sel.col_idx, g.B, g.H, g.nb)
+    assert np.array_equal(host(cp), rcp)
+    assert np.array_equal(host(ri)[:len(rri)], rri)
+
+
+def _attn_fwd_check(name, flags):
+    wl, data, shape = _setup(name)
+    ch = OracleChain(wl, data)
+    st = status_word()
+    o, lse = sp.attn_fwd(shape, dev(ch.qb, wl), dev(ch.kb, wl), dev(ch.vb, wl), i32(ch.sel.row_ptr),
+                         i32(ch.sel.col_idx), flags=flags, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    O, L = orc.attn_fwd(ch.qb, ch.kb, ch.vb, ch.sel.row_ptr, ch.sel.col_idx, ch.g.Bt, ch.scale)
+    compare_values(host(o), O, wl, "O")
+    compare_values(host(lse), L, wl, "LSE")
+    return o, lse
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_attn_fwd(name):
+    _attn_fwd_check(name, 0)
+
+
+@pytest.mark.parametrize("name", ["medium", "r128", "wave"])
+def test_attn_fwd_schedules_and_kernels_agree_bitwise(name):
+    o1, l1 = _attn_fwd_check(name, 0)
+    o2, l2 = _attn_fwd_check(name, sp.SCHED_FLAT)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    o3, l3 = _attn_fwd_check(name, sp.KERNEL_PORTABLE)
+    o4, l4 = _attn_fwd_check(name, sp.KERNEL_PORTABLE | sp.SCHED_FLAT)
+    assert torch.equal(o3, o4) and torch.equal(l3, l4)
+    o5, l5 = _attn_fwd_check(name, 0)
+    assert torch.equal(o1, o5) and torch.equal(l1, l5)
+
+
+@pytest.mark.parametrize("portable", [False, True])
+@pytest.mark.parametrize("name", ["r128", "tiny", "r64"])
+def test_attn_fwd_empty_and_bad_rows(name, portable):
+    wl, data, shape = _setup(name)
+    ch = OracleChain(wl, data)
+    g = ch.g
+    rp = ch.sel.row_ptr.astype(np.int64)
+    counts = np.diff(rp)
+    counts[1] = 0                                   # an empty row
+    counts[-1] = 0
+    rows = [np.asarray(ch.sel.col_idx[rp[r]:rp[r + 1]]) if counts[r] else np.zeros(0, np.int64)
+            for r in range(len(counts))]
+    rows[2] = rows[2].copy()
+    rows[2][0] = g.nb + 5                           # out of range -> the row is skipped
+    ci = np.concatenate(rows).astype(np.int32)
+    rp2 = np.concatenate([[0], np.cumsum([len(x) for x in rows])]).astype(np.int32)
+    st = status_word()
+    sentinel = 7.0
+    o = torch.full((g.B, g.H, g.N, g.d), sentinel, dtype=shape.torch_dtype, device="cuda")
+    lse = torch.full((g.B, g.H, g.N), sentinel, device="cuda")
+    sp.attn_fwd(shape, dev(ch.qb, wl), dev(ch.kb, wl), dev(ch.vb, wl), i32(rp2), i32(ci), o=o, lse=lse,
+                flags=sp.KERNEL_PORTABLE if portable else 0, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == sp.DATA
+    O, L = host(o), host(lse)
+    Bt = g.Bt
+    assert (O[0, 0, Bt:2 * Bt] == 0).all() and np.isneginf(L[0, 0, Bt:2 * Bt]).all()
+    assert (O[0, 0, 2 * Bt:3 * Bt] == sentinel).all() and (L[0, 0, 2 * Bt:3 * Bt] == sentinel).all()
+    ok = [r for r in range(len(counts)) if r not in (1, 2, len(counts) - 1)]
+    rows_ok = [(r // (g.H * g.nb), (r // g.nb) % g.H, r % g.nb) for r in ok[:6]]
+    Oref, Lref = orc.attn_fwd(ch.qb, ch.kb, ch.vb, rp2, ci, Bt, ch.scale, rows=rows_ok)
+    for (b, h, i) in rows_ok:
+        sl = slice(i * Bt, (i + 1) * Bt)
+        compare_values(O[b, h, sl], Oref[b, h, sl], wl, "O")
+
+
+@pytest.mark.parametrize("name", BWD)
+def test_attn_bwd(name):
+    wl, data, shape = _setup(name)
+    ch = OracleChain(wl, data)
+    dob = orc.reorder(data["do"], ch.g)
+    st = status_word()
+    q, k, v = dev(ch.qb, wl), dev(ch.kb, wl), dev(ch.vb, wl)
+    rp, ci = i32(ch.sel.row_ptr), i32(ch.sel.col_idx)
+    o, lse = sp.attn_fwd(shape, q, k, v, rp, ci, status=st)
+    dq, dk, dv = sp.attn_bwd(shape, q, k, v, o, lse, dev(dob, wl), rp, ci, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    dQ, dK, dV = orc.attn_bwd(ch.qb, ch.kb, ch.vb, dob, ch.sel.row_ptr, ch.sel.col_idx, ch.g.Bt, ch.scale)
+    compare_values(host(dq), dQ, wl, "dQ")
+    compare_values(host(dk), dK, wl, "dK")
+    compare_values(host(dv), dV, wl, "dV")
+    # deterministic: a second run is bitwise identical
+    dq2, dk2, dv2 = sp.attn_bwd(shape, q, k, v, o, lse, dev(dob, wl), rp, ci, flags=sp.SCHED_FLAT)
+    assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
+
+
+@pytest.mark.parametrize("name", ["tiny", "medium", "r128", "wave"])
+def test_pipeline_end_to_end(name):
+    """The whole chain on the GPU (its own scores and selection) against the
+    oracle's own chain: selection agreement is reported, outputs are compared
+    on every row whose block set agrees."""
+    wl, data, shape = _setup(name)
+    ch = OracleChain(wl, data)
+    g = ch.g
+    pipe = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P, backward=wl.backward)
+    args = [dev(data[x], wl) for x in ("q", "k", "v")]
+    kw = {}
+    if wl.estimator == "lowrank":
+        kw = dict(wq=torch.from_numpy(data["wq"]).cuda(), wk=torch.from_numpy(data["wk"]).cuda())
+    o, lse = pipe.forward(*args, **kw)
+    torch.cuda.synchronize()
+    assert pipe.status.item() == 0
+    rp, ci = host(pipe.row_ptr), host(pipe.col_idx)
+    jac = jaccard_rows(rp, ci, ch.sel.row_ptr, ch.sel.col_idx)
+    print(f"{wl.name}: block-set agreement (mean row Jaccard) {jac:.6f}")
+    assert jac > 0.99
+    same = [r for r in range(len(rp) - 1)
+            if np.array_equal(ci[rp[r]:rp[r + 1]], ch.sel.col_idx[ch.sel.row_ptr[r]:ch.sel.row_ptr[r + 1]])]
+    O, _ = orc.attn_fwd(ch.qb, ch.kb, ch.vb, ch.sel.row_ptr, ch.sel.col_idx, g.Bt, ch.scale)
+    ob = orc.reorder(host(o), g)
+    for r in same:
+        b, h, i = r // (g.H * g.nb), (r // g.nb) % g.H, r % g.nb
+        sl = slice(i * g.Bt, (i + 1) * g.Bt)
+        compare_values(ob[b, h, sl], O[b, h, sl], wl, f"O row {r}")

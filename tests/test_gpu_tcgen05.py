@@ -1,0 +1,39 @@
+"""The tcgen05 building blocks of the attention kernel on one 128x128x128 tile:
+TMA boxes with 128-byte swizzle, K-major and MN-major shared-memory
+descriptors, and a TMEM-resident A operand, against a float64 product."""
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_attention_token_gb300 as sp
+
+pytestmark = [pytest.mark.gpu, pytest.mark.timeout(300)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _tiles(seed):
+    g = torch.Generator().manual_seed(seed)
+    a = torch.randn(128, 128, generator=g).bfloat16()
+    b = torch.randn(128, 128, generator=g).bfloat16()
+    return a, b
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_umma_tile(mode):
+    a, b = _tiles(mode + 1)
+    d = sp.diag_umma_tile(a.cuda(), b.cuda(), mode)
+    torch.cuda.synchronize()
+    A, Bm = a.double().numpy(), b.double().numpy()
+    ref = A @ Bm.T if mode == 0 else A @ Bm
+    got = d.cpu().double().numpy()
+    err = np.abs(got - ref).max()
+    if err > 1e-3 and mode > 0:
+        # report whether the other assignment of leading/stride offsets would have matched
+        alt = sp.diag_umma_tile(a.cuda(), b.cuda(), mode, lbo=1024, sbo=16384).cpu().double().numpy()
+        print(f"mode {mode}: max err {err:.3g}; with lbo/sbo swapped {np.abs(alt - ref).max():.3g}")
+    assert err < 1e-3, f"mode {mode}: max err {err:.3g}"
