@@ -177,9 +177,13 @@ def main():
     ap.add_argument("--portable", action="store_true", help="mma.sync attention kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--heads", type=int, default=0, help="override the head count (smaller profiling case)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     wl = synth.WORKLOADS[args.workload]
+    if args.heads:
+        import dataclasses
+        wl = dataclasses.replace(wl, H=args.heads, name=f"{wl.name}-h{args.heads}")
     if args.impl == "reference":
         return run_reference(args, wl)
 

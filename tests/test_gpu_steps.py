@@ -88,7 +88,7 @@ def test_select_bitexact_on_oracle_scores(name):
 
 @pytest.mark.parametrize("p,k", [(0.0, 0), (0.0, 3), (1.0, 0), (0.5, 999), (0.3, 1), (0.999, 2)])
 def test_select_extremes(p, k):
-    shape = sp.make_shape(1, 3, 4, 8, 16, 64, 2, 4, 4, "bf16")      # nb = 2*2*4 = 16
+    shape = sp.make_shape(1, 3, 4, 8, 32, 64, 4, 4, 4, "bf16")      # nb = 1*2*8 = 16
     S = synth.random_scores(41, 3 * 16, 16, scale=3.0)
     S[5, 3] = S[5, 7]          # exact ties
     S[9, :] = 0.0              # a flat row
@@ -98,7 +98,7 @@ def test_select_extremes(p, k):
 
 
 def test_select_nan_row_is_empty_and_reported():
-    shape = sp.make_shape(1, 1, 4, 8, 16, 64, 2, 4, 4, "bf16")
+    shape = sp.make_shape(1, 1, 4, 8, 32, 64, 4, 4, 4, "bf16")
     S = synth.random_scores(42, 16, 16)
     S[4, 2] = np.nan
     S[11, 0] = np.inf
@@ -248,7 +248,11 @@ def test_attn_fwd_empty_and_bad_rows(name, portable):
 def test_attn_bwd(name):
     wl, data, shape = _setup(name)
     ch = OracleChain(wl, data)
-    dob = orc.reorder(data["do"], ch.g)
+    do = data.get("do")
+    if do is None:      # forward-only workload: a seeded upstream gradient
+        do = synth.round_bf16(np.random.default_rng(wl.seed + 100).standard_normal(data["q"].shape,
+                                                                                   dtype=np.float32))
+    dob = orc.reorder(do, ch.g)
     st = status_word()
     q, k, v = dev(ch.qb, wl), dev(ch.kb, wl), dev(ch.vb, wl)
     rp, ci = i32(ch.sel.row_ptr), i32(ch.sel.col_idx)
