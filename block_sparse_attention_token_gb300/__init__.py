@@ -80,6 +80,7 @@ _SIG = {
     "sparsp_block_scores": (_I32, [_P, _I32, _P, _P, _P, _P, _I32, _P, _P, ctypes.c_size_t, _P]),
     "sparsp_select_workspace_size": (ctypes.c_size_t, [_P]),
     "sparsp_select": (_I32, [_P, _P, ctypes.c_float, _I32, _P, _P, _P, ctypes.c_size_t, _P, _P]),
+    "sparsp_select_noalloc": (_I32, [_P, _P, ctypes.c_float, _I32, _P, _P, _P, _P]),
     "sparsp_kv_demand": (_I32, [_P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int64, _P, _P, _P]),
     "sparsp_lpt_workspace_size": (ctypes.c_size_t, [_P]),
     "sparsp_lpt_schedule": (_I32, [_P, _P, ctypes.c_uint32, _P, _P, ctypes.c_size_t, _P]),

@@ -179,6 +179,23 @@ sparsp_status_t sparsp_select(const sparsp_shape_t* shape, const float* scores, 
                        (cudaStream_t)stream);
 }
 
+sparsp_status_t sparsp_select_noalloc(const sparsp_shape_t* shape, const float* scores, float top_p,
+                                      int32_t k_floor, int32_t* row_ptr, int32_t* col_idx,
+                                      int32_t* d_status, sparsp_stream_t stream) {
+  Dims s;
+  sparsp_status_t r = check_shape(shape, &s);
+  if (r != SPARSP_OK) return r;
+  if (isnan(top_p)) return SPARSP_ERR_INVALID_ARG;
+  if (k_floor < 0) return SPARSP_ERR_INVALID_ARG;
+  CHECK_PTR(scores);
+  CHECK_PTR(row_ptr);
+  CHECK_PTR(col_idx);
+  CHECK_OPT_PTR(d_status);
+  if (s.rows() > kSelectNoAllocMaxRows) return SPARSP_ERR_WORKSPACE;
+  return launch_select_noalloc(s, scores, top_p, k_floor, row_ptr, col_idx, d_status,
+                               (cudaStream_t)stream);
+}
+
 sparsp_status_t sparsp_kv_demand(const sparsp_shape_t* shape, int32_t P, const int32_t* row_ptr,
                                  const int32_t* col_idx, uint32_t* bitmap, int32_t* dem_ptr,
                                  int32_t* dem_idx, const void* k, const void* v, void* kg,

@@ -61,6 +61,10 @@ sparsp_status_t launch_select(const Dims& s, const float* scores, float top_p, i
                               int32_t* row_ptr, int32_t* col_idx, void* ws, int32_t* d_status,
                               cudaStream_t st);
 size_t select_ws(const Dims& s);
+constexpr int64_t kSelectNoAllocMaxRows = 65536;
+sparsp_status_t launch_select_noalloc(const Dims& s, const float* scores, float top_p, int k_floor,
+                                      int32_t* row_ptr, int32_t* col_idx, int32_t* d_status,
+                                      cudaStream_t st);
 
 sparsp_status_t launch_kv_demand(const Dims& s, int P, const int32_t* row_ptr,
                                  const int32_t* col_idx, uint32_t* bitmap, int32_t* dem_ptr,

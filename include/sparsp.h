@@ -158,6 +158,33 @@ SPARSP_API sparsp_status_t sparsp_select(const sparsp_shape_t* shape, const floa
                               size_t ws_bytes, int32_t* d_status, sparsp_stream_t stream);
 
 /*
+ * sparsp_select without a workspace argument, for callers that cannot
+ * allocate device memory when they call: for example an inference-engine
+ * plug-in whose enqueue step must not allocate, or a service that reserves all
+ * of its device memory at start-up and forbids allocation afterwards. The
+ * pages have no counterpart to this call; it is an interface convenience.
+ * Same arguments, results and errors as sparsp_select, except that its scratch
+ * (one 64-bit key per row) lives in a fixed array inside the library:
+ *  - at most SPARSP_SELECT_NOALLOC_MAX_ROWS rows (B*H*nb); a larger shape
+ *    returns SPARSP_ERR_WORKSPACE before any work is enqueued;
+ *  - the array costs 512 KB of device memory on every device that loads the
+ *    library, held until the process exits;
+ *  - the first call on each device looks the array's device address up (a
+ *    runtime query, no allocation); make that first call before any stream
+ *    capture;
+ *  - every call shares the one array, which keeps the last call's contents
+ *    (nothing in it needs to start at zero): calls whose work can overlap on
+ *    the GPU (different streams, or different host threads) race and must be
+ *    serialised by the caller.
+ * It never calls cudaMalloc, cudaFree or any allocating routine.
+ */
+#define SPARSP_SELECT_NOALLOC_MAX_ROWS 65536
+SPARSP_API sparsp_status_t sparsp_select_noalloc(const sparsp_shape_t* shape, const float* scores,
+                                                 float top_p, int32_t k_floor, int32_t* row_ptr,
+                                                 int32_t* col_idx, int32_t* d_status,
+                                                 sparsp_stream_t stream);
+
+/*
  * Step 4 - KV demand of P contiguous virtual query partitions, the one-GPU
  * analogue of Demand-Directed KV Routing ("SparSP: Exploiting Communication
  * Sparsity for Sequence-Parallel Video DiTs", abstract). Partition r owns query

@@ -136,6 +136,15 @@ def test_call_validation_codes(lib):
     assert lib.sparsp_csr_transpose(S, FAKE, None, FAKE, FAKE, None, None) == sp.INVALID_ARG
 
 
+def test_no_alloc_select_host_checks(lib):
+    f = ctypes.c_float
+    big = shape(B=1, H=65, T=16, Y=64, X=128, d=128, ta=2, tb=8, tc=8)    # 66,560 rows
+    assert lib.sparsp_select_noalloc(ctypes.byref(big), FAKE, f(0.9), 1, FAKE, FAKE, None, None) == sp.WORKSPACE
+    s = shape()
+    assert lib.sparsp_select_noalloc(ctypes.byref(s), None, f(0.9), 1, FAKE, FAKE, None, None) == sp.INVALID_ARG
+    assert lib.sparsp_select_noalloc(ctypes.byref(s), FAKE, f(0.9), -1, FAKE, FAKE, None, None) == sp.INVALID_ARG
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(sp, "_lib", None)
     monkeypatch.setattr(sp, "LIB_PATH", str(tmp_path / "missing.so"))
