@@ -8,7 +8,7 @@
 //              tiles (128 x 128 bf16, two 64-column boxes with 128-byte swizzle)
 //              into a 3-stage K ring and a 2-stage V ring, addressed through
 //              the CSR (row coordinate = bh*N + j*128).
-//   warp 5     MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM S
+//   warp 5     MMA issuer (whole warp; one elected lane issues): S_j = Q K_j^T into one of two TMEM S
 //              buffers (M=N=128, K=16 per instruction, both operands K-major
 //              from shared memory), issued one block ahead of O += P_j V_j
 //              (A = P_j read from TMEM as packed bf16, B = V_j MN-major from
@@ -41,7 +41,8 @@ constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
 constexpr uint32_t kOffK = kTile, kOffV = kOffK + kNK * kTile, kOffBar = kOffV + kNV * kTile;
 enum Bar {
   Q_FULL = 0, Q_EMPTY, K_FULL, K_EMPTY = K_FULL + kNK, V_FULL = K_EMPTY + kNK, V_EMPTY = V_FULL + kNV,
-  S_FULL = V_EMPTY + kNV, S_FREE = S_FULL + 2, P_FULL = S_FREE + 2, PV_DONE = P_FULL + 2, O_FULL, O_EMPTY,
+  S_FULL = V_EMPTY + kNV, S_FREE = S_FULL + 2, P_FULL = S_FREE + 2, PV_DONE = P_FULL + 2, O_FULL = PV_DONE + 2,
+  O_EMPTY,
   I_FULL, I_EMPTY = I_FULL + kNI, TEAR = I_EMPTY + kNI, NBAR
 };
 constexpr uint32_t kOffRing = kOffBar + 8 * NBAR;
@@ -62,6 +63,12 @@ __device__ __forceinline__ float ex2f(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -116,6 +123,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       mbar_init(bar(P_FULL + b), 128);
     }
     mbar_init(bar(PV_DONE), 1);
+    mbar_init(bar(PV_DONE + 1), 1);
     mbar_init(bar(O_FULL), 1);
     mbar_init(bar(O_EMPTY), 128);
     for (int r = 0; r < kNI; ++r) {
@@ -222,25 +230,28 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {
       constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idO = idesc_bf16(128, 128, 0, 1);
       uint32_t it_use = 0, q_use = 0, k_use = 0, v_use = 0, s_issue = 0, pv = 0, o_items = 0;
       bool issued_any = false;
       auto issue_s = [&]() -> bool {
         const uint32_t b = s_issue & 1u, ks = k_use % kNK;
-        if (!wait(bar(S_FREE + b), ((s_issue >> 1) & 1u) ^ 1u, g)) return false;
-        if (!wait(bar(K_FULL + ks), (k_use / kNK) & 1u, g)) return false;
+        if (!wait_warp(bar(S_FREE + b), ((s_issue >> 1) & 1u) ^ 1u, g)) return false;
+        if (!wait_warp(bar(K_FULL + ks), (k_use / kNK) & 1u, g)) return false;
         fence_after();
         const uint32_t kb = sK + ks * kTile;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
-          mma_ss(tmem + kColS + b * 128u, smem_desc(sQ + off, 16, 1024, kSwizzle128B),
-                 smem_desc(kb + off, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
+            mma_ss(tmem + kColS + b * 128u, smem_desc(sQ + off, 16, 1024, kSwizzle128B),
+                   smem_desc(kb + off, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
+          }
+          commit(bar(S_FULL + b));
+          commit(bar(K_EMPTY + ks));
         }
-        commit(bar(S_FULL + b));
-        commit(bar(K_EMPTY + ks));
+        __syncwarp();
         ++s_issue;
         ++k_use;
         issued_any = true;
@@ -248,44 +259,52 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       };
       for (;;) {
         const int ri = (int)(it_use % kNI);
-        if (!wait(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
+        if (!wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
         const int2 ent = make_int2(ring[ri].x, ring[ri].y);
-        mbar_arrive(bar(I_EMPTY + ri));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
         ++it_use;
         if (ent.y == -2) break;
         if (ent.y <= 0) continue;
         const int len = ent.y;
-        if (!wait(bar(Q_FULL), q_use & 1u, g)) break;
+        if (!wait_warp(bar(Q_FULL), q_use & 1u, g)) break;
         ++q_use;
         bool ok = issue_s();
         for (int e = 0; e < len && ok; ++e) {
           if (e + 1 < len) {
             if (!(ok = issue_s())) break;
           } else {
-            commit(bar(Q_EMPTY));   // every S of this item is issued: Q may be replaced
+            if (elect_one()) commit(bar(Q_EMPTY));   // every S of this item is issued: Q may be replaced
+            __syncwarp();
           }
           const uint32_t b = pv & 1u, vs = v_use % kNV;
-          if (!(ok = wait(bar(V_FULL + vs), (v_use / kNV) & 1u, g))) break;
-          if (!(ok = wait(bar(P_FULL + b), (pv >> 1) & 1u, g))) break;
-          if (e == 0 && !(ok = wait(bar(O_EMPTY), (o_items & 1u) ^ 1u, g))) break;
+          if (!(ok = wait_warp(bar(V_FULL + vs), (v_use / kNV) & 1u, g))) break;
+          if (!(ok = wait_warp(bar(P_FULL + b), (pv >> 1) & 1u, g))) break;
+          if (e == 0 && !(ok = wait_warp(bar(O_EMPTY), (o_items & 1u) ^ 1u, g))) break;
           fence_after();
           const uint32_t vb = sV + vs * kTile;
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < BT / 16; ++kk)
-            mma_ts(tmem + kColO, tmem + kColP + b * 64u + (uint32_t)kk * 8u,
-                   smem_desc(vb + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), idO,
-                   (e > 0 || kk > 0) ? 1u : 0u);
-          commit(bar(V_EMPTY + vs));
-          commit(bar(PV_DONE));
+            for (int kk = 0; kk < BT / 16; ++kk)
+              mma_ts(tmem + kColO, tmem + kColP + b * 64u + (uint32_t)kk * 8u,
+                     smem_desc(vb + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), idO,
+                     (e > 0 || kk > 0) ? 1u : 0u);
+            commit(bar(V_EMPTY + vs));
+            commit(bar(PV_DONE + b));
+          }
+          __syncwarp();
           ++v_use;
           ++pv;
         }
         if (!ok) break;
-        commit(bar(O_FULL));
+        if (elect_one()) commit(bar(O_FULL));
+        __syncwarp();
         ++o_items;
       }
       if (*abort_flag && issued_any) {
-        commit(bar(TEAR));
+        // the elected lane issued every MMA; its commit covers all of them
+        if (elect_one()) commit(bar(TEAR));
+        __syncwarp();
         wait_raw(bar(TEAR), 0, kDrainNs);
       }
     }
@@ -331,16 +350,25 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         fence_before();
         mbar_arrive(bar(S_FREE + b));
         ++s_use;
-        float mx = __uint_as_float(s[0]);
+        // row max as a tree of 3-input maxima (8 independent partials): max is
+        // exact in any order, and a serial chain would sit on the critical path
+        float part[8];
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+        for (int u = 0; u < 8; ++u) part[u] = __uint_as_float(s[u]);
+#pragma unroll
+        for (int c = 8; c < 128; c += 16)
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            part[u] = fmax3(part[u], __uint_as_float(s[c + u]), __uint_as_float(s[c + 8 + u]));
+        const float mx = fmax3(fmax3(part[0], part[1], part[2]), fmax3(part[3], part[4], part[5]),
+                               fmaxf(part[6], part[7]));
         const float m_new = fmaxf(m, mx * sl2);
-        bool waited = false;
         if (e == 0) {
           m = m_new;
         } else if (__any_sync(0xffffffffu, m_new > m + kRescaleThreshold)) {
-          if (!(ok = wait_warp(bar(PV_DONE), (uint32_t)((blocks_done + e - 1) & 1u), g))) break;
-          waited = true;
+          // O must not change under the PV of block g-1 (g = global block index)
+          const uint64_t gp = blocks_done + e - 1;
+          if (!(ok = wait_warp(bar(PV_DONE + (uint32_t)(gp & 1u)), (uint32_t)((gp >> 1) & 1u), g))) break;
           fence_after();
           const float f = ex2f(m - m_new);
 #pragma unroll
@@ -357,17 +385,21 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           m = m_new;
         }
         uint32_t pk[64];
-        float rs = 0.f;
+        float rs[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) rs[u] = 0.f;
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           const float p0 = ex2f(fmaf(__uint_as_float(s[2 * c]), sl2, -m));
           const float p1 = ex2f(fmaf(__uint_as_float(s[2 * c + 1]), sl2, -m));
-          rs += p0 + p1;
+          rs[c & 7] += p0 + p1;
           pk[c] = pack2(p0, p1);
         }
-        l += rs;
-        if (e > 0 && !waited) {
-          if (!(ok = wait_warp(bar(PV_DONE), (uint32_t)((blocks_done + e - 1) & 1u), g))) break;
+        l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+        // P buffer b was last read by the PV of block g-2
+        const uint64_t gb = blocks_done + e;
+        if (gb >= 2) {
+          if (!(ok = wait_warp(bar(PV_DONE + b), (uint32_t)(((gb - 2) >> 1) & 1u), g))) break;
           fence_after();
         }
         tmem_st32(t_row + kColP + b * 64u, pk);
