@@ -1,18 +1,21 @@
 // Step 5a, bf16, Bt = d = 128 on sm_103a: block-sparse flash-attention forward
 // on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
 //
-// One persistent CTA per SM, 6 warps:
+// One persistent CTA per SM, 7 warps:
 //   warp 4     producer: pulls (b, h, query block) items longest-first through
 //              an atomic counter, validates the CSR row, publishes the item in
 //              a shared-memory ring, and TMA-loads Q_i and the selected K_j / V_j
 //              tiles (128 x 128 bf16, two 64-column boxes with 128-byte swizzle)
-//              into a 3-stage K ring and a 2-stage V ring, addressed through
+//              into 3-stage K and V rings, addressed through
 //              the CSR (row coordinate = bh*N + j*128).
-//   warp 5     MMA issuer (whole warp; one elected lane issues): S_j = Q K_j^T into one of two TMEM S
-//              buffers (M=N=128, K=16 per instruction, both operands K-major
-//              from shared memory), issued one block ahead of O += P_j V_j
-//              (A = P_j read from TMEM as packed bf16, B = V_j MN-major from
-//              shared memory). Completion is signalled with tcgen05.commit.
+//   warp 5     S issuer: S_j = Q K_j^T into one of two TMEM S buffers (M=N=128,
+//              K=16 per instruction, both operands K-major from shared memory).
+//   warp 6     PV issuer: O += P_j V_j (A = P_j read from TMEM as packed bf16,
+//              B = V_j MN-major from shared memory).
+//              The two GEMM streams are issued by different warps so that a
+//              wait in one (for P, or for a free S buffer) never holds back the
+//              other; each warp runs uniformly and one elected lane issues
+//              tcgen05.mma / tcgen05.commit.
 //   warps 0-3  softmax and epilogue: thread t owns query row t = TMEM lane t.
 //              It reads its S row from TMEM, keeps a running max m and sum l in
 //              base 2, writes P = exp2(S*scale*log2e - m) as bf16 into TMEM, and
@@ -33,17 +36,17 @@ namespace {
 using namespace tc;
 
 constexpr int BT = 128, D = 128;
-constexpr int kNK = 3, kNV = 2, kNI = 4;
+constexpr int kNK = 3, kNV = 3, kNI = 4;
 constexpr uint32_t kTile = BT * D * 2;      // 32 KB
 constexpr uint32_t kHalfTile = BT * 64 * 2; // one 64-column swizzled box: 16 KB
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;   // 4 softmax warps, producer, S issuer, PV issuer
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
 constexpr uint32_t kOffK = kTile, kOffV = kOffK + kNK * kTile, kOffBar = kOffV + kNV * kTile;
 enum Bar {
   Q_FULL = 0, Q_EMPTY, K_FULL, K_EMPTY = K_FULL + kNK, V_FULL = K_EMPTY + kNK, V_EMPTY = V_FULL + kNV,
   S_FULL = V_EMPTY + kNV, S_FREE = S_FULL + 2, P_FULL = S_FREE + 2, PV_DONE = P_FULL + 2, O_FULL = PV_DONE + 2,
   O_EMPTY,
-  I_FULL, I_EMPTY = I_FULL + kNI, TEAR = I_EMPTY + kNI, NBAR
+  I_FULL, I_EMPTY = I_FULL + kNI, TEAR = I_EMPTY + kNI, TEAR_PV, NBAR
 };
 constexpr uint32_t kOffRing = kOffBar + 8 * NBAR;
 constexpr uint32_t kOffMisc = kOffRing + 8 * kNI;
@@ -128,9 +131,10 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     mbar_init(bar(O_EMPTY), 128);
     for (int r = 0; r < kNI; ++r) {
       mbar_init(bar(I_FULL + r), 1);
-      mbar_init(bar(I_EMPTY + r), 5);
+      mbar_init(bar(I_EMPTY + r), 6);
     }
     mbar_init(bar(TEAR), 1);
+    mbar_init(bar(TEAR_PV), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -229,16 +233,27 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         if (v_fill > s) wait_raw(bar(V_FULL + s), ((v_fill - 1 - s) / kNV) & 1u, kDrainNs);
     }
   } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
-    {
-      constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t idO = idesc_bf16(128, 128, 0, 1);
-      uint32_t it_use = 0, q_use = 0, k_use = 0, v_use = 0, s_issue = 0, pv = 0, o_items = 0;
-      bool issued_any = false;
-      auto issue_s = [&]() -> bool {
+    // ------------------------------------------------------------ S = Q K^T issuer
+    constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
+    uint32_t it_use = 0, q_use = 0, k_use = 0, s_issue = 0;
+    bool issued_any = false;
+    for (;;) {
+      const int ri = (int)(it_use % kNI);
+      if (!wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
+      const int2 ent = make_int2(ring[ri].x, ring[ri].y);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
+      ++it_use;
+      if (ent.y == -2) break;
+      if (ent.y <= 0) continue;
+      const int len = ent.y;
+      if (!wait_warp(bar(Q_FULL), q_use & 1u, g)) break;
+      ++q_use;
+      bool ok = true;
+      for (int e = 0; e < len; ++e) {
         const uint32_t b = s_issue & 1u, ks = k_use % kNK;
-        if (!wait_warp(bar(S_FREE + b), ((s_issue >> 1) & 1u) ^ 1u, g)) return false;
-        if (!wait_warp(bar(K_FULL + ks), (k_use / kNK) & 1u, g)) return false;
+        if (!(ok = wait_warp(bar(S_FREE + b), ((s_issue >> 1) & 1u) ^ 1u, g))) break;
+        if (!(ok = wait_warp(bar(K_FULL + ks), (k_use / kNK) & 1u, g))) break;
         fence_after();
         const uint32_t kb = sK + ks * kTile;
         if (elect_one()) {
@@ -250,63 +265,66 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           }
           commit(bar(S_FULL + b));
           commit(bar(K_EMPTY + ks));
+          if (e + 1 == len) commit(bar(Q_EMPTY));   // every S of this item is issued
         }
         __syncwarp();
         ++s_issue;
         ++k_use;
         issued_any = true;
-        return true;
-      };
-      for (;;) {
-        const int ri = (int)(it_use % kNI);
-        if (!wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
-        const int2 ent = make_int2(ring[ri].x, ring[ri].y);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
-        ++it_use;
-        if (ent.y == -2) break;
-        if (ent.y <= 0) continue;
-        const int len = ent.y;
-        if (!wait_warp(bar(Q_FULL), q_use & 1u, g)) break;
-        ++q_use;
-        bool ok = issue_s();
-        for (int e = 0; e < len && ok; ++e) {
-          if (e + 1 < len) {
-            if (!(ok = issue_s())) break;
-          } else {
-            if (elect_one()) commit(bar(Q_EMPTY));   // every S of this item is issued: Q may be replaced
-            __syncwarp();
-          }
-          const uint32_t b = pv & 1u, vs = v_use % kNV;
-          if (!(ok = wait_warp(bar(V_FULL + vs), (v_use / kNV) & 1u, g))) break;
-          if (!(ok = wait_warp(bar(P_FULL + b), (pv >> 1) & 1u, g))) break;
-          if (e == 0 && !(ok = wait_warp(bar(O_EMPTY), (o_items & 1u) ^ 1u, g))) break;
-          fence_after();
-          const uint32_t vb = sV + vs * kTile;
-          if (elect_one()) {
+      }
+      if (!ok) break;
+    }
+    if (*abort_flag && issued_any) {
+      if (elect_one()) commit(bar(TEAR));
+      __syncwarp();
+      wait_raw(bar(TEAR), 0, kDrainNs);
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ O += P V issuer
+    constexpr uint32_t idO = idesc_bf16(128, 128, 0, 1);
+    uint32_t it_use = 0, v_use = 0, pv = 0, o_items = 0;
+    bool issued_any = false;
+    for (;;) {
+      const int ri = (int)(it_use % kNI);
+      if (!wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
+      const int2 ent = make_int2(ring[ri].x, ring[ri].y);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
+      ++it_use;
+      if (ent.y == -2) break;
+      if (ent.y <= 0) continue;
+      const int len = ent.y;
+      bool ok = true;
+      for (int e = 0; e < len; ++e) {
+        const uint32_t b = pv & 1u, vs = v_use % kNV;
+        if (!(ok = wait_warp(bar(V_FULL + vs), (v_use / kNV) & 1u, g))) break;
+        if (!(ok = wait_warp(bar(P_FULL + b), (pv >> 1) & 1u, g))) break;
+        if (e == 0 && !(ok = wait_warp(bar(O_EMPTY), (o_items & 1u) ^ 1u, g))) break;
+        fence_after();
+        const uint32_t vb = sV + vs * kTile;
+        if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < BT / 16; ++kk)
-              mma_ts(tmem + kColO, tmem + kColP + b * 64u + (uint32_t)kk * 8u,
-                     smem_desc(vb + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), idO,
-                     (e > 0 || kk > 0) ? 1u : 0u);
-            commit(bar(V_EMPTY + vs));
-            commit(bar(PV_DONE + b));
-          }
-          __syncwarp();
-          ++v_use;
-          ++pv;
+          for (int kk = 0; kk < BT / 16; ++kk)
+            mma_ts(tmem + kColO, tmem + kColP + b * 64u + (uint32_t)kk * 8u,
+                   smem_desc(vb + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), idO,
+                   (e > 0 || kk > 0) ? 1u : 0u);
+          commit(bar(V_EMPTY + vs));
+          commit(bar(PV_DONE + b));
+          if (e + 1 == len) commit(bar(O_FULL));
         }
-        if (!ok) break;
-        if (elect_one()) commit(bar(O_FULL));
         __syncwarp();
-        ++o_items;
+        ++v_use;
+        ++pv;
+        issued_any = true;
       }
-      if (*abort_flag && issued_any) {
-        // the elected lane issued every MMA; its commit covers all of them
-        if (elect_one()) commit(bar(TEAR));
-        __syncwarp();
-        wait_raw(bar(TEAR), 0, kDrainNs);
-      }
+      if (!ok) break;
+      ++o_items;
+    }
+    if (*abort_flag && issued_any) {
+      if (elect_one()) commit(bar(TEAR_PV));
+      __syncwarp();
+      wait_raw(bar(TEAR_PV), 0, kDrainNs);
     }
     __syncwarp();
   } else {
