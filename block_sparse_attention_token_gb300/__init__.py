@@ -300,3 +300,4 @@ def default_scale(d: int) -> float:
 
 
 from .pipeline import Pipeline  # noqa: E402,F401
+from .streaming import HostPipeline  # noqa: E402,F401

@@ -65,9 +65,10 @@ class Pipeline:
             self.dq, self.dk, self.dv = (torch.empty((s.B, s.N, s.H, s.d), dtype=dt, device=dev)
                                          for _ in range(3))
 
-    def forward(self, q, k, v, wq=None, wk=None, prof: bool = False, mark=None):
+    def forward(self, q, k, v, wq=None, wk=None, prof: bool = False, mark=None, out=None):
         """mark: optional callable(stage_name) invoked after each stage is enqueued
-        (used to record CUDA events on the current stream)."""
+        (used to record CUDA events on the current stream). out: optional raster
+        output buffer (default: self.o)."""
         s = self.shape
         mark = mark or (lambda name: None)
         reorder(s, q, self.qb)
@@ -83,9 +84,10 @@ class Pipeline:
         attn_fwd(s, self.qb, self.kb, self.vb, self.row_ptr, self.col_idx, 0.0, self.ob, self.lse, self.ws_attn,
                  self.flags, self.prof if prof else None, self.status)
         mark("attn_fwd")
-        reorder(s, self.ob, self.o, inverse=True)
+        o = self.o if out is None else out
+        reorder(s, self.ob, o, inverse=True)
         mark("reorder_out")
-        return self.o, self.lse
+        return o, self.lse
 
     def backward(self, dout, prof: bool = False, mark=None):
         s = self.shape

@@ -1,0 +1,61 @@
+"""Forward steps from pinned host memory to pinned host memory, overlapped.
+
+HostPipeline.step() enqueues one whole forward step for inputs that live in
+pinned host buffers and writes O back to a pinned host buffer. The device
+input and output buffers are double-buffered and the copies run on their own
+streams, so the host-to-device copy of step n+1 and the device-to-host copy of
+step n-1 overlap the kernels of step n. Every step still copies its own inputs
+in and its own result out; events order each buffer's reuse.
+"""
+from __future__ import annotations
+
+import torch
+
+from .pipeline import Pipeline
+
+
+class HostPipeline:
+    def __init__(self, pipe: Pipeline):
+        self.pipe = pipe
+        s = pipe.shape
+        dt = s.torch_dtype
+        raster = (s.B, s.N, s.H, s.d)
+        self.inp = [[torch.empty(raster, dtype=dt, device="cuda") for _ in range(3)] for _ in range(2)]
+        self.out = [torch.empty(raster, dtype=dt, device="cuda") for _ in range(2)]
+        self.h2d = torch.cuda.Stream()
+        self.d2h = torch.cuda.Stream()
+        cur = torch.cuda.current_stream()
+        mk = lambda: [torch.cuda.Event() for _ in range(2)]
+        self.in_ready, self.in_free, self.out_ready, self.out_free = mk(), mk(), mk(), mk()
+        for evs in (self.in_ready, self.in_free, self.out_ready, self.out_free):
+            for e in evs:
+                e.record(cur)
+        self.n = 0
+
+    def step(self, hq, hk, hv, ho, wq=None, wk=None):
+        """One forward step: pinned host q, k, v (raster) in, pinned host O out."""
+        b = self.n & 1
+        cur = torch.cuda.current_stream()
+        with torch.cuda.stream(self.h2d):
+            self.h2d.wait_event(self.in_free[b])          # step n-2 has consumed these buffers
+            for dst, src in zip(self.inp[b], (hq, hk, hv)):
+                dst.copy_(src, non_blocking=True)
+            self.in_ready[b].record(self.h2d)
+        cur.wait_event(self.in_ready[b])
+        cur.wait_event(self.out_free[b])                   # step n-2's O has left the device
+
+        def mark(name):
+            if name == "reorder":                          # raster inputs are no longer read
+                self.in_free[b].record(cur)
+
+        self.pipe.forward(*self.inp[b], wq=wq, wk=wk, mark=mark, out=self.out[b])
+        self.out_ready[b].record(cur)
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(self.out_ready[b])
+            ho.copy_(self.out[b], non_blocking=True)
+            self.out_free[b].record(self.d2h)
+        self.n += 1
+        return ho
+
+    def synchronize(self):
+        self.d2h.synchronize()

@@ -297,3 +297,28 @@ def test_pipeline_end_to_end(name):
         b, h, i = r // (g.H * g.nb), (r // g.nb) % g.H, r % g.nb
         sl = slice(i * g.Bt, (i + 1) * g.Bt)
         compare_values(ob[b, h, sl], O[b, h, sl], wl, f"O row {r}")
+
+
+def test_host_pipeline_overlapped_steps_match_device_pipeline():
+    """Pinned-host streaming (copies overlapped with neighbouring steps) gives,
+    step for step, exactly what the device pipeline gives."""
+    wl = SMALL["r128"]
+    _, data = workload(wl)
+    shape = sp.shape_of(wl)
+    pipe = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P)
+    hp = sp.HostPipeline(pipe)
+    steps = []
+    for n in range(4):
+        scale = 1.0 + 0.25 * n
+        hq, hk, hv = (torch.from_numpy(synth.round_bf16(data[x] * np.float32(scale))).bfloat16().pin_memory()
+                      for x in "qkv")
+        steps.append((hq, hk, hv, torch.empty_like(hq).pin_memory()))
+    for hq, hk, hv, ho in steps:
+        hp.step(hq, hk, hv, ho)
+    hp.synchronize()
+    torch.cuda.synchronize()
+    for hq, hk, hv, ho in steps:
+        o, _ = pipe.forward(hq.cuda(), hk.cuda(), hv.cuda())
+        torch.cuda.synchronize()
+        assert torch.equal(ho, o.cpu())
+    assert pipe.status.item() == 0
