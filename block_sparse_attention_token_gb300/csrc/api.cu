@@ -61,6 +61,7 @@ struct AttnWs {
   int32_t* row_idx;    // [B*H*nb*nb]
   int32_t* items2;     // [rows] order over CSC columns
   float* delta;        // [B*H*N]
+  float* lse2;         // [B*H*N] LSE * log2(e)
   size_t bytes;
 };
 
@@ -82,6 +83,7 @@ AttnWs attn_ws_layout(const Dims& s, bool backward, void* base) {
     w.row_idx = (int32_t*)take(rows * (size_t)s.nb * 4);
     w.items2 = (int32_t*)take(rows * 4);
     w.delta = (float*)take((size_t)s.B * s.H * s.N * 4);
+    w.lse2 = (float*)take((size_t)s.B * s.H * s.N * 4);
   }
   w.bytes = off;
   return w;
@@ -337,12 +339,26 @@ sparsp_status_t sparsp_attn_bwd(const sparsp_shape_t* shape, const void* q, cons
   cudaStream_t st = (cudaStream_t)stream;
   const bool flat = (flags & SPARSP_SCHED_FLAT) != 0;
   typedef const __nv_bfloat16* cb;
-  r = launch_bwd_rowdot(s, (cb)o, (cb)dout, w.delta, st);
+  const bool tc = !(flags & SPARSP_KERNEL_PORTABLE) && attn_bwd_tc_supported(s);
+  r = launch_bwd_rowdot(s, (cb)o, (cb)dout, w.delta, lse, tc ? w.lse2 : nullptr, st);
   if (r != SPARSP_OK) return r;
   r = launch_csr_transpose(s, row_ptr, col_idx, w.col_ptr, w.row_idx, d_status, st);
   if (r != SPARSP_OK) return r;
   r = launch_lpt(s, row_ptr, flat, w.items, w.counter, w.hist, st);
   if (r != SPARSP_OK) return r;
+  if (tc) {
+    r = launch_attn_bwd_tc(s, 0, (cb)q, (cb)k, (cb)v, (cb)dout, w.lse2, w.delta, row_ptr, col_idx, scale,
+                           (__nv_bfloat16*)dq, w.items, w.counter, prof, d_status, st);
+    if (r != SPARSP_OK) return r;
+    r = launch_lpt(s, w.col_ptr, flat, w.items2, w.counter + 1, w.hist, st);
+    if (r != SPARSP_OK) return r;
+    r = launch_attn_bwd_tc(s, 1, (cb)q, (cb)k, (cb)v, (cb)dout, w.lse2, w.delta, w.col_ptr, w.row_idx,
+                           scale, (__nv_bfloat16*)dk, w.items2, w.counter + 1, prof, d_status, st);
+    if (r != SPARSP_OK) return r;
+    if (cudaMemsetAsync(w.counter + 2, 0, sizeof(int32_t), st) != cudaSuccess) return SPARSP_ERR_CUDA;
+    return launch_attn_bwd_tc(s, 2, (cb)q, (cb)k, (cb)v, (cb)dout, w.lse2, w.delta, w.col_ptr, w.row_idx,
+                              scale, (__nv_bfloat16*)dv, w.items2, w.counter + 2, prof, d_status, st);
+  }
   r = launch_attn_bwd_dq(s, (cb)q, (cb)k, (cb)v, (cb)dout, lse, w.delta, row_ptr, col_idx, scale,
                          (__nv_bfloat16*)dq, w.items, w.counter, prof, d_status, st);
   if (r != SPARSP_OK) return r;

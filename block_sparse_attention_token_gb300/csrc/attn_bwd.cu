@@ -1,7 +1,8 @@
 // Step 5b: block-sparse attention backward (bf16 in, fp32 accumulate), with
 // the selection held fixed.
 //
-//  rowdot_kernel - D = rowsum(dO * O) per query token (fp32).
+//  rowdot_kernel - D = rowsum(dO * O) per query token (fp32), and optionally
+//                  LSE * log2(e) for the tcgen05 backward.
 //  dq_kernel     - one work item per query block (CSR row): for each selected
 //                  key block, recompute P = exp2(S*log2e*scale - LSE*log2e),
 //                  dP = dO V^T, dS = P (dP - D), dQ += dS K. dQ stays in
@@ -24,7 +25,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 __global__ void __launch_bounds__(256)
 rowdot_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
-              int64_t rows, int d, float* __restrict__ delta) {
+              int64_t rows, int d, float* __restrict__ delta, const float* __restrict__ lse,
+              float* __restrict__ lse2) {
   // 8 threads per row (d <= 128: 16 bf16 each) -> 32 rows per CTA
   const int64_t row = (int64_t)blockIdx.x * 32 + (threadIdx.x >> 3);
   const int sub = threadIdx.x & 7;
@@ -46,7 +48,10 @@ rowdot_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restri
   }
 #pragma unroll
   for (int off = 4; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (row < rows && sub == 0) delta[row] = acc;
+  if (row < rows && sub == 0) {
+    delta[row] = acc;
+    if (lse2 != nullptr) lse2[row] = lse[row] * kLog2e;   // -inf stays -inf
+  }
 }
 
 template <int BT, int D>
@@ -393,9 +398,9 @@ sparsp_status_t persistent_grid(K kern, int threads, int smem, int64_t n_items, 
 }  // namespace
 
 sparsp_status_t launch_bwd_rowdot(const Dims& s, const __nv_bfloat16* o, const __nv_bfloat16* dout,
-                                  float* delta, cudaStream_t st) {
+                                  float* delta, const float* lse, float* lse2, cudaStream_t st) {
   const int64_t rows = (int64_t)s.B * s.H * s.N;
-  rowdot_kernel<<<(unsigned)((rows + 31) / 32), 256, 0, st>>>(o, dout, rows, s.d, delta);
+  rowdot_kernel<<<(unsigned)((rows + 31) / 32), 256, 0, st>>>(o, dout, rows, s.d, delta, lse, lse2);
   SPARSP_LAUNCH_CHECK();
   return SPARSP_OK;
 }

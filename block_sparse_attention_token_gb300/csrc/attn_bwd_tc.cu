@@ -1,0 +1,486 @@
+// Step 5b, bf16, Bt = d = 128 on sm_103a: block-sparse attention backward on
+// the tcgen05 tensor cores, as three persistent kernels of one template.
+//
+//   mode 0 (dQ): item = query block i, blocks = its CSR row.
+//                S = Q_i K_c^T, dP = dO_i V_c^T, dS = P (dP - D), dQ += dS K_c.
+//   mode 1 (dK): item = key block j, blocks = the query blocks that selected it.
+//                S^T = K_j Q_c^T, dP^T = V_j dO_c^T, dS^T = P^T (dP^T - D), dK += dS^T Q_c.
+//   mode 2 (dV): item = key block j, as mode 1.  S^T = K_j Q_c^T, dV += P^T dO_c.
+// with P = exp2(S * scale*log2e - LSE*log2e) from the forward's LSE (no online
+// maximum is needed), D = rowsum(dO * O), and dQ, dK scaled by `scale` at the
+// end. The three kernels recompute S (and dP) instead of sharing it so that
+// every one fits TMEM without aliasing: S [0,128), dP [128,256), the fp32
+// accumulator [256,384), and two bf16 operand buffers X0 [384,448),
+// X1 [448,512) holding P or dS for the accumulate MMA. Sums are taken in a
+// fixed order (no atomics), so results are bitwise reproducible.
+//
+// One persistent CTA per SM, 7 warps (the forward kernel's structure):
+//   warp 4     producer: pulls items longest-first, validates the block list,
+//              TMA-loads the item's two row tiles (A1, A2) once and, per block,
+//              the two column tiles (B1, B2; two 64-column boxes each, 128-byte
+//              swizzle) into a 2-stage ring; in modes 1 and 2 also the block's
+//              LSE*log2e and D (512 bytes each) by 1-D bulk copy.
+//   warp 5     S issuer: S = A1 B1^T and (modes 0, 1) dP = A2 B2^T, both
+//              operands K-major from shared memory.
+//   warp 6     accumulate issuer: ACC += X B3 with X from TMEM and B3 (the
+//              column tile K_c, Q_c or dO_c) MN-major from shared memory.
+//   warps 0-3  thread t owns row t (TMEM lane t): P and dS in fp32 from S, dP
+//              and the statistics, packed to bf16 into X; epilogue ACC -> global.
+// Every mbarrier wait is bounded (2 s): on expiry the CTA reports
+// SPARSP_ERR_TIMEOUT, all roles leave, in-flight copies and MMAs are drained
+// with a second bounded wait and TMEM is released.
+#include "tc_helpers.cuh"
+
+namespace sparsp {
+namespace {
+
+using namespace tc;
+
+constexpr int BT = 128, D = 128;
+constexpr int kNS = 2, kNI = 4;
+constexpr uint32_t kTile = BT * D * 2;        // 32 KB
+constexpr uint32_t kHalfTile = BT * 64 * 2;   // one 64-column swizzled box
+constexpr uint32_t kStats = 1024;             // LSE*log2e [128] + D [128] of a column block
+constexpr int kThreads = 224;
+constexpr uint32_t kColS = 0, kColP = 128, kColAcc = 256, kColX = 384;
+constexpr uint32_t kOffA2 = kTile, kOffStage = 2 * kTile;
+constexpr uint32_t kStageBytes = 2 * kTile + kStats;   // a multiple of 1024: tiles stay aligned
+constexpr uint32_t kOffBar = kOffStage + kNS * kStageBytes;
+enum Bar {
+  A_FULL = 0, A_EMPTY, C_FULL, C_EMPTY = C_FULL + kNS, SD_FULL = C_EMPTY + kNS, SD_FREE, X_FULL,
+  X_DONE = X_FULL + 2, ACC_FULL = X_DONE + 2, ACC_EMPTY, I_FULL, I_EMPTY = I_FULL + kNI,
+  TEAR = I_EMPTY + kNI, TEAR2, NBAR
+};
+constexpr uint32_t kOffRing = kOffBar + 8 * NBAR;
+constexpr uint32_t kOffMisc = kOffRing + 8 * kNI;
+constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kDrainNs = 200000000ull;
+
+__device__ __forceinline__ bool wait_raw(uint32_t bar, uint32_t parity, uint64_t limit) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > limit) return false;
+  return true;
+}
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+struct Params {
+  const int32_t* ptr;    // CSR row_ptr (mode 0) or CSC col_ptr (modes 1, 2)
+  const int32_t* idx;    // CSR col_idx or CSC row_idx
+  int64_t N;
+  int nb;
+  int64_t n_items;
+  float sl2;             // scale * log2(e)
+  float out_scale;       // scale for dQ and dK, 1 for dV
+  const float* lse2;     // LSE * log2(e), [B*H*N]
+  const float* delta;    // rowsum(dO * O), [B*H*N]
+  __nv_bfloat16* out;
+  const int32_t* items;
+  int32_t* counter;
+  uint64_t* prof;
+  int32_t* d_status;
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constant__ CUtensorMap ta2,
+                   const __grid_constant__ CUtensorMap tb1, const __grid_constant__ CUtensorMap tb2,
+                   const Params p) {
+  constexpr bool kHasDP = MODE != 2;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sA1 = base, sA2 = base + kOffA2;
+  auto stage = [&](uint32_t st) -> uint32_t { return base + kOffStage + st * kStageBytes; };
+  auto bar = [&](int idx) -> uint32_t { return base + kOffBar + 8u * (uint32_t)idx; };
+  volatile int2* ring = reinterpret_cast<volatile int2*>(gbase + kOffRing);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kOffMisc);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + kOffMisc + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t t_start = globaltimer_ns();
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(A_FULL), 1);
+    mbar_init(bar(A_EMPTY), 1);
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(bar(C_FULL + s), 1);
+      mbar_init(bar(C_EMPTY + s), 1);
+    }
+    mbar_init(bar(SD_FULL), 1);
+    mbar_init(bar(SD_FREE), 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(X_FULL + b), 128);
+      mbar_init(bar(X_DONE + b), 1);
+    }
+    mbar_init(bar(ACC_FULL), 1);
+    mbar_init(bar(ACC_EMPTY), 128);
+    for (int r = 0; r < kNI; ++r) {
+      mbar_init(bar(I_FULL + r), 1);
+      mbar_init(bar(I_EMPTY + r), 6);
+    }
+    mbar_init(bar(TEAR), 1);
+    mbar_init(bar(TEAR2), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 4 && lane == 0) {
+    prefetch_tmap(&ta1);
+    prefetch_tmap(&ta2);
+    prefetch_tmap(&tb1);
+    prefetch_tmap(&tb2);
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Guard g{abort_flag, p.d_status, kWaitNs};
+  const int nb = p.nb;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    uint32_t it_fill = 0, a_fill = 0, c_fill = 0;
+    for (;;) {
+      int32_t slot = 0;
+      if (lane == 0) slot = atomicAdd(p.counter, 1);
+      slot = __shfl_sync(0xffffffffu, slot, 0);
+      int32_t item = -1, len = -2;
+      if (slot < p.n_items) {
+        item = p.items[slot];
+        const int32_t a = p.ptr[item], b = p.ptr[item + 1];
+        bool bad = (b < a) || (b - a > nb);
+        if (!bad)
+          for (int32_t e = a + lane; e < b; e += 32) {
+            const int32_t j = p.idx[e];
+            if (j < 0 || j >= nb) bad = true;
+          }
+        bad = __any_sync(0xffffffffu, bad);
+        if (bad) {
+          if (lane == 0) report(p.d_status, SPARSP_ERR_DATA);
+          len = -1;
+        } else {
+          len = b - a;
+        }
+      }
+      const int ri = (int)(it_fill % kNI);
+      if (!wait_warp(bar(I_EMPTY + ri), ((it_fill / kNI) & 1u) ^ 1u, g)) break;
+      if (lane == 0) {
+        ring[ri].x = item;
+        ring[ri].y = len;
+        mbar_arrive(bar(I_FULL + ri));
+      }
+      __syncwarp();
+      ++it_fill;
+      if (len == -2) break;
+      if (len <= 0) continue;
+      const int64_t bh = item / nb;
+      const int i = item % nb;
+      const int32_t ya = (int32_t)(bh * p.N + (int64_t)i * BT);
+      if (!wait_warp(bar(A_EMPTY), (a_fill & 1u) ^ 1u, g)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(A_FULL), kHasDP ? 2 * kTile : kTile);
+        tma_load_2d(sA1, &ta1, bar(A_FULL), 0, ya);
+        tma_load_2d(sA1 + kHalfTile, &ta1, bar(A_FULL), 64, ya);
+        if (kHasDP) {
+          tma_load_2d(sA2, &ta2, bar(A_FULL), 0, ya);
+          tma_load_2d(sA2 + kHalfTile, &ta2, bar(A_FULL), 64, ya);
+        }
+      }
+      ++a_fill;
+      const int32_t e0 = p.ptr[item];
+      bool ok = true;
+      for (int e = 0; e < len; ++e) {
+        const int32_t c = p.idx[e0 + e];
+        const int64_t yc64 = bh * p.N + (int64_t)c * BT;
+        const int32_t yc = (int32_t)yc64;
+        const uint32_t st = c_fill % kNS;
+        if (!(ok = wait_warp(bar(C_EMPTY + st), ((c_fill / kNS) & 1u) ^ 1u, g))) break;
+        if (lane == 0) {
+          const uint32_t sb = stage(st);
+          mbar_arrive_expect_tx(bar(C_FULL + st), 2 * kTile + (MODE != 0 ? kStats : 0u));
+          tma_load_2d(sb, &tb1, bar(C_FULL + st), 0, yc);
+          tma_load_2d(sb + kHalfTile, &tb1, bar(C_FULL + st), 64, yc);
+          tma_load_2d(sb + kTile, &tb2, bar(C_FULL + st), 0, yc);
+          tma_load_2d(sb + kTile + kHalfTile, &tb2, bar(C_FULL + st), 64, yc);
+          if (MODE != 0) {
+            bulk_load(sb + 2 * kTile, p.lse2 + yc64, 512, bar(C_FULL + st));
+            bulk_load(sb + 2 * kTile + 512, p.delta + yc64, 512, bar(C_FULL + st));
+          }
+        }
+        ++c_fill;
+      }
+      if (!ok) break;
+    }
+    if (*abort_flag && lane == 0) {
+      if (a_fill) wait_raw(bar(A_FULL), (a_fill - 1) & 1u, kDrainNs);
+      for (uint32_t s = 0; s < kNS; ++s)
+        if (c_fill > s) wait_raw(bar(C_FULL + s), ((c_fill - 1 - s) / kNS) & 1u, kDrainNs);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ S (and dP) issuer
+    constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
+    uint32_t it_use = 0, a_use = 0, c_use = 0, sd_issue = 0;
+    bool issued_any = false;
+    for (;;) {
+      const int ri = (int)(it_use % kNI);
+      if (!wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
+      const int2 ent = make_int2(ring[ri].x, ring[ri].y);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
+      ++it_use;
+      if (ent.y == -2) break;
+      if (ent.y <= 0) continue;
+      const int len = ent.y;
+      if (!wait_warp(bar(A_FULL), a_use & 1u, g)) break;
+      ++a_use;
+      bool ok = true;
+      for (int e = 0; e < len; ++e) {
+        const uint32_t st = c_use % kNS;
+        if (!(ok = wait_warp(bar(SD_FREE), (sd_issue & 1u) ^ 1u, g))) break;
+        if (!(ok = wait_warp(bar(C_FULL + st), (c_use / kNS) & 1u, g))) break;
+        fence_after();
+        const uint32_t sb = stage(st);
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
+            mma_ss(tmem + kColS, smem_desc(sA1 + off, 16, 1024, kSwizzle128B),
+                   smem_desc(sb + off, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
+          }
+          if (kHasDP) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
+              mma_ss(tmem + kColP, smem_desc(sA2 + off, 16, 1024, kSwizzle128B),
+                     smem_desc(sb + kTile + off, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
+            }
+          }
+          commit(bar(SD_FULL));
+          if (e + 1 == len) commit(bar(A_EMPTY));   // every MMA reading A1/A2 is issued
+        }
+        __syncwarp();
+        ++sd_issue;
+        ++c_use;
+        issued_any = true;
+      }
+      if (!ok) break;
+    }
+    if (*abort_flag && issued_any) {
+      if (elect_one()) commit(bar(TEAR));
+      __syncwarp();
+      wait_raw(bar(TEAR), 0, kDrainNs);
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ accumulate issuer
+    constexpr uint32_t idAcc = idesc_bf16(128, 128, 0, 1);
+    // the column tile the accumulator multiplies: K_c / Q_c (B1) or dO_c (B2)
+    constexpr uint32_t kB3 = MODE == 2 ? kTile : 0u;
+    uint32_t it_use = 0, c_use = 0, xg = 0, acc_items = 0;
+    bool issued_any = false;
+    for (;;) {
+      const int ri = (int)(it_use % kNI);
+      if (!wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
+      const int2 ent = make_int2(ring[ri].x, ring[ri].y);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
+      ++it_use;
+      if (ent.y == -2) break;
+      if (ent.y <= 0) continue;
+      const int len = ent.y;
+      bool ok = true;
+      for (int e = 0; e < len; ++e) {
+        const uint32_t b = xg & 1u, st = c_use % kNS;
+        if (!(ok = wait_warp(bar(X_FULL + b), (xg >> 1) & 1u, g))) break;
+        if (e == 0 && !(ok = wait_warp(bar(ACC_EMPTY), (acc_items & 1u) ^ 1u, g))) break;
+        fence_after();
+        const uint32_t b3 = stage(st) + kB3;
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < BT / 16; ++kk)
+            mma_ts(tmem + kColAcc, tmem + kColX + b * 64u + (uint32_t)kk * 8u,
+                   smem_desc(b3 + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), idAcc,
+                   (e > 0 || kk > 0) ? 1u : 0u);
+          commit(bar(X_DONE + b));
+          commit(bar(C_EMPTY + st));   // last reader of this stage
+          if (e + 1 == len) commit(bar(ACC_FULL));
+        }
+        __syncwarp();
+        ++xg;
+        ++c_use;
+        issued_any = true;
+      }
+      if (!ok) break;
+      ++acc_items;
+    }
+    if (*abort_flag && issued_any) {
+      if (elect_one()) commit(bar(TEAR2));
+      __syncwarp();
+      wait_raw(bar(TEAR2), 0, kDrainNs);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ P / dS and epilogue
+    const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
+    const float sl2 = p.sl2;
+    uint32_t it_use = 0, c_use = 0, sd_use = 0, xg = 0, acc_items = 0;
+    for (;;) {
+      const int ri = (int)(it_use % kNI);
+      if (!wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
+      const int2 ent = make_int2(ring[ri].x, ring[ri].y);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
+      ++it_use;
+      if (ent.y == -2) break;
+      if (ent.y == -1) continue;
+      const int64_t item = ent.x;
+      const int64_t bh = item / nb;
+      const int i = (int)(item % nb);
+      const int64_t row = bh * p.N + (int64_t)i * BT + threadIdx.x;
+      uint4* orow = reinterpret_cast<uint4*>(p.out + row * D);
+      const int len = ent.y;
+      if (len == 0) {
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      // mode 0: this thread's query row has one LSE and one D
+      const float own_l2 = MODE == 0 ? p.lse2[row] : 0.f;
+      const float own_d = MODE == 0 ? p.delta[row] : 0.f;
+      bool ok = true;
+      for (int e = 0; e < len; ++e) {
+        const uint32_t b = xg & 1u, st = c_use % kNS;
+        if (!(ok = wait_warp(bar(SD_FULL), sd_use & 1u, g))) break;
+        fence_after();
+        const float4* stats = reinterpret_cast<const float4*>(gbase + kOffStage + st * kStageBytes + 2 * kTile);
+        uint32_t xk[64];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sv[32], dv[32];
+          tmem_ld32(t_row + kColS + 32u * c, sv);
+          if (kHasDP) tmem_ld32(t_row + kColP + 32u * c, dv);
+          wait_ld();
+#pragma unroll
+          for (int x4 = 0; x4 < 8; ++x4) {
+            float l2[4], dd[4];
+            if (MODE == 0) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u) { l2[u] = own_l2; dd[u] = own_d; }
+            } else {
+              const float4 L = stats[c * 8 + x4];          // LSE*log2e of columns 32c+4x4 .. +3
+              const float4 Dv = stats[32 + c * 8 + x4];    // D of the same columns
+              l2[0] = L.x; l2[1] = L.y; l2[2] = L.z; l2[3] = L.w;
+              dd[0] = Dv.x; dd[1] = Dv.y; dd[2] = Dv.z; dd[3] = Dv.w;
+            }
+            float v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int x = 4 * x4 + u;
+              const float pr = ex2f(fmaf(__uint_as_float(sv[x]), sl2, -l2[u]));
+              v[u] = kHasDP ? pr * (__uint_as_float(dv[x]) - dd[u]) : pr;
+            }
+            xk[16 * c + 2 * x4] = pack2(v[0], v[1]);
+            xk[16 * c + 2 * x4 + 1] = pack2(v[2], v[3]);
+          }
+        }
+        fence_before();
+        mbar_arrive(bar(SD_FREE));
+        ++sd_use;
+        // X buffer b was last read by the accumulate MMA of block xg - 2
+        if (xg >= 2) {
+          if (!(ok = wait_warp(bar(X_DONE + b), ((xg - 2) >> 1) & 1u, g))) break;
+          fence_after();
+        }
+        tmem_st32(t_row + kColX + b * 64u, xk);
+        tmem_st32(t_row + kColX + b * 64u + 32u, xk + 32);
+        wait_st();
+        fence_before();
+        mbar_arrive(bar(X_FULL + b));
+        ++xg;
+        ++c_use;
+      }
+      if (!ok) break;
+      if (!wait_warp(bar(ACC_FULL), acc_items & 1u, g)) break;
+      ++acc_items;
+      fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(t_row + kColAcc + c * 32u, o);
+        wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x)
+          w[x] = pack2(__uint_as_float(o[2 * x]) * p.out_scale, __uint_as_float(o[2 * x + 1]) * p.out_scale);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) orow[c * 4 + x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+      }
+      fence_before();
+      mbar_arrive(bar(ACC_EMPTY));
+    }
+  }
+
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 5) tmem_dealloc(tmem, 512);
+  if (p.prof != nullptr && threadIdx.x == 0)
+    atomicAdd((unsigned long long*)&p.prof[smid() % SPARSP_PROF_SLOTS],
+              (unsigned long long)(globaltimer_ns() - t_start));
+}
+
+template <int MODE>
+sparsp_status_t go(const Dims& s, const CUtensorMap& a1, const CUtensorMap& a2, const CUtensorMap& b1,
+                   const CUtensorMap& b2, const Params& prm, cudaStream_t st) {
+  auto kern = attn_bwd_tc_kernel<MODE>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
+    return SPARSP_ERR_CUDA;
+  const int sms = device_sm_count();
+  if (sms <= 0) return SPARSP_ERR_CUDA;
+  int64_t grid = sms;
+  if (grid > s.rows()) grid = s.rows();
+  if (grid < 1) grid = 1;
+  kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(a1, a2, b1, b2, prm);
+  SPARSP_LAUNCH_CHECK();
+  return SPARSP_OK;
+}
+
+}  // namespace
+
+bool attn_bwd_tc_supported(const Dims& s) { return attn_fwd_tc_supported(s); }
+
+sparsp_status_t launch_attn_bwd_tc(const Dims& s, int mode, const __nv_bfloat16* q,
+                                   const __nv_bfloat16* k, const __nv_bfloat16* v,
+                                   const __nv_bfloat16* dout, const float* lse2,
+                                   const float* delta, const int32_t* ptr, const int32_t* idx,
+                                   float scale, __nv_bfloat16* out, const int32_t* items,
+                                   int32_t* counter, uint64_t* prof, int32_t* d_status,
+                                   cudaStream_t st) {
+  const uint64_t rows = (uint64_t)s.B * s.H * s.N;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_tmap_bf16_rows(&tq, q, rows, D, BT) || !make_tmap_bf16_rows(&tk, k, rows, D, BT) ||
+      !make_tmap_bf16_rows(&tv, v, rows, D, BT) || !make_tmap_bf16_rows(&tdo, dout, rows, D, BT))
+    return SPARSP_ERR_CUDA;
+  Params prm{ptr, idx, s.N, s.nb, s.rows(), scale * 1.4426950408889634f, mode == 2 ? 1.0f : scale,
+             lse2, delta, out, items, counter, prof, d_status};
+  if (mode == 0) return go<0>(s, tq, tdo, tk, tv, prm, st);
+  if (mode == 1) return go<1>(s, tk, tv, tq, tdo, prm, st);
+  return go<2>(s, tk, tk, tq, tdo, prm, st);
+}
+
+}  // namespace sparsp
