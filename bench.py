@@ -175,6 +175,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--flat", action="store_true", help="flat (cross-head) longest-first order")
     ap.add_argument("--portable", action="store_true", help="mma.sync attention kernel")
+    ap.add_argument("--unfused", action="store_true", help="separate pooling pass instead of reorder+pool")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--heads", type=int, default=0, help="override the head count (smaller profiling case)")
@@ -208,7 +209,8 @@ def main():
     data = synth.make(wl)
     shape = sp.shape_of(wl)
     flags = (sp.SCHED_FLAT if args.flat else 0) | (sp.KERNEL_PORTABLE if args.portable else 0)
-    pipe = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P, backward=wl.backward, flags=flags)
+    pipe = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P, backward=wl.backward, flags=flags,
+                       fused_estimation=not args.unfused)
     tdt = shape.torch_dtype
     host_in = {x: torch.from_numpy(data[x]).to(tdt).pin_memory() for x in ("q", "k", "v")}
     dev_in = {x: host_in[x].cuda() for x in host_in}
@@ -362,6 +364,7 @@ def main():
                    "row_len_min_max": [int(counts.min()), int(counts.max())],
                    "schedule": "flat" if args.flat else "head-grouped longest-first",
                    "kernel": "portable mma.sync" if args.portable else "default",
+                   "estimation": "separate pooling pass" if args.unfused else "fused with the reorder",
                    "l2": f"inputs larger than L2 ({shape.B * shape.H * shape.N * shape.d * 2 / 1e6:.0f} MB per tensor)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "stages_ms": stage_ms,

@@ -78,6 +78,9 @@ _SIG = {
     "sparsp_reorder": (_I32, [_P, _P, _P, _I32, _P]),
     "sparsp_block_scores_workspace_size": (ctypes.c_size_t, [_P, _I32, _I32]),
     "sparsp_block_scores": (_I32, [_P, _I32, _P, _P, _P, _P, _I32, _P, _P, ctypes.c_size_t, _P]),
+    "sparsp_reorder_pool": (_I32, [_P, _P, _P, _P, _P]),
+    "sparsp_block_scores_pooled_workspace_size": (ctypes.c_size_t, [_P, _I32, _I32]),
+    "sparsp_block_scores_pooled": (_I32, [_P, _I32, _P, _P, _P, _P, _I32, _P, _P, ctypes.c_size_t, _P]),
     "sparsp_select_workspace_size": (ctypes.c_size_t, [_P]),
     "sparsp_select": (_I32, [_P, _P, ctypes.c_float, _I32, _P, _P, _P, ctypes.c_size_t, _P, _P]),
     "sparsp_select_noalloc": (_I32, [_P, _P, ctypes.c_float, _I32, _P, _P, _P, _P]),
@@ -166,6 +169,31 @@ def block_scores(shape: Shape, q, k, estimator=EST_MEAN, wq=None, wk=None, rank=
         ws = _empty(block_scores_workspace_size(shape, estimator, rank), q.device)
     _check("sparsp_block_scores", lib().sparsp_block_scores(
         _sref(shape), estimator, _ptr(q), _ptr(k), _ptr(wq), _ptr(wk), rank, _ptr(out), _ptr(ws),
+        ws.numel(), _stream(stream)))
+    return out
+
+
+def reorder_pool(shape: Shape, x: torch.Tensor, out: torch.Tensor | None = None,
+                 means: torch.Tensor | None = None, stream=None):
+    """Raster -> blocked, plus the fp32 tile means [B, H, nb, d] from the same pass."""
+    if out is None:
+        out = torch.empty((shape.B, shape.H, shape.N, shape.d), dtype=x.dtype, device=x.device)
+    if means is None:
+        means = torch.empty((shape.B, shape.H, shape.nb, shape.d), dtype=torch.float32, device=x.device)
+    _check("sparsp_reorder_pool", lib().sparsp_reorder_pool(_sref(shape), _ptr(x), _ptr(out), _ptr(means),
+                                                            _stream(stream)))
+    return out, means
+
+
+def block_scores_pooled(shape: Shape, qmeans, kmeans, estimator=EST_MEAN, wq=None, wk=None, rank=16, out=None,
+                        ws=None, stream=None) -> torch.Tensor:
+    if out is None:
+        out = torch.empty((shape.B, shape.H, shape.nb, shape.nb), dtype=torch.float32, device=qmeans.device)
+    if ws is None:
+        n = lib().sparsp_block_scores_pooled_workspace_size(_sref(shape), estimator, rank)
+        ws = _empty(n, qmeans.device)
+    _check("sparsp_block_scores_pooled", lib().sparsp_block_scores_pooled(
+        _sref(shape), estimator, _ptr(qmeans), _ptr(kmeans), _ptr(wq), _ptr(wk), rank, _ptr(out), _ptr(ws),
         ws.numel(), _stream(stream)))
     return out
 

@@ -127,6 +127,53 @@ sparsp_status_t sparsp_reorder(const sparsp_shape_t* shape, const void* in, void
   return launch_reorder(s, in, out, inverse != 0, (cudaStream_t)stream);
 }
 
+sparsp_status_t sparsp_reorder_pool(const sparsp_shape_t* shape, const void* in, void* out,
+                                    float* means, sparsp_stream_t stream) {
+  Dims s;
+  sparsp_status_t r = check_shape(shape, &s);
+  if (r != SPARSP_OK) return r;
+  CHECK_PTR(in);
+  CHECK_PTR(out);
+  CHECK_PTR(means);
+  const size_t bytes = (size_t)s.B * s.H * s.N * s.d * s.elem;
+  const uint8_t* a = (const uint8_t*)in;
+  const uint8_t* b = (const uint8_t*)out;
+  if (a < b + bytes && b < a + bytes) return SPARSP_ERR_INVALID_ARG;   // overlap
+  return launch_reorder(s, in, out, false, (cudaStream_t)stream, means);
+}
+
+size_t sparsp_block_scores_pooled_workspace_size(const sparsp_shape_t* shape, int32_t estimator,
+                                                 int32_t rank) {
+  Dims s;
+  if (check_shape(shape, &s) != SPARSP_OK) return 0;
+  if (estimator == SPARSP_EST_LOWRANK && (rank < 1 || rank > 64)) return 0;
+  return scores_from_means_ws(s, estimator, rank);
+}
+
+sparsp_status_t sparsp_block_scores_pooled(const sparsp_shape_t* shape, int32_t estimator,
+                                           const float* qmeans, const float* kmeans,
+                                           const float* wq, const float* wk, int32_t rank,
+                                           float* scores, void* ws, size_t ws_bytes,
+                                           sparsp_stream_t stream) {
+  Dims s;
+  sparsp_status_t r = check_shape(shape, &s);
+  if (r != SPARSP_OK) return r;
+  if (estimator != SPARSP_EST_MEAN && estimator != SPARSP_EST_LOWRANK)
+    return SPARSP_ERR_INVALID_ARG;
+  CHECK_PTR(qmeans);
+  CHECK_PTR(kmeans);
+  CHECK_PTR(scores);
+  if (estimator == SPARSP_EST_LOWRANK) {
+    if (rank < 1 || rank > 64) return SPARSP_ERR_UNSUPPORTED;
+    CHECK_PTR(wq);
+    CHECK_PTR(wk);
+    CHECK_PTR(ws);
+    if (ws_bytes < scores_from_means_ws(s, estimator, rank)) return SPARSP_ERR_WORKSPACE;
+  }
+  return launch_scores_from_means(s, estimator, qmeans, kmeans, wq, wk, rank, scores, ws,
+                                  (cudaStream_t)stream);
+}
+
 size_t sparsp_block_scores_workspace_size(const sparsp_shape_t* shape, int32_t estimator,
                                           int32_t rank) {
   Dims s;

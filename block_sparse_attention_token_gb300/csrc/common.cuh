@@ -49,8 +49,14 @@ int device_sm_count();   // cached per device; -1 on error
 
 // Launchers (each returns SPARSP_OK or SPARSP_ERR_CUDA). -------------------
 
+// means != nullptr: forward reorder that also writes the fp32 tile means [B,H,nb,d]
 sparsp_status_t launch_reorder(const Dims& s, const void* in, void* out, bool inverse,
-                               cudaStream_t st);
+                               cudaStream_t st, float* means = nullptr);
+// scores from pooled means (low-rank: projected through W first, into ws)
+sparsp_status_t launch_scores_from_means(const Dims& s, int estimator, const float* qm,
+                                         const float* km, const float* wq, const float* wk,
+                                         int rank, float* scores, void* ws, cudaStream_t st);
+size_t scores_from_means_ws(const Dims& s, int estimator, int rank);
 
 sparsp_status_t launch_block_scores(const Dims& s, int estimator, const void* q, const void* k,
                                     const float* wq, const float* wk, int rank, float* scores,

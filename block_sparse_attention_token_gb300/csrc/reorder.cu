@@ -1,5 +1,7 @@
 // Step 1: video-aware block organisation - a permutation copy between the
-// raster layout [B,N,H,d] and the tile-ordered layout [B,H,N,d].
+// raster layout [B,N,H,d] and the tile-ordered layout [B,H,N,d]; optionally
+// fused with the block pooling of step 2 (the tile means come out of the same
+// pass, so the scores need no second read of Q and K).
 //
 // One CTA per (b, h, tile j) copies the tile's Bt rows of d elements with
 // 16-byte vectors. Each thread issues all of its loads before its stores so
@@ -12,10 +14,15 @@ namespace {
 
 constexpr int kThreads = 256;
 
-template <int VEC_PER_ROW, int BT>
+// POOL (forward direction only): the same pass also writes the tile's fp32
+// column means to `means` [B, H, nb, d]. Thread t always handles vector column
+// t % VEC_PER_ROW; its tokens are summed in order, then the thread groups in
+// group order: a fixed summation order.
+template <int VEC_PER_ROW, int BT, bool POOL>
 __global__ void __launch_bounds__(kThreads)
 reorder_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, int H, int64_t N, int Y,
-               int X, int tb, int tc, int ta, int nY, int nX, int inverse) {
+               int X, int tb, int tc, int ta, int nY, int nX, int inverse, int bf16,
+               float* __restrict__ means) {
   const int j = blockIdx.x;      // tile
   const int h = blockIdx.y;
   const int b = blockIdx.z;
@@ -52,30 +59,69 @@ reorder_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, int H, int
 #pragma unroll
   for (int u = 0; u < kPer; ++u)
     if (dst_off[u] >= 0) __stcs(out + dst_off[u], buf[u]);
+  if (POOL) {
+    __shared__ float part[kThreads][9];
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      if (dst_off[u] < 0) continue;
+      if (bf16) {
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&buf[u]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(h2[e]);
+          acc[2 * e] += f.x;
+          acc[2 * e + 1] += f.y;
+        }
+      } else {
+        const float* f = reinterpret_cast<const float*>(&buf[u]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] += f[e];
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) part[threadIdx.x][e] = acc[e];
+    __syncthreads();
+    const int epv = bf16 ? 8 : 4;                 // elements per 16-byte vector
+    const int d = VEC_PER_ROW * epv;
+    constexpr int kGroups = kThreads / VEC_PER_ROW;
+    if (threadIdx.x < d) {
+      const int c = threadIdx.x, vc = c / epv, e = c % epv;
+      float sum = 0.f;
+      for (int g2 = 0; g2 < kGroups; ++g2) sum += part[g2 * VEC_PER_ROW + vc][e];
+      const int64_t nb = N / BT;
+      means[(((int64_t)b * H + h) * nb + j) * d + c] = sum * (1.0f / (float)BT);
+    }
+  }
 }
 
 template <int VEC, int BT>
-void go(const Dims& s, const void* in, void* out, bool inverse, cudaStream_t st) {
+void go(const Dims& s, const void* in, void* out, bool inverse, float* means, cudaStream_t st) {
   dim3 grid(s.nb, s.H, s.B);
-  reorder_kernel<VEC, BT><<<grid, kThreads, 0, st>>>(
-      (const uint4*)in, (uint4*)out, s.H, s.N, s.Y, s.X, s.tb, s.tc, s.ta, s.nY, s.nX,
-      inverse ? 1 : 0);
+  const int bf16 = s.dtype == SPARSP_BF16;
+  if (means != nullptr)
+    reorder_kernel<VEC, BT, true><<<grid, kThreads, 0, st>>>(
+        (const uint4*)in, (uint4*)out, s.H, s.N, s.Y, s.X, s.tb, s.tc, s.ta, s.nY, s.nX, 0, bf16, means);
+  else
+    reorder_kernel<VEC, BT, false><<<grid, kThreads, 0, st>>>(
+        (const uint4*)in, (uint4*)out, s.H, s.N, s.Y, s.X, s.tb, s.tc, s.ta, s.nY, s.nX,
+        inverse ? 1 : 0, bf16, nullptr);
 }
 
 }  // namespace
 
 sparsp_status_t launch_reorder(const Dims& s, const void* in, void* out, bool inverse,
-                               cudaStream_t st) {
+                               cudaStream_t st, float* means) {
   const int row_bytes = s.d * s.elem;  // 128, 256 or 512
   const int vec = row_bytes / 16;
   if (s.Bt == 64) {
-    if (vec == 8) go<8, 64>(s, in, out, inverse, st);
-    else if (vec == 16) go<16, 64>(s, in, out, inverse, st);
-    else go<32, 64>(s, in, out, inverse, st);
+    if (vec == 8) go<8, 64>(s, in, out, inverse, means, st);
+    else if (vec == 16) go<16, 64>(s, in, out, inverse, means, st);
+    else go<32, 64>(s, in, out, inverse, means, st);
   } else {
-    if (vec == 8) go<8, 128>(s, in, out, inverse, st);
-    else if (vec == 16) go<16, 128>(s, in, out, inverse, st);
-    else go<32, 128>(s, in, out, inverse, st);
+    if (vec == 8) go<8, 128>(s, in, out, inverse, means, st);
+    else if (vec == 16) go<16, 128>(s, in, out, inverse, means, st);
+    else go<32, 128>(s, in, out, inverse, means, st);
   }
   SPARSP_LAUNCH_CHECK();
   return SPARSP_OK;

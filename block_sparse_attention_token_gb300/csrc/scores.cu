@@ -125,7 +125,50 @@ product_kernel(const float* __restrict__ A, const float* __restrict__ Bm, int nb
   }
 }
 
+// Low-rank projection of pooled means: out[blk, r] = sum_c mean[blk, c] W[h, c, r]
+// (c in order, fmaf). blockIdx.x = tile, blockIdx.y = b*H + h, blockIdx.z = Q (0) or K (1).
+__global__ void __launch_bounds__(64)
+project_kernel(const float* __restrict__ qm, const float* __restrict__ km, const float* __restrict__ wq,
+               const float* __restrict__ wk, int H, int nb, int d, int rank, float* __restrict__ pq,
+               float* __restrict__ pk) {
+  const int r = threadIdx.x;
+  if (r >= rank) return;
+  const bool is_k = blockIdx.z != 0;
+  const int bh = blockIdx.y, h = bh % H;
+  const int64_t blk = (int64_t)bh * nb + blockIdx.x;
+  const float* mean = (is_k ? km : qm) + blk * d;
+  const float* W = (is_k ? wk : wq) + (int64_t)h * d * rank;
+  float acc = 0.f;
+  for (int c = 0; c < d; ++c) acc = fmaf(mean[c], W[(int64_t)c * rank + r], acc);
+  (is_k ? pk : pq)[blk * rank + r] = acc;
+}
+
 }  // namespace
+
+size_t scores_from_means_ws(const Dims& s, int estimator, int rank) {
+  return estimator == SPARSP_EST_LOWRANK ? 2 * (size_t)s.B * s.H * s.nb * rank * sizeof(float) : 0;
+}
+
+sparsp_status_t launch_scores_from_means(const Dims& s, int estimator, const float* qm,
+                                         const float* km, const float* wq, const float* wk,
+                                         int rank, float* scores, void* ws, cudaStream_t st) {
+  const float* a = qm;
+  const float* bm = km;
+  int dd = s.d;
+  if (estimator == SPARSP_EST_LOWRANK) {
+    float* pq = (float*)ws;
+    float* pk = pq + (size_t)s.B * s.H * s.nb * rank;
+    project_kernel<<<dim3(s.nb, s.B * s.H, 2), 64, 0, st>>>(qm, km, wq, wk, s.H, s.nb, s.d, rank, pq, pk);
+    SPARSP_LAUNCH_CHECK();
+    a = pq;
+    bm = pk;
+    dd = rank;
+  }
+  dim3 g2((s.nb + kTile - 1) / kTile, (s.nb + kTile - 1) / kTile, s.B * s.H);
+  product_kernel<<<g2, 256, 0, st>>>(a, bm, s.nb, dd, scores);
+  SPARSP_LAUNCH_CHECK();
+  return SPARSP_OK;
+}
 
 size_t block_scores_ws(const Dims& s, int estimator, int rank) {
   const int dd = estimator == SPARSP_EST_LOWRANK ? rank : s.d;

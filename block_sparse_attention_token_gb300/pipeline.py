@@ -11,8 +11,8 @@ from __future__ import annotations
 import torch
 
 from . import (EST_LOWRANK, EST_MEAN, PROF_SLOTS, Shape, attn_bwd, attn_fwd, attn_workspace_size,
-               block_scores, block_scores_workspace_size, kv_demand, reorder, select,
-               select_workspace_size, DemandOut)
+               block_scores, block_scores_pooled, block_scores_workspace_size, kv_demand, lib, reorder,
+               reorder_pool, select, select_workspace_size, DemandOut)
 
 
 class Pipeline:
@@ -22,7 +22,8 @@ class Pipeline:
         flat order) + attention, inverse reorder."""
         lpt = 2 if self.flags & 1 else 1
         gather = 1 if self.demand.kg is not None else 0
-        return 3 + 2 + 3 + 3 + gather + lpt + 1 + 1
+        scores = (2 if self.est == EST_LOWRANK else 1) if self.fused else 2
+        return 3 + scores + 3 + 3 + gather + lpt + 1 + 1
 
     def kernels_per_backward(self) -> int:
         """reorder dO, rowdot, CSR transpose, schedule, dQ, schedule, dK/dV, 3 inverse reorders."""
@@ -30,9 +31,11 @@ class Pipeline:
         return 1 + 1 + 1 + lpt + 1 + lpt + 1 + 3
 
     def __init__(self, shape: Shape, estimator: str, top_p: float, k_floor: int, P: int, rank: int = 16,
-                 gather: bool = True, flags: int = 0, backward: bool = False, device="cuda"):
+                 gather: bool = True, flags: int = 0, backward: bool = False, device="cuda",
+                 fused_estimation: bool = True):
         self.shape, self.top_p, self.k_floor, self.P, self.rank, self.flags = shape, top_p, k_floor, P, rank, flags
         self.est = EST_LOWRANK if estimator == "lowrank" else EST_MEAN
+        self.fused = fused_estimation
         s = shape
         dt = s.torch_dtype
         dev = torch.device(device)
@@ -43,6 +46,11 @@ class Pipeline:
         self.scores = torch.empty((s.B, s.H, s.nb, s.nb), dtype=torch.float32, device=dev)
         self.ws_scores = torch.empty(max(block_scores_workspace_size(s, self.est, rank), 16), dtype=torch.uint8,
                                      device=dev)
+        self.qmeans, self.kmeans = (torch.empty((s.B, s.H, s.nb, s.d), dtype=torch.float32, device=dev)
+                                    for _ in range(2))
+        import ctypes
+        n = lib().sparsp_block_scores_pooled_workspace_size(ctypes.byref(s), self.est, rank)
+        self.ws_pooled = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
         self.row_ptr = torch.empty(s.rows + 1, dtype=torch.int32, device=dev)
         self.col_idx = torch.empty(s.rows * s.nb, dtype=torch.int32, device=dev)
         self.ws_sel = torch.empty(max(select_workspace_size(s), 16), dtype=torch.uint8, device=dev)
@@ -71,11 +79,19 @@ class Pipeline:
         output buffer (default: self.o)."""
         s = self.shape
         mark = mark or (lambda name: None)
-        reorder(s, q, self.qb)
-        reorder(s, k, self.kb)
-        reorder(s, v, self.vb)
-        mark("reorder")
-        block_scores(s, self.qb, self.kb, self.est, wq, wk, self.rank, out=self.scores, ws=self.ws_scores)
+        if self.fused:   # the tile means come out of the reorder pass itself
+            reorder_pool(s, q, self.qb, self.qmeans)
+            reorder_pool(s, k, self.kb, self.kmeans)
+            reorder(s, v, self.vb)
+            mark("reorder")
+            block_scores_pooled(s, self.qmeans, self.kmeans, self.est, wq, wk, self.rank, out=self.scores,
+                                ws=self.ws_pooled)
+        else:
+            reorder(s, q, self.qb)
+            reorder(s, k, self.kb)
+            reorder(s, v, self.vb)
+            mark("reorder")
+            block_scores(s, self.qb, self.kb, self.est, wq, wk, self.rank, out=self.scores, ws=self.ws_scores)
         mark("scores")
         select(s, self.scores, self.top_p, self.k_floor, self.row_ptr, self.col_idx, self.ws_sel, self.status)
         mark("select")

@@ -141,6 +141,28 @@ SPARSP_API sparsp_status_t sparsp_block_scores(const sparsp_shape_t* shape, int3
                                     size_t ws_bytes, sparsp_stream_t stream);
 
 /*
+ * Steps 1 + 2 fused ("Dynamic Sparsity in Large-Scale Video DiT Training",
+ * "How DSV works" and "Why it works": critical-KV estimation fused into the
+ * passes that already touch Q and K). sparsp_reorder_pool is the forward
+ * sparsp_reorder of one tensor that also writes the fp32 mean of every tile
+ * to `means` [B, H, nb, d] from the same read (a fixed summation order), so
+ * the block scores need no second pass over Q and K.
+ * sparsp_block_scores_pooled: the scores of sparsp_block_scores from those
+ * means (estimator MEAN: q_mean . k_mean; LOWRANK: (q_mean Wq)(k_mean Wk)^T);
+ * ws is used by LOWRANK only (sparsp_block_scores_pooled_workspace_size(),
+ * 0 for MEAN, when ws may be NULL).
+ */
+SPARSP_API sparsp_status_t sparsp_reorder_pool(const sparsp_shape_t* shape, const void* in, void* out,
+                                               float* means, sparsp_stream_t stream);
+SPARSP_API size_t sparsp_block_scores_pooled_workspace_size(const sparsp_shape_t* shape,
+                                                            int32_t estimator, int32_t rank);
+SPARSP_API sparsp_status_t sparsp_block_scores_pooled(const sparsp_shape_t* shape, int32_t estimator,
+                                                      const float* qmeans, const float* kmeans,
+                                                      const float* wq, const float* wk, int32_t rank,
+                                                      float* scores, void* ws, size_t ws_bytes,
+                                                      sparsp_stream_t stream);
+
+/*
  * Step 3 - Top-p routing with a Top-k safety floor ("mlsift.com tag listing",
  * Top-p video sparse-attention entry, abstract), per (b, h, i) row of scores:
  *   e_j = expf(S_j - max_j S_j) in float32; Z and prefix sums in float64;

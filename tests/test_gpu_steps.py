@@ -75,6 +75,26 @@ def test_block_scores(name):
 
 
 @pytest.mark.parametrize("name", list(SMALL))
+def test_reorder_pool_fused(name):
+    """Fused tile reorder + pooling: the reorder is bit-exact, the means and the
+    scores computed from them match the oracle."""
+    wl, data, shape = _setup(name)
+    ch = OracleChain(wl, data)
+    qb, qm = sp.reorder_pool(shape, dev(data["q"], wl))
+    kb, km = sp.reorder_pool(shape, dev(data["k"], wl))
+    assert np.array_equal(host(qb), ch.qb) and np.array_equal(host(kb), ch.kb)
+    np.testing.assert_allclose(host(qm), orc.pool_means(ch.qb, ch.g.Bt), rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(host(km), orc.pool_means(ch.kb, ch.g.Bt), rtol=1e-5, atol=1e-6)
+    if wl.estimator == "lowrank":
+        wq, wk = (torch.from_numpy(data[x]).cuda() for x in ("wq", "wk"))
+        S = sp.block_scores_pooled(shape, qm, km, sp.EST_LOWRANK, wq, wk, 16)
+    else:
+        S = sp.block_scores_pooled(shape, qm, km)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(host(S).astype(np.float64), ch.S64, rtol=2e-5, atol=2e-5 * np.abs(ch.S64).max())
+
+
+@pytest.mark.parametrize("name", list(SMALL))
 def test_select_bitexact_on_oracle_scores(name):
     wl, data, shape = _setup(name)
     ch = OracleChain(wl, data)
@@ -269,15 +289,17 @@ def test_attn_bwd(name):
     assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
 
 
+@pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("name", ["tiny", "medium", "r128", "wave"])
-def test_pipeline_end_to_end(name):
+def test_pipeline_end_to_end(name, fused):
     """The whole chain on the GPU (its own scores and selection) against the
     oracle's own chain: selection agreement is reported, outputs are compared
     on every row whose block set agrees."""
     wl, data, shape = _setup(name)
     ch = OracleChain(wl, data)
     g = ch.g
-    pipe = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P, backward=wl.backward)
+    pipe = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P, backward=wl.backward,
+                       fused_estimation=fused)
     args = [dev(data[x], wl) for x in ("q", "k", "v")]
     kw = {}
     if wl.estimator == "lowrank":
