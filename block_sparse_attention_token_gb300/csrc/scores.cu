@@ -7,8 +7,8 @@
 // order, then the 16 partial sums are added in lane order.
 //
 // product_kernel: S = A . B^T per head with A, B = pooled [nb, dd] fp32,
-// dd = d (mean) or rank (low-rank); a 32x32 output tile per CTA, the dd
-// reduction in index order with fmaf.
+// dd = d (mean) or rank (low-rank); a 64x64 output tile per CTA (4x4 per
+// thread), the dd reduction in index order with fmaf.
 #include "common.cuh"
 
 namespace sparsp {
@@ -88,41 +88,66 @@ pool_kernel(const uint4* __restrict__ q, const uint4* __restrict__ k, int H, int
   }
 }
 
-constexpr int kTile = 32;
+constexpr int kTile = 64;        // output tile kTile x kTile per CTA
 
+// S = A B^T for one head, A, B: [nb, dd] fp32. 256 threads, each owning a 4x4
+// block of outputs (rows 4*ty.., columns 4*tx..); the whole dd extent of both
+// input tiles is staged in shared memory (rows padded by one word). Every
+// output is one fmaf chain over c = 0..dd-1 in order.
 // blockIdx.x = column tile, blockIdx.y = row tile, blockIdx.z = b*H + h.
 __global__ void __launch_bounds__(256)
 product_kernel(const float* __restrict__ A, const float* __restrict__ Bm, int nb, int dd,
                float* __restrict__ S) {
-  __shared__ float sa[kTile][kTile + 1];
-  __shared__ float sb[kTile][kTile + 1];
+  extern __shared__ float sm[];
+  const int ld = dd + 1;
+  float* sa = sm;                  // [kTile][ld]
+  float* sb = sm + kTile * ld;     // [kTile][ld]
   const int bh = blockIdx.z;
   const int i0 = blockIdx.y * kTile, j0 = blockIdx.x * kTile;
   const float* a = A + (int64_t)bh * nb * dd;
   const float* bm = Bm + (int64_t)bh * nb * dd;
-  const int tx = threadIdx.x % kTile;        // output column within tile
-  const int ty = threadIdx.x / kTile;        // 0..7: rows ty, ty+8, ty+16, ty+24
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int c0 = 0; c0 < dd; c0 += kTile) {
-    for (int e = threadIdx.x; e < kTile * kTile; e += 256) {
-      const int r = e / kTile, c = e % kTile;
-      sa[r][c] = (i0 + r < nb && c0 + c < dd) ? a[(int64_t)(i0 + r) * dd + c0 + c] : 0.f;
-      sb[r][c] = (j0 + r < nb && c0 + c < dd) ? bm[(int64_t)(j0 + r) * dd + c0 + c] : 0.f;
-    }
-    __syncthreads();
-    const int cmax = min(kTile, dd - c0);
-    for (int c = 0; c < cmax; ++c) {
-      const float bv = sb[tx][c];
+  for (int e = threadIdx.x; e < kTile * dd; e += 256) {
+    const int r = e / dd, c = e % dd;
+    sa[r * ld + c] = i0 + r < nb ? a[(int64_t)(i0 + r) * dd + c] : 0.f;
+    sb[r * ld + c] = j0 + r < nb ? bm[(int64_t)(j0 + r) * dd + c] : 0.f;
+  }
+  __syncthreads();
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[4][4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) acc[u] = fmaf(sa[ty + 8 * u][c], bv, acc[u]);
-    }
-    __syncthreads();
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int v = 0; v < 4; ++v) acc[u][v] = 0.f;
+  for (int c = 0; c < dd; ++c) {
+    float av[4], bv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) av[u] = sa[(4 * ty + u) * ld + c];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) bv[v] = sb[(4 * tx + v) * ld + c];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int v = 0; v < 4; ++v) acc[u][v] = fmaf(av[u], bv[v], acc[u][v]);
   }
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int i = i0 + ty + 8 * u, jj = j0 + tx;
-    if (i < nb && jj < nb) S[((int64_t)bh * nb + i) * nb + jj] = acc[u];
-  }
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int i = i0 + 4 * ty + u, jj = j0 + 4 * tx + v;
+      if (i < nb && jj < nb) S[((int64_t)bh * nb + i) * nb + jj] = acc[u][v];
+    }
+}
+
+sparsp_status_t launch_product(const float* a, const float* b, int nb, int dd, int BH, float* S,
+                               cudaStream_t st) {
+  const size_t smem = 2 * (size_t)kTile * (dd + 1) * sizeof(float);
+  if (cudaFuncSetAttribute(product_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return SPARSP_ERR_CUDA;
+  dim3 grid((nb + kTile - 1) / kTile, (nb + kTile - 1) / kTile, BH);
+  product_kernel<<<grid, 256, smem, st>>>(a, b, nb, dd, S);
+  SPARSP_LAUNCH_CHECK();
+  return SPARSP_OK;
 }
 
 // Low-rank projection of pooled means: out[blk, r] = sum_c mean[blk, c] W[h, c, r]
@@ -164,10 +189,7 @@ sparsp_status_t launch_scores_from_means(const Dims& s, int estimator, const flo
     bm = pk;
     dd = rank;
   }
-  dim3 g2((s.nb + kTile - 1) / kTile, (s.nb + kTile - 1) / kTile, s.B * s.H);
-  product_kernel<<<g2, 256, 0, st>>>(a, bm, s.nb, dd, scores);
-  SPARSP_LAUNCH_CHECK();
-  return SPARSP_OK;
+  return launch_product(a, bm, s.nb, dd, s.B * s.H, scores, st);
 }
 
 size_t block_scores_ws(const Dims& s, int estimator, int rank) {
@@ -187,10 +209,7 @@ sparsp_status_t launch_block_scores(const Dims& s, int estimator, const void* q,
                                            s.dtype == SPARSP_BF16, low ? wq : nullptr,
                                            low ? wk : nullptr, rank, pq, pk, dd);
   SPARSP_LAUNCH_CHECK();
-  dim3 g2((s.nb + kTile - 1) / kTile, (s.nb + kTile - 1) / kTile, s.B * s.H);
-  product_kernel<<<g2, 256, 0, st>>>(pq, pk, s.nb, dd, scores);
-  SPARSP_LAUNCH_CHECK();
-  return SPARSP_OK;
+  return launch_product(pq, pk, s.nb, dd, s.B * s.H, scores, st);
 }
 
 }  // namespace sparsp
