@@ -289,7 +289,7 @@ class Demand:
     bytes: np.ndarray      # uint64 [4]: demanded, all, remote_demanded, remote_all
 
 
-def kv_demand(row_ptr, col_idx, B, H, nb, P, Bt, d, elem_bytes, kb=None, vb=None) -> Demand:
+def kv_demand(row_ptr, col_idx, B, H, nb, P, Bt, d, elem_bytes, kb=None, vb=None, owner=None) -> Demand:
     """The key/value blocks each query partition needs, as the one-GPU analogue
     of routing KV blocks only to the ranks that request them ("SparSP", abstract).
 
@@ -299,6 +299,8 @@ def kv_demand(row_ptr, col_idx, B, H, nb, P, Bt, d, elem_bytes, kb=None, vb=None
       all             = B*H*P*nb * Bt*d*elem * 2   (every partition receives all KV)
       remote_demanded = demanded blocks outside the partition's own range
       remote_all      = all blocks outside the partition's own range
+    owner: optional [B, nb] partition of every block (see placement); default:
+    the contiguous split partition_bounds.
     """
     W = (nb + 31) // 32
     bitmap = np.zeros((B, H, P, W), dtype=np.uint32)
@@ -307,10 +309,15 @@ def kv_demand(row_ptr, col_idx, B, H, nb, P, Bt, d, elem_bytes, kb=None, vb=None
     demanded = remote_dem = remote_all = 0
     bounds = partition_bounds(nb, P)
     for b in range(B):
+        if owner is None:
+            members = [list(range(lo, hi)) for (lo, hi) in bounds]
+        else:
+            members = [[i for i in range(nb) if int(owner[b][i]) == r] for r in range(P)]
         for h in range(H):
-            for r, (lo, hi) in enumerate(bounds):
+            for r in range(P):
+                own = set(members[r])
                 want = set()
-                for i in range(lo, hi):
+                for i in members[r]:
                     row = (b * H + h) * nb + i
                     want.update(int(j) for j in col_idx[row_ptr[row]:row_ptr[row + 1]])
                 ordered = sorted(want)
@@ -318,8 +325,8 @@ def kv_demand(row_ptr, col_idx, B, H, nb, P, Bt, d, elem_bytes, kb=None, vb=None
                 for j in ordered:
                     bitmap[b, h, r, j // 32] |= np.uint32(1 << (j % 32))
                 demanded += len(ordered) * tile
-                remote_dem += sum(1 for j in ordered if not (lo <= j < hi)) * tile
-                remote_all += (nb - (hi - lo)) * tile
+                remote_dem += sum(1 for j in ordered if j not in own) * tile
+                remote_all += (nb - len(own)) * tile
     dem_ptr = np.zeros(len(sets) + 1, dtype=np.int64)
     dem_ptr[1:] = np.cumsum([len(s) for s in sets])
     dem_idx = np.array([j for s in sets for j in s], dtype=np.int32)
@@ -338,6 +345,58 @@ def kv_demand(row_ptr, col_idx, B, H, nb, P, Bt, d, elem_bytes, kb=None, vb=None
     all_bytes = B * H * P * nb * tile
     byts = np.array([demanded, all_bytes, remote_dem, remote_all], dtype=np.uint64)
     return Demand(bitmap, dem_ptr.astype(np.int32), dem_idx, kg, vg, byts)
+
+
+def affinity(row_ptr, col_idx, H, nb, b):
+    """Co-selection counts of batch element b: W[i][j] = number of heads in which
+    query block i selected key block j, plus the same with i and j swapped
+    (i != j; the diagonal is 0)."""
+    W = np.zeros((nb, nb), dtype=np.int64)
+    for h in range(H):
+        for i in range(nb):
+            r = (b * H + h) * nb + i
+            for j in col_idx[row_ptr[r]:row_ptr[r + 1]]:
+                j = int(j)
+                if j != i:
+                    W[i, j] += 1
+                    W[j, i] += 1
+    return W
+
+
+def placement(row_ptr, col_idx, B, H, nb, P) -> np.ndarray:
+    """Dependency-aware placement of blocks on P partitions ("SparSP:
+    Exploiting Communication Sparsity for Sequence-Parallel Video DiTs",
+    abstract: sequence blocks distributed according to the sparse attention
+    pattern), one assignment per batch element shared by all heads, with the
+    partition sizes of the contiguous split.
+
+    Deterministic greedy on the co-selection affinity W:
+      blocks in order of total affinity sum_j W[i][j] descending (ties: lower i);
+      each goes to the partition with spare capacity whose already-placed
+      blocks have the largest affinity to it (ties: more spare capacity, then
+      lower partition index).
+    Returns owner [B, nb] int32.
+    """
+    caps0 = [hi - lo for (lo, hi) in partition_bounds(nb, P)]
+    owner = np.full((B, nb), -1, dtype=np.int32)
+    for b in range(B):
+        W = affinity(row_ptr, col_idx, H, nb, b)
+        total = W.sum(axis=1)
+        order = sorted(range(nb), key=lambda i: (-int(total[i]), i))
+        caps = list(caps0)
+        for i in order:
+            best = None
+            for r in range(P):
+                if caps[r] == 0:
+                    continue
+                score = int(sum(W[i, j] for j in range(nb) if owner[b, j] == r))
+                key = (score, caps[r], -r)
+                if best is None or key > best[0]:
+                    best = (key, r)
+            r = best[1]
+            owner[b, i] = r
+            caps[r] -= 1
+    return owner
 
 
 # ---------------------------------------------------------------------------

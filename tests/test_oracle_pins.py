@@ -382,3 +382,51 @@ def test_csc_is_transpose():
         for j in range(g.nb):
             c = h * g.nb + j
             assert ri[cp[c]:cp[c + 1]].tolist() == np.nonzero(M[0, h, :, j])[0].tolist()
+
+
+# ----------------------------------------------------------------- placement
+
+def _csr(rows):
+    rp = np.concatenate([[0], np.cumsum([len(r) for r in rows])]).astype(np.int64)
+    return rp, np.concatenate([np.asarray(r, dtype=np.int64) for r in rows])
+
+
+def test_placement_hand_example():
+    gold = _load("placement_hand.json")
+    rp, ci = _csr(gold["rows"])
+    owner = orc.placement(rp, ci, gold["B"], gold["H"], gold["nb"], gold["P"])
+    assert owner[0].tolist() == gold["owner"]
+    dem = orc.kv_demand(rp, ci, 1, 1, gold["nb"], gold["P"], 1, 1, 1, owner=owner)
+    assert int(dem.bytes[2]) == gold["remote_blocks_placed"] * 2      # tile bytes 1*1*1, K and V
+
+
+def test_placement_separates_independent_groups():
+    # two groups of blocks that only select each other: an optimal placement
+    # puts each group on one partition and ships nothing
+    nb, groups = 8, [[0, 1, 4, 5], [2, 3, 6, 7]]
+    rows = [sorted(next(g for g in groups if i in g)) for i in range(nb)]
+    rp, ci = _csr(rows * 2)                         # two heads with the same pattern
+    owner = orc.placement(rp, ci, 1, 2, nb, 2)
+    for g in groups:
+        assert len({int(owner[0, i]) for i in g}) == 1
+    placed = orc.kv_demand(rp, ci, 1, 2, nb, 2, 1, 1, 1, owner=owner)
+    contiguous = orc.kv_demand(rp, ci, 1, 2, nb, 2, 1, 1, 1)
+    assert int(placed.bytes[2]) == 0 < int(contiguous.bytes[2])
+    assert int(placed.bytes[3]) == int(contiguous.bytes[3])
+
+
+def test_placement_is_a_balanced_assignment_and_contiguous_owner_is_the_default():
+    wl, g, data, qb, kb, vb = _tiny()
+    S = orc.scores_mean(qb, kb, g.Bt).astype(np.float32).reshape(-1, g.nb)
+    sel = orc.select(S, wl.top_p, wl.k_floor)
+    for P in (1, 2, 3, 16):
+        owner = orc.placement(sel.row_ptr, sel.col_idx, g.B, g.H, g.nb, P)
+        counts = np.bincount(owner[0], minlength=P)
+        assert counts.tolist() == [hi - lo for (lo, hi) in orc.partition_bounds(g.nb, P)]
+    contiguous = np.zeros((1, g.nb), np.int32)
+    for r, (lo, hi) in enumerate(orc.partition_bounds(g.nb, 4)):
+        contiguous[0, lo:hi] = r
+    a = orc.kv_demand(sel.row_ptr, sel.col_idx, g.B, g.H, g.nb, 4, g.Bt, g.d, 4, kb, vb)
+    b = orc.kv_demand(sel.row_ptr, sel.col_idx, g.B, g.H, g.nb, 4, g.Bt, g.d, 4, kb, vb, owner=contiguous)
+    assert np.array_equal(a.bitmap, b.bitmap) and np.array_equal(a.dem_idx, b.dem_idx)
+    assert a.bytes.tolist() == b.bytes.tolist() and np.array_equal(a.kg, b.kg)
