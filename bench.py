@@ -176,6 +176,8 @@ def main():
     ap.add_argument("--flat", action="store_true", help="flat (cross-head) longest-first order")
     ap.add_argument("--portable", action="store_true", help="mma.sync attention kernel")
     ap.add_argument("--unfused", action="store_true", help="separate pooling pass instead of reorder+pool")
+    ap.add_argument("--placement", action="store_true",
+                    help="dependency-aware block placement inside the step (default: contiguous partitions)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--heads", type=int, default=0, help="override the head count (smaller profiling case)")
@@ -210,7 +212,7 @@ def main():
     shape = sp.shape_of(wl)
     flags = (sp.SCHED_FLAT if args.flat else 0) | (sp.KERNEL_PORTABLE if args.portable else 0)
     pipe = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P, backward=wl.backward, flags=flags,
-                       fused_estimation=not args.unfused)
+                       fused_estimation=not args.unfused, placement=args.placement)
     tdt = shape.torch_dtype
     host_in = {x: torch.from_numpy(data[x]).to(tdt).pin_memory() for x in ("q", "k", "v")}
     dev_in = {x: host_in[x].cuda() for x in host_in}
@@ -234,7 +236,7 @@ def main():
     if pipe.status.item() != 0:
         raise SystemExit(f"device status {sp.status_string(pipe.status.item())}")
     nnz = int(pipe.row_ptr[-1].item())
-    demanded, all_bytes = (int(x) for x in pipe.demand.bytes[:2].tolist())
+    demanded, all_bytes, remote_dem, remote_all = (int(x) for x in pipe.demand.bytes.tolist())
 
     # ---- timed region: K steps, events around every stage
     marks = []
@@ -342,6 +344,26 @@ def main():
     busy = busy[busy > 0]
     imbalance = float(busy.max() / busy.mean()) if len(busy) else None
 
+    # dependency-aware placement against the contiguous split on this step's CSR
+    # (untimed by the step; its own kernels timed here)
+    ws_pl = torch.empty(max(sp.placement_workspace_size(shape), 16), dtype=torch.uint8, device="cuda")
+    owner = torch.empty((shape.B, shape.nb), dtype=torch.int32, device="cuda")
+    contiguous = sp.kv_demand(shape, wl.P, pipe.row_ptr, pipe.col_idx)
+    placed = sp.kv_demand(shape, wl.P, pipe.row_ptr, pipe.col_idx, owner=sp.placement(
+        shape, wl.P, pipe.row_ptr, pipe.col_idx, owner, ws_pl))
+    p0 = torch.cuda.Event(enable_timing=True)
+    p1 = torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    for _ in range(5):
+        sp.placement(shape, wl.P, pipe.row_ptr, pipe.col_idx, owner, ws_pl)
+    p1.record(stream)
+    torch.cuda.synchronize()
+    cb, pb = contiguous.bytes.tolist(), placed.bytes.tolist()
+    placement_info = {"remote_demanded_contiguous": int(cb[2]), "remote_demanded_placed": int(pb[2]),
+                      "demanded_contiguous": int(cb[0]), "demanded_placed": int(pb[0]),
+                      "remote_reduction": 1.0 - pb[2] / cb[2] if cb[2] else None,
+                      "placement_ms": p0.elapsed_time(p1) / 5, "in_step": bool(args.placement)}
+
     launches = args.steps * (pipe.kernels_per_forward() + (pipe.kernels_per_backward() if wl.backward else 0))
     if rank != 0:
         if world > 1:
@@ -365,10 +387,13 @@ def main():
                    "schedule": "flat" if args.flat else "head-grouped longest-first",
                    "kernel": "portable mma.sync" if args.portable else "default",
                    "estimation": "separate pooling pass" if args.unfused else "fused with the reorder",
+                   "partitions": "dependency-aware placement" if args.placement else "contiguous",
                    "l2": f"inputs larger than L2 ({shape.B * shape.H * shape.N * shape.d * 2 / 1e6:.0f} MB per tensor)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "stages_ms": stage_ms,
-        "kv_bytes": {"demanded": demanded, "all": all_bytes},
+        "kv_bytes": {"demanded": demanded, "all": all_bytes, "remote_demanded": remote_dem,
+                     "remote_all": remote_all},
+        "placement": placement_info,
         "attn_sm_imbalance": imbalance,
         "clocks": clk, "e2e": e2e, "gpu_launches": launches, "roofline": roofline, "cpu_baseline": cpu,
     }

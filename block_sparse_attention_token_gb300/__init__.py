@@ -84,7 +84,10 @@ _SIG = {
     "sparsp_select_workspace_size": (ctypes.c_size_t, [_P]),
     "sparsp_select": (_I32, [_P, _P, ctypes.c_float, _I32, _P, _P, _P, ctypes.c_size_t, _P, _P]),
     "sparsp_select_noalloc": (_I32, [_P, _P, ctypes.c_float, _I32, _P, _P, _P, _P]),
-    "sparsp_kv_demand": (_I32, [_P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int64, _P, _P, _P]),
+    "sparsp_kv_demand": (_I32, [_P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int64, _P, _P,
+                                _P]),
+    "sparsp_placement_workspace_size": (ctypes.c_size_t, [_P]),
+    "sparsp_placement": (_I32, [_P, _I32, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
     "sparsp_lpt_workspace_size": (ctypes.c_size_t, [_P]),
     "sparsp_lpt_schedule": (_I32, [_P, _P, ctypes.c_uint32, _P, _P, ctypes.c_size_t, _P]),
     "sparsp_attn_workspace_size": (ctypes.c_size_t, [_P, _I32]),
@@ -233,7 +236,9 @@ class DemandOut:
 
 
 def kv_demand(shape: Shape, P: int, row_ptr, col_idx, k=None, v=None, gather_cap: int | None = None,
-              out: DemandOut | None = None, status=None, stream=None) -> DemandOut:
+              out: DemandOut | None = None, status=None, stream=None, owner=None) -> DemandOut:
+    """KV demand of P partitions: contiguous query-block ranges, or the block
+    owner map `owner` [B, nb] int32 (e.g. from `placement`)."""
     dev = row_ptr.device
     if out is None:
         W = (shape.nb + 31) // 32
@@ -249,10 +254,29 @@ def kv_demand(shape: Shape, P: int, row_ptr, col_idx, k=None, v=None, gather_cap
                         torch.empty(4, dtype=torch.int64, device=dev))
     cap = 0 if out.kg is None else (out.kg.shape[0] if gather_cap is None else gather_cap)
     _check("sparsp_kv_demand", lib().sparsp_kv_demand(
-        _sref(shape), int(P), _ptr(row_ptr), _ptr(col_idx), _ptr(out.bitmap), _ptr(out.dem_ptr),
+        _sref(shape), int(P), _ptr(row_ptr), _ptr(col_idx), _ptr(owner), _ptr(out.bitmap), _ptr(out.dem_ptr),
         _ptr(out.dem_idx), _ptr(k), _ptr(v), _ptr(out.kg), _ptr(out.vg), int(cap), _ptr(out.bytes),
         _ptr(status), _stream(stream)))
     return out
+
+
+def placement_workspace_size(shape: Shape) -> int:
+    return lib().sparsp_placement_workspace_size(_sref(shape))
+
+
+def placement(shape: Shape, P: int, row_ptr, col_idx, owner=None, ws=None, status=None,
+              stream=None) -> torch.Tensor:
+    """Block -> partition assignment [B, nb] int32 from the co-selection
+    affinity of the CSR (dependency-aware placement)."""
+    dev = row_ptr.device
+    if owner is None:
+        owner = torch.empty((shape.B, shape.nb), dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = _empty(placement_workspace_size(shape), dev)
+    _check("sparsp_placement", lib().sparsp_placement(
+        _sref(shape), int(P), _ptr(row_ptr), _ptr(col_idx), _ptr(owner), _ptr(ws), ws.numel(),
+        _ptr(status), _stream(stream)))
+    return owner
 
 
 # ----------------------------------------------------------------- step 5

@@ -246,9 +246,9 @@ sparsp_status_t sparsp_select_noalloc(const sparsp_shape_t* shape, const float* 
 }
 
 sparsp_status_t sparsp_kv_demand(const sparsp_shape_t* shape, int32_t P, const int32_t* row_ptr,
-                                 const int32_t* col_idx, uint32_t* bitmap, int32_t* dem_ptr,
-                                 int32_t* dem_idx, const void* k, const void* v, void* kg,
-                                 void* vg, int64_t gather_cap_blocks, uint64_t* bytes,
+                                 const int32_t* col_idx, const int32_t* owner, uint32_t* bitmap,
+                                 int32_t* dem_ptr, int32_t* dem_idx, const void* k, const void* v,
+                                 void* kg, void* vg, int64_t gather_cap_blocks, uint64_t* bytes,
                                  int32_t* d_status, sparsp_stream_t stream) {
   Dims s;
   sparsp_status_t r = check_shape(shape, &s);
@@ -257,6 +257,7 @@ sparsp_status_t sparsp_kv_demand(const sparsp_shape_t* shape, int32_t P, const i
   if ((int64_t)s.B * s.H * P > INT32_MAX / 1024) return SPARSP_ERR_UNSUPPORTED;
   CHECK_PTR(row_ptr);
   CHECK_PTR(col_idx);
+  CHECK_OPT_PTR(owner);
   CHECK_PTR(bitmap);
   CHECK_PTR(dem_ptr);
   CHECK_PTR(dem_idx);
@@ -270,8 +271,30 @@ sparsp_status_t sparsp_kv_demand(const sparsp_shape_t* shape, int32_t P, const i
     CHECK_PTR(v);
     if (gather_cap_blocks < 0) return SPARSP_ERR_INVALID_ARG;
   }
-  return launch_kv_demand(s, P, row_ptr, col_idx, bitmap, dem_ptr, dem_idx, k, v, kg, vg,
+  return launch_kv_demand(s, P, row_ptr, col_idx, owner, bitmap, dem_ptr, dem_idx, k, v, kg, vg,
                           gather_cap_blocks, bytes, d_status, (cudaStream_t)stream);
+}
+
+size_t sparsp_placement_workspace_size(const sparsp_shape_t* shape) {
+  Dims s;
+  if (check_shape(shape, &s) != SPARSP_OK) return 0;
+  return placement_ws(s);
+}
+
+sparsp_status_t sparsp_placement(const sparsp_shape_t* shape, int32_t P, const int32_t* row_ptr,
+                                 const int32_t* col_idx, int32_t* owner, void* ws, size_t ws_bytes,
+                                 int32_t* d_status, sparsp_stream_t stream) {
+  Dims s;
+  sparsp_status_t r = check_shape(shape, &s);
+  if (r != SPARSP_OK) return r;
+  if (P < 1 || P > s.nb) return SPARSP_ERR_SHAPE;
+  CHECK_PTR(row_ptr);
+  CHECK_PTR(col_idx);
+  CHECK_PTR(owner);
+  CHECK_PTR(ws);
+  CHECK_OPT_PTR(d_status);
+  if (ws_bytes < placement_ws(s)) return SPARSP_ERR_WORKSPACE;
+  return launch_placement(s, row_ptr, col_idx, P, owner, ws, d_status, (cudaStream_t)stream);
 }
 
 size_t sparsp_lpt_workspace_size(const sparsp_shape_t* shape) {

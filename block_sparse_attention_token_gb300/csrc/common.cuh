@@ -73,10 +73,14 @@ sparsp_status_t launch_select_noalloc(const Dims& s, const float* scores, float 
                                       cudaStream_t st);
 
 sparsp_status_t launch_kv_demand(const Dims& s, int P, const int32_t* row_ptr,
-                                 const int32_t* col_idx, uint32_t* bitmap, int32_t* dem_ptr,
+                                 const int32_t* col_idx, const int32_t* owner, uint32_t* bitmap, int32_t* dem_ptr,
                                  int32_t* dem_idx, const void* k, const void* v, void* kg,
                                  void* vg, int64_t cap, uint64_t* bytes, int32_t* d_status,
                                  cudaStream_t st);
+
+size_t placement_ws(const Dims& s);
+sparsp_status_t launch_placement(const Dims& s, const int32_t* row_ptr, const int32_t* col_idx, int P,
+                                 int32_t* owner, void* ws, int32_t* d_status, cudaStream_t st);
 
 size_t lpt_ws(const Dims& s);
 sparsp_status_t launch_lpt(const Dims& s, const int32_t* row_ptr, bool flat, int32_t* items,

@@ -1,9 +1,11 @@
-// Step 4: KV demand of P contiguous virtual query partitions.
+// Step 4: KV demand of P virtual query partitions.
 //
-//  1. bitmap_kernel - one CTA per partition (b, h, r): the partition's rows
-//     are consecutive CSR rows, so its entries are one contiguous range of
-//     col_idx; each index is OR-ed into a shared bitmap. Writes the bitmap,
-//     its population into dem_ptr[part] and the byte counters.
+//  1. bitmap_kernel - one CTA per partition (b, h, r). Contiguous split: the
+//     partition's rows are consecutive CSR rows, so its entries are one
+//     contiguous range of col_idx. With a block owner map: warps scan the
+//     head's rows and take those whose owner is r. Each index is OR-ed into a
+//     shared bitmap. Writes the bitmap, its population into dem_ptr[part] and
+//     the byte counters.
 //  2. scan          - dem_ptr counts -> offsets.
 //  3. list_kernel   - one warp per partition writes the set bits ascending.
 //  4. gather_kernel - one CTA per demanded slot copies the K and V tiles
@@ -17,53 +19,80 @@ namespace {
 
 constexpr int kMaxWords = 32;   // nb <= 1024
 
+__device__ __forceinline__ void or_row(const int32_t* __restrict__ col_idx, int32_t e0, int32_t e1,
+                                       int step, int first, int nb, uint32_t* bits, int32_t* d_status) {
+  for (int32_t e = e0 + first; e < e1; e += step) {
+    const int32_t j = col_idx[e];
+    if (j < 0 || j >= nb) {
+      report(d_status, SPARSP_ERR_DATA);
+      continue;
+    }
+    atomicOr(&bits[j >> 5], 1u << (j & 31));
+  }
+}
+
 __global__ void __launch_bounds__(256)
-bitmap_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ col_idx, int H,
-              int nb, int P, uint64_t tile2, uint32_t* __restrict__ bitmap,
-              int32_t* __restrict__ counts, uint64_t* __restrict__ bytes, int32_t* d_status) {
-  __shared__ uint32_t bits[kMaxWords];
+bitmap_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ col_idx,
+              const int32_t* __restrict__ owner, int H, int nb, int P, uint64_t tile2,
+              uint32_t* __restrict__ bitmap, int32_t* __restrict__ counts,
+              uint64_t* __restrict__ bytes, int32_t* d_status) {
+  __shared__ uint32_t bits[kMaxWords], mine[kMaxWords];
   const int part = blockIdx.x;           // (b*H + h)*P + r
   const int bh = part / P, r = part % P;
-  const int lo = (int)(((int64_t)r * nb) / P), hi = (int)(((int64_t)(r + 1) * nb) / P);
   const int W = (nb + 31) / 32;
-  if (threadIdx.x < kMaxWords) bits[threadIdx.x] = 0u;
+  if (threadIdx.x < kMaxWords) {
+    bits[threadIdx.x] = 0u;
+    mine[threadIdx.x] = 0u;
+  }
   __syncthreads();
-  const int64_t row0 = (int64_t)bh * nb + lo, row1 = (int64_t)bh * nb + hi;
-  const int32_t e0 = row_ptr[row0], e1 = row_ptr[row1];
-  if (e1 < e0) {
-    if (threadIdx.x == 0) report(d_status, SPARSP_ERR_DATA);
+  if (owner == nullptr) {
+    const int lo = (int)(((int64_t)r * nb) / P), hi = (int)(((int64_t)(r + 1) * nb) / P);
+    for (int j = lo + (int)threadIdx.x; j < hi; j += blockDim.x) atomicOr(&mine[j >> 5], 1u << (j & 31));
+    const int64_t row0 = (int64_t)bh * nb + lo, row1 = (int64_t)bh * nb + hi;
+    const int32_t e0 = row_ptr[row0], e1 = row_ptr[row1];
+    if (e1 < e0) {
+      if (threadIdx.x == 0) report(d_status, SPARSP_ERR_DATA);
+    } else {
+      or_row(col_idx, e0, e1, blockDim.x, threadIdx.x, nb, bits, d_status);
+    }
   } else {
-    for (int32_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
-      const int32_t j = col_idx[e];
-      if (j < 0 || j >= nb) {
-        report(d_status, SPARSP_ERR_DATA);
+    const int32_t* own_b = owner + (int64_t)(bh / H) * nb;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    for (int i = warp; i < nb; i += nwarps) {
+      const int32_t oi = own_b[i];
+      if (oi < 0 || oi >= P) {
+        if (lane == 0 && r == 0) report(d_status, SPARSP_ERR_DATA);
         continue;
       }
-      atomicOr(&bits[j >> 5], 1u << (j & 31));
+      if (oi != r) continue;
+      if (lane == 0) atomicOr(&mine[i >> 5], 1u << (i & 31));
+      const int64_t row = (int64_t)bh * nb + i;
+      const int32_t e0 = row_ptr[row], e1 = row_ptr[row + 1];
+      if (e1 < e0) {
+        if (lane == 0) report(d_status, SPARSP_ERR_DATA);
+        continue;
+      }
+      or_row(col_idx, e0, e1, 32, lane, nb, bits, d_status);
     }
   }
   __syncthreads();
   if (threadIdx.x < 32) {
     const int w = threadIdx.x;
-    uint32_t word = w < W ? bits[w] : 0u;
+    const uint32_t word = w < W ? bits[w] : 0u;
+    const uint32_t own = w < W ? mine[w] : 0u;
     if (w < W) bitmap[(int64_t)part * W + w] = word;
-    // blocks of this partition's own range [lo, hi)
-    uint32_t own = 0u;
-    for (int bit = 0; bit < 32; ++bit) {
-      const int j = w * 32 + bit;
-      if (j >= lo && j < hi) own |= 1u << bit;
-    }
-    int total = __popc(word), remote = __popc(word & ~own);
+    int total = __popc(word), remote = __popc(word & ~own), owned = __popc(own);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       total += __shfl_xor_sync(0xffffffffu, total, off);
       remote += __shfl_xor_sync(0xffffffffu, remote, off);
+      owned += __shfl_xor_sync(0xffffffffu, owned, off);
     }
     if (w == 0) {
       counts[part] = total;
       atomicAdd((unsigned long long*)&bytes[0], (unsigned long long)total * tile2);
       atomicAdd((unsigned long long*)&bytes[2], (unsigned long long)remote * tile2);
-      atomicAdd((unsigned long long*)&bytes[3], (unsigned long long)(nb - (hi - lo)) * tile2);
+      atomicAdd((unsigned long long*)&bytes[3], (unsigned long long)(nb - owned) * tile2);
       atomicAdd((unsigned long long*)&bytes[1], (unsigned long long)nb * tile2);
     }
   }
@@ -138,7 +167,7 @@ gather_kernel(const int32_t* __restrict__ dem_ptr, const int32_t* __restrict__ d
 }  // namespace
 
 sparsp_status_t launch_kv_demand(const Dims& s, int P, const int32_t* row_ptr,
-                                 const int32_t* col_idx, uint32_t* bitmap, int32_t* dem_ptr,
+                                 const int32_t* col_idx, const int32_t* owner, uint32_t* bitmap, int32_t* dem_ptr,
                                  int32_t* dem_idx, const void* k, const void* v, void* kg,
                                  void* vg, int64_t cap, uint64_t* bytes, int32_t* d_status,
                                  cudaStream_t st) {
@@ -146,7 +175,7 @@ sparsp_status_t launch_kv_demand(const Dims& s, int P, const int32_t* row_ptr,
   const int W = (s.nb + 31) / 32;
   const uint64_t tile2 = (uint64_t)s.Bt * s.d * s.elem * 2;
   if (cudaMemsetAsync(bytes, 0, 4 * sizeof(uint64_t), st) != cudaSuccess) return SPARSP_ERR_CUDA;
-  bitmap_kernel<<<nparts, 256, 0, st>>>(row_ptr, col_idx, s.H, s.nb, P, tile2, bitmap, dem_ptr,
+  bitmap_kernel<<<nparts, 256, 0, st>>>(row_ptr, col_idx, owner, s.H, s.nb, P, tile2, bitmap, dem_ptr,
                                         bytes, d_status);
   SPARSP_LAUNCH_CHECK();
   sparsp_status_t r = launch_scan_counts(dem_ptr, nparts, st);

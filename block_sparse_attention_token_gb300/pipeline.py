@@ -1,7 +1,8 @@
 """The whole hot path as one object with preallocated device buffers.
 
 forward(): reorder Q, K, V into tiles -> block scores -> Top-p/Top-k selection
--> KV demand of P partitions (+ gather) -> block-sparse attention -> O back to
+-> (optional) dependency-aware placement of blocks on the P partitions -> KV
+demand of P partitions (+ gather) -> block-sparse attention -> O back to
 raster order. backward(): dO into tiles -> attention backward -> dQ, dK, dV
 back to raster order. Every step is one or more libsparsp kernels on the
 current stream; nothing here allocates after construction.
@@ -11,19 +12,21 @@ from __future__ import annotations
 import torch
 
 from . import (EST_LOWRANK, EST_MEAN, PROF_SLOTS, Shape, attn_bwd, attn_fwd, attn_workspace_size,
-               block_scores, block_scores_pooled, block_scores_workspace_size, kv_demand, lib, reorder,
-               reorder_pool, select, select_workspace_size, DemandOut)
+               block_scores, block_scores_pooled, block_scores_workspace_size, kv_demand, lib, placement,
+               placement_workspace_size, reorder, reorder_pool, select, select_workspace_size, DemandOut)
 
 
 class Pipeline:
     def kernels_per_forward(self) -> int:
         """Kernels forward() launches: reorder x3, pool + product, select x3 (count,
-        scan, fill), demand x4 (bitmap, scan, list, gather), schedule (1, or 2 in
-        flat order) + attention, inverse reorder."""
+        scan, fill), placement x2 (affinity, greedy) when enabled, demand x4
+        (bitmap, scan, list, gather), schedule (1, or 2 in flat order) +
+        attention, inverse reorder."""
         lpt = 2 if self.flags & 1 else 1
         gather = 1 if self.demand.kg is not None else 0
         scores = (2 if self.est == EST_LOWRANK else 1) if self.fused else 2
-        return 3 + scores + 3 + 3 + gather + lpt + 1 + 1
+        place = 2 if self.owner is not None else 0
+        return 3 + scores + 3 + place + 3 + gather + lpt + 1 + 1
 
     def kernels_per_backward(self) -> int:
         """reorder dO, rowdot, CSR transpose, schedule, dQ, schedule, dK/dV, 3 inverse reorders."""
@@ -32,7 +35,7 @@ class Pipeline:
 
     def __init__(self, shape: Shape, estimator: str, top_p: float, k_floor: int, P: int, rank: int = 16,
                  gather: bool = True, flags: int = 0, backward: bool = False, device="cuda",
-                 fused_estimation: bool = True):
+                 fused_estimation: bool = True, placement: bool = False):
         self.shape, self.top_p, self.k_floor, self.P, self.rank, self.flags = shape, top_p, k_floor, P, rank, flags
         self.est = EST_LOWRANK if estimator == "lowrank" else EST_MEAN
         self.fused = fused_estimation
@@ -64,6 +67,10 @@ class Pipeline:
                                 torch.empty(parts + 1, dtype=torch.int32, device=dev),
                                 torch.empty(parts * s.nb, dtype=torch.int32, device=dev), kg, vg,
                                 torch.empty(4, dtype=torch.int64, device=dev))
+        self.owner = self.ws_place = None
+        if placement:
+            self.owner = torch.empty((s.B, s.nb), dtype=torch.int32, device=dev)
+            self.ws_place = torch.empty(max(placement_workspace_size(s), 16), dtype=torch.uint8, device=dev)
         self.ws_attn = torch.empty(max(attn_workspace_size(s, backward), 16), dtype=torch.uint8, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.prof = torch.zeros(PROF_SLOTS, dtype=torch.int64, device=dev)
@@ -95,7 +102,11 @@ class Pipeline:
         mark("scores")
         select(s, self.scores, self.top_p, self.k_floor, self.row_ptr, self.col_idx, self.ws_sel, self.status)
         mark("select")
-        kv_demand(s, self.P, self.row_ptr, self.col_idx, self.kb, self.vb, out=self.demand, status=self.status)
+        if self.owner is not None:
+            placement(s, self.P, self.row_ptr, self.col_idx, self.owner, self.ws_place, self.status)
+            mark("placement")
+        kv_demand(s, self.P, self.row_ptr, self.col_idx, self.kb, self.vb, out=self.demand, status=self.status,
+                  owner=self.owner)
         mark("kv_demand")
         attn_fwd(s, self.qb, self.kb, self.vb, self.row_ptr, self.col_idx, 0.0, self.ob, self.lse, self.ws_attn,
                  self.flags, self.prof if prof else None, self.status)

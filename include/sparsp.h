@@ -207,11 +207,14 @@ SPARSP_API sparsp_status_t sparsp_select_noalloc(const sparsp_shape_t* shape, co
                                                  sparsp_stream_t stream);
 
 /*
- * Step 4 - KV demand of P contiguous virtual query partitions, the one-GPU
- * analogue of Demand-Directed KV Routing ("SparSP: Exploiting Communication
- * Sparsity for Sequence-Parallel Video DiTs", abstract). Partition r owns query
- * blocks [floor(r*nb/P), floor((r+1)*nb/P)); its demand is the union of their
- * CSR rows.
+ * Step 4 - KV demand of P virtual query partitions, the one-GPU analogue of
+ * Demand-Directed KV Routing ("SparSP: Exploiting Communication Sparsity for
+ * Sequence-Parallel Video DiTs", abstract). With owner == NULL partition r owns
+ * the contiguous query blocks [floor(r*nb/P), floor((r+1)*nb/P)); otherwise
+ * owner is int32 [B, nb] (device) and partition r of batch element b owns the
+ * blocks i with owner[b*nb + i] == r, in every head (an entry outside [0, P)
+ * sets SPARSP_ERR_DATA and its block belongs to no partition). A partition's
+ * demand is the union of the CSR rows of the blocks it owns.
  *   bitmap  uint32 [B,H,P,ceil(nb/32)]: bit j of partition (b,h,r).
  *   dem_ptr int32 [B*H*P+1], dem_idx int32 (capacity B*H*P*nb): ascending set bits.
  *   kg, vg  [gather_cap_blocks, Bt, d] of shape->dtype: slot s holds the K/V tile
@@ -219,13 +222,35 @@ SPARSP_API sparsp_status_t sparsp_select_noalloc(const sparsp_shape_t* shape, co
  *           skips the gather (k, v may then be NULL). Slots beyond
  *           gather_cap_blocks are not written and set SPARSP_ERR_CAPACITY.
  *   bytes   uint64 [4]: demanded, all (every partition receives all KV),
- *           remote_demanded, remote_all (blocks outside the partition's own
- *           range); K and V both counted.
+ *           remote_demanded, remote_all (blocks the partition does not own);
+ *           K and V both counted.
  */
 SPARSP_API sparsp_status_t sparsp_kv_demand(const sparsp_shape_t* shape, int32_t P, const int32_t* row_ptr,
-                                 const int32_t* col_idx, uint32_t* bitmap, int32_t* dem_ptr,
-                                 int32_t* dem_idx, const void* k, const void* v, void* kg,
-                                 void* vg, int64_t gather_cap_blocks, uint64_t* bytes,
+                                 const int32_t* col_idx, const int32_t* owner, uint32_t* bitmap,
+                                 int32_t* dem_ptr, int32_t* dem_idx, const void* k, const void* v,
+                                 void* kg, void* vg, int64_t gather_cap_blocks, uint64_t* bytes,
+                                 int32_t* d_status, sparsp_stream_t stream);
+
+/*
+ * Step 4b - Dependency-Aware Placement ("SparSP: Exploiting Communication
+ * Sparsity for Sequence-Parallel Video DiTs", abstract: sequence blocks placed
+ * on ranks according to the sparse attention pattern), over the P virtual
+ * partitions of sparsp_kv_demand. The pages give no algorithm; this is a
+ * deterministic greedy on the co-selection affinity of batch element b,
+ *   A[i][j] = #heads whose row i holds j + #heads whose row j holds i (i != j),
+ * with one assignment per batch element shared by all heads and the partition
+ * sizes of the contiguous split (floor((r+1)*nb/P) - floor(r*nb/P)):
+ *   blocks in order of sum_j A[i][j] descending (ties: lower i); each goes to
+ *   the partition with spare capacity whose placed blocks have the largest
+ *   summed affinity to it (ties: more spare capacity, then lower r).
+ * owner: int32 [B, nb] (device), written with the partition of every block, to
+ * pass to sparsp_kv_demand. ws: at least sparsp_placement_workspace_size()
+ * bytes (B*nb*nb int32 affinity counts). A column index outside [0, nb) or a
+ * row with more than nb entries sets SPARSP_ERR_DATA and is skipped.
+ */
+SPARSP_API size_t sparsp_placement_workspace_size(const sparsp_shape_t* shape);
+SPARSP_API sparsp_status_t sparsp_placement(const sparsp_shape_t* shape, int32_t P, const int32_t* row_ptr,
+                                 const int32_t* col_idx, int32_t* owner, void* ws, size_t ws_bytes,
                                  int32_t* d_status, sparsp_stream_t stream);
 
 /*

@@ -115,11 +115,20 @@ def test_call_validation_codes(lib):
                                    None) == sp.UNSUPPORTED
     assert lib.sparsp_block_scores(S, sp.EST_MEAN, FAKE, FAKE, None, None, 16, FAKE, FAKE, 4, None) == sp.WORKSPACE
     # demand: P out of range, kg without vg, negative capacity
-    args = (FAKE, FAKE, FAKE, FAKE, FAKE)
+    args = (FAKE, FAKE, None, FAKE, FAKE, FAKE)
     assert lib.sparsp_kv_demand(S, 0, *args, None, None, None, None, 0, FAKE, None, None) == sp.SHAPE
     assert lib.sparsp_kv_demand(S, s.nb + 1, *args, None, None, None, None, 0, FAKE, None, None) == sp.SHAPE
     assert lib.sparsp_kv_demand(S, 2, *args, FAKE, FAKE, FAKE, None, 4, FAKE, None, None) == sp.INVALID_ARG
     assert lib.sparsp_kv_demand(S, 2, *args, FAKE, FAKE, FAKE, FAKE, -1, FAKE, None, None) == sp.INVALID_ARG
+    assert lib.sparsp_kv_demand(S, 2, FAKE, FAKE, FAKE + 4, FAKE, FAKE, FAKE, None, None, None, None, 0, FAKE,
+                                None, None) == sp.ALIGN
+    # placement: P out of range, missing owner, small workspace
+    need = lib.sparsp_placement_workspace_size(S)
+    assert need == s.B * s.nb * s.nb * 4
+    assert lib.sparsp_placement(S, 0, FAKE, FAKE, FAKE, FAKE, need, None, None) == sp.SHAPE
+    assert lib.sparsp_placement(S, s.nb + 1, FAKE, FAKE, FAKE, FAKE, need, None, None) == sp.SHAPE
+    assert lib.sparsp_placement(S, 2, FAKE, FAKE, None, FAKE, need, None, None) == sp.INVALID_ARG
+    assert lib.sparsp_placement(S, 2, FAKE, FAKE, FAKE, FAKE, need - 1, None, None) == sp.WORKSPACE
     # attention: NaN scale, small workspace, misaligned optional pointer, fp32 backward
     p7 = (FAKE,) * 5
     assert lib.sparsp_attn_fwd(S, *p7, f(float("nan")), FAKE, FAKE, FAKE, 1 << 30, 0, None, None,

@@ -98,6 +98,25 @@ def test_demand_sets_bitexact_and_gather_sampled(run):
           f"({100 * ref.bytes[0] / ref.bytes[1]:.1f}%); remote {100 * ref.bytes[2] / ref.bytes[3]:.1f}%")
 
 
+def test_placement_and_placed_demand_bitexact(run):
+    wl, ch, g = run.wl, run.ch, run.ch.g
+    own_ref = orc.placement(ch.sel.row_ptr, ch.sel.col_idx, g.B, g.H, g.nb, wl.P)
+    st = status_word()
+    owner = sp.placement(run.shape, wl.P, i32(ch.sel.row_ptr), i32(ch.sel.col_idx), status=st)
+    out = sp.kv_demand(run.shape, wl.P, i32(ch.sel.row_ptr), i32(ch.sel.col_idx), status=st, owner=owner)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert np.array_equal(host(owner), own_ref)
+    ref = orc.kv_demand(ch.sel.row_ptr, ch.sel.col_idx, g.B, g.H, g.nb, wl.P, g.Bt, g.d, wl.elem_bytes,
+                        owner=own_ref)
+    assert np.array_equal(host(out.dem_ptr), ref.dem_ptr)
+    assert np.array_equal(host(out.dem_idx)[:int(ref.dem_ptr[-1])], ref.dem_idx)
+    assert host(out.bytes).astype(np.uint64).tolist() == ref.bytes.tolist()
+    contiguous = orc.kv_demand(ch.sel.row_ptr, ch.sel.col_idx, g.B, g.H, g.nb, wl.P, g.Bt, g.d, wl.elem_bytes)
+    print(f"{wl.name}: remote demanded bytes contiguous {contiguous.bytes[2] / 1e9:.3f} GB, "
+          f"placed {ref.bytes[2] / 1e9:.3f} GB ({100 * (1 - ref.bytes[2] / contiguous.bytes[2]):+.1f}% saved)")
+
+
 def _sample_rows(ch, n, seed):
     g = ch.g
     counts = np.diff(ch.sel.row_ptr)

@@ -2,6 +2,7 @@
 workloads the oracle finishes in seconds (several tiles, ragged item counts,
 both tile sizes, both head dimensions, fp32 and bf16), plus edge cases."""
 import math
+import os
 
 import numpy as np
 import pytest
@@ -176,6 +177,86 @@ def test_kv_demand_capacity_shortfall():
 
 
 @pytest.mark.parametrize("name", list(SMALL))
+def test_placement_and_placed_demand_bitexact(name):
+    wl, data, shape = _setup(name)
+    ch = OracleChain(wl, data)
+    g = ch.g
+    own_ref = orc.placement(ch.sel.row_ptr, ch.sel.col_idx, g.B, g.H, g.nb, wl.P)
+    st = status_word()
+    owner = sp.placement(shape, wl.P, i32(ch.sel.row_ptr), i32(ch.sel.col_idx), status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert np.array_equal(host(owner), own_ref)
+    ref = orc.kv_demand(ch.sel.row_ptr, ch.sel.col_idx, g.B, g.H, g.nb, wl.P, g.Bt, g.d, wl.elem_bytes,
+                        ch.kb, ch.vb, owner=own_ref)
+    out = sp.kv_demand(shape, wl.P, i32(ch.sel.row_ptr), i32(ch.sel.col_idx), dev(ch.kb, wl), dev(ch.vb, wl),
+                       status=st, owner=owner)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert np.array_equal(host(out.bitmap).view(np.uint32).ravel(), ref.bitmap.ravel())
+    assert np.array_equal(host(out.dem_ptr), ref.dem_ptr)
+    total = int(ref.dem_ptr[-1])
+    assert np.array_equal(host(out.dem_idx)[:total], ref.dem_idx)
+    assert np.array_equal(host(out.kg)[:total], ref.kg)
+    assert np.array_equal(host(out.vg)[:total], ref.vg)
+    assert host(out.bytes).astype(np.uint64).tolist() == ref.bytes.tolist()
+
+
+def test_placement_hand_example_and_extremes():
+    import json
+    gold = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "placement_hand.json")))
+    # 6 tiles of 4x4x4 tokens in one head
+    shape = sp.make_shape(1, 1, 24, 4, 4, 64, 4, 4, 4, "bf16")
+    assert shape.nb == gold["nb"]
+    rows = gold["rows"]
+    rp = np.concatenate([[0], np.cumsum([len(r) for r in rows])]).astype(np.int32)
+    ci = np.array([j for r in rows for j in r], dtype=np.int32)
+    owner = sp.placement(shape, gold["P"], i32(rp), i32(ci))
+    dem = sp.kv_demand(shape, gold["P"], i32(rp), i32(ci), owner=owner)
+    torch.cuda.synchronize()
+    assert host(owner)[0].tolist() == gold["owner"]
+    tile2 = shape.Bt * shape.d * 2 * 2
+    assert int(host(dem.bytes)[2]) == gold["remote_blocks_placed"] * tile2
+    # one partition, and one partition per block, on a selected workload
+    wl, data, shape = _setup("r64")
+    ch = OracleChain(wl, data)
+    g = ch.g
+    for P in (1, g.nb):
+        own_ref = orc.placement(ch.sel.row_ptr, ch.sel.col_idx, g.B, g.H, g.nb, P)
+        owner = sp.placement(shape, P, i32(ch.sel.row_ptr), i32(ch.sel.col_idx))
+        assert np.array_equal(host(owner), own_ref)
+        r2 = orc.kv_demand(ch.sel.row_ptr, ch.sel.col_idx, g.B, g.H, g.nb, P, g.Bt, g.d, 2, owner=own_ref)
+        o2 = sp.kv_demand(shape, P, i32(ch.sel.row_ptr), i32(ch.sel.col_idx), owner=owner)
+        assert np.array_equal(host(o2.dem_ptr), r2.dem_ptr)
+        assert np.array_equal(host(o2.dem_idx)[:int(r2.dem_ptr[-1])], r2.dem_idx)
+        assert host(o2.bytes).astype(np.uint64).tolist() == r2.bytes.tolist()
+
+
+def test_placed_demand_rejects_bad_owner():
+    wl, data, shape = _setup("r64")
+    ch = OracleChain(wl, data)
+    g = ch.g
+    own = orc.placement(ch.sel.row_ptr, ch.sel.col_idx, g.B, g.H, g.nb, wl.P)
+    bad = own.copy()
+    bad[0, 3] = wl.P          # block 3 belongs to no partition
+    st = status_word()
+    out = sp.kv_demand(shape, wl.P, i32(ch.sel.row_ptr), i32(ch.sel.col_idx), status=st,
+                       owner=torch.from_numpy(bad).cuda())
+    torch.cuda.synchronize()
+    assert st.item() == sp.DATA
+    # the other blocks are still served: the sets equal the oracle's with block 3 in no partition
+    members = [[i for i in range(g.nb) if bad[0, i] == r] for r in range(wl.P)]
+    ptr = host(out.dem_ptr)
+    idx = host(out.dem_idx)
+    for h in range(g.H):
+        for r in range(wl.P):
+            part = h * wl.P + r
+            want = sorted({int(j) for i in members[r]
+                           for j in ch.sel.col_idx[ch.sel.row_ptr[h * g.nb + i]:ch.sel.row_ptr[h * g.nb + i + 1]]})
+            assert idx[ptr[part]:ptr[part + 1]].tolist() == want
+
+
+@pytest.mark.parametrize("name", list(SMALL))
 @pytest.mark.parametrize("flat", [False, True])
 def test_lpt_schedule_bitexact(name, flat):
     wl, data, shape = _setup(name)
@@ -319,6 +400,29 @@ def test_pipeline_end_to_end(name, fused):
         b, h, i = r // (g.H * g.nb), (r // g.nb) % g.H, r % g.nb
         sl = slice(i * g.Bt, (i + 1) * g.Bt)
         compare_values(ob[b, h, sl], O[b, h, sl], wl, f"O row {r}")
+
+
+@pytest.mark.parametrize("name", ["medium", "r128"])
+def test_pipeline_with_placement(name):
+    """Placement inside the pipeline: owner and demand equal the oracle's on
+    the GPU's own CSR, and attention output is unchanged (placement only moves
+    KV demand, never the attended sets)."""
+    wl, data, shape = _setup(name)
+    args = [dev(data[x], wl) for x in ("q", "k", "v")]
+    plain = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P)
+    placed = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P, placement=True)
+    o1, _ = plain.forward(*args)
+    o2, _ = placed.forward(*args)
+    torch.cuda.synchronize()
+    assert placed.status.item() == 0
+    assert torch.equal(o1, o2)
+    g = orc.grid_of(wl)
+    rp, ci = host(placed.row_ptr), host(placed.col_idx)
+    own_ref = orc.placement(rp, ci, g.B, g.H, g.nb, wl.P)
+    assert np.array_equal(host(placed.owner), own_ref)
+    ref = orc.kv_demand(rp, ci, g.B, g.H, g.nb, wl.P, g.Bt, g.d, wl.elem_bytes, owner=own_ref)
+    assert host(placed.demand.bytes).astype(np.uint64).tolist() == ref.bytes.tolist()
+    assert placed.kernels_per_forward() == plain.kernels_per_forward() + 2
 
 
 def test_host_pipeline_overlapped_steps_match_device_pipeline():
