@@ -22,6 +22,9 @@ Plain NumPy, float64 accumulation, written step by step from the pages:
   score matrix), and the FlashAttention comparison of the mlsift.com entry.
 * The longest-first work order: the straggler problem of the mlsift.com entry
   and the lopsided per-head work of "How DSV works" (third paragraph).
+* Dependency-aware placement of blocks on the P partitions: SparSP, abstract.
+* Virtual-rank load balancing (head migration) and slack-aware sparse
+  augmentation: the mlsift.com entry, abstract.
 
 Parity pins for every function live in tests/test_oracle_*.py. Every
 function here has at least one pin that does not re-run its own formula.
@@ -579,3 +582,150 @@ def csc_of(row_ptr, col_idx, B, H, nb):
     col_ptr[1:] = np.cumsum([len(x) for x in lists])
     row_idx = np.array([i for x in lists for i in x], dtype=np.int32)
     return col_ptr.astype(np.int32), row_idx
+
+
+# ---------------------------------------------------------------------------
+# Virtual-rank load balancing and slack-aware augmentation
+# ---------------------------------------------------------------------------
+
+def head_costs(row_ptr, B, H, nb) -> np.ndarray:
+    """Attention work of every head: the number of selected block pairs of its
+    rows (each pair costs the same 4*Bt^2*d flops). Returns int64 [B, H]."""
+    rp = np.asarray(row_ptr, dtype=np.int64)
+    return np.array([[int(rp[(b * H + h + 1) * nb] - rp[(b * H + h) * nb]) for h in range(H)]
+                     for b in range(B)], dtype=np.int64)
+
+
+def rank_loads(costs_b, head_rank_b, P) -> np.ndarray:
+    """Sum of the head costs held by each of the P ranks (one batch element)."""
+    loads = np.zeros(P, dtype=np.int64)
+    for h, c in enumerate(costs_b):
+        loads[int(head_rank_b[h])] += int(c)
+    return loads
+
+
+def imbalance(loads) -> float:
+    """Critical (maximum) rank load over the mean rank load; 1.0 when idle."""
+    loads = np.asarray(loads, dtype=np.int64)
+    total = int(loads.sum())
+    return 1.0 if total == 0 else float(loads.max()) * len(loads) / total
+
+
+def balance_heads(costs, P, max_migrations):
+    """Runtime Load Balancing over P virtual ranks (the mlsift.com tag listing,
+    Top-p video sparse-attention entry, abstract: a few heavy heads migrate to
+    shorten the critical path), one batch element at a time.
+
+    Start: the contiguous head split, rank r holding heads
+    [floor(r*H/P), floor((r+1)*H/P)). Then, at most max_migrations times:
+      c = the most loaded rank, t = the least loaded (ties: lower rank);
+      among the heads on c pick the one whose move to t gives the smallest
+      max(L_c - cost, L_t + cost) (ties: lower head index);
+      move it only if that value is below L_c, else stop.
+    Every move lowers the sum of squared loads, so the loop ends.
+    Returns (head_rank [B, H] int32, migrations [B] int64).
+    """
+    costs = np.asarray(costs, dtype=np.int64)
+    B, H = costs.shape
+    head_rank = np.zeros((B, H), dtype=np.int32)
+    moves = np.zeros(B, dtype=np.int64)
+    for b in range(B):
+        for r, (lo, hi) in enumerate(partition_bounds(H, P)):
+            head_rank[b, lo:hi] = r
+        loads = rank_loads(costs[b], head_rank[b], P)
+        for _ in range(int(max_migrations)):
+            c = int(np.argmax(loads))
+            t = int(np.argmin(loads))
+            best = None
+            for h in range(H):
+                if head_rank[b, h] != c:
+                    continue
+                x = int(costs[b, h])
+                new_max = max(int(loads[c]) - x, int(loads[t]) + x)
+                if best is None or new_max < best[0]:
+                    best = (new_max, h)
+            if best is None or best[0] >= loads[c]:
+                break
+            h = best[1]
+            head_rank[b, h] = t
+            loads[c] -= costs[b, h]
+            loads[t] += costs[b, h]
+            moves[b] += 1
+    return head_rank, moves
+
+
+def block_values(S) -> np.ndarray:
+    """The value of every block of a row: its softmax mass, taken as selection
+    takes it (e_j = exp(S_j - max) in float32, Z = sum e in float64), rounded
+    to float32: v_j = fl32(e_j / Z). S: float32 [R, nb]."""
+    S = np.asarray(S)
+    if S.dtype != np.float32:
+        raise TypeError("scores must be float32")
+    out = np.zeros(S.shape, dtype=np.float32)
+    for r in range(S.shape[0]):
+        row = S[r] + np.float32(0.0)
+        e32 = np.exp((row - row.max()).astype(np.float32)).astype(np.float32)
+        e = e32.astype(np.float64)
+        out[r] = (e / e.sum()).astype(np.float32)
+    return out
+
+
+@dataclass
+class Augmented:
+    row_ptr: np.ndarray        # int32 [R+1], the augmented CSR
+    col_idx: np.ndarray        # int32 [nnz'], ascending per row
+    added: np.ndarray          # int64 [B, P], blocks added per rank
+    loads: np.ndarray          # int64 [B, P], rank loads after augmentation
+    cut: np.ndarray            # float32 [B, P], value of the last block added (0 if none)
+    next_value: np.ndarray     # float32 [B, P], best value left out (0 if none)
+
+
+def augment(S, row_ptr, col_idx, B, H, nb, head_rank, P) -> Augmented:
+    """Slack-Aware Sparse Augmentation (the mlsift.com tag listing, Top-p video
+    sparse-attention entry, abstract: slack left on non-critical ranks is
+    filled with additional high-value blocks).
+
+    With the heads placed on ranks (head_rank [B, H]) and loads L_r in block
+    pairs, the critical load is L* = max_r L_r; rank r has slack L* - L_r.
+    Its candidates are the unselected blocks (h, i, j) of the rows of its
+    heads, valued by block_values; it takes the min(slack, #candidates) best,
+    ordered by (value descending, row (b*H + h)*nb + i ascending, j ascending).
+    The critical path (L*) is unchanged. Returns the augmented CSR (rows stay
+    ascending) with per-rank counts.
+    """
+    V = block_values(S)
+    rp = np.asarray(row_ptr, dtype=np.int64)
+    costs = head_costs(rp, B, H, nb)
+    rows = [set(int(j) for j in col_idx[rp[r]:rp[r + 1]]) for r in range(B * H * nb)]
+    added = np.zeros((B, P), dtype=np.int64)
+    loads_out = np.zeros((B, P), dtype=np.int64)
+    cut = np.zeros((B, P), dtype=np.float32)
+    nxt = np.zeros((B, P), dtype=np.float32)
+    for b in range(B):
+        loads = rank_loads(costs[b], head_rank[b], P)
+        top = int(loads.max())
+        for r in range(P):
+            cands = []
+            for h in range(H):
+                if int(head_rank[b, h]) != r:
+                    continue
+                for i in range(nb):
+                    row = (b * H + h) * nb + i
+                    for j in range(nb):
+                        if j not in rows[row]:
+                            cands.append((-float(V[row, j]), row, j))
+            cands.sort()
+            take = min(top - int(loads[r]), len(cands))
+            for (_, row, j) in cands[:take]:
+                rows[row].add(j)
+            added[b, r] = take
+            loads_out[b, r] = int(loads[r]) + take
+            if take > 0:
+                cut[b, r] = -cands[take - 1][0]
+            if take < len(cands):
+                nxt[b, r] = -cands[take][0]
+    counts = [len(x) for x in rows]
+    new_ptr = np.zeros(len(rows) + 1, dtype=np.int64)
+    new_ptr[1:] = np.cumsum(counts)
+    new_idx = np.array([j for x in rows for j in sorted(x)], dtype=np.int32)
+    return Augmented(new_ptr.astype(np.int32), new_idx, added, loads_out, cut, nxt)

@@ -430,3 +430,104 @@ def test_placement_is_a_balanced_assignment_and_contiguous_owner_is_the_default(
     b = orc.kv_demand(sel.row_ptr, sel.col_idx, g.B, g.H, g.nb, 4, g.Bt, g.d, 4, kb, vb, owner=contiguous)
     assert np.array_equal(a.bitmap, b.bitmap) and np.array_equal(a.dem_idx, b.dem_idx)
     assert a.bytes.tolist() == b.bytes.tolist() and np.array_equal(a.kg, b.kg)
+
+
+# ------------------------------------------- load balancing and augmentation
+
+def test_balance_hand_example():
+    gold = _load("balance_hand.json")
+    costs = np.array([gold["costs"]], dtype=np.int64)
+    P = gold["P"]
+    hr0, mv0 = orc.balance_heads(costs, P, 0)
+    assert orc.rank_loads(costs[0], hr0[0], P).tolist() == gold["contiguous_loads"] and mv0[0] == 0
+    hr, mv = orc.balance_heads(costs, P, 10)
+    assert hr[0].tolist() == gold["head_rank"] and int(mv[0]) == gold["migrations"]
+    assert orc.rank_loads(costs[0], hr[0], P).tolist() == gold["loads"]
+    hr1, _ = orc.balance_heads(costs, P, 1)
+    assert hr1[0].tolist() == gold["head_rank_one_move"]
+    assert orc.imbalance(gold["contiguous_loads"]) == gold["imbalance_before"]
+    assert orc.imbalance(gold["loads"]) == gold["imbalance_after"]
+
+
+def test_balance_invariants_and_stopping_rule():
+    rng = np.random.default_rng(7)
+    for trial in range(40):
+        H = int(rng.integers(2, 13))
+        P = int(rng.integers(1, H + 1))
+        costs = rng.integers(0, 50, size=(2, H)) ** 2         # heavy-tailed head costs
+        hr0, _ = orc.balance_heads(costs, P, 0)
+        hr, mv = orc.balance_heads(costs, P, H * P * 4)
+        for b in range(2):
+            before = orc.rank_loads(costs[b], hr0[b], P)
+            after = orc.rank_loads(costs[b], hr[b], P)
+            assert after.sum() == costs[b].sum()               # work is conserved
+            assert after.max() <= before.max()                 # never worse than the contiguous split
+            assert set(hr[b].tolist()) <= set(range(P))
+            # stopped because no head of the critical rank improves the pair
+            c, t = int(np.argmax(after)), int(np.argmin(after))
+            for h in range(H):
+                if hr[b, h] == c:
+                    assert max(after[c] - costs[b, h], after[t] + costs[b, h]) >= after[c]
+    # equal costs and H divisible by P: already balanced, nothing moves
+    hr, mv = orc.balance_heads(np.full((1, 12), 5), 4, 100)
+    assert mv[0] == 0 and orc.imbalance(orc.rank_loads(np.full(12, 5), hr[0], 4)) == 1.0
+
+
+def test_block_values_are_the_row_softmax():
+    from scipy.special import softmax
+    rng = np.random.default_rng(8)
+    S = (rng.standard_normal((20, 37)) * 3).astype(np.float32)
+    V = orc.block_values(S)
+    ref = softmax(S.astype(np.float64), axis=1)
+    np.testing.assert_allclose(V, ref, rtol=2e-6, atol=0)
+    assert np.abs(V.astype(np.float64).sum(axis=1) - 1).max() < 1e-5
+
+
+def test_augment_hand_example():
+    gold = _load("augment_hand.json")
+    rp, ci = _csr(gold["rows"])
+    S = np.array(gold["scores"], dtype=np.float32)
+    aug = orc.augment(S, rp, ci, gold["B"], gold["H"], gold["nb"], np.array([gold["head_rank"]]), gold["P"])
+    rows = [aug.col_idx[aug.row_ptr[r]:aug.row_ptr[r + 1]].tolist() for r in range(len(gold["rows"]))]
+    assert rows == gold["augmented_rows"]
+    assert aug.added[0].tolist() == gold["added"] and aug.loads[0].tolist() == gold["loads"]
+    np.testing.assert_allclose(aug.cut[0], gold["cut"], rtol=1e-6)
+    np.testing.assert_allclose(aug.next_value[0], gold["next_value"], rtol=1e-6)
+
+
+def test_augment_fills_slack_with_the_best_blocks():
+    from scipy.special import softmax
+    wl, g, data, qb, kb, vb = _tiny()
+    S = orc.scores_mean(qb, kb, g.Bt).astype(np.float32).reshape(-1, g.nb)
+    # a lopsided selection: head 0 keeps 3 blocks per row, head 1 one block
+    rows = []
+    for h in range(g.H):
+        for i in range(g.nb):
+            order = np.argsort(-S[h * g.nb + i], kind="stable")
+            rows.append(sorted(order[:3 if h == 0 else 1].tolist()))
+    rp, ci = _csr(rows)
+    hr, _ = orc.balance_heads(orc.head_costs(rp, 1, g.H, g.nb), 2, 0)
+    aug = orc.augment(S, rp, ci, 1, g.H, g.nb, hr, 2)
+    V = softmax(S.astype(np.float64), axis=1)
+    top = 3 * g.nb
+    assert aug.loads[0].tolist() == [top, top] and aug.added[0].tolist() == [0, 2 * g.nb]
+    added, left = [], []
+    for i in range(g.nb):
+        r = g.nb + i
+        new = set(aug.col_idx[aug.row_ptr[r]:aug.row_ptr[r + 1]].tolist())
+        assert set(rows[r]) <= new                              # nothing is dropped
+        added += [V[r, j] for j in new - set(rows[r])]
+        left += [V[r, j] for j in range(g.nb) if j not in new]
+        assert sorted(new) == list(aug.col_idx[aug.row_ptr[r]:aug.row_ptr[r + 1]])
+    assert min(added) >= max(left) * (1 - 1e-6)                 # the best candidates were taken
+    for r in range(g.nb):                                        # the critical head is untouched
+        assert aug.col_idx[aug.row_ptr[r]:aug.row_ptr[r + 1]].tolist() == rows[r]
+
+
+def test_augment_without_slack_changes_nothing():
+    rows = [[0, 1], [1], [0], [0, 1]]          # two heads of 2 blocks, 3 pairs each
+    rp, ci = _csr(rows)
+    S = np.zeros((4, 2), dtype=np.float32)
+    aug = orc.augment(S, rp, ci, 1, 2, 2, np.array([[0, 1]]), 2)
+    assert aug.added.sum() == 0
+    assert aug.row_ptr.tolist() == rp.tolist() and aug.col_idx.tolist() == ci.tolist()
