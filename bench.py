@@ -178,6 +178,8 @@ def main():
     ap.add_argument("--unfused", action="store_true", help="separate pooling pass instead of reorder+pool")
     ap.add_argument("--placement", action="store_true",
                     help="dependency-aware block placement inside the step (default: contiguous partitions)")
+    ap.add_argument("--augment", action="store_true",
+                    help="head balancing over P virtual ranks + slack-aware augmentation inside the step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--heads", type=int, default=0, help="override the head count (smaller profiling case)")
@@ -212,7 +214,8 @@ def main():
     shape = sp.shape_of(wl)
     flags = (sp.SCHED_FLAT if args.flat else 0) | (sp.KERNEL_PORTABLE if args.portable else 0)
     pipe = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P, backward=wl.backward, flags=flags,
-                       fused_estimation=not args.unfused, placement=args.placement)
+                       fused_estimation=not args.unfused, placement=args.placement,
+                       migrations=wl.P if args.augment else None, augment=args.augment)
     tdt = shape.torch_dtype
     host_in = {x: torch.from_numpy(data[x]).to(tdt).pin_memory() for x in ("q", "k", "v")}
     dev_in = {x: host_in[x].cuda() for x in host_in}
@@ -235,7 +238,7 @@ def main():
     torch.cuda.synchronize()
     if pipe.status.item() != 0:
         raise SystemExit(f"device status {sp.status_string(pipe.status.item())}")
-    nnz = int(pipe.row_ptr[-1].item())
+    nnz = int(pipe.csr[0][-1].item())     # the CSR attention ran on
     demanded, all_bytes, remote_dem, remote_all = (int(x) for x in pipe.demand.bytes.tolist())
 
     # ---- timed region: K steps, events around every stage
@@ -364,6 +367,33 @@ def main():
                       "remote_reduction": 1.0 - pb[2] / cb[2] if cb[2] else None,
                       "placement_ms": p0.elapsed_time(p1) / 5, "in_step": bool(args.placement)}
 
+    # virtual-rank balancing and slack-aware augmentation on this step's selection
+    bal = sp.balance_heads(shape, wl.P, pipe.row_ptr, wl.P)
+    bal0 = sp.balance_heads(shape, wl.P, pipe.row_ptr, 0)
+    ws_aug = torch.empty(max(sp.augment_workspace_size(shape, wl.P), 16), dtype=torch.uint8, device="cuda")
+    rp_aug = torch.empty(shape.rows + 1, dtype=torch.int32, device="cuda")
+    ci_aug = torch.empty(shape.rows * shape.nb, dtype=torch.int32, device="cuda")
+    added = torch.empty((shape.B, wl.P), dtype=torch.int64, device="cuda")
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(5):
+        sp.balance_heads(shape, wl.P, pipe.row_ptr, wl.P, out=bal)
+        sp.augment(shape, wl.P, pipe.scores, pipe.row_ptr, pipe.col_idx, bal.head_rank, rp_aug, ci_aug, added,
+                   ws_aug)
+    a1.record(stream)
+    torch.cuda.synchronize()
+    L = bal.loads.cpu().numpy()
+    L0 = bal0.loads.cpu().numpy()
+
+    def _imb(x):
+        return float(x.max() * x.shape[-1] / x.sum()) if x.sum() else 1.0
+
+    balance_info = {"ranks": wl.P, "imbalance_contiguous": _imb(L0[0, 0]), "imbalance_balanced": _imb(L[0, 1]),
+                    "migrations": int(bal.migrations[0].item()), "blocks_added": int(added.sum().item()),
+                    "nnz_after_augment": int(rp_aug[-1].item()),
+                    "balance_augment_ms": a0.elapsed_time(a1) / 5, "in_step": bool(args.augment)}
+
     launches = args.steps * (pipe.kernels_per_forward() + (pipe.kernels_per_backward() if wl.backward else 0))
     if rank != 0:
         if world > 1:
@@ -373,7 +403,7 @@ def main():
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(wl, data)
         cpu.pop("seconds", None)
-    counts = np.diff(pipe.row_ptr.cpu().numpy())
+    counts = np.diff(pipe.csr[0].cpu().numpy())
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -388,12 +418,14 @@ def main():
                    "kernel": "portable mma.sync" if args.portable else "default",
                    "estimation": "separate pooling pass" if args.unfused else "fused with the reorder",
                    "partitions": "dependency-aware placement" if args.placement else "contiguous",
+                   "augmentation": "balanced heads + slack fill" if args.augment else "none",
                    "l2": f"inputs larger than L2 ({shape.B * shape.H * shape.N * shape.d * 2 / 1e6:.0f} MB per tensor)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "stages_ms": stage_ms,
         "kv_bytes": {"demanded": demanded, "all": all_bytes, "remote_demanded": remote_dem,
                      "remote_all": remote_all},
         "placement": placement_info,
+        "balance": balance_info,
         "attn_sm_imbalance": imbalance,
         "clocks": clk, "e2e": e2e, "gpu_launches": launches, "roofline": roofline, "cpu_baseline": cpu,
     }

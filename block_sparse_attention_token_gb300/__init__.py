@@ -88,6 +88,9 @@ _SIG = {
                                 _P]),
     "sparsp_placement_workspace_size": (ctypes.c_size_t, [_P]),
     "sparsp_placement": (_I32, [_P, _I32, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
+    "sparsp_balance_heads": (_I32, [_P, _I32, _I32, _P, _P, _P, _P, _P]),
+    "sparsp_augment_workspace_size": (ctypes.c_size_t, [_P, _I32]),
+    "sparsp_augment": (_I32, [_P, _I32, _P, _P, _P, _P, _P, _P, ctypes.c_int64, _P, _P, ctypes.c_size_t, _P, _P]),
     "sparsp_lpt_workspace_size": (ctypes.c_size_t, [_P]),
     "sparsp_lpt_schedule": (_I32, [_P, _P, ctypes.c_uint32, _P, _P, ctypes.c_size_t, _P]),
     "sparsp_attn_workspace_size": (ctypes.c_size_t, [_P, _I32]),
@@ -277,6 +280,53 @@ def placement(shape: Shape, P: int, row_ptr, col_idx, owner=None, ws=None, statu
         _sref(shape), int(P), _ptr(row_ptr), _ptr(col_idx), _ptr(owner), _ptr(ws), ws.numel(),
         _ptr(status), _stream(stream)))
     return owner
+
+
+@dataclass
+class Balance:
+    head_rank: torch.Tensor     # int32 [B, H]
+    loads: torch.Tensor         # int64 [B, 2, P]: before, after
+    migrations: torch.Tensor    # int32 [B]
+
+
+def balance_heads(shape: Shape, P: int, row_ptr, max_migrations: int, out: Balance | None = None,
+                  stream=None) -> Balance:
+    """Heads of each batch element on P virtual ranks: contiguous split, then
+    greedy migrations of heavy heads off the critical rank."""
+    dev = row_ptr.device
+    if out is None:
+        out = Balance(torch.empty((shape.B, shape.H), dtype=torch.int32, device=dev),
+                      torch.empty((shape.B, 2, P), dtype=torch.int64, device=dev),
+                      torch.empty(max(shape.B, 4), dtype=torch.int32, device=dev))
+    _check("sparsp_balance_heads", lib().sparsp_balance_heads(
+        _sref(shape), int(P), int(max_migrations), _ptr(row_ptr), _ptr(out.head_rank), _ptr(out.loads),
+        _ptr(out.migrations), _stream(stream)))
+    return out
+
+
+def augment_workspace_size(shape: Shape, P: int) -> int:
+    return lib().sparsp_augment_workspace_size(_sref(shape), int(P))
+
+
+def augment(shape: Shape, P: int, scores, row_ptr, col_idx, head_rank, row_ptr_out=None, col_idx_out=None,
+            added=None, ws=None, status=None, stream=None):
+    """Slack-aware augmentation of the CSR: each rank's slack up to the critical
+    load is filled with its heads' best unselected blocks. Returns
+    (row_ptr_out, col_idx_out, added [B, P])."""
+    dev = row_ptr.device
+    if row_ptr_out is None:
+        row_ptr_out = torch.empty(shape.rows + 1, dtype=torch.int32, device=dev)
+    if col_idx_out is None:
+        col_idx_out = torch.empty(shape.rows * shape.nb, dtype=torch.int32, device=dev)
+    if added is None:
+        added = torch.empty((shape.B, P), dtype=torch.int64, device=dev)
+    if ws is None:
+        ws = _empty(augment_workspace_size(shape, P), dev)
+    _check("sparsp_augment", lib().sparsp_augment(
+        _sref(shape), int(P), _ptr(scores), _ptr(row_ptr), _ptr(col_idx), _ptr(head_rank), _ptr(row_ptr_out),
+        _ptr(col_idx_out), int(col_idx_out.numel()), _ptr(added), _ptr(ws), ws.numel(), _ptr(status),
+        _stream(stream)))
+    return row_ptr_out, col_idx_out, added
 
 
 # ----------------------------------------------------------------- step 5

@@ -297,6 +297,52 @@ sparsp_status_t sparsp_placement(const sparsp_shape_t* shape, int32_t P, const i
   return launch_placement(s, row_ptr, col_idx, P, owner, ws, d_status, (cudaStream_t)stream);
 }
 
+sparsp_status_t sparsp_balance_heads(const sparsp_shape_t* shape, int32_t P, int32_t max_migrations,
+                                     const int32_t* row_ptr, int32_t* head_rank, int64_t* loads,
+                                     int32_t* migrations, sparsp_stream_t stream) {
+  Dims s;
+  sparsp_status_t r = check_shape(shape, &s);
+  if (r != SPARSP_OK) return r;
+  if (s.H > kBalanceMaxHeads) return SPARSP_ERR_UNSUPPORTED;
+  if (P < 1 || P > s.H) return SPARSP_ERR_SHAPE;
+  if (max_migrations < 0) return SPARSP_ERR_INVALID_ARG;
+  CHECK_PTR(row_ptr);
+  CHECK_PTR(head_rank);
+  CHECK_PTR(loads);
+  CHECK_OPT_PTR(migrations);
+  return launch_balance(s, row_ptr, P, max_migrations, head_rank, loads, migrations, (cudaStream_t)stream);
+}
+
+size_t sparsp_augment_workspace_size(const sparsp_shape_t* shape, int32_t P) {
+  Dims s;
+  if (check_shape(shape, &s) != SPARSP_OK || P < 1) return 0;
+  return augment_ws(s, P);
+}
+
+sparsp_status_t sparsp_augment(const sparsp_shape_t* shape, int32_t P, const float* scores,
+                               const int32_t* row_ptr, const int32_t* col_idx, const int32_t* head_rank,
+                               int32_t* row_ptr_out, int32_t* col_idx_out, int64_t col_cap, int64_t* added,
+                               void* ws, size_t ws_bytes, int32_t* d_status, sparsp_stream_t stream) {
+  Dims s;
+  sparsp_status_t r = check_shape(shape, &s);
+  if (r != SPARSP_OK) return r;
+  if (s.H > kBalanceMaxHeads) return SPARSP_ERR_UNSUPPORTED;
+  if (P < 1 || P > s.H) return SPARSP_ERR_SHAPE;
+  if (col_cap < 0) return SPARSP_ERR_INVALID_ARG;
+  CHECK_PTR(scores);
+  CHECK_PTR(row_ptr);
+  CHECK_PTR(col_idx);
+  CHECK_PTR(head_rank);
+  CHECK_PTR(row_ptr_out);
+  CHECK_PTR(col_idx_out);
+  CHECK_OPT_PTR(added);
+  CHECK_PTR(ws);
+  CHECK_OPT_PTR(d_status);
+  if (ws_bytes < augment_ws(s, P)) return SPARSP_ERR_WORKSPACE;
+  return launch_augment(s, P, scores, row_ptr, col_idx, head_rank, row_ptr_out, col_idx_out, col_cap, added, ws,
+                        d_status, (cudaStream_t)stream);
+}
+
 size_t sparsp_lpt_workspace_size(const sparsp_shape_t* shape) {
   Dims s;
   if (check_shape(shape, &s) != SPARSP_OK) return 0;

@@ -82,6 +82,15 @@ size_t placement_ws(const Dims& s);
 sparsp_status_t launch_placement(const Dims& s, const int32_t* row_ptr, const int32_t* col_idx, int P,
                                  int32_t* owner, void* ws, int32_t* d_status, cudaStream_t st);
 
+sparsp_status_t launch_balance(const Dims& s, const int32_t* row_ptr, int P, int max_moves,
+                               int32_t* head_rank, int64_t* loads, int32_t* moves, cudaStream_t st);
+size_t augment_ws(const Dims& s, int P);
+sparsp_status_t launch_augment(const Dims& s, int P, const float* scores, const int32_t* row_ptr,
+                               const int32_t* col_idx, const int32_t* head_rank, int32_t* out_ptr,
+                               int32_t* out_idx, int64_t cap, int64_t* added, void* ws, int32_t* d_status,
+                               cudaStream_t st);
+constexpr int kBalanceMaxHeads = 2048;
+
 size_t lpt_ws(const Dims& s);
 sparsp_status_t launch_lpt(const Dims& s, const int32_t* row_ptr, bool flat, int32_t* items,
                            int32_t* counter, void* ws, cudaStream_t st);

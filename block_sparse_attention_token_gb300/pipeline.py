@@ -1,9 +1,10 @@
 """The whole hot path as one object with preallocated device buffers.
 
 forward(): reorder Q, K, V into tiles -> block scores -> Top-p/Top-k selection
--> (optional) dependency-aware placement of blocks on the P partitions -> KV
-demand of P partitions (+ gather) -> block-sparse attention -> O back to
-raster order. backward(): dO into tiles -> attention backward -> dQ, dK, dV
+-> (optional) head balancing over P virtual ranks and slack-aware augmentation
+of the CSR -> (optional) dependency-aware placement of blocks on the P
+partitions -> KV demand of P partitions (+ gather) -> block-sparse attention
+-> O back to raster order. backward(): dO into tiles -> attention backward -> dQ, dK, dV
 back to raster order. Every step is one or more libsparsp kernels on the
 current stream; nothing here allocates after construction.
 """
@@ -11,7 +12,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (EST_LOWRANK, EST_MEAN, PROF_SLOTS, Shape, attn_bwd, attn_fwd, attn_workspace_size,
+from . import (EST_LOWRANK, EST_MEAN, PROF_SLOTS, Shape, attn_bwd, attn_fwd, attn_workspace_size, augment,
+               augment_workspace_size, balance_heads, Balance,
                block_scores, block_scores_pooled, block_scores_workspace_size, kv_demand, lib, placement,
                placement_workspace_size, reorder, reorder_pool, select, select_workspace_size, DemandOut)
 
@@ -19,14 +21,16 @@ from . import (EST_LOWRANK, EST_MEAN, PROF_SLOTS, Shape, attn_bwd, attn_fwd, att
 class Pipeline:
     def kernels_per_forward(self) -> int:
         """Kernels forward() launches: reorder x3, pool + product, select x3 (count,
-        scan, fill), placement x2 (affinity, greedy) when enabled, demand x4
-        (bitmap, scan, list, gather), schedule (1, or 2 in flat order) +
-        attention, inverse reorder."""
+        scan, fill), balancing (1) and augmentation x4 (keys, rank select,
+        scan, fill) when enabled, placement x2 (affinity, greedy) when
+        enabled, demand x4 (bitmap, scan, list, gather), schedule (1, or 2 in
+        flat order) + attention, inverse reorder."""
         lpt = 2 if self.flags & 1 else 1
         gather = 1 if self.demand.kg is not None else 0
         scores = (2 if self.est == EST_LOWRANK else 1) if self.fused else 2
         place = 2 if self.owner is not None else 0
-        return 3 + scores + 3 + place + 3 + gather + lpt + 1 + 1
+        bal = (1 if self.migrations is not None else 0) + (4 if self.augment else 0)
+        return 3 + scores + 3 + bal + place + 3 + gather + lpt + 1 + 1
 
     def kernels_per_backward(self) -> int:
         """reorder dO, rowdot, CSR transpose, schedule, dQ, schedule, dK/dV, 3 inverse reorders."""
@@ -35,7 +39,12 @@ class Pipeline:
 
     def __init__(self, shape: Shape, estimator: str, top_p: float, k_floor: int, P: int, rank: int = 16,
                  gather: bool = True, flags: int = 0, backward: bool = False, device="cuda",
-                 fused_estimation: bool = True, placement: bool = False):
+                 fused_estimation: bool = True, placement: bool = False, migrations: int | None = None,
+                 augment: bool = False):
+        """migrations: balance heads over P virtual ranks with at most this many
+        migrations (None: no balancing). augment: fill each rank's slack with
+        extra blocks (on the balanced ranks, or the contiguous head split);
+        attention then runs on the augmented CSR."""
         self.shape, self.top_p, self.k_floor, self.P, self.rank, self.flags = shape, top_p, k_floor, P, rank, flags
         self.est = EST_LOWRANK if estimator == "lowrank" else EST_MEAN
         self.fused = fused_estimation
@@ -67,6 +76,21 @@ class Pipeline:
                                 torch.empty(parts + 1, dtype=torch.int32, device=dev),
                                 torch.empty(parts * s.nb, dtype=torch.int32, device=dev), kg, vg,
                                 torch.empty(4, dtype=torch.int64, device=dev))
+        self.migrations, self.augment = migrations, augment
+        self.balance = None
+        if migrations is not None or augment:
+            if migrations is None:
+                self.migrations = 0
+            self.balance = Balance(
+                torch.empty((s.B, s.H), dtype=torch.int32, device=dev),
+                torch.empty((s.B, 2, P), dtype=torch.int64, device=dev),
+                torch.empty(max(s.B, 4), dtype=torch.int32, device=dev))
+        if augment:
+            self.row_ptr_aug = torch.empty(s.rows + 1, dtype=torch.int32, device=dev)
+            self.col_idx_aug = torch.empty(s.rows * s.nb, dtype=torch.int32, device=dev)
+            self.added = torch.empty((s.B, P), dtype=torch.int64, device=dev)
+            self.ws_aug = torch.empty(max(augment_workspace_size(s, P), 16), dtype=torch.uint8, device=dev)
+        self.csr = (self.row_ptr, self.col_idx)
         self.owner = self.ws_place = None
         if placement:
             self.owner = torch.empty((s.B, s.nb), dtype=torch.int32, device=dev)
@@ -102,13 +126,21 @@ class Pipeline:
         mark("scores")
         select(s, self.scores, self.top_p, self.k_floor, self.row_ptr, self.col_idx, self.ws_sel, self.status)
         mark("select")
+        rp, ci = self.row_ptr, self.col_idx
+        if self.balance is not None:
+            balance_heads(s, self.P, self.row_ptr, self.migrations, out=self.balance)
+            mark("balance")
+        if self.augment:
+            rp, ci, _ = augment(s, self.P, self.scores, self.row_ptr, self.col_idx, self.balance.head_rank,
+                                self.row_ptr_aug, self.col_idx_aug, self.added, self.ws_aug, self.status)
+            mark("augment")
+        self.csr = (rp, ci)
         if self.owner is not None:
-            placement(s, self.P, self.row_ptr, self.col_idx, self.owner, self.ws_place, self.status)
+            placement(s, self.P, rp, ci, self.owner, self.ws_place, self.status)
             mark("placement")
-        kv_demand(s, self.P, self.row_ptr, self.col_idx, self.kb, self.vb, out=self.demand, status=self.status,
-                  owner=self.owner)
+        kv_demand(s, self.P, rp, ci, self.kb, self.vb, out=self.demand, status=self.status, owner=self.owner)
         mark("kv_demand")
-        attn_fwd(s, self.qb, self.kb, self.vb, self.row_ptr, self.col_idx, 0.0, self.ob, self.lse, self.ws_attn,
+        attn_fwd(s, self.qb, self.kb, self.vb, rp, ci, 0.0, self.ob, self.lse, self.ws_attn,
                  self.flags, self.prof if prof else None, self.status)
         mark("attn_fwd")
         o = self.o if out is None else out
@@ -121,7 +153,8 @@ class Pipeline:
         mark = mark or (lambda name: None)
         reorder(s, dout, self.dob)
         mark("reorder_dout")
-        attn_bwd(s, self.qb, self.kb, self.vb, self.ob, self.lse, self.dob, self.row_ptr, self.col_idx, 0.0,
+        rp, ci = self.csr
+        attn_bwd(s, self.qb, self.kb, self.vb, self.ob, self.lse, self.dob, rp, ci, 0.0,
                  self.dqb, self.dkb, self.dvb, self.ws_attn, self.flags, self.prof if prof else None, self.status)
         mark("attn_bwd")
         reorder(s, self.dqb, self.dq, inverse=True)

@@ -254,6 +254,53 @@ SPARSP_API sparsp_status_t sparsp_placement(const sparsp_shape_t* shape, int32_t
                                  int32_t* d_status, sparsp_stream_t stream);
 
 /*
+ * Virtual-rank load balancing ("mlsift.com tag listing", Top-p video
+ * sparse-attention entry, abstract: Runtime Load Balancing migrates a few heavy
+ * heads to shorten the critical path of sequence-parallel ranks), modelled on
+ * one GPU over P virtual ranks per batch element. The cost of head (b, h) is
+ * its number of selected block pairs (row_ptr[(bh+1)*nb] - row_ptr[bh*nb]).
+ * Start: the contiguous split, rank r holding heads [floor(r*H/P),
+ * floor((r+1)*H/P)). Then at most max_migrations times: c = most loaded rank,
+ * t = least loaded (ties: lower rank); among c's heads take the one whose move
+ * to t gives the smallest max(L_c - cost, L_t + cost) (ties: lower head); move
+ * it only if that is below L_c, else stop.
+ *   head_rank  int32 [B, H] (device): the rank of every head.
+ *   loads      int64 [B, 2, P] (device): rank loads before and after.
+ *   migrations int32 [B] (device) or NULL: moves made.
+ * Requires 1 <= P <= H <= 2048 (else SPARSP_ERR_SHAPE / SPARSP_ERR_UNSUPPORTED)
+ * and max_migrations >= 0.
+ */
+SPARSP_API sparsp_status_t sparsp_balance_heads(const sparsp_shape_t* shape, int32_t P, int32_t max_migrations,
+                                     const int32_t* row_ptr, int32_t* head_rank, int64_t* loads,
+                                     int32_t* migrations, sparsp_stream_t stream);
+
+/*
+ * Slack-Aware Sparse Augmentation (same entry: slack on non-critical ranks is
+ * filled with additional high-value blocks). With heads on ranks (head_rank
+ * [B, H], e.g. from sparsp_balance_heads) and rank loads L_r, the critical load
+ * is L* = max_r L_r. Rank r adds min(L* - L_r, #candidates) blocks: its heads'
+ * unselected blocks (h, i, j) of largest value v = fl32(e_j / Z), where
+ * e_j = exp(S_j - max_j S) in fp32 and Z = sum_j e_j in fp64 over the row of
+ * scores (the mass selection assigns the block), ties by row (b*H + h)*nb + i
+ * then j ascending. The critical load is unchanged.
+ *   scores       float32 [B, H, nb, nb]: the block scores selection ran on.
+ *   row_ptr/col_idx: the selection's CSR (ascending rows).
+ *   row_ptr_out  int32 [B*H*nb + 1], col_idx_out int32 [col_cap]: the augmented
+ *                CSR, ascending rows (col_cap >= B*H*nb*nb always suffices;
+ *                overflow sets SPARSP_ERR_CAPACITY).
+ *   added        int64 [B, P] (device) or NULL: blocks added per rank.
+ *   ws           at least sparsp_augment_workspace_size() bytes.
+ * A head_rank entry outside [0, P), a bad CSR row or a non-finite score row
+ * sets SPARSP_ERR_DATA; such rows are copied without additions. Requires
+ * 1 <= P <= H <= 2048.
+ */
+SPARSP_API size_t sparsp_augment_workspace_size(const sparsp_shape_t* shape, int32_t P);
+SPARSP_API sparsp_status_t sparsp_augment(const sparsp_shape_t* shape, int32_t P, const float* scores,
+                               const int32_t* row_ptr, const int32_t* col_idx, const int32_t* head_rank,
+                               int32_t* row_ptr_out, int32_t* col_idx_out, int64_t col_cap, int64_t* added,
+                               void* ws, size_t ws_bytes, int32_t* d_status, sparsp_stream_t stream);
+
+/*
  * Step 5c - longest-first work order for the attention kernels (the per-head
  * straggler problem of the "mlsift.com tag listing" entry; the lopsided
  * per-head work of "Dynamic Sparsity in Large-Scale Video DiT Training",

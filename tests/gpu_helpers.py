@@ -106,3 +106,46 @@ def jaccard_rows(rp_a, ci_a, rp_b, ci_b) -> float:
         u = len(a | b)
         tot += 1.0 if u == 0 else len(a & b) / u
     return tot / R
+
+
+def compare_augmented(rp, ci, ref: orc.Augmented, rp0, ci0, V, head_rank, B, H, nb, P, rel=1e-6) -> int:
+    """The GPU's augmented CSR against the oracle's. Per rank, the number of
+    added blocks is exact; every row keeps its selected blocks; every added
+    block is worth at least the oracle's cut and every candidate left out at
+    most the cut (both within `rel`, the float32 rounding of the values).
+    Where no candidate value lies strictly inside that band around a cut, the
+    whole CSR must equal the oracle's bit for bit. Returns the number of rows
+    that differ from the oracle."""
+    R = B * H * nb
+    assert rp.shape == (R + 1,)
+    diff_rows = 0
+    band_empty = True
+    for b in range(B):
+        for r in range(P):
+            cut = float(ref.cut[b, r])
+            n_add = 0
+            for h in range(H):
+                if int(head_rank[b, h]) != r:
+                    continue
+                for i in range(nb):
+                    row = (b * H + h) * nb + i
+                    old = set(int(j) for j in ci0[rp0[row]:rp0[row + 1]])
+                    new_list = [int(j) for j in ci[rp[row]:rp[row + 1]]]
+                    assert new_list == sorted(set(new_list)), f"row {row} not ascending/unique"
+                    new = set(new_list)
+                    assert old <= new, f"row {row} lost selected blocks"
+                    ref_new = set(int(j) for j in ref.col_idx[ref.row_ptr[row]:ref.row_ptr[row + 1]])
+                    diff_rows += new != ref_new
+                    for j in new - old:
+                        assert V[row, j] >= cut * (1 - rel), (row, j, V[row, j], cut)
+                    for j in range(nb):
+                        if j not in new:
+                            assert j in old or V[row, j] <= cut * (1 + rel) or ref.added[b, r] == 0, \
+                                (row, j, V[row, j], cut)
+                        if j not in old and V[row, j] != cut and abs(V[row, j] - cut) <= cut * rel:
+                            band_empty = False
+                    n_add += len(new - old)
+            assert n_add == int(ref.added[b, r]), (b, r, n_add, int(ref.added[b, r]))
+    if band_empty:
+        assert np.array_equal(rp, ref.row_ptr) and np.array_equal(ci[:rp[-1]], ref.col_idx)
+    return diff_rows

@@ -9,7 +9,7 @@ import torch
 import block_sparse_attention_token_gb300 as sp
 import synth
 from oracle import sparsp_oracle as orc
-from tests.gpu_helpers import OracleChain, compare_csr, compare_values, dev, host, i32, jaccard_rows, status_word
+from tests.gpu_helpers import OracleChain, compare_augmented, compare_csr, compare_values, dev, host, i32, jaccard_rows, status_word
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow, pytest.mark.timeout(1800)]
 
@@ -115,6 +115,32 @@ def test_placement_and_placed_demand_bitexact(run):
     contiguous = orc.kv_demand(ch.sel.row_ptr, ch.sel.col_idx, g.B, g.H, g.nb, wl.P, g.Bt, g.d, wl.elem_bytes)
     print(f"{wl.name}: remote demanded bytes contiguous {contiguous.bytes[2] / 1e9:.3f} GB, "
           f"placed {ref.bytes[2] / 1e9:.3f} GB ({100 * (1 - ref.bytes[2] / contiguous.bytes[2]):+.1f}% saved)")
+
+
+def test_balance_and_augment(run):
+    """Head migration bit for bit; slack-aware augmentation against the oracle
+    (added counts exact, chosen blocks valid, CSR exact where unambiguous)."""
+    wl, ch, g = run.wl, run.ch, run.ch.g
+    costs = orc.head_costs(ch.sel.row_ptr, g.B, g.H, g.nb)
+    hr, mv = orc.balance_heads(costs, wl.P, wl.P)
+    hr0, _ = orc.balance_heads(costs, wl.P, 0)
+    bal = sp.balance_heads(run.shape, wl.P, i32(ch.sel.row_ptr), wl.P)
+    st = status_word()
+    rp2, ci2, added = sp.augment(run.shape, wl.P, torch.from_numpy(ch.S32).cuda(), i32(ch.sel.row_ptr),
+                                 i32(ch.sel.col_idx), bal.head_rank, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert np.array_equal(host(bal.head_rank), hr)
+    assert host(bal.migrations)[:g.B].tolist() == mv.tolist()
+    ref = orc.augment(ch.S32.reshape(-1, g.nb), ch.sel.row_ptr, ch.sel.col_idx, g.B, g.H, g.nb, hr, wl.P)
+    assert host(added).tolist() == ref.added.tolist()
+    V = orc.block_values(ch.S32.reshape(-1, g.nb))
+    n = compare_augmented(host(rp2), host(ci2), ref, ch.sel.row_ptr, ch.sel.col_idx, V, hr, g.B, g.H, g.nb, wl.P)
+    before = orc.imbalance(orc.rank_loads(costs[0], hr0[0], wl.P))
+    after = orc.imbalance(orc.rank_loads(costs[0], hr[0], wl.P))
+    print(f"{wl.name}: rank imbalance {before:.3f} -> {after:.3f} after {int(mv[0])} migrations; "
+          f"blocks added {int(ref.added.sum())} ({100 * ref.added.sum() / ch.sel.row_ptr[-1]:.2f}% of nnz); "
+          f"rows differing from the oracle {n}")
 
 
 def _sample_rows(ch, n, seed):

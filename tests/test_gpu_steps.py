@@ -11,8 +11,8 @@ import torch
 import block_sparse_attention_token_gb300 as sp
 import synth
 from oracle import sparsp_oracle as orc
-from tests.gpu_helpers import (OracleChain, compare_csr, compare_values, dev, host, i32, jaccard_rows,
-                               status_word, workload)
+from tests.gpu_helpers import (OracleChain, compare_augmented, compare_csr, compare_values, dev, host, i32,
+                               jaccard_rows, status_word, workload)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.timeout(900)]
 
@@ -256,6 +256,126 @@ def test_placed_demand_rejects_bad_owner():
             assert idx[ptr[part]:ptr[part + 1]].tolist() == want
 
 
+def _csr_np(rows):
+    rp = np.concatenate([[0], np.cumsum([len(r) for r in rows])]).astype(np.int32)
+    return rp, np.array([j for r in rows for j in r], dtype=np.int32)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_balance_heads_bitexact(name):
+    wl, data, shape = _setup(name)
+    ch = OracleChain(wl, data)
+    g = ch.g
+    costs = orc.head_costs(ch.sel.row_ptr, g.B, g.H, g.nb)
+    for M in sorted({0, 1, wl.P, g.H * wl.P}):
+        hr, mv = orc.balance_heads(costs, wl.P, M)
+        out = sp.balance_heads(shape, wl.P, i32(ch.sel.row_ptr), M)
+        torch.cuda.synchronize()
+        assert np.array_equal(host(out.head_rank), hr), M
+        assert host(out.migrations)[:g.B].tolist() == mv.tolist()
+        hr0, _ = orc.balance_heads(costs, wl.P, 0)
+        loads = host(out.loads)
+        for b in range(g.B):
+            assert loads[b, 0].tolist() == orc.rank_loads(costs[b], hr0[b], wl.P).tolist()
+            assert loads[b, 1].tolist() == orc.rank_loads(costs[b], hr[b], wl.P).tolist()
+
+
+def test_balance_hand_example():
+    import json
+    gold = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "balance_hand.json")))
+    # 6 heads of 6 tiles (4x4x4 tokens); head h holds costs[h] pairs spread over its rows
+    shape = sp.make_shape(1, 6, 24, 4, 4, 64, 4, 4, 4, "bf16")
+    rows = []
+    for c in gold["costs"]:
+        for i in range(6):
+            n = min(6, max(0, c - 6 * i))
+            rows.append(list(range(n)))
+    rp, _ = _csr_np(rows)
+    out = sp.balance_heads(shape, gold["P"], i32(rp), 10)
+    one = sp.balance_heads(shape, gold["P"], i32(rp), 1)
+    torch.cuda.synchronize()
+    assert host(out.head_rank)[0].tolist() == gold["head_rank"]
+    assert int(host(out.migrations)[0]) == gold["migrations"]
+    assert host(out.loads)[0, 0].tolist() == gold["contiguous_loads"]
+    assert host(out.loads)[0, 1].tolist() == gold["loads"]
+    assert host(one.head_rank)[0].tolist() == gold["head_rank_one_move"]
+
+
+def test_augment_hand_example():
+    import json
+    gold = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "augment_hand.json")))
+    # 3 tiles of 4x4x4 tokens, 2 heads
+    shape = sp.make_shape(1, 2, 12, 4, 4, 64, 4, 4, 4, "bf16")
+    assert shape.nb == gold["nb"]
+    rp, ci = _csr_np(gold["rows"])
+    S = torch.tensor(gold["scores"], dtype=torch.float32).cuda()
+    st = status_word()
+    rp2, ci2, added = sp.augment(shape, gold["P"], S, i32(rp), i32(ci), i32([gold["head_rank"]]), status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    rp2, ci2 = host(rp2), host(ci2)
+    rows = [ci2[rp2[r]:rp2[r + 1]].tolist() for r in range(len(gold["rows"]))]
+    assert rows == gold["augmented_rows"]
+    assert host(added)[0].tolist() == gold["added"]
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_augment_matches_oracle(name):
+    wl, data, shape = _setup(name)
+    ch = OracleChain(wl, data)
+    g = ch.g
+    hr, _ = orc.balance_heads(orc.head_costs(ch.sel.row_ptr, g.B, g.H, g.nb), wl.P, wl.P)
+    ref = orc.augment(ch.S32.reshape(-1, g.nb), ch.sel.row_ptr, ch.sel.col_idx, g.B, g.H, g.nb, hr, wl.P)
+    st = status_word()
+    rp2, ci2, added = sp.augment(shape, wl.P, torch.from_numpy(ch.S32).cuda(), i32(ch.sel.row_ptr),
+                                 i32(ch.sel.col_idx), i32(hr), status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert host(added).tolist() == ref.added.tolist()
+    V = orc.block_values(ch.S32.reshape(-1, g.nb))
+    n = compare_augmented(host(rp2), host(ci2), ref, ch.sel.row_ptr, ch.sel.col_idx, V, hr, g.B, g.H, g.nb, wl.P)
+    print(f"{wl.name}: added {ref.added.tolist()}, rows differing from the oracle {n}")
+
+
+def test_augment_edges():
+    wl, data, shape = _setup("r64")
+    ch = OracleChain(wl, data)
+    g = ch.g
+    S = torch.from_numpy(ch.S32).cuda()
+    rp, ci = i32(ch.sel.row_ptr), i32(ch.sel.col_idx)
+    # one rank: it is the critical one, nothing is added
+    rp2, ci2, added = sp.augment(shape, 1, S, rp, ci, i32(np.zeros((g.B, g.H))))
+    torch.cuda.synchronize()
+    assert host(added).sum() == 0
+    assert np.array_equal(host(rp2), ch.sel.row_ptr)
+    assert np.array_equal(host(ci2)[:int(ch.sel.row_ptr[-1])], ch.sel.col_idx)
+    # one head per rank and an empty selection: every rank is filled up to the critical head
+    hr = np.arange(g.H, dtype=np.int32)[None, :].repeat(g.B, 0)
+    ref = orc.augment(ch.S32.reshape(-1, g.nb), ch.sel.row_ptr, ch.sel.col_idx, g.B, g.H, g.nb, hr, g.H)
+    rp2, ci2, added = sp.augment(shape, g.H, S, rp, ci, i32(hr))
+    torch.cuda.synchronize()
+    assert host(added).tolist() == ref.added.tolist()
+    V = orc.block_values(ch.S32.reshape(-1, g.nb))
+    compare_augmented(host(rp2), host(ci2), ref, ch.sel.row_ptr, ch.sel.col_idx, V, hr, g.B, g.H, g.nb, g.H)
+    # a head on no rank: reported, its rows are copied unchanged
+    bad = hr.copy()
+    bad[0, 1] = g.H
+    st = status_word()
+    rp2, ci2, _ = sp.augment(shape, g.H, S, rp, ci, i32(bad), status=st)
+    torch.cuda.synchronize()
+    assert st.item() == sp.DATA
+    rp2, ci2 = host(rp2), host(ci2)
+    for i in range(g.nb):
+        r = g.nb + i
+        assert ci2[rp2[r]:rp2[r + 1]].tolist() == ch.sel.col_idx[ch.sel.row_ptr[r]:ch.sel.row_ptr[r + 1]].tolist()
+    # a CSR capacity that is too small
+    st = status_word()
+    sp.augment(shape, g.H, S, rp, ci, i32(hr), col_idx_out=torch.empty(int(ch.sel.row_ptr[-1]), dtype=torch.int32,
+                                                                        device="cuda"), status=st)
+    torch.cuda.synchronize()
+    assert st.item() == sp.CAPACITY
+
+
 @pytest.mark.parametrize("name", list(SMALL))
 @pytest.mark.parametrize("flat", [False, True])
 def test_lpt_schedule_bitexact(name, flat):
@@ -423,6 +543,39 @@ def test_pipeline_with_placement(name):
     ref = orc.kv_demand(rp, ci, g.B, g.H, g.nb, wl.P, g.Bt, g.d, wl.elem_bytes, owner=own_ref)
     assert host(placed.demand.bytes).astype(np.uint64).tolist() == ref.bytes.tolist()
     assert placed.kernels_per_forward() == plain.kernels_per_forward() + 2
+
+
+@pytest.mark.parametrize("name", ["medium", "wave"])
+def test_pipeline_with_balance_and_augment(name):
+    """Balancing + augmentation inside the pipeline: attention runs on the
+    augmented CSR, whose outputs match the oracle's attention on that CSR, and
+    the backward uses the same CSR."""
+    wl, data, shape = _setup(name)
+    g = orc.grid_of(wl)
+    args = [dev(data[x], wl) for x in ("q", "k", "v")]
+    kw = {}
+    if wl.estimator == "lowrank":
+        kw = dict(wq=torch.from_numpy(data["wq"]).cuda(), wk=torch.from_numpy(data["wk"]).cuda())
+    pipe = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P, migrations=wl.P, augment=True,
+                       backward=True)
+    o, lse = pipe.forward(*args, **kw)
+    torch.cuda.synchronize()
+    assert pipe.status.item() == 0
+    rp, ci = (host(t) for t in pipe.csr)
+    rp0 = host(pipe.row_ptr)
+    costs = orc.head_costs(rp0, g.B, g.H, g.nb)
+    hr, _ = orc.balance_heads(costs, wl.P, wl.P)
+    assert np.array_equal(host(pipe.balance.head_rank), hr)
+    assert int(rp[-1]) == int(rp0[-1]) + int(host(pipe.added).sum())
+    assert pipe.kernels_per_forward() == sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor,
+                                                      wl.P).kernels_per_forward() + 5
+    qb, kb, vb = (orc.reorder(data[x], g) for x in ("q", "k", "v"))
+    O, _ = orc.attn_fwd(qb, kb, vb, rp, ci, g.Bt, 1.0 / math.sqrt(g.d))
+    compare_values(orc.reorder(host(o), g), O, wl, "O on the augmented CSR")
+    dout = torch.randn_like(args[0])
+    pipe.backward(dout)
+    torch.cuda.synchronize()
+    assert pipe.status.item() == 0
 
 
 def test_host_pipeline_overlapped_steps_match_device_pipeline():
