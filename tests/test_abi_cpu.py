@@ -129,6 +129,21 @@ def test_call_validation_codes(lib):
     assert lib.sparsp_placement(S, s.nb + 1, FAKE, FAKE, FAKE, FAKE, need, None, None) == sp.SHAPE
     assert lib.sparsp_placement(S, 2, FAKE, FAKE, None, FAKE, need, None, None) == sp.INVALID_ARG
     assert lib.sparsp_placement(S, 2, FAKE, FAKE, FAKE, FAKE, need - 1, None, None) == sp.WORKSPACE
+    # balancing: P out of range, negative migrations, too many heads
+    assert lib.sparsp_balance_heads(S, 0, 1, FAKE, FAKE, FAKE, None, None) == sp.SHAPE
+    assert lib.sparsp_balance_heads(S, s.H + 1, 1, FAKE, FAKE, FAKE, None, None) == sp.SHAPE
+    assert lib.sparsp_balance_heads(S, 1, -1, FAKE, FAKE, FAKE, None, None) == sp.INVALID_ARG
+    big = ctypes.byref(shape(H=4096))
+    assert lib.sparsp_balance_heads(big, 2, 1, FAKE, FAKE, FAKE, None, None) == sp.UNSUPPORTED
+    # augmentation: small workspace, negative capacity, missing head ranks
+    need = lib.sparsp_augment_workspace_size(S, 2)
+    assert need >= s.B * s.H * s.nb * s.nb * 4
+    assert lib.sparsp_augment(S, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, None, FAKE, need - 1, None,
+                              None) == sp.WORKSPACE
+    assert lib.sparsp_augment(S, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, -1, None, FAKE, need, None,
+                              None) == sp.INVALID_ARG
+    assert lib.sparsp_augment(S, 2, FAKE, FAKE, FAKE, None, FAKE, FAKE, 16, None, FAKE, need, None,
+                              None) == sp.INVALID_ARG
     # attention: NaN scale, small workspace, misaligned optional pointer, fp32 backward
     p7 = (FAKE,) * 5
     assert lib.sparsp_attn_fwd(S, *p7, f(float("nan")), FAKE, FAKE, FAKE, 1 << 30, 0, None, None,
