@@ -368,18 +368,20 @@ def main():
                       "placement_ms": p0.elapsed_time(p1) / 5, "in_step": bool(args.placement)}
 
     # virtual-rank balancing and slack-aware augmentation on this step's selection
-    bal = sp.balance_heads(shape, wl.P, pipe.row_ptr, wl.P)
-    bal0 = sp.balance_heads(shape, wl.P, pipe.row_ptr, 0)
-    ws_aug = torch.empty(max(sp.augment_workspace_size(shape, wl.P), 16), dtype=torch.uint8, device="cuda")
+    # (ranks hold whole heads, so there are at most H of them)
+    R = min(wl.P, shape.H)
+    bal = sp.balance_heads(shape, R, pipe.row_ptr, R)
+    bal0 = sp.balance_heads(shape, R, pipe.row_ptr, 0)
+    ws_aug = torch.empty(max(sp.augment_workspace_size(shape, R), 16), dtype=torch.uint8, device="cuda")
     rp_aug = torch.empty(shape.rows + 1, dtype=torch.int32, device="cuda")
     ci_aug = torch.empty(shape.rows * shape.nb, dtype=torch.int32, device="cuda")
-    added = torch.empty((shape.B, wl.P), dtype=torch.int64, device="cuda")
+    added = torch.empty((shape.B, R), dtype=torch.int64, device="cuda")
     a0 = torch.cuda.Event(enable_timing=True)
     a1 = torch.cuda.Event(enable_timing=True)
     a0.record(stream)
     for _ in range(5):
-        sp.balance_heads(shape, wl.P, pipe.row_ptr, wl.P, out=bal)
-        sp.augment(shape, wl.P, pipe.scores, pipe.row_ptr, pipe.col_idx, bal.head_rank, rp_aug, ci_aug, added,
+        sp.balance_heads(shape, R, pipe.row_ptr, R, out=bal)
+        sp.augment(shape, R, pipe.scores, pipe.row_ptr, pipe.col_idx, bal.head_rank, rp_aug, ci_aug, added,
                    ws_aug)
     a1.record(stream)
     torch.cuda.synchronize()
@@ -389,7 +391,7 @@ def main():
     def _imb(x):
         return float(x.max() * x.shape[-1] / x.sum()) if x.sum() else 1.0
 
-    balance_info = {"ranks": wl.P, "imbalance_contiguous": _imb(L0[0, 0]), "imbalance_balanced": _imb(L[0, 1]),
+    balance_info = {"ranks": R, "imbalance_contiguous": _imb(L0[0, 0]), "imbalance_balanced": _imb(L[0, 1]),
                     "migrations": int(bal.migrations[0].item()), "blocks_added": int(added.sum().item()),
                     "nnz_after_augment": int(rp_aug[-1].item()),
                     "balance_augment_ms": a0.elapsed_time(a1) / 5, "in_step": bool(args.augment)}
