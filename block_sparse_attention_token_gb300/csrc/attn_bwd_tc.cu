@@ -8,11 +8,14 @@
 //   mode 2 (dV): item = key block j, as mode 1.  S^T = K_j Q_c^T, dV += P^T dO_c.
 // with P = exp2(S * scale*log2e - LSE*log2e) from the forward's LSE (no online
 // maximum is needed), D = rowsum(dO * O), and dQ, dK scaled by `scale` at the
-// end. The three kernels recompute S (and dP) instead of sharing it so that
-// every one fits TMEM without aliasing: S [0,128), dP [128,256), the fp32
-// accumulator [256,384), and two bf16 operand buffers X0 [384,448),
-// X1 [448,512) holding P or dS for the accumulate MMA. Sums are taken in a
-// fixed order (no atomics), so results are bitwise reproducible.
+// end. Each column block is processed in two halves of 64 columns, double
+// buffered in TMEM so that the softmax warps work on one half while the
+// tensor pipe computes the next half's S and dP and the previous half's
+// accumulate: half buffer b holds S_b [128b, 128b+64) and dP_b
+// [128b+64, 128b+128); the fp32 accumulator is [256,384) and the bf16 operand
+// buffers X_b [384+32b, 416+32b) hold P or dS of a half. The three kernels
+// recompute S (and dP) instead of sharing it so that each fits TMEM. Sums are
+// taken in a fixed order (no atomics), so results are bitwise reproducible.
 //
 // One persistent CTA per SM, 7 warps (the forward kernel's structure):
 //   warp 4     producer: pulls items longest-first, validates the block list,
@@ -20,12 +23,15 @@
 //              the two column tiles (B1, B2; two 64-column boxes each, 128-byte
 //              swizzle) into a 2-stage ring; in modes 1 and 2 also the block's
 //              LSE*log2e and D (512 bytes each) by 1-D bulk copy.
-//   warp 5     S issuer: S = A1 B1^T and (modes 0, 1) dP = A2 B2^T, both
-//              operands K-major from shared memory.
-//   warp 6     accumulate issuer: ACC += X B3 with X from TMEM and B3 (the
-//              column tile K_c, Q_c or dO_c) MN-major from shared memory.
-//   warps 0-3  thread t owns row t (TMEM lane t): P and dS in fp32 from S, dP
-//              and the statistics, packed to bf16 into X; epilogue ACC -> global.
+//   warp 5     S issuer: per half, S = A1 B1_h^T and (modes 0, 1)
+//              dP = A2 B2_h^T (N = 64), both operands K-major from shared
+//              memory.
+//   warp 6     accumulate issuer: per half, ACC += X B3_h (K = 64) with X from
+//              TMEM and B3 (the column tile K_c, Q_c or dO_c) MN-major from
+//              shared memory.
+//   warps 0-3  thread t owns row t (TMEM lane t): loads a half's S and dP,
+//              frees the buffer, computes P and dS in fp32 from them and the
+//              statistics, packs them to bf16 into X; epilogue ACC -> global.
 // Every mbarrier wait is bounded (2 s): on expiry the CTA reports
 // SPARSP_ERR_TIMEOUT, all roles leave, in-flight copies and MMAs are drained
 // with a second bounded wait and TMEM is released.
@@ -42,12 +48,14 @@ constexpr uint32_t kTile = BT * D * 2;        // 32 KB
 constexpr uint32_t kHalfTile = BT * 64 * 2;   // one 64-column swizzled box
 constexpr uint32_t kStats = 1024;             // LSE*log2e [128] + D [128] of a column block
 constexpr int kThreads = 224;
-constexpr uint32_t kColS = 0, kColP = 128, kColAcc = 256, kColX = 384;
+constexpr uint32_t kColAcc = 256, kColX = 384;
+constexpr int HB = 64;   // columns of a half block
 constexpr uint32_t kOffA2 = kTile, kOffStage = 2 * kTile;
 constexpr uint32_t kStageBytes = 2 * kTile + kStats;   // a multiple of 1024: tiles stay aligned
 constexpr uint32_t kOffBar = kOffStage + kNS * kStageBytes;
 enum Bar {
-  A_FULL = 0, A_EMPTY, C_FULL, C_EMPTY = C_FULL + kNS, SD_FULL = C_EMPTY + kNS, SD_FREE, X_FULL,
+  A_FULL = 0, A_EMPTY, C_FULL, C_EMPTY = C_FULL + kNS, SD_FULL = C_EMPTY + kNS, SD_FREE = SD_FULL + 2,
+  X_FULL = SD_FREE + 2,
   X_DONE = X_FULL + 2, ACC_FULL = X_DONE + 2, ACC_EMPTY, I_FULL, I_EMPTY = I_FULL + kNI,
   TEAR = I_EMPTY + kNI, TEAR2, NBAR
 };
@@ -118,9 +126,9 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
       mbar_init(bar(C_FULL + s), 1);
       mbar_init(bar(C_EMPTY + s), 1);
     }
-    mbar_init(bar(SD_FULL), 1);
-    mbar_init(bar(SD_FREE), 128);
     for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(SD_FULL + b), 1);
+      mbar_init(bar(SD_FREE + b), 128);
       mbar_init(bar(X_FULL + b), 128);
       mbar_init(bar(X_DONE + b), 1);
     }
@@ -233,8 +241,8 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ S (and dP) issuer
-    constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
-    uint32_t it_use = 0, a_use = 0, c_use = 0, sd_issue = 0;
+    constexpr uint32_t idS = idesc_bf16(128, HB, 0, 0);
+    uint32_t it_use = 0, a_use = 0, c_use = 0, hg = 0;
     bool issued_any = false;
     for (;;) {
       const int ri = (int)(it_use % kNI);
@@ -249,34 +257,39 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
       if (!wait_warp(bar(A_FULL), a_use & 1u, g)) break;
       ++a_use;
       bool ok = true;
-      for (int e = 0; e < len; ++e) {
+      for (int e = 0; e < len && ok; ++e) {
         const uint32_t st = c_use % kNS;
-        if (!(ok = wait_warp(bar(SD_FREE), (sd_issue & 1u) ^ 1u, g))) break;
         if (!(ok = wait_warp(bar(C_FULL + st), (c_use / kNS) & 1u, g))) break;
-        fence_after();
         const uint32_t sb = stage(st);
-        if (elect_one()) {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
-            mma_ss(tmem + kColS, smem_desc(sA1 + off, 16, 1024, kSwizzle128B),
-                   smem_desc(sb + off, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
-          }
-          if (kHasDP) {
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t b = hg & 1u;
+          if (!(ok = wait_warp(bar(SD_FREE + b), ((hg >> 1) & 1u) ^ 1u, g))) break;
+          fence_after();
+          // rows [64h, 64h+64) of the column tile: 64 rows x 128 B = 8 KB into each box
+          const uint32_t rows_h = (uint32_t)h * (HB * 128u);
+          if (elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
-              mma_ss(tmem + kColP, smem_desc(sA2 + off, 16, 1024, kSwizzle128B),
-                     smem_desc(sb + kTile + off, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
+              mma_ss(tmem + 128u * b, smem_desc(sA1 + off, 16, 1024, kSwizzle128B),
+                     smem_desc(sb + rows_h + off, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
             }
+            if (kHasDP) {
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
+                mma_ss(tmem + 128u * b + HB, smem_desc(sA2 + off, 16, 1024, kSwizzle128B),
+                       smem_desc(sb + kTile + rows_h + off, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
+              }
+            }
+            commit(bar(SD_FULL + b));
+            if (e + 1 == len && h == 1) commit(bar(A_EMPTY));   // every MMA reading A1/A2 is issued
           }
-          commit(bar(SD_FULL));
-          if (e + 1 == len) commit(bar(A_EMPTY));   // every MMA reading A1/A2 is issued
+          __syncwarp();
+          ++hg;
+          issued_any = true;
         }
-        __syncwarp();
-        ++sd_issue;
         ++c_use;
-        issued_any = true;
       }
       if (!ok) break;
     }
@@ -291,7 +304,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
     constexpr uint32_t idAcc = idesc_bf16(128, 128, 0, 1);
     // the column tile the accumulator multiplies: K_c / Q_c (B1) or dO_c (B2)
     constexpr uint32_t kB3 = MODE == 2 ? kTile : 0u;
-    uint32_t it_use = 0, c_use = 0, xg = 0, acc_items = 0;
+    uint32_t it_use = 0, c_use = 0, hg = 0, acc_items = 0;
     bool issued_any = false;
     for (;;) {
       const int ri = (int)(it_use % kNI);
@@ -304,26 +317,30 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
       if (ent.y <= 0) continue;
       const int len = ent.y;
       bool ok = true;
-      for (int e = 0; e < len; ++e) {
-        const uint32_t b = xg & 1u, st = c_use % kNS;
-        if (!(ok = wait_warp(bar(X_FULL + b), (xg >> 1) & 1u, g))) break;
-        if (e == 0 && !(ok = wait_warp(bar(ACC_EMPTY), (acc_items & 1u) ^ 1u, g))) break;
-        fence_after();
+      for (int e = 0; e < len && ok; ++e) {
+        const uint32_t st = c_use % kNS;
         const uint32_t b3 = stage(st) + kB3;
-        if (elect_one()) {
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t b = hg & 1u;
+          if (!(ok = wait_warp(bar(X_FULL + b), (hg >> 1) & 1u, g))) break;
+          if (e == 0 && h == 0 && !(ok = wait_warp(bar(ACC_EMPTY), (acc_items & 1u) ^ 1u, g))) break;
+          fence_after();
+          if (elect_one()) {
+            // K = the half's 64 rows of the column tile: k-steps 4h .. 4h+3 of 16 rows (2 KB each)
 #pragma unroll
-          for (int kk = 0; kk < BT / 16; ++kk)
-            mma_ts(tmem + kColAcc, tmem + kColX + b * 64u + (uint32_t)kk * 8u,
-                   smem_desc(b3 + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), idAcc,
-                   (e > 0 || kk > 0) ? 1u : 0u);
-          commit(bar(X_DONE + b));
-          commit(bar(C_EMPTY + st));   // last reader of this stage
-          if (e + 1 == len) commit(bar(ACC_FULL));
+            for (int kk = 0; kk < HB / 16; ++kk)
+              mma_ts(tmem + kColAcc, tmem + kColX + b * 32u + (uint32_t)kk * 8u,
+                     smem_desc(b3 + (uint32_t)(4 * h + kk) * 2048u, 16384, 1024, kSwizzle128B), idAcc,
+                     (e > 0 || h > 0 || kk > 0) ? 1u : 0u);
+            commit(bar(X_DONE + b));
+            if (h == 1) commit(bar(C_EMPTY + st));   // last reader of this stage
+            if (e + 1 == len && h == 1) commit(bar(ACC_FULL));
+          }
+          __syncwarp();
+          ++hg;
+          issued_any = true;
         }
-        __syncwarp();
-        ++xg;
         ++c_use;
-        issued_any = true;
       }
       if (!ok) break;
       ++acc_items;
@@ -338,7 +355,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
     // ------------------------------------------------------------ P / dS and epilogue
     const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
     const float sl2 = p.sl2;
-    uint32_t it_use = 0, c_use = 0, sd_use = 0, xg = 0, acc_items = 0;
+    uint32_t it_use = 0, c_use = 0, hg = 0, acc_items = 0;
     for (;;) {
       const int ri = (int)(it_use % kNI);
       if (!wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
@@ -363,27 +380,33 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
       const float own_l2 = MODE == 0 ? p.lse2[row] : 0.f;
       const float own_d = MODE == 0 ? p.delta[row] : 0.f;
       bool ok = true;
-      for (int e = 0; e < len; ++e) {
-        const uint32_t b = xg & 1u, st = c_use % kNS;
-        if (!(ok = wait_warp(bar(SD_FULL), sd_use & 1u, g))) break;
-        fence_after();
+      for (int e = 0; e < len && ok; ++e) {
+        const uint32_t st = c_use % kNS;
         const float4* stats = reinterpret_cast<const float4*>(gbase + kOffStage + st * kStageBytes + 2 * kTile);
-        uint32_t xk[64];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t sv[32], dv[32];
-          tmem_ld32(t_row + kColS + 32u * c, sv);
-          if (kHasDP) tmem_ld32(t_row + kColP + 32u * c, dv);
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t b = hg & 1u;
+          if (!(ok = wait_warp(bar(SD_FULL + b), (hg >> 1) & 1u, g))) break;
+          fence_after();
+          uint32_t sv[HB], dv[HB];
+          tmem_ld32(t_row + 128u * b, sv);
+          tmem_ld32(t_row + 128u * b + 32u, sv + 32);
+          if (kHasDP) {
+            tmem_ld32(t_row + 128u * b + HB, dv);
+            tmem_ld32(t_row + 128u * b + HB + 32u, dv + 32);
+          }
           wait_ld();
+          fence_before();
+          mbar_arrive(bar(SD_FREE + b));   // the buffer can take the next half's S and dP
+          uint32_t xk[HB / 2];
 #pragma unroll
-          for (int x4 = 0; x4 < 8; ++x4) {
+          for (int x4 = 0; x4 < HB / 4; ++x4) {
             float l2[4], dd[4];
             if (MODE == 0) {
 #pragma unroll
               for (int u = 0; u < 4; ++u) { l2[u] = own_l2; dd[u] = own_d; }
             } else {
-              const float4 L = stats[c * 8 + x4];          // LSE*log2e of columns 32c+4x4 .. +3
-              const float4 Dv = stats[32 + c * 8 + x4];    // D of the same columns
+              const float4 L = stats[16 * h + x4];          // LSE*log2e of columns 64h+4x4 .. +3
+              const float4 Dv = stats[32 + 16 * h + x4];    // D of the same columns
               l2[0] = L.x; l2[1] = L.y; l2[2] = L.z; l2[3] = L.w;
               dd[0] = Dv.x; dd[1] = Dv.y; dd[2] = Dv.z; dd[3] = Dv.w;
             }
@@ -394,24 +417,20 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
               const float pr = ex2f(fmaf(__uint_as_float(sv[x]), sl2, -l2[u]));
               v[u] = kHasDP ? pr * (__uint_as_float(dv[x]) - dd[u]) : pr;
             }
-            xk[16 * c + 2 * x4] = pack2(v[0], v[1]);
-            xk[16 * c + 2 * x4 + 1] = pack2(v[2], v[3]);
+            xk[2 * x4] = pack2(v[0], v[1]);
+            xk[2 * x4 + 1] = pack2(v[2], v[3]);
           }
+          // X buffer b was last read by the accumulate MMA of half hg - 2
+          if (hg >= 2) {
+            if (!(ok = wait_warp(bar(X_DONE + b), ((hg - 2) >> 1) & 1u, g))) break;
+            fence_after();
+          }
+          tmem_st32(t_row + kColX + b * 32u, xk);
+          wait_st();
+          fence_before();
+          mbar_arrive(bar(X_FULL + b));
+          ++hg;
         }
-        fence_before();
-        mbar_arrive(bar(SD_FREE));
-        ++sd_use;
-        // X buffer b was last read by the accumulate MMA of block xg - 2
-        if (xg >= 2) {
-          if (!(ok = wait_warp(bar(X_DONE + b), ((xg - 2) >> 1) & 1u, g))) break;
-          fence_after();
-        }
-        tmem_st32(t_row + kColX + b * 64u, xk);
-        tmem_st32(t_row + kColX + b * 64u + 32u, xk + 32);
-        wait_st();
-        fence_before();
-        mbar_arrive(bar(X_FULL + b));
-        ++xg;
         ++c_use;
       }
       if (!ok) break;
