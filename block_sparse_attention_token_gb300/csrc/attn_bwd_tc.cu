@@ -12,26 +12,36 @@
 // buffered in TMEM so that the softmax warps work on one half while the
 // tensor pipe computes the next half's S and dP and the previous half's
 // accumulate: half buffer b holds S_b [128b, 128b+64) and dP_b
-// [128b+64, 128b+128); the fp32 accumulator is [256,384) and the bf16 operand
-// buffers X_b [384+32b, 416+32b) hold P or dS of a half. The three kernels
-// recompute S (and dP) instead of sharing it so that each fits TMEM. Sums are
-// taken in a fixed order (no atomics), so results are bitwise reproducible.
+// [128b+64, 128b+128), and the half's bf16 operand X (P or dS) is written over
+// the first 32 columns of S_b; the fp32 accumulator is [256,384); the item's
+// row tiles A1 [384,448) and A2 [448,512) sit in TMEM as packed bf16, so every
+// MMA takes A from TMEM and only B from shared memory (a 128x64x16 MMA with
+// both operands in shared memory is bound by shared-memory bandwidth at 62% of
+// the tensor rate; with A in TMEM it runs at the full rate). A half buffer is
+// free again once the accumulate MMA that read its X has completed. The three
+// kernels recompute S (and dP) instead of sharing it so that each fits TMEM.
+// Sums are taken in a fixed order (no atomics), so results are bitwise
+// reproducible.
 //
 // One persistent CTA per SM, 7 warps (the forward kernel's structure):
 //   warp 4     producer: pulls items longest-first, validates the block list,
-//              TMA-loads the item's two row tiles (A1, A2) once and, per block,
+//              TMA-loads the item's two row tiles (A1, A2) once (the softmax
+//              warps copy them into TMEM) and, per block,
 //              the two column tiles (B1, B2; two 64-column boxes each, 128-byte
 //              swizzle) into a 2-stage ring; in modes 1 and 2 also the block's
 //              LSE*log2e and D (512 bytes each) by 1-D bulk copy.
 //   warp 5     S issuer: per half, S = A1 B1_h^T and (modes 0, 1)
-//              dP = A2 B2_h^T (N = 64), both operands K-major from shared
+//              dP = A2 B2_h^T (N = 64), A from TMEM, B K-major from shared
 //              memory.
 //   warp 6     accumulate issuer: per half, ACC += X B3_h (K = 64) with X from
 //              TMEM and B3 (the column tile K_c, Q_c or dO_c) MN-major from
 //              shared memory.
-//   warps 0-3  thread t owns row t (TMEM lane t): loads a half's S and dP,
-//              frees the buffer, computes P and dS in fp32 from them and the
-//              statistics, packs them to bf16 into X; epilogue ACC -> global.
+//   warps 0-3  thread t owns row t (TMEM lane t): copies its rows of A1, A2
+//              into TMEM at the start of an item; per half loads S and dP,
+//              computes P and dS in fp32 from them and the statistics, packs
+//              the operand to bf16 into X; epilogue ACC -> global, deferred
+//              until the next item's row tiles are in TMEM so that its first
+//              MMAs overlap the epilogue.
 // Every mbarrier wait is bounded (2 s): on expiry the CTA reports
 // SPARSP_ERR_TIMEOUT, all roles leave, in-flight copies and MMAs are drained
 // with a second bounded wait and TMEM is released.
@@ -48,14 +58,14 @@ constexpr uint32_t kTile = BT * D * 2;        // 32 KB
 constexpr uint32_t kHalfTile = BT * 64 * 2;   // one 64-column swizzled box
 constexpr uint32_t kStats = 1024;             // LSE*log2e [128] + D [128] of a column block
 constexpr int kThreads = 224;
-constexpr uint32_t kColAcc = 256, kColX = 384;
+constexpr uint32_t kColAcc = 256, kColA1 = 384, kColA2 = 448;
 constexpr int HB = 64;   // columns of a half block
 constexpr uint32_t kOffA2 = kTile, kOffStage = 2 * kTile;
 constexpr uint32_t kStageBytes = 2 * kTile + kStats;   // a multiple of 1024: tiles stay aligned
 constexpr uint32_t kOffBar = kOffStage + kNS * kStageBytes;
 enum Bar {
-  A_FULL = 0, A_EMPTY, C_FULL, C_EMPTY = C_FULL + kNS, SD_FULL = C_EMPTY + kNS, SD_FREE = SD_FULL + 2,
-  X_FULL = SD_FREE + 2,
+  A_FULL = 0, A_EMPTY, AT_FULL, C_FULL, C_EMPTY = C_FULL + kNS, SD_FULL = C_EMPTY + kNS,
+  X_FULL = SD_FULL + 2,
   X_DONE = X_FULL + 2, ACC_FULL = X_DONE + 2, ACC_EMPTY, I_FULL, I_EMPTY = I_FULL + kNI,
   TEAR = I_EMPTY + kNI, TEAR2, NBAR
 };
@@ -121,14 +131,14 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
 
   if (threadIdx.x == 0) {
     mbar_init(bar(A_FULL), 1);
-    mbar_init(bar(A_EMPTY), 1);
+    mbar_init(bar(A_EMPTY), 128);
+    mbar_init(bar(AT_FULL), 128);
     for (int s = 0; s < kNS; ++s) {
       mbar_init(bar(C_FULL + s), 1);
       mbar_init(bar(C_EMPTY + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(SD_FULL + b), 1);
-      mbar_init(bar(SD_FREE + b), 128);
       mbar_init(bar(X_FULL + b), 128);
       mbar_init(bar(X_DONE + b), 1);
     }
@@ -254,7 +264,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
       if (ent.y == -2) break;
       if (ent.y <= 0) continue;
       const int len = ent.y;
-      if (!wait_warp(bar(A_FULL), a_use & 1u, g)) break;
+      if (!wait_warp(bar(AT_FULL), a_use & 1u, g)) break;   // the item's row tiles are in TMEM
       ++a_use;
       bool ok = true;
       for (int e = 0; e < len && ok; ++e) {
@@ -263,7 +273,8 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
         const uint32_t sb = stage(st);
         for (int h = 0; h < 2; ++h) {
           const uint32_t b = hg & 1u;
-          if (!(ok = wait_warp(bar(SD_FREE + b), ((hg >> 1) & 1u) ^ 1u, g))) break;
+          // buffer b holds X of half hg - 2 until that half's accumulate MMA has completed
+          if (!(ok = wait_warp(bar(X_DONE + b), ((hg >> 1) & 1u) ^ 1u, g))) break;
           fence_after();
           // rows [64h, 64h+64) of the column tile: 64 rows x 128 B = 8 KB into each box
           const uint32_t rows_h = (uint32_t)h * (HB * 128u);
@@ -271,19 +282,18 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
-              mma_ss(tmem + 128u * b, smem_desc(sA1 + off, 16, 1024, kSwizzle128B),
+              mma_ts(tmem + 128u * b, tmem + kColA1 + (uint32_t)kk * 8u,
                      smem_desc(sb + rows_h + off, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
             }
             if (kHasDP) {
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
-                mma_ss(tmem + 128u * b + HB, smem_desc(sA2 + off, 16, 1024, kSwizzle128B),
+                mma_ts(tmem + 128u * b + HB, tmem + kColA2 + (uint32_t)kk * 8u,
                        smem_desc(sb + kTile + rows_h + off, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
               }
             }
             commit(bar(SD_FULL + b));
-            if (e + 1 == len && h == 1) commit(bar(A_EMPTY));   // every MMA reading A1/A2 is issued
           }
           __syncwarp();
           ++hg;
@@ -329,7 +339,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
             // K = the half's 64 rows of the column tile: k-steps 4h .. 4h+3 of 16 rows (2 KB each)
 #pragma unroll
             for (int kk = 0; kk < HB / 16; ++kk)
-              mma_ts(tmem + kColAcc, tmem + kColX + b * 32u + (uint32_t)kk * 8u,
+              mma_ts(tmem + kColAcc, tmem + 128u * b + (uint32_t)kk * 8u,
                      smem_desc(b3 + (uint32_t)(4 * h + kk) * 2048u, 16384, 1024, kSwizzle128B), idAcc,
                      (e > 0 || h > 0 || kk > 0) ? 1u : 0u);
             commit(bar(X_DONE + b));
@@ -355,10 +365,52 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
     // ------------------------------------------------------------ P / dS and epilogue
     const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
     const float sl2 = p.sl2;
-    uint32_t it_use = 0, c_use = 0, hg = 0, acc_items = 0;
+    uint32_t it_use = 0, c_use = 0, hg = 0, acc_items = 0, a_use = 0;
+    uint4* pending = nullptr;   // output row of the previous item, written once its accumulator is full
+    bool ok = true;
+    // accumulator -> bf16 output row; frees the accumulator for the next item
+    auto epilogue = [&](uint4* orow) -> bool {
+      if (!wait_warp(bar(ACC_FULL), acc_items & 1u, g)) return false;
+      ++acc_items;
+      fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(t_row + kColAcc + c * 32u, o);
+        wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x)
+          w[x] = pack2(__uint_as_float(o[2 * x]) * p.out_scale, __uint_as_float(o[2 * x + 1]) * p.out_scale);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) orow[c * 4 + x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+      }
+      fence_before();
+      mbar_arrive(bar(ACC_EMPTY));
+      return true;
+    };
+    // this thread's row of a 128x128 row tile (two 64-column boxes, 128-byte
+    // swizzle: 16-byte chunk c of row t sits at chunk c ^ (t & 7)) -> 64 TMEM columns
+    auto row_to_tmem = [&](uint32_t tile_off, uint32_t col) {
+      const int t = threadIdx.x;
+      uint32_t w[64];
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(gbase + tile_off + (uint32_t)h * kHalfTile +
+                                                          (uint32_t)t * 128u + (uint32_t)((c ^ (t & 7)) * 16));
+          w[32 * h + 4 * c] = v.x;
+          w[32 * h + 4 * c + 1] = v.y;
+          w[32 * h + 4 * c + 2] = v.z;
+          w[32 * h + 4 * c + 3] = v.w;
+        }
+      tmem_st32(t_row + col, w);
+      tmem_st32(t_row + col + 32u, w + 32);
+    };
     for (;;) {
       const int ri = (int)(it_use % kNI);
-      if (!wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
+      if (!(ok = wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g))) break;
       const int2 ent = make_int2(ring[ri].x, ring[ri].y);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
@@ -376,10 +428,25 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
         for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
         continue;
       }
+      // the item's row tiles -> TMEM; the A region is free because every S/dP
+      // MMA of the previous item has completed (this thread consumed their SD_FULL)
+      if (!(ok = wait_warp(bar(A_FULL), a_use & 1u, g))) break;
+      ++a_use;
+      fence_after();
+      row_to_tmem(0u, kColA1);
+      if (kHasDP) row_to_tmem(kOffA2, kColA2);
+      wait_st();
+      fence_before();
+      mbar_arrive(bar(A_EMPTY));   // the shared-memory tiles can take the next item's
+      mbar_arrive(bar(AT_FULL));   // the S issuer may start this item
+      // the previous item's output, while this item's first S and dP run
+      if (pending != nullptr) {
+        if (!(ok = epilogue(pending))) break;
+        pending = nullptr;
+      }
       // mode 0: this thread's query row has one LSE and one D
       const float own_l2 = MODE == 0 ? p.lse2[row] : 0.f;
       const float own_d = MODE == 0 ? p.delta[row] : 0.f;
-      bool ok = true;
       for (int e = 0; e < len && ok; ++e) {
         const uint32_t st = c_use % kNS;
         const float4* stats = reinterpret_cast<const float4*>(gbase + kOffStage + st * kStageBytes + 2 * kTile);
@@ -395,8 +462,6 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
             tmem_ld32(t_row + 128u * b + HB + 32u, dv + 32);
           }
           wait_ld();
-          fence_before();
-          mbar_arrive(bar(SD_FREE + b));   // the buffer can take the next half's S and dP
           uint32_t xk[HB / 2];
 #pragma unroll
           for (int x4 = 0; x4 < HB / 4; ++x4) {
@@ -420,12 +485,8 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
             xk[2 * x4] = pack2(v[0], v[1]);
             xk[2 * x4 + 1] = pack2(v[2], v[3]);
           }
-          // X buffer b was last read by the accumulate MMA of half hg - 2
-          if (hg >= 2) {
-            if (!(ok = wait_warp(bar(X_DONE + b), ((hg - 2) >> 1) & 1u, g))) break;
-            fence_after();
-          }
-          tmem_st32(t_row + kColX + b * 32u, xk);
+          // X over the first 32 columns of this half's S (already in registers)
+          tmem_st32(t_row + 128u * b, xk);
           wait_st();
           fence_before();
           mbar_arrive(bar(X_FULL + b));
@@ -434,24 +495,9 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
         ++c_use;
       }
       if (!ok) break;
-      if (!wait_warp(bar(ACC_FULL), acc_items & 1u, g)) break;
-      ++acc_items;
-      fence_after();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o[32];
-        tmem_ld32(t_row + kColAcc + c * 32u, o);
-        wait_ld();
-        uint32_t w[16];
-#pragma unroll
-        for (int x = 0; x < 16; ++x)
-          w[x] = pack2(__uint_as_float(o[2 * x]) * p.out_scale, __uint_as_float(o[2 * x + 1]) * p.out_scale);
-#pragma unroll
-        for (int x = 0; x < 4; ++x) orow[c * 4 + x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
-      }
-      fence_before();
-      mbar_arrive(bar(ACC_EMPTY));
+      pending = orow;
     }
+    if (ok && pending != nullptr) epilogue(pending);
   }
 
   fence_before();
