@@ -25,6 +25,8 @@ Plain NumPy, float64 accumulation, written step by step from the pages:
 * Dependency-aware placement of blocks on the P partitions: SparSP, abstract.
 * Virtual-rank load balancing (head migration) and slack-aware sparse
   augmentation: the mlsift.com entry, abstract.
+* Predictor fitting: "How DSV works / The idea" (the loss is read as the mean
+  squared error of the predicted block scores; the pages do not define it).
 
 Parity pins for every function live in tests/test_oracle_*.py. Every
 function here has at least one pin that does not re-run its own formula.
@@ -729,3 +731,50 @@ def augment(S, row_ptr, col_idx, B, H, nb, head_rank, P) -> Augmented:
     new_ptr[1:] = np.cumsum(counts)
     new_idx = np.array([j for x in rows for j in sorted(x)], dtype=np.int32)
     return Augmented(new_ptr.astype(np.int32), new_idx, added, loads_out, cut, nxt)
+
+
+# ---------------------------------------------------------------------------
+# Predictor fitting
+# ---------------------------------------------------------------------------
+
+def predictor_loss_grad(qm, km, wq, wk):
+    """Loss and gradients for fitting the per-head low-rank predictor
+    ("Dynamic Sparsity in Large-Scale Video DiT Training", "How DSV works / The
+    idea": two small per-head matrices whose product approximates the real
+    query-key scores, trained beside the main graph with a magnitude-preserving
+    loss that the pages do not define).
+
+    Read as the mean squared error between the predictor's block scores and the
+    real block scores of the same pooled means, per head over the batch and all
+    block pairs (the squared error keeps the scores' magnitudes, not only their
+    order):
+        E[b,h,i,j] = (qm[b,h,i] Wq[h]) . (km[b,h,j] Wk[h]) - qm[b,h,i] . km[b,h,j]
+        L[h] = sum_{b,i,j} E^2 / (B nb^2)
+    qm, km: [B, H, nb, d]; wq, wk: [H, d, r]. Returns (L [H], dL/dWq [H, d, r],
+    dL/dWk [H, d, r]) in float64. The gradients are the chain rule of L:
+        dL/dWq[h] = 2/(B nb^2) sum_b qm[b,h]^T (E[b,h] (km[b,h] Wk[h]))
+        dL/dWk[h] = 2/(B nb^2) sum_b km[b,h]^T (E[b,h]^T (qm[b,h] Wq[h]))
+    """
+    qm = np.asarray(qm, dtype=np.float64)
+    km = np.asarray(km, dtype=np.float64)
+    wq = np.asarray(wq, dtype=np.float64)
+    wk = np.asarray(wk, dtype=np.float64)
+    B, H, nb, d = qm.shape
+    A = np.einsum("bhid,hdr->bhir", qm, wq)
+    Bk = np.einsum("bhjd,hdr->bhjr", km, wk)
+    E = np.einsum("bhir,bhjr->bhij", A, Bk) - np.einsum("bhid,bhjd->bhij", qm, km)
+    n = B * nb * nb
+    loss = (E ** 2).sum(axis=(0, 2, 3)) / n
+    GA = np.einsum("bhij,bhjr->bhir", E, Bk)
+    GB = np.einsum("bhij,bhir->bhjr", E, A)
+    gwq = 2.0 / n * np.einsum("bhid,bhir->hdr", qm, GA)
+    gwk = 2.0 / n * np.einsum("bhjd,bhjr->hdr", km, GB)
+    return loss, gwq, gwk
+
+
+def predictor_step(qm, km, wq, wk, lr):
+    """One plain gradient step on predictor_loss_grad's loss (the predictor is
+    updated as the forward pass runs): W <- W - lr dL/dW for both matrices,
+    with the gradients taken at the current weights. Returns (wq', wk', L)."""
+    loss, gwq, gwk = predictor_loss_grad(qm, km, wq, wk)
+    return np.asarray(wq, np.float64) - lr * gwq, np.asarray(wk, np.float64) - lr * gwk, loss

@@ -531,3 +531,63 @@ def test_augment_without_slack_changes_nothing():
     aug = orc.augment(S, rp, ci, 1, 2, 2, np.array([[0, 1]]), 2)
     assert aug.added.sum() == 0
     assert aug.row_ptr.tolist() == rp.tolist() and aug.col_idx.tolist() == ci.tolist()
+
+
+# --------------------------------------------------------- predictor fitting
+
+def test_predictor_hand_example():
+    gold = _load("predictor_hand.json")
+    qm = np.full((1, 1, 1, 1), gold["qm"])
+    km = np.full((1, 1, 1, 1), gold["km"])
+    wq = np.full((1, 1, 1), gold["wq"])
+    wk = np.full((1, 1, 1), gold["wk"])
+    loss, gwq, gwk = orc.predictor_loss_grad(qm, km, wq, wk)
+    assert loss[0] == gold["loss"] and gwq.item() == gold["gwq"] and gwk.item() == gold["gwk"]
+    wq2, wk2, _ = orc.predictor_step(qm, km, wq, wk, gold["lr"])
+    assert abs(wq2.item() - gold["wq_next"]) < 1e-12 and abs(wk2.item() - gold["wk_next"]) < 1e-12
+
+
+def test_predictor_gradient_matches_central_differences():
+    rng = np.random.default_rng(11)
+    B, H, nb, d, r = 2, 2, 5, 6, 3
+    qm, km = rng.standard_normal((2, B, H, nb, d))
+    wq, wk = rng.standard_normal((2, H, d, r)) * 0.5
+    _, gwq, gwk = orc.predictor_loss_grad(qm, km, wq, wk)
+    eps = 1e-6
+    for W, G, which in ((wq, gwq, 0), (wk, gwk, 1)):
+        for idx in np.ndindex(W.shape):
+            Wp, Wm = W.copy(), W.copy()
+            Wp[idx] += eps
+            Wm[idx] -= eps
+            args_p = (qm, km, Wp, wk) if which == 0 else (qm, km, wq, Wp)
+            args_m = (qm, km, Wm, wk) if which == 0 else (qm, km, wq, Wm)
+            num = (orc.predictor_loss_grad(*args_p)[0] - orc.predictor_loss_grad(*args_m)[0]) / (2 * eps)
+            h = idx[0]
+            assert abs(num[h] - G[idx]) <= 1e-6 * max(1.0, abs(G[idx])), (which, idx, num[h], G[idx])
+            other = [x for x in range(H) if x != h]
+            assert np.all(np.abs(num[other]) < 1e-9)            # a head's weights touch only its loss
+
+
+def test_predictor_exact_fit_has_zero_loss():
+    # r = d with Wk = Wq^{-T}: (q Wq)(k Wk)^T = q k^T exactly, so loss and gradients vanish
+    rng = np.random.default_rng(12)
+    B, H, nb, d = 2, 3, 4, 5
+    qm, km = rng.standard_normal((2, B, H, nb, d))
+    wq = rng.standard_normal((H, d, d)) + 3 * np.eye(d)
+    wk = np.stack([np.linalg.inv(w).T for w in wq])
+    loss, gwq, gwk = orc.predictor_loss_grad(qm, km, wq, wk)
+    assert np.abs(loss).max() < 1e-18 and np.abs(gwq).max() < 1e-9 and np.abs(gwk).max() < 1e-9
+
+
+def test_predictor_steps_descend():
+    rng = np.random.default_rng(13)
+    B, H, nb, d, r = 1, 2, 8, 16, 4
+    qm, km = rng.standard_normal((2, B, H, nb, d)) * 0.5
+    wq, wk = rng.standard_normal((2, H, d, r)) * 0.3
+    losses = []
+    for _ in range(20):
+        wq, wk, loss = orc.predictor_step(qm, km, wq, wk, 0.01)
+        losses.append(loss)
+    losses = np.array(losses)
+    assert np.all(np.diff(losses, axis=0) < 0)                   # every step lowers every head's loss
+    assert np.all(losses[-1] < 0.9 * losses[0])
