@@ -396,6 +396,20 @@ def main():
                     "nnz_after_augment": int(rp_aug[-1].item()),
                     "balance_augment_ms": a0.elapsed_time(a1) / 5, "in_step": bool(args.augment)}
 
+    # predictor fitting on this step's tile means (low-rank workloads), outside the step
+    predictor_info = None
+    if wl.estimator == "lowrank" and not args.unfused:
+        wq_f, wk_f = kw["wq"].clone(), kw["wk"].clone()
+        ploss, _, _ = sp.predictor_fit(shape, pipe.qmeans, pipe.kmeans, wq_f, wk_f, lr=0.0)
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(5):
+            sp.predictor_fit(shape, pipe.qmeans, pipe.kmeans, wq_f, wk_f, lr=1e-3)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        predictor_info = {"loss_mean": float(ploss.mean().item()), "fit_step_ms": f0.elapsed_time(f1) / 5}
+
     launches = args.steps * (pipe.kernels_per_forward() + (pipe.kernels_per_backward() if wl.backward else 0))
     if rank != 0:
         if world > 1:
@@ -428,6 +442,7 @@ def main():
                      "remote_all": remote_all},
         "placement": placement_info,
         "balance": balance_info,
+        "predictor": predictor_info,
         "attn_sm_imbalance": imbalance,
         "clocks": clk, "e2e": e2e, "gpu_launches": launches, "roofline": roofline, "cpu_baseline": cpu,
     }

@@ -91,6 +91,8 @@ _SIG = {
     "sparsp_balance_heads": (_I32, [_P, _I32, _I32, _P, _P, _P, _P, _P]),
     "sparsp_augment_workspace_size": (ctypes.c_size_t, [_P, _I32]),
     "sparsp_augment": (_I32, [_P, _I32, _P, _P, _P, _P, _P, _P, ctypes.c_int64, _P, _P, ctypes.c_size_t, _P, _P]),
+    "sparsp_predictor_workspace_size": (ctypes.c_size_t, [_P, _I32]),
+    "sparsp_predictor_fit": (_I32, [_P, _I32, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "sparsp_lpt_workspace_size": (ctypes.c_size_t, [_P]),
     "sparsp_lpt_schedule": (_I32, [_P, _P, ctypes.c_uint32, _P, _P, ctypes.c_size_t, _P]),
     "sparsp_attn_workspace_size": (ctypes.c_size_t, [_P, _I32]),
@@ -327,6 +329,27 @@ def augment(shape: Shape, P: int, scores, row_ptr, col_idx, head_rank, row_ptr_o
         _ptr(col_idx_out), int(col_idx_out.numel()), _ptr(added), _ptr(ws), ws.numel(), _ptr(status),
         _stream(stream)))
     return row_ptr_out, col_idx_out, added
+
+
+def predictor_fit(shape: Shape, qmeans, kmeans, wq, wk, lr: float = 0.0, rank: int | None = None,
+                  loss=None, gwq=None, gwk=None, ws=None, stream=None):
+    """Loss and gradients of the low-rank predictor against the real block
+    scores (mean squared error per head), and the step W -= lr * grad in place
+    when lr != 0. Returns (loss [H], gwq, gwk) at the weights before the step."""
+    dev = qmeans.device
+    rank = wq.shape[-1] if rank is None else rank
+    if loss is None:
+        loss = torch.empty(shape.H, dtype=torch.float32, device=dev)
+    if gwq is None:
+        gwq = torch.empty_like(wq)
+    if gwk is None:
+        gwk = torch.empty_like(wk)
+    if ws is None:
+        ws = _empty(lib().sparsp_predictor_workspace_size(_sref(shape), int(rank)), dev)
+    _check("sparsp_predictor_fit", lib().sparsp_predictor_fit(
+        _sref(shape), int(rank), _ptr(qmeans), _ptr(kmeans), _ptr(wq), _ptr(wk), float(lr), _ptr(loss),
+        _ptr(gwq), _ptr(gwk), _ptr(ws), ws.numel(), _stream(stream)))
+    return loss, gwq, gwk
 
 
 # ----------------------------------------------------------------- step 5

@@ -343,6 +343,33 @@ sparsp_status_t sparsp_augment(const sparsp_shape_t* shape, int32_t P, const flo
                         d_status, (cudaStream_t)stream);
 }
 
+size_t sparsp_predictor_workspace_size(const sparsp_shape_t* shape, int32_t rank) {
+  Dims s;
+  if (check_shape(shape, &s) != SPARSP_OK || rank < 1 || rank > 64) return 0;
+  return predictor_ws(s, rank);
+}
+
+sparsp_status_t sparsp_predictor_fit(const sparsp_shape_t* shape, int32_t rank, const float* qmeans,
+                                     const float* kmeans, float* wq, float* wk, float lr, float* loss,
+                                     float* gwq, float* gwk, void* ws, size_t ws_bytes,
+                                     sparsp_stream_t stream) {
+  Dims s;
+  sparsp_status_t r = check_shape(shape, &s);
+  if (r != SPARSP_OK) return r;
+  if (rank < 1 || rank > 64) return SPARSP_ERR_UNSUPPORTED;
+  if (!isfinite(lr)) return SPARSP_ERR_INVALID_ARG;
+  CHECK_PTR(qmeans);
+  CHECK_PTR(kmeans);
+  CHECK_PTR(wq);
+  CHECK_PTR(wk);
+  CHECK_OPT_PTR(loss);
+  CHECK_OPT_PTR(gwq);
+  CHECK_OPT_PTR(gwk);
+  CHECK_PTR(ws);
+  if (ws_bytes < predictor_ws(s, rank)) return SPARSP_ERR_WORKSPACE;
+  return launch_predictor_fit(s, rank, qmeans, kmeans, wq, wk, lr, loss, gwq, gwk, ws, (cudaStream_t)stream);
+}
+
 size_t sparsp_lpt_workspace_size(const sparsp_shape_t* shape) {
   Dims s;
   if (check_shape(shape, &s) != SPARSP_OK) return 0;

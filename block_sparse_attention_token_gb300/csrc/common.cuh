@@ -91,6 +91,11 @@ sparsp_status_t launch_augment(const Dims& s, int P, const float* scores, const 
                                cudaStream_t st);
 constexpr int kBalanceMaxHeads = 2048;
 
+size_t predictor_ws(const Dims& s, int rank);
+sparsp_status_t launch_predictor_fit(const Dims& s, int rank, const float* qm, const float* km, float* wq,
+                                     float* wk, float lr, float* loss, float* gwq, float* gwk, void* ws,
+                                     cudaStream_t st);
+
 size_t lpt_ws(const Dims& s);
 sparsp_status_t launch_lpt(const Dims& s, const int32_t* row_ptr, bool flat, int32_t* items,
                            int32_t* counter, void* ws, cudaStream_t st);

@@ -13,7 +13,7 @@ from __future__ import annotations
 import torch
 
 from . import (EST_LOWRANK, EST_MEAN, PROF_SLOTS, Shape, attn_bwd, attn_fwd, attn_workspace_size, augment,
-               augment_workspace_size, balance_heads, Balance,
+               augment_workspace_size, balance_heads, Balance, predictor_fit,
                block_scores, block_scores_pooled, block_scores_workspace_size, kv_demand, lib, placement,
                placement_workspace_size, reorder, reorder_pool, select, select_workspace_size, DemandOut)
 
@@ -21,7 +21,7 @@ from . import (EST_LOWRANK, EST_MEAN, PROF_SLOTS, Shape, attn_bwd, attn_fwd, att
 class Pipeline:
     def kernels_per_forward(self) -> int:
         """Kernels forward() launches: reorder x3, pool + product, select x3 (count,
-        scan, fill), balancing (1) and augmentation x4 (keys, rank select,
+        scan, fill), predictor fitting x5 when enabled, balancing (1) and augmentation x4 (keys, rank select,
         scan, fill) when enabled, placement x2 (affinity, greedy) when
         enabled, demand x4 (bitmap, scan, list, gather), schedule (1, or 2 in
         flat order) + attention, inverse reorder."""
@@ -30,7 +30,8 @@ class Pipeline:
         scores = (2 if self.est == EST_LOWRANK else 1) if self.fused else 2
         place = 2 if self.owner is not None else 0
         bal = (1 if self.migrations is not None else 0) + (4 if self.augment else 0)
-        return 3 + scores + 3 + bal + place + 3 + gather + lpt + 1 + 1
+        pred = 5 if self.predictor_lr is not None else 0   # projection, two score products, two gradient kernels
+        return 3 + scores + pred + 3 + bal + place + 3 + gather + lpt + 1 + 1
 
     def kernels_per_backward(self) -> int:
         """reorder dO, rowdot, CSR transpose, schedule, dQ, schedule, dK/dV, 3 inverse reorders."""
@@ -40,11 +41,13 @@ class Pipeline:
     def __init__(self, shape: Shape, estimator: str, top_p: float, k_floor: int, P: int, rank: int = 16,
                  gather: bool = True, flags: int = 0, backward: bool = False, device="cuda",
                  fused_estimation: bool = True, placement: bool = False, migrations: int | None = None,
-                 augment: bool = False):
+                 augment: bool = False, predictor_lr: float | None = None):
         """migrations: balance heads over P virtual ranks with at most this many
         migrations (None: no balancing). augment: fill each rank's slack with
         extra blocks (on the balanced ranks, or the contiguous head split);
-        attention then runs on the augmented CSR."""
+        attention then runs on the augmented CSR. predictor_lr: with the
+        low-rank estimator, after the scores are taken, one fitting step of the
+        predictor weights (updated in place) against the real block scores."""
         self.shape, self.top_p, self.k_floor, self.P, self.rank, self.flags = shape, top_p, k_floor, P, rank, flags
         self.est = EST_LOWRANK if estimator == "lowrank" else EST_MEAN
         self.fused = fused_estimation
@@ -77,6 +80,14 @@ class Pipeline:
                                 torch.empty(parts * s.nb, dtype=torch.int32, device=dev), kg, vg,
                                 torch.empty(4, dtype=torch.int64, device=dev))
         self.migrations, self.augment = migrations, augment
+        self.predictor_lr = predictor_lr
+        if predictor_lr is not None:
+            if self.est != EST_LOWRANK or not fused_estimation:
+                raise ValueError("predictor fitting needs the low-rank estimator with fused estimation")
+            self.predictor_loss = torch.empty(s.H, dtype=torch.float32, device=dev)
+            self.gwq, self.gwk = (torch.empty((s.H, s.d, rank), dtype=torch.float32, device=dev) for _ in range(2))
+            self.ws_pred = torch.empty(max(lib().sparsp_predictor_workspace_size(ctypes.byref(s), rank), 16),
+                                       dtype=torch.uint8, device=dev)
         self.balance = None
         if migrations is not None or augment:
             if migrations is None:
@@ -124,6 +135,10 @@ class Pipeline:
             mark("reorder")
             block_scores(s, self.qb, self.kb, self.est, wq, wk, self.rank, out=self.scores, ws=self.ws_scores)
         mark("scores")
+        if self.predictor_lr is not None:
+            predictor_fit(s, self.qmeans, self.kmeans, wq, wk, self.predictor_lr, self.rank, self.predictor_loss,
+                          self.gwq, self.gwk, self.ws_pred)
+            mark("predictor")
         select(s, self.scores, self.top_p, self.k_floor, self.row_ptr, self.col_idx, self.ws_sel, self.status)
         mark("select")
         rp, ci = self.row_ptr, self.col_idx

@@ -301,6 +301,29 @@ SPARSP_API sparsp_status_t sparsp_augment(const sparsp_shape_t* shape, int32_t P
                                void* ws, size_t ws_bytes, int32_t* d_status, sparsp_stream_t stream);
 
 /*
+ * Predictor fitting ("Dynamic Sparsity in Large-Scale Video DiT Training",
+ * "How DSV works / The idea": the two per-head matrices are trained so that
+ * their product approximates the real query-key scores, beside the main graph
+ * and during the forward pass). The pages call the loss magnitude-preserving
+ * without defining it; here it is the mean squared error between the
+ * predictor's block scores and the real block scores of the same pooled
+ * means, per head:
+ *   E[b,h,i,j] = (qm[b,h,i] Wq[h]) . (km[b,h,j] Wk[h]) - qm[b,h,i] . km[b,h,j]
+ *   loss[h]    = sum_{b,i,j} E^2 / (B nb^2)
+ * qmeans, kmeans: float32 [B,H,nb,d] tile means (sparsp_reorder_pool).
+ * wq, wk: float32 [H,d,rank], 1 <= rank <= 64. Writes loss [H], gwq and gwk
+ * [H,d,rank] = dloss/dWq, dloss/dWk (each may be NULL), all at the current
+ * weights; then, if lr != 0, takes the step W -= lr * dloss/dW in place.
+ * ws: at least sparsp_predictor_workspace_size() bytes. Sums run in a fixed
+ * order: results are bitwise reproducible.
+ */
+SPARSP_API size_t sparsp_predictor_workspace_size(const sparsp_shape_t* shape, int32_t rank);
+SPARSP_API sparsp_status_t sparsp_predictor_fit(const sparsp_shape_t* shape, int32_t rank, const float* qmeans,
+                                     const float* kmeans, float* wq, float* wk, float lr, float* loss,
+                                     float* gwq, float* gwk, void* ws, size_t ws_bytes,
+                                     sparsp_stream_t stream);
+
+/*
  * Step 5c - longest-first work order for the attention kernels (the per-head
  * straggler problem of the "mlsift.com tag listing" entry; the lopsided
  * per-head work of "Dynamic Sparsity in Large-Scale Video DiT Training",

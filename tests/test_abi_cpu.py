@@ -144,6 +144,15 @@ def test_call_validation_codes(lib):
                               None) == sp.INVALID_ARG
     assert lib.sparsp_augment(S, 2, FAKE, FAKE, FAKE, None, FAKE, FAKE, 16, None, FAKE, need, None,
                               None) == sp.INVALID_ARG
+    # predictor fitting: rank out of range, NaN step, small workspace
+    needp = lib.sparsp_predictor_workspace_size(S, 16)
+    assert needp > 0 and lib.sparsp_predictor_workspace_size(S, 65) == 0
+    assert lib.sparsp_predictor_fit(S, 65, FAKE, FAKE, FAKE, FAKE, f(0.0), None, None, None, FAKE, needp,
+                                    None) == sp.UNSUPPORTED
+    assert lib.sparsp_predictor_fit(S, 16, FAKE, FAKE, FAKE, FAKE, f(float("nan")), None, None, None, FAKE,
+                                    needp, None) == sp.INVALID_ARG
+    assert lib.sparsp_predictor_fit(S, 16, FAKE, FAKE, FAKE, FAKE, f(0.1), None, None, None, FAKE, needp - 1,
+                                    None) == sp.WORKSPACE
     # attention: NaN scale, small workspace, misaligned optional pointer, fp32 backward
     p7 = (FAKE,) * 5
     assert lib.sparsp_attn_fwd(S, *p7, f(float("nan")), FAKE, FAKE, FAKE, 1 << 30, 0, None, None,

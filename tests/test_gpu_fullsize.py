@@ -143,6 +143,25 @@ def test_balance_and_augment(run):
           f"rows differing from the oracle {n}")
 
 
+def test_predictor_fit(run):
+    """Predictor loss and gradients at the full size, against the oracle on the
+    same pooled means (the low-rank workload uses its own weights)."""
+    wl, ch, g = run.wl, run.ch, run.ch.g
+    if wl.estimator != "lowrank":
+        pytest.skip("mean-estimator workload")
+    qm = orc.pool_means(ch.qb, g.Bt).astype(np.float32)
+    km = orc.pool_means(ch.kb, g.Bt).astype(np.float32)
+    wq, wk = run.data["wq"].astype(np.float32), run.data["wk"].astype(np.float32)
+    loss_ref, gq_ref, gk_ref = orc.predictor_loss_grad(qm, km, wq, wk)
+    loss, gq, gk = sp.predictor_fit(run.shape, torch.from_numpy(qm).cuda(), torch.from_numpy(km).cuda(),
+                                    torch.from_numpy(wq).cuda(), torch.from_numpy(wk).cuda(), lr=0.0)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(host(loss), loss_ref, rtol=1e-4)
+    for got, ref in ((host(gq), gq_ref), (host(gk), gk_ref)):
+        assert np.abs(got - ref).max() <= 1e-4 * np.abs(ref).max()
+    print(f"{wl.name}: predictor loss per head min {loss_ref.min():.4g} max {loss_ref.max():.4g}")
+
+
 def _sample_rows(ch, n, seed):
     g = ch.g
     counts = np.diff(ch.sel.row_ptr)

@@ -376,6 +376,42 @@ def test_augment_edges():
     assert st.item() == sp.CAPACITY
 
 
+@pytest.mark.parametrize("name", ["tiny", "medium", "r128", "wave"])
+def test_predictor_fit_matches_oracle(name):
+    wl, data, shape = _setup(name)
+    g = orc.grid_of(wl)
+    qb, kb = (orc.reorder(data[x], g) for x in ("q", "k"))
+    qm = orc.pool_means(qb, g.Bt).astype(np.float32)
+    km = orc.pool_means(kb, g.Bt).astype(np.float32)
+    rank = 16
+    rng = np.random.default_rng(40)
+    wq = (rng.standard_normal((g.H, g.d, rank)) / np.sqrt(g.d)).astype(np.float32)
+    wk = (rng.standard_normal((g.H, g.d, rank)) / np.sqrt(g.d)).astype(np.float32)
+    loss_ref, gq_ref, gk_ref = orc.predictor_loss_grad(qm, km, wq, wk)
+    Wq, Wk = torch.from_numpy(wq).cuda(), torch.from_numpy(wk).cuda()
+    Qm, Km = torch.from_numpy(qm).cuda(), torch.from_numpy(km).cuda()
+    loss, gq, gk = sp.predictor_fit(shape, Qm, Km, Wq, Wk, lr=0.0)
+    torch.cuda.synchronize()
+    assert torch.equal(Wq, torch.from_numpy(wq).cuda()) and torch.equal(Wk, torch.from_numpy(wk).cuda())
+    np.testing.assert_allclose(host(loss), loss_ref, rtol=1e-4)
+    for got, ref in ((host(gq), gq_ref), (host(gk), gk_ref)):
+        assert np.abs(got - ref).max() <= 1e-4 * np.abs(ref).max()
+    # the step, and bitwise reproducibility
+    lr = 0.05
+    loss2, gq2, gk2 = sp.predictor_fit(shape, Qm, Km, Wq, Wk, lr=lr)
+    torch.cuda.synchronize()
+    assert torch.equal(loss2, loss) and torch.equal(gq2, gq) and torch.equal(gk2, gk)
+    wq_ref, wk_ref, _ = orc.predictor_step(qm, km, wq, wk, lr)
+    for got, ref, gr in ((host(Wq), wq_ref, gq_ref), (host(Wk), wk_ref, gk_ref)):
+        assert np.abs(got - ref).max() <= lr * 1e-4 * np.abs(gr).max() + 1e-6 * np.abs(ref).max()
+    # a few steps lower every head's loss
+    for _ in range(5):
+        sp.predictor_fit(shape, Qm, Km, Wq, Wk, lr=lr)
+    loss3, _, _ = sp.predictor_fit(shape, Qm, Km, Wq, Wk, lr=0.0)
+    torch.cuda.synchronize()
+    assert (host(loss3) < host(loss)).all()
+
+
 @pytest.mark.parametrize("name", list(SMALL))
 @pytest.mark.parametrize("flat", [False, True])
 def test_lpt_schedule_bitexact(name, flat):
@@ -576,6 +612,33 @@ def test_pipeline_with_balance_and_augment(name):
     pipe.backward(dout)
     torch.cuda.synchronize()
     assert pipe.status.item() == 0
+
+
+def test_pipeline_with_predictor_fitting():
+    """A fitting step inside the pipeline: selection uses the weights before
+    the step, the weights afterwards equal a standalone step from the same
+    start, and the reported loss is the oracle's."""
+    wl, data, shape = _setup("wave")
+    g = orc.grid_of(wl)
+    args = [dev(data[x], wl) for x in ("q", "k", "v")]
+    wq0, wk0 = (torch.from_numpy(data[x]).cuda() for x in ("wq", "wk"))
+    plain = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P)
+    o1, _ = plain.forward(*args, wq=wq0, wk=wk0)
+    wq, wk = wq0.clone(), wk0.clone()
+    fit = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P, predictor_lr=0.01)
+    o2, _ = fit.forward(*args, wq=wq, wk=wk)
+    torch.cuda.synchronize()
+    assert fit.status.item() == 0
+    assert torch.equal(o1, o2)
+    wq2, wk2 = wq0.clone(), wk0.clone()
+    sp.predictor_fit(shape, fit.qmeans, fit.kmeans, wq2, wk2, lr=0.01)
+    torch.cuda.synchronize()
+    assert torch.equal(wq, wq2) and torch.equal(wk, wk2) and not torch.equal(wq, wq0)
+    qb, kb = (orc.reorder(data[x], g) for x in ("q", "k"))
+    loss_ref, _, _ = orc.predictor_loss_grad(orc.pool_means(qb, g.Bt), orc.pool_means(kb, g.Bt),
+                                             data["wq"], data["wk"])
+    np.testing.assert_allclose(host(fit.predictor_loss), loss_ref, rtol=1e-4)
+    assert fit.kernels_per_forward() == plain.kernels_per_forward() + 5
 
 
 def test_host_pipeline_overlapped_steps_match_device_pipeline():
