@@ -301,21 +301,13 @@ def main():
             host_grads = [torch.empty(pipe.o.shape, dtype=tdt).pin_memory() for _ in range(3)]
             d2h += 3 * host_out.numel() * host_out.element_size()
 
-        overlapped = not wl.backward
-        if overlapped:
-            hp = sp.HostPipeline(pipe)
-
+        hp = sp.HostPipeline(pipe)
+        if wl.backward:
             def e2e_step():
-                hp.step(host_in["q"], host_in["k"], host_in["v"], host_out, **kw)
+                hp.train_step(host_in["q"], host_in["k"], host_in["v"], host_in["do"], host_out, *host_grads, **kw)
         else:
             def e2e_step():
-                for x in ("q", "k", "v"):
-                    dev_in[x].copy_(host_in[x], non_blocking=True)
-                dout.copy_(host_in["do"], non_blocking=True)
-                step()
-                host_out.copy_(pipe.o, non_blocking=True)
-                for hg, g in zip(host_grads, (pipe.dq, pipe.dk, pipe.dv)):
-                    hg.copy_(g, non_blocking=True)
+                hp.step(host_in["q"], host_in["k"], host_in["v"], host_out, **kw)
 
         for _ in range(2):
             e2e_step()
@@ -326,8 +318,7 @@ def main():
         e0.record(stream)
         for _ in range(args.steps):
             e2e_step()
-        if overlapped:
-            stream.wait_stream(hp.d2h)     # the last result has reached the host
+        stream.wait_stream(hp.d2h)         # the last result has reached the host
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / args.steps
@@ -337,7 +328,7 @@ def main():
             e2e_ms = float(t.item())
         e2e = {"value": world * f_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "copies": "overlapped with neighbouring steps (HostPipeline)" if overlapped else "serial"}
+               "copies": "overlapped with neighbouring steps (HostPipeline)"}
 
     # per-SM busy imbalance of the attention kernel (one extra profiled step, untimed)
     pipe.prof.zero_()

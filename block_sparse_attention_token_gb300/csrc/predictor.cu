@@ -10,10 +10,10 @@
 //     km Wk come out of the low-rank pass, in the workspace);
 //  2. ge_kernel   - grid (b*H + h, chunk of 256 outputs): GA = E (km Wk),
 //     GB = E^T (qm Wq), one output element per thread;
-//  3. gw_kernel   - grid (h, chunk of 256 weights): the weight gradients (sums
-//     over b and i in a fixed order) and, when lr != 0, the step
-//     W -= lr dL/dW in place (the projections were taken before it); chunk 0
-//     of each head also sums the loss (a fixed-shape tree).
+//  3. loss_kernel - one CTA per head: the loss (fp64 partials, a fixed tree);
+//  4. gw_kernel   - grid (h, dd): the weight gradients (row slices summed in a
+//     fixed tree) and, when lr != 0, the step W -= lr dL/dW in place (the
+//     projections were taken before it).
 // Every sum has a fixed order, so results are bitwise reproducible.
 #include "common.cuh"
 
@@ -44,28 +44,39 @@ ge_kernel(const float* __restrict__ sp, const float* __restrict__ st, const floa
   GB[idx] = bsum;
 }
 
+// One CTA per (h, dd): thread (slice, c) sums column c over its slice of the
+// B*nb rows; the slices are then added in a fixed tree.
 __global__ void __launch_bounds__(kThreads)
-gw_kernel(const float* __restrict__ qm, const float* __restrict__ km, const float* __restrict__ sp,
-          const float* __restrict__ st, const float* __restrict__ ga, const float* __restrict__ gb, int B,
-          int H, int nb, int d, int rank, float lr, float* __restrict__ wq, float* __restrict__ wk,
-          float* __restrict__ loss, float* __restrict__ gwq, float* __restrict__ gwk) {
-  __shared__ double red[kThreads];
-  const int h = blockIdx.x;
-  const double n = (double)B * nb * nb;
-  const float scale = (float)(2.0 / n);
-  const int idx = blockIdx.y * kThreads + threadIdx.x;
-  if (idx < d * rank) {
-    const int dd = idx / rank, c = idx % rank;
-    float q = 0.f, k = 0.f;
+gw_kernel(const float* __restrict__ qm, const float* __restrict__ km, const float* __restrict__ ga,
+          const float* __restrict__ gb, int B, int H, int nb, int d, int rank, float lr, float* __restrict__ wq,
+          float* __restrict__ wk, float* __restrict__ gwq, float* __restrict__ gwk) {
+  __shared__ float part[2][kThreads];
+  const int h = blockIdx.x, dd = blockIdx.y;
+  const int nslices = kThreads / rank;
+  const int c = threadIdx.x % rank, slice = threadIdx.x / rank;
+  float q = 0.f, k = 0.f;
+  if (slice < nslices) {
     for (int b = 0; b < B; ++b) {
       const int64_t bh = (int64_t)b * H + h;
-      for (int i = 0; i < nb; ++i) {
-        q = fmaf(qm[(bh * nb + i) * d + dd], ga[(bh * nb + i) * rank + c], q);
-        k = fmaf(km[(bh * nb + i) * d + dd], gb[(bh * nb + i) * rank + c], k);
+      for (int i = slice; i < nb; i += nslices) {
+        const int64_t row = bh * nb + i;
+        q = fmaf(qm[row * d + dd], ga[row * rank + c], q);
+        k = fmaf(km[row * d + dd], gb[row * rank + c], k);
       }
     }
-    const float g1 = q * scale, g2 = k * scale;
-    const int64_t w = (int64_t)h * d * rank + idx;
+  }
+  part[0][threadIdx.x] = q;
+  part[1][threadIdx.x] = k;
+  __syncthreads();
+  if (threadIdx.x < rank) {
+    float sq = 0.f, sk = 0.f;
+    for (int sl = 0; sl < nslices; ++sl) {
+      sq += part[0][sl * rank + threadIdx.x];
+      sk += part[1][sl * rank + threadIdx.x];
+    }
+    const float scale = (float)(2.0 / ((double)B * nb * nb));
+    const float g1 = sq * scale, g2 = sk * scale;
+    const int64_t w = ((int64_t)h * d + dd) * rank + threadIdx.x;
     if (gwq != nullptr) gwq[w] = g1;
     if (gwk != nullptr) gwk[w] = g2;
     if (lr != 0.f) {
@@ -73,8 +84,15 @@ gw_kernel(const float* __restrict__ qm, const float* __restrict__ km, const floa
       wk[w] -= lr * g2;
     }
   }
-  if (blockIdx.y != 0) return;
-  // loss: every thread sums a fixed strided subset in fp64, then a fixed tree
+}
+
+// One CTA per head: every thread sums a fixed strided subset in fp64, then a
+// fixed tree.
+__global__ void __launch_bounds__(kThreads)
+loss_kernel(const float* __restrict__ sp, const float* __restrict__ st, int B, int H, int nb,
+            float* __restrict__ loss) {
+  __shared__ double red[kThreads];
+  const int h = blockIdx.x;
   double acc = 0.0;
   for (int b = 0; b < B; ++b) {
     const int64_t base = ((int64_t)b * H + h) * nb * nb;
@@ -89,7 +107,7 @@ gw_kernel(const float* __restrict__ qm, const float* __restrict__ km, const floa
     if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
     __syncthreads();
   }
-  if (threadIdx.x == 0 && loss != nullptr) loss[h] = (float)(red[0] / n);
+  if (threadIdx.x == 0) loss[h] = (float)(red[0] / ((double)B * nb * nb));
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -129,8 +147,12 @@ sparsp_status_t launch_predictor_fit(const Dims& s, int rank, const float* qm, c
   ge_kernel<<<dim3((unsigned)bh, (unsigned)((s.nb * rank + kThreads - 1) / kThreads)), kThreads, 0, st>>>(
       sp, strue, pq, pk, s.nb, rank, ga, gb);
   SPARSP_LAUNCH_CHECK();
-  gw_kernel<<<dim3((unsigned)s.H, (unsigned)((s.d * rank + kThreads - 1) / kThreads)), kThreads, 0, st>>>(
-      qm, km, sp, strue, ga, gb, s.B, s.H, s.nb, s.d, rank, lr, wq, wk, loss, gwq, gwk);
+  if (loss != nullptr) {
+    loss_kernel<<<s.H, kThreads, 0, st>>>(sp, strue, s.B, s.H, s.nb, loss);
+    SPARSP_LAUNCH_CHECK();
+  }
+  gw_kernel<<<dim3((unsigned)s.H, (unsigned)s.d), kThreads, 0, st>>>(qm, km, ga, gb, s.B, s.H, s.nb, s.d, rank, lr,
+                                                                    wq, wk, gwq, gwk);
   SPARSP_LAUNCH_CHECK();
   return SPARSP_OK;
 }

@@ -21,7 +21,7 @@ from . import (EST_LOWRANK, EST_MEAN, PROF_SLOTS, Shape, attn_bwd, attn_fwd, att
 class Pipeline:
     def kernels_per_forward(self) -> int:
         """Kernels forward() launches: reorder x3, pool + product, select x3 (count,
-        scan, fill), predictor fitting x5 when enabled, balancing (1) and augmentation x4 (keys, rank select,
+        scan, fill), predictor fitting x6 when enabled, balancing (1) and augmentation x4 (keys, rank select,
         scan, fill) when enabled, placement x2 (affinity, greedy) when
         enabled, demand x4 (bitmap, scan, list, gather), schedule (1, or 2 in
         flat order) + attention, inverse reorder."""
@@ -30,7 +30,7 @@ class Pipeline:
         scores = (2 if self.est == EST_LOWRANK else 1) if self.fused else 2
         place = 2 if self.owner is not None else 0
         bal = (1 if self.migrations is not None else 0) + (4 if self.augment else 0)
-        pred = 5 if self.predictor_lr is not None else 0   # projection, two score products, two gradient kernels
+        pred = 6 if self.predictor_lr is not None else 0   # projection, two score products, loss, two gradient kernels
         return 3 + scores + pred + 3 + bal + place + 3 + gather + lpt + 1 + 1
 
     def kernels_per_backward(self) -> int:
@@ -163,7 +163,8 @@ class Pipeline:
         mark("reorder_out")
         return o, self.lse
 
-    def backward(self, dout, prof: bool = False, mark=None):
+    def backward(self, dout, prof: bool = False, mark=None, outs=None):
+        """outs: optional raster (dQ, dK, dV) output buffers (default: self.dq, self.dk, self.dv)."""
         s = self.shape
         mark = mark or (lambda name: None)
         reorder(s, dout, self.dob)
@@ -172,8 +173,9 @@ class Pipeline:
         attn_bwd(s, self.qb, self.kb, self.vb, self.ob, self.lse, self.dob, rp, ci, 0.0,
                  self.dqb, self.dkb, self.dvb, self.ws_attn, self.flags, self.prof if prof else None, self.status)
         mark("attn_bwd")
-        reorder(s, self.dqb, self.dq, inverse=True)
-        reorder(s, self.dkb, self.dk, inverse=True)
-        reorder(s, self.dvb, self.dv, inverse=True)
+        dq, dk, dv = (self.dq, self.dk, self.dv) if outs is None else outs
+        reorder(s, self.dqb, dq, inverse=True)
+        reorder(s, self.dkb, dk, inverse=True)
+        reorder(s, self.dvb, dv, inverse=True)
         mark("reorder_grads")
-        return self.dq, self.dk, self.dv
+        return dq, dk, dv

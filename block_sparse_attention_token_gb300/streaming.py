@@ -1,11 +1,13 @@
-"""Forward steps from pinned host memory to pinned host memory, overlapped.
+"""Steps from pinned host memory to pinned host memory, overlapped.
 
 HostPipeline.step() enqueues one whole forward step for inputs that live in
-pinned host buffers and writes O back to a pinned host buffer. The device
-input and output buffers are double-buffered and the copies run on their own
-streams, so the host-to-device copy of step n+1 and the device-to-host copy of
-step n-1 overlap the kernels of step n. Every step still copies its own inputs
-in and its own result out; events order each buffer's reuse.
+pinned host buffers and writes O back to a pinned host buffer;
+HostPipeline.train_step() does the same for a forward + backward step (Q, K, V
+and dO in; O, dQ, dK and dV out). The device input and output buffers are
+double-buffered and the copies run on their own streams, so the host-to-device
+copy of step n+1 and the device-to-host copy of step n-1 overlap the kernels
+of step n. Every step still copies its own inputs in and its own results out;
+events order each buffer's reuse.
 """
 from __future__ import annotations
 
@@ -31,6 +33,7 @@ class HostPipeline:
             for e in evs:
                 e.record(cur)
         self.n = 0
+        self.t_inp = self.t_out = None
 
     def step(self, hq, hk, hv, ho, wq=None, wk=None):
         """One forward step: pinned host q, k, v (raster) in, pinned host O out."""
@@ -56,6 +59,42 @@ class HostPipeline:
             self.out_free[b].record(self.d2h)
         self.n += 1
         return ho
+
+    def train_step(self, hq, hk, hv, hdo, ho, hdq, hdk, hdv, wq=None, wk=None):
+        """One forward + backward step: pinned host q, k, v, dO (raster) in;
+        pinned host O, dQ, dK, dV out. Needs a Pipeline built with backward=True."""
+        if self.t_inp is None:
+            s = self.pipe.shape
+            raster = (s.B, s.N, s.H, s.d)
+            mk = lambda n: [[torch.empty(raster, dtype=s.torch_dtype, device="cuda") for _ in range(n)]
+                            for _ in range(2)]
+            self.t_inp, self.t_out = mk(4), mk(4)
+        b = self.n & 1
+        cur = torch.cuda.current_stream()
+        with torch.cuda.stream(self.h2d):
+            self.h2d.wait_event(self.in_free[b])          # step n-2 has consumed these buffers
+            for dst, src in zip(self.t_inp[b], (hq, hk, hv, hdo)):
+                dst.copy_(src, non_blocking=True)
+            self.in_ready[b].record(self.h2d)
+        cur.wait_event(self.in_ready[b])
+        cur.wait_event(self.out_free[b])                   # step n-2's results have left the device
+
+        def mark(name):
+            if name == "reorder_dout":                     # every raster input has been read
+                self.in_free[b].record(cur)
+
+        q, k, v, do = self.t_inp[b]
+        o, dq, dk, dv = self.t_out[b]
+        self.pipe.forward(q, k, v, wq=wq, wk=wk, out=o)
+        self.pipe.backward(do, mark=mark, outs=(dq, dk, dv))
+        self.out_ready[b].record(cur)
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(self.out_ready[b])
+            for dst, src in zip((ho, hdq, hdk, hdv), self.t_out[b]):
+                dst.copy_(src, non_blocking=True)
+            self.out_free[b].record(self.d2h)
+        self.n += 1
+        return ho, hdq, hdk, hdv
 
     def synchronize(self):
         self.d2h.synchronize()

@@ -638,7 +638,7 @@ def test_pipeline_with_predictor_fitting():
     loss_ref, _, _ = orc.predictor_loss_grad(orc.pool_means(qb, g.Bt), orc.pool_means(kb, g.Bt),
                                              data["wq"], data["wk"])
     np.testing.assert_allclose(host(fit.predictor_loss), loss_ref, rtol=1e-4)
-    assert fit.kernels_per_forward() == plain.kernels_per_forward() + 5
+    assert fit.kernels_per_forward() == plain.kernels_per_forward() + 6
 
 
 def test_host_pipeline_overlapped_steps_match_device_pipeline():
@@ -663,4 +663,36 @@ def test_host_pipeline_overlapped_steps_match_device_pipeline():
         o, _ = pipe.forward(hq.cuda(), hk.cuda(), hv.cuda())
         torch.cuda.synchronize()
         assert torch.equal(ho, o.cpu())
+    assert pipe.status.item() == 0
+
+
+def test_host_pipeline_training_steps_match_device_pipeline():
+    """Overlapped forward + backward steps from pinned host memory give, step
+    for step, exactly the device pipeline's O, dQ, dK and dV."""
+    wl = SMALL["r128"]
+    _, data = workload(wl)
+    shape = sp.shape_of(wl)
+    pipe = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P, backward=True)
+    hp = sp.HostPipeline(pipe)
+    rng = np.random.default_rng(50)
+    steps = []
+    for n in range(3):
+        scale = np.float32(1.0 + 0.25 * n)
+        hq, hk, hv = (torch.from_numpy(synth.round_bf16(data[x] * scale)).bfloat16().pin_memory() for x in "qkv")
+        hdo = torch.from_numpy(synth.round_bf16(rng.standard_normal(data["q"].shape).astype(np.float32))
+                               ).bfloat16().pin_memory()
+        outs = tuple(torch.empty_like(hq).pin_memory() for _ in range(4))
+        steps.append(((hq, hk, hv, hdo), outs))
+    for ins, outs in steps:
+        hp.train_step(*ins, *outs)
+    hp.synchronize()
+    torch.cuda.synchronize()
+    for (hq, hk, hv, hdo), (ho, hdq, hdk, hdv) in steps:
+        o, _ = pipe.forward(hq.cuda(), hk.cuda(), hv.cuda())
+        o = o.clone()
+        dq, dk, dv = pipe.backward(hdo.cuda())
+        torch.cuda.synchronize()
+        assert torch.equal(ho, o.cpu())
+        for h, d in ((hdq, dq), (hdk, dk), (hdv, dv)):
+            assert torch.equal(h, d.cpu())
     assert pipe.status.item() == 0
