@@ -291,6 +291,45 @@ def main():
     if wl.backward:
         roofline["bwd_achieved"] = bwd_flops(nnz, wl) / (stage_ms["attn_bwd"] * 1e-3) / 1e12
 
+    # ---- algorithmic bytes of the memory-bound stages, against the measured copy peak
+    el = 2 if wl.dtype == "bf16" else 4
+    BH = shape.B * shape.H
+    tensor = BH * shape.N * shape.d * el
+    means = BH * shape.nb * shape.d * 4
+    rows = BH * shape.nb
+    stage_bytes = {
+        "reorder": 6 * tensor + (2 * means if not args.unfused else 0),
+        "scores": (2 * means if not args.unfused else 2 * tensor) + 4 * BH * shape.nb * shape.nb,
+        "select": 4 * BH * shape.nb * shape.nb + 4 * (nnz + rows + 1),
+        "kv_demand": 4 * nnz + 2 * demanded + BH * wl.P * ((shape.nb + 31) // 32) * 4,
+        "reorder_out": 2 * tensor,
+    }
+    hbm = {}
+    for name, nbytes in stage_bytes.items():
+        if name in stage_ms and stage_ms[name] > 0:
+            gbs = nbytes / (stage_ms[name] * 1e-3) / 1e9
+            hbm[name] = {"bytes": int(nbytes), "gbs": gbs, "frac": gbs / pk["hbm_gbs"]}
+
+    # ---- context only: dense attention (PyTorch SDPA) over the same tensors
+    dense = None
+    try:
+        import torch.nn.functional as F
+        qd, kd, vd = pipe.qb, pipe.kb, pipe.vb
+        for _ in range(2):
+            F.scaled_dot_product_attention(qd, kd, vd)
+        d0 = torch.cuda.Event(enable_timing=True)
+        d1 = torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        for _ in range(3):
+            F.scaled_dot_product_attention(qd, kd, vd)
+        d1.record(stream)
+        torch.cuda.synchronize()
+        dms = d0.elapsed_time(d1) / 3
+        dense = {"sdpa_ms": dms, "sdpa_tflops": 4.0 * BH * shape.N * shape.N * shape.d / (dms * 1e-3) / 1e12,
+                 "sparse_attn_speedup": dms / stage_ms["attn_fwd"], "kind": "torch SDPA, dense, same Q/K/V"}
+    except Exception as exc:   # context only: never fails the bench
+        dense = {"unavailable": str(exc)[:120]}
+
     # ---- end to end through the public API: pinned host -> device, step, O -> pinned host
     e2e = None
     if not args.no_e2e:
@@ -429,6 +468,8 @@ def main():
                    "l2": f"inputs larger than L2 ({shape.B * shape.H * shape.N * shape.d * 2 / 1e6:.0f} MB per tensor)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "stages_ms": stage_ms,
+        "hbm_stages": hbm,
+        "dense_context": dense,
         "kv_bytes": {"demanded": demanded, "all": all_bytes, "remote_demanded": remote_dem,
                      "remote_all": remote_all},
         "placement": placement_info,
