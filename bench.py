@@ -301,7 +301,9 @@ def main():
         "reorder": 6 * tensor + (2 * means if not args.unfused else 0),
         "scores": (2 * means if not args.unfused else 2 * tensor) + 4 * BH * shape.nb * shape.nb,
         "select": 4 * BH * shape.nb * shape.nb + 4 * (nnz + rows + 1),
-        "kv_demand": 4 * nnz + 2 * demanded + BH * wl.P * ((shape.nb + 31) // 32) * 4,
+        # the gathered copy is written once; each source K/V tile is read from HBM once (its
+        # P-fold reuse across partitions hits in L2)
+        "kv_demand": 4 * nnz + demanded + 2 * tensor + BH * wl.P * ((shape.nb + 31) // 32) * 4,
         "reorder_out": 2 * tensor,
     }
     hbm = {}
