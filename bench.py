@@ -196,19 +196,16 @@ def main():
     import torch.distributed as dist
 
     import block_sparse_attention_token_gb300 as sp
+    from block_sparse_attention_token_gb300 import replicas
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank, local, world = replicas.rank_world()
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device")
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
-    def barrier():
-        if world > 1:
-            dist.barrier()
+    barrier = replicas.barrier
 
     data = synth.make(wl)
     shape = sp.shape_of(wl)
@@ -272,15 +269,12 @@ def main():
         prev = ev
     stage_ms = {k: v / args.steps for k, v in stage_ms.items()}
     ms_step = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = replicas.max_over_ranks(ms_step)
 
     pk = peaks()
     f_fwd = attn_flops(nnz, wl)
     f_step = f_fwd + (bwd_flops(nnz, wl) if wl.backward else 0.0)
-    value = world * f_step / (ms_step * 1e-3) / 1e12
+    value = replicas.whole_job_rate(f_step, ms_step, world) / 1e12
     attn_ms = stage_ms["attn_fwd"]
     achieved = f_fwd / (attn_ms * 1e-3) / 1e12
     peak = pk["bf16_tflops_sustained"]
@@ -363,11 +357,8 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / args.steps
-        if world > 1:
-            t = torch.tensor([e2e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * f_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+        e2e_ms = replicas.max_over_ranks(e2e_ms)
+        e2e = {"value": replicas.whole_job_rate(f_step, e2e_ms, world) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "copies": "overlapped with neighbouring steps (HostPipeline)"}
 
