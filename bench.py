@@ -48,6 +48,13 @@ def peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+# DRAM bytes (read + write) per launch of the tcgen05 forward kernel, from an ncu capture of the
+# Wan-layer shape with 8 of its 40 heads (236.5 MB: Q, K, V read once, O written), scaled by the
+# heads a full launch processes; the traffic grows with the heads, each head's tiles being
+# independent. The algorithmic bytes are Q + K + V + O + LSE = 1,263 MB.
+ATTN_TRAFFIC = {"wan14b-layer-30k-bf16": 236.5e6 * 40 / 8}
+
+
 def attn_flops(nnz: int, wl) -> float:
     """Algorithmic forward flops over the selected blocks: QK^T and PV, 2 flops per MAC."""
     return 4.0 * nnz * wl.Bt * wl.Bt * wl.d
@@ -280,7 +287,7 @@ def main():
     peak = pk["bf16_tflops_sustained"]
     roofline = {"bound": "tensor", "kernel": "attn_fwd", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "peak_kind": f"bf16 sustained ({pk['source']})",
-                "frac_of_burst": achieved / pk["bf16_tflops"], "traffic": None,
+                "frac_of_burst": achieved / pk["bf16_tflops"], "traffic": ATTN_TRAFFIC.get(wl.name) if not args.portable else None,
                 "work": f"4*nnz*Bt^2*d = {f_fwd:.4g} flop per launch (nnz={nnz})"}
     if wl.backward:
         roofline["bwd_achieved"] = bwd_flops(nnz, wl) / (stage_ms["attn_bwd"] * 1e-3) / 1e12
