@@ -102,6 +102,7 @@ _SIG = {
                                ctypes.c_size_t, ctypes.c_uint32, _P, _P, _P]),
     "sparsp_csr_transpose": (_I32, [_P, _P, _P, _P, _P, _P, _P]),
     "sparsp_diag_umma_tile": (_I32, [_P, _P, _P, _I32, _I32, _I32, _P]),
+    "sparsp_diag_wait_timeout": (_I32, [ctypes.c_uint64, _P, _P]),
 }
 
 
@@ -418,6 +419,12 @@ def diag_umma_tile(a: torch.Tensor, b: torch.Tensor, mode: int, lbo: int = 16384
     _check("sparsp_diag_umma_tile", lib().sparsp_diag_umma_tile(_ptr(a), _ptr(b), _ptr(d), int(mode), int(lbo),
                                                                 int(sbo), _stream(stream)))
     return d
+
+
+def diag_wait_timeout(limit_ns: int, status: torch.Tensor, stream=None) -> None:
+    """Runs the tensor-core kernels' bounded wait on a barrier nothing completes
+    (include/sparsp_diag.h); *status receives SPARSP_ERR_TIMEOUT after limit_ns."""
+    _check("sparsp_diag_wait_timeout", lib().sparsp_diag_wait_timeout(int(limit_ns), _ptr(status), _stream(stream)))
 
 
 def default_scale(d: int) -> float:

@@ -21,7 +21,7 @@ diag_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUte
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sA = base, sB = base + kTile, bar_ld = base + 4 * kTile, bar_mma = bar_ld + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + 4 * kTile + 16);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     mbar_init(bar_ld, 1);
     mbar_init(bar_mma, 1);
@@ -95,8 +95,31 @@ diag_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUte
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// One warp waits, with the attention kernels' bounded wait, on phase 0 of a
+// barrier that expects one arrival nobody makes.
+__global__ void __launch_bounds__(32, 1) wait_timeout_kernel(uint64_t limit_ns, int32_t* d_status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const Guard g{&abort_flag, d_status, limit_ns};
+  wait_warp(smem_u32(&bar), 0u, g);
+}
+
 }  // namespace
 }  // namespace sparsp
+
+extern "C" sparsp_status_t sparsp_diag_wait_timeout(uint64_t limit_ns, int32_t* d_status, sparsp_stream_t stream) {
+  using namespace sparsp;
+  if (d_status == nullptr || ((uintptr_t)d_status & 3u)) return SPARSP_ERR_INVALID_ARG;
+  if (limit_ns < 1000000ull || limit_ns > 5000000000ull) return SPARSP_ERR_INVALID_ARG;
+  wait_timeout_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(limit_ns, d_status);
+  return cudaGetLastError() == cudaSuccess ? SPARSP_OK : SPARSP_ERR_CUDA;
+}
 
 extern "C" sparsp_status_t sparsp_diag_umma_tile(const void* a, const void* b, float* d, int32_t mode,
                                                  int32_t lbo, int32_t sbo, sparsp_stream_t stream) {

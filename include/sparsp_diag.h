@@ -28,6 +28,17 @@ extern "C" {
 SPARSP_API sparsp_status_t sparsp_diag_umma_tile(const void* a, const void* b, float* d, int32_t mode,
                                                  int32_t lbo, int32_t sbo, sparsp_stream_t stream);
 
+/*
+ * The bounded-wait path of the tensor-core kernels, exercised on purpose: one
+ * CTA waits, through the same bounded mbarrier wait the attention kernels use,
+ * on a barrier phase that nothing completes. After limit_ns nanoseconds
+ * (1e6 <= limit_ns <= 5e9, else SPARSP_ERR_INVALID_ARG) the wait gives up,
+ * SPARSP_ERR_TIMEOUT is written to *d_status (device int32, required) and the
+ * kernel returns normally, so the context stays usable. No fault, trap or
+ * unbounded wait is involved.
+ */
+SPARSP_API sparsp_status_t sparsp_diag_wait_timeout(uint64_t limit_ns, int32_t* d_status, sparsp_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -153,6 +153,10 @@ def test_call_validation_codes(lib):
                                     needp, None) == sp.INVALID_ARG
     assert lib.sparsp_predictor_fit(S, 16, FAKE, FAKE, FAKE, FAKE, f(0.1), None, None, None, FAKE, needp - 1,
                                     None) == sp.WORKSPACE
+    # bounded-wait diagnostic: limit out of range, missing status word
+    assert lib.sparsp_diag_wait_timeout(10, FAKE, None) == sp.INVALID_ARG
+    assert lib.sparsp_diag_wait_timeout(10_000_000_000, FAKE, None) == sp.INVALID_ARG
+    assert lib.sparsp_diag_wait_timeout(50_000_000, None, None) == sp.INVALID_ARG
     # attention: NaN scale, small workspace, misaligned optional pointer, fp32 backward
     p7 = (FAKE,) * 5
     assert lib.sparsp_attn_fwd(S, *p7, f(float("nan")), FAKE, FAKE, FAKE, 1 << 30, 0, None, None,
