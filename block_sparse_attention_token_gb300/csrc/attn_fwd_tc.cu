@@ -374,10 +374,12 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 #pragma unroll
         for (int u = 0; u < 8; ++u) part[u] = __uint_as_float(s[u]);
 #pragma unroll
-        for (int c = 8; c < 128; c += 16)
+        for (int c = 8; c + 16 <= 128; c += 16)
 #pragma unroll
           for (int u = 0; u < 8; ++u)
             part[u] = fmax3(part[u], __uint_as_float(s[c + u]), __uint_as_float(s[c + 8 + u]));
+#pragma unroll
+        for (int u = 0; u < 8; ++u) part[u] = fmaxf(part[u], __uint_as_float(s[120 + u]));
         const float mx = fmax3(fmax3(part[0], part[1], part[2]), fmax3(part[3], part[4], part[5]),
                                fmaxf(part[6], part[7]));
         const float m_new = fmaxf(m, mx * sl2);
