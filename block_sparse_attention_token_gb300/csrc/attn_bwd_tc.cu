@@ -527,7 +527,7 @@ sparsp_status_t go(const Dims& s, const CUtensorMap& a1, const CUtensorMap& a2, 
 
 }  // namespace
 
-bool attn_bwd_tc_supported(const Dims& s) { return attn_fwd_tc_supported(s); }
+bool attn_bwd_tc_supported(const Dims& s) { return s.Bt == 128 && s.d == 128 && attn_fwd_tc_supported(s); }
 
 sparsp_status_t launch_attn_bwd_tc(const Dims& s, int mode, const __nv_bfloat16* q,
                                    const __nv_bfloat16* k, const __nv_bfloat16* v,

@@ -1,5 +1,7 @@
-// Step 5a, bf16, Bt = d = 128 on sm_103a: block-sparse flash-attention forward
-// on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+// Step 5a, bf16, Bt and d in {64, 128} on sm_103a: block-sparse flash-attention
+// forward on the 5th-generation tensor cores (tcgen05 + TMEM + TMA). The query
+// tile is always the MMA's 128 rows; with 64-token blocks its second half holds
+// the next block's rows, computed and not stored.
 //
 // One persistent CTA per SM, 7 warps:
 //   warp 4     producer: pulls (b, h, query block) items longest-first through
@@ -35,22 +37,31 @@ namespace {
 
 using namespace tc;
 
-constexpr int BT = 128, D = 128;
 constexpr int kNK = 3, kNV = 3, kNI = 4;
-constexpr uint32_t kTile = BT * D * 2;      // 32 KB
-constexpr uint32_t kHalfTile = BT * 64 * 2; // one 64-column swizzled box: 16 KB
 constexpr int kThreads = 224;   // 4 softmax warps, producer, S issuer, PV issuer
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
-constexpr uint32_t kOffK = kTile, kOffV = kOffK + kNK * kTile, kOffBar = kOffV + kNV * kTile;
 enum Bar {
   Q_FULL = 0, Q_EMPTY, K_FULL, K_EMPTY = K_FULL + kNK, V_FULL = K_EMPTY + kNK, V_EMPTY = V_FULL + kNV,
   S_FULL = V_EMPTY + kNV, S_FREE = S_FULL + 2, P_FULL = S_FREE + 2, PV_DONE = P_FULL + 2, O_FULL = PV_DONE + 2,
   O_EMPTY,
   I_FULL, I_EMPTY = I_FULL + kNI, TEAR = I_EMPTY + kNI, TEAR_PV, NBAR
 };
-constexpr uint32_t kOffRing = kOffBar + 8 * NBAR;
-constexpr uint32_t kOffMisc = kOffRing + 8 * kNI;
-constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
+// Tile geometry for key blocks of BT tokens and head dimension D. The query
+// tile is always 128 rows (the MMA's M; the 128 TMEM lanes): with BT = 64 the
+// rows past the block belong to the next block (or are zero past the tensor's
+// end), are computed and never stored. Tiles are TMA'd as 64-column boxes of
+// 128-byte rows with 128-byte swizzle.
+template <int BT_, int D_>
+struct Cfg {
+  static constexpr int BT = BT_, D = D_, QR = 128;
+  static constexpr int NBOX = D / 64;                     // 64-column boxes per row tile
+  static constexpr uint32_t kQBox = QR * 128, kKBox = BT * 128;
+  static constexpr uint32_t kQTile = kQBox * NBOX, kKTile = kKBox * NBOX;
+  static constexpr uint32_t kOffK = kQTile, kOffV = kOffK + kNK * kKTile, kOffBar = kOffV + kNV * kKTile;
+  static constexpr uint32_t kOffRing = kOffBar + 8 * NBAR;
+  static constexpr uint32_t kOffMisc = kOffRing + 8 * kNI;
+  static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
+};
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
@@ -94,6 +105,7 @@ struct Params {
   int32_t* d_status;
 };
 
+template <int BT, int D>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const Params p) {
@@ -101,11 +113,12 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t sQ = base, sK = base + kOffK, sV = base + kOffV;
-  auto bar = [&](int idx) -> uint32_t { return base + kOffBar + 8u * (uint32_t)idx; };
-  volatile int2* ring = reinterpret_cast<volatile int2*>(gbase + kOffRing);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kOffMisc);
-  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + kOffMisc + 4);
+  using C = Cfg<BT, D>;
+  const uint32_t sQ = base, sK = base + C::kOffK, sV = base + C::kOffV;
+  auto bar = [&](int idx) -> uint32_t { return base + C::kOffBar + 8u * (uint32_t)idx; };
+  volatile int2* ring = reinterpret_cast<volatile int2*>(gbase + C::kOffRing);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + C::kOffMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t t_start = globaltimer_ns();
 
@@ -195,9 +208,9 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       const int32_t yq = (int32_t)(bh * p.N + (int64_t)i * BT);
       if (!wait_warp(bar(Q_EMPTY), (q_fill & 1u) ^ 1u, g)) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar(Q_FULL), kTile);
-        tma_load_2d(sQ, &tq, bar(Q_FULL), 0, yq);
-        tma_load_2d(sQ + kHalfTile, &tq, bar(Q_FULL), 64, yq);
+        mbar_arrive_expect_tx(bar(Q_FULL), C::kQTile);
+#pragma unroll
+        for (int h = 0; h < C::NBOX; ++h) tma_load_2d(sQ + h * C::kQBox, &tq, bar(Q_FULL), 64 * h, yq);
       }
       ++q_fill;
       const int32_t e0 = p.row_ptr[item];
@@ -208,17 +221,19 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         const uint32_t ks = k_fill % kNK;
         if (!(ok = wait_warp(bar(K_EMPTY + ks), ((k_fill / kNK) & 1u) ^ 1u, g))) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar(K_FULL + ks), kTile);
-          tma_load_2d(sK + ks * kTile, &tk, bar(K_FULL + ks), 0, yk);
-          tma_load_2d(sK + ks * kTile + kHalfTile, &tk, bar(K_FULL + ks), 64, yk);
+          mbar_arrive_expect_tx(bar(K_FULL + ks), C::kKTile);
+#pragma unroll
+          for (int h = 0; h < C::NBOX; ++h)
+            tma_load_2d(sK + ks * C::kKTile + h * C::kKBox, &tk, bar(K_FULL + ks), 64 * h, yk);
         }
         ++k_fill;
         const uint32_t vs = v_fill % kNV;
         if (!(ok = wait_warp(bar(V_EMPTY + vs), ((v_fill / kNV) & 1u) ^ 1u, g))) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar(V_FULL + vs), kTile);
-          tma_load_2d(sV + vs * kTile, &tv, bar(V_FULL + vs), 0, yk);
-          tma_load_2d(sV + vs * kTile + kHalfTile, &tv, bar(V_FULL + vs), 64, yk);
+          mbar_arrive_expect_tx(bar(V_FULL + vs), C::kKTile);
+#pragma unroll
+          for (int h = 0; h < C::NBOX; ++h)
+            tma_load_2d(sV + vs * C::kKTile + h * C::kKBox, &tv, bar(V_FULL + vs), 64 * h, yk);
         }
         ++v_fill;
       }
@@ -234,7 +249,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ S = Q K^T issuer
-    constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
+    constexpr uint32_t idS = idesc_bf16(128, BT, 0, 0);
     uint32_t it_use = 0, q_use = 0, k_use = 0, s_issue = 0;
     bool issued_any = false;
     for (;;) {
@@ -255,13 +270,15 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         if (!(ok = wait_warp(bar(S_FREE + b), ((s_issue >> 1) & 1u) ^ 1u, g))) break;
         if (!(ok = wait_warp(bar(K_FULL + ks), (k_use / kNK) & 1u, g))) break;
         fence_after();
-        const uint32_t kb = sK + ks * kTile;
+        const uint32_t kb = sK + ks * C::kKTile;
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
-            mma_ss(tmem + kColS + b * 128u, smem_desc(sQ + off, 16, 1024, kSwizzle128B),
-                   smem_desc(kb + off, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
+            // k-step kk: 16 columns = 32 bytes into the row, in box kk / 4
+            const uint32_t offq = (uint32_t)(kk >> 2) * C::kQBox + (uint32_t)(kk & 3) * 32u;
+            const uint32_t offk = (uint32_t)(kk >> 2) * C::kKBox + (uint32_t)(kk & 3) * 32u;
+            mma_ss(tmem + kColS + b * 128u, smem_desc(sQ + offq, 16, 1024, kSwizzle128B),
+                   smem_desc(kb + offk, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
           }
           commit(bar(S_FULL + b));
           commit(bar(K_EMPTY + ks));
@@ -282,7 +299,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     __syncwarp();
   } else if (warp == 6) {
     // ------------------------------------------------------------ O += P V issuer
-    constexpr uint32_t idO = idesc_bf16(128, 128, 0, 1);
+    constexpr uint32_t idO = idesc_bf16(128, D, 0, 1);
     uint32_t it_use = 0, v_use = 0, pv = 0, o_items = 0;
     bool issued_any = false;
     for (;;) {
@@ -302,12 +319,12 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         if (!(ok = wait_warp(bar(P_FULL + b), (pv >> 1) & 1u, g))) break;
         if (e == 0 && !(ok = wait_warp(bar(O_EMPTY), (o_items & 1u) ^ 1u, g))) break;
         fence_after();
-        const uint32_t vb = sV + vs * kTile;
+        const uint32_t vb = sV + vs * C::kKTile;
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < BT / 16; ++kk)
             mma_ts(tmem + kColO, tmem + kColP + b * 64u + (uint32_t)kk * 8u,
-                   smem_desc(vb + (uint32_t)kk * 2048u, 16384, 1024, kSwizzle128B), idO,
+                   smem_desc(vb + (uint32_t)kk * 2048u, C::kKBox, 1024, kSwizzle128B), idO,
                    (e > 0 || kk > 0) ? 1u : 0u);
           commit(bar(V_EMPTY + vs));
           commit(bar(PV_DONE + b));
@@ -347,12 +364,15 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       const int64_t bh = item / nb;
       const int i = (int)(item % nb);
       const int64_t row = bh * p.N + (int64_t)i * BT + threadIdx.x;
+      const bool stores = threadIdx.x < BT;   // rows past the block are computed, never stored
       uint4* orow = reinterpret_cast<uint4*>(p.o + row * D);
       const int len = ent.y;
       if (len == 0) {
+        if (stores) {
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
-        p.lse[row] = -INFINITY;
+          for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
+          p.lse[row] = -INFINITY;
+        }
         continue;
       }
       float m = -INFINITY, l = 0.f;
@@ -361,9 +381,9 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         const uint32_t b = s_use & 1u;
         if (!(ok = wait_warp(bar(S_FULL + b), (s_use >> 1) & 1u, g))) break;
         fence_after();
-        uint32_t s[128];
+        uint32_t s[BT];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(t_row + kColS + b * 128u + c * 32u, s + 32 * c);
+        for (int c = 0; c < BT / 32; ++c) tmem_ld32(t_row + kColS + b * 128u + c * 32u, s + 32 * c);
         wait_ld();
         fence_before();
         mbar_arrive(bar(S_FREE + b));
@@ -374,12 +394,12 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 #pragma unroll
         for (int u = 0; u < 8; ++u) part[u] = __uint_as_float(s[u]);
 #pragma unroll
-        for (int c = 8; c + 16 <= 128; c += 16)
+        for (int c = 8; c + 16 <= BT; c += 16)
 #pragma unroll
           for (int u = 0; u < 8; ++u)
             part[u] = fmax3(part[u], __uint_as_float(s[c + u]), __uint_as_float(s[c + 8 + u]));
 #pragma unroll
-        for (int u = 0; u < 8; ++u) part[u] = fmaxf(part[u], __uint_as_float(s[120 + u]));
+        for (int u = 0; u < 8; ++u) part[u] = fmaxf(part[u], __uint_as_float(s[BT - 8 + u]));
         const float mx = fmax3(fmax3(part[0], part[1], part[2]), fmax3(part[3], part[4], part[5]),
                                fmaxf(part[6], part[7]));
         const float m_new = fmaxf(m, mx * sl2);
@@ -392,7 +412,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           fence_after();
           const float f = ex2f(m - m_new);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
             tmem_ld32(t_row + kColO + c * 32u, o);
             wait_ld();
@@ -404,12 +424,12 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           l *= f;
           m = m_new;
         }
-        uint32_t pk[64];
+        uint32_t pk[BT / 2];
         float rs[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) rs[u] = 0.f;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
+        for (int c = 0; c < BT / 2; ++c) {
           const float p0 = ex2f(fmaf(__uint_as_float(s[2 * c]), sl2, -m));
           const float p1 = ex2f(fmaf(__uint_as_float(s[2 * c + 1]), sl2, -m));
           rs[c & 7] += p0 + p1;
@@ -422,8 +442,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           if (!(ok = wait_warp(bar(PV_DONE + b), (uint32_t)(((gb - 2) >> 1) & 1u), g))) break;
           fence_after();
         }
-        tmem_st32(t_row + kColP + b * 64u, pk);
-        tmem_st32(t_row + kColP + b * 64u + 32u, pk + 32);
+#pragma unroll
+        for (int c = 0; c < BT / 64; ++c) tmem_st32(t_row + kColP + b * 64u + 32u * c, pk + 32 * c);
         wait_st();
         fence_before();
         mbar_arrive(bar(P_FULL + b));
@@ -435,10 +455,11 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       fence_after();
       const float inv = 1.0f / l;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(t_row + kColO + c * 32u, o);
         wait_ld();
+        if (!stores) continue;
         uint32_t w[16];
 #pragma unroll
         for (int x = 0; x < 16; ++x)
@@ -448,7 +469,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       }
       fence_before();
       mbar_arrive(bar(O_EMPTY));
-      p.lse[row] = (m + log2f(l)) * 0.69314718055994531f;
+      if (stores) p.lse[row] = (m + log2f(l)) * 0.69314718055994531f;
     }
   }
 
@@ -464,13 +485,34 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 }  // namespace
 
 bool attn_fwd_tc_supported(const Dims& s) {
-  if (s.dtype != SPARSP_BF16 || s.Bt != 128 || s.d != 128) return false;
+  if (s.dtype != SPARSP_BF16 || (s.Bt != 64 && s.Bt != 128) || (s.d != 64 && s.d != 128)) return false;
   if ((int64_t)s.B * s.H * s.N >= (int64_t)1 << 31) return false;
   int dev = 0, major = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return false;
   return major == 10;
 }
+
+namespace {
+
+template <int BT, int D>
+sparsp_status_t go_fwd(const Dims& s, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const Params& prm, cudaStream_t st) {
+  using C = Cfg<BT, D>;
+  auto kern = attn_fwd_tc_kernel<BT, D>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes) != cudaSuccess)
+    return SPARSP_ERR_CUDA;
+  const int sms = device_sm_count();
+  if (sms <= 0) return SPARSP_ERR_CUDA;
+  int64_t grid = sms;
+  if (grid > s.rows()) grid = s.rows();
+  if (grid < 1) grid = 1;
+  kern<<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, prm);
+  SPARSP_LAUNCH_CHECK();
+  return SPARSP_OK;
+}
+
+}  // namespace
 
 sparsp_status_t launch_attn_fwd_tc(const Dims& s, const __nv_bfloat16* q, const __nv_bfloat16* k,
                                    const __nv_bfloat16* v, const int32_t* row_ptr,
@@ -479,22 +521,18 @@ sparsp_status_t launch_attn_fwd_tc(const Dims& s, const __nv_bfloat16* q, const 
                                    uint64_t* prof, int32_t* d_status, cudaStream_t st) {
   const uint64_t rows = (uint64_t)s.B * s.H * s.N;
   CUtensorMap tq, tk, tv;
-  if (!make_tmap_bf16_rows(&tq, q, rows, D, BT) || !make_tmap_bf16_rows(&tk, k, rows, D, BT) ||
-      !make_tmap_bf16_rows(&tv, v, rows, D, BT))
+  // Q boxes are 128 rows (the MMA's M) whatever the block size; K and V boxes one block
+  if (!make_tmap_bf16_rows(&tq, q, rows, (uint64_t)s.d, 128) ||
+      !make_tmap_bf16_rows(&tk, k, rows, (uint64_t)s.d, (uint32_t)s.Bt) ||
+      !make_tmap_bf16_rows(&tv, v, rows, (uint64_t)s.d, (uint32_t)s.Bt))
     return SPARSP_ERR_CUDA;
-  if (cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kSmemBytes) != cudaSuccess)
-    return SPARSP_ERR_CUDA;
-  const int sms = device_sm_count();
-  if (sms <= 0) return SPARSP_ERR_CUDA;
-  int64_t grid = sms;
-  if (grid > s.rows()) grid = s.rows();
-  if (grid < 1) grid = 1;
   Params prm{row_ptr, col_idx, s.N, s.nb, s.rows(), scale * 1.4426950408889634f, o, lse, items,
              counter, prof, d_status};
-  attn_fwd_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, prm);
-  SPARSP_LAUNCH_CHECK();
-  return SPARSP_OK;
+  if (s.Bt == 128 && s.d == 128) return go_fwd<128, 128>(s, tq, tk, tv, prm, st);
+  if (s.Bt == 128 && s.d == 64) return go_fwd<128, 64>(s, tq, tk, tv, prm, st);
+  if (s.Bt == 64 && s.d == 128) return go_fwd<64, 128>(s, tq, tk, tv, prm, st);
+  if (s.Bt == 64 && s.d == 64) return go_fwd<64, 64>(s, tq, tk, tv, prm, st);
+  return SPARSP_ERR_UNSUPPORTED;
 }
 
 }  // namespace sparsp

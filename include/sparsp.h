@@ -348,9 +348,9 @@ SPARSP_API sparsp_status_t sparsp_lpt_schedule(const sparsp_shape_t* shape, cons
  * q, k, v, o: blocked [B,H,N,d]; lse: float32 [B,H,N]. scale <= 0 means
  * 1/sqrt(d). An empty row gives O = 0, LSE = -inf. A row with an index outside
  * [0, nb) or more than nb entries sets SPARSP_ERR_DATA and is skipped.
- * bf16 on sm_103a with Bt = d = 128 runs the tcgen05/TMEM/TMA kernel;
- * otherwise (or with SPARSP_KERNEL_PORTABLE) an mma.sync kernel; float32 runs
- * an fp32 FFMA kernel. Work items are pulled longest-first by persistent CTAs.
+ * bf16 on sm_103a runs the tcgen05/TMEM/TMA kernel (Bt and d in {64, 128});
+ * with SPARSP_KERNEL_PORTABLE an mma.sync kernel; float32 runs an fp32 FFMA
+ * kernel. Work items are pulled longest-first by persistent CTAs.
  * prof: NULL or uint64 [SPARSP_PROF_SLOTS], caller-zeroed; receives per-SM busy
  * nanoseconds (index = SM id).
  * ws: at least sparsp_attn_workspace_size(shape, 0) bytes.
