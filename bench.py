@@ -150,6 +150,13 @@ def cpu_baseline(wl, data, budget_s: float = 12.0) -> dict:
             "seconds": dt}
 
 
+def static_config(wl) -> dict:
+    """The workload's own keys, shared by both arms' config."""
+    return {"workload": wl.name, "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d, "tile": [wl.ta, wl.tb, wl.tc],
+            "nb": wl.nb, "estimator": wl.estimator, "top_p": wl.top_p, "k_floor": wl.k_floor, "P": wl.P,
+            "backward": wl.backward}
+
+
 def run_reference(args, wl):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -166,7 +173,7 @@ def run_reference(args, wl):
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / len(timed),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": wl.name, "parallelism": "host cores"},
+            "data": "synthetic", "config": {**static_config(wl), "parallelism": "host cores"},
             "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cb["cores"], "kind": "oracle",
                              "sample": cb["sample"]},
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -456,9 +463,7 @@ def main():
         "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
         "pct_of_peak": 100.0 * value / world / peak,
         "tokens_per_s": world * wl.B * wl.N / (ms_step * 1e-3),
-        "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d, "tile": [wl.ta, wl.tb, wl.tc],
-                   "nb": shape.nb, "estimator": wl.estimator, "top_p": wl.top_p, "k_floor": wl.k_floor, "P": wl.P,
-                   "backward": wl.backward, "nnz_blocks": nnz, "density": nnz / (shape.rows * shape.nb),
+        "config": {**static_config(wl), "nnz_blocks": nnz, "density": nnz / (shape.rows * shape.nb),
                    "row_len_min_max": [int(counts.min()), int(counts.max())],
                    "schedule": "flat" if args.flat else "head-grouped longest-first",
                    "kernel": "portable mma.sync" if args.portable else "default",
