@@ -10,12 +10,17 @@
 //  aug_keys_kernel - one warp per CSR row: each unselected block's value
 //                    v = fl32(e_j / Z) (e_j = expf(S_j - max) in fp32, Z summed
 //                    in fp64), stored as the orderable key bits(v) + 1; selected
-//                    blocks get key 0. Also writes the row's base count.
-//  aug_rank_kernel - one CTA per (batch element, rank): slack = L* - L_r; a
-//                    4-pass radix select finds the key T of the slack-th best
-//                    candidate; keys above T are taken, and of the keys equal to
-//                    T the first ones in (row, block) order. Writes each row's
-//                    new count and its share of the ties.
+//                    blocks get key 0. Also writes the row's base count. Rows
+//                    of ranks without slack get no keys (nothing is read there).
+//  aug_slack/count/hist/digit kernels - per (batch element, rank): slack =
+//                    L* - L_r; candidates and the 8-bit digit histograms of a
+//                    4-pass radix select are accumulated over all the rank's
+//                    heads by CTAs of (head, key range); one CTA per rank fixes
+//                    each digit. The result is the key T of the slack-th best
+//                    candidate: keys above T are taken, and of the keys equal to
+//                    T the first ones in (row, block) order.
+//  aug_rowcount/tie kernels - each row's keys above T (one warp per row), and
+//                    the ties shared out in (head, row) order where there are any.
 //  scan            - counts -> row offsets.
 //  aug_fill_kernel - one warp per row merges the selected and the added blocks
 //                    in ascending order.
@@ -114,12 +119,31 @@ balance_kernel(const int32_t* __restrict__ row_ptr, int H, int nb, int P, int ma
 
 // --------------------------------------------------------------- augmentation
 
+constexpr int kRankThreads = 1024;
+constexpr int kRankWarps = kRankThreads / 32;
+constexpr int kKeysPerCta = 8192;   // key range of one CTA of a histogram pass
+
+struct RankOut {
+  uint32_t T;        // keys > T are taken
+  uint32_t pad;
+  int64_t need_eq;   // and this many keys == T, first in (head, row, block) order
+};
+
+// Selection state of one (batch element, rank), in the workspace.
+struct RankState {
+  unsigned long long slack;   // L* - L_r
+  unsigned long long rem;     // rank of the cut among the keys matching prefix
+  uint32_t prefix, mask;      // digits fixed so far
+  int32_t done, pad;
+};
+
 constexpr int kMaxWords = 32;   // nb <= 1024
 
 __global__ void __launch_bounds__(256)
 aug_keys_kernel(const float* __restrict__ scores, const int32_t* __restrict__ row_ptr,
-                const int32_t* __restrict__ col_idx, int nb, int64_t rows, uint32_t* __restrict__ keys,
-                int32_t* __restrict__ counts, int32_t* d_status) {
+                const int32_t* __restrict__ col_idx, const int32_t* __restrict__ head_rank,
+                const RankState* __restrict__ state, int H, int nb, int P, int64_t rows,
+                uint32_t* __restrict__ keys, int32_t* __restrict__ counts, int32_t* d_status) {
   __shared__ uint32_t bits_all[8][kMaxWords];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * 8 + warp;
@@ -145,6 +169,10 @@ aug_keys_kernel(const float* __restrict__ scores, const int32_t* __restrict__ ro
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) sel += __shfl_xor_sync(0xffffffffu, sel, off);
   if (lane == 0) counts[row] = sel;
+  // rows of a rank without slack (or of no rank) take nothing: no keys
+  const int64_t bh = row / nb;
+  const int q = head_rank[bh];
+  if (q < 0 || q >= P || state[(bh / H) * P + q].slack == 0ull) return;
   const float* S = scores + row * nb;
   uint32_t* K = keys + row * nb;
   float m = -INFINITY;
@@ -166,158 +194,284 @@ aug_keys_kernel(const float* __restrict__ scores, const int32_t* __restrict__ ro
   for (int j = lane; j < nb; j += 32) Z += (double)expf(S[j] - m);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, off);
-  for (int j = lane; j < nb; j += 32) {
-    const bool selected = (bits[j >> 5] >> (j & 31)) & 1u;
+  // Selected blocks get key 0. The candidates are compacted first, so that
+  // the slow double-precision division runs on full warps of them.
+  for (int j = lane; j < nb; j += 32)
+    if ((bits[j >> 5] >> (j & 31)) & 1u) K[j] = 0u;
+  const int words = (nb + 31) >> 5;
+  uint32_t cw = 0u;
+  if (lane < words) {
+    const int tail = nb - lane * 32;
+    cw = ~bits[lane] & (tail >= 32 ? 0xffffffffu : (1u << tail) - 1u);
+  }
+  const int pc = __popc(cw);
+  int incl = pc;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  const int n_cand = __shfl_sync(0xffffffffu, incl, 31);
+  __shared__ int32_t cpre_all[8][32];
+  __shared__ uint32_t cword_all[8][32];
+  int32_t* cpre = cpre_all[warp];
+  uint32_t* cword = cword_all[warp];
+  cpre[lane] = incl - pc;
+  cword[lane] = cw;
+  __syncwarp();
+  for (int c = lane; c < n_cand; c += 32) {
+    int w = 0;   // the last word that starts at or before candidate c
+#pragma unroll
+    for (int step = 16; step > 0; step >>= 1)   // w + step stays <= 31
+      if (cpre[w + step] <= c) w += step;
+    uint32_t x = cword[w];
+    for (int n = c - cpre[w]; n > 0; --n) x &= x - 1u;   // drop the lower candidates of the word
+    const int j = w * 32 + __ffs(x) - 1;
     const float v = (float)((double)expf(S[j] - m) / Z);
-    K[j] = selected ? 0u : __float_as_uint(v) + 1u;
+    K[j] = __float_as_uint(v) + 1u;
   }
 }
 
-constexpr int kRankThreads = 1024;
-constexpr int kRankWarps = kRankThreads / 32;
-constexpr int kHist = 16;        // histogram copies (two warps share one)
-
-struct RankOut {
-  uint32_t T;        // keys > T are taken
-  int32_t need_eq;   // and this many keys == T, first in (row, block) order
-};
-
+// One CTA per batch element: rank loads, slack, fresh selection state and
+// cleared histograms. A rank without slack is finished here.
 __global__ void __launch_bounds__(kRankThreads)
-aug_rank_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ head_rank, int H, int nb,
-                int P, const uint32_t* __restrict__ keys, int32_t* __restrict__ counts,
-                int32_t* __restrict__ taken, RankOut* __restrict__ rank_out, int64_t* __restrict__ added,
-                int32_t* d_status) {
+aug_slack_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ head_rank, int H, int nb, int P,
+                 RankState* __restrict__ state, RankOut* __restrict__ rank_out, int64_t* __restrict__ added,
+                 unsigned long long* __restrict__ hist, int32_t* d_status) {
   __shared__ unsigned long long load[kMaxHeads];
-  __shared__ int32_t heads[kMaxHeads];
-  __shared__ int32_t hist[kHist][256];
-  __shared__ int32_t eqs[kRankWarps];
   __shared__ unsigned long long red[32];
-  __shared__ int n_heads, s_digit, s_rem;
-  __shared__ unsigned long long s_ncand;
-  const int b = blockIdx.x / P, r = blockIdx.x % P;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int q = tid; q < P; q += kRankThreads) load[q] = 0ull;
-  if (tid == 0) s_ncand = 0ull;
+  const int b = blockIdx.x;
+  for (int q = threadIdx.x; q < P; q += kRankThreads) load[q] = 0ull;
+  for (int i = threadIdx.x; i < P * 256; i += kRankThreads) hist[(int64_t)b * P * 256 + i] = 0ull;
   __syncthreads();
-  for (int h = tid; h < H; h += kRankThreads) {
+  for (int h = threadIdx.x; h < H; h += kRankThreads) {
     const int q = head_rank[(int64_t)b * H + h];
     if (q < 0 || q >= P) {
-      if (r == 0) report(d_status, SPARSP_ERR_DATA);
+      report(d_status, SPARSP_ERR_DATA);
       continue;
     }
     atomicAdd(&load[q], (unsigned long long)head_cost(row_ptr, (int64_t)b * H + h, nb));
   }
-  if (tid == 0) {   // this rank's heads, ascending
-    int n = 0;
-    for (int h = 0; h < H; ++h)
-      if (head_rank[(int64_t)b * H + h] == r) heads[n++] = h;
-    n_heads = n;
-  }
   __syncthreads();
   unsigned long long top = 0ull;
-  for (int q = tid; q < P; q += kRankThreads) top = load[q] > top ? load[q] : top;
+  for (int q = threadIdx.x; q < P; q += kRankThreads) top = load[q] > top ? load[q] : top;
   top = ~block_min(~top, red);
-  const unsigned long long slack = top - load[r];
-  const int nh = n_heads;
-  const int per_head = nb * nb;
-  // candidates
-  unsigned long long nc = 0ull;
-  for (int hh = 0; hh < nh; ++hh) {
-    const uint32_t* K = keys + ((int64_t)b * H + heads[hh]) * per_head;
-    for (int e = tid; e < per_head; e += kRankThreads) nc += K[e] != 0u;
+  for (int q = threadIdx.x; q < P; q += kRankThreads) {
+    const int64_t br = (int64_t)b * P + q;
+    const unsigned long long slack = top - load[q];
+    state[br] = RankState{slack, 0ull, 0u, 0u, slack == 0ull, 0};
+    if (slack == 0ull) {
+      rank_out[br] = RankOut{0xffffffffu, 0u, 0};
+      if (added != nullptr) added[br] = 0;
+    }
+  }
+}
+
+// grid (b*H + h, key range): histogram of the 8-bit digit at `shift` of the
+// head's nonzero keys that match its rank's prefix, added into the rank's
+// global histogram.
+__global__ void __launch_bounds__(256)
+aug_hist_kernel(const int32_t* __restrict__ head_rank, int H, int P, int nb, const uint32_t* __restrict__ keys,
+                const RankState* __restrict__ state, unsigned long long* __restrict__ hist, int shift) {
+  __shared__ int32_t h2[2][256];
+  const int64_t bh = blockIdx.x;
+  const int q = head_rank[bh];
+  if (q < 0 || q >= P) return;
+  const int64_t br = (bh / H) * P + q;
+  const RankState st = state[br];
+  if (st.done) return;
+  h2[0][threadIdx.x] = 0;
+  h2[1][threadIdx.x] = 0;
+  __syncthreads();
+  const int64_t per_head = (int64_t)nb * nb;
+  const int64_t e0 = (int64_t)blockIdx.y * kKeysPerCta;
+  const int64_t e1 = e0 + kKeysPerCta < per_head ? e0 + kKeysPerCta : per_head;
+  const uint32_t* K = keys + bh * per_head;
+  int32_t* mine = h2[(threadIdx.x >> 5) & 1];
+  for (int64_t e = e0 + threadIdx.x; e < e1; e += 256) {
+    const uint32_t k = K[e];
+    if (k != 0u && (k & st.mask) == st.prefix) atomicAdd(&mine[(k >> shift) & 255u], 1);
+  }
+  __syncthreads();
+  const int c = h2[0][threadIdx.x] + h2[1][threadIdx.x];
+  if (c) atomicAdd(&hist[br * 256 + threadIdx.x], (unsigned long long)c);
+}
+
+// One CTA of 256 threads per (batch element, rank): fixes the digit at
+// `shift` from the pass's histogram and clears it. The first pass (shift 24,
+// empty prefix) also counts the candidates: a rank whose slack covers them
+// all takes every one (T = 0), one without any takes none.
+__global__ void __launch_bounds__(256)
+aug_digit_kernel(RankState* __restrict__ state, unsigned long long* __restrict__ hist,
+                 RankOut* __restrict__ rank_out, int64_t* __restrict__ added, int shift) {
+  __shared__ unsigned long long warp_sum[8];
+  __shared__ unsigned long long s_rem;
+  __shared__ int s_stop;
+  const int64_t br = blockIdx.x;
+  RankState* st = state + br;
+  const int done0 = st->done;
+  const unsigned long long slack = st->slack;
+  unsigned long long rem = st->rem;
+  __syncthreads();   // every thread has read the state before thread 0 updates it
+  if (done0) return;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  unsigned long long* hh = hist + br * 256;
+  const int d = 255 - t;   // thread t holds digit 255 - t: an inclusive scan gives suffix sums
+  const unsigned long long c = hh[d];
+  unsigned long long incl = c;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const unsigned long long o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  unsigned long long total = 0ull;
+  for (int w = 0; w < 8; ++w) {
+    if (w < warp) incl += warp_sum[w];
+    total += warp_sum[w];
+  }
+  hh[d] = 0ull;   // every thread has read its digit
+  if (t == 0) s_stop = 0;
+  if (shift == 24) {
+    const unsigned long long sel = slack < total ? slack : total;
+    if (t == 0) {
+      if (added != nullptr) added[br] = (int64_t)sel;
+      if (sel == 0ull || sel == total) {
+        rank_out[br] = RankOut{sel == 0ull ? 0xffffffffu : 0u, 0u, 0};
+        st->done = 1;
+        s_stop = 1;
+      }
+    }
+    rem = sel;
+  }
+  __syncthreads();
+  if (s_stop) return;
+  // The cut's digit is the largest d whose suffix sum reaches rem (the suffix
+  // sums grow as d falls, and the one at d = 0 is the total, at least rem).
+  const int reach = __syncthreads_count(incl >= rem);
+  const int dstar = reach - 1;
+  if (d == dstar) s_rem = rem - (incl - c);
+  __syncthreads();
+  if (t == 0) {
+    st->prefix |= (uint32_t)dstar << shift;
+    st->mask |= 255u << shift;
+    st->rem = s_rem;
+    if (shift == 0) {
+      rank_out[br] = RankOut{st->prefix, 0u, (int64_t)s_rem};
+      st->done = 1;
+    }
+  }
+}
+
+// One warp per CSR row: blocks above the rank's cut, and keys equal to it.
+// Without ties to share (need_eq = 0) the row's count is final here.
+__global__ void __launch_bounds__(256)
+aug_rowcount_kernel(const int32_t* __restrict__ head_rank, int H, int P, int nb, int64_t rows,
+                    const uint32_t* __restrict__ keys, const RankOut* __restrict__ rank_out,
+                    int32_t* __restrict__ counts, int32_t* __restrict__ taken, int32_t* __restrict__ gtrow,
+                    int32_t* __restrict__ eqrow) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int64_t bh = row / nb;
+  const int q = head_rank[bh];
+  if (q < 0 || q >= P) {
+    if (lane == 0) taken[row] = 0;
+    return;
+  }
+  const RankOut ro = rank_out[(bh / H) * P + q];
+  const uint32_t* K = keys + row * nb;
+  int gt = 0, eq = 0;
+  if (ro.T != 0xffffffffu) {   // else the rank takes nothing and may have no keys
+    for (int j = lane; j < nb; j += 32) {
+      const uint32_t key = K[j];
+      gt += key > ro.T && key != 0u;
+      eq += key == ro.T && key != 0u;
+    }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) nc += __shfl_xor_sync(0xffffffffu, nc, off);
-  if (lane == 0) atomicAdd(&s_ncand, nc);
-  __syncthreads();
-  const unsigned long long ncand = s_ncand;
-  const unsigned long long s = slack < ncand ? slack : ncand;
-  uint32_t T;
-  int need_eq;
-  if (s == 0ull) {
-    T = 0xffffffffu;
-    need_eq = 0;
-  } else if (s == ncand) {
-    T = 0u;
-    need_eq = 0;
-  } else {
-    uint32_t prefix = 0u, mask = 0u;
-    int rem = (int)s;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int d = tid; d < kHist * 256; d += kRankThreads) hist[d >> 8][d & 255] = 0;
-      __syncthreads();
-      int32_t* my_hist = hist[warp % kHist];
-      for (int hh = 0; hh < nh; ++hh) {
-        const uint32_t* K = keys + ((int64_t)b * H + heads[hh]) * per_head;
-        for (int e = tid; e < per_head; e += kRankThreads) {
-          const uint32_t k = K[e];
-          if (k != 0u && (k & mask) == prefix) atomicAdd(&my_hist[(k >> shift) & 255u], 1);
-        }
-      }
-      __syncthreads();
-      if (tid < 256) {
-        int c = 0;
-        for (int w = 0; w < kHist; ++w) c += hist[w][tid];
-        hist[0][tid] = c;
-      }
-      __syncthreads();
-      if (tid == 0) {
-        int d = 255;
-        for (; d > 0; --d) {
-          if (hist[0][d] >= rem) break;
-          rem -= hist[0][d];
-        }
-        s_digit = d;
-        s_rem = rem;
-      }
-      __syncthreads();
-      prefix |= (uint32_t)s_digit << shift;
-      mask |= 255u << shift;
-      rem = s_rem;
-      __syncthreads();
-    }
-    T = prefix;
-    need_eq = rem;
+  for (int off = 16; off > 0; off >>= 1) {
+    gt += __shfl_xor_sync(0xffffffffu, gt, off);
+    eq += __shfl_xor_sync(0xffffffffu, eq, off);
   }
-  // per-row counts; ties go to rows in (head, row) order
-  int tie_base = 0;
-  const int nrows = nh * nb;
-  for (int k0 = 0; k0 < nrows; k0 += kRankWarps) {
-    const int k = k0 + warp;
-    int gt = 0, eq = 0;
+  if (lane == 0) {
+    if (ro.need_eq == 0) {
+      counts[row] += gt;
+      taken[row] = 0;
+    } else {
+      gtrow[row] = gt;
+      eqrow[row] = eq;
+    }
+  }
+}
+
+// Exclusive prefix sum over the CTA (kRankThreads threads); `total` gets the
+// sum of all. `warp_sum` holds kRankWarps entries.
+__device__ int64_t block_excl_scan(int64_t v, int64_t* warp_sum, int64_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int64_t incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int64_t o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  __syncthreads();   // earlier readers of warp_sum are done
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  int64_t before = 0, all = 0;
+  for (int w = 0; w < kRankWarps; ++w) {
+    const int64_t x = warp_sum[w];
+    before += w < warp ? x : 0;
+    all += x;
+  }
+  total = all;
+  return before + incl - v;
+}
+
+// One CTA per (batch element, rank) with ties to share: the first need_eq
+// keys equal to the cut, in (head, row, block) order, go to their rows. The
+// rank's heads are compacted in ascending order, then its rows are taken
+// kRankThreads at a time with a prefix sum of their tie counts.
+__global__ void __launch_bounds__(kRankThreads)
+aug_tie_kernel(const int32_t* __restrict__ head_rank, int H, int nb, int P, const RankOut* __restrict__ rank_out,
+               const int32_t* __restrict__ gtrow, const int32_t* __restrict__ eqrow, int32_t* __restrict__ counts,
+               int32_t* __restrict__ taken) {
+  __shared__ int32_t heads[kMaxHeads];
+  __shared__ int64_t warp_sum[kRankWarps];
+  const int b = blockIdx.x / P, r = blockIdx.x % P;
+  const int64_t need_eq = rank_out[blockIdx.x].need_eq;
+  if (need_eq == 0) return;
+  const int tid = threadIdx.x;
+  int64_t n_heads = 0;
+  for (int h0 = 0; h0 < H; h0 += kRankThreads) {
+    const int h = h0 + tid;
+    const bool mine = h < H && head_rank[(int64_t)b * H + h] == r;
+    int64_t n;
+    const int64_t pos = n_heads + block_excl_scan(mine ? 1 : 0, warp_sum, n);
+    if (mine) heads[pos] = h;
+    n_heads += n;
+  }
+  __syncthreads();
+  const int64_t nrows = n_heads * nb;
+  int64_t tie_base = 0;
+  for (int64_t k0 = 0; k0 < nrows; k0 += kRankThreads) {
+    const int64_t k = k0 + tid;
     int64_t row = -1;
+    int eq = 0;
     if (k < nrows) {
       row = ((int64_t)b * H + heads[k / nb]) * nb + k % nb;
-      const uint32_t* K = keys + row * nb;
-      for (int j = lane; j < nb; j += 32) {
-        const uint32_t key = K[j];
-        gt += key > T && key != 0u;
-        eq += key == T && key != 0u;
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        gt += __shfl_xor_sync(0xffffffffu, gt, off);
-        eq += __shfl_xor_sync(0xffffffffu, eq, off);
-      }
+      eq = eqrow[row];
     }
-    if (lane == 0) eqs[warp] = eq;
-    __syncthreads();
-    if (k < nrows && lane == 0) {
-      int before = tie_base;
-      for (int w = 0; w < warp; ++w) before += eqs[w];
-      int t = need_eq - before;
-      t = t < 0 ? 0 : (t > eq ? eq : t);
-      taken[row] = t;
-      counts[row] += gt + t;
+    int64_t sum;
+    const int64_t before = tie_base + block_excl_scan(eq, warp_sum, sum);
+    if (row >= 0) {
+      int64_t tk = need_eq - before;
+      tk = tk < 0 ? 0 : (tk > eq ? eq : tk);
+      taken[row] = (int32_t)tk;
+      counts[row] += gtrow[row] + (int32_t)tk;
     }
-    int sum = 0;
-    for (int w = 0; w < kRankWarps; ++w) sum += eqs[w];
     tie_base += sum;
-    __syncthreads();
-  }
-  if (tid == 0) {
-    rank_out[blockIdx.x] = RankOut{T, need_eq};
-    if (added != nullptr) added[blockIdx.x] = (int64_t)s;
   }
 }
 
@@ -344,7 +498,8 @@ aug_fill_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__
   const int64_t bh = row / nb;
   const int q = head_rank[bh];
   const bool valid = q >= 0 && q < P;
-  const RankOut ro = valid ? rank_out[(bh / H) * P + q] : RankOut{0xffffffffu, 0};
+  const RankOut ro = valid ? rank_out[(bh / H) * P + q] : RankOut{0xffffffffu, 0u, 0};
+  const bool takes = ro.T != 0xffffffffu;   // else the row may have no keys
   const int my_ties = valid ? taken[row] : 0;
   const uint32_t* K = keys + row * nb;
   int64_t pos = out_ptr[row];
@@ -355,7 +510,7 @@ aug_fill_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__
     bool keep = false, tie = false;
     if (j < nb) {
       const bool sel = (bits[j >> 5] >> (j & 31)) & 1u;
-      const uint32_t key = K[j];
+      const uint32_t key = takes ? K[j] : 0u;
       tie = !sel && key != 0u && key == ro.T;
       keep = sel || (key != 0u && key > ro.T);
     }
@@ -386,8 +541,10 @@ sparsp_status_t launch_balance(const Dims& s, const int32_t* row_ptr, int P, int
 
 size_t augment_ws(const Dims& s, int P) {
   const int64_t rows = s.rows();
-  return align256((size_t)rows * s.nb * sizeof(uint32_t)) + align256((size_t)rows * sizeof(int32_t)) +
-         align256((size_t)s.B * P * sizeof(RankOut));
+  const size_t br = (size_t)s.B * P;
+  return align256((size_t)rows * s.nb * sizeof(uint32_t)) + 3 * align256((size_t)rows * sizeof(int32_t)) +
+         align256(br * sizeof(RankOut)) + align256(br * sizeof(RankState)) +
+         align256(br * 256 * sizeof(unsigned long long));
 }
 
 sparsp_status_t launch_augment(const Dims& s, int P, const float* scores, const int32_t* row_ptr,
@@ -395,17 +552,40 @@ sparsp_status_t launch_augment(const Dims& s, int P, const float* scores, const 
                                int32_t* out_idx, int64_t cap, int64_t* added, void* ws, int32_t* d_status,
                                cudaStream_t st) {
   const int64_t rows = s.rows();
+  const size_t br = (size_t)s.B * P;
   char* w = (char*)ws;
   uint32_t* keys = (uint32_t*)w;
   w += align256((size_t)rows * s.nb * sizeof(uint32_t));
   int32_t* taken = (int32_t*)w;
   w += align256((size_t)rows * sizeof(int32_t));
+  int32_t* gtrow = (int32_t*)w;
+  w += align256((size_t)rows * sizeof(int32_t));
+  int32_t* eqrow = (int32_t*)w;
+  w += align256((size_t)rows * sizeof(int32_t));
   RankOut* ro = (RankOut*)w;
+  w += align256(br * sizeof(RankOut));
+  RankState* state = (RankState*)w;
+  w += align256(br * sizeof(RankState));
+  unsigned long long* hist = (unsigned long long*)w;
+
   const unsigned grid = (unsigned)((rows + 7) / 8);
-  aug_keys_kernel<<<grid, 256, 0, st>>>(scores, row_ptr, col_idx, s.nb, rows, keys, out_ptr, d_status);
+  aug_slack_kernel<<<s.B, kRankThreads, 0, st>>>(row_ptr, head_rank, s.H, s.nb, P, state, ro, added, hist,
+                                                 d_status);
   SPARSP_LAUNCH_CHECK();
-  aug_rank_kernel<<<s.B * P, kRankThreads, 0, st>>>(row_ptr, head_rank, s.H, s.nb, P, keys, out_ptr, taken, ro,
-                                                    added, d_status);
+  aug_keys_kernel<<<grid, 256, 0, st>>>(scores, row_ptr, col_idx, head_rank, state, s.H, s.nb, P, rows, keys,
+                                        out_ptr, d_status);
+  SPARSP_LAUNCH_CHECK();
+  const int64_t per_head = (int64_t)s.nb * s.nb;
+  const dim3 hgrid((unsigned)(s.B * s.H), (unsigned)((per_head + kKeysPerCta - 1) / kKeysPerCta));
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    aug_hist_kernel<<<hgrid, 256, 0, st>>>(head_rank, s.H, P, s.nb, keys, state, hist, shift);
+    SPARSP_LAUNCH_CHECK();
+    aug_digit_kernel<<<(unsigned)br, 256, 0, st>>>(state, hist, ro, added, shift);
+    SPARSP_LAUNCH_CHECK();
+  }
+  aug_rowcount_kernel<<<grid, 256, 0, st>>>(head_rank, s.H, P, s.nb, rows, keys, ro, out_ptr, taken, gtrow, eqrow);
+  SPARSP_LAUNCH_CHECK();
+  aug_tie_kernel<<<(unsigned)br, kRankThreads, 0, st>>>(head_rank, s.H, s.nb, P, ro, gtrow, eqrow, out_ptr, taken);
   SPARSP_LAUNCH_CHECK();
   sparsp_status_t r = launch_scan_counts(out_ptr, rows, st);
   if (r != SPARSP_OK) return r;

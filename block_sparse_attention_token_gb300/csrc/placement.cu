@@ -10,7 +10,8 @@
 //     affinity (descending; ties: lower index), each placed on the partition
 //     with spare capacity whose blocks have the largest affinity to it (ties:
 //     more spare capacity, then lower index). Scores are integer sums, so the
-//     assignment is deterministic.
+//     assignment is deterministic. The steps are sequential: each costs two
+//     barriers, with the affinity rows read two steps ahead.
 #include "common.cuh"
 
 namespace sparsp {
@@ -43,6 +44,7 @@ affinity_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__
 }
 
 constexpr int kThreads = 1024;
+constexpr int kSmallP = 32;   // up to this many partitions one warp picks the winner
 
 __device__ __forceinline__ unsigned long long max_key(unsigned long long v) {
 #pragma unroll
@@ -53,63 +55,109 @@ __device__ __forceinline__ unsigned long long max_key(unsigned long long v) {
   return v;
 }
 
+// key = (score, spare capacity, -r): larger is better; full partitions are out
+__device__ __forceinline__ unsigned long long place_key(uint32_t score, int cap, int r) {
+  return cap > 0 ? ((unsigned long long)score << 22) | ((unsigned long long)cap << 11) |
+                       (unsigned long long)(1023 - r)
+                 : 0ull;
+}
+
+// One CTA of ceil(nb/32) warps per batch element; thread t owns block t. The
+// affinity rows of the next two blocks in order are loaded ahead.
+//
+// Few partitions (kFew): shared memory keeps, for every block u and partition
+// r, A[u][r] = the affinity of u to the blocks placed on r so far. A step
+// adds the last placed block's row into its partition's column (one add per
+// thread), then warp 0 reads the next block's A row and picks the partition
+// with two warp reductions (score, then spare capacity and index).
+// Otherwise the scores are summed with shared-memory atomics and the pick is a
+// block-wide maximum.
+template <bool kFew>
 __global__ void __launch_bounds__(kThreads)
 greedy_kernel(const int32_t* __restrict__ W, int nb, int P, int32_t* __restrict__ owner) {
-  __shared__ int32_t total[1024], order[1024], own[1024], caps[1024];
-  __shared__ unsigned long long score[1024];
+  __shared__ int32_t total[1024], order[1024], caps[1024];
+  __shared__ uint32_t score[kFew ? 1 : 1024];
   __shared__ unsigned long long warp_best[32];
+  __shared__ int s_pick;
+  extern __shared__ uint32_t aff[];   // kFew: [nb][stride]
+  const int stride = P | 1;           // odd: the column updates and the row reads are conflict-free
   const int b = blockIdx.x;
   const int32_t* Wb = W + (int64_t)b * nb * nb;
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5, nt = blockDim.x, nw = nt >> 5;
   // W is symmetric: the row sum of i is its column sum, read coalesced
-  for (int i = t; i < nb; i += kThreads) {
+  if (t < nb) {
     int32_t s = 0;
-    for (int j = 0; j < nb; ++j) s += Wb[(int64_t)j * nb + i];
-    total[i] = s;
-    own[i] = -1;
+    for (int j = 0; j < nb; ++j) s += Wb[(int64_t)j * nb + t];
+    total[t] = s;
+    if (kFew)
+      for (int r = 0; r < P; ++r) aff[t * stride + r] = 0u;
   }
-  for (int r = t; r < P; r += kThreads)
+  for (int r = t; r < P; r += nt)
     caps[r] = (int)(((int64_t)(r + 1) * nb) / P - ((int64_t)r * nb) / P);
   __syncthreads();
-  for (int i = t; i < nb; i += kThreads) {
+  if (t < nb) {
     int rank = 0;
-    for (int k = 0; k < nb; ++k) rank += (total[k] > total[i]) || (total[k] == total[i] && k < i);
-    order[rank] = i;
+    for (int k = 0; k < nb; ++k) rank += (total[k] > total[t]) || (total[k] == total[t] && k < t);
+    order[rank] = t;
   }
   __syncthreads();
+  int my_own = -1;   // partition of block t
+  uint32_t w0 = t < nb ? (uint32_t)Wb[(int64_t)order[0] * nb + t] : 0u;
+  uint32_t w1 = t < nb && nb > 1 ? (uint32_t)Wb[(int64_t)order[1] * nb + t] : 0u;
+  uint32_t w_last = 0u;   // row of the block placed in the previous step (kFew)
+  int r_last = -1;
   for (int step = 0; step < nb; ++step) {
     const int i = order[step];
-    for (int r = t; r < P; r += kThreads) score[r] = 0ull;
-    __syncthreads();
-    for (int j = t; j < nb; j += kThreads) {
-      const int r = own[j];
-      if (r >= 0) atomicAdd(&score[r], (unsigned long long)Wb[(int64_t)i * nb + j]);
-    }
-    __syncthreads();
-    // key = (score, spare capacity, -r): larger is better; full partitions are out
-    unsigned long long best = 0ull;
-    for (int r = t; r < P; r += kThreads)
-      if (caps[r] > 0) {
-        const unsigned long long key = (score[r] << 22) | ((unsigned long long)caps[r] << 11) |
-                                       (unsigned long long)(1023 - r);
+    const uint32_t w = w0;
+    w0 = w1;
+    if (t < nb && step + 2 < nb) w1 = (uint32_t)Wb[(int64_t)order[step + 2] * nb + t];
+    if (kFew) {
+      if (r_last >= 0 && t < nb) aff[t * stride + r_last] += w_last;   // W[u][i_last] = W[i_last][u]
+      __syncthreads();
+      if (warp == 0) {
+        const bool open = lane < P && caps[lane] > 0;
+        const uint32_t sc = open ? aff[i * stride + lane] : 0u;
+        const uint32_t top = __reduce_max_sync(0xffffffffu, sc);
+        const uint32_t tie = open && sc == top ? ((uint32_t)caps[lane] << 11) | (uint32_t)(1023 - lane) : 0u;
+        const uint32_t best = __reduce_max_sync(0xffffffffu, tie);
+        if (lane == 0) {
+          const int r = 1023 - (int)(best & 1023u);
+          caps[r] -= 1;
+          s_pick = r;
+        }
+      }
+    } else {
+      for (int r = t; r < P; r += nt) score[r] = 0u;
+      __syncthreads();
+      if (my_own >= 0) atomicAdd(&score[my_own], w);
+      __syncthreads();
+      unsigned long long best = 0ull;
+      for (int r = t; r < P; r += nt) {
+        const unsigned long long key = place_key(score[r], caps[r], r);
         best = key > best ? key : best;
       }
-    best = max_key(best);
-    if (lane == 0) warp_best[warp] = best;
-    __syncthreads();
-    if (warp == 0) {
-      unsigned long long v = warp_best[lane];
-      v = max_key(v);
-      if (lane == 0) {
-        const int r = 1023 - (int)(v & 1023ull);
-        own[i] = r;
-        caps[r] -= 1;
+      best = max_key(best);
+      if (lane == 0) warp_best[warp] = best;
+      __syncthreads();
+      if (warp == 0) {
+        unsigned long long v = lane < nw ? warp_best[lane] : 0ull;
+        v = max_key(v);
+        if (lane == 0) {
+          const int r = 1023 - (int)(v & 1023ull);
+          caps[r] -= 1;
+          s_pick = r;
+        }
       }
     }
     __syncthreads();
+    r_last = s_pick;
+    w_last = w;
+    if (t == i) my_own = r_last;
   }
-  for (int i = t; i < nb; i += kThreads) owner[(int64_t)b * nb + i] = own[i];
+  if (t < nb) owner[(int64_t)b * nb + t] = my_own;
 }
+
+size_t placement_few_smem(int nb, int P) { return (size_t)nb * (size_t)(P | 1) * sizeof(uint32_t); }
 
 }  // namespace
 
@@ -122,7 +170,16 @@ sparsp_status_t launch_placement(const Dims& s, const int32_t* row_ptr, const in
   const int64_t rows = s.rows();
   affinity_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(row_ptr, col_idx, s.H, s.nb, rows, W, d_status);
   SPARSP_LAUNCH_CHECK();
-  greedy_kernel<<<s.B, kThreads, 0, st>>>(W, s.nb, P, owner);
+  const unsigned threads = (unsigned)((s.nb + 31) / 32 * 32);
+  if (P <= kSmallP) {
+    const size_t smem = placement_few_smem(s.nb, P);
+    if (cudaFuncSetAttribute(greedy_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return SPARSP_ERR_CUDA;
+    greedy_kernel<true><<<s.B, threads, smem, st>>>(W, s.nb, P, owner);
+  } else {
+    greedy_kernel<false><<<s.B, threads, 0, st>>>(W, s.nb, P, owner);
+  }
   SPARSP_LAUNCH_CHECK();
   return SPARSP_OK;
 }

@@ -8,9 +8,11 @@
 //
 //  1. scores of both kinds from the pooled means (the projections qm Wq and
 //     km Wk come out of the low-rank pass, in the workspace);
-//  2. ge_kernel   - grid (b*H + h, chunk of 256 outputs): GA = E (km Wk),
-//     GB = E^T (qm Wq), one output element per thread;
-//  3. loss_kernel - one CTA per head: the loss (fp64 partials, a fixed tree);
+//  2. ge_kernel   - grid (b*H + h, block of 32 rows): GA = E (km Wk),
+//     GB = E^T (qm Wq), with E's row and column tiles staged in shared memory;
+//  3. loss_part_kernel - grid (h, chunk): fp64 partial sums of the squared
+//     errors (fixed strided subsets, a fixed tree); loss_final_kernel adds
+//     each head's partials in chunk order;
 //  4. gw_kernel   - grid (h, dd): the weight gradients (row slices summed in a
 //     fixed tree) and, when lr != 0, the step W -= lr dL/dW in place (the
 //     projections were taken before it).
@@ -22,26 +24,66 @@ namespace {
 
 constexpr int kThreads = 256;
 
+constexpr int kGeRows = 32;   // rows i of GA and GB per CTA
+constexpr int kGeJ = 32;      // j per shared-memory stage
+constexpr int kGeOut = 8;     // outputs per thread: 32 * rank / kThreads, rank <= 64
+
+// grid (b*H + h, block of kGeRows rows): GA[i,c] = sum_j E[i,j] B[j,c] and
+// GB[i,c] = sum_j E[j,i] A[j,c] with E = Sp - St. E's row and column tiles
+// and the matching rows of A and B are staged in shared memory kGeJ at a time;
+// every output is one sequential fmaf chain over j.
 __global__ void __launch_bounds__(kThreads)
 ge_kernel(const float* __restrict__ sp, const float* __restrict__ st, const float* __restrict__ pq,
           const float* __restrict__ pk, int nb, int rank, float* __restrict__ ga, float* __restrict__ gb) {
+  __shared__ float er[kGeRows][kGeJ + 1];   // E[i0 + ii][j0 + jj]
+  __shared__ float ec[kGeJ][kGeRows + 1];   // E[j0 + jj][i0 + ii]
+  __shared__ float as[kGeJ * 64], bs[kGeJ * 64];
   const int64_t bh = blockIdx.x;
-  const int idx = blockIdx.y * kThreads + threadIdx.x;
-  if (idx >= nb * rank) return;
+  const int i0 = blockIdx.y * kGeRows;
   const float* P = sp + bh * nb * nb;
   const float* T = st + bh * nb * nb;
   const float* A = pq + bh * nb * rank;
   const float* Bk = pk + bh * nb * rank;
-  float* GA = ga + bh * nb * rank;
-  float* GB = gb + bh * nb * rank;
-  const int i = idx / rank, c = idx % rank;
-  float a = 0.f, bsum = 0.f;
-  for (int j = 0; j < nb; ++j) {
-    a = fmaf(P[(int64_t)i * nb + j] - T[(int64_t)i * nb + j], Bk[(int64_t)j * rank + c], a);
-    bsum = fmaf(P[(int64_t)j * nb + i] - T[(int64_t)j * nb + i], A[(int64_t)j * rank + c], bsum);
+  const int nout = kGeRows * rank;
+  float a[kGeOut], b[kGeOut];
+#pragma unroll
+  for (int k = 0; k < kGeOut; ++k) a[k] = b[k] = 0.f;
+  for (int j0 = 0; j0 < nb; j0 += kGeJ) {
+    for (int x = threadIdx.x; x < kGeRows * kGeJ; x += kThreads) {
+      const int r = x / kGeJ, c = x % kGeJ;   // consecutive threads: consecutive columns
+      const int i = i0 + r, j = j0 + c;
+      er[r][c] = i < nb && j < nb ? P[(int64_t)i * nb + j] - T[(int64_t)i * nb + j] : 0.f;
+      const int jr = j0 + r, ic = i0 + c;
+      ec[r][c] = jr < nb && ic < nb ? P[(int64_t)jr * nb + ic] - T[(int64_t)jr * nb + ic] : 0.f;
+    }
+    const int jn = nb - j0 < kGeJ ? nb - j0 : kGeJ;
+    for (int x = threadIdx.x; x < jn * rank; x += kThreads) {
+      as[x] = A[(int64_t)j0 * rank + x];
+      bs[x] = Bk[(int64_t)j0 * rank + x];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kGeOut; ++k) {
+      const int o = threadIdx.x + k * kThreads;
+      if (o < nout) {
+        const int ii = o / rank, c = o % rank;
+        for (int jj = 0; jj < jn; ++jj) {
+          a[k] = fmaf(er[ii][jj], bs[jj * rank + c], a[k]);
+          b[k] = fmaf(ec[jj][ii], as[jj * rank + c], b[k]);
+        }
+      }
+    }
+    __syncthreads();
   }
-  GA[idx] = a;
-  GB[idx] = bsum;
+#pragma unroll
+  for (int k = 0; k < kGeOut; ++k) {
+    const int o = threadIdx.x + k * kThreads;
+    const int i = i0 + o / rank;
+    if (o < nout && i < nb) {
+      ga[bh * nb * rank + (int64_t)i * rank + o % rank] = a[k];
+      gb[bh * nb * rank + (int64_t)i * rank + o % rank] = b[k];
+    }
+  }
 }
 
 // One CTA per (h, dd): thread (slice, c) sums column c over its slice of the
@@ -86,20 +128,31 @@ gw_kernel(const float* __restrict__ qm, const float* __restrict__ km, const floa
   }
 }
 
-// One CTA per head: every thread sums a fixed strided subset in fp64, then a
-// fixed tree.
+constexpr int kLossChunks = 64;        // most partial sums per head
+constexpr int kLossPerChunk = 4096;    // fewest elements per partial sum
+
+__host__ __device__ inline int loss_chunks(int64_t n) {
+  const int64_t c = (n + kLossPerChunk - 1) / kLossPerChunk;
+  return c < 1 ? 1 : (c > kLossChunks ? kLossChunks : (int)c);
+}
+
+// grid (h, chunk): chunk c of head h's B*nb^2 squared errors, summed in fp64
+// (each thread a fixed strided subset, then a fixed tree).
 __global__ void __launch_bounds__(kThreads)
-loss_kernel(const float* __restrict__ sp, const float* __restrict__ st, int B, int H, int nb,
-            float* __restrict__ loss) {
+loss_part_kernel(const float* __restrict__ sp, const float* __restrict__ st, int B, int H, int nb,
+                 double* __restrict__ part) {
   __shared__ double red[kThreads];
-  const int h = blockIdx.x;
+  const int h = blockIdx.x, chunk = blockIdx.y, nchunks = gridDim.y;
+  const int64_t per_b = (int64_t)nb * nb, n = (int64_t)B * per_b;
+  const int64_t len = (n + nchunks - 1) / nchunks;
+  const int64_t e0 = (int64_t)chunk * len;
+  const int64_t e1 = e0 + len < n ? e0 + len : n;
   double acc = 0.0;
-  for (int b = 0; b < B; ++b) {
-    const int64_t base = ((int64_t)b * H + h) * nb * nb;
-    for (int64_t e = threadIdx.x; e < (int64_t)nb * nb; e += kThreads) {
-      const double x = (double)sp[base + e] - (double)st[base + e];
-      acc += x * x;
-    }
+  for (int64_t e = e0 + threadIdx.x; e < e1; e += kThreads) {
+    const int64_t b = e / per_b;
+    const int64_t at = ((int64_t)b * H + h) * per_b + (e - b * per_b);
+    const double x = (double)sp[at] - (double)st[at];
+    acc += x * x;
   }
   red[threadIdx.x] = acc;
   __syncthreads();
@@ -107,7 +160,17 @@ loss_kernel(const float* __restrict__ sp, const float* __restrict__ st, int B, i
     if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
     __syncthreads();
   }
-  if (threadIdx.x == 0) loss[h] = (float)(red[0] / ((double)B * nb * nb));
+  if (threadIdx.x == 0) part[(int64_t)h * nchunks + chunk] = red[0];
+}
+
+// One thread per head: its partial sums in chunk order.
+__global__ void loss_final_kernel(const double* __restrict__ part, int B, int H, int nb, int nchunks,
+                                  float* __restrict__ loss) {
+  const int h = blockIdx.x * blockDim.x + threadIdx.x;
+  if (h >= H) return;
+  double s = 0.0;
+  for (int c = 0; c < nchunks; ++c) s += part[(int64_t)h * nchunks + c];
+  loss[h] = (float)(s / ((double)B * nb * nb));
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -118,6 +181,7 @@ size_t predictor_ws(const Dims& s, int rank) {
   const size_t bh = (size_t)s.B * s.H;
   return align256(scores_from_means_ws(s, SPARSP_EST_LOWRANK, rank)) +
          2 * align256(bh * s.nb * s.nb * sizeof(float)) + 2 * align256(bh * s.nb * rank * sizeof(float)) +
+         align256((size_t)s.H * kLossChunks * sizeof(double)) +
          align256(scores_from_means_ws(s, SPARSP_EST_MEAN, rank));
 }
 
@@ -137,6 +201,8 @@ sparsp_status_t launch_predictor_fit(const Dims& s, int rank, const float* qm, c
   w += align256(bh * s.nb * rank * sizeof(float));
   float* gb = (float*)w;
   w += align256(bh * s.nb * rank * sizeof(float));
+  double* part = (double*)w;
+  w += align256((size_t)s.H * kLossChunks * sizeof(double));
   void* ws_mean = w;
   sparsp_status_t r = launch_scores_from_means(s, SPARSP_EST_LOWRANK, qm, km, wq, wk, rank, sp, proj, st);
   if (r != SPARSP_OK) return r;
@@ -144,11 +210,14 @@ sparsp_status_t launch_predictor_fit(const Dims& s, int rank, const float* qm, c
   if (r != SPARSP_OK) return r;
   const float* pq = proj;
   const float* pk = proj + bh * s.nb * rank;
-  ge_kernel<<<dim3((unsigned)bh, (unsigned)((s.nb * rank + kThreads - 1) / kThreads)), kThreads, 0, st>>>(
+  ge_kernel<<<dim3((unsigned)bh, (unsigned)((s.nb + kGeRows - 1) / kGeRows)), kThreads, 0, st>>>(
       sp, strue, pq, pk, s.nb, rank, ga, gb);
   SPARSP_LAUNCH_CHECK();
   if (loss != nullptr) {
-    loss_kernel<<<s.H, kThreads, 0, st>>>(sp, strue, s.B, s.H, s.nb, loss);
+    const int nchunks = loss_chunks((int64_t)s.B * s.nb * s.nb);
+    loss_part_kernel<<<dim3((unsigned)s.H, (unsigned)nchunks), kThreads, 0, st>>>(sp, strue, s.B, s.H, s.nb, part);
+    SPARSP_LAUNCH_CHECK();
+    loss_final_kernel<<<(s.H + 127) / 128, 128, 0, st>>>(part, s.B, s.H, s.nb, nchunks, loss);
     SPARSP_LAUNCH_CHECK();
   }
   gw_kernel<<<dim3((unsigned)s.H, (unsigned)s.d), kThreads, 0, st>>>(qm, km, ga, gb, s.B, s.H, s.nb, s.d, rank, lr,

@@ -21,16 +21,17 @@ from . import (EST_LOWRANK, EST_MEAN, PROF_SLOTS, Shape, attn_bwd, attn_fwd, att
 class Pipeline:
     def kernels_per_forward(self) -> int:
         """Kernels forward() launches: reorder x3, pool + product, select x3 (count,
-        scan, fill), predictor fitting x6 when enabled, balancing (1) and augmentation x4 (keys, rank select,
-        scan, fill) when enabled, placement x2 (affinity, greedy) when
+        scan, fill), predictor fitting x7 when enabled, balancing (1) and augmentation x14 (keys, slack, four
+        histogram + digit passes, row counts, ties, scan, fill) when enabled, placement x2 (affinity, greedy) when
         enabled, demand x4 (bitmap, scan, list, gather), schedule (1, or 2 in
         flat order) + attention, inverse reorder."""
         lpt = 2 if self.flags & 1 else 1
         gather = 1 if self.demand.kg is not None else 0
         scores = (2 if self.est == EST_LOWRANK else 1) if self.fused else 2
         place = 2 if self.owner is not None else 0
-        bal = (1 if self.migrations is not None else 0) + (4 if self.augment else 0)
-        pred = 6 if self.predictor_lr is not None else 0   # projection, two score products, loss, two gradient kernels
+        bal = (1 if self.migrations is not None else 0) + (14 if self.augment else 0)
+        # projection, two score products, gradient products, loss (partials, sum), weight gradients
+        pred = 7 if self.predictor_lr is not None else 0
         return 3 + scores + pred + 3 + bal + place + 3 + gather + lpt + 1 + 1
 
     def kernels_per_backward(self) -> int:
