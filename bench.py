@@ -194,6 +194,9 @@ def main():
                     help="dependency-aware block placement inside the step (default: contiguous partitions)")
     ap.add_argument("--augment", action="store_true",
                     help="head balancing over P virtual ranks + slack-aware augmentation inside the step")
+    ap.add_argument("--serial-demand", action="store_true",
+                    help="run the KV demand stage before attention on one stream (default: beside it, on a "
+                         "side stream), so that every stage has its own time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--heads", type=int, default=0, help="override the head count (smaller profiling case)")
@@ -226,7 +229,8 @@ def main():
     flags = (sp.SCHED_FLAT if args.flat else 0) | (sp.KERNEL_PORTABLE if args.portable else 0)
     pipe = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P, backward=wl.backward, flags=flags,
                        fused_estimation=not args.unfused, placement=args.placement,
-                       migrations=wl.P if args.augment else None, augment=args.augment)
+                       migrations=wl.P if args.augment else None, augment=args.augment,
+                       overlap_demand=not args.serial_demand)
     tdt = shape.torch_dtype
     host_in = {x: torch.from_numpy(data[x]).to(tdt).pin_memory() for x in ("q", "k", "v")}
     dev_in = {x: host_in[x].cuda() for x in host_in}
@@ -255,9 +259,9 @@ def main():
     # ---- timed region: K steps, events around every stage
     marks = []
 
-    def mark(name):
+    def mark(name, on=None):
         ev = torch.cuda.Event(enable_timing=True)
-        ev.record(stream)
+        ev.record(on if on is not None else stream)
         marks.append((name, ev))
 
     clocks = ClockSampler(local)
@@ -275,12 +279,20 @@ def main():
     barrier()
     clk = clocks.stop()
     total_ms = start.elapsed_time(end)
+    # a stage runs from its "<name>:begin" mark if it has one (stages overlapped on
+    # their own streams), else from the mark before it
     stage_ms = {}
     prev = None
+    begins = {}
     for name, ev in marks:
-        if prev is not None and name != "step_start":
-            stage_ms[name] = stage_ms.get(name, 0.0) + prev.elapsed_time(ev)
-        prev = ev
+        if name.endswith(":begin"):
+            begins[name[:-len(":begin")]] = ev
+            continue
+        if name != "step_start":
+            first = begins.pop(name, prev)
+            stage_ms[name] = stage_ms.get(name, 0.0) + first.elapsed_time(ev)
+        if name not in ("attn_fwd", "kv_gather") or not pipe.overlap_demand:
+            prev = ev
     stage_ms = {k: v / args.steps for k, v in stage_ms.items()}
     ms_step = total_ms / args.steps
     ms_step = replicas.max_over_ranks(ms_step)
@@ -298,6 +310,21 @@ def main():
                 "work": f"4*nnz*Bt^2*d = {f_fwd:.4g} flop per launch (nnz={nnz})"}
     if wl.backward:
         roofline["bwd_achieved"] = bwd_flops(nnz, wl) / (stage_ms["attn_bwd"] * 1e-3) / 1e12
+    if pipe.overlap_demand and not args.portable:
+        # the same kernel with nothing beside it (in the step it shares its SMs with the KV gather)
+        rp_, ci_ = pipe.csr
+        b0 = torch.cuda.Event(enable_timing=True)
+        b1 = torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for _ in range(5):
+            sp.attn_fwd(shape, pipe.qb, pipe.kb, pipe.vb, rp_, ci_, 0.0, pipe.ob, pipe.lse, pipe.ws_attn,
+                        pipe.flags, None, pipe.status)
+        b1.record(stream)
+        torch.cuda.synchronize()
+        alone = f_fwd / (b0.elapsed_time(b1) / 5 * 1e-3) / 1e12
+        roofline["achieved_alone"] = alone
+        roofline["frac_alone"] = alone / peak
+        roofline["in_step"] = "shares its SMs with the KV demand gather (side stream)"
 
     # ---- algorithmic bytes of the memory-bound stages, against the measured copy peak
     el = 2 if wl.dtype == "bf16" else 4
@@ -309,16 +336,25 @@ def main():
         "reorder": 6 * tensor + (2 * means if not args.unfused else 0),
         "scores": (2 * means if not args.unfused else 2 * tensor) + 4 * BH * shape.nb * shape.nb,
         "select": 4 * BH * shape.nb * shape.nb + 4 * (nnz + rows + 1),
-        # the gathered copy is written once; each source K/V tile is read from HBM once (its
-        # P-fold reuse across partitions hits in L2)
-        "kv_demand": 4 * nnz + demanded + 2 * tensor + BH * wl.P * ((shape.nb + 31) // 32) * 4,
         "reorder_out": 2 * tensor,
     }
+    # demand lists: the CSR read, the bitmap and the index lists written; the gather: the
+    # gathered copy written once, each source K/V tile read from HBM once (its P-fold reuse
+    # across partitions hits in L2)
+    lists_bytes = 4 * nnz + BH * wl.P * ((shape.nb + 31) // 32) * 4 + 4 * (demanded // (2 * shape.Bt * shape.d * el))
+    gather_bytes = demanded + 2 * tensor
+    if pipe.overlap_demand:
+        stage_bytes["kv_demand"] = lists_bytes
+        stage_bytes["kv_gather"] = gather_bytes
+    else:
+        stage_bytes["kv_demand"] = lists_bytes + gather_bytes
     hbm = {}
     for name, nbytes in stage_bytes.items():
         if name in stage_ms and stage_ms[name] > 0:
             gbs = nbytes / (stage_ms[name] * 1e-3) / 1e9
             hbm[name] = {"bytes": int(nbytes), "gbs": gbs, "frac": gbs / pk["hbm_gbs"]}
+            if name == "kv_gather":
+                hbm[name]["note"] = "runs beside attention, sharing its SMs: not a standalone rate"
 
     # ---- context only: dense attention (PyTorch SDPA) over the same tensors
     dense = None
@@ -470,6 +506,8 @@ def main():
                    "estimation": "separate pooling pass" if args.unfused else "fused with the reorder",
                    "partitions": "dependency-aware placement" if args.placement else "contiguous",
                    "augmentation": "balanced heads + slack fill" if args.augment else "none",
+                   "kv_demand": "lists and gather serial, before attention" if args.serial_demand else
+                                "lists before attention; gather beside it on a low-priority side stream",
                    "l2": f"inputs larger than L2 ({shape.B * shape.H * shape.N * shape.d * 2 / 1e6:.0f} MB per tensor)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "stages_ms": stage_ms,

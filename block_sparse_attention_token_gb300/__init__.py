@@ -86,6 +86,7 @@ _SIG = {
     "sparsp_select_noalloc": (_I32, [_P, _P, ctypes.c_float, _I32, _P, _P, _P, _P]),
     "sparsp_kv_demand": (_I32, [_P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int64, _P, _P,
                                 _P]),
+    "sparsp_kv_gather": (_I32, [_P, _I32, _P, _P, _P, _P, _P, _P, ctypes.c_int64, _P, _P]),
     "sparsp_placement_workspace_size": (ctypes.c_size_t, [_P]),
     "sparsp_placement": (_I32, [_P, _I32, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
     "sparsp_balance_heads": (_I32, [_P, _I32, _I32, _P, _P, _P, _P, _P]),
@@ -264,6 +265,20 @@ def kv_demand(shape: Shape, P: int, row_ptr, col_idx, k=None, v=None, gather_cap
         _ptr(out.dem_idx), _ptr(k), _ptr(v), _ptr(out.kg), _ptr(out.vg), int(cap), _ptr(out.bytes),
         _ptr(status), _stream(stream)))
     return out
+
+
+def kv_gather(shape: Shape, P: int, dem: DemandOut, k, v, gather_cap: int | None = None, status=None,
+              stream=None) -> DemandOut:
+    """The gather of kv_demand alone, into dem.kg / dem.vg, from the lists
+    (dem.dem_ptr, dem.dem_idx) of an earlier kv_demand call; it can run on a
+    second stream beside attention."""
+    if dem.kg is None or dem.vg is None:
+        raise ValueError("kv_gather needs DemandOut with kg and vg buffers")
+    cap = dem.kg.shape[0] if gather_cap is None else gather_cap
+    _check("sparsp_kv_gather", lib().sparsp_kv_gather(
+        _sref(shape), int(P), _ptr(dem.dem_ptr), _ptr(dem.dem_idx), _ptr(k), _ptr(v), _ptr(dem.kg), _ptr(dem.vg),
+        int(cap), _ptr(status), _stream(stream)))
+    return dem
 
 
 def placement_workspace_size(shape: Shape) -> int:

@@ -41,6 +41,7 @@ __device__ __forceinline__ uint32_t smid() {
 
 int device_sm_count();   // cached per device; -1 on error
 
+
 #define SPARSP_LAUNCH_CHECK()                                       \
   do {                                                              \
     cudaError_t e_ = cudaGetLastError();                            \
@@ -76,6 +77,9 @@ sparsp_status_t launch_kv_demand(const Dims& s, int P, const int32_t* row_ptr,
                                  const int32_t* col_idx, const int32_t* owner, uint32_t* bitmap, int32_t* dem_ptr,
                                  int32_t* dem_idx, const void* k, const void* v, void* kg,
                                  void* vg, int64_t cap, uint64_t* bytes, int32_t* d_status,
+                                 cudaStream_t st);
+sparsp_status_t launch_kv_gather(const Dims& s, int P, const int32_t* dem_ptr, const int32_t* dem_idx,
+                                 const void* k, const void* v, void* kg, void* vg, int64_t cap, int32_t* d_status,
                                  cudaStream_t st);
 
 size_t placement_ws(const Dims& s);

@@ -1,5 +1,6 @@
 // Step 4: KV demand of P virtual query partitions.
 //
+//  0. zero_bytes_kernel - clears the four byte counters.
 //  1. bitmap_kernel - one CTA per partition (b, h, r). Contiguous split: the
 //     partition's rows are consecutive CSR rows, so its entries are one
 //     contiguous range of col_idx. With a block owner map: warps scan the
@@ -11,7 +12,10 @@
 //  4. gather_kernel - one CTA per demanded slot copies the K and V tiles
 //     (Bt x d, contiguous in the block-ordered layout) with 16-byte vectors;
 //     stores are streaming (the gathered copy is not re-read here), loads keep
-//     the default policy so the P-fold reuse of a source tile hits in L2.
+//     the default policy so the P-fold reuse of a source tile hits in L2. It
+//     also runs alone (sparsp_kv_gather): with no shared memory and one warp of
+//     at most 64 registers per SM sub-partition it fits beside the attention
+//     kernel's CTA, on another stream.
 #include "common.cuh"
 
 namespace sparsp {
@@ -120,9 +124,16 @@ list_kernel(const uint32_t* __restrict__ bitmap, const int32_t* __restrict__ dem
   }
 }
 
+__global__ void zero_bytes_kernel(uint64_t* bytes) {
+  if (threadIdx.x < 4) bytes[threadIdx.x] = 0ull;
+}
+
 // One CTA per slot < min(total, cap). The owning partition is found by binary
-// search in dem_ptr.
-__global__ void __launch_bounds__(256)
+// search in dem_ptr. Four warps of at most 64 registers: one warp per SM
+// sub-partition, which is what the attention kernel's CTA leaves room for.
+constexpr int kGatherThreads = 128;
+
+__global__ void __launch_bounds__(kGatherThreads, 8)
 gather_kernel(const int32_t* __restrict__ dem_ptr, const int32_t* __restrict__ dem_idx, int nparts,
               int P, int64_t N, int Bt, int vec_per_row, const uint4* __restrict__ k,
               const uint4* __restrict__ v, uint4* __restrict__ kg, uint4* __restrict__ vg,
@@ -143,6 +154,24 @@ gather_kernel(const int32_t* __restrict__ dem_ptr, const int32_t* __restrict__ d
   const uint4* vs = v + ((int64_t)bh * N + (int64_t)j * Bt) * vec_per_row;
   uint4* kd = kg + slot * nvec;
   uint4* vd = vg + slot * nvec;
+  constexpr int kUnroll = 4;
+  if (nvec % (kUnroll * kGatherThreads) == 0) {   // whole rounds: no per-vector bounds checks
+    const int t = threadIdx.x;
+    for (int64_t e = 0; e < nvec; e += kUnroll * kGatherThreads) {
+      uint4 a[kUnroll], b[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        a[u] = ks[e + u * kGatherThreads + t];
+        b[u] = vs[e + u * kGatherThreads + t];
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        __stcs(kd + e + u * kGatherThreads + t, a[u]);
+        __stcs(vd + e + u * kGatherThreads + t, b[u]);
+      }
+    }
+    return;
+  }
   for (int64_t e = threadIdx.x; e < nvec; e += 4 * blockDim.x) {
     uint4 a[4], b[4];
 #pragma unroll
@@ -174,7 +203,8 @@ sparsp_status_t launch_kv_demand(const Dims& s, int P, const int32_t* row_ptr,
   const int nparts = s.B * s.H * P;
   const int W = (s.nb + 31) / 32;
   const uint64_t tile2 = (uint64_t)s.Bt * s.d * s.elem * 2;
-  if (cudaMemsetAsync(bytes, 0, 4 * sizeof(uint64_t), st) != cudaSuccess) return SPARSP_ERR_CUDA;
+  zero_bytes_kernel<<<1, 32, 0, st>>>(bytes);
+  SPARSP_LAUNCH_CHECK();
   bitmap_kernel<<<nparts, 256, 0, st>>>(row_ptr, col_idx, owner, s.H, s.nb, P, tile2, bitmap, dem_ptr,
                                         bytes, d_status);
   SPARSP_LAUNCH_CHECK();
@@ -182,17 +212,23 @@ sparsp_status_t launch_kv_demand(const Dims& s, int P, const int32_t* row_ptr,
   if (r != SPARSP_OK) return r;
   list_kernel<<<(nparts + 7) / 8, 256, 0, st>>>(bitmap, dem_ptr, nparts, W, dem_idx);
   SPARSP_LAUNCH_CHECK();
-  if (kg != nullptr && vg != nullptr) {
-    // grid >= 1 so that slot 0 can report a capacity shortfall even when cap == 0
-    const int64_t upper = (int64_t)nparts * s.nb;
-    int64_t grid = upper < cap ? upper : cap;
-    if (grid < 1) grid = 1;
-    const int vec_per_row = s.d * s.elem / 16;
-    gather_kernel<<<(unsigned)grid, 256, 0, st>>>(dem_ptr, dem_idx, nparts, P, s.N, s.Bt,
-                                                   vec_per_row, (const uint4*)k, (const uint4*)v,
-                                                   (uint4*)kg, (uint4*)vg, cap, d_status);
-    SPARSP_LAUNCH_CHECK();
-  }
+  if (kg != nullptr && vg != nullptr) return launch_kv_gather(s, P, dem_ptr, dem_idx, k, v, kg, vg, cap, d_status, st);
+  return SPARSP_OK;
+}
+
+sparsp_status_t launch_kv_gather(const Dims& s, int P, const int32_t* dem_ptr, const int32_t* dem_idx,
+                                 const void* k, const void* v, void* kg, void* vg, int64_t cap, int32_t* d_status,
+                                 cudaStream_t st) {
+  const int nparts = s.B * s.H * P;
+  // grid >= 1 so that slot 0 can report a capacity shortfall even when cap == 0
+  const int64_t upper = (int64_t)nparts * s.nb;
+  int64_t grid = upper < cap ? upper : cap;
+  if (grid < 1) grid = 1;
+  const int vec_per_row = s.d * s.elem / 16;
+  gather_kernel<<<(unsigned)grid, kGatherThreads, 0, st>>>(dem_ptr, dem_idx, nparts, P, s.N, s.Bt, vec_per_row,
+                                                 (const uint4*)k, (const uint4*)v, (uint4*)kg, (uint4*)vg, cap,
+                                                 d_status);
+  SPARSP_LAUNCH_CHECK();
   return SPARSP_OK;
 }
 

@@ -6,13 +6,14 @@
 namespace sparsp {
 namespace {
 
-constexpr int kScanThreads = 1024;
-constexpr int kScanPer = 4;
+constexpr int kScanThreads = 256;
+constexpr int kScanWarps = kScanThreads / 32;
+constexpr int kScanPer = 16;
 
 // One CTA scans a[0..n) in place into exclusive offsets and writes a[n] = total.
 // Chunks of 4096 entries are processed in order with a running carry.
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(int32_t* a, int64_t n) {
-  __shared__ int32_t warp_tot[32];
+  __shared__ int32_t warp_tot[kScanWarps];
   __shared__ int32_t carry_s;
   if (threadIdx.x == 0) carry_s = 0;
   __syncthreads();
@@ -35,13 +36,13 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(int32_t* a, int64_t 
     if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-      int32_t t = warp_tot[lane];
+      int32_t t = lane < kScanWarps ? warp_tot[lane] : 0;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         int32_t o = __shfl_up_sync(0xffffffffu, t, off);
         if (lane >= off) t += o;
       }
-      warp_tot[lane] = t;   // inclusive over warps
+      if (lane < kScanWarps) warp_tot[lane] = t;   // inclusive over warps
     }
     __syncthreads();
     const int32_t carry = carry_s;
@@ -52,7 +53,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(int32_t* a, int64_t 
       run += v[u];
     }
     __syncthreads();
-    if (threadIdx.x == 0) carry_s = carry + warp_tot[31];
+    if (threadIdx.x == 0) carry_s = carry + warp_tot[kScanWarps - 1];
     __syncthreads();
   }
   if (threadIdx.x == 0) a[n] = carry_s;

@@ -6,15 +6,19 @@ of the CSR -> (optional) dependency-aware placement of blocks on the P
 partitions -> KV demand of P partitions (+ gather) -> block-sparse attention
 -> O back to raster order. backward(): dO into tiles -> attention backward -> dQ, dK, dV
 back to raster order. Every step is one or more libsparsp kernels on the
-current stream; nothing here allocates after construction.
+current stream, except that by default the KV demand gather runs on a side
+stream beside attention (the caller's stream waits for both); nothing here
+allocates after construction.
 """
 from __future__ import annotations
+
+import dataclasses
 
 import torch
 
 from . import (EST_LOWRANK, EST_MEAN, PROF_SLOTS, Shape, attn_bwd, attn_fwd, attn_workspace_size, augment,
                augment_workspace_size, balance_heads, Balance, predictor_fit,
-               block_scores, block_scores_pooled, block_scores_workspace_size, kv_demand, lib, placement,
+               block_scores, block_scores_pooled, block_scores_workspace_size, kv_demand, kv_gather, lib, placement,
                placement_workspace_size, reorder, reorder_pool, select, select_workspace_size, DemandOut)
 
 
@@ -23,7 +27,7 @@ class Pipeline:
         """Kernels forward() launches: reorder x3, pool + product, select x3 (count,
         scan, fill), predictor fitting x7 when enabled, balancing (1) and augmentation x14 (keys, slack, four
         histogram + digit passes, row counts, ties, scan, fill) when enabled, placement x2 (affinity, greedy) when
-        enabled, demand x4 (bitmap, scan, list, gather), schedule (1, or 2 in
+        enabled, demand x5 (counter reset, bitmap, scan, list, gather), schedule (1, or 2 in
         flat order) + attention, inverse reorder."""
         lpt = 2 if self.flags & 1 else 1
         gather = 1 if self.demand.kg is not None else 0
@@ -32,7 +36,7 @@ class Pipeline:
         bal = (1 if self.migrations is not None else 0) + (14 if self.augment else 0)
         # projection, two score products, gradient products, loss (partials, sum), weight gradients
         pred = 7 if self.predictor_lr is not None else 0
-        return 3 + scores + pred + 3 + bal + place + 3 + gather + lpt + 1 + 1
+        return 3 + scores + pred + 3 + bal + place + 4 + gather + lpt + 1 + 1
 
     def kernels_per_backward(self) -> int:
         """reorder dO, rowdot, CSR transpose, schedule, dQ, schedule, dK/dV, 3 inverse reorders."""
@@ -42,8 +46,12 @@ class Pipeline:
     def __init__(self, shape: Shape, estimator: str, top_p: float, k_floor: int, P: int, rank: int = 16,
                  gather: bool = True, flags: int = 0, backward: bool = False, device="cuda",
                  fused_estimation: bool = True, placement: bool = False, migrations: int | None = None,
-                 augment: bool = False, predictor_lr: float | None = None):
-        """migrations: balance heads over P virtual ranks with at most this many
+                 augment: bool = False, predictor_lr: float | None = None, overlap_demand: bool = True):
+        """overlap_demand: after the KV demand lists (bitmap, offsets, indices),
+        run the demand gather on a low-priority side stream while attention runs
+        on a high-priority one; the two only read the same K/V, and the
+        gather's CTAs (no shared memory) fit beside the persistent attention
+        CTAs. forward() returns after both on the caller's stream. migrations: balance heads over P virtual ranks with at most this many
         migrations (None: no balancing). augment: fill each rank's slack with
         extra blocks (on the balanced ranks, or the contiguous head split);
         attention then runs on the augmented CSR. predictor_lr: with the
@@ -89,6 +97,12 @@ class Pipeline:
             self.gwq, self.gwk = (torch.empty((s.H, s.d, rank), dtype=torch.float32, device=dev) for _ in range(2))
             self.ws_pred = torch.empty(max(lib().sparsp_predictor_workspace_size(ctypes.byref(s), rank), 16),
                                        dtype=torch.uint8, device=dev)
+        self.overlap_demand = overlap_demand
+        if overlap_demand:
+            lo, hi = torch.cuda.Stream.priority_range()   # least, greatest
+            self._attn_stream = torch.cuda.Stream(device=dev, priority=hi)
+            self._demand_stream = torch.cuda.Stream(device=dev, priority=lo)
+            self._selected = torch.cuda.Event()
         self.balance = None
         if migrations is not None or augment:
             if migrations is None:
@@ -117,11 +131,14 @@ class Pipeline:
                                          for _ in range(3))
 
     def forward(self, q, k, v, wq=None, wk=None, prof: bool = False, mark=None, out=None):
-        """mark: optional callable(stage_name) invoked after each stage is enqueued
-        (used to record CUDA events on the current stream). out: optional raster
-        output buffer (default: self.o)."""
+        """mark: optional callable(stage_name, stream=None) invoked after each
+        stage is enqueued (used to record CUDA events; stream None is the
+        current stream). With overlap_demand the overlapped stages are marked on
+        their own streams, each preceded by a "<stage>:begin" mark, and the
+        region they share by "overlap". out: optional raster output buffer
+        (default: self.o)."""
         s = self.shape
-        mark = mark or (lambda name: None)
+        mark = mark or (lambda name, stream=None: None)
         if self.fused:   # the tile means come out of the reorder pass itself
             reorder_pool(s, q, self.qb, self.qmeans)
             reorder_pool(s, k, self.kb, self.kmeans)
@@ -154,11 +171,37 @@ class Pipeline:
         if self.owner is not None:
             placement(s, self.P, rp, ci, self.owner, self.ws_place, self.status)
             mark("placement")
-        kv_demand(s, self.P, rp, ci, self.kb, self.vb, out=self.demand, status=self.status, owner=self.owner)
-        mark("kv_demand")
-        attn_fwd(s, self.qb, self.kb, self.vb, rp, ci, 0.0, self.ob, self.lse, self.ws_attn,
-                 self.flags, self.prof if prof else None, self.status)
-        mark("attn_fwd")
+        if self.overlap_demand and self.demand.kg is not None:
+            # the lists (bitmap, offsets, indices) first, on this stream: they need a
+            # little shared memory, which attention leaves none of; then the gather
+            # (no shared memory) beside attention
+            main = torch.cuda.current_stream()
+            lists = dataclasses.replace(self.demand, kg=None, vg=None)
+            kv_demand(s, self.P, rp, ci, out=lists, status=self.status, owner=self.owner)
+            mark("kv_demand")
+            hi, lo = self._attn_stream, self._demand_stream
+            mark("overlap:begin")
+            self._selected.record(main)
+            hi.wait_event(self._selected)
+            lo.wait_event(self._selected)
+            with torch.cuda.stream(hi):   # enqueued first: the persistent CTAs take their SMs first
+                mark("attn_fwd:begin", hi)
+                attn_fwd(s, self.qb, self.kb, self.vb, rp, ci, 0.0, self.ob, self.lse, self.ws_attn,
+                         self.flags, self.prof if prof else None, self.status, stream=hi)
+                mark("attn_fwd", hi)
+            with torch.cuda.stream(lo):
+                mark("kv_gather:begin", lo)
+                kv_gather(s, self.P, self.demand, self.kb, self.vb, status=self.status, stream=lo)
+                mark("kv_gather", lo)
+            main.wait_stream(hi)
+            main.wait_stream(lo)
+            mark("overlap")
+        else:
+            kv_demand(s, self.P, rp, ci, self.kb, self.vb, out=self.demand, status=self.status, owner=self.owner)
+            mark("kv_demand")
+            attn_fwd(s, self.qb, self.kb, self.vb, rp, ci, 0.0, self.ob, self.lse, self.ws_attn,
+                     self.flags, self.prof if prof else None, self.status)
+            mark("attn_fwd")
         o = self.o if out is None else out
         reorder(s, self.ob, o, inverse=True)
         mark("reorder_out")

@@ -47,7 +47,7 @@ class HostPipeline:
         cur.wait_event(self.in_ready[b])
         cur.wait_event(self.out_free[b])                   # step n-2's O has left the device
 
-        def mark(name):
+        def mark(name, stream=None):
             if name == "reorder":                          # raster inputs are no longer read
                 self.in_free[b].record(cur)
 
@@ -79,7 +79,7 @@ class HostPipeline:
         cur.wait_event(self.in_ready[b])
         cur.wait_event(self.out_free[b])                   # step n-2's results have left the device
 
-        def mark(name):
+        def mark(name, stream=None):
             if name == "reorder_dout":                     # every raster input has been read
                 self.in_free[b].record(cur)
 

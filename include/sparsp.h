@@ -232,6 +232,22 @@ SPARSP_API sparsp_status_t sparsp_kv_demand(const sparsp_shape_t* shape, int32_t
                                  int32_t* d_status, sparsp_stream_t stream);
 
 /*
+ * Step 4, the copy alone: the gather of sparsp_kv_demand from the lists a
+ * previous sparsp_kv_demand call (with kg == vg == NULL) wrote on the same
+ * stream, or with the stream ordering made by the caller. Same P, dem_ptr,
+ * dem_idx, k, v, kg, vg, gather_cap_blocks and results as the gather there:
+ * slot s < min(dem_ptr[B*H*P], gather_cap_blocks) of kg / vg receives the K / V
+ * tile dem_idx[s] of its partition's head; a total above gather_cap_blocks
+ * sets SPARSP_ERR_CAPACITY. It only reads k, v, dem_ptr and dem_idx and uses no
+ * shared memory, so it can run on a second stream beside the attention kernel
+ * (which holds almost all of each SM's shared memory); the lists need a small
+ * amount of it and do not fit there.
+ */
+SPARSP_API sparsp_status_t sparsp_kv_gather(const sparsp_shape_t* shape, int32_t P, const int32_t* dem_ptr,
+                                 const int32_t* dem_idx, const void* k, const void* v, void* kg, void* vg,
+                                 int64_t gather_cap_blocks, int32_t* d_status, sparsp_stream_t stream);
+
+/*
  * Step 4b - Dependency-Aware Placement ("SparSP: Exploiting Communication
  * Sparsity for Sequence-Parallel Video DiTs", abstract: sequence blocks placed
  * on ranks according to the sparse attention pattern), over the P virtual

@@ -122,6 +122,14 @@ def test_call_validation_codes(lib):
     assert lib.sparsp_kv_demand(S, 2, *args, FAKE, FAKE, FAKE, FAKE, -1, FAKE, None, None) == sp.INVALID_ARG
     assert lib.sparsp_kv_demand(S, 2, FAKE, FAKE, FAKE + 4, FAKE, FAKE, FAKE, None, None, None, None, 0, FAKE,
                                 None, None) == sp.ALIGN
+    # gather alone: P out of range, a missing buffer, negative capacity, misaligned list
+    g = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)
+    assert lib.sparsp_kv_gather(S, 0, *g, 4, None, None) == sp.SHAPE
+    assert lib.sparsp_kv_gather(S, s.nb + 1, *g, 4, None, None) == sp.SHAPE
+    assert lib.sparsp_kv_gather(S, 2, FAKE, FAKE, FAKE, FAKE, FAKE, None, 4, None, None) == sp.INVALID_ARG
+    assert lib.sparsp_kv_gather(S, 2, None, FAKE, FAKE, FAKE, FAKE, FAKE, 4, None, None) == sp.INVALID_ARG
+    assert lib.sparsp_kv_gather(S, 2, *g, -1, None, None) == sp.INVALID_ARG
+    assert lib.sparsp_kv_gather(S, 2, FAKE, FAKE + 4, FAKE, FAKE, FAKE, FAKE, 4, None, None) == sp.ALIGN
     # placement: P out of range, missing owner, small workspace
     need = lib.sparsp_placement_workspace_size(S)
     assert need == s.B * s.nb * s.nb * 4

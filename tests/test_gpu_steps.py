@@ -176,6 +176,40 @@ def test_kv_demand_capacity_shortfall():
         assert host(o2.bytes).astype(np.uint64).tolist() == r2.bytes.tolist()
 
 
+@pytest.mark.parametrize("name", ["r64", "medium", "wave"])
+def test_kv_gather_alone(name):
+    """The lists from kv_demand without buffers, then kv_gather on another
+    stream: the gathered tiles equal the oracle's; a short capacity is
+    reported and the slots below it are still right."""
+    wl, data, shape = _setup(name)
+    ch = OracleChain(wl, data)
+    g = ch.g
+    ref = orc.kv_demand(ch.sel.row_ptr, ch.sel.col_idx, g.B, g.H, g.nb, wl.P, g.Bt, g.d, wl.elem_bytes,
+                        ch.kb, ch.vb)
+    total = int(ref.dem_ptr[-1])
+    kb, vb = dev(ch.kb, wl), dev(ch.vb, wl)
+    st = status_word()
+    lists = sp.kv_demand(shape, wl.P, i32(ch.sel.row_ptr), i32(ch.sel.col_idx), status=st)
+    assert lists.kg is None
+    kg = torch.empty((total + 3, g.Bt, g.d), dtype=kb.dtype, device="cuda")
+    out = sp.DemandOut(lists.bitmap, lists.dem_ptr, lists.dem_idx, kg, torch.empty_like(kg), lists.bytes)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        sp.kv_gather(shape, wl.P, out, kb, vb, status=st, stream=side)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert np.array_equal(host(out.kg)[:total], ref.kg)
+    assert np.array_equal(host(out.vg)[:total], ref.vg)
+    cap = total // 3
+    out.kg.zero_()
+    st2 = status_word()
+    sp.kv_gather(shape, wl.P, out, kb, vb, gather_cap=cap, status=st2)
+    torch.cuda.synchronize()
+    assert st2.item() == sp.CAPACITY
+    assert np.array_equal(host(out.kg)[:cap], ref.kg[:cap])
+
+
 @pytest.mark.parametrize("name", list(SMALL))
 def test_placement_and_placed_demand_bitexact(name):
     wl, data, shape = _setup(name)
@@ -614,6 +648,32 @@ def test_pipeline_end_to_end(name, fused):
         b, h, i = r // (g.H * g.nb), (r // g.nb) % g.H, r % g.nb
         sl = slice(i * g.Bt, (i + 1) * g.Bt)
         compare_values(ob[b, h, sl], O[b, h, sl], wl, f"O row {r}")
+
+
+@pytest.mark.parametrize("name", ["medium", "r128", "wave"])
+def test_pipeline_overlapped_demand_equals_serial(name):
+    """KV demand beside attention on its own stream gives the same O, LSE,
+    bitmap, lists, gathered tiles and byte counts as the serial order, over
+    several back-to-back steps (the side streams' buffers are reused)."""
+    wl, data, shape = _setup(name)
+    args = [dev(data[x], wl) for x in ("q", "k", "v")]
+    kw = {}
+    if wl.estimator == "lowrank":
+        kw = dict(wq=torch.from_numpy(data["wq"]).cuda(), wk=torch.from_numpy(data["wk"]).cuda())
+    serial = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P, overlap_demand=False)
+    over = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P, overlap_demand=True)
+    o1, l1 = serial.forward(*args, **kw)
+    for _ in range(3):
+        o2, l2 = over.forward(*args, **kw)
+    torch.cuda.synchronize()
+    assert serial.status.item() == 0 and over.status.item() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    d1, d2 = serial.demand, over.demand
+    assert torch.equal(d1.bitmap, d2.bitmap) and torch.equal(d1.dem_ptr, d2.dem_ptr)
+    assert torch.equal(d1.bytes, d2.bytes)
+    total = int(d1.dem_ptr[-1].item())
+    assert torch.equal(d1.dem_idx[:total], d2.dem_idx[:total])
+    assert torch.equal(d1.kg[:total], d2.kg[:total]) and torch.equal(d1.vg[:total], d2.vg[:total])
 
 
 @pytest.mark.parametrize("name", ["medium", "r128"])
