@@ -189,6 +189,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--flat", action="store_true", help="flat (cross-head) longest-first order")
     ap.add_argument("--portable", action="store_true", help="mma.sync attention kernel")
+    ap.add_argument("--bwd-split-kv", action="store_true",
+                    help="backward: dK and dV by two tcgen05 kernels instead of one")
     ap.add_argument("--unfused", action="store_true", help="separate pooling pass instead of reorder+pool")
     ap.add_argument("--placement", action="store_true",
                     help="dependency-aware block placement inside the step (default: contiguous partitions)")
@@ -226,7 +228,8 @@ def main():
 
     data = synth.make(wl)
     shape = sp.shape_of(wl)
-    flags = (sp.SCHED_FLAT if args.flat else 0) | (sp.KERNEL_PORTABLE if args.portable else 0)
+    flags = ((sp.SCHED_FLAT if args.flat else 0) | (sp.KERNEL_PORTABLE if args.portable else 0)
+             | (sp.BWD_SPLIT_KV if args.bwd_split_kv else 0))
     pipe = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P, backward=wl.backward, flags=flags,
                        fused_estimation=not args.unfused, placement=args.placement,
                        migrations=wl.P if args.augment else None, augment=args.augment,
@@ -502,6 +505,8 @@ def main():
         "config": {**static_config(wl), "nnz_blocks": nnz, "density": nnz / (shape.rows * shape.nb),
                    "row_len_min_max": [int(counts.min()), int(counts.max())],
                    "schedule": "flat" if args.flat else "head-grouped longest-first",
+                   **({"backward_kernels": "dQ; dK and dV split" if args.bwd_split_kv else "dQ; dK + dV fused"}
+                      if wl.backward else {}),
                    "kernel": "portable mma.sync" if args.portable else "default",
                    "estimation": "separate pooling pass" if args.unfused else "fused with the reorder",
                    "partitions": "dependency-aware placement" if args.placement else "contiguous",

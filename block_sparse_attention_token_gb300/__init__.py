@@ -24,6 +24,7 @@ F32, BF16 = 0, 1
 EST_MEAN, EST_LOWRANK = 0, 1
 SCHED_FLAT = 1
 KERNEL_PORTABLE = 2
+BWD_SPLIT_KV = 4
 PROF_SLOTS = 1024
 
 

@@ -511,16 +511,20 @@ sparsp_status_t sparsp_attn_bwd(const sparsp_shape_t* shape, const void* q, cons
   if (r != SPARSP_OK) return r;
   if (tc) {
     r = launch_attn_bwd_tc(s, 0, (cb)q, (cb)k, (cb)v, (cb)dout, w.lse2, w.delta, row_ptr, col_idx, scale,
-                           (__nv_bfloat16*)dq, w.items, w.counter, prof, d_status, st);
+                           (__nv_bfloat16*)dq, nullptr, w.items, w.counter, prof, d_status, st);
     if (r != SPARSP_OK) return r;
     r = launch_lpt(s, w.col_ptr, flat, w.items2, w.counter + 1, w.hist, st);
     if (r != SPARSP_OK) return r;
+    if (!(flags & SPARSP_BWD_SPLIT_KV))
+      return launch_attn_bwd_tc(s, 3, (cb)q, (cb)k, (cb)v, (cb)dout, w.lse2, w.delta, w.col_ptr, w.row_idx,
+                                scale, (__nv_bfloat16*)dk, (__nv_bfloat16*)dv, w.items2, w.counter + 1, prof,
+                                d_status, st);
     r = launch_attn_bwd_tc(s, 1, (cb)q, (cb)k, (cb)v, (cb)dout, w.lse2, w.delta, w.col_ptr, w.row_idx,
-                           scale, (__nv_bfloat16*)dk, w.items2, w.counter + 1, prof, d_status, st);
+                           scale, (__nv_bfloat16*)dk, nullptr, w.items2, w.counter + 1, prof, d_status, st);
     if (r != SPARSP_OK) return r;
     if (cudaMemsetAsync(w.counter + 2, 0, sizeof(int32_t), st) != cudaSuccess) return SPARSP_ERR_CUDA;
     return launch_attn_bwd_tc(s, 2, (cb)q, (cb)k, (cb)v, (cb)dout, w.lse2, w.delta, w.col_ptr, w.row_idx,
-                              scale, (__nv_bfloat16*)dv, w.items2, w.counter + 2, prof, d_status, st);
+                              scale, (__nv_bfloat16*)dv, nullptr, w.items2, w.counter + 2, prof, d_status, st);
   }
   r = launch_attn_bwd_dq(s, (cb)q, (cb)k, (cb)v, (cb)dout, lse, w.delta, row_ptr, col_idx, scale,
                          (__nv_bfloat16*)dq, w.items, w.counter, prof, d_status, st);

@@ -6,6 +6,12 @@
 //   mode 1 (dK): item = key block j, blocks = the query blocks that selected it.
 //                S^T = K_j Q_c^T, dP^T = V_j dO_c^T, dS^T = P^T (dP^T - D), dK += dS^T Q_c.
 //   mode 2 (dV): item = key block j, as mode 1.  S^T = K_j Q_c^T, dV += P^T dO_c.
+//   mode 3 (dK and dV): modes 1 and 2 in one pass, both accumulators in TMEM
+//                [256,384) and [384,512); P^T is written over S^T and dS^T over
+//                dP^T, and the row tiles K_j, V_j stay in shared memory (no
+//                TMEM left for them), so S^T and dP^T take both operands from
+//                shared memory; the row tiles are released by an MMA commit
+//                after the item's last S^T / dP^T.
 // with P = exp2(S * scale*log2e - LSE*log2e) from the forward's LSE (no online
 // maximum is needed), D = rowsum(dO * O), and dQ, dK scaled by `scale` at the
 // end. Each column block is processed in two halves of 64 columns, double
@@ -59,6 +65,7 @@ constexpr uint32_t kHalfTile = BT * 64 * 2;   // one 64-column swizzled box
 constexpr uint32_t kStats = 1024;             // LSE*log2e [128] + D [128] of a column block
 constexpr int kThreads = 224;
 constexpr uint32_t kColAcc = 256, kColA1 = 384, kColA2 = 448;
+constexpr uint32_t kColAcc2 = 384;   // mode 3: the dV accumulator (A1, A2 stay in shared memory)
 constexpr int HB = 64;   // columns of a half block
 constexpr uint32_t kOffA2 = kTile, kOffStage = 2 * kTile;
 constexpr uint32_t kStageBytes = 2 * kTile + kStats;   // a multiple of 1024: tiles stay aligned
@@ -104,6 +111,8 @@ struct Params {
   const float* lse2;     // LSE * log2(e), [B*H*N]
   const float* delta;    // rowsum(dO * O), [B*H*N]
   __nv_bfloat16* out;
+  __nv_bfloat16* out2;   // mode 3: dV (out is dK)
+  float out_scale2;      // mode 3: scale for dV
   const int32_t* items;
   int32_t* counter;
   uint64_t* prof;
@@ -131,7 +140,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
 
   if (threadIdx.x == 0) {
     mbar_init(bar(A_FULL), 1);
-    mbar_init(bar(A_EMPTY), 128);
+    mbar_init(bar(A_EMPTY), MODE == 3 ? 1 : 128);   // mode 3: an MMA commit
     mbar_init(bar(AT_FULL), 128);
     for (int s = 0; s < kNS; ++s) {
       mbar_init(bar(C_FULL + s), 1);
@@ -264,8 +273,10 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
       if (ent.y == -2) break;
       if (ent.y <= 0) continue;
       const int len = ent.y;
-      if (!wait_warp(bar(AT_FULL), a_use & 1u, g)) break;   // the item's row tiles are in TMEM
+      // the item's row tiles: in TMEM (modes 0-2), in shared memory (mode 3)
+      if (!wait_warp(bar(MODE == 3 ? A_FULL : AT_FULL), a_use & 1u, g)) break;
       ++a_use;
+      fence_after();
       bool ok = true;
       for (int e = 0; e < len && ok; ++e) {
         const uint32_t st = c_use % kNS;
@@ -278,7 +289,23 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
           fence_after();
           // rows [64h, 64h+64) of the column tile: 64 rows x 128 B = 8 KB into each box
           const uint32_t rows_h = (uint32_t)h * (HB * 128u);
-          if (elect_one()) {
+          if constexpr (MODE == 3) {
+            if (elect_one()) {
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
+                mma_ss(tmem + 128u * b, smem_desc(sA1 + off, 16, 1024, kSwizzle128B),
+                       smem_desc(sb + rows_h + off, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
+              }
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
+                mma_ss(tmem + 128u * b + HB, smem_desc(sA2 + off, 16, 1024, kSwizzle128B),
+                       smem_desc(sb + kTile + rows_h + off, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
+              }
+              commit(bar(SD_FULL + b));
+            }
+          } else if (elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
@@ -302,6 +329,10 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
         ++c_use;
       }
       if (!ok) break;
+      if (MODE == 3) {   // the row tiles are free once this item's S^T and dP^T are done
+        if (elect_one()) commit(bar(A_EMPTY));
+        __syncwarp();
+      }
     }
     if (*abort_flag && issued_any) {
       if (elect_one()) commit(bar(TEAR));
@@ -337,11 +368,26 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
           fence_after();
           if (elect_one()) {
             // K = the half's 64 rows of the column tile: k-steps 4h .. 4h+3 of 16 rows (2 KB each)
+            const uint32_t acc = (e > 0 || h > 0) ? 1u : 0u;
+            if (MODE == 3) {
+              const uint32_t bq = stage(st), bdo = stage(st) + kTile;
 #pragma unroll
-            for (int kk = 0; kk < HB / 16; ++kk)
-              mma_ts(tmem + kColAcc, tmem + 128u * b + (uint32_t)kk * 8u,
-                     smem_desc(b3 + (uint32_t)(4 * h + kk) * 2048u, 16384, 1024, kSwizzle128B), idAcc,
-                     (e > 0 || h > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < HB / 16; ++kk)   // dV += P^T dO_c
+                mma_ts(tmem + kColAcc2, tmem + 128u * b + (uint32_t)kk * 8u,
+                       smem_desc(bdo + (uint32_t)(4 * h + kk) * 2048u, 16384, 1024, kSwizzle128B), idAcc,
+                       acc | (kk > 0 ? 1u : 0u));
+#pragma unroll
+              for (int kk = 0; kk < HB / 16; ++kk)   // dK += dS^T Q_c
+                mma_ts(tmem + kColAcc, tmem + 128u * b + HB + (uint32_t)kk * 8u,
+                       smem_desc(bq + (uint32_t)(4 * h + kk) * 2048u, 16384, 1024, kSwizzle128B), idAcc,
+                       acc | (kk > 0 ? 1u : 0u));
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < HB / 16; ++kk)
+                mma_ts(tmem + kColAcc, tmem + 128u * b + (uint32_t)kk * 8u,
+                       smem_desc(b3 + (uint32_t)(4 * h + kk) * 2048u, 16384, 1024, kSwizzle128B), idAcc,
+                       acc | (kk > 0 ? 1u : 0u));
+            }
             commit(bar(X_DONE + b));
             if (h == 1) commit(bar(C_EMPTY + st));   // last reader of this stage
             if (e + 1 == len && h == 1) commit(bar(ACC_FULL));
@@ -366,25 +412,31 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
     const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
     const float sl2 = p.sl2;
     uint32_t it_use = 0, c_use = 0, hg = 0, acc_items = 0, a_use = 0;
-    uint4* pending = nullptr;   // output row of the previous item, written once its accumulator is full
+    uint4* pending = nullptr;    // output row of the previous item, written once its accumulator is full
+    uint4* pending2 = nullptr;   // mode 3: its dV row
     bool ok = true;
-    // accumulator -> bf16 output row; frees the accumulator for the next item
-    auto epilogue = [&](uint4* orow) -> bool {
-      if (!wait_warp(bar(ACC_FULL), acc_items & 1u, g)) return false;
-      ++acc_items;
-      fence_after();
+    // one accumulator (128 columns at col) -> bf16 output row
+    auto acc_out = [&](uint32_t col, float scale, uint4* orow) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
-        tmem_ld32(t_row + kColAcc + c * 32u, o);
+        tmem_ld32(t_row + col + c * 32u, o);
         wait_ld();
         uint32_t w[16];
 #pragma unroll
         for (int x = 0; x < 16; ++x)
-          w[x] = pack2(__uint_as_float(o[2 * x]) * p.out_scale, __uint_as_float(o[2 * x + 1]) * p.out_scale);
+          w[x] = pack2(__uint_as_float(o[2 * x]) * scale, __uint_as_float(o[2 * x + 1]) * scale);
 #pragma unroll
         for (int x = 0; x < 4; ++x) orow[c * 4 + x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
       }
+    };
+    // accumulator(s) -> output row(s); frees the accumulators for the next item
+    auto epilogue = [&](uint4* orow, uint4* orow2) -> bool {
+      if (!wait_warp(bar(ACC_FULL), acc_items & 1u, g)) return false;
+      ++acc_items;
+      fence_after();
+      acc_out(kColAcc, p.out_scale, orow);
+      if (MODE == 3) acc_out(kColAcc2, p.out_scale2, orow2);
       fence_before();
       mbar_arrive(bar(ACC_EMPTY));
       return true;
@@ -422,27 +474,33 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
       const int i = (int)(item % nb);
       const int64_t row = bh * p.N + (int64_t)i * BT + threadIdx.x;
       uint4* orow = reinterpret_cast<uint4*>(p.out + row * D);
+      uint4* orow2 = MODE == 3 ? reinterpret_cast<uint4*>(p.out2 + row * D) : nullptr;
       const int len = ent.y;
       if (len == 0) {
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
+        if (MODE == 3)
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) orow2[c] = make_uint4(0, 0, 0, 0);
         continue;
       }
-      // the item's row tiles -> TMEM; the A region is free because every S/dP
-      // MMA of the previous item has completed (this thread consumed their SD_FULL)
-      if (!(ok = wait_warp(bar(A_FULL), a_use & 1u, g))) break;
-      ++a_use;
-      fence_after();
-      row_to_tmem(0u, kColA1);
-      if (kHasDP) row_to_tmem(kOffA2, kColA2);
-      wait_st();
-      fence_before();
-      mbar_arrive(bar(A_EMPTY));   // the shared-memory tiles can take the next item's
-      mbar_arrive(bar(AT_FULL));   // the S issuer may start this item
+      if (MODE != 3) {
+        // the item's row tiles -> TMEM; the A region is free because every S/dP
+        // MMA of the previous item has completed (this thread consumed their SD_FULL)
+        if (!(ok = wait_warp(bar(A_FULL), a_use & 1u, g))) break;
+        ++a_use;
+        fence_after();
+        row_to_tmem(0u, kColA1);
+        if (kHasDP) row_to_tmem(kOffA2, kColA2);
+        wait_st();
+        fence_before();
+        mbar_arrive(bar(A_EMPTY));   // the shared-memory tiles can take the next item's
+        mbar_arrive(bar(AT_FULL));   // the S issuer may start this item
+      }
       // the previous item's output, while this item's first S and dP run
       if (pending != nullptr) {
-        if (!(ok = epilogue(pending))) break;
-        pending = nullptr;
+        if (!(ok = epilogue(pending, pending2))) break;
+        pending = pending2 = nullptr;
       }
       // mode 0: this thread's query row has one LSE and one D
       const float own_l2 = MODE == 0 ? p.lse2[row] : 0.f;
@@ -463,41 +521,69 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
           }
           wait_ld();
           uint32_t xk[HB / 2];
+          if constexpr (MODE == 3) {
+            // P^T over S^T; dS^T = P^T (dP^T - D) over dP^T (both already in registers)
+            uint32_t xd[HB / 2];
 #pragma unroll
-          for (int x4 = 0; x4 < HB / 4; ++x4) {
-            float l2[4], dd[4];
-            if (MODE == 0) {
+            for (int x4 = 0; x4 < HB / 4; ++x4) {
+              const float4 L = stats[16 * h + x4];
+              const float4 Dv = stats[32 + 16 * h + x4];
+              const float l2[4] = {L.x, L.y, L.z, L.w}, dd[4] = {Dv.x, Dv.y, Dv.z, Dv.w};
+              float pr[4], ds[4];
 #pragma unroll
-              for (int u = 0; u < 4; ++u) { l2[u] = own_l2; dd[u] = own_d; }
-            } else {
-              const float4 L = stats[16 * h + x4];          // LSE*log2e of columns 64h+4x4 .. +3
-              const float4 Dv = stats[32 + 16 * h + x4];    // D of the same columns
-              l2[0] = L.x; l2[1] = L.y; l2[2] = L.z; l2[3] = L.w;
-              dd[0] = Dv.x; dd[1] = Dv.y; dd[2] = Dv.z; dd[3] = Dv.w;
+              for (int u = 0; u < 4; ++u) {
+                const int x = 4 * x4 + u;
+                pr[u] = ex2f(fmaf(__uint_as_float(sv[x]), sl2, -l2[u]));
+                ds[u] = pr[u] * (__uint_as_float(dv[x]) - dd[u]);
+              }
+              xk[2 * x4] = pack2(pr[0], pr[1]);
+              xk[2 * x4 + 1] = pack2(pr[2], pr[3]);
+              xd[2 * x4] = pack2(ds[0], ds[1]);
+              xd[2 * x4 + 1] = pack2(ds[2], ds[3]);
             }
-            float v[4];
+            tmem_st32(t_row + 128u * b, xk);
+            tmem_st32(t_row + 128u * b + HB, xd);
+            wait_st();
+            fence_before();
+            mbar_arrive(bar(X_FULL + b));
+          } else {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int x = 4 * x4 + u;
-              const float pr = ex2f(fmaf(__uint_as_float(sv[x]), sl2, -l2[u]));
-              v[u] = kHasDP ? pr * (__uint_as_float(dv[x]) - dd[u]) : pr;
+            for (int x4 = 0; x4 < HB / 4; ++x4) {
+              float l2[4], dd[4];
+              if (MODE == 0) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) { l2[u] = own_l2; dd[u] = own_d; }
+              } else {
+                const float4 L = stats[16 * h + x4];          // LSE*log2e of columns 64h+4x4 .. +3
+                const float4 Dv = stats[32 + 16 * h + x4];    // D of the same columns
+                l2[0] = L.x; l2[1] = L.y; l2[2] = L.z; l2[3] = L.w;
+                dd[0] = Dv.x; dd[1] = Dv.y; dd[2] = Dv.z; dd[3] = Dv.w;
+              }
+              float v[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int x = 4 * x4 + u;
+                const float pr = ex2f(fmaf(__uint_as_float(sv[x]), sl2, -l2[u]));
+                v[u] = kHasDP ? pr * (__uint_as_float(dv[x]) - dd[u]) : pr;
+              }
+              xk[2 * x4] = pack2(v[0], v[1]);
+              xk[2 * x4 + 1] = pack2(v[2], v[3]);
             }
-            xk[2 * x4] = pack2(v[0], v[1]);
-            xk[2 * x4 + 1] = pack2(v[2], v[3]);
+            // X over the first 32 columns of this half's S (already in registers)
+            tmem_st32(t_row + 128u * b, xk);
+            wait_st();
+            fence_before();
+            mbar_arrive(bar(X_FULL + b));
           }
-          // X over the first 32 columns of this half's S (already in registers)
-          tmem_st32(t_row + 128u * b, xk);
-          wait_st();
-          fence_before();
-          mbar_arrive(bar(X_FULL + b));
           ++hg;
         }
         ++c_use;
       }
       if (!ok) break;
       pending = orow;
+      pending2 = orow2;
     }
-    if (ok && pending != nullptr) epilogue(pending);
+    if (ok && pending != nullptr) epilogue(pending, pending2);
   }
 
   fence_before();
@@ -533,8 +619,8 @@ sparsp_status_t launch_attn_bwd_tc(const Dims& s, int mode, const __nv_bfloat16*
                                    const __nv_bfloat16* k, const __nv_bfloat16* v,
                                    const __nv_bfloat16* dout, const float* lse2,
                                    const float* delta, const int32_t* ptr, const int32_t* idx,
-                                   float scale, __nv_bfloat16* out, const int32_t* items,
-                                   int32_t* counter, uint64_t* prof, int32_t* d_status,
+                                   float scale, __nv_bfloat16* out, __nv_bfloat16* out2,
+                                   const int32_t* items, int32_t* counter, uint64_t* prof, int32_t* d_status,
                                    cudaStream_t st) {
   const uint64_t rows = (uint64_t)s.B * s.H * s.N;
   CUtensorMap tq, tk, tv, tdo;
@@ -542,9 +628,10 @@ sparsp_status_t launch_attn_bwd_tc(const Dims& s, int mode, const __nv_bfloat16*
       !make_tmap_bf16_rows(&tv, v, rows, D, BT) || !make_tmap_bf16_rows(&tdo, dout, rows, D, BT))
     return SPARSP_ERR_CUDA;
   Params prm{ptr, idx, s.N, s.nb, s.rows(), scale * 1.4426950408889634f, mode == 2 ? 1.0f : scale,
-             lse2, delta, out, items, counter, prof, d_status};
+             lse2, delta, out, out2, 1.0f, items, counter, prof, d_status};
   if (mode == 0) return go<0>(s, tq, tdo, tk, tv, prm, st);
   if (mode == 1) return go<1>(s, tk, tv, tq, tdo, prm, st);
+  if (mode == 3) return go<3>(s, tk, tv, tq, tdo, prm, st);
   return go<2>(s, tk, tk, tq, tdo, prm, st);
 }
 

@@ -134,14 +134,15 @@ sparsp_status_t launch_attn_fwd_tc(const Dims& s, const __nv_bfloat16* q, const 
 sparsp_status_t launch_bwd_rowdot(const Dims& s, const __nv_bfloat16* o, const __nv_bfloat16* dout,
                                   float* delta, const float* lse, float* lse2, cudaStream_t st);
 // tcgen05 backward (bf16, Bt = d = 128). mode 0: dQ over the CSR rows;
-// mode 1: dK, mode 2: dV over the transposed CSR. `lse2` = LSE * log2(e).
+// mode 1: dK, mode 2: dV, mode 3: dK (out) and dV (out2) over the transposed
+// CSR. `lse2` = LSE * log2(e).
 bool attn_bwd_tc_supported(const Dims& s);
 sparsp_status_t launch_attn_bwd_tc(const Dims& s, int mode, const __nv_bfloat16* q,
                                    const __nv_bfloat16* k, const __nv_bfloat16* v,
                                    const __nv_bfloat16* dout, const float* lse2,
                                    const float* delta, const int32_t* ptr, const int32_t* idx,
-                                   float scale, __nv_bfloat16* out, const int32_t* items,
-                                   int32_t* counter, uint64_t* prof, int32_t* d_status,
+                                   float scale, __nv_bfloat16* out, __nv_bfloat16* out2,
+                                   const int32_t* items, int32_t* counter, uint64_t* prof, int32_t* d_status,
                                    cudaStream_t st);
 sparsp_status_t launch_attn_bwd_dq(const Dims& s, const __nv_bfloat16* q, const __nv_bfloat16* k,
                                    const __nv_bfloat16* v, const __nv_bfloat16* dout,

@@ -39,9 +39,11 @@ class Pipeline:
         return 3 + scores + pred + 3 + bal + place + 4 + gather + lpt + 1 + 1
 
     def kernels_per_backward(self) -> int:
-        """reorder dO, rowdot, CSR transpose, schedule, dQ, schedule, dK/dV, 3 inverse reorders."""
+        """reorder dO, rowdot, CSR transpose, schedule, dQ, schedule, dK + dV (one
+        kernel, two with BWD_SPLIT_KV), 3 inverse reorders."""
         lpt = 2 if self.flags & 1 else 1
-        return 1 + 1 + 1 + lpt + 1 + lpt + 1 + 3
+        kv = 2 if self.flags & 4 else 1
+        return 1 + 1 + 1 + lpt + 1 + lpt + kv + 3
 
     def __init__(self, shape: Shape, estimator: str, top_p: float, k_floor: int, P: int, rank: int = 16,
                  gather: bool = True, flags: int = 0, backward: bool = False, device="cuda",

@@ -90,7 +90,10 @@ enum {
    * head-grouped longest-first (see sparsp_lpt_schedule). */
   SPARSP_SCHED_FLAT = 1u << 0,
   /* Use the portable mma.sync kernel even where the tcgen05 kernel applies. */
-  SPARSP_KERNEL_PORTABLE = 1u << 1
+  SPARSP_KERNEL_PORTABLE = 1u << 1,
+  /* Backward on tcgen05: dK and dV by two kernels (each recomputing S^T)
+   * instead of one kernel that accumulates both. */
+  SPARSP_BWD_SPLIT_KV = 1u << 2
 };
 
 /* Per-SM profile slots that attention kernels accumulate into (see prof). */
@@ -385,7 +388,8 @@ SPARSP_API sparsp_status_t sparsp_attn_fwd(const sparsp_shape_t* shape, const vo
  *   dV = P^T dO; dS = P * (dO V^T - D); dQ = scale dS K; dK = scale dS^T Q.
  * bf16 only. dq, dk, dv: blocked [B,H,N,d] bf16. dQ is accumulated per query
  * block over its CSR row and dK/dV per key block over the transposed CSR, so
- * the result is deterministic (no atomics on values).
+ * the result is deterministic (no atomics on values). On tcgen05 one kernel
+ * computes dQ and one both dK and dV (two with SPARSP_BWD_SPLIT_KV).
  * ws: at least sparsp_attn_workspace_size(shape, 1) bytes.
  */
 SPARSP_API sparsp_status_t sparsp_attn_bwd(const sparsp_shape_t* shape, const void* q, const void* k,

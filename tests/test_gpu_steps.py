@@ -616,6 +616,14 @@ def test_attn_bwd(name):
     # deterministic: a second run is bitwise identical
     dq2, dk2, dv2 = sp.attn_bwd(shape, q, k, v, o, lse, dev(dob, wl), rp, ci, flags=sp.SCHED_FLAT)
     assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
+    # dK and dV by two kernels instead of one: the same gradients against the oracle
+    st3 = status_word()
+    dq3, dk3, dv3 = sp.attn_bwd(shape, q, k, v, o, lse, dev(dob, wl), rp, ci, flags=sp.BWD_SPLIT_KV, status=st3)
+    torch.cuda.synchronize()
+    assert st3.item() == 0
+    assert torch.equal(dq, dq3)
+    compare_values(host(dk3), dK, wl, "dK (two kernels)")
+    compare_values(host(dv3), dV, wl, "dV (two kernels)")
 
 
 @pytest.mark.parametrize("fused", [True, False])
