@@ -1,5 +1,6 @@
 // Step 5b, bf16, Bt = d = 128 on sm_103a: block-sparse attention backward on
-// the tcgen05 tensor cores, as three persistent kernels of one template.
+// the tcgen05 tensor cores, as persistent kernels of one template: mode 0 and
+// mode 3 by default, modes 0, 1 and 2 when dK and dV are asked for apart.
 //
 //   mode 0 (dQ): item = query block i, blocks = its CSR row.
 //                S = Q_i K_c^T, dP = dO_i V_c^T, dS = P (dP - D), dQ += dS K_c.
@@ -24,8 +25,9 @@
 // MMA takes A from TMEM and only B from shared memory (a 128x64x16 MMA with
 // both operands in shared memory is bound by shared-memory bandwidth at 62% of
 // the tensor rate; with A in TMEM it runs at the full rate). A half buffer is
-// free again once the accumulate MMA that read its X has completed. The three
-// kernels recompute S (and dP) instead of sharing it so that each fits TMEM.
+// free again once the accumulate MMA that read its X has completed. The dQ
+// and the dK/dV kernels recompute S (and dP) instead of sharing it so that
+// each fits TMEM. Modes 0-2 are laid out as above; mode 3 as described with it.
 // Sums are taken in a fixed order (no atomics), so results are bitwise
 // reproducible.
 //
@@ -34,16 +36,16 @@
 //              TMA-loads the item's two row tiles (A1, A2) once (the softmax
 //              warps copy them into TMEM) and, per block,
 //              the two column tiles (B1, B2; two 64-column boxes each, 128-byte
-//              swizzle) into a 2-stage ring; in modes 1 and 2 also the block's
+//              swizzle) into a 2-stage ring; in modes 1-3 also the block's
 //              LSE*log2e and D (512 bytes each) by 1-D bulk copy.
-//   warp 5     S issuer: per half, S = A1 B1_h^T and (modes 0, 1)
-//              dP = A2 B2_h^T (N = 64), A from TMEM, B K-major from shared
-//              memory.
+//   warp 5     S issuer: per half, S = A1 B1_h^T and (modes 0, 1, 3)
+//              dP = A2 B2_h^T (N = 64), A from TMEM (from shared memory in
+//              mode 3), B K-major from shared memory.
 //   warp 6     accumulate issuer: per half, ACC += X B3_h (K = 64) with X from
 //              TMEM and B3 (the column tile K_c, Q_c or dO_c) MN-major from
-//              shared memory.
+//              shared memory; mode 3 issues dV += P^T dO_c and dK += dS^T Q_c.
 //   warps 0-3  thread t owns row t (TMEM lane t): copies its rows of A1, A2
-//              into TMEM at the start of an item; per half loads S and dP,
+//              into TMEM at the start of an item (modes 0-2); per half loads S and dP,
 //              computes P and dS in fp32 from them and the statistics, packs
 //              the operand to bf16 into X; epilogue ACC -> global, deferred
 //              until the next item's row tiles are in TMEM so that its first
