@@ -19,7 +19,10 @@
 //              other; each warp runs uniformly and one elected lane issues
 //              tcgen05.mma / tcgen05.commit.
 //   warps 0-3  softmax and epilogue: thread t owns query row t = TMEM lane t.
-//              It reads its S row from TMEM, keeps a running max m and sum l in
+//              It reads its S row from TMEM with the sm_103 load-with-maximum
+//              (tcgen05.ld.red: each 32-column load also returns the maximum of
+//              the 32 values, so the row max costs no extra instructions), keeps
+//              a running max m and sum l in
 //              base 2, writes P = exp2(S*scale*log2e - m) as bf16 into TMEM, and
 //              rescales its O row in TMEM only when the row max grows by more
 //              than 8 (a factor 256); otherwise the stale max is kept, which
@@ -79,10 +82,20 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
+// 32 columns of this thread's TMEM lane, and their maximum (sm_103 load with
+// reduction)
+__device__ __forceinline__ float tmem_ld32_max(uint32_t taddr, uint32_t* r) {
+  float m;
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=f"(m)
+      : "r"(taddr));
+  return m;
 }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -382,26 +395,16 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         if (!(ok = wait_warp(bar(S_FULL + b), (s_use >> 1) & 1u, g))) break;
         fence_after();
         uint32_t s[BT];
+        float cm[BT / 32];   // the maximum of each 32-column load (exact, as any order of max)
 #pragma unroll
-        for (int c = 0; c < BT / 32; ++c) tmem_ld32(t_row + kColS + b * 128u + c * 32u, s + 32 * c);
+        for (int c = 0; c < BT / 32; ++c) cm[c] = tmem_ld32_max(t_row + kColS + b * 128u + c * 32u, s + 32 * c);
         wait_ld();
         fence_before();
         mbar_arrive(bar(S_FREE + b));
         ++s_use;
-        // row max as a tree of 3-input maxima (8 independent partials): max is
-        // exact in any order, and a serial chain would sit on the critical path
-        float part[8];
+        float mx = cm[0];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) part[u] = __uint_as_float(s[u]);
-#pragma unroll
-        for (int c = 8; c + 16 <= BT; c += 16)
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            part[u] = fmax3(part[u], __uint_as_float(s[c + u]), __uint_as_float(s[c + 8 + u]));
-#pragma unroll
-        for (int u = 0; u < 8; ++u) part[u] = fmaxf(part[u], __uint_as_float(s[BT - 8 + u]));
-        const float mx = fmax3(fmax3(part[0], part[1], part[2]), fmax3(part[3], part[4], part[5]),
-                               fmaxf(part[6], part[7]));
+        for (int c = 1; c < BT / 32; ++c) mx = fmaxf(mx, cm[c]);
         const float m_new = fmaxf(m, mx * sl2);
         if (e == 0) {
           m = m_new;
