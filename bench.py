@@ -38,6 +38,27 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
+def stage_times(marks, side, elapsed, steps):
+    """Per-step stage times (ms) from [(name, event)] in enqueue order. A stage
+    runs from its "<name>:begin" mark if it has one (a stage overlapped on its
+    own stream), else from the mark before it; marks of the names in `side`
+    (recorded on side streams) do not start the next stage. elapsed(a, b) is
+    the time from event a to event b; "step_start" opens each step."""
+    out = {}
+    prev = None
+    begins = {}
+    for name, ev in marks:
+        if name.endswith(":begin"):
+            begins[name[:-len(":begin")]] = ev
+            continue
+        if name != "step_start":
+            first = begins.pop(name, prev)
+            out[name] = out.get(name, 0.0) + elapsed(first, ev)
+        if name not in side:
+            prev = ev
+    return {k: v / steps for k, v in out.items()}
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -282,21 +303,8 @@ def main():
     barrier()
     clk = clocks.stop()
     total_ms = start.elapsed_time(end)
-    # a stage runs from its "<name>:begin" mark if it has one (stages overlapped on
-    # their own streams), else from the mark before it
-    stage_ms = {}
-    prev = None
-    begins = {}
-    for name, ev in marks:
-        if name.endswith(":begin"):
-            begins[name[:-len(":begin")]] = ev
-            continue
-        if name != "step_start":
-            first = begins.pop(name, prev)
-            stage_ms[name] = stage_ms.get(name, 0.0) + first.elapsed_time(ev)
-        if name not in ("attn_fwd", "kv_gather") or not pipe.overlap_demand:
-            prev = ev
-    stage_ms = {k: v / args.steps for k, v in stage_ms.items()}
+    side = ("attn_fwd", "kv_gather") if pipe.overlap_demand else ()
+    stage_ms = stage_times(marks, side, lambda a, b: a.elapsed_time(b), args.steps)
     ms_step = total_ms / args.steps
     ms_step = replicas.max_over_ranks(ms_step)
 
