@@ -25,6 +25,7 @@ EST_MEAN, EST_LOWRANK = 0, 1
 SCHED_FLAT = 1
 KERNEL_PORTABLE = 2
 BWD_SPLIT_KV = 4
+OUT_RASTER = 8
 PROF_SLOTS = 1024
 
 
@@ -398,10 +399,11 @@ def attn_workspace_size(shape: Shape, backward: bool = False) -> int:
 
 def attn_fwd(shape: Shape, q, k, v, row_ptr, col_idx, scale: float = 0.0, o=None, lse=None, ws=None,
              flags: int = 0, prof=None, status=None, stream=None):
-    """Returns (O blocked [B,H,N,d], LSE [B,H,N] fp32)."""
+    """Returns (O blocked [B,H,N,d], or raster [B,N,H,d] with OUT_RASTER; LSE [B,H,N] fp32)."""
     dev = q.device
     if o is None:
-        o = torch.empty_like(q)
+        o = (torch.empty((shape.B, shape.N, shape.H, shape.d), dtype=q.dtype, device=dev)
+             if flags & OUT_RASTER else torch.empty_like(q))
     if lse is None:
         lse = torch.empty((shape.B, shape.H, shape.N), dtype=torch.float32, device=dev)
     if ws is None:

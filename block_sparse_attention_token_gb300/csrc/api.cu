@@ -455,6 +455,9 @@ sparsp_status_t sparsp_attn_fwd(const sparsp_shape_t* shape, const void* q, cons
   AttnWs w = attn_ws_layout(s, false, ws);
   if (ws_bytes < w.bytes) return SPARSP_ERR_WORKSPACE;
   if (scale <= 0.f) scale = 1.0f / sqrtf((float)s.d);
+  const bool tc = s.dtype != SPARSP_F32 && !(flags & SPARSP_KERNEL_PORTABLE) && attn_fwd_tc_supported(s);
+  const bool raster = (flags & SPARSP_OUT_RASTER) != 0;
+  if (raster && !tc) return SPARSP_ERR_UNSUPPORTED;   // only the tcgen05 kernel writes raster rows
   cudaStream_t st = (cudaStream_t)stream;
   r = launch_lpt(s, row_ptr, (flags & SPARSP_SCHED_FLAT) != 0, w.items, w.counter, w.hist, st);
   if (r != SPARSP_OK) return r;
@@ -462,10 +465,10 @@ sparsp_status_t sparsp_attn_fwd(const sparsp_shape_t* shape, const void* q, cons
     return launch_attn_fwd_f32(s, (const float*)q, (const float*)k, (const float*)v, row_ptr,
                                col_idx, scale, (float*)o, lse, w.items, w.counter, prof, d_status,
                                st);
-  if (!(flags & SPARSP_KERNEL_PORTABLE) && attn_fwd_tc_supported(s))
+  if (tc)
     return launch_attn_fwd_tc(s, (const __nv_bfloat16*)q, (const __nv_bfloat16*)k,
                               (const __nv_bfloat16*)v, row_ptr, col_idx, scale,
-                              (__nv_bfloat16*)o, lse, w.items, w.counter, prof, d_status, st);
+                              (__nv_bfloat16*)o, lse, raster, w.items, w.counter, prof, d_status, st);
   return launch_attn_fwd_mma(s, (const __nv_bfloat16*)q, (const __nv_bfloat16*)k,
                              (const __nv_bfloat16*)v, row_ptr, col_idx, scale, (__nv_bfloat16*)o,
                              lse, w.items, w.counter, prof, d_status, st);

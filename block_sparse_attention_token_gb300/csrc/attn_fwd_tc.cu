@@ -112,6 +112,9 @@ struct Params {
   float scale_log2;
   __nv_bfloat16* o;
   float* lse;
+  // raster output: O row (b, h, token) at ((b*N + n)*H + h)*d with n the token's
+  // raster index (t slowest, x fastest); otherwise block order like Q
+  int raster, H, Y, X, ta, tb, tc, nY, nX;
   const int32_t* items;
   int32_t* counter;
   uint64_t* prof;
@@ -378,7 +381,17 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       const int i = (int)(item % nb);
       const int64_t row = bh * p.N + (int64_t)i * BT + threadIdx.x;
       const bool stores = threadIdx.x < BT;   // rows past the block are computed, never stored
-      uint4* orow = reinterpret_cast<uint4*>(p.o + row * D);
+      int64_t orow_idx = row;
+      if (p.raster && stores) {
+        // tile i = (bt, by, bx) block-raster; token o = (it, iy, ix) raster inside the tile
+        const int o = threadIdx.x, tbc = p.tb * p.tc;
+        const int bx = i % p.nX, by = (i / p.nX) % p.nY, bt = i / (p.nX * p.nY);
+        const int it = o / tbc, iy = (o - it * tbc) / p.tc, ix = o - it * tbc - iy * p.tc;
+        const int64_t n = ((int64_t)bt * p.ta + it) * p.Y * p.X + ((int64_t)by * p.tb + iy) * p.X +
+                          (int64_t)bx * p.tc + ix;
+        orow_idx = ((bh / p.H) * p.N + n) * p.H + bh % p.H;
+      }
+      uint4* orow = reinterpret_cast<uint4*>(p.o + orow_idx * D);
       const int len = ent.y;
       if (len == 0) {
         if (stores) {
@@ -520,7 +533,7 @@ sparsp_status_t go_fwd(const Dims& s, const CUtensorMap& tq, const CUtensorMap& 
 sparsp_status_t launch_attn_fwd_tc(const Dims& s, const __nv_bfloat16* q, const __nv_bfloat16* k,
                                    const __nv_bfloat16* v, const int32_t* row_ptr,
                                    const int32_t* col_idx, float scale, __nv_bfloat16* o,
-                                   float* lse, const int32_t* items, int32_t* counter,
+                                   float* lse, bool raster, const int32_t* items, int32_t* counter,
                                    uint64_t* prof, int32_t* d_status, cudaStream_t st) {
   const uint64_t rows = (uint64_t)s.B * s.H * s.N;
   CUtensorMap tq, tk, tv;
@@ -529,8 +542,8 @@ sparsp_status_t launch_attn_fwd_tc(const Dims& s, const __nv_bfloat16* q, const 
       !make_tmap_bf16_rows(&tk, k, rows, (uint64_t)s.d, (uint32_t)s.Bt) ||
       !make_tmap_bf16_rows(&tv, v, rows, (uint64_t)s.d, (uint32_t)s.Bt))
     return SPARSP_ERR_CUDA;
-  Params prm{row_ptr, col_idx, s.N, s.nb, s.rows(), scale * 1.4426950408889634f, o, lse, items,
-             counter, prof, d_status};
+  Params prm{row_ptr, col_idx, s.N, s.nb, s.rows(), scale * 1.4426950408889634f, o, lse,
+             raster ? 1 : 0, s.H, s.Y, s.X, s.ta, s.tb, s.tc, s.nY, s.nX, items, counter, prof, d_status};
   if (s.Bt == 128 && s.d == 128) return go_fwd<128, 128>(s, tq, tk, tv, prm, st);
   if (s.Bt == 128 && s.d == 64) return go_fwd<128, 64>(s, tq, tk, tv, prm, st);
   if (s.Bt == 64 && s.d == 128) return go_fwd<64, 128>(s, tq, tk, tv, prm, st);

@@ -127,7 +127,7 @@ bool attn_fwd_tc_supported(const Dims& s);
 sparsp_status_t launch_attn_fwd_tc(const Dims& s, const __nv_bfloat16* q, const __nv_bfloat16* k,
                                    const __nv_bfloat16* v, const int32_t* row_ptr,
                                    const int32_t* col_idx, float scale, __nv_bfloat16* o,
-                                   float* lse, const int32_t* items, int32_t* counter,
+                                   float* lse, bool raster, const int32_t* items, int32_t* counter,
                                    uint64_t* prof, int32_t* d_status, cudaStream_t st);
 
 // Attention backward pieces.

@@ -19,7 +19,8 @@ import torch
 from . import (EST_LOWRANK, EST_MEAN, PROF_SLOTS, Shape, attn_bwd, attn_fwd, attn_workspace_size, augment,
                augment_workspace_size, balance_heads, Balance, predictor_fit,
                block_scores, block_scores_pooled, block_scores_workspace_size, kv_demand, kv_gather, lib, placement,
-               placement_workspace_size, reorder, reorder_pool, select, select_workspace_size, DemandOut)
+               placement_workspace_size, reorder, reorder_pool, select, select_workspace_size, DemandOut,
+               OUT_RASTER)
 
 
 class Pipeline:
@@ -28,7 +29,7 @@ class Pipeline:
         scan, fill), predictor fitting x7 when enabled, balancing (1) and augmentation x14 (keys, slack, four
         histogram + digit passes, row counts, ties, scan, fill) when enabled, placement x2 (affinity, greedy) when
         enabled, demand x5 (counter reset, bitmap, scan, list, gather), schedule (1, or 2 in
-        flat order) + attention, inverse reorder."""
+        flat order) + attention, inverse reorder (none when attention writes raster O)."""
         lpt = 2 if self.flags & 1 else 1
         gather = 1 if self.demand.kg is not None else 0
         scores = (2 if self.est == EST_LOWRANK else 1) if self.fused else 2
@@ -36,7 +37,7 @@ class Pipeline:
         bal = (1 if self.migrations is not None else 0) + (14 if self.augment else 0)
         # projection, two score products, gradient products, loss (partials, sum), weight gradients
         pred = 7 if self.predictor_lr is not None else 0
-        return 3 + scores + pred + 3 + bal + place + 4 + gather + lpt + 1 + 1
+        return 3 + scores + pred + 3 + bal + place + 4 + gather + lpt + 1 + (0 if self.raster_out else 1)
 
     def kernels_per_backward(self) -> int:
         """reorder dO, rowdot, CSR transpose, schedule, dQ, schedule, dK + dV (one
@@ -99,6 +100,10 @@ class Pipeline:
             self.gwq, self.gwk = (torch.empty((s.H, s.d, rank), dtype=torch.float32, device=dev) for _ in range(2))
             self.ws_pred = torch.empty(max(lib().sparsp_predictor_workspace_size(ctypes.byref(s), rank), 16),
                                        dtype=torch.uint8, device=dev)
+        # forward-only steps on the tcgen05 kernel take O straight into raster order (the
+        # backward needs it in block order)
+        self.raster_out = (not backward and s.torch_dtype == torch.bfloat16 and not (flags & 2)
+                           and s.Bt in (64, 128) and s.d in (64, 128))
         self.overlap_demand = overlap_demand
         if overlap_demand:
             lo, hi = torch.cuda.Stream.priority_range()   # least, greatest
@@ -173,6 +178,9 @@ class Pipeline:
         if self.owner is not None:
             placement(s, self.P, rp, ci, self.owner, self.ws_place, self.status)
             mark("placement")
+        o = self.o if out is None else out
+        # attention output: raster O directly, or block order and an inverse reorder
+        o_attn, aflags = (o, self.flags | OUT_RASTER) if self.raster_out else (self.ob, self.flags)
         if self.overlap_demand and self.demand.kg is not None:
             # the lists (bitmap, offsets, indices) first, on this stream: they need a
             # little shared memory, which attention leaves none of; then the gather
@@ -188,8 +196,8 @@ class Pipeline:
             lo.wait_event(self._selected)
             with torch.cuda.stream(hi):   # enqueued first: the persistent CTAs take their SMs first
                 mark("attn_fwd:begin", hi)
-                attn_fwd(s, self.qb, self.kb, self.vb, rp, ci, 0.0, self.ob, self.lse, self.ws_attn,
-                         self.flags, self.prof if prof else None, self.status, stream=hi)
+                attn_fwd(s, self.qb, self.kb, self.vb, rp, ci, 0.0, o_attn, self.lse, self.ws_attn,
+                         aflags, self.prof if prof else None, self.status, stream=hi)
                 mark("attn_fwd", hi)
             with torch.cuda.stream(lo):
                 mark("kv_gather:begin", lo)
@@ -201,12 +209,12 @@ class Pipeline:
         else:
             kv_demand(s, self.P, rp, ci, self.kb, self.vb, out=self.demand, status=self.status, owner=self.owner)
             mark("kv_demand")
-            attn_fwd(s, self.qb, self.kb, self.vb, rp, ci, 0.0, self.ob, self.lse, self.ws_attn,
-                     self.flags, self.prof if prof else None, self.status)
+            attn_fwd(s, self.qb, self.kb, self.vb, rp, ci, 0.0, o_attn, self.lse, self.ws_attn,
+                     aflags, self.prof if prof else None, self.status)
             mark("attn_fwd")
-        o = self.o if out is None else out
-        reorder(s, self.ob, o, inverse=True)
-        mark("reorder_out")
+        if not self.raster_out:
+            reorder(s, self.ob, o, inverse=True)
+            mark("reorder_out")
         return o, self.lse
 
     def backward(self, dout, prof: bool = False, mark=None, outs=None):

@@ -93,7 +93,13 @@ enum {
   SPARSP_KERNEL_PORTABLE = 1u << 1,
   /* Backward on tcgen05: dK and dV by two kernels (each recomputing S^T)
    * instead of one kernel that accumulates both. */
-  SPARSP_BWD_SPLIT_KV = 1u << 2
+  SPARSP_BWD_SPLIT_KV = 1u << 2,
+  /* Forward: write O in raster order [B, N, H, d] (the layout of the inverse
+   * sparsp_reorder) instead of block order; LSE stays [B, H, N] in block
+   * order. Only the tcgen05 kernel (bf16 on sm_103a, Bt and d in {64, 128},
+   * without SPARSP_KERNEL_PORTABLE) does this; elsewhere the call returns
+   * SPARSP_ERR_UNSUPPORTED before enqueuing anything. */
+  SPARSP_OUT_RASTER = 1u << 3
 };
 
 /* Per-SM profile slots that attention kernels accumulate into (see prof). */
@@ -364,7 +370,8 @@ SPARSP_API sparsp_status_t sparsp_lpt_schedule(const sparsp_shape_t* shape, cons
  * selected pairs, never materialising the full score matrix). For each query
  * token q of block i, over the key tokens of the blocks in row (b,h,i):
  *   O_q = sum_k softmax_k(scale q.k) v_k,   LSE_q = ln sum_k exp(scale q.k).
- * q, k, v, o: blocked [B,H,N,d]; lse: float32 [B,H,N]. scale <= 0 means
+ * q, k, v, o: blocked [B,H,N,d] (o raster [B,N,H,d] with SPARSP_OUT_RASTER);
+ * lse: float32 [B,H,N]. scale <= 0 means
  * 1/sqrt(d). An empty row gives O = 0, LSE = -inf. A row with an index outside
  * [0, nb) or more than nb entries sets SPARSP_ERR_DATA and is skipped.
  * bf16 on sm_103a runs the tcgen05/TMEM/TMA kernel (Bt and d in {64, 128});

@@ -557,6 +557,27 @@ def test_attn_fwd_schedules_and_kernels_agree_bitwise(name):
     assert torch.equal(o1, o5) and torch.equal(l1, l5)
 
 
+@pytest.mark.parametrize("name", ["medium", "r128", "r64", "r128d64", "wave"])
+def test_attn_fwd_raster_output(name):
+    """O written straight into raster order equals the inverse reorder of the
+    block-ordered O, bit for bit, and LSE is unchanged; the kernels without
+    raster stores refuse the flag."""
+    wl, data, shape = _setup(name)
+    ch = OracleChain(wl, data)
+    q, k, v = dev(ch.qb, wl), dev(ch.kb, wl), dev(ch.vb, wl)
+    rp, ci = i32(ch.sel.row_ptr), i32(ch.sel.col_idx)
+    st = status_word()
+    ob, lb = sp.attn_fwd(shape, q, k, v, rp, ci, status=st)
+    o_r, lr = sp.attn_fwd(shape, q, k, v, rp, ci, flags=sp.OUT_RASTER, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert o_r.shape == (shape.B, shape.N, shape.H, shape.d)
+    assert torch.equal(o_r, sp.reorder(shape, ob, inverse=True))
+    assert torch.equal(lr, lb)
+    with pytest.raises(sp.SparspError):
+        sp.attn_fwd(shape, q, k, v, rp, ci, flags=sp.OUT_RASTER | sp.KERNEL_PORTABLE)
+
+
 @pytest.mark.parametrize("portable", [False, True])
 @pytest.mark.parametrize("name", ["r128", "tiny", "r64"])
 def test_attn_fwd_empty_and_bad_rows(name, portable):
@@ -729,8 +750,8 @@ def test_pipeline_with_balance_and_augment(name):
     hr, _ = orc.balance_heads(costs, wl.P, wl.P)
     assert np.array_equal(host(pipe.balance.head_rank), hr)
     assert int(rp[-1]) == int(rp0[-1]) + int(host(pipe.added).sum())
-    assert pipe.kernels_per_forward() == sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor,
-                                                      wl.P).kernels_per_forward() + 15
+    assert pipe.kernels_per_forward() == sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P,
+                                                      backward=True).kernels_per_forward() + 15
     qb, kb, vb = (orc.reorder(data[x], g) for x in ("q", "k", "v"))
     O, _ = orc.attn_fwd(qb, kb, vb, rp, ci, g.Bt, 1.0 / math.sqrt(g.d))
     compare_values(orc.reorder(host(o), g), O, wl, "O on the augmented CSR")
