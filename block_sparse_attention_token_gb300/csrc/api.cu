@@ -51,6 +51,10 @@ sparsp_status_t check_shape(const sparsp_shape_t* sh, Dims* s) {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Every attention option bit; a call ignores the ones that do not concern it.
+constexpr uint32_t kKnownFlags =
+    SPARSP_SCHED_FLAT | SPARSP_KERNEL_PORTABLE | SPARSP_BWD_SPLIT_KV | SPARSP_OUT_RASTER;
+
 // Attention workspace layout: items, counter(s), then backward extras.
 struct AttnWs {
   int32_t* items;      // [rows]
@@ -402,6 +406,7 @@ sparsp_status_t sparsp_lpt_schedule(const sparsp_shape_t* shape, const int32_t* 
   Dims s;
   sparsp_status_t r = check_shape(shape, &s);
   if (r != SPARSP_OK) return r;
+  if (flags & ~kKnownFlags) return SPARSP_ERR_INVALID_ARG;
   CHECK_PTR(row_ptr);
   CHECK_PTR(items);
   const bool flat = (flags & SPARSP_SCHED_FLAT) != 0;
@@ -442,6 +447,7 @@ sparsp_status_t sparsp_attn_fwd(const sparsp_shape_t* shape, const void* q, cons
   sparsp_status_t r = check_shape(shape, &s);
   if (r != SPARSP_OK) return r;
   if (isnan(scale) || isinf(scale)) return SPARSP_ERR_INVALID_ARG;
+  if (flags & ~kKnownFlags) return SPARSP_ERR_INVALID_ARG;
   CHECK_PTR(q);
   CHECK_PTR(k);
   CHECK_PTR(v);
@@ -485,6 +491,7 @@ sparsp_status_t sparsp_attn_bwd(const sparsp_shape_t* shape, const void* q, cons
   if (r != SPARSP_OK) return r;
   if (s.dtype != SPARSP_BF16) return SPARSP_ERR_UNSUPPORTED;
   if (isnan(scale) || isinf(scale)) return SPARSP_ERR_INVALID_ARG;
+  if (flags & ~kKnownFlags) return SPARSP_ERR_INVALID_ARG;
   CHECK_PTR(q);
   CHECK_PTR(k);
   CHECK_PTR(v);

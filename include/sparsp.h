@@ -84,7 +84,9 @@ typedef enum { SPARSP_F32 = 0, SPARSP_BF16 = 1 } sparsp_dtype_t;
 
 typedef enum { SPARSP_EST_MEAN = 0, SPARSP_EST_LOWRANK = 1 } sparsp_estimator_t;
 
-/* Attention options (bit flags). */
+/* Attention options (bit flags). sparsp_lpt_schedule, sparsp_attn_fwd and
+ * sparsp_attn_bwd accept any of them (each ignores the ones that do not
+ * concern it) and return SPARSP_ERR_INVALID_ARG for any other bit. */
 enum {
   /* Order work items purely by row cost across all heads instead of
    * head-grouped longest-first (see sparsp_lpt_schedule). */

@@ -173,6 +173,12 @@ def test_call_validation_codes(lib):
     assert lib.sparsp_attn_fwd(S, *p7, f(0.0), FAKE, FAKE, FAKE, 1 << 30, 0, FAKE + 4, None,
                                None) == sp.ALIGN
     s32 = shape(dtype=sp.F32)
+    # option bits outside the defined ones are refused by every call that takes options
+    assert lib.sparsp_attn_fwd(S, *p7, f(0.0), FAKE, FAKE, FAKE, 1 << 30, 1 << 9, None, None,
+                               None) == sp.INVALID_ARG
+    assert lib.sparsp_attn_bwd(S, *((FAKE,) * 8), f(0.0), FAKE, FAKE, FAKE, FAKE, 1 << 30, 1 << 9, None, None,
+                               None) == sp.INVALID_ARG
+    assert lib.sparsp_lpt_schedule(S, FAKE, 1 << 9, FAKE, FAKE, 1 << 30, None) == sp.INVALID_ARG
     # raster O is written by the tcgen05 kernel only: fp32, or the portable kernel, is refused
     assert lib.sparsp_attn_fwd(ctypes.byref(s32), *p7, f(0.0), FAKE, FAKE, FAKE, 1 << 30, sp.OUT_RASTER, None,
                                None, None) == sp.UNSUPPORTED
