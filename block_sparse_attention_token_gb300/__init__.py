@@ -104,7 +104,7 @@ _SIG = {
     "sparsp_attn_bwd": (_I32, [_P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P,
                                ctypes.c_size_t, ctypes.c_uint32, _P, _P, _P]),
     "sparsp_csr_transpose": (_I32, [_P, _P, _P, _P, _P, _P, _P]),
-    "sparsp_diag_umma_tile": (_I32, [_P, _P, _P, _I32, _I32, _I32, _P]),
+    "sparsp_diag_umma_tile": (_I32, [_P, _P, _P, _I32, _I32, _I32, _P, _P]),
     "sparsp_diag_wait_timeout": (_I32, [ctypes.c_uint64, _P, _P]),
 }
 
@@ -431,11 +431,15 @@ def attn_bwd(shape: Shape, q, k, v, o, lse, dout, row_ptr, col_idx, scale: float
 
 
 def diag_umma_tile(a: torch.Tensor, b: torch.Tensor, mode: int, lbo: int = 16384, sbo: int = 1024,
-                   stream=None) -> torch.Tensor:
-    """One 128x128x128 bf16 tcgen05 tile product (layout diagnostic, include/sparsp_diag.h)."""
+                   status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One 128x128x128 bf16 tcgen05 tile product (layout diagnostic, include/sparsp_diag.h).
+    status: device int32 word that receives SPARSP_ERR_TIMEOUT if a bounded wait
+    expires (a fresh zeroed one is used when None; check it after synchronising)."""
     d = torch.empty((128, 128), dtype=torch.float32, device=a.device)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=a.device)
     _check("sparsp_diag_umma_tile", lib().sparsp_diag_umma_tile(_ptr(a), _ptr(b), _ptr(d), int(mode), int(lbo),
-                                                                int(sbo), _stream(stream)))
+                                                                int(sbo), _ptr(status), _stream(stream)))
     return d
 
 

@@ -12,8 +12,6 @@
 //     with ballots.
 #include "common.cuh"
 
-#include <atomic>
-
 namespace sparsp {
 
 // Scratch of sparsp_select_noalloc: one 64-bit threshold key per CSR row, for
@@ -217,24 +215,16 @@ sparsp_status_t launch_select(const Dims& s, const float* scores, float top_p, i
   return SPARSP_OK;
 }
 
-namespace {
-std::atomic<void*> g_select_scratch_addr[64];
-}  // namespace
-
 sparsp_status_t launch_select_noalloc(const Dims& s, const float* scores, float top_p, int k_floor,
                                       int32_t* row_ptr, int32_t* col_idx, int32_t* d_status,
                                       cudaStream_t st) {
   if (s.rows() > kSelectNoAllocMaxRows) return SPARSP_ERR_WORKSPACE;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPARSP_ERR_CUDA;
-  void* ptr = g_select_scratch_addr[dev].load(std::memory_order_acquire);
-  if (ptr == nullptr) {
-    // One-time set-up on this device (the device is current): the host-side
-    // name of the array is not a device address, so ask the runtime for it.
-    if (cudaGetSymbolAddress(&ptr, g_select_scratch) != cudaSuccess || ptr == nullptr)
-      return SPARSP_ERR_CUDA;
-    g_select_scratch_addr[dev].store(ptr, std::memory_order_release);
-  }
+  // The host-side name of the array is not a device address: ask the runtime,
+  // for the device and context current now, on every call. The answer is not
+  // cached, because the array moves when the caller resets the device or
+  // switches to another context on it. The query allocates nothing.
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_select_scratch) != cudaSuccess || ptr == nullptr) return SPARSP_ERR_CUDA;
   // Every row's threshold is written by the count pass before the fill pass
   // reads it, so nothing in the array has to start at zero.
   return launch_select(s, scores, top_p, k_floor, row_ptr, col_idx, ptr, d_status, st);

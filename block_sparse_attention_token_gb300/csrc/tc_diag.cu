@@ -10,6 +10,14 @@ using namespace tc;
 constexpr uint32_t kTile = 128 * 128 * 2, kHalf = 128 * 64 * 2;
 // A tile, B tile, then 64 KB of slack so that any lbo/sbo <= 32 KB stays inside
 constexpr uint32_t kSmem = 4 * kTile + 64 + 1024;
+constexpr uint64_t kWaitNs = 1000000000ull, kDrainNs = 200000000ull;
+
+__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, uint64_t limit) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > limit) return false;
+  return true;
+}
 
 __global__ void __launch_bounds__(128, 1)
 diag_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
@@ -49,7 +57,10 @@ diag_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUte
   fence_before();
   __syncthreads();
   fence_after();
-  bool ok = true;
+  // thread 0 loads and multiplies; every wait is bounded. On a time-out the
+  // copies or MMAs still in flight are drained (with a second bounded wait)
+  // before TMEM is read or freed, and TMEM is then not read at all.
+  volatile int32_t* ok_flag = reinterpret_cast<volatile int32_t*>(gbase + 4 * kTile + 20);
   if (threadIdx.x == 0) {
     const uint32_t bytes = mode == 1 ? kTile : 2 * kTile;
     mbar_arrive_expect_tx(bar_ld, bytes);
@@ -59,10 +70,10 @@ diag_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUte
     }
     tma_load_2d(sB, &tb, bar_ld, 0, 0);
     tma_load_2d(sB + kHalf, &tb, bar_ld, 64, 0);
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar_ld, 0))
-      if (globaltimer_ns() - t0 > 1000000000ull) { ok = false; break; }
-    if (ok) {
+    bool ok = bounded_wait(bar_ld, 0, kWaitNs);
+    if (!ok) {
+      bounded_wait(bar_ld, 0, kDrainNs);   // the copies may still land
+    } else {
       fence_after();
       const uint32_t id = idesc_bf16(128, 128, 0, mode == 0 ? 0 : 1);
       for (int kk = 0; kk < 8; ++kk) {
@@ -75,19 +86,21 @@ diag_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUte
           mma_ss(tmem, smem_desc(sA + koff, 16, 1024, kSwizzle128B), bdesc, id, kk > 0);
       }
       commit(bar_mma);
-      const uint64_t t1 = globaltimer_ns();
-      while (!mbar_try_wait(bar_mma, 0))
-        if (globaltimer_ns() - t1 > 1000000000ull) { ok = false; break; }
+      ok = bounded_wait(bar_mma, 0, kWaitNs);
+      if (!ok) bounded_wait(bar_mma, 0, kDrainNs);   // let the MMAs finish before TMEM is freed
     }
-    if (!ok && err != nullptr) atomicExch(err, SPARSP_ERR_TIMEOUT);
+    if (!ok) report(err, SPARSP_ERR_TIMEOUT);
+    *ok_flag = ok ? 1 : 0;
   }
   __syncthreads();
   fence_after();
-  for (int c = 0; c < 4; ++c) {
-    uint32_t r[32];
-    tmem_ld32(tmem + lane_base + c * 32u, r);
-    wait_ld();
-    for (int x = 0; x < 32; ++x) d[threadIdx.x * 128 + c * 32 + x] = __uint_as_float(r[x]);
+  if (*ok_flag) {
+    for (int c = 0; c < 4; ++c) {
+      uint32_t r[32];
+      tmem_ld32(tmem + lane_base + c * 32u, r);
+      wait_ld();
+      for (int x = 0; x < 32; ++x) d[threadIdx.x * 128 + c * 32 + x] = __uint_as_float(r[x]);
+    }
   }
   fence_before();
   __syncthreads();
@@ -122,11 +135,13 @@ extern "C" sparsp_status_t sparsp_diag_wait_timeout(uint64_t limit_ns, int32_t* 
 }
 
 extern "C" sparsp_status_t sparsp_diag_umma_tile(const void* a, const void* b, float* d, int32_t mode,
-                                                 int32_t lbo, int32_t sbo, sparsp_stream_t stream) {
+                                                 int32_t lbo, int32_t sbo, int32_t* d_status,
+                                                 sparsp_stream_t stream) {
   using namespace sparsp;
   if (a == nullptr || b == nullptr || d == nullptr) return SPARSP_ERR_INVALID_ARG;
   if (((uintptr_t)a | (uintptr_t)b | (uintptr_t)d) & 15u) return SPARSP_ERR_ALIGN;
   if (mode < 0 || mode > 2) return SPARSP_ERR_INVALID_ARG;
+  if (d_status == nullptr || ((uintptr_t)d_status & 3u)) return SPARSP_ERR_INVALID_ARG;
   if (lbo < 16 || sbo < 16 || lbo > 32768 || sbo > 32768 || (lbo & 15) || (sbo & 15))
     return SPARSP_ERR_INVALID_ARG;
   int dev = 0, major = 0;
@@ -140,6 +155,6 @@ extern "C" sparsp_status_t sparsp_diag_umma_tile(const void* a, const void* b, f
   if (cudaFuncSetAttribute(diag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem) != cudaSuccess)
     return SPARSP_ERR_CUDA;
   diag_kernel<<<1, 128, kSmem, (cudaStream_t)stream>>>(ta, tb, (const __nv_bfloat16*)a, d, mode, (uint32_t)lbo,
-                                                       (uint32_t)sbo, nullptr);
+                                                       (uint32_t)sbo, d_status);
   return cudaGetLastError() == cudaSuccess ? SPARSP_OK : SPARSP_ERR_CUDA;
 }

@@ -202,9 +202,11 @@ SPARSP_API sparsp_status_t sparsp_select(const sparsp_shape_t* shape, const floa
  *    returns SPARSP_ERR_WORKSPACE before any work is enqueued;
  *  - the array costs 512 KB of device memory on every device that loads the
  *    library, held until the process exits;
- *  - the first call on each device looks the array's device address up (a
- *    runtime query, no allocation); make that first call before any stream
- *    capture;
+ *  - every call asks the CUDA runtime for the array's address in the device
+ *    and context current at the call (a query that allocates nothing; the
+ *    address is not cached, so a device reset or another context on the same
+ *    device is safe); the first call on a device may also load the library's
+ *    device code there, so make that first call before any stream capture;
  *  - every call shares the one array, which keeps the last call's contents
  *    (nothing in it needs to start at zero): calls whose work can overlap on
  *    the GPU (different streams, or different host threads) race and must be

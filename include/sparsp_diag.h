@@ -24,9 +24,14 @@ extern "C" {
  *   mode 2: D = A B,   A staged by TMA (K-major), B MN-major.
  * lbo, sbo: leading / stride byte offsets of the MN-major B descriptor
  * (multiples of 16, at most 32768; ignored in mode 0).
+ * d_status: device int32 (required, caller-zeroed). Every wait of the kernel
+ * is bounded (1 s); if the tile copies or the MMAs do not complete in time,
+ * SPARSP_ERR_TIMEOUT is written there, the work still in flight is drained
+ * with a second bounded wait, and d is left unwritten.
  */
 SPARSP_API sparsp_status_t sparsp_diag_umma_tile(const void* a, const void* b, float* d, int32_t mode,
-                                                 int32_t lbo, int32_t sbo, sparsp_stream_t stream);
+                                                 int32_t lbo, int32_t sbo, int32_t* d_status,
+                                                 sparsp_stream_t stream);
 
 /*
  * The bounded-wait path of the tensor-core kernels, exercised on purpose: one

@@ -165,6 +165,8 @@ def test_call_validation_codes(lib):
     assert lib.sparsp_diag_wait_timeout(10, FAKE, None) == sp.INVALID_ARG
     assert lib.sparsp_diag_wait_timeout(10_000_000_000, FAKE, None) == sp.INVALID_ARG
     assert lib.sparsp_diag_wait_timeout(50_000_000, None, None) == sp.INVALID_ARG
+    # tile diagnostic: the status word is required
+    assert lib.sparsp_diag_umma_tile(FAKE, FAKE, FAKE, 0, 16, 1024, None, None) == sp.INVALID_ARG
     # attention: NaN scale, small workspace, misaligned optional pointer, fp32 backward
     p7 = (FAKE,) * 5
     assert lib.sparsp_attn_fwd(S, *p7, f(float("nan")), FAKE, FAKE, FAKE, 1 << 30, 0, None, None,

@@ -26,8 +26,10 @@ def _tiles(seed):
 @pytest.mark.parametrize("mode", [0, 1, 2])
 def test_umma_tile(mode):
     a, b = _tiles(mode + 1)
-    d = sp.diag_umma_tile(a.cuda(), b.cuda(), mode)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    d = sp.diag_umma_tile(a.cuda(), b.cuda(), mode, status=st)
     torch.cuda.synchronize()
+    assert st.item() == 0
     A, Bm = a.double().numpy(), b.double().numpy()
     ref = A @ Bm.T if mode == 0 else A @ Bm
     got = d.cpu().double().numpy()
