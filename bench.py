@@ -8,7 +8,10 @@ training workload, the backward) -> outputs back to raster order.
 
 Default workload: the Wan-14B attention-layer shape (B=1, H=40, d=128,
 30,720 tokens in 2x8x8 tiles, Top-p 0.95, floor 8, P = 8), bf16, synthetic
-seeded inputs. Prints one JSON line (rank 0).
+seeded inputs. Prints one JSON line (rank 0). On one GPU the line also
+carries a compact "workloads" object with the other four seeded workloads
+(skewed per-head sparsity, the 65,536-token training step, the medium and
+the tiny case), each timed over its own short run.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload wan|skewed|training|medium|tiny]
   python bench.py --impl reference ...   # the CPU oracle on the host cores, same metric
@@ -68,6 +71,9 @@ def peaks():
                 "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
+
+L2_BYTES = 129e6          # GB300 L2; a stage whose bytes fit was fed from L2, not HBM
+EXTRA_WORKLOADS = ("skewed", "training", "medium", "tiny")
 
 # DRAM bytes (read + write) per launch of the tcgen05 forward kernel, from an ncu capture of the
 # Wan-layer shape with 8 of its 40 heads (236.8 MB: Q, K, V read once, O written), scaled by the
@@ -201,6 +207,183 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
+def stage_bytes(shape, wl, nnz: int, demanded: int, fused: bool, overlapped: bool) -> dict:
+    """Algorithmic HBM bytes of the memory-bound stages of one step: what each
+    stage must read and write at least (the roofline's numerator)."""
+    el = 2 if wl.dtype == "bf16" else 4
+    BH = shape.B * shape.H
+    tensor = BH * shape.N * shape.d * el
+    means = BH * shape.nb * shape.d * 4
+    rows = BH * shape.nb
+    out = {
+        "reorder": 6 * tensor + (2 * means if fused else 0),
+        "scores": (2 * means if fused else 2 * tensor) + 4 * BH * shape.nb * shape.nb,
+        "select": 4 * BH * shape.nb * shape.nb + 4 * (nnz + rows + 1),
+        "reorder_out": 2 * tensor,
+    }
+    # demand lists: the CSR read, the bitmap and the index lists written; the gather: the
+    # gathered copy written once, each source K/V tile read from HBM once (its P-fold reuse
+    # across partitions hits in L2)
+    lists = 4 * nnz + BH * wl.P * ((shape.nb + 31) // 32) * 4 + 4 * (demanded // (2 * shape.Bt * shape.d * el))
+    gather = demanded + 2 * tensor
+    if overlapped:
+        out["kv_demand"] = lists
+        out["kv_gather"] = gather
+    else:
+        out["kv_demand"] = lists + gather
+    return out
+
+
+def hbm_fractions(stage_ms: dict, nbytes: dict, hbm_gbs: float) -> dict:
+    """GB/s of each memory-bound stage against the measured copy peak. A stage
+    whose bytes fit in L2 (its inputs were written just before by the previous
+    stage) is fed from L2: it gets its GB/s but no fraction of the HBM peak."""
+    out = {}
+    for name, b in nbytes.items():
+        ms = stage_ms.get(name)
+        if not ms or ms <= 0:
+            continue
+        gbs = b / (ms * 1e-3) / 1e9
+        if b <= L2_BYTES:
+            out[name] = {"bytes": int(b), "gbs": gbs, "frac": None, "l2_resident": True}
+        else:
+            out[name] = {"bytes": int(b), "gbs": gbs, "frac": gbs / hbm_gbs}
+    return out
+
+
+class Run:
+    """One workload on the device: inputs resident in HBM, a Pipeline in the
+    benchmark's configuration, and timed steps."""
+
+    def __init__(self, sp, wl, args, flags=0, overlap=True):
+        import torch
+        self.torch, self.sp, self.wl = torch, sp, wl
+        self.data = synth.make(wl)
+        self.shape = sp.shape_of(wl)
+        self.pipe = sp.Pipeline(self.shape, wl.estimator, wl.top_p, wl.k_floor, wl.P, backward=wl.backward,
+                                flags=flags, fused_estimation=not args.unfused, placement=args.placement,
+                                migrations=wl.P if args.augment else None, augment=args.augment,
+                                overlap_demand=overlap)
+        tdt = self.shape.torch_dtype
+        self.host_in = {x: torch.from_numpy(self.data[x]).to(tdt).pin_memory() for x in ("q", "k", "v")}
+        self.dev_in = {x: self.host_in[x].cuda() for x in self.host_in}
+        self.kw = {}
+        if wl.estimator == "lowrank":
+            self.kw = {"wq": torch.from_numpy(self.data["wq"]).cuda(), "wk": torch.from_numpy(self.data["wk"]).cuda()}
+        self.dout = None
+        if wl.backward:
+            self.host_in["do"] = torch.from_numpy(self.data["do"]).to(tdt).pin_memory()
+            self.dout = self.host_in["do"].cuda()
+        self.stream = torch.cuda.current_stream()
+
+    def step(self, mark=None, prof=False):
+        self.pipe.forward(self.dev_in["q"], self.dev_in["k"], self.dev_in["v"], prof=prof, mark=mark, **self.kw)
+        if self.wl.backward:
+            self.pipe.backward(self.dout, prof=prof, mark=mark)
+
+    def warm(self, n):
+        for _ in range(n):
+            self.step()
+        self.torch.cuda.synchronize()
+        st = self.pipe.status.item()
+        if st != 0:
+            raise SystemExit(f"{self.wl.name}: device status {self.sp.status_string(st)}")
+        self.nnz = int(self.pipe.csr[0][-1].item())     # the CSR attention ran on
+        self.kv_bytes = [int(x) for x in self.pipe.demand.bytes.tolist()]
+
+    def timed(self, steps, before=None):
+        """K steps between two events on the launching stream, with an event
+        after every stage; returns (ms per step, {stage: ms per step})."""
+        torch = self.torch
+        marks = []
+
+        def mark(name, on=None):
+            ev = torch.cuda.Event(enable_timing=True)
+            ev.record(on if on is not None else self.stream)
+            marks.append((name, ev))
+
+        if before is not None:
+            before()
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(self.stream)
+        for _ in range(steps):
+            mark("step_start")
+            self.step(mark=mark)
+        end.record(self.stream)
+        torch.cuda.synchronize()
+        side = ("attn_fwd", "kv_gather") if self.pipe.overlap_demand else ()
+        return start.elapsed_time(end) / steps, stage_times(marks, side, lambda a, b: a.elapsed_time(b), steps)
+
+    def attn_alone_ms(self, calls=5):
+        """The forward attention kernel with nothing beside it (in the step it
+        may share its SMs with the KV gather)."""
+        torch, sp, pipe = self.torch, self.sp, self.pipe
+        rp, ci = pipe.csr
+        flags = pipe.flags | (sp.OUT_RASTER if pipe.raster_out else 0)
+        o = pipe.o if pipe.raster_out else pipe.ob
+        b0 = torch.cuda.Event(enable_timing=True)
+        b1 = torch.cuda.Event(enable_timing=True)
+        b0.record(self.stream)
+        for _ in range(calls):
+            sp.attn_fwd(self.shape, pipe.qb, pipe.kb, pipe.vb, rp, ci, 0.0, o, pipe.lse, pipe.ws_attn, flags,
+                        None, pipe.status)
+        b1.record(self.stream)
+        torch.cuda.synchronize()
+        return b0.elapsed_time(b1) / calls
+
+    def sm_imbalance(self):
+        """Per-SM busy time of the attention kernel, max over mean (one profiled step)."""
+        torch = self.torch
+        self.pipe.prof.zero_()
+        self.pipe.forward(self.dev_in["q"], self.dev_in["k"], self.dev_in["v"], prof=True, **self.kw)
+        torch.cuda.synchronize()
+        busy = self.pipe.prof.cpu().numpy().astype(np.float64)
+        busy = busy[busy > 0]
+        return float(busy.max() / busy.mean()) if len(busy) else None
+
+
+def workload_summary(sp, name, args, pk) -> dict:
+    """One of the other seeded workloads, in the default configuration: its own
+    short timed run (3 warm-ups, min(K, 10) steps), no CPU baseline."""
+    import torch
+    wl = synth.WORKLOADS[name]
+    run = Run(sp, wl, args)
+    run.warm(3)
+    ms, st = run.timed(min(args.steps, 10))
+    shape = run.shape
+    f_fwd = attn_flops(run.nnz, wl)
+    f_step = f_fwd + (bwd_flops(run.nnz, wl) if wl.backward else 0.0)
+    alone = run.attn_alone_ms()
+    tensor = wl.dtype == "bf16"
+    peak = pk["bf16_tflops"]
+    out = {"workload": wl.name, "ms_per_step": ms, "tflops": f_step / (ms * 1e-3) / 1e12,
+           "tokens_per_s": wl.B * wl.N / (ms * 1e-3), "nnz_blocks": run.nnz,
+           "density": run.nnz / (shape.rows * shape.nb),
+           "attn_fwd_ms": st["attn_fwd"], "attn_fwd_tflops": f_fwd / (st["attn_fwd"] * 1e-3) / 1e12,
+           "attn_fwd_alone_ms": alone, "attn_fwd_alone_tflops": f_fwd / (alone * 1e-3) / 1e12}
+    if tensor:
+        out["attn_fwd_frac_of_burst"] = out["attn_fwd_tflops"] / peak
+        out["attn_fwd_alone_frac_of_burst"] = out["attn_fwd_alone_tflops"] / peak
+    else:
+        out["attn_fwd_bound"] = "fp32 FFMA kernel (no tensor-core peak applies)"
+    if wl.backward:
+        fb = bwd_flops(run.nnz, wl)
+        out["attn_bwd_ms"] = st["attn_bwd"]
+        out["attn_bwd_tflops"] = fb / (st["attn_bwd"] * 1e-3) / 1e12
+        out["attn_bwd_frac_of_burst"] = out["attn_bwd_tflops"] / peak
+    nbytes = stage_bytes(shape, wl, run.nnz, run.kv_bytes[0], not args.unfused, run.pipe.overlap_demand)
+    out["hbm_stages"] = {k: (round(v["frac"], 4) if v["frac"] is not None else "l2-resident")
+                         for k, v in hbm_fractions(st, nbytes, pk["hbm_gbs"]).items()}
+    out["stages_ms"] = {k: round(v, 5) for k, v in st.items()}
+    if wl.skew:
+        out["attn_sm_imbalance"] = run.sm_imbalance()
+    del run
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -218,10 +401,11 @@ def main():
     ap.add_argument("--augment", action="store_true",
                     help="head balancing over P virtual ranks + slack-aware augmentation inside the step")
     ap.add_argument("--serial-demand", action="store_true",
-                    help="run the KV demand stage before attention on one stream (default: beside it, on a "
-                         "side stream), so that every stage has its own time")
+                    help="time the step with the KV demand stage before attention on one stream (default: the "
+                         "gather beside attention on a side stream)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the other seeded workloads")
     ap.add_argument("--heads", type=int, default=0, help="override the head count (smaller profiling case)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -246,67 +430,31 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
     barrier = replicas.barrier
-
-    data = synth.make(wl)
-    shape = sp.shape_of(wl)
     flags = ((sp.SCHED_FLAT if args.flat else 0) | (sp.KERNEL_PORTABLE if args.portable else 0)
              | (sp.BWD_SPLIT_KV if args.bwd_split_kv else 0))
-    pipe = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P, backward=wl.backward, flags=flags,
-                       fused_estimation=not args.unfused, placement=args.placement,
-                       migrations=wl.P if args.augment else None, augment=args.augment,
-                       overlap_demand=not args.serial_demand)
-    tdt = shape.torch_dtype
-    host_in = {x: torch.from_numpy(data[x]).to(tdt).pin_memory() for x in ("q", "k", "v")}
-    dev_in = {x: host_in[x].cuda() for x in host_in}
-    kw = {}
-    if wl.estimator == "lowrank":
-        kw = {"wq": torch.from_numpy(data["wq"]).cuda(), "wk": torch.from_numpy(data["wk"]).cuda()}
-    dout = None
-    if wl.backward:
-        host_in["do"] = torch.from_numpy(data["do"]).to(tdt).pin_memory()
-        dout = host_in["do"].cuda()
-    stream = torch.cuda.current_stream()
+    run = Run(sp, wl, args, flags=flags, overlap=True)
+    pipe, shape, stream = run.pipe, run.shape, run.stream
+    run.warm(args.warmup)
+    nnz = run.nnz
+    demanded, all_bytes, remote_dem, remote_all = run.kv_bytes
+    default_overlap = not args.serial_demand
 
-    def step(mark=None, prof=False):
-        pipe.forward(dev_in["q"], dev_in["k"], dev_in["v"], prof=prof, mark=mark, **kw)
-        if wl.backward:
-            pipe.backward(dout, prof=prof, mark=mark)
+    # ---- the other order of the KV demand gather, untimed warm-up then its own timed steps
+    # (A/B in one process; the headline takes the default order)
+    pipe.overlap_demand = not default_overlap
+    run.warm(2)
+    other_ms, other_stages = run.timed(args.steps)
+    pipe.overlap_demand = default_overlap
+    run.warm(2)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if pipe.status.item() != 0:
-        raise SystemExit(f"device status {sp.status_string(pipe.status.item())}")
-    nnz = int(pipe.csr[0][-1].item())     # the CSR attention ran on
-    demanded, all_bytes, remote_dem, remote_all = (int(x) for x in pipe.demand.bytes.tolist())
-
-    # ---- timed region: K steps, events around every stage
-    marks = []
-
-    def mark(name, on=None):
-        ev = torch.cuda.Event(enable_timing=True)
-        ev.record(on if on is not None else stream)
-        marks.append((name, ev))
-
+    # ---- timed region: K steps, events around every stage, clocks sampled meanwhile
     clocks = ClockSampler(local)
     time.sleep(0.5)
-    barrier()
-    torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for _ in range(args.steps):
-        mark("step_start")
-        step(mark=mark)
-    end.record(stream)
-    torch.cuda.synchronize()
+    ms_step, stage_ms = run.timed(args.steps, before=barrier)
     barrier()
     clk = clocks.stop()
-    total_ms = start.elapsed_time(end)
-    side = ("attn_fwd", "kv_gather") if pipe.overlap_demand else ()
-    stage_ms = stage_times(marks, side, lambda a, b: a.elapsed_time(b), args.steps)
-    ms_step = total_ms / args.steps
     ms_step = replicas.max_over_ranks(ms_step)
+    overlap_ms, serial_ms = (ms_step, other_ms) if default_overlap else (other_ms, ms_step)
 
     pk = peaks()
     f_fwd = attn_flops(nnz, wl)
@@ -314,60 +462,36 @@ def main():
     value = replicas.whole_job_rate(f_step, ms_step, world) / 1e12
     attn_ms = stage_ms["attn_fwd"]
     achieved = f_fwd / (attn_ms * 1e-3) / 1e12
-    peak = pk["bf16_tflops_sustained"]
+    peak = pk["bf16_tflops"]
     roofline = {"bound": "tensor", "kernel": "attn_fwd", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "peak_kind": f"bf16 sustained ({pk['source']})",
-                "frac_of_burst": achieved / pk["bf16_tflops"], "traffic": ATTN_TRAFFIC.get(wl.name) if not args.portable else None,
+                "frac": achieved / peak, "peak_kind": f"bf16 burst ({pk['source']}; the kernel runs at full clock "
+                                                      f"inside a sub-second timed region)",
+                "frac_of_sustained": achieved / pk["bf16_tflops_sustained"],
+                "traffic": ATTN_TRAFFIC.get(wl.name) if not args.portable else None,
                 "work": f"4*nnz*Bt^2*d = {f_fwd:.4g} flop per launch (nnz={nnz})"}
     if wl.backward:
         roofline["bwd_achieved"] = bwd_flops(nnz, wl) / (stage_ms["attn_bwd"] * 1e-3) / 1e12
-    if pipe.overlap_demand and not args.portable:
-        # the same kernel with nothing beside it (in the step it shares its SMs with the KV gather)
-        rp_, ci_ = pipe.csr
-        b0 = torch.cuda.Event(enable_timing=True)
-        b1 = torch.cuda.Event(enable_timing=True)
-        b0.record(stream)
-        for _ in range(5):
-            sp.attn_fwd(shape, pipe.qb, pipe.kb, pipe.vb, rp_, ci_, 0.0, pipe.ob, pipe.lse, pipe.ws_attn,
-                        pipe.flags, None, pipe.status)
-        b1.record(stream)
-        torch.cuda.synchronize()
-        alone = f_fwd / (b0.elapsed_time(b1) / 5 * 1e-3) / 1e12
+        roofline["bwd_frac"] = roofline["bwd_achieved"] / peak
+    if not args.portable:
+        alone = f_fwd / (run.attn_alone_ms() * 1e-3) / 1e12
         roofline["achieved_alone"] = alone
         roofline["frac_alone"] = alone / peak
-        roofline["in_step"] = "shares its SMs with the KV demand gather (side stream)"
+        if default_overlap:
+            roofline["in_step"] = "shares its SMs with the KV demand gather (side stream)"
 
-    # ---- algorithmic bytes of the memory-bound stages, against the measured copy peak
-    el = 2 if wl.dtype == "bf16" else 4
-    BH = shape.B * shape.H
-    tensor = BH * shape.N * shape.d * el
-    means = BH * shape.nb * shape.d * 4
-    rows = BH * shape.nb
-    stage_bytes = {
-        "reorder": 6 * tensor + (2 * means if not args.unfused else 0),
-        "scores": (2 * means if not args.unfused else 2 * tensor) + 4 * BH * shape.nb * shape.nb,
-        "select": 4 * BH * shape.nb * shape.nb + 4 * (nnz + rows + 1),
-        "reorder_out": 2 * tensor,
-    }
-    # demand lists: the CSR read, the bitmap and the index lists written; the gather: the
-    # gathered copy written once, each source K/V tile read from HBM once (its P-fold reuse
-    # across partitions hits in L2)
-    lists_bytes = 4 * nnz + BH * wl.P * ((shape.nb + 31) // 32) * 4 + 4 * (demanded // (2 * shape.Bt * shape.d * el))
-    gather_bytes = demanded + 2 * tensor
-    if pipe.overlap_demand:
-        stage_bytes["kv_demand"] = lists_bytes
-        stage_bytes["kv_gather"] = gather_bytes
-    else:
-        stage_bytes["kv_demand"] = lists_bytes + gather_bytes
-    hbm = {}
-    for name, nbytes in stage_bytes.items():
-        if name in stage_ms and stage_ms[name] > 0:
-            gbs = nbytes / (stage_ms[name] * 1e-3) / 1e9
-            hbm[name] = {"bytes": int(nbytes), "gbs": gbs, "frac": gbs / pk["hbm_gbs"]}
-            if name == "kv_gather":
-                hbm[name]["note"] = "runs beside attention, sharing its SMs: not a standalone rate"
+    nbytes = stage_bytes(shape, wl, nnz, demanded, not args.unfused, default_overlap)
+    hbm = hbm_fractions(stage_ms, nbytes, pk["hbm_gbs"])
+    if "kv_gather" in hbm:
+        hbm["kv_gather"]["note"] = "runs beside attention, sharing its SMs: not a standalone rate"
+    other_bytes = stage_bytes(shape, wl, nnz, demanded, not args.unfused, not default_overlap)
+    demand_order = {"overlapped_ms_per_step": overlap_ms, "serial_ms_per_step": serial_ms,
+                    "default": "overlapped" if default_overlap else "serial",
+                    ("serial" if default_overlap else "overlapped") + "_stages_ms": other_stages,
+                    ("serial" if default_overlap else "overlapped") + "_hbm_stages":
+                        hbm_fractions(other_stages, other_bytes, pk["hbm_gbs"])}
 
     # ---- context only: dense attention (PyTorch SDPA) over the same tensors
+    BH = shape.B * shape.H
     dense = None
     try:
         import torch.nn.functional as F
@@ -383,13 +507,16 @@ def main():
         torch.cuda.synchronize()
         dms = d0.elapsed_time(d1) / 3
         dense = {"sdpa_ms": dms, "sdpa_tflops": 4.0 * BH * shape.N * shape.N * shape.d / (dms * 1e-3) / 1e12,
-                 "sparse_attn_speedup": dms / stage_ms["attn_fwd"], "kind": "torch SDPA, dense, same Q/K/V"}
+                 "sparse_attn_speedup": dms / stage_ms["attn_fwd"],
+                 "kind": "torch SDPA, dense, same Q/K/V (a library baseline of unknown tuning: context only)"}
     except Exception as exc:   # context only: never fails the bench
         dense = {"unavailable": str(exc)[:120]}
 
     # ---- end to end through the public API: pinned host -> device, step, O -> pinned host
+    tdt = shape.torch_dtype
     e2e = None
     if not args.no_e2e:
+        host_in, kw = run.host_in, run.kw
         host_out = torch.empty(pipe.o.shape, dtype=tdt).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
         d2h = host_out.numel() * host_out.element_size()
@@ -423,13 +550,7 @@ def main():
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "copies": "overlapped with neighbouring steps (HostPipeline)"}
 
-    # per-SM busy imbalance of the attention kernel (one extra profiled step, untimed)
-    pipe.prof.zero_()
-    pipe.forward(dev_in["q"], dev_in["k"], dev_in["v"], prof=True, **kw)
-    torch.cuda.synchronize()
-    busy = pipe.prof.cpu().numpy().astype(np.float64)
-    busy = busy[busy > 0]
-    imbalance = float(busy.max() / busy.mean()) if len(busy) else None
+    imbalance = run.sm_imbalance()
 
     # dependency-aware placement against the contiguous split on this step's CSR
     # (untimed by the step; its own kernels timed here)
@@ -483,6 +604,7 @@ def main():
     # predictor fitting on this step's tile means (low-rank workloads), outside the step
     predictor_info = None
     if wl.estimator == "lowrank" and not args.unfused:
+        kw = run.kw
         wq_f, wk_f = kw["wq"].clone(), kw["wk"].clone()
         ploss, _, _ = sp.predictor_fit(shape, pipe.qmeans, pipe.kmeans, wq_f, wk_f, lr=0.0)
         f0 = torch.cuda.Event(enable_timing=True)
@@ -495,6 +617,20 @@ def main():
         predictor_info = {"loss_mean": float(ploss.mean().item()), "fit_step_ms": f0.elapsed_time(f1) / 5}
 
     launches = args.steps * (pipe.kernels_per_forward() + (pipe.kernels_per_backward() if wl.backward else 0))
+    counts = np.diff(pipe.csr[0].cpu().numpy())
+    data = run.data
+    del run, pipe, contiguous, placed, owner, ws_pl, ws_aug, rp_aug, ci_aug
+    torch.cuda.empty_cache()
+
+    # the other seeded workloads, each its own short run (one GPU only; rank 0 prints)
+    workloads = None
+    if world == 1 and not args.no_workloads and not args.heads:
+        workloads = {}
+        for name in EXTRA_WORKLOADS:
+            if synth.WORKLOADS[name].name == wl.name:
+                continue
+            workloads[name] = workload_summary(sp, name, args, pk)
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -503,7 +639,6 @@ def main():
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(wl, data)
         cpu.pop("seconds", None)
-    counts = np.diff(pipe.csr[0].cpu().numpy())
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -519,12 +654,13 @@ def main():
                    "estimation": "separate pooling pass" if args.unfused else "fused with the reorder",
                    "partitions": "dependency-aware placement" if args.placement else "contiguous",
                    "augmentation": "balanced heads + slack fill" if args.augment else "none",
-                   "kv_demand": "lists and gather serial, before attention" if args.serial_demand else
+                   "kv_demand": "lists and gather serial, before attention" if not default_overlap else
                                 "lists before attention; gather beside it on a low-priority side stream",
                    "l2": f"inputs larger than L2 ({shape.B * shape.H * shape.N * shape.d * 2 / 1e6:.0f} MB per tensor)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "stages_ms": stage_ms,
         "hbm_stages": hbm,
+        "demand_order": demand_order,
         "dense_context": dense,
         "kv_bytes": {"demanded": demanded, "all": all_bytes, "remote_demanded": remote_dem,
                      "remote_all": remote_all},
@@ -532,6 +668,7 @@ def main():
         "balance": balance_info,
         "predictor": predictor_info,
         "attn_sm_imbalance": imbalance,
+        "workloads": workloads,
         "clocks": clk, "e2e": e2e, "gpu_launches": launches, "roofline": roofline, "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)

@@ -26,6 +26,14 @@ SCHED_FLAT = 1
 KERNEL_PORTABLE = 2
 BWD_SPLIT_KV = 4
 OUT_RASTER = 8
+GRID_CAP_SHIFT = 16
+
+
+def GRID_CAP(n: int) -> int:
+    """Option bits that cap the attention kernels' persistent grid at n CTAs (1..4095)."""
+    if not 1 <= n <= 4095:
+        raise ValueError("grid cap must be in [1, 4095]")
+    return n << GRID_CAP_SHIFT
 PROF_SLOTS = 1024
 
 

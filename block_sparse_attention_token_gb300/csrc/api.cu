@@ -52,8 +52,8 @@ sparsp_status_t check_shape(const sparsp_shape_t* sh, Dims* s) {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Every attention option bit; a call ignores the ones that do not concern it.
-constexpr uint32_t kKnownFlags =
-    SPARSP_SCHED_FLAT | SPARSP_KERNEL_PORTABLE | SPARSP_BWD_SPLIT_KV | SPARSP_OUT_RASTER;
+constexpr uint32_t kKnownFlags = SPARSP_SCHED_FLAT | SPARSP_KERNEL_PORTABLE | SPARSP_BWD_SPLIT_KV |
+                                 SPARSP_OUT_RASTER | SPARSP_GRID_CAP_MASK;
 
 // Attention workspace layout: items, counter(s), then backward extras.
 struct AttnWs {
@@ -448,6 +448,7 @@ sparsp_status_t sparsp_attn_fwd(const sparsp_shape_t* shape, const void* q, cons
   if (r != SPARSP_OK) return r;
   if (isnan(scale) || isinf(scale)) return SPARSP_ERR_INVALID_ARG;
   if (flags & ~kKnownFlags) return SPARSP_ERR_INVALID_ARG;
+  s.max_ctas = (int)((flags & SPARSP_GRID_CAP_MASK) >> SPARSP_GRID_CAP_SHIFT);
   CHECK_PTR(q);
   CHECK_PTR(k);
   CHECK_PTR(v);
@@ -492,6 +493,7 @@ sparsp_status_t sparsp_attn_bwd(const sparsp_shape_t* shape, const void* q, cons
   if (s.dtype != SPARSP_BF16) return SPARSP_ERR_UNSUPPORTED;
   if (isnan(scale) || isinf(scale)) return SPARSP_ERR_INVALID_ARG;
   if (flags & ~kKnownFlags) return SPARSP_ERR_INVALID_ARG;
+  s.max_ctas = (int)((flags & SPARSP_GRID_CAP_MASK) >> SPARSP_GRID_CAP_SHIFT);
   CHECK_PTR(q);
   CHECK_PTR(k);
   CHECK_PTR(v);

@@ -380,7 +380,7 @@ dkdv_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict
 }
 
 template <typename K>
-sparsp_status_t persistent_grid(K kern, int threads, int smem, int64_t n_items, int64_t* grid) {
+sparsp_status_t persistent_grid(const Dims& s, K kern, int threads, int smem, int64_t n_items, int64_t* grid) {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return SPARSP_ERR_CUDA;
   const int sms = device_sm_count();
@@ -388,10 +388,7 @@ sparsp_status_t persistent_grid(K kern, int threads, int smem, int64_t n_items, 
   int per_sm = 1;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
   if (per_sm < 1) per_sm = 1;
-  int64_t gsz = (int64_t)sms * per_sm;
-  if (gsz > n_items) gsz = n_items;
-  if (gsz < 1) gsz = 1;
-  *grid = gsz;
+  *grid = cap_grid(s, (int64_t)sms * per_sm, n_items);
   return SPARSP_OK;
 }
 
@@ -416,7 +413,7 @@ sparsp_status_t launch_attn_bwd_dq(const Dims& s, const __nv_bfloat16* q, const 
     using C = BwdCfg<BT, D>;                                                                     \
     int64_t grid;                                                                                \
     auto kern = dq_kernel<BT, D>;                                                                \
-    sparsp_status_t r = persistent_grid(kern, C::kThreads, C::kSmem, s.rows(), &grid);           \
+    sparsp_status_t r = persistent_grid(s, kern, C::kThreads, C::kSmem, s.rows(), &grid);           \
     if (r != SPARSP_OK) return r;                                                                \
     kern<<<(unsigned)grid, C::kThreads, C::kSmem, st>>>(q, k, v, dout, lse, delta, row_ptr,     \
                                                         col_idx, s.N, s.nb, s.rows(), scale, dq, \
@@ -444,7 +441,7 @@ sparsp_status_t launch_attn_bwd_dkdv(const Dims& s, const __nv_bfloat16* q,
     using C = BwdCfg<BT, D>;                                                                     \
     int64_t grid;                                                                                \
     auto kern = dkdv_kernel<BT, D>;                                                              \
-    sparsp_status_t r = persistent_grid(kern, C::kThreads, C::kSmem, s.rows(), &grid);           \
+    sparsp_status_t r = persistent_grid(s, kern, C::kThreads, C::kSmem, s.rows(), &grid);           \
     if (r != SPARSP_OK) return r;                                                                \
     kern<<<(unsigned)grid, C::kThreads, C::kSmem, st>>>(q, k, v, dout, lse, delta, col_ptr,     \
                                                         row_idx, s.N, s.nb, s.rows(), scale, dk, \

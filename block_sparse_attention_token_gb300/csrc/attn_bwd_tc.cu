@@ -605,9 +605,7 @@ sparsp_status_t go(const Dims& s, const CUtensorMap& a1, const CUtensorMap& a2, 
     return SPARSP_ERR_CUDA;
   const int sms = device_sm_count();
   if (sms <= 0) return SPARSP_ERR_CUDA;
-  int64_t grid = sms;
-  if (grid > s.rows()) grid = s.rows();
-  if (grid < 1) grid = 1;
+  const int64_t grid = cap_grid(s, sms, s.rows());
   kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(a1, a2, b1, b2, prm);
   SPARSP_LAUNCH_CHECK();
   return SPARSP_OK;

@@ -220,9 +220,7 @@ sparsp_status_t go(const Dims& s, const __nv_bfloat16* q, const __nv_bfloat16* k
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::kThreads, C::kSmem);
   if (per_sm < 1) per_sm = 1;
   const int64_t n_items = s.rows();
-  int64_t grid = (int64_t)sms * per_sm;
-  if (grid > n_items) grid = n_items;
-  if (grid < 1) grid = 1;
+  const int64_t grid = cap_grid(s, (int64_t)sms * per_sm, n_items);
   kern<<<(unsigned)grid, C::kThreads, C::kSmem, st>>>(q, k, v, row_ptr, col_idx, s.N, s.nb,
                                                       n_items, scale * 1.4426950408889634f, o, lse,
                                                       items, counter, prof, d_status);

@@ -151,9 +151,7 @@ sparsp_status_t go(const Dims& s, const float* q, const float* k, const float* v
   int per_sm = 1;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, BT, smem);
   if (per_sm < 1) per_sm = 1;
-  int64_t grid = (int64_t)sms * per_sm;
-  if (grid > n_items) grid = n_items;
-  if (grid < 1) grid = 1;
+  const int64_t grid = cap_grid(s, (int64_t)sms * per_sm, n_items);
   const float scale_log2 = scale * 1.4426950408889634f;
   kern<<<(unsigned)grid, BT, smem, st>>>(q, k, v, row_ptr, col_idx, s.N, s.nb, n_items, scale_log2,
                                          o, lse, items, counter, prof, d_status);

@@ -520,9 +520,7 @@ sparsp_status_t go_fwd(const Dims& s, const CUtensorMap& tq, const CUtensorMap& 
     return SPARSP_ERR_CUDA;
   const int sms = device_sm_count();
   if (sms <= 0) return SPARSP_ERR_CUDA;
-  int64_t grid = sms;
-  if (grid > s.rows()) grid = s.rows();
-  if (grid < 1) grid = 1;
+  const int64_t grid = cap_grid(s, sms, s.rows());
   kern<<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, prm);
   SPARSP_LAUNCH_CHECK();
   return SPARSP_OK;

@@ -17,8 +17,17 @@ struct Dims {
   int nb;         // tiles per (b, h)
   int nT, nY, nX; // tile lattice
   int elem;       // bytes per element
+  int max_ctas = 0;   // attention kernels: persistent grid cap (0 = one per SM x occupancy)
   int64_t rows() const { return (int64_t)B * H * nb; }  // CSR rows = work items
 };
+
+// A persistent kernel's grid: `g` CTAs, at most one per work item and at most
+// the caller's cap (SPARSP_GRID_CAP), never fewer than one.
+inline int64_t cap_grid(const Dims& s, int64_t g, int64_t n_items) {
+  if (s.max_ctas > 0 && g > s.max_ctas) g = s.max_ctas;
+  if (g > n_items) g = n_items;
+  return g < 1 ? 1 : g;
+}
 
 // First-error-wins device status word.
 __device__ __forceinline__ void report(int32_t* st, int32_t code) {

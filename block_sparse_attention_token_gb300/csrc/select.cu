@@ -3,8 +3,10 @@
 // Three launches, no atomics on data, deterministic:
 //  1. count_kernel  - one warp per row: bitonic sort of 64-bit keys
 //     (score descending as an order-preserving integer, then block index) held
-//     in registers and exchanged with shuffles; e_j = expf(S_j - max) in fp32;
-//     Z and the prefix masses in fp64; m = min(nb, max(m_p, k_floor, 1)).
+//     in registers and exchanged with shuffles; e_j = exp(S_j - max) rounded
+//     to fp32 (expf, or the correctly rounded value for rows whose Top-p
+//     crossing lies within 1e-6 of p); Z and the prefix masses in fp64;
+//     m = min(nb, max(m_p, k_floor, 1)).
 //     Writes m into row_ptr[row] and the key of the m-th kept block into ws.
 //  2. scan          - exclusive scan of the counts -> row_ptr.
 //  3. fill_kernel   - one warp per row: block j is kept iff its key <= the
@@ -41,6 +43,53 @@ __device__ __forceinline__ uint64_t make_key(float s, int j) {
 
 __device__ __forceinline__ float key_score(uint64_t key) {
   return from_ordered(~(uint32_t)(key >> 32));
+}
+
+// m_p of one row held sorted in the warp's registers (positions lane*E + e):
+// the smallest m whose leading prefix of e_j = exp(S_j - max) holds mass
+// >= top_p * Z, with Z and the prefixes summed in float64. exact: e_j is the
+// correctly rounded float32 of the exponential (evaluated in float64);
+// otherwise expf. *near: some prefix lies within 1e-6 of Z of the target.
+template <int E>
+__device__ __forceinline__ int topp_count(const uint64_t (&key)[E], float smax, int lane, int nb, double top_p,
+                                          bool exact, bool* near) {
+  double ev[E];
+  double lane_sum = 0.0;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int p = lane * E + e;
+    ev[e] = 0.0;
+    if (p < nb) {
+      const float x = key_score(key[e]) - smax;
+      ev[e] = exact ? (double)__double2float_rn(exp((double)x)) : (double)expf(x);
+    }
+    lane_sum += ev[e];
+  }
+  // inclusive scan of lane sums
+  double incl = lane_sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const double o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  const double Z = __shfl_sync(0xffffffffu, incl, 31);
+  const double target = top_p * Z, band = 1e-6 * Z;
+  double c = incl - lane_sum;   // exclusive prefix of this lane
+  int below = 0;
+  bool close = false;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int p = lane * E + e;
+    c += ev[e];
+    if (p < nb) {
+      if (c < target) ++below;
+      if (fabs(c - target) < band) close = true;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) below += __shfl_xor_sync(0xffffffffu, below, off);
+  *near = __any_sync(0xffffffffu, close);
+  return min(nb, below + 1);
 }
 
 template <int E>   // elements per lane; padded row length = 32*E
@@ -106,43 +155,22 @@ count_kernel(const float* __restrict__ S, int64_t rows, int nb, double top_p, in
       }
     }
   }
-  // softmax mass in sorted order
-  const float smax = __shfl_sync(0xffffffffu, key_score(key[0]), 0);
-  double ev[E];
-  double lane_sum = 0.0;
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const int p = lane * E + e;
-    ev[e] = 0.0;
-    if (p < nb) ev[e] = (double)expf(key_score(key[e]) - smax);
-    lane_sum += ev[e];
-  }
-  // inclusive scan of lane sums
-  double incl = lane_sum;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const double o = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += o;
-  }
-  const double Z = __shfl_sync(0xffffffffu, incl, 31);
+  // Top-p cutoff from the softmax mass in sorted order (no exponentials are
+  // needed for p <= 0 or p >= 1)
   int m_p;
   if (top_p <= 0.0) {
     m_p = 0;
   } else if (top_p >= 1.0) {
     m_p = nb;
   } else {
-    const double target = top_p * Z;
-    double c = incl - lane_sum;   // exclusive prefix of this lane
-    int below = 0;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const int p = lane * E + e;
-      c += ev[e];
-      if (p < nb && c < target) ++below;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) below += __shfl_xor_sync(0xffffffffu, below, off);
-    m_p = min(nb, below + 1);
+    const float smax = __shfl_sync(0xffffffffu, key_score(key[0]), 0);
+    bool near = false;
+    m_p = topp_count<E>(key, smax, lane, nb, top_p, false, &near);
+    // e_j is defined as the float32 rounding of exp(S_j - max). expf is within
+    // 2 ulp of the exact value, which moves any prefix sum (and Z) by at most
+    // 3e-7 of Z; only a row whose crossing lies that close to p can decide
+    // differently, and it is recomputed with the correctly rounded e_j.
+    if (near) m_p = topp_count<E>(key, smax, lane, nb, top_p, true, &near);
   }
   const int m = min(nb, max(m_p, max(k_floor, 1)));
   // threshold key = key at sorted position m-1

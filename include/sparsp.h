@@ -103,6 +103,15 @@ enum {
    * SPARSP_ERR_UNSUPPORTED before enqueuing anything. */
   SPARSP_OUT_RASTER = 1u << 3
 };
+/* Attention kernels: at most n persistent CTAs (1 <= n <= 4095) instead of
+ * one per SM (times the kernel's occupancy), encoded in bits 16..27 of the
+ * options as SPARSP_GRID_CAP(n); 0 there means no cap. Work items are pulled
+ * from one counter in a fixed order and each item's sums run in a fixed
+ * order inside its CTA, so the results are bitwise the same for every grid;
+ * the cap exists to show that, and to leave SMs to other work. */
+#define SPARSP_GRID_CAP_SHIFT 16
+#define SPARSP_GRID_CAP_MASK (0xFFFu << SPARSP_GRID_CAP_SHIFT)
+#define SPARSP_GRID_CAP(n) (((uint32_t)(n) << SPARSP_GRID_CAP_SHIFT) & SPARSP_GRID_CAP_MASK)
 
 /* Per-SM profile slots that attention kernels accumulate into (see prof). */
 #define SPARSP_PROF_SLOTS 1024

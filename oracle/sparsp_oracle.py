@@ -197,6 +197,14 @@ def row_softmax(s: np.ndarray) -> np.ndarray:
     return e / e.sum()
 
 
+def _exp_f32(row: np.ndarray) -> np.ndarray:
+    """e_j = exp(S_j - max S) of one float32 score row, correctly rounded to
+    float32: the difference is taken in float32, its exponential in float64,
+    and that is rounded once to float32."""
+    diff = (row - row.max()).astype(np.float32)
+    return np.exp(diff.astype(np.float64)).astype(np.float32)
+
+
 @dataclass
 class Selection:
     row_ptr: np.ndarray        # int32 [R+1]
@@ -207,7 +215,7 @@ class Selection:
     margin: np.ndarray         # per row: distance of the Top-p crossing from p (relative mass)
 
 
-def select(S: np.ndarray, top_p: float, k_floor: int, ambiguity: float = 1e-5) -> Selection:
+def select(S: np.ndarray, top_p: float, k_floor: int, ambiguity: float = 1e-12) -> Selection:
     """Top-p routing with a Top-k safety floor, per query-block row.
 
     S: float32 [R, nb] (R = B*H*nb rows, row r = (b*H + h)*nb + i).
@@ -218,10 +226,13 @@ def select(S: np.ndarray, top_p: float, k_floor: int, ambiguity: float = 1e-5) -
          (m_p = 0 when p <= 0, m_p = nb when p >= 1);
       4. m = min(nb, max(m_p, k_floor, 1))  (the safety floor; never empty);
       5. keep the first m blocks of that order, stored in ascending index order.
-    The cutoff compares prefix sums in float64 of e_j evaluated in float32,
-    the precision the device takes this decision in. Rows whose crossing lies
-    within `ambiguity` (relative mass) of p admit the neighbouring count too;
-    m_lo..m_hi records that.
+    e_j is the float32 rounding of exp(S_j - max S) (the exponent argument
+    itself a float32 difference), and Z and the prefix masses are float64 sums
+    of those values: the precision the device takes this decision in. Both
+    sides then hold identical e_j, and their prefix sums differ only by the
+    order of float64 additions (about 1e-13 of Z for nb <= 4096). Rows whose
+    crossing lies within `ambiguity` (relative mass) of p admit the
+    neighbouring count too; m_lo..m_hi records that.
     """
     S = np.asarray(S)
     if S.dtype != np.float32:
@@ -241,9 +252,7 @@ def select(S: np.ndarray, top_p: float, k_floor: int, ambiguity: float = 1e-5) -
         row = S[r] + np.float32(0.0)                       # -0.0 == +0.0
         order = np.argsort(-row.astype(np.float64), kind="stable")
         orders.append(order)
-        mx = row.max()
-        e32 = np.exp((row - mx).astype(np.float32)).astype(np.float32)
-        e = e32.astype(np.float64)
+        e = _exp_f32(row).astype(np.float64)
         Z = e.sum()
         if p <= 0.0:
             m_p = 0
@@ -658,16 +667,15 @@ def balance_heads(costs, P, max_migrations):
 
 def block_values(S) -> np.ndarray:
     """The value of every block of a row: its softmax mass, taken as selection
-    takes it (e_j = exp(S_j - max) in float32, Z = sum e in float64), rounded
-    to float32: v_j = fl32(e_j / Z). S: float32 [R, nb]."""
+    takes it (e_j = exp(S_j - max) correctly rounded to float32, Z = sum e in
+    float64), rounded to float32: v_j = fl32(e_j / Z). S: float32 [R, nb]."""
     S = np.asarray(S)
     if S.dtype != np.float32:
         raise TypeError("scores must be float32")
     out = np.zeros(S.shape, dtype=np.float32)
     for r in range(S.shape[0]):
         row = S[r] + np.float32(0.0)
-        e32 = np.exp((row - row.max()).astype(np.float32)).astype(np.float32)
-        e = e32.astype(np.float64)
+        e = _exp_f32(row).astype(np.float64)
         out[r] = (e / e.sum()).astype(np.float32)
     return out
 

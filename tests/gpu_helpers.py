@@ -74,11 +74,20 @@ def compare_values(got: np.ndarray, ref: np.ndarray, wl, what: str):
     return float(err.max()), float(err.mean())
 
 
+def bf16_floor(ref: np.ndarray) -> tuple[float, float]:
+    """Max and mean absolute error of the oracle's own values rounded to bf16:
+    the error a bf16 output cannot avoid."""
+    r32 = np.ascontiguousarray(ref, dtype=np.float32)
+    err = np.abs(synth.round_bf16(r32.copy()).astype(np.float64) - ref)
+    return float(err.max()), float(err.mean())
+
+
 def compare_csr(row_ptr: np.ndarray, col_idx: np.ndarray, sel: orc.Selection) -> int:
-    """Bit-exact CSR, except rows the oracle flags as within 1e-5 of the Top-p
-    threshold, where any count in its admissible range (and the corresponding
-    prefix of the score order) is accepted. Returns the number of such rows
-    whose count differed from the oracle's first choice."""
+    """Bit-exact CSR, except rows the oracle flags as within its ambiguity band
+    of the Top-p threshold (1e-12 of the row's mass: float64 summation order),
+    where any count in the admissible range (and the corresponding prefix of
+    the score order) is accepted. Returns the number of such rows whose count
+    differed from the oracle's first choice."""
     R = len(sel.row_ptr) - 1
     assert row_ptr.shape == (R + 1,)
     if np.array_equal(row_ptr, sel.row_ptr) and np.array_equal(col_idx[:row_ptr[-1]], sel.col_idx):

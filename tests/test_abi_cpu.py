@@ -181,6 +181,16 @@ def test_call_validation_codes(lib):
     assert lib.sparsp_attn_bwd(S, *((FAKE,) * 8), f(0.0), FAKE, FAKE, FAKE, FAKE, 1 << 30, 1 << 9, None, None,
                                None) == sp.INVALID_ARG
     assert lib.sparsp_lpt_schedule(S, FAKE, 1 << 9, FAKE, FAKE, 1 << 30, None) == sp.INVALID_ARG
+    assert lib.sparsp_attn_fwd(S, *p7, f(0.0), FAKE, FAKE, FAKE, 1 << 30, 1 << 28, None, None,
+                               None) == sp.INVALID_ARG     # above the grid-cap field
+    # the grid-cap field itself is accepted (the call then fails on the next check: the workspace)
+    assert lib.sparsp_attn_fwd(S, *p7, f(0.0), FAKE, FAKE, FAKE, 8, sp.GRID_CAP(7), None, None,
+                               None) == sp.WORKSPACE
+    assert lib.sparsp_attn_bwd(S, *((FAKE,) * 8), f(0.0), FAKE, FAKE, FAKE, FAKE, 8, sp.GRID_CAP(4095), None,
+                               None, None) == sp.WORKSPACE
+    assert sp.GRID_CAP(7) == 7 << 16
+    with pytest.raises(ValueError):
+        sp.GRID_CAP(0)
     # raster O is written by the tcgen05 kernel only: fp32, or the portable kernel, is refused
     assert lib.sparsp_attn_fwd(ctypes.byref(s32), *p7, f(0.0), FAKE, FAKE, FAKE, 1 << 30, sp.OUT_RASTER, None,
                                None, None) == sp.UNSUPPORTED

@@ -41,3 +41,26 @@ def test_overlapped_stages_use_their_begin_marks(bench):
     assert st["reorder_out"] == pytest.approx(0.5)
     assert st["select"] == pytest.approx(1.4)
     assert st["kv_demand"] == pytest.approx(0.1)
+
+
+def test_stage_bytes_and_l2_resident_stages(bench):
+    """Algorithmic bytes of the Wan-layer step's memory-bound stages, and the
+    rule that a stage whose bytes fit in L2 gets no fraction of the HBM peak."""
+    import synth
+    wl = synth.WORKLOADS["wan"]
+
+    class Shape:
+        B, H, N, d, nb, Bt = wl.B, wl.H, wl.N, wl.d, wl.nb, wl.Bt
+
+    nnz, demanded = 2_076_448, 5_000_000_000
+    tensor = 40 * 30720 * 128 * 2
+    b = bench.stage_bytes(Shape, wl, nnz, demanded, fused=True, overlapped=True)
+    assert b["reorder"] == 6 * tensor + 2 * 40 * 240 * 128 * 4
+    assert b["select"] == 4 * 40 * 240 * 240 + 4 * (nnz + 40 * 240 + 1)
+    assert b["kv_gather"] == demanded + 2 * tensor
+    serial = bench.stage_bytes(Shape, wl, nnz, demanded, fused=True, overlapped=False)
+    assert "kv_gather" not in serial and serial["kv_demand"] == b["kv_demand"] + b["kv_gather"]
+    h = bench.hbm_fractions({"reorder": 0.3, "select": 0.05, "missing": 1.0}, b, 6700.0)
+    assert h["reorder"]["frac"] == pytest.approx(b["reorder"] / 0.3e-3 / 1e9 / 6700.0)
+    assert h["select"]["frac"] is None and h["select"]["l2_resident"]
+    assert "scores" not in h
