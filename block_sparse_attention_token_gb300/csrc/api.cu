@@ -59,7 +59,8 @@ constexpr uint32_t kKnownFlags = SPARSP_SCHED_FLAT | SPARSP_KERNEL_PORTABLE | SP
 struct AttnWs {
   int32_t* items;      // [rows]
   int32_t* counter;    // [4]
-  int32_t* hist;       // [B*H*(nb+1)] flat-order scratch
+  int32_t* hist;       // [B*H*(2nb+1)] flat-order scratch
+  int32_t* pair_ptr;   // [B*H*ceil(nb/2)+1] row offsets of query-block pairs (64-token blocks)
   // backward only
   int32_t* col_ptr;    // [rows+1]
   int32_t* row_idx;    // [B*H*nb*nb]
@@ -82,6 +83,7 @@ AttnWs attn_ws_layout(const Dims& s, bool backward, void* base) {
   w.items = (int32_t*)take(rows * 4);
   w.counter = (int32_t*)take(16);
   w.hist = (int32_t*)take(lpt_ws(s));
+  w.pair_ptr = (int32_t*)take(((size_t)s.B * s.H * ((s.nb + 1) / 2) + 1) * 4);
   if (backward) {
     w.col_ptr = (int32_t*)take((rows + 1) * 4);
     w.row_idx = (int32_t*)take(rows * (size_t)s.nb * 4);
@@ -466,7 +468,18 @@ sparsp_status_t sparsp_attn_fwd(const sparsp_shape_t* shape, const void* q, cons
   const bool raster = (flags & SPARSP_OUT_RASTER) != 0;
   if (raster && !tc) return SPARSP_ERR_UNSUPPORTED;   // only the tcgen05 kernel writes raster rows
   cudaStream_t st = (cudaStream_t)stream;
-  r = launch_lpt(s, row_ptr, (flags & SPARSP_SCHED_FLAT) != 0, w.items, w.counter, w.hist, st);
+  const bool flat = (flags & SPARSP_SCHED_FLAT) != 0;
+  if (tc && attn_fwd_tc_items_per_head(s) != s.nb) {
+    // the tcgen05 kernel's items are pairs of query blocks: order the pairs,
+    // each costing the sum of its two rows
+    r = launch_pair_ptr(s, row_ptr, w.pair_ptr, st);
+    if (r != SPARSP_OK) return r;
+    Dims sp = s;
+    sp.nb = attn_fwd_tc_items_per_head(s);
+    r = launch_lpt(sp, w.pair_ptr, flat, w.items, w.counter, w.hist, st, 2 * s.nb);
+  } else {
+    r = launch_lpt(s, row_ptr, flat, w.items, w.counter, w.hist, st);
+  }
   if (r != SPARSP_OK) return r;
   if (s.dtype == SPARSP_F32)
     return launch_attn_fwd_f32(s, (const float*)q, (const float*)k, (const float*)v, row_ptr,

@@ -1,24 +1,37 @@
 // Step 5a, bf16, Bt and d in {64, 128} on sm_103a: block-sparse flash-attention
-// forward on the 5th-generation tensor cores (tcgen05 + TMEM + TMA). The query
-// tile is always the MMA's 128 rows; with 64-token blocks its second half holds
-// the next block's rows, computed and not stored.
+// forward on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
 //
-// One persistent CTA per SM, 7 warps:
-//   warp 4     producer: pulls (b, h, query block) items longest-first through
-//              an atomic counter, validates the CSR row, publishes the item in
-//              a shared-memory ring, and TMA-loads Q_i and the selected K_j / V_j
-//              tiles (128 x 128 bf16, two 64-column boxes with 128-byte swizzle)
-//              into 3-stage K and V rings, addressed through
-//              the CSR (row coordinate = bh*N + j*128).
-//   warp 5     S issuer: S_j = Q K_j^T into one of two TMEM S buffers (M=N=128,
+// Every MMA works on 128 query rows (M = 128, the 128 TMEM lanes) and on
+// stages of 128 key tokens. With 128-token blocks a work item is one query
+// block and a stage one key block. With 64-token blocks a work item is a PAIR
+// of neighbouring query blocks of a head (2p and 2p + 1: 128 contiguous rows)
+// processed over the union of their two CSR rows, and a stage holds two key
+// blocks of that union (two 64-row TMA boxes side by side); each 64-column half
+// of S is masked, for each of the two query blocks, when that block did not
+// select the key block (its P is zero there and no exponential is evaluated).
+// So no MMA row or column is computed for nothing except where the two rows'
+// selections differ ("Dynamic Sparsity in Large-Scale Video DiT Training",
+// "How DSV works": queries grouped so that one key set serves several).
+//
+// One persistent CTA per SM; for d = 128, 7 warps (4 softmax warps, then the
+// producer, the S issuer and the PV issuer), for d = 64, 11 warps (8 softmax
+// warps in two groups, one per 64-column half of a stage, each with its own
+// running max, sum and O accumulator, combined once per item; see Cfg::SPLIT):
+//   producer: pulls items longest-first through an atomic counter,
+//              validates the CSR row(s), publishes the item in a shared-memory
+//              ring (for pairs with the two rows as bitmaps), and TMA-loads the
+//              query tile and the K / V tiles of each stage (64-column boxes
+//              with 128-byte swizzle) into 3-stage K and V rings, addressed
+//              through the CSR (row coordinate = bh*N + j*Bt).
+//   S issuer: S = Q K^T into one of two TMEM S buffers (M=N=128,
 //              K=16 per instruction, both operands K-major from shared memory).
-//   warp 6     PV issuer: O += P_j V_j (A = P_j read from TMEM as packed bf16,
-//              B = V_j MN-major from shared memory).
+//   PV issuer: O += P V (A = P read from TMEM as packed bf16,
+//              B = V MN-major from shared memory).
 //              The two GEMM streams are issued by different warps so that a
 //              wait in one (for P, or for a free S buffer) never holds back the
 //              other; each warp runs uniformly and one elected lane issues
 //              tcgen05.mma / tcgen05.commit.
-//   warps 0-3  softmax and epilogue: thread t owns query row t = TMEM lane t.
+//   softmax and epilogue: thread t owns query row t = TMEM lane t.
 //              It reads its S row from TMEM with the sm_103 load-with-maximum
 //              (tcgen05.ld.red: each 32-column load also returns the maximum of
 //              the 32 values, so the row max costs no extra instructions), keeps
@@ -28,9 +41,11 @@
 //              than 8 (a factor 256); otherwise the stale max is kept, which
 //              leaves the result unchanged up to rounding because O and l use
 //              the same reference. At the end of the row: O / l to global
-//              memory, LSE = (m + log2 l) ln 2.
-// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256,384), P0 [384,448),
-// P1 [448,512). Every mbarrier wait is bounded (2 s); on expiry the CTA sets
+//              memory, LSE = (m + log2 l) ln 2 (O = 0, LSE = -inf for a row
+//              that attended to nothing). A warp's 32 rows belong to one query
+//              block, so the masks of a pair are warp-uniform.
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256,384) (d = 64: O_a
+// [256,320) and O_b [320,384)), P0 [384,448), P1 [448,512). Every mbarrier wait is bounded (2 s); on expiry the CTA sets
 // SPARSP_ERR_TIMEOUT, all roles leave their loops, copies and MMAs in flight
 // are drained with a second bounded wait, and TMEM is released.
 #include "tc_helpers.cuh"
@@ -40,30 +55,48 @@ namespace {
 
 using namespace tc;
 
-constexpr int kNK = 3, kNV = 3, kNI = 4;
-constexpr int kThreads = 224;   // 4 softmax warps, producer, S issuer, PV issuer
+constexpr int kMaxStages = 6, kNI = 4;   // K / V ring depth <= kMaxStages (Cfg::NK)
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
 enum Bar {
-  Q_FULL = 0, Q_EMPTY, K_FULL, K_EMPTY = K_FULL + kNK, V_FULL = K_EMPTY + kNK, V_EMPTY = V_FULL + kNV,
-  S_FULL = V_EMPTY + kNV, S_FREE = S_FULL + 2, P_FULL = S_FREE + 2, PV_DONE = P_FULL + 2, O_FULL = PV_DONE + 2,
+  Q_FULL = 0, Q_EMPTY, K_FULL, K_EMPTY = K_FULL + kMaxStages, V_FULL = K_EMPTY + kMaxStages,
+  V_EMPTY = V_FULL + kMaxStages, S_FULL = V_EMPTY + kMaxStages, S_FREE = S_FULL + 2, P_FULL = S_FREE + 2, PV_DONE = P_FULL + 2, O_FULL = PV_DONE + 2,
   O_EMPTY,
-  I_FULL, I_EMPTY = I_FULL + kNI, TEAR = I_EMPTY + kNI, TEAR_PV, NBAR
+  I_FULL, I_EMPTY = I_FULL + kNI, TEAR = I_EMPTY + kNI, TEAR_PV, STAT, NBAR
 };
-// Tile geometry for key blocks of BT tokens and head dimension D. The query
-// tile is always 128 rows (the MMA's M; the 128 TMEM lanes): with BT = 64 the
-// rows past the block belong to the next block (or are zero past the tensor's
-// end), are computed and never stored. Tiles are TMA'd as 64-column boxes of
-// 128-byte rows with 128-byte swizzle.
+// Tile geometry for blocks of BT tokens and head dimension D. The query tile
+// and a key/value stage are 128 rows each: one block, or two 64-token blocks
+// (PAIR). Tiles are TMA'd as 64-column boxes of 128-byte rows with 128-byte
+// swizzle; a stage of two blocks is two 64-row boxes per column box, the
+// second 64 rows (8 KB, a whole number of 1 KB swizzle atoms) after the first.
+constexpr int kMaxWords = 32;   // bitmap words of one CSR row (nb <= 1024)
 template <int BT_, int D_>
 struct Cfg {
-  static constexpr int BT = BT_, D = D_, QR = 128;
+  static constexpr int BT = BT_, D = D_, QR = 128, KR = 128;
+  static constexpr bool PAIR = BT == 64;
+  // d = 64: two softmax warpgroups, one per 64-column half of a stage, each
+  // with its own running max, sum and O accumulator (TMEM O_a [256,320),
+  // O_b [320,384)), combined once per item. Two softmax warps per SM
+  // sub-partition hide each other's latencies.
+  static constexpr bool SPLIT = D == 64;
+  static constexpr int NSM = SPLIT ? 8 : 4;               // softmax warps
+  static constexpr int THREADS = 32 * (NSM + 3);           // + producer, S issuer, PV issuer
+  static constexpr int W_PROD = NSM, W_S = NSM + 1, W_PV = NSM + 2;
+  // K and V ring stages: 3 fit beside a d = 128 query tile; with d = 64 the
+  // tiles are half the size and 6 stages keep more L2 loads in flight (a stage
+  // then takes half the tensor time, so the same latency needs twice the depth)
+  static constexpr int NK = D == 64 ? 6 : 3, NV = NK;
   static constexpr int NBOX = D / 64;                     // 64-column boxes per row tile
-  static constexpr uint32_t kQBox = QR * 128, kKBox = BT * 128;
+  static constexpr uint32_t kQBox = QR * 128, kKBox = KR * 128, kHalfBox = 64 * 128;
   static constexpr uint32_t kQTile = kQBox * NBOX, kKTile = kKBox * NBOX;
-  static constexpr uint32_t kOffK = kQTile, kOffV = kOffK + kNK * kKTile, kOffBar = kOffV + kNV * kKTile;
+  static constexpr uint32_t kOffK = kQTile, kOffV = kOffK + NK * kKTile, kOffBar = kOffV + NV * kKTile;
   static constexpr uint32_t kOffRing = kOffBar + 8 * NBAR;
-  static constexpr uint32_t kOffMisc = kOffRing + 8 * kNI;
+  static constexpr uint32_t kOffBits = kOffRing + 16 * kNI;
+  static constexpr uint32_t kBitsBytes = PAIR ? kNI * 2 * kMaxWords * 4 : 0;
+  static constexpr uint32_t kOffStat = kOffBits + kBitsBytes;   // [2 parities][2 groups][128 rows] (m, l)
+  static constexpr uint32_t kStatBytes = SPLIT ? 2 * 2 * 128 * 8 : 0;
+  static constexpr uint32_t kOffMisc = kOffStat + kStatBytes;
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory");
 };
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
@@ -108,6 +141,7 @@ struct Params {
   const int32_t* col_idx;
   int64_t N;
   int nb;
+  int nbp;           // items per head: nb, or ceil(nb/2) pairs of 64-token blocks
   int64_t n_items;
   float scale_log2;
   __nv_bfloat16* o;
@@ -121,8 +155,59 @@ struct Params {
   int32_t* d_status;
 };
 
+// Walk over the set bits of (a | b) in ascending order, two at a time: the
+// key blocks of the stages of a pair item. The same walk runs in the producer
+// and in every softmax warp (uniformly), so they agree on each stage's blocks.
+struct UnionWalk {
+  const uint32_t* a;
+  const uint32_t* b;
+  int words, w;
+  uint32_t cur;
+  __device__ __forceinline__ UnionWalk(const uint32_t* a_, const uint32_t* b_, int words_)
+      : a(a_), b(b_), words(words_), w(0), cur(words_ > 0 ? (a_[0] | b_[0]) : 0u) {}
+  __device__ __forceinline__ int next() {
+    while (cur == 0u) {
+      if (++w >= words) return -1;
+      cur = a[w] | b[w];
+    }
+    const int j = w * 32 + __ffs(cur) - 1;
+    cur &= cur - 1u;
+    return j;
+  }
+};
+
+__device__ __forceinline__ bool bit_of(const uint32_t* m, int j) { return (m[j >> 5] >> (j & 31)) & 1u; }
+
+// Validates CSR row r (length <= nb, indices in [0, nb), no index twice) and
+// writes its bitmap (words zeroed before). Warp-collective; returns false for
+// a bad row, whose bitmap is then cleared.
+__device__ __forceinline__ bool row_bitmap(const Params& p, int64_t r, uint32_t* bm, int words, int lane) {
+  const int32_t a = p.row_ptr[r], b = p.row_ptr[r + 1];
+  bool bad = (b < a) || (b - a > p.nb);
+  if (!bad)
+    for (int32_t e = a + lane; e < b; e += 32) {
+      const int32_t j = p.col_idx[e];
+      if (j < 0 || j >= p.nb) bad = true;
+      else atomicOr(&bm[j >> 5], 1u << (j & 31));
+    }
+  bad = __any_sync(0xffffffffu, bad);
+  __syncwarp();
+  if (!bad) {
+    int cnt = 0;
+    for (int w = lane; w < words; w += 32) cnt += __popc(bm[w]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+    bad = cnt != b - a;   // an index listed twice
+  }
+  if (bad) {
+    for (int w = lane; w < words; w += 32) bm[w] = 0u;
+    __syncwarp();
+  }
+  return !bad;
+}
+
 template <int BT, int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<BT, D>::THREADS, 1)
 attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -130,49 +215,54 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   using C = Cfg<BT, D>;
+  constexpr bool PAIR = C::PAIR;
   const uint32_t sQ = base, sK = base + C::kOffK, sV = base + C::kOffV;
   auto bar = [&](int idx) -> uint32_t { return base + C::kOffBar + 8u * (uint32_t)idx; };
-  volatile int2* ring = reinterpret_cast<volatile int2*>(gbase + C::kOffRing);
+  // ring entry: x = item, y = stages (-1: skip, -2: end), z = bad-row bits (pairs)
+  volatile int4* ring = reinterpret_cast<volatile int4*>(gbase + C::kOffRing);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(gbase + C::kOffBits);   // [kNI][2][kMaxWords] (pairs)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + C::kOffMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t t_start = globaltimer_ns();
+  const int words = (p.nb + 31) >> 5;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(Q_FULL), 1);
     mbar_init(bar(Q_EMPTY), 1);
-    for (int s = 0; s < kNK; ++s) {
+    for (int s = 0; s < C::NK; ++s) {
       mbar_init(bar(K_FULL + s), 1);
       mbar_init(bar(K_EMPTY + s), 1);
     }
-    for (int s = 0; s < kNV; ++s) {
+    for (int s = 0; s < C::NV; ++s) {
       mbar_init(bar(V_FULL + s), 1);
       mbar_init(bar(V_EMPTY + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(S_FULL + b), 1);
-      mbar_init(bar(S_FREE + b), 128);
-      mbar_init(bar(P_FULL + b), 128);
+      mbar_init(bar(S_FREE + b), 32 * C::NSM);
+      mbar_init(bar(P_FULL + b), 32 * C::NSM);
     }
     mbar_init(bar(PV_DONE), 1);
     mbar_init(bar(PV_DONE + 1), 1);
     mbar_init(bar(O_FULL), 1);
-    mbar_init(bar(O_EMPTY), 128);
+    mbar_init(bar(O_EMPTY), 32 * C::NSM);
     for (int r = 0; r < kNI; ++r) {
       mbar_init(bar(I_FULL + r), 1);
-      mbar_init(bar(I_EMPTY + r), 6);
+      mbar_init(bar(I_EMPTY + r), C::NSM + 2);
     }
     mbar_init(bar(TEAR), 1);
     mbar_init(bar(TEAR_PV), 1);
+    mbar_init(bar(STAT), 32 * C::NSM);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == C::W_PROD && lane == 0) {
     prefetch_tmap(&tq);
     prefetch_tmap(&tk);
     prefetch_tmap(&tv);
   }
-  if (warp == 5) {
+  if (warp == C::W_S) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -181,47 +271,68 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   fence_after();
   const uint32_t tmem = *tmem_slot;
   const Guard g{abort_flag, p.d_status, kWaitNs};
-  const int nb = p.nb;
+  const int nb = p.nb, nbp = p.nbp;
 
-  if (warp == 4) {
+  if (warp == C::W_PROD) {
     // ------------------------------------------------------------ producer
     uint32_t it_fill = 0, q_fill = 0, k_fill = 0, v_fill = 0;
     for (;;) {
       int32_t slot = 0;
       if (lane == 0) slot = atomicAdd(p.counter, 1);
       slot = __shfl_sync(0xffffffffu, slot, 0);
-      int32_t item = -1, len = -2;
-      if (slot < p.n_items) {
-        item = p.items[slot];
-        const int32_t a = p.row_ptr[item], b = p.row_ptr[item + 1];
-        bool bad = (b < a) || (b - a > nb);
-        if (!bad)
-          for (int32_t e = a + lane; e < b; e += 32) {
-            const int32_t j = p.col_idx[e];
-            if (j < 0 || j >= nb) bad = true;
-          }
-        bad = __any_sync(0xffffffffu, bad);
-        if (bad) {
-          if (lane == 0) report(p.d_status, SPARSP_ERR_DATA);
-          len = -1;
-        } else {
-          len = b - a;
-        }
-      }
       const int ri = (int)(it_fill % kNI);
       if (!wait_warp(bar(I_EMPTY + ri), ((it_fill / kNI) & 1u) ^ 1u, g)) break;
+      uint32_t* bmA = bits + ri * 2 * kMaxWords;
+      uint32_t* bmB = bmA + kMaxWords;
+      int32_t item = -1, len = -2, badbits = 0;
+      if (slot < p.n_items) {
+        item = p.items[slot];
+        if constexpr (PAIR) {
+          // the two rows as bitmaps in the ring slot; a bad row counts as empty
+          const int64_t bh = item / nbp;
+          const int iA = 2 * (item % nbp);
+          for (int w = lane; w < 2 * kMaxWords; w += 32) bmA[w] = 0u;
+          __syncwarp();
+          const bool okA = row_bitmap(p, bh * nb + iA, bmA, words, lane);
+          const bool okB = iA + 1 < nb ? row_bitmap(p, bh * nb + iA + 1, bmB, words, lane) : true;
+          badbits = (okA ? 0 : 1) | (okB ? 0 : 2);
+          if (badbits && lane == 0) report(p.d_status, SPARSP_ERR_DATA);
+          int u = 0;
+          for (int w = lane; w < words; w += 32) u += __popc(bmA[w] | bmB[w]);
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) u += __shfl_xor_sync(0xffffffffu, u, off);
+          len = (badbits == 3) ? -1 : (u + 1) / 2;   // stages of two key blocks
+        } else {
+          const int32_t a = p.row_ptr[item], b = p.row_ptr[item + 1];
+          bool bad = (b < a) || (b - a > nb);
+          if (!bad)
+            for (int32_t e = a + lane; e < b; e += 32) {
+              const int32_t j = p.col_idx[e];
+              if (j < 0 || j >= nb) bad = true;
+            }
+          bad = __any_sync(0xffffffffu, bad);
+          if (bad) {
+            if (lane == 0) report(p.d_status, SPARSP_ERR_DATA);
+            len = -1;
+          } else {
+            len = b - a;
+          }
+        }
+      }
+      __syncwarp();
       if (lane == 0) {
         ring[ri].x = item;
         ring[ri].y = len;
+        ring[ri].z = badbits;
         mbar_arrive(bar(I_FULL + ri));
       }
       __syncwarp();
       ++it_fill;
       if (len == -2) break;
       if (len <= 0) continue;
-      const int64_t bh = item / nb;
-      const int i = item % nb;
-      const int32_t yq = (int32_t)(bh * p.N + (int64_t)i * BT);
+      const int64_t bh = item / nbp;
+      const int i0 = PAIR ? 2 * (item % nbp) : item % nb;   // first query block of the item
+      const int32_t yq = (int32_t)(bh * p.N + (int64_t)i0 * BT);
       if (!wait_warp(bar(Q_EMPTY), (q_fill & 1u) ^ 1u, g)) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(bar(Q_FULL), C::kQTile);
@@ -229,27 +340,42 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         for (int h = 0; h < C::NBOX; ++h) tma_load_2d(sQ + h * C::kQBox, &tq, bar(Q_FULL), 64 * h, yq);
       }
       ++q_fill;
-      const int32_t e0 = p.row_ptr[item];
+      const int32_t e0 = PAIR ? 0 : p.row_ptr[item];
+      UnionWalk walk(bmA, bmB, PAIR ? words : 0);
       bool ok = true;
       for (int e = 0; e < len && ok; ++e) {
-        const int32_t j = p.col_idx[e0 + e];
-        const int32_t yk = (int32_t)(bh * p.N + (int64_t)j * BT);
-        const uint32_t ks = k_fill % kNK;
-        if (!(ok = wait_warp(bar(K_EMPTY + ks), ((k_fill / kNK) & 1u) ^ 1u, g))) break;
+        int32_t j1, j2 = 0;
+        if constexpr (PAIR) {
+          j1 = walk.next();
+          j2 = walk.next();
+          if (j2 < 0) j2 = j1;   // a lone last block: loaded twice, its second half masked
+        } else {
+          j1 = p.col_idx[e0 + e];
+        }
+        const int32_t yk1 = (int32_t)(bh * p.N + (int64_t)j1 * BT);
+        const int32_t yk2 = (int32_t)(bh * p.N + (int64_t)j2 * BT);
+        const uint32_t ks = k_fill % C::NK;
+        if (!(ok = wait_warp(bar(K_EMPTY + ks), ((k_fill / C::NK) & 1u) ^ 1u, g))) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(K_FULL + ks), C::kKTile);
 #pragma unroll
-          for (int h = 0; h < C::NBOX; ++h)
-            tma_load_2d(sK + ks * C::kKTile + h * C::kKBox, &tk, bar(K_FULL + ks), 64 * h, yk);
+          for (int h = 0; h < C::NBOX; ++h) {
+            const uint32_t dst = sK + ks * C::kKTile + h * C::kKBox;
+            tma_load_2d(dst, &tk, bar(K_FULL + ks), 64 * h, yk1);
+            if (PAIR) tma_load_2d(dst + C::kHalfBox, &tk, bar(K_FULL + ks), 64 * h, yk2);
+          }
         }
         ++k_fill;
-        const uint32_t vs = v_fill % kNV;
-        if (!(ok = wait_warp(bar(V_EMPTY + vs), ((v_fill / kNV) & 1u) ^ 1u, g))) break;
+        const uint32_t vs = v_fill % C::NV;
+        if (!(ok = wait_warp(bar(V_EMPTY + vs), ((v_fill / C::NV) & 1u) ^ 1u, g))) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(V_FULL + vs), C::kKTile);
 #pragma unroll
-          for (int h = 0; h < C::NBOX; ++h)
-            tma_load_2d(sV + vs * C::kKTile + h * C::kKBox, &tv, bar(V_FULL + vs), 64 * h, yk);
+          for (int h = 0; h < C::NBOX; ++h) {
+            const uint32_t dst = sV + vs * C::kKTile + h * C::kKBox;
+            tma_load_2d(dst, &tv, bar(V_FULL + vs), 64 * h, yk1);
+            if (PAIR) tma_load_2d(dst + C::kHalfBox, &tv, bar(V_FULL + vs), 64 * h, yk2);
+          }
         }
         ++v_fill;
       }
@@ -258,33 +384,32 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     if (*abort_flag && lane == 0) {
       // drain copies still in flight before the shared memory goes away
       if (q_fill) wait_raw(bar(Q_FULL), (q_fill - 1) & 1u, kDrainNs);
-      for (uint32_t s = 0; s < kNK; ++s)
-        if (k_fill > s) wait_raw(bar(K_FULL + s), ((k_fill - 1 - s) / kNK) & 1u, kDrainNs);
-      for (uint32_t s = 0; s < kNV; ++s)
-        if (v_fill > s) wait_raw(bar(V_FULL + s), ((v_fill - 1 - s) / kNV) & 1u, kDrainNs);
+      for (uint32_t s = 0; s < C::NK; ++s)
+        if (k_fill > s) wait_raw(bar(K_FULL + s), ((k_fill - 1 - s) / C::NK) & 1u, kDrainNs);
+      for (uint32_t s = 0; s < C::NV; ++s)
+        if (v_fill > s) wait_raw(bar(V_FULL + s), ((v_fill - 1 - s) / C::NV) & 1u, kDrainNs);
     }
-  } else if (warp == 5) {
+  } else if (warp == C::W_S) {
     // ------------------------------------------------------------ S = Q K^T issuer
-    constexpr uint32_t idS = idesc_bf16(128, BT, 0, 0);
+    constexpr uint32_t idS = idesc_bf16(128, C::KR, 0, 0);
     uint32_t it_use = 0, q_use = 0, k_use = 0, s_issue = 0;
     bool issued_any = false;
     for (;;) {
       const int ri = (int)(it_use % kNI);
       if (!wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
-      const int2 ent = make_int2(ring[ri].x, ring[ri].y);
+      const int len = ring[ri].y;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
       ++it_use;
-      if (ent.y == -2) break;
-      if (ent.y <= 0) continue;
-      const int len = ent.y;
+      if (len == -2) break;
+      if (len <= 0) continue;
       if (!wait_warp(bar(Q_FULL), q_use & 1u, g)) break;
       ++q_use;
       bool ok = true;
       for (int e = 0; e < len; ++e) {
-        const uint32_t b = s_issue & 1u, ks = k_use % kNK;
+        const uint32_t b = s_issue & 1u, ks = k_use % C::NK;
         if (!(ok = wait_warp(bar(S_FREE + b), ((s_issue >> 1) & 1u) ^ 1u, g))) break;
-        if (!(ok = wait_warp(bar(K_FULL + ks), (k_use / kNK) & 1u, g))) break;
+        if (!(ok = wait_warp(bar(K_FULL + ks), (k_use / C::NK) & 1u, g))) break;
         fence_after();
         const uint32_t kb = sK + ks * C::kKTile;
         if (elect_one()) {
@@ -313,7 +438,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       wait_raw(bar(TEAR), 0, kDrainNs);
     }
     __syncwarp();
-  } else if (warp == 6) {
+  } else if (warp == C::W_PV) {
     // ------------------------------------------------------------ O += P V issuer
     constexpr uint32_t idO = idesc_bf16(128, D, 0, 1);
     uint32_t it_use = 0, v_use = 0, pv = 0, o_items = 0;
@@ -321,27 +446,37 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     for (;;) {
       const int ri = (int)(it_use % kNI);
       if (!wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
-      const int2 ent = make_int2(ring[ri].x, ring[ri].y);
+      const int len = ring[ri].y;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
       ++it_use;
-      if (ent.y == -2) break;
-      if (ent.y <= 0) continue;
-      const int len = ent.y;
+      if (len == -2) break;
+      if (len <= 0) continue;
       bool ok = true;
       for (int e = 0; e < len; ++e) {
-        const uint32_t b = pv & 1u, vs = v_use % kNV;
-        if (!(ok = wait_warp(bar(V_FULL + vs), (v_use / kNV) & 1u, g))) break;
+        const uint32_t b = pv & 1u, vs = v_use % C::NV;
+        if (!(ok = wait_warp(bar(V_FULL + vs), (v_use / C::NV) & 1u, g))) break;
         if (!(ok = wait_warp(bar(P_FULL + b), (pv >> 1) & 1u, g))) break;
         if (e == 0 && !(ok = wait_warp(bar(O_EMPTY), (o_items & 1u) ^ 1u, g))) break;
         fence_after();
         const uint32_t vb = sV + vs * C::kKTile;
         if (elect_one()) {
+          if constexpr (C::SPLIT) {
+            // O_g += P_g V[64g, 64g + 64): the keys of half g into accumulator g
 #pragma unroll
-          for (int kk = 0; kk < BT / 16; ++kk)
-            mma_ts(tmem + kColO, tmem + kColP + b * 64u + (uint32_t)kk * 8u,
-                   smem_desc(vb + (uint32_t)kk * 2048u, C::kKBox, 1024, kSwizzle128B), idO,
-                   (e > 0 || kk > 0) ? 1u : 0u);
+            for (int hg = 0; hg < 2; ++hg)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ts(tmem + kColO + (uint32_t)hg * 64u, tmem + kColP + b * 64u + (uint32_t)hg * 32u + (uint32_t)kk * 8u,
+                       smem_desc(vb + (uint32_t)(hg * 4 + kk) * 2048u, C::kKBox, 1024, kSwizzle128B), idO,
+                       (e > 0 || kk > 0) ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < C::KR / 16; ++kk)
+              mma_ts(tmem + kColO, tmem + kColP + b * 64u + (uint32_t)kk * 8u,
+                     smem_desc(vb + (uint32_t)kk * 2048u, C::kKBox, 1024, kSwizzle128B), idO,
+                     (e > 0 || kk > 0) ? 1u : 0u);
+          }
           commit(bar(V_EMPTY + vs));
           commit(bar(PV_DONE + b));
           if (e + 1 == len) commit(bar(O_FULL));
@@ -361,95 +496,127 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax + epilogue
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    if constexpr (C::SPLIT) {
+    // ------------------------------------------------------------ softmax + epilogue, d = 64
+    // Warp w: lanes (rows) 32*(w & 3) .. +31 of the tile, columns [64g, 64g + 64)
+    // of every stage with g = w >> 2: group g owns one half of the stage's keys
+    // (one key block of a pair), with its own max m, sum l and accumulator O_g.
+    const int grp = warp >> 2;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t t_row = tmem + lane_base;
+    const int r = (warp & 3) * 32 + lane;   // tile row = TMEM lane
     uint32_t it_use = 0, s_use = 0, o_items = 0;
     uint64_t blocks_done = 0;
     const float sl2 = p.scale_log2;
+    const int half = PAIR ? (r >> 6) : 0;   // with pairs: the row's query block within the pair
+    float2* stat = reinterpret_cast<float2*>(gbase + C::kOffStat);   // [parity][group][row]
+    bool ok = true;
     for (;;) {
       const int ri = (int)(it_use % kNI);
       if (!wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
-      const int2 ent = make_int2(ring[ri].x, ring[ri].y);
+      const int64_t item = ring[ri].x;
+      const int len = ring[ri].y;
+      const int badbits = ring[ri].z;
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
+      auto release = [&]() {
+        if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
+      };
+      if (!PAIR) release();
       ++it_use;
-      if (ent.y == -2) break;
-      if (ent.y == -1) continue;
-      const int64_t item = ent.x;
-      const int64_t bh = item / nb;
-      const int i = (int)(item % nb);
-      const int64_t row = bh * p.N + (int64_t)i * BT + threadIdx.x;
-      const bool stores = threadIdx.x < BT;   // rows past the block are computed, never stored
+      if (len == -2) {
+        if (PAIR) release();
+        break;
+      }
+      if (len == -1) {
+        if (PAIR) release();
+        continue;
+      }
+      const int64_t bh = item / nbp;
+      const int i = PAIR ? 2 * (int)(item % nbp) + half : (int)(item % nb);
+      const int o = PAIR ? (r & 63) : r;
+      const int64_t row = bh * p.N + (int64_t)i * BT + o;
+      const bool stores = o < BT && i < nb && !((badbits >> half) & 1);
       int64_t orow_idx = row;
       if (p.raster && stores) {
-        // tile i = (bt, by, bx) block-raster; token o = (it, iy, ix) raster inside the tile
-        const int o = threadIdx.x, tbc = p.tb * p.tc;
+        const int tbc = p.tb * p.tc;
         const int bx = i % p.nX, by = (i / p.nX) % p.nY, bt = i / (p.nX * p.nY);
         const int it = o / tbc, iy = (o - it * tbc) / p.tc, ix = o - it * tbc - iy * p.tc;
         const int64_t n = ((int64_t)bt * p.ta + it) * p.Y * p.X + ((int64_t)by * p.tb + iy) * p.X +
                           (int64_t)bx * p.tc + ix;
         orow_idx = ((bh / p.H) * p.N + n) * p.H + bh % p.H;
       }
-      uint4* orow = reinterpret_cast<uint4*>(p.o + orow_idx * D);
-      const int len = ent.y;
+      // this group stores columns [32*grp, 32*grp + 32) of the row
+      uint4* orow = reinterpret_cast<uint4*>(p.o + orow_idx * D) + grp * 4;
       if (len == 0) {
         if (stores) {
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
-          p.lse[row] = -INFINITY;
+          for (int c = 0; c < 4; ++c) orow[c] = make_uint4(0, 0, 0, 0);
+          if (grp == 0) p.lse[row] = -INFINITY;
         }
+        if (PAIR) release();
         continue;
       }
+      const uint32_t* bmA = bits + ri * 2 * kMaxWords;
+      const uint32_t* mine = bmA + half * kMaxWords;
+      UnionWalk walk(bmA, bmA + kMaxWords, PAIR ? words : 0);
       float m = -INFINITY, l = 0.f;
-      bool ok = true;
       for (int e = 0; e < len; ++e) {
+        // does this row attend to this group's key block of the stage (warp-uniform)
+        bool has = true;
+        if constexpr (PAIR) {
+          const int j1 = walk.next(), j2 = walk.next();
+          const int j = grp == 0 ? j1 : j2;
+          has = j >= 0 && bit_of(mine, j);
+        }
         const uint32_t b = s_use & 1u;
         if (!(ok = wait_warp(bar(S_FULL + b), (s_use >> 1) & 1u, g))) break;
         fence_after();
-        uint32_t s[BT];
-        float cm[BT / 32];   // the maximum of each 32-column load (exact, as any order of max)
-#pragma unroll
-        for (int c = 0; c < BT / 32; ++c) cm[c] = tmem_ld32_max(t_row + kColS + b * 128u + c * 32u, s + 32 * c);
+        uint32_t sv[64];
+        float cm0 = tmem_ld32_max(t_row + kColS + b * 128u + (uint32_t)grp * 64u, sv);
+        float cm1 = tmem_ld32_max(t_row + kColS + b * 128u + (uint32_t)grp * 64u + 32u, sv + 32);
         wait_ld();
         fence_before();
         mbar_arrive(bar(S_FREE + b));
         ++s_use;
-        float mx = cm[0];
-#pragma unroll
-        for (int c = 1; c < BT / 32; ++c) mx = fmaxf(mx, cm[c]);
-        const float m_new = fmaxf(m, mx * sl2);
+        if (!has) cm0 = cm1 = -INFINITY;
+        const float m_new = fmaxf(m, fmaxf(cm0, cm1) * sl2);
         if (e == 0) {
           m = m_new;
         } else if (__any_sync(0xffffffffu, m_new > m + kRescaleThreshold)) {
-          // O must not change under the PV of block g-1 (g = global block index)
+          // O_grp must not change under the PV of block g-1
           const uint64_t gp = blocks_done + e - 1;
           if (!(ok = wait_warp(bar(PV_DONE + (uint32_t)(gp & 1u)), (uint32_t)((gp >> 1) & 1u), g))) break;
           fence_after();
           const float f = ex2f(m - m_new);
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(t_row + kColO + c * 32u, o);
+          for (int c = 0; c < 2; ++c) {
+            uint32_t ov[32];
+            const uint32_t a = t_row + kColO + (uint32_t)grp * 64u + c * 32u;
+            tmem_ld32(a, ov);
             wait_ld();
 #pragma unroll
-            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * f);
-            tmem_st32(t_row + kColO + c * 32u, o);
+            for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * f);
+            tmem_st32(a, ov);
           }
           wait_st();
           l *= f;
           m = m_new;
         }
-        uint32_t pk[BT / 2];
+        uint32_t pk[32];
         float rs[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) rs[u] = 0.f;
+        if (has) {
 #pragma unroll
-        for (int c = 0; c < BT / 2; ++c) {
-          const float p0 = ex2f(fmaf(__uint_as_float(s[2 * c]), sl2, -m));
-          const float p1 = ex2f(fmaf(__uint_as_float(s[2 * c + 1]), sl2, -m));
-          rs[c & 7] += p0 + p1;
-          pk[c] = pack2(p0, p1);
+          for (int c = 0; c < 32; ++c) {
+            const float p0 = ex2f(fmaf(__uint_as_float(sv[2 * c]), sl2, -m));
+            const float p1 = ex2f(fmaf(__uint_as_float(sv[2 * c + 1]), sl2, -m));
+            rs[c & 7] += p0 + p1;
+            pk[c] = pack2(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pk[c] = 0u;
         }
         l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
         // P buffer b was last read by the PV of block g-2
@@ -458,47 +625,228 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           if (!(ok = wait_warp(bar(PV_DONE + b), (uint32_t)(((gb - 2) >> 1) & 1u), g))) break;
           fence_after();
         }
-#pragma unroll
-        for (int c = 0; c < BT / 64; ++c) tmem_st32(t_row + kColP + b * 64u + 32u * c, pk + 32 * c);
+        tmem_st32(t_row + kColP + b * 64u + (uint32_t)grp * 32u, pk);
         wait_st();
         fence_before();
         mbar_arrive(bar(P_FULL + b));
       }
+      if (PAIR) release();
       if (!ok) break;
       blocks_done += (uint64_t)len;
-      if (!wait_warp(bar(O_FULL), o_items & 1u, g)) break;
-      ++o_items;
+      if (!(ok = wait_warp(bar(O_FULL), o_items & 1u, g))) break;
       fence_after();
-      const float inv = 1.0f / l;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(t_row + kColO + c * 32u, o);
-        wait_ld();
-        if (!stores) continue;
+      // combine the two groups' partial softmax sums: exchange (m, l) per row
+      const uint32_t par = o_items & 1u;
+      stat[(par * 2 + grp) * 128 + r] = make_float2(m, l);
+      mbar_arrive(bar(STAT));
+      if (!(ok = wait_warp(bar(STAT), par, g))) break;
+      const float2 st0 = stat[(par * 2 + 0) * 128 + r], st1 = stat[(par * 2 + 1) * 128 + r];
+      ++o_items;
+      const float M = fmaxf(st0.x, st1.x);
+      const float f0 = st0.y > 0.f ? ex2f(st0.x - M) : 0.f;
+      const float f1 = st1.y > 0.f ? ex2f(st1.x - M) : 0.f;
+      const float L = st0.y * f0 + st1.y * f1;
+      const float inv = L > 0.f ? 1.0f / L : 0.f;
+      const float a0 = f0 * inv, a1 = f1 * inv;
+      uint32_t oa[32], ob[32];
+      tmem_ld32(t_row + kColO + (uint32_t)grp * 32u, oa);
+      tmem_ld32(t_row + kColO + 64u + (uint32_t)grp * 32u, ob);
+      wait_ld();
+      fence_before();
+      mbar_arrive(bar(O_EMPTY));
+      if (stores) {
         uint32_t w[16];
 #pragma unroll
         for (int x = 0; x < 16; ++x)
-          w[x] = pack2(__uint_as_float(o[2 * x]) * inv, __uint_as_float(o[2 * x + 1]) * inv);
+          w[x] = pack2(fmaf(__uint_as_float(oa[2 * x]), a0, __uint_as_float(ob[2 * x]) * a1),
+                       fmaf(__uint_as_float(oa[2 * x + 1]), a0, __uint_as_float(ob[2 * x + 1]) * a1));
 #pragma unroll
-        for (int x = 0; x < 4; ++x) orow[c * 4 + x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+        for (int x = 0; x < 4; ++x) orow[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+        if (grp == 0) p.lse[row] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
       }
-      fence_before();
-      mbar_arrive(bar(O_EMPTY));
-      if (stores) p.lse[row] = (m + log2f(l)) * 0.69314718055994531f;
+    }
+    } else {
+    // ------------------------------------------------------------ softmax + epilogue
+      const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+      const uint32_t t_row = tmem + lane_base;
+      uint32_t it_use = 0, s_use = 0, o_items = 0;
+      uint64_t blocks_done = 0;
+      const float sl2 = p.scale_log2;
+      // with pairs, rows 0-63 are query block 2p and rows 64-127 block 2p + 1
+      const int half = PAIR ? (int)(threadIdx.x >> 6) : 0;
+      bool ok = true;
+      for (;;) {
+        const int ri = (int)(it_use % kNI);
+        if (!wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
+        const int64_t item = ring[ri].x;
+        const int len = ring[ri].y;
+        const int badbits = ring[ri].z;
+        __syncwarp();
+        // pairs read the item's bitmaps until the item ends; release the slot then
+        auto release = [&]() {
+          if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
+        };
+        if (!PAIR) release();
+        ++it_use;
+        if (len == -2) {
+          if (PAIR) release();
+          break;
+        }
+        if (len == -1) {
+          if (PAIR) release();
+          continue;
+        }
+        const int64_t bh = item / nbp;
+        const int i = PAIR ? 2 * (int)(item % nbp) + half : (int)(item % nb);   // this thread's query block
+        const int o = PAIR ? (int)(threadIdx.x & 63) : (int)threadIdx.x;       // its token in the block
+        const int64_t row = bh * p.N + (int64_t)i * BT + o;
+        // rows past the block (or past the last block of a pair) are computed, never stored
+        const bool stores = o < BT && i < nb && !((badbits >> half) & 1);
+        int64_t orow_idx = row;
+        if (p.raster && stores) {
+          // tile i = (bt, by, bx) block-raster; token o = (it, iy, ix) raster inside the tile
+          const int tbc = p.tb * p.tc;
+          const int bx = i % p.nX, by = (i / p.nX) % p.nY, bt = i / (p.nX * p.nY);
+          const int it = o / tbc, iy = (o - it * tbc) / p.tc, ix = o - it * tbc - iy * p.tc;
+          const int64_t n = ((int64_t)bt * p.ta + it) * p.Y * p.X + ((int64_t)by * p.tb + iy) * p.X +
+                            (int64_t)bx * p.tc + ix;
+          orow_idx = ((bh / p.H) * p.N + n) * p.H + bh % p.H;
+        }
+        uint4* orow = reinterpret_cast<uint4*>(p.o + orow_idx * D);
+        if (len == 0) {
+          if (stores) {
+  #pragma unroll
+            for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
+            p.lse[row] = -INFINITY;
+          }
+          if (PAIR) release();
+          continue;
+        }
+        const uint32_t* bmA = bits + ri * 2 * kMaxWords;
+        const uint32_t* mine = bmA + half * kMaxWords;
+        UnionWalk walk(bmA, bmA + kMaxWords, PAIR ? words : 0);
+        float m = -INFINITY, l = 0.f;
+        for (int e = 0; e < len; ++e) {
+          // which halves of this stage's 128 columns this row attends to (warp-uniform)
+          bool has1 = true, has2 = true;
+          if constexpr (PAIR) {
+            const int j1 = walk.next(), j2 = walk.next();
+            has1 = bit_of(mine, j1);
+            has2 = j2 >= 0 && bit_of(mine, j2);
+          }
+          const uint32_t b = s_use & 1u;
+          if (!(ok = wait_warp(bar(S_FULL + b), (s_use >> 1) & 1u, g))) break;
+          fence_after();
+          uint32_t s[C::KR];
+          float cm[C::KR / 32];   // the maximum of each 32-column load (exact, as any order of max)
+  #pragma unroll
+          for (int c = 0; c < C::KR / 32; ++c)
+            cm[c] = tmem_ld32_max(t_row + kColS + b * 128u + c * 32u, s + 32 * c);
+          wait_ld();
+          fence_before();
+          mbar_arrive(bar(S_FREE + b));
+          ++s_use;
+          if (!has1) cm[0] = cm[1] = -INFINITY;
+          if (!has2) cm[2] = cm[3] = -INFINITY;
+          float mx = cm[0];
+  #pragma unroll
+          for (int c = 1; c < C::KR / 32; ++c) mx = fmaxf(mx, cm[c]);
+          const float m_new = fmaxf(m, mx * sl2);
+          if (e == 0) {
+            m = m_new;
+          } else if (__any_sync(0xffffffffu, m_new > m + kRescaleThreshold)) {
+            // O must not change under the PV of block g-1 (g = global block index)
+            const uint64_t gp = blocks_done + e - 1;
+            if (!(ok = wait_warp(bar(PV_DONE + (uint32_t)(gp & 1u)), (uint32_t)((gp >> 1) & 1u), g))) break;
+            fence_after();
+            const float f = ex2f(m - m_new);
+  #pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t ov[32];
+              tmem_ld32(t_row + kColO + c * 32u, ov);
+              wait_ld();
+  #pragma unroll
+              for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * f);
+              tmem_st32(t_row + kColO + c * 32u, ov);
+            }
+            wait_st();
+            l *= f;
+            m = m_new;
+          }
+          uint32_t pk[C::KR / 2];
+          float rs[8];
+  #pragma unroll
+          for (int u = 0; u < 8; ++u) rs[u] = 0.f;
+  #pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            // columns [64*hh, 64*hh + 64): one key block of a pair (both halves of
+            // one block otherwise)
+            if (hh == 0 ? has1 : has2) {
+  #pragma unroll
+              for (int c = 32 * hh; c < 32 * hh + 32; ++c) {
+                const float p0 = ex2f(fmaf(__uint_as_float(s[2 * c]), sl2, -m));
+                const float p1 = ex2f(fmaf(__uint_as_float(s[2 * c + 1]), sl2, -m));
+                rs[c & 7] += p0 + p1;
+                pk[c] = pack2(p0, p1);
+              }
+            } else {
+  #pragma unroll
+              for (int c = 32 * hh; c < 32 * hh + 32; ++c) pk[c] = 0u;
+            }
+          }
+          l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+          // P buffer b was last read by the PV of block g-2
+          const uint64_t gb = blocks_done + e;
+          if (gb >= 2) {
+            if (!(ok = wait_warp(bar(PV_DONE + b), (uint32_t)(((gb - 2) >> 1) & 1u), g))) break;
+            fence_after();
+          }
+  #pragma unroll
+          for (int c = 0; c < C::KR / 64; ++c) tmem_st32(t_row + kColP + b * 64u + 32u * c, pk + 32 * c);
+          wait_st();
+          fence_before();
+          mbar_arrive(bar(P_FULL + b));
+        }
+        if (PAIR) release();
+        if (!ok) break;
+        blocks_done += (uint64_t)len;
+        if (!(ok = wait_warp(bar(O_FULL), o_items & 1u, g))) break;
+        ++o_items;
+        fence_after();
+        // a row that attended to no key (its block's own row is empty in a pair) has l = 0
+        const float inv = l > 0.f ? 1.0f / l : 0.f;
+  #pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(t_row + kColO + c * 32u, ov);
+          wait_ld();
+          if (!stores) continue;
+          uint32_t w[16];
+  #pragma unroll
+          for (int x = 0; x < 16; ++x)
+            w[x] = pack2(__uint_as_float(ov[2 * x]) * inv, __uint_as_float(ov[2 * x + 1]) * inv);
+  #pragma unroll
+          for (int x = 0; x < 4; ++x) orow[c * 4 + x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+        }
+        fence_before();
+        mbar_arrive(bar(O_EMPTY));
+        if (stores) p.lse[row] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      }
     }
   }
 
   fence_before();
   __syncthreads();
   fence_after();
-  if (warp == 5) tmem_dealloc(tmem, 512);
+  if (warp == C::W_S) tmem_dealloc(tmem, 512);
   if (p.prof != nullptr && threadIdx.x == 0)
     atomicAdd((unsigned long long*)&p.prof[smid() % SPARSP_PROF_SLOTS],
               (unsigned long long)(globaltimer_ns() - t_start));
 }
 
 }  // namespace
+
+int attn_fwd_tc_items_per_head(const Dims& s) { return s.Bt == 64 ? (s.nb + 1) / 2 : s.nb; }
 
 bool attn_fwd_tc_supported(const Dims& s) {
   if (s.dtype != SPARSP_BF16 || (s.Bt != 64 && s.Bt != 128) || (s.d != 64 && s.d != 128)) return false;
@@ -520,8 +868,8 @@ sparsp_status_t go_fwd(const Dims& s, const CUtensorMap& tq, const CUtensorMap& 
     return SPARSP_ERR_CUDA;
   const int sms = device_sm_count();
   if (sms <= 0) return SPARSP_ERR_CUDA;
-  const int64_t grid = cap_grid(s, sms, s.rows());
-  kern<<<(unsigned)grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, prm);
+  const int64_t grid = cap_grid(s, sms, prm.n_items);
+  kern<<<(unsigned)grid, C::THREADS, C::kSmemBytes, st>>>(tq, tk, tv, prm);
   SPARSP_LAUNCH_CHECK();
   return SPARSP_OK;
 }
@@ -540,7 +888,10 @@ sparsp_status_t launch_attn_fwd_tc(const Dims& s, const __nv_bfloat16* q, const 
       !make_tmap_bf16_rows(&tk, k, rows, (uint64_t)s.d, (uint32_t)s.Bt) ||
       !make_tmap_bf16_rows(&tv, v, rows, (uint64_t)s.d, (uint32_t)s.Bt))
     return SPARSP_ERR_CUDA;
-  Params prm{row_ptr, col_idx, s.N, s.nb, s.rows(), scale * 1.4426950408889634f, o, lse,
+  // 64-token blocks: items are pairs of query blocks, ordered by the caller
+  // over the pair rows (attn_fwd_tc_items)
+  const int nbp = attn_fwd_tc_items_per_head(s);
+  Params prm{row_ptr, col_idx, s.N, s.nb, nbp, (int64_t)s.B * s.H * nbp, scale * 1.4426950408889634f, o, lse,
              raster ? 1 : 0, s.H, s.Y, s.X, s.ta, s.tb, s.tc, s.nY, s.nX, items, counter, prof, d_status};
   if (s.Bt == 128 && s.d == 128) return go_fwd<128, 128>(s, tq, tk, tv, prm, st);
   if (s.Bt == 128 && s.d == 64) return go_fwd<128, 64>(s, tq, tk, tv, prm, st);

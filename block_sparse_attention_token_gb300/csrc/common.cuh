@@ -110,8 +110,12 @@ sparsp_status_t launch_predictor_fit(const Dims& s, int rank, const float* qm, c
                                      cudaStream_t st);
 
 size_t lpt_ws(const Dims& s);
+// cmax: the largest item cost the flat order distinguishes (0 = nb).
 sparsp_status_t launch_lpt(const Dims& s, const int32_t* row_ptr, bool flat, int32_t* items,
-                           int32_t* counter, void* ws, cudaStream_t st);
+                           int32_t* counter, void* ws, cudaStream_t st, int cmax = 0);
+// The CSR row offsets of the query-block pairs of 64-token blocks (pair p of
+// head bh = blocks 2p and 2p+1): pair_ptr [B*H*ceil(nb/2) + 1].
+sparsp_status_t launch_pair_ptr(const Dims& s, const int32_t* row_ptr, int32_t* pair_ptr, cudaStream_t st);
 
 // Exclusive scan in place of n+1 int32 entries: a[0..n) counts -> offsets,
 // a[n] = total. `base` (may be null) is added to every output.
@@ -133,6 +137,10 @@ sparsp_status_t launch_attn_fwd_mma(const Dims& s, const __nv_bfloat16* q, const
                                     float* lse, const int32_t* items, int32_t* counter,
                                     uint64_t* prof, int32_t* d_status, cudaStream_t st);
 bool attn_fwd_tc_supported(const Dims& s);
+// Work items per head of the tcgen05 forward kernel: nb, or ceil(nb/2) pairs of
+// query blocks with 64-token blocks. `items` must then order the pair items
+// (b*H + h)*ceil(nb/2) + p (launch_pair_ptr + launch_lpt over the pairs).
+int attn_fwd_tc_items_per_head(const Dims& s);
 sparsp_status_t launch_attn_fwd_tc(const Dims& s, const __nv_bfloat16* q, const __nv_bfloat16* k,
                                    const __nv_bfloat16* v, const int32_t* row_ptr,
                                    const int32_t* col_idx, float scale, __nv_bfloat16* o,

@@ -43,37 +43,39 @@ lpt_grouped_kernel(const int32_t* __restrict__ row_ptr, int BH, int nb, int32_t*
   if (bh == 0 && threadIdx.x == 0 && counter != nullptr) *counter = 0;
 }
 
-// Flat order, pass 1: per-head histogram of row costs (0..nb).
+constexpr int kMaxCost = 2048;   // item costs are clamped to [0, cmax], cmax <= kMaxCost
+
+// Flat order, pass 1: per-head histogram of item costs (0..cmax).
 __global__ void __launch_bounds__(kThreads)
-lpt_hist_kernel(const int32_t* __restrict__ row_ptr, int nb, int32_t* __restrict__ hist) {
-  __shared__ int32_t h[1025];
+lpt_hist_kernel(const int32_t* __restrict__ row_ptr, int nb, int cmax, int32_t* __restrict__ hist) {
+  __shared__ int32_t h[kMaxCost + 1];
   const int bh = blockIdx.x;
-  for (int c = threadIdx.x; c <= nb; c += blockDim.x) h[c] = 0;
+  for (int c = threadIdx.x; c <= cmax; c += blockDim.x) h[c] = 0;
   __syncthreads();
   const int64_t r0 = (int64_t)bh * nb;
   for (int i = threadIdx.x; i < nb; i += blockDim.x) {
     int32_t c = row_ptr[r0 + i + 1] - row_ptr[r0 + i];
-    c = c < 0 ? 0 : (c > nb ? nb : c);
+    c = c < 0 ? 0 : (c > cmax ? cmax : c);
     atomicAdd(&h[c], 1);
   }
   __syncthreads();
-  for (int c = threadIdx.x; c <= nb; c += blockDim.x) hist[(int64_t)bh * (nb + 1) + c] = h[c];
+  for (int c = threadIdx.x; c <= cmax; c += blockDim.x) hist[(int64_t)bh * (cmax + 1) + c] = h[c];
 }
 
 // Flat order, pass 2: slot = #items with larger cost + #items of equal cost in
 // earlier heads + #rows of equal cost earlier in this head.
 __global__ void __launch_bounds__(kThreads)
 lpt_place_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ hist, int BH,
-                 int nb, int32_t* __restrict__ items, int32_t* __restrict__ counter) {
-  __shared__ int32_t greater[1026];
-  __shared__ int32_t before[1025];
+                 int nb, int cmax, int32_t* __restrict__ items, int32_t* __restrict__ counter) {
+  __shared__ int32_t greater[kMaxCost + 2];
+  __shared__ int32_t before[kMaxCost + 1];
   __shared__ int32_t cost[1024];
   const int bh = blockIdx.x;
   const int64_t r0 = (int64_t)bh * nb;
-  for (int c = threadIdx.x; c <= nb; c += blockDim.x) {
+  for (int c = threadIdx.x; c <= cmax; c += blockDim.x) {
     int32_t tot = 0, bef = 0;
     for (int g = 0; g < BH; ++g) {
-      const int32_t v = hist[(int64_t)g * (nb + 1) + c];
+      const int32_t v = hist[(int64_t)g * (cmax + 1) + c];
       tot += v;
       if (g < bh) bef += v;
     }
@@ -82,12 +84,12 @@ lpt_place_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict_
   }
   for (int i = threadIdx.x; i < nb; i += blockDim.x) {
     int32_t c = row_ptr[r0 + i + 1] - row_ptr[r0 + i];
-    cost[i] = c < 0 ? 0 : (c > nb ? nb : c);
+    cost[i] = c < 0 ? 0 : (c > cmax ? cmax : c);
   }
   __syncthreads();
   if (threadIdx.x == 0) {   // suffix sums: greater[c] = #items with cost > c
     int32_t run = 0;
-    for (int c = nb; c >= 0; --c) {
+    for (int c = cmax; c >= 0; --c) {
       const int32_t t = greater[c];
       greater[c] = run;
       run += t;
@@ -167,21 +169,51 @@ csr_transpose_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restr
 
 }  // namespace
 
-size_t lpt_ws(const Dims& s) { return (size_t)s.B * s.H * (s.nb + 1) * sizeof(int32_t); }
+// Histogram space for costs up to 2*nb (the pair items of 64-token blocks cost
+// the sum of two rows).
+size_t lpt_ws(const Dims& s) { return (size_t)s.B * s.H * (2 * s.nb + 1) * sizeof(int32_t); }
 
 sparsp_status_t launch_lpt(const Dims& s, const int32_t* row_ptr, bool flat, int32_t* items,
-                           int32_t* counter, void* ws, cudaStream_t st) {
+                           int32_t* counter, void* ws, cudaStream_t st, int cmax) {
   const int BH = s.B * s.H;
+  if (cmax <= 0) cmax = s.nb;
+  if (cmax > kMaxCost) return SPARSP_ERR_UNSUPPORTED;
   if (!flat) {
     lpt_grouped_kernel<<<BH, kThreads, 0, st>>>(row_ptr, BH, s.nb, items, counter);
     SPARSP_LAUNCH_CHECK();
   } else {
     int32_t* hist = (int32_t*)ws;
-    lpt_hist_kernel<<<BH, kThreads, 0, st>>>(row_ptr, s.nb, hist);
+    lpt_hist_kernel<<<BH, kThreads, 0, st>>>(row_ptr, s.nb, cmax, hist);
     SPARSP_LAUNCH_CHECK();
-    lpt_place_kernel<<<BH, kThreads, 0, st>>>(row_ptr, hist, BH, s.nb, items, counter);
+    lpt_place_kernel<<<BH, kThreads, 0, st>>>(row_ptr, hist, BH, s.nb, cmax, items, counter);
     SPARSP_LAUNCH_CHECK();
   }
+  return SPARSP_OK;
+}
+
+namespace {
+
+// Pair rows of 64-token blocks: pair p of head bh covers query blocks 2p and
+// 2p + 1 (2p alone when nb is odd and 2p = nb - 1), so its "row" in a CSR of
+// B*H*ceil(nb/2) rows starts where row 2p starts.
+__global__ void pair_ptr_kernel(const int32_t* __restrict__ row_ptr, int64_t BH, int nb, int nbp,
+                                int32_t* __restrict__ pair_ptr) {
+  const int64_t n = BH * nbp;
+  for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x <= n; x += (int64_t)gridDim.x * blockDim.x)
+    pair_ptr[x] = x == n ? row_ptr[BH * nb] : row_ptr[(x / nbp) * nb + 2 * (x % nbp)];
+}
+
+}  // namespace
+
+sparsp_status_t launch_pair_ptr(const Dims& s, const int32_t* row_ptr, int32_t* pair_ptr, cudaStream_t st) {
+  const int64_t BH = (int64_t)s.B * s.H;
+  const int nbp = (s.nb + 1) / 2;
+  const int64_t n = BH * nbp + 1;
+  const int threads = 256;
+  int64_t blocks = (n + threads - 1) / threads;
+  if (blocks > 4096) blocks = 4096;
+  pair_ptr_kernel<<<(unsigned)blocks, threads, 0, st>>>(row_ptr, BH, s.nb, nbp, pair_ptr);
+  SPARSP_LAUNCH_CHECK();
   return SPARSP_OK;
 }
 

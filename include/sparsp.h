@@ -386,10 +386,15 @@ SPARSP_API sparsp_status_t sparsp_lpt_schedule(const sparsp_shape_t* shape, cons
  * q, k, v, o: blocked [B,H,N,d] (o raster [B,N,H,d] with SPARSP_OUT_RASTER);
  * lse: float32 [B,H,N]. scale <= 0 means
  * 1/sqrt(d). An empty row gives O = 0, LSE = -inf. A row with an index outside
- * [0, nb) or more than nb entries sets SPARSP_ERR_DATA and is skipped.
- * bf16 on sm_103a runs the tcgen05/TMEM/TMA kernel (Bt and d in {64, 128});
- * with SPARSP_KERNEL_PORTABLE an mma.sync kernel; float32 runs an fp32 FFMA
- * kernel. Work items are pulled longest-first by persistent CTAs.
+ * [0, nb) or more than nb entries sets SPARSP_ERR_DATA and is skipped. Rows
+ * must list distinct blocks (sparsp_select writes them ascending); the
+ * 64-token-block tcgen05 kernel also reports a repeated index as
+ * SPARSP_ERR_DATA and skips that row, the other kernels do not check.
+ * bf16 on sm_103a runs the tcgen05/TMEM/TMA kernel (Bt and d in {64, 128};
+ * with 64-token blocks each work item is a pair of neighbouring query blocks
+ * over the union of their rows, so that every MMA has 128 query rows and 128
+ * key columns); with SPARSP_KERNEL_PORTABLE an mma.sync kernel; float32 runs
+ * an fp32 FFMA kernel. Work items are pulled longest-first by persistent CTAs.
  * prof: NULL or uint64 [SPARSP_PROF_SLOTS], caller-zeroed; receives per-SM busy
  * nanoseconds (index = SM id).
  * ws: at least sparsp_attn_workspace_size(shape, 0) bytes.

@@ -91,7 +91,7 @@ def test_workspace_sizes(lib):
     assert lib.sparsp_select_workspace_size(ctypes.byref(s)) == rows * 8
     assert lib.sparsp_block_scores_workspace_size(ctypes.byref(s), sp.EST_MEAN, 16) == 2 * rows * s.d * 4
     assert lib.sparsp_block_scores_workspace_size(ctypes.byref(s), sp.EST_LOWRANK, 16) == 2 * rows * 16 * 4
-    assert lib.sparsp_lpt_workspace_size(ctypes.byref(s)) == s.B * s.H * (s.nb + 1) * 4
+    assert lib.sparsp_lpt_workspace_size(ctypes.byref(s)) == s.B * s.H * (2 * s.nb + 1) * 4
     fwd = lib.sparsp_attn_workspace_size(ctypes.byref(s), 0)
     bwd = lib.sparsp_attn_workspace_size(ctypes.byref(s), 1)
     assert fwd >= rows * 4 + 16 and bwd > fwd + s.B * s.H * s.N * 4

@@ -30,8 +30,11 @@ SMALL = {
     "f32big": W("f32-1k-d128", 1, 3, 128, 4, 8, 32, 2, 8, 8, "f32", "mean", 0.9, 1, 2, 1, False, False, 34),
     # 640 items: more than one wave of persistent CTAs with a ragged tail; low-rank scores
     "wave": W("wave-4k-lowrank-bf16", 1, 20, 128, 4, 32, 32, 2, 8, 8, "bf16", "lowrank", 0.0, 6, 4, 4, False, True, 35),
+    # Bt = 64, d = 64 with an odd number of blocks (3 x 1 x 3 = 9): the last query
+    # block of every head has no partner in the paired tcgen05 forward
+    "r64odd": W("ragged-odd-576-bf16", 2, 3, 64, 6, 4, 24, 2, 4, 8, "bf16", "mean", 0.6, 2, 3, 2, False, True, 36),
 }
-BWD = ["medium", "r128", "r64", "r128d64", "wave"]
+BWD = ["medium", "r128", "r64", "r128d64", "wave", "r64odd"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -672,6 +675,64 @@ def test_attn_fwd_empty_and_bad_rows(name, portable):
     for (b, h, i) in rows_ok:
         sl = slice(i * Bt, (i + 1) * Bt)
         compare_values(O[b, h, sl], Oref[b, h, sl], wl, "O")
+
+
+@pytest.mark.parametrize("name,seed", [("r64odd", 0), ("r64", 1), ("medium", 2)])
+def test_attn_fwd_pairs_with_unrelated_rows(name, seed):
+    """64-token blocks run as pairs of neighbouring query blocks over the union
+    of their two rows. Random rows of random lengths (some empty, some with
+    every block, most sharing few blocks with their neighbour) exercise every
+    mask: O and LSE match the oracle, empty rows give O = 0 and LSE = -inf."""
+    wl, data, shape = _setup(name)
+    g = orc.grid_of(wl)
+    rng = np.random.default_rng(500 + seed)
+    rows = []
+    for r in range(g.B * g.H * g.nb):
+        kind = rng.integers(0, 6)
+        n = 0 if kind == 0 else (g.nb if kind == 1 else int(rng.integers(1, g.nb + 1)))
+        rows.append(np.sort(rng.choice(g.nb, size=n, replace=False)))
+    rp = np.concatenate([[0], np.cumsum([len(x) for x in rows])]).astype(np.int32)
+    ci = np.concatenate(rows).astype(np.int32)
+    qb, kb, vb = (orc.reorder(data[x], g) for x in ("q", "k", "v"))
+    st = status_word()
+    o, lse = sp.attn_fwd(shape, dev(qb, wl), dev(kb, wl), dev(vb, wl), i32(rp), i32(ci), status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    O, L = orc.attn_fwd(qb, kb, vb, rp, ci, g.Bt, 1.0 / math.sqrt(g.d))
+    on, ln = host(o), host(lse)
+    empty = [r for r in range(len(rows)) if len(rows[r]) == 0]
+    assert empty, "the seed must give some empty rows"
+    for r in empty:
+        b, h, i = r // (g.H * g.nb), (r // g.nb) % g.H, r % g.nb
+        sl = slice(i * g.Bt, (i + 1) * g.Bt)
+        assert (on[b, h, sl] == 0).all() and np.isneginf(ln[b, h, sl]).all()
+        O[b, h, sl] = 0.0
+        L[b, h, sl] = 0.0
+        ln[b, h, sl] = 0.0
+    compare_values(on, O, wl, "O")
+    compare_values(ln, L, wl, "LSE")
+
+
+def test_attn_fwd_pair_rejects_a_repeated_index():
+    """A row listing a key block twice is reported (SPARSP_ERR_DATA) by the
+    paired 64-token kernel and skipped; its partner row is still computed."""
+    wl, data, shape = _setup("r64odd")
+    ch = OracleChain(wl, data)
+    g = ch.g
+    rows = [ch.sel.col_idx[ch.sel.row_ptr[r]:ch.sel.row_ptr[r + 1]].copy() for r in range(g.B * g.H * g.nb)]
+    rows[2] = np.concatenate([rows[2], rows[2][:1]])            # row 2 repeats its first block
+    rp = np.concatenate([[0], np.cumsum([len(x) for x in rows])]).astype(np.int32)
+    ci = np.concatenate(rows).astype(np.int32)
+    st = status_word()
+    o = torch.full((g.B, g.H, g.N, g.d), 7.0, dtype=shape.torch_dtype, device="cuda")
+    lse = torch.full((g.B, g.H, g.N), 7.0, device="cuda")
+    sp.attn_fwd(shape, dev(ch.qb, wl), dev(ch.kb, wl), dev(ch.vb, wl), i32(rp), i32(ci), o=o, lse=lse, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == sp.DATA
+    on = host(o)
+    assert (on[0, 0, 2 * g.Bt:3 * g.Bt] == 7.0).all()
+    O, _ = orc.attn_fwd(ch.qb, ch.kb, ch.vb, ch.sel.row_ptr, ch.sel.col_idx, g.Bt, ch.scale, rows=[(0, 0, 3)])
+    compare_values(on[0, 0, 3 * g.Bt:4 * g.Bt], O[0, 0, 3 * g.Bt:4 * g.Bt], wl, "O of the partner row")
 
 
 @pytest.mark.parametrize("name", BWD)
