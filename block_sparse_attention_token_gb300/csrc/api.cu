@@ -11,7 +11,7 @@ namespace {
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Validates the shape and fills Dims. Accepts d in {64,128}, Bt in {64,128},
-// nb <= 1024, B*H <= 65535.
+// nb <= kMaxBlocks, B*H <= 65535.
 sparsp_status_t check_shape(const sparsp_shape_t* sh, Dims* s) {
   if (sh == nullptr) return SPARSP_ERR_INVALID_ARG;
   if (sh->B <= 0 || sh->H <= 0 || sh->T <= 0 || sh->Y <= 0 || sh->X <= 0 || sh->d <= 0 ||
@@ -24,7 +24,7 @@ sparsp_status_t check_shape(const sparsp_shape_t* sh, Dims* s) {
   if (Bt != 64 && Bt != 128) return SPARSP_ERR_UNSUPPORTED;
   const int64_t nT = sh->T / sh->ta, nY = sh->Y / sh->tb, nX = sh->X / sh->tc;
   const int64_t nb = nT * nY * nX;
-  if (nb > 1024) return SPARSP_ERR_UNSUPPORTED;
+  if (nb > kMaxBlocks) return SPARSP_ERR_UNSUPPORTED;
   if ((int64_t)sh->B * sh->H > 65535) return SPARSP_ERR_UNSUPPORTED;
   // int32 CSR offsets must hold B*H*nb*nb entries
   if ((int64_t)sh->B * sh->H * nb * nb > INT32_MAX) return SPARSP_ERR_UNSUPPORTED;
@@ -260,7 +260,7 @@ sparsp_status_t sparsp_kv_demand(const sparsp_shape_t* shape, int32_t P, const i
   sparsp_status_t r = check_shape(shape, &s);
   if (r != SPARSP_OK) return r;
   if (P < 1 || P > s.nb) return SPARSP_ERR_SHAPE;
-  if ((int64_t)s.B * s.H * P > INT32_MAX / 1024) return SPARSP_ERR_UNSUPPORTED;
+  if ((int64_t)s.B * s.H * P * s.nb > INT32_MAX) return SPARSP_ERR_UNSUPPORTED;   // int32 list offsets
   CHECK_PTR(row_ptr);
   CHECK_PTR(col_idx);
   CHECK_OPT_PTR(owner);
@@ -288,7 +288,7 @@ sparsp_status_t sparsp_kv_gather(const sparsp_shape_t* shape, int32_t P, const i
   sparsp_status_t r = check_shape(shape, &s);
   if (r != SPARSP_OK) return r;
   if (P < 1 || P > s.nb) return SPARSP_ERR_SHAPE;
-  if ((int64_t)s.B * s.H * P > INT32_MAX / 1024) return SPARSP_ERR_UNSUPPORTED;
+  if ((int64_t)s.B * s.H * P * s.nb > INT32_MAX) return SPARSP_ERR_UNSUPPORTED;   // int32 list offsets
   CHECK_PTR(dem_ptr);
   CHECK_PTR(dem_idx);
   CHECK_PTR(k);
@@ -303,7 +303,7 @@ sparsp_status_t sparsp_kv_gather(const sparsp_shape_t* shape, int32_t P, const i
 
 size_t sparsp_placement_workspace_size(const sparsp_shape_t* shape) {
   Dims s;
-  if (check_shape(shape, &s) != SPARSP_OK) return 0;
+  if (check_shape(shape, &s) != SPARSP_OK || s.nb > kMaxBlocksNext) return 0;
   return placement_ws(s);
 }
 
@@ -313,6 +313,7 @@ sparsp_status_t sparsp_placement(const sparsp_shape_t* shape, int32_t P, const i
   Dims s;
   sparsp_status_t r = check_shape(shape, &s);
   if (r != SPARSP_OK) return r;
+  if (s.nb > kMaxBlocksNext) return SPARSP_ERR_UNSUPPORTED;
   if (P < 1 || P > s.nb) return SPARSP_ERR_SHAPE;
   CHECK_PTR(row_ptr);
   CHECK_PTR(col_idx);
@@ -341,7 +342,7 @@ sparsp_status_t sparsp_balance_heads(const sparsp_shape_t* shape, int32_t P, int
 
 size_t sparsp_augment_workspace_size(const sparsp_shape_t* shape, int32_t P) {
   Dims s;
-  if (check_shape(shape, &s) != SPARSP_OK || P < 1) return 0;
+  if (check_shape(shape, &s) != SPARSP_OK || P < 1 || s.nb > kMaxBlocksNext) return 0;
   return augment_ws(s, P);
 }
 
@@ -352,7 +353,7 @@ sparsp_status_t sparsp_augment(const sparsp_shape_t* shape, int32_t P, const flo
   Dims s;
   sparsp_status_t r = check_shape(shape, &s);
   if (r != SPARSP_OK) return r;
-  if (s.H > kBalanceMaxHeads) return SPARSP_ERR_UNSUPPORTED;
+  if (s.H > kBalanceMaxHeads || s.nb > kMaxBlocksNext) return SPARSP_ERR_UNSUPPORTED;
   if (P < 1 || P > s.H) return SPARSP_ERR_SHAPE;
   if (col_cap < 0) return SPARSP_ERR_INVALID_ARG;
   CHECK_PTR(scores);

@@ -68,7 +68,6 @@ enum Bar {
 // (PAIR). Tiles are TMA'd as 64-column boxes of 128-byte rows with 128-byte
 // swizzle; a stage of two blocks is two 64-row boxes per column box, the
 // second 64 rows (8 KB, a whole number of 1 KB swizzle atoms) after the first.
-constexpr int kMaxWords = 32;   // bitmap words of one CSR row (nb <= 1024)
 template <int BT_, int D_>
 struct Cfg {
   static constexpr int BT = BT_, D = D_, QR = 128, KR = 128;
@@ -85,13 +84,17 @@ struct Cfg {
   // tiles are half the size and 6 stages keep more L2 loads in flight (a stage
   // then takes half the tensor time, so the same latency needs twice the depth)
   static constexpr int NK = D == 64 ? 6 : 3, NV = NK;
+  // bitmap words of one CSR row in the item ring (pairs): up to kMaxBlocks
+  // blocks, except for d = 128 whose tiles leave room for 1,024 blocks only
+  // (larger shapes run the portable kernel, see attn_fwd_tc_supported)
+  static constexpr int MAXW = D == 64 ? kMaxBlocks / 32 : 32;
   static constexpr int NBOX = D / 64;                     // 64-column boxes per row tile
   static constexpr uint32_t kQBox = QR * 128, kKBox = KR * 128, kHalfBox = 64 * 128;
   static constexpr uint32_t kQTile = kQBox * NBOX, kKTile = kKBox * NBOX;
   static constexpr uint32_t kOffK = kQTile, kOffV = kOffK + NK * kKTile, kOffBar = kOffV + NV * kKTile;
   static constexpr uint32_t kOffRing = kOffBar + 8 * NBAR;
   static constexpr uint32_t kOffBits = kOffRing + 16 * kNI;
-  static constexpr uint32_t kBitsBytes = PAIR ? kNI * 2 * kMaxWords * 4 : 0;
+  static constexpr uint32_t kBitsBytes = PAIR ? kNI * 2 * MAXW * 4 : 0;
   static constexpr uint32_t kOffStat = kOffBits + kBitsBytes;   // [2 parities][2 groups][128 rows] (m, l)
   static constexpr uint32_t kStatBytes = SPLIT ? 2 * 2 * 128 * 8 : 0;
   static constexpr uint32_t kOffMisc = kOffStat + kStatBytes;
@@ -220,7 +223,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   auto bar = [&](int idx) -> uint32_t { return base + C::kOffBar + 8u * (uint32_t)idx; };
   // ring entry: x = item, y = stages (-1: skip, -2: end), z = bad-row bits (pairs)
   volatile int4* ring = reinterpret_cast<volatile int4*>(gbase + C::kOffRing);
-  uint32_t* bits = reinterpret_cast<uint32_t*>(gbase + C::kOffBits);   // [kNI][2][kMaxWords] (pairs)
+  uint32_t* bits = reinterpret_cast<uint32_t*>(gbase + C::kOffBits);   // [kNI][2][C::MAXW] (pairs)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + C::kOffMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -282,8 +285,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       slot = __shfl_sync(0xffffffffu, slot, 0);
       const int ri = (int)(it_fill % kNI);
       if (!wait_warp(bar(I_EMPTY + ri), ((it_fill / kNI) & 1u) ^ 1u, g)) break;
-      uint32_t* bmA = bits + ri * 2 * kMaxWords;
-      uint32_t* bmB = bmA + kMaxWords;
+      uint32_t* bmA = bits + ri * 2 * C::MAXW;
+      uint32_t* bmB = bmA + C::MAXW;
       int32_t item = -1, len = -2, badbits = 0;
       if (slot < p.n_items) {
         item = p.items[slot];
@@ -291,7 +294,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           // the two rows as bitmaps in the ring slot; a bad row counts as empty
           const int64_t bh = item / nbp;
           const int iA = 2 * (item % nbp);
-          for (int w = lane; w < 2 * kMaxWords; w += 32) bmA[w] = 0u;
+          for (int w = lane; w < 2 * C::MAXW; w += 32) bmA[w] = 0u;
           __syncwarp();
           const bool okA = row_bitmap(p, bh * nb + iA, bmA, words, lane);
           const bool okB = iA + 1 < nb ? row_bitmap(p, bh * nb + iA + 1, bmB, words, lane) : true;
@@ -556,9 +559,9 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         if (PAIR) release();
         continue;
       }
-      const uint32_t* bmA = bits + ri * 2 * kMaxWords;
-      const uint32_t* mine = bmA + half * kMaxWords;
-      UnionWalk walk(bmA, bmA + kMaxWords, PAIR ? words : 0);
+      const uint32_t* bmA = bits + ri * 2 * C::MAXW;
+      const uint32_t* mine = bmA + half * C::MAXW;
+      UnionWalk walk(bmA, bmA + C::MAXW, PAIR ? words : 0);
       float m = -INFINITY, l = 0.f;
       for (int e = 0; e < len; ++e) {
         // does this row attend to this group's key block of the stage (warp-uniform)
@@ -722,9 +725,9 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           if (PAIR) release();
           continue;
         }
-        const uint32_t* bmA = bits + ri * 2 * kMaxWords;
-        const uint32_t* mine = bmA + half * kMaxWords;
-        UnionWalk walk(bmA, bmA + kMaxWords, PAIR ? words : 0);
+        const uint32_t* bmA = bits + ri * 2 * C::MAXW;
+        const uint32_t* mine = bmA + half * C::MAXW;
+        UnionWalk walk(bmA, bmA + C::MAXW, PAIR ? words : 0);
         float m = -INFINITY, l = 0.f;
         for (int e = 0; e < len; ++e) {
           // which halves of this stage's 128 columns this row attends to (warp-uniform)
@@ -850,6 +853,7 @@ int attn_fwd_tc_items_per_head(const Dims& s) { return s.Bt == 64 ? (s.nb + 1) /
 
 bool attn_fwd_tc_supported(const Dims& s) {
   if (s.dtype != SPARSP_BF16 || (s.Bt != 64 && s.Bt != 128) || (s.d != 64 && s.d != 128)) return false;
+  if (s.Bt == 64 && s.nb > 32 * (s.d == 64 ? Cfg<64, 64>::MAXW : Cfg<64, 128>::MAXW)) return false;
   if ((int64_t)s.B * s.H * s.N >= (int64_t)1 << 31) return false;
   int dev = 0, major = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;

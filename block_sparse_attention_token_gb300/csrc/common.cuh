@@ -9,6 +9,13 @@
 
 namespace sparsp {
 
+// Largest number of blocks per (b, h) sequence: 4,096 (524,288 tokens in
+// 128-token blocks). Dependency-aware placement and slack-aware augmentation
+// keep shared-memory tables of one entry per block and take at most
+// kMaxBlocksNext.
+constexpr int kMaxBlocks = 4096;
+constexpr int kMaxBlocksNext = 1024;
+
 // Derived shape, validated by the API layer before any launcher sees it.
 struct Dims {
   int B, H, T, Y, X, d, ta, tb, tc, dtype;

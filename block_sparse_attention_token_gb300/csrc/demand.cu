@@ -21,7 +21,7 @@
 namespace sparsp {
 namespace {
 
-constexpr int kMaxWords = 32;   // nb <= 1024
+constexpr int kMaxWords = kMaxBlocks / 32;   // bitmap words of nb <= kMaxBlocks blocks
 
 __device__ __forceinline__ void or_row(const int32_t* __restrict__ col_idx, int32_t e0, int32_t e1,
                                        int step, int first, int nb, uint32_t* bits, int32_t* d_status) {
@@ -44,9 +44,9 @@ bitmap_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ c
   const int part = blockIdx.x;           // (b*H + h)*P + r
   const int bh = part / P, r = part % P;
   const int W = (nb + 31) / 32;
-  if (threadIdx.x < kMaxWords) {
-    bits[threadIdx.x] = 0u;
-    mine[threadIdx.x] = 0u;
+  for (int w = threadIdx.x; w < kMaxWords; w += blockDim.x) {
+    bits[w] = 0u;
+    mine[w] = 0u;
   }
   __syncthreads();
   if (owner == nullptr) {
@@ -81,11 +81,15 @@ bitmap_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ c
   }
   __syncthreads();
   if (threadIdx.x < 32) {
+    int total = 0, remote = 0, owned = 0;
+    for (int w = threadIdx.x; w < W; w += 32) {
+      const uint32_t word = bits[w], own = mine[w];
+      bitmap[(int64_t)part * W + w] = word;
+      total += __popc(word);
+      remote += __popc(word & ~own);
+      owned += __popc(own);
+    }
     const int w = threadIdx.x;
-    const uint32_t word = w < W ? bits[w] : 0u;
-    const uint32_t own = w < W ? mine[w] : 0u;
-    if (w < W) bitmap[(int64_t)part * W + w] = word;
-    int total = __popc(word), remote = __popc(word & ~own), owned = __popc(own);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       total += __shfl_xor_sync(0xffffffffu, total, off);
@@ -108,8 +112,11 @@ list_kernel(const uint32_t* __restrict__ bitmap, const int32_t* __restrict__ dem
   const int lane = threadIdx.x & 31;
   const int part = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (part >= nparts) return;
-  uint32_t word = lane < W ? bitmap[(int64_t)part * W + lane] : 0u;
-  int cnt = __popc(word);
+  // lane l takes words [l*per, l*per + per): the set bits come out ascending
+  const int per = (W + 31) / 32, w0 = lane * per, w1 = min(W, w0 + per);
+  const uint32_t* bm = bitmap + (int64_t)part * W;
+  int cnt = 0;
+  for (int w = w0; w < w1; ++w) cnt += __popc(bm[w]);
   int incl = cnt;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -117,10 +124,13 @@ list_kernel(const uint32_t* __restrict__ bitmap, const int32_t* __restrict__ dem
     if (lane >= off) incl += o;
   }
   int pos = dem_ptr[part] + incl - cnt;
-  while (word) {
-    const int bit = __ffs(word) - 1;
-    dem_idx[pos++] = lane * 32 + bit;
-    word &= word - 1;
+  for (int w = w0; w < w1; ++w) {
+    uint32_t word = bm[w];
+    while (word) {
+      const int bit = __ffs(word) - 1;
+      dem_idx[pos++] = w * 32 + bit;
+      word &= word - 1;
+    }
   }
 }
 

@@ -15,7 +15,7 @@ constexpr int kThreads = 1024;
 __global__ void __launch_bounds__(kThreads)
 lpt_grouped_kernel(const int32_t* __restrict__ row_ptr, int BH, int nb, int32_t* __restrict__ items,
                    int32_t* __restrict__ counter) {
-  __shared__ int32_t cost[1024];
+  __shared__ int32_t cost[kMaxBlocks];
   __shared__ int32_t head_rank;
   const int bh = blockIdx.x;
   if (threadIdx.x == 0) head_rank = 0;
@@ -43,7 +43,7 @@ lpt_grouped_kernel(const int32_t* __restrict__ row_ptr, int BH, int nb, int32_t*
   if (bh == 0 && threadIdx.x == 0 && counter != nullptr) *counter = 0;
 }
 
-constexpr int kMaxCost = 2048;   // item costs are clamped to [0, cmax], cmax <= kMaxCost
+constexpr int kMaxCost = kMaxBlocks;   // item costs are clamped to [0, cmax], cmax <= kMaxCost
 
 // Flat order, pass 1: per-head histogram of item costs (0..cmax).
 __global__ void __launch_bounds__(kThreads)
@@ -69,7 +69,7 @@ lpt_place_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict_
                  int nb, int cmax, int32_t* __restrict__ items, int32_t* __restrict__ counter) {
   __shared__ int32_t greater[kMaxCost + 2];
   __shared__ int32_t before[kMaxCost + 1];
-  __shared__ int32_t cost[1024];
+  __shared__ int16_t cost[kMaxBlocks];   // clamped to [0, cmax], cmax <= kMaxCost
   const int bh = blockIdx.x;
   const int64_t r0 = (int64_t)bh * nb;
   for (int c = threadIdx.x; c <= cmax; c += blockDim.x) {
@@ -84,7 +84,7 @@ lpt_place_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict_
   }
   for (int i = threadIdx.x; i < nb; i += blockDim.x) {
     int32_t c = row_ptr[r0 + i + 1] - row_ptr[r0 + i];
-    cost[i] = c < 0 ? 0 : (c > cmax ? cmax : c);
+    cost[i] = (int16_t)(c < 0 ? 0 : (c > cmax ? cmax : c));
   }
   __syncthreads();
   if (threadIdx.x == 0) {   // suffix sums: greater[c] = #items with cost > c
@@ -111,8 +111,8 @@ __global__ void __launch_bounds__(kThreads)
 csr_transpose_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ col_idx,
                      int BH, int nb, int32_t* __restrict__ col_ptr, int32_t* __restrict__ row_idx,
                      int32_t* d_status) {
-  __shared__ int32_t cnt[1024];
-  __shared__ int32_t cursor[1024];
+  __shared__ int32_t cnt[kMaxBlocks];
+  __shared__ int32_t cursor[kMaxBlocks];
   __shared__ int32_t warp_tot[32];
   const int bh = blockIdx.x;
   const int64_t r0 = (int64_t)bh * nb;
@@ -125,10 +125,14 @@ csr_transpose_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restr
     else report(d_status, SPARSP_ERR_DATA);
   }
   __syncthreads();
-  // exclusive scan of cnt[0..nb) (nb <= 1024 = blockDim)
+  // exclusive scan of cnt[0..nb): thread t takes the kPer entries from kPer*t
+  // (nb <= kMaxBlocks = kPer * blockDim)
+  constexpr int kPer = kMaxBlocks / kThreads;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int j = threadIdx.x;
-  const int32_t v = j < nb ? cnt[j] : 0;
+  const int j0 = threadIdx.x * kPer;
+  int32_t v = 0;
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) v += j0 + u < nb ? cnt[j0 + u] : 0;
   int32_t incl = v;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -147,10 +151,15 @@ csr_transpose_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restr
     warp_tot[lane] = t;
   }
   __syncthreads();
-  const int32_t excl = (warp > 0 ? warp_tot[warp - 1] : 0) + incl - v;
-  if (j < nb) {
-    col_ptr[r0 + j] = e0 + excl;
-    cursor[j] = e0 + excl;
+  int32_t excl = (warp > 0 ? warp_tot[warp - 1] : 0) + incl - v;
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int j = j0 + u;
+    if (j < nb) {
+      col_ptr[r0 + j] = e0 + excl;
+      cursor[j] = e0 + excl;
+      excl += cnt[j];
+    }
   }
   if (bh == BH - 1 && threadIdx.x == 0) col_ptr[(int64_t)BH * nb] = row_ptr[(int64_t)BH * nb];
   __syncthreads();
@@ -177,7 +186,7 @@ sparsp_status_t launch_lpt(const Dims& s, const int32_t* row_ptr, bool flat, int
                            int32_t* counter, void* ws, cudaStream_t st, int cmax) {
   const int BH = s.B * s.H;
   if (cmax <= 0) cmax = s.nb;
-  if (cmax > kMaxCost) return SPARSP_ERR_UNSUPPORTED;
+  if (cmax > kMaxCost) cmax = kMaxCost;   // the flat order then ties the costliest items
   if (!flat) {
     lpt_grouped_kernel<<<BH, kThreads, 0, st>>>(row_ptr, BH, s.nb, items, counter);
     SPARSP_LAUNCH_CHECK();

@@ -1,7 +1,8 @@
 // Step 3: Top-p routing with a Top-k floor, compacted into a per-head CSR.
 //
 // Three launches, no atomics on data, deterministic:
-//  1. count_kernel  - one warp per row: bitonic sort of 64-bit keys
+//  1. count_kernel  - one warp per row (one CTA per row beyond 1,024 blocks,
+//     count_row_kernel): bitonic sort of 64-bit keys
 //     (score descending as an order-preserving integer, then block index) held
 //     in registers and exchanged with shuffles; e_j = exp(S_j - max) rounded
 //     to fp32 (expf, or the correctly rounded value for rows whose Top-p
@@ -187,6 +188,140 @@ count_kernel(const float* __restrict__ S, int64_t rows, int nb, double top_p, in
   }
 }
 
+// Rows longer than 1,024 blocks: one CTA of kRowThreads threads per row. The
+// keys are sorted ascending with a bitonic network in shared memory (NP = the
+// next power of two >= nb, at most 4,096); thread t then owns sorted positions
+// [t*E, t*E + E) for the prefix masses, summed with a block-wide float64 scan.
+// Same keys, same e_j (expf, or correctly rounded near the crossing), same
+// cutoff rule as the warp-per-row kernel.
+constexpr int kRowThreads = 512;
+constexpr int kRowWarps = kRowThreads / 32;
+constexpr int kRowMaxE = 8;   // 4,096 / 512
+
+struct RowScratch {
+  double wsum[kRowWarps];
+  int32_t wcnt[kRowWarps];
+  int32_t flag;
+};
+
+// Exclusive prefix (in sorted order) of this thread's chunk and the row total
+// Z, from the chunk sums: a block-wide float64 scan.
+__device__ __forceinline__ double block_excl_scan(double v, double* total, RowScratch& sc) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  double incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const double o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  __syncthreads();   // sc.wsum may still be read from a previous call
+  if (lane == 31) sc.wsum[warp] = incl;
+  __syncthreads();
+  double before = 0.0, all = 0.0;
+  for (int w = 0; w < kRowWarps; ++w) {
+    if (w < warp) before += sc.wsum[w];
+    all += sc.wsum[w];
+  }
+  *total = all;
+  return before + incl - v;
+}
+
+__device__ __forceinline__ int block_topp_count(const uint64_t* keys, int nb, int E, float smax, double top_p,
+                                                bool exact, bool* near, RowScratch& sc) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  double ev[kRowMaxE];
+  double sum = 0.0;
+#pragma unroll
+  for (int e = 0; e < kRowMaxE; ++e) {
+    const int p = (int)threadIdx.x * E + e;
+    ev[e] = 0.0;
+    if (e < E && p < nb) {
+      const float x = key_score(keys[p]) - smax;
+      ev[e] = exact ? (double)__double2float_rn(exp((double)x)) : (double)expf(x);
+    }
+    sum += ev[e];
+  }
+  double Z;
+  double c = block_excl_scan(sum, &Z, sc);
+  const double target = top_p * Z, band = 1e-6 * Z;
+  int below = 0;
+  bool close = false;
+#pragma unroll
+  for (int e = 0; e < kRowMaxE; ++e) {
+    const int p = (int)threadIdx.x * E + e;
+    c += ev[e];
+    if (e < E && p < nb) {
+      if (c < target) ++below;
+      if (fabs(c - target) < band) close = true;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) below += __shfl_xor_sync(0xffffffffu, below, off);
+  if (lane == 0) sc.wcnt[warp] = below;
+  *near = __syncthreads_or(close) != 0;
+  int tot = 0;
+  for (int w = 0; w < kRowWarps; ++w) tot += sc.wcnt[w];
+  return min(nb, tot + 1);
+}
+
+__global__ void __launch_bounds__(kRowThreads)
+count_row_kernel(const float* __restrict__ S, int nb, int NP, double top_p, int k_floor,
+                 int32_t* __restrict__ counts, uint64_t* __restrict__ thr, int32_t* d_status) {
+  extern __shared__ uint64_t keys[];   // [NP]
+  __shared__ RowScratch sc;
+  const int64_t row = blockIdx.x;
+  const float* srow = S + row * nb;
+  bool bad = false;
+  for (int p = threadIdx.x; p < NP; p += kRowThreads) {
+    if (p < nb) {
+      const float v = srow[p];
+      if (!isfinite(v)) bad = true;
+      keys[p] = make_key(v, p);
+    } else {
+      keys[p] = ~0ull;
+    }
+  }
+  if (__syncthreads_or(bad)) {
+    if (threadIdx.x == 0) {
+      report(d_status, SPARSP_ERR_DATA);
+      counts[row] = 0;
+      thr[row] = 0;
+    }
+    return;
+  }
+  // bitonic sort, ascending
+  for (int size = 2; size <= NP; size <<= 1)
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int q = threadIdx.x; q < NP / 2; q += kRowThreads) {
+        const int i = (q / stride) * 2 * stride + (q % stride), j = i + stride;
+        const bool asc = (i & size) == 0;
+        const uint64_t a = keys[i], b = keys[j];
+        if (asc ? a > b : a < b) {
+          keys[i] = b;
+          keys[j] = a;
+        }
+      }
+      __syncthreads();
+    }
+  int m_p;
+  if (top_p <= 0.0) {
+    m_p = 0;
+  } else if (top_p >= 1.0) {
+    m_p = nb;
+  } else {
+    const float smax = key_score(keys[0]);
+    const int E = (nb + kRowThreads - 1) / kRowThreads;
+    bool near = false;
+    m_p = block_topp_count(keys, nb, E, smax, top_p, false, &near, sc);
+    if (near) m_p = block_topp_count(keys, nb, E, smax, top_p, true, &near, sc);
+  }
+  const int m = min(nb, max(m_p, max(k_floor, 1)));
+  if (threadIdx.x == 0) {
+    counts[row] = m;
+    thr[row] = keys[m - 1];
+  }
+}
+
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
 fill_kernel(const float* __restrict__ S, int64_t rows, int nb, const int32_t* __restrict__ row_ptr,
             const uint64_t* __restrict__ thr, int32_t* __restrict__ col_idx) {
@@ -233,7 +368,16 @@ sparsp_status_t launch_select(const Dims& s, const float* scores, float top_p, i
   else if (nb <= 128) count_go<4>(scores, rows, nb, p, k_floor, row_ptr, thr, d_status, st);
   else if (nb <= 256) count_go<8>(scores, rows, nb, p, k_floor, row_ptr, thr, d_status, st);
   else if (nb <= 512) count_go<16>(scores, rows, nb, p, k_floor, row_ptr, thr, d_status, st);
-  else count_go<32>(scores, rows, nb, p, k_floor, row_ptr, thr, d_status, st);
+  else if (nb <= 1024) count_go<32>(scores, rows, nb, p, k_floor, row_ptr, thr, d_status, st);
+  else {
+    if (nb > kRowThreads * kRowMaxE) return SPARSP_ERR_UNSUPPORTED;
+    int NP = 1;
+    while (NP < nb) NP <<= 1;
+    const size_t smem = (size_t)NP * sizeof(uint64_t);
+    if (cudaFuncSetAttribute(count_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return SPARSP_ERR_CUDA;
+    count_row_kernel<<<(unsigned)rows, kRowThreads, smem, st>>>(scores, nb, NP, p, k_floor, row_ptr, thr, d_status);
+  }
   SPARSP_LAUNCH_CHECK();
   sparsp_status_t r = launch_scan_counts(row_ptr, rows, st);
   if (r != SPARSP_OK) return r;

@@ -102,8 +102,11 @@ class Pipeline:
                                        dtype=torch.uint8, device=dev)
         # forward-only steps on the tcgen05 kernel take O straight into raster order (the
         # backward needs it in block order)
+        # (64-token blocks with d = 128 beyond 1,024 blocks run the portable kernel,
+        # which writes block order only)
         self.raster_out = (not backward and s.torch_dtype == torch.bfloat16 and not (flags & 2)
-                           and s.Bt in (64, 128) and s.d in (64, 128))
+                           and s.Bt in (64, 128) and s.d in (64, 128)
+                           and not (s.Bt == 64 and s.d == 128 and s.nb > 1024))
         self.overlap_demand = overlap_demand
         if overlap_demand:
             lo, hi = torch.cuda.Stream.priority_range()   # least, greatest

@@ -32,8 +32,11 @@
  *    Calls are thread-safe.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default).
  *  - All device pointers must be 16-byte aligned; tensors are contiguous.
- *  - Shapes: d in {64, 128}; Bt = ta*tb*tc in {64, 128}; nb = N/Bt <= 1024;
- *    dtype SPARSP_F32 or SPARSP_BF16 (bf16 inputs accumulate in fp32).
+ *  - Shapes: d in {64, 128}; Bt = ta*tb*tc in {64, 128}; nb = N/Bt <= 4096
+ *    (524,288 tokens in 128-token blocks) and B*H*nb*nb < 2^31 (int32 CSR
+ *    offsets); dtype SPARSP_F32 or SPARSP_BF16 (bf16 inputs accumulate in
+ *    fp32). sparsp_placement and sparsp_augment take nb <= 1024 and return
+ *    SPARSP_ERR_UNSUPPORTED beyond.
  *
  * Layouts
  * -------
@@ -99,8 +102,9 @@ enum {
   /* Forward: write O in raster order [B, N, H, d] (the layout of the inverse
    * sparsp_reorder) instead of block order; LSE stays [B, H, N] in block
    * order. Only the tcgen05 kernel (bf16 on sm_103a, Bt and d in {64, 128},
-   * without SPARSP_KERNEL_PORTABLE) does this; elsewhere the call returns
-   * SPARSP_ERR_UNSUPPORTED before enqueuing anything. */
+   * nb <= 1024 when Bt = 64 and d = 128, without SPARSP_KERNEL_PORTABLE) does
+   * this; elsewhere the call returns SPARSP_ERR_UNSUPPORTED before enqueuing
+   * anything. */
   SPARSP_OUT_RASTER = 1u << 3
 };
 /* Attention kernels: at most n persistent CTAs (1 <= n <= 4095) instead of
@@ -390,7 +394,8 @@ SPARSP_API sparsp_status_t sparsp_lpt_schedule(const sparsp_shape_t* shape, cons
  * must list distinct blocks (sparsp_select writes them ascending); the
  * 64-token-block tcgen05 kernel also reports a repeated index as
  * SPARSP_ERR_DATA and skips that row, the other kernels do not check.
- * bf16 on sm_103a runs the tcgen05/TMEM/TMA kernel (Bt and d in {64, 128};
+ * bf16 on sm_103a runs the tcgen05/TMEM/TMA kernel (Bt and d in {64, 128},
+ * except 64-token blocks with d = 128 beyond 1,024 blocks;
  * with 64-token blocks each work item is a pair of neighbouring query blocks
  * over the union of their rows, so that every MMA has 128 query rows and 128
  * key columns); with SPARSP_KERNEL_PORTABLE an mma.sync kernel; float32 runs

@@ -69,7 +69,8 @@ def shape(**kw):
     (dict(d=96), sp.UNSUPPORTED),
     (dict(ta=2), sp.UNSUPPORTED),       # Bt = 32
     (dict(dtype=7), sp.UNSUPPORTED),
-    (dict(T=64, Y=64, X=64), sp.UNSUPPORTED),   # nb = 4096 > 1024
+    (dict(T=128, Y=64, X=64), sp.UNSUPPORTED),  # nb = 8192 > 4096
+    (dict(H=128, T=64, Y=64, X=64), sp.UNSUPPORTED),   # B*H*nb^2 = 128 * 4096^2 >= 2^31
 ])
 def test_shape_validation(lib, kw, code):
     s = shape(**kw)
@@ -218,3 +219,23 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(sp, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         sp.lib()
+
+
+def test_block_limits(lib):
+    """nb up to 4,096 is accepted by the hot-path calls (their workspace sizes
+    are non-zero); placement and augmentation stop at 1,024 blocks."""
+    big = shape(T=64, Y=64, X=64)                       # 4x4x4 tiles: nb = 16*16*16 = 4096
+    assert big.nb == 4096
+    b = ctypes.byref(big)
+    assert lib.sparsp_select_workspace_size(b) == big.rows * 8
+    assert lib.sparsp_attn_workspace_size(b, 1) > 0
+    assert lib.sparsp_lpt_workspace_size(b) > 0
+    assert lib.sparsp_placement_workspace_size(b) == 0
+    assert lib.sparsp_augment_workspace_size(b, 2) == 0
+    assert lib.sparsp_placement(b, 2, FAKE, FAKE, FAKE, FAKE, 1 << 40, None, None) == sp.UNSUPPORTED
+    assert lib.sparsp_augment(b, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, None, FAKE, 1 << 40, None,
+                              None) == sp.UNSUPPORTED
+    at_limit = shape(T=32, Y=64, X=64)                  # nb = 2048: placement still refused above 1024
+    assert lib.sparsp_placement_workspace_size(ctypes.byref(at_limit)) == 0
+    small = shape(T=16, Y=64, X=64)                     # nb = 1024
+    assert lib.sparsp_placement_workspace_size(ctypes.byref(small)) > 0
