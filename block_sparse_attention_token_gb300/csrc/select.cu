@@ -46,145 +46,232 @@ __device__ __forceinline__ float key_score(uint64_t key) {
   return from_ordered(~(uint32_t)(key >> 32));
 }
 
-// m_p of one row held sorted in the warp's registers (positions lane*E + e):
-// the smallest m whose leading prefix of e_j = exp(S_j - max) holds mass
-// >= top_p * Z, with Z and the prefixes summed in float64. exact: e_j is the
-// correctly rounded float32 of the exponential (evaluated in float64);
-// otherwise expf. *near: some prefix lies within 1e-6 of Z of the target.
-template <int E>
-__device__ __forceinline__ int topp_count(const uint64_t (&key)[E], float smax, int lane, int nb, double top_p,
-                                          bool exact, bool* near) {
-  double ev[E];
-  double lane_sum = 0.0;
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const int p = lane * E + e;
-    ev[e] = 0.0;
-    if (p < nb) {
-      const float x = key_score(key[e]) - smax;
-      ev[e] = exact ? (double)__double2float_rn(exp((double)x)) : (double)expf(x);
-    }
-    lane_sum += ev[e];
-  }
-  // inclusive scan of lane sums
-  double incl = lane_sum;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const double o = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += o;
-  }
-  const double Z = __shfl_sync(0xffffffffu, incl, 31);
-  const double target = top_p * Z, band = 1e-6 * Z;
-  double c = incl - lane_sum;   // exclusive prefix of this lane
-  int below = 0;
-  bool close = false;
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const int p = lane * E + e;
-    c += ev[e];
-    if (p < nb) {
-      if (c < target) ++below;
-      if (fabs(c - target) < band) close = true;
-    }
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) below += __shfl_xor_sync(0xffffffffu, below, off);
-  *near = __any_sync(0xffffffffu, close);
-  return min(nb, below + 1);
+// One warp per row of nb <= 32*E blocks, without sorting. Block j of the row
+// has the order-preserving score bits u_j (larger score = larger u) and sits
+// at position p = e*32 + lane. The kept set is the first m blocks in the order
+// (score descending, index ascending); it is described by its last member,
+// whose key (score bits, index) becomes the row's threshold for the fill
+// pass. Two searches over the bits of u find it:
+//  - Top-p: t* = the largest t whose mass M(t) = sum of e_j over u_j >= t
+//    still reaches top_p * Z; the blocks with u > t* hold less than that, so
+//    the crossing lies among the blocks tied at t*, which follow in index
+//    order: m_p = #(u > t*) + the fewest of those ties that reach the target.
+//  - the m-th block (m = min(nb, max(m_p, k_floor, 1))): the largest t with
+//    #(u >= t) >= m, then the (m - #(u > t))-th of its ties by index.
+// e_j = expf(s_j - max) in fp32 (correctly rounded instead for a row whose
+// crossing lies within 1e-6 of p). The t* search runs on fp32 sums; t* and
+// the tie count are then decided on exact sums of e_j in 64-bit fixed point
+// (resolution 2^-52, each term truncated by less than that: for nb <= 1024
+// the sums lie within 4e-13 of Z of float64 sums of the same values in any
+// order, inside the 1e-12 band in which the two may disagree at all),
+// stepping to a neighbouring score if the fp32 search landed off the crossing.
+constexpr double kFix = 4503599627370496.0;   // 2^52
+
+// e (0 <= e <= 1, fp32) in units of 2^-52, truncated: exact for e >= 2^-29
+__device__ __forceinline__ uint64_t to_fix(float e) {
+  const uint32_t b = __float_as_uint(e);
+  const int ex = (int)((b >> 23) & 0xffu);
+  if (ex == 0) return 0ull;   // zero or subnormal: below 2^-126
+  const uint64_t mant = (uint64_t)((b & 0x7fffffu) | 0x800000u);
+  const int sh = ex - 98;     // e * 2^52 = mant * 2^(ex - 127 - 23 + 52)
+  return sh >= 0 ? mant << sh : (sh > -64 ? mant >> (-sh) : 0ull);
 }
 
-template <int E>   // elements per lane; padded row length = 32*E
+template <int E>
+struct WarpRow {
+  uint32_t u[E];
+  float ev[E];
+  int nb, lane;
+
+  __device__ __forceinline__ bool valid(int e) const { return e * 32 + lane < nb; }
+
+  // number of blocks with u >= t (warp total)
+  __device__ __forceinline__ int count_ge(uint32_t t) const {
+    int c = 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) c += (valid(e) && u[e] >= t) ? 1 : 0;
+    return (int)__reduce_add_sync(0xffffffffu, (unsigned)c);
+  }
+  // fp32 mass of the blocks with u >= t (warp total; only steers the search)
+  __device__ __forceinline__ float mass32(uint32_t t) const {
+    float m = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      if (valid(e) && u[e] >= t) m += ev[e];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m += __shfl_xor_sync(0xffffffffu, m, off);
+    return m;
+  }
+  // exact fixed-point mass of the blocks with u >= t (ge) or u > t (!ge)
+  __device__ __forceinline__ uint64_t massq(uint32_t t, bool ge) const {
+    uint64_t m = 0ull;
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      if (valid(e) && (ge ? u[e] >= t : u[e] > t)) m += to_fix(ev[e]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m += __shfl_xor_sync(0xffffffffu, m, off);
+    return m;
+  }
+  // the largest u below t / the smallest u above t (warp-wide)
+  __device__ __forceinline__ uint32_t below(uint32_t t) const {
+    uint32_t b = 0u;
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      if (valid(e) && u[e] < t) b = max(b, u[e]);
+    return __reduce_max_sync(0xffffffffu, b);
+  }
+  __device__ __forceinline__ uint32_t above(uint32_t t) const {
+    uint32_t a = 0xffffffffu;
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      if (valid(e) && u[e] > t) a = min(a, u[e]);
+    return __reduce_min_sync(0xffffffffu, a);
+  }
+  // index of the k-th (1-based) block with u == t, in index order
+  __device__ __forceinline__ int kth_tie(uint32_t t, int k) const {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const uint32_t ball = __ballot_sync(0xffffffffu, valid(e) && u[e] == t);
+      const int c = __popc(ball);
+      if (k <= c) {
+        uint32_t b = ball;
+        for (int r = 1; r < k; ++r) b &= b - 1u;
+        return e * 32 + __ffs(b) - 1;
+      }
+      k -= c;
+    }
+    return -1;   // not reached for 1 <= k <= #ties
+  }
+};
+
+// Bits of the search: every t below the common prefix of umin and umax counts
+// every block, so only the bits from the highest differing one need trying.
+__device__ __forceinline__ int search_top_bit(uint32_t umin, uint32_t umax) {
+  return umin == umax ? -1 : 31 - __clz(umin ^ umax);
+}
+
+__device__ __forceinline__ uint32_t search_start(uint32_t umin, int hb) {
+  return hb < 0 ? umin : (umin & ~((2u << hb) - 1u));   // hb = 31: 2u << 31 == 0, start at 0
+}
+
+// Top-p cutoff m_p from e_j held in row.ev; *near when a prefix sum around the
+// crossing lies within 1e-6 of Z of the target.
+template <int E>
+__device__ __forceinline__ int topp_count(const WarpRow<E>& row, uint32_t umin, uint32_t umax, double top_p,
+                                          bool* near) {
+  const uint64_t Zq = row.massq(0u, true);
+  const double Z = (double)Zq, target = top_p * Z, band = 1e-6 * Z;
+  const float target32 = (float)(top_p * (double)row.mass32(0u));
+  const int hb = search_top_bit(umin, umax);
+  uint32_t t = search_start(umin, hb);
+  for (int bit = hb; bit >= 0; --bit) {
+    const uint32_t cand = t | (1u << bit);
+    if (row.mass32(cand) >= target32) t = cand;
+  }
+  // exact: M(t) >= target > M(> t), with t a score of the row
+  uint64_t ge = 0ull, gt = 0ull;
+  for (int step = 0; step <= 2 * row.nb; ++step) {
+    ge = row.massq(t, true);
+    gt = row.massq(t, false);
+    if ((double)ge < target) {
+      t = row.below(t);          // exists: M(umin) = Z >= target
+    } else if ((double)gt >= target) {
+      t = row.above(t);          // exists: M(> umax) = 0 < target
+    } else {
+      break;
+    }
+  }
+  const int gtc = t == 0xffffffffu ? 0 : row.count_ge(t + 1u);
+  const int eq = row.count_ge(t) - gtc;
+  // the ties all hold the same e_j: that of any of them
+  float et = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    if (row.valid(e) && row.u[e] == t) et = row.ev[e];
+  et = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(et)));   // et >= 0: bits order as values
+  const uint64_t etq = to_fix(et);
+  uint64_t cq = gt + etq, cq_prev = gt;
+  int k = 1;
+  while ((double)cq < target && k < eq) {
+    cq_prev = cq;
+    cq += etq;
+    ++k;
+  }
+  *near = fabs((double)cq - target) < band || fabs((double)cq_prev - target) < band;
+  return min(row.nb, gtc + k);
+}
+
+template <int E>   // blocks per lane; nb <= 32*E
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
 count_kernel(const float* __restrict__ S, int64_t rows, int nb, double top_p, int k_floor,
              int32_t* __restrict__ counts, uint64_t* __restrict__ thr, int32_t* d_status) {
   const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-  if (row >= rows) return;
-  const float* srow = S + row * nb;
-  uint64_t key[E];
+  const int64_t r = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  const float* srow = S + r * nb;
+  WarpRow<E> row;
+  row.nb = nb;
+  row.lane = lane;
   bool bad = false;
+  uint32_t umin = 0xffffffffu, umax = 0u;
 #pragma unroll
   for (int e = 0; e < E; ++e) {
-    const int p = lane * E + e;
-    if (p < nb) {
-      const float s = srow[p];
-      if (!isfinite(s)) bad = true;
-      key[e] = make_key(s, p);
-    } else {
-      key[e] = ~0ull;
+    row.u[e] = 0u;
+    row.ev[e] = 0.f;
+    if (row.valid(e)) {
+      const float sv = srow[e * 32 + lane];
+      if (!isfinite(sv)) bad = true;
+      row.u[e] = ordered_bits(sv);
+      umin = min(umin, row.u[e]);
+      umax = max(umax, row.u[e]);
     }
   }
   if (__any_sync(0xffffffffu, bad)) {
     if (lane == 0) {
       report(d_status, SPARSP_ERR_DATA);
-      counts[row] = 0;
-      thr[row] = 0;
+      counts[r] = 0;
+      thr[r] = 0;
     }
     return;
   }
-  // bitonic sort, ascending key, positions p = lane*E + e
-  constexpr int NP = 32 * E;
-#pragma unroll
-  for (int size = 2; size <= NP; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      if (stride < E) {
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const int e2 = e ^ stride;
-          if (e2 > e) {
-            const int p = lane * E + e;
-            const bool asc = (p & size) == 0;
-            const uint64_t a = key[e], b = key[e2];
-            const bool swap = asc ? (a > b) : (a < b);
-            key[e] = swap ? b : a;
-            key[e2] = swap ? a : b;
-          }
-        }
-      } else {
-        const int lmask = stride / E;
-        const bool lo = (lane & lmask) == 0;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const int p = lane * E + e;
-          const bool asc = (p & size) == 0;
-          const uint64_t other = __shfl_xor_sync(0xffffffffu, key[e], lmask);
-          const uint64_t mn = key[e] < other ? key[e] : other;
-          const uint64_t mx = key[e] < other ? other : key[e];
-          key[e] = (lo == asc) ? mn : mx;
-        }
-      }
-    }
-  }
-  // Top-p cutoff from the softmax mass in sorted order (no exponentials are
-  // needed for p <= 0 or p >= 1)
+  umin = __reduce_min_sync(0xffffffffu, umin);
+  umax = __reduce_max_sync(0xffffffffu, umax);
   int m_p;
   if (top_p <= 0.0) {
     m_p = 0;
   } else if (top_p >= 1.0) {
     m_p = nb;
   } else {
-    const float smax = __shfl_sync(0xffffffffu, key_score(key[0]), 0);
+    const float smax = from_ordered(umax);
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      if (row.valid(e)) row.ev[e] = expf(from_ordered(row.u[e]) - smax);
     bool near = false;
-    m_p = topp_count<E>(key, smax, lane, nb, top_p, false, &near);
+    m_p = topp_count<E>(row, umin, umax, top_p, &near);
     // e_j is defined as the float32 rounding of exp(S_j - max). expf is within
-    // 2 ulp of the exact value, which moves any prefix sum (and Z) by at most
-    // 3e-7 of Z; only a row whose crossing lies that close to p can decide
+    // 2 ulp of the exact value, which moves any of these sums (and Z) by at
+    // most 3e-7 of Z; only a row whose crossing lies that close to p can decide
     // differently, and it is recomputed with the correctly rounded e_j.
-    if (near) m_p = topp_count<E>(key, smax, lane, nb, top_p, true, &near);
+    if (near) {
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        if (row.valid(e)) row.ev[e] = __double2float_rn(exp((double)(from_ordered(row.u[e]) - smax)));
+      m_p = topp_count<E>(row, umin, umax, top_p, &near);
+    }
   }
   const int m = min(nb, max(m_p, max(k_floor, 1)));
-  // threshold key = key at sorted position m-1
-  const int pos = m - 1;
-  const int src_lane = pos / E, src_e = pos % E;
-  uint64_t mine = 0;
-#pragma unroll
-  for (int e = 0; e < E; ++e)
-    if (e == src_e) mine = key[e];
-  const uint64_t tk = __shfl_sync(0xffffffffu, mine, src_lane);
+  // the m-th block in (score descending, index ascending) order
+  const int hb = search_top_bit(umin, umax);
+  uint32_t t = search_start(umin, hb);
+  for (int bit = hb; bit >= 0; --bit) {
+    const uint32_t cand = t | (1u << bit);
+    if (row.count_ge(cand) >= m) t = cand;
+  }
+  const int gt = t == 0xffffffffu ? 0 : row.count_ge(t + 1u);
+  const int j = row.kth_tie(t, m - gt);
   if (lane == 0) {
-    counts[row] = m;
-    thr[row] = tk;
+    counts[r] = m;
+    thr[r] = ((uint64_t)(~t) << 32) | (uint32_t)j;   // = make_key(score of t, j)
   }
 }
 
