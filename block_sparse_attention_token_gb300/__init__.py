@@ -17,7 +17,10 @@ from dataclasses import dataclass
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libsparsp.so")
+# SPARSP_DEBUG=1 in the environment selects the debug build (build(debug=True)),
+# whose kernels also bounds-check the addresses they derive themselves
+DEBUG = os.environ.get("SPARSP_DEBUG") == "1"
+LIB_PATH = os.path.join(_PKG, "libsparsp_debug.so" if DEBUG else "libsparsp.so")
 
 OK, INVALID_ARG, UNSUPPORTED, SHAPE, ALIGN, WORKSPACE, CAPACITY, DATA, CUDA, TIMEOUT = range(10)
 F32, BF16 = 0, 1
@@ -122,7 +125,8 @@ def lib():
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"libsparsp.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+            raise RuntimeError(f"{os.path.basename(LIB_PATH)} is not built ({LIB_PATH}); run "
+                               f"block_sparse_attention_token_gb300.build.build(debug={DEBUG})")
         h = ctypes.CDLL(LIB_PATH)
         for name, (res, args) in _SIG.items():
             fn = getattr(h, name)

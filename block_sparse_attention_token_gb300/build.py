@@ -4,6 +4,12 @@ Each .cu under csrc/ compiles to an object in parallel; the objects link into
 block_sparse_attention_token_gb300/libsparsp.so with the CUDA runtime linked
 statically, so loading the library needs no CUDA driver (the ABI checks run
 on machines without a GPU).
+
+build(debug=True) makes libsparsp_debug.so instead, compiled with
+-DSPARSP_DEBUG: its kernels also check every address they derive themselves
+(TMA coordinates, output rows, list and CSR write positions) and report
+SPARSP_ERR_DATA rather than use one out of range. The binding loads it when
+the environment sets SPARSP_DEBUG=1.
 """
 from __future__ import annotations
 
@@ -20,6 +26,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsparsp.so")
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libsparsp_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -47,8 +55,8 @@ def _headers_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def _compile(src: str, extra: list[str], verbose: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _compile(src: str, extra: list[str], verbose: bool, build_dir: str = BUILD) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
     cmd = [_nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
@@ -60,11 +68,13 @@ def _compile(src: str, extra: list[str], verbose: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    """Compile every CUDA source and link libsparsp.so; returns its path."""
-    extra = list(extra or [])
-    os.makedirs(BUILD, exist_ok=True)
-    stamp_path = os.path.join(BUILD, "stamp")
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None, debug: bool = False) -> str:
+    """Compile every CUDA source and link libsparsp.so (libsparsp_debug.so with
+    debug=True); returns its path."""
+    extra = list(extra or []) + (["-DSPARSP_DEBUG"] if debug else [])
+    build_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    os.makedirs(build_dir, exist_ok=True)
+    stamp_path = os.path.join(build_dir, "stamp")
     srcs = _sources()
     key = hashlib.sha256()
     for s in srcs:
@@ -72,23 +82,23 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
             key.update(s.encode() + fh.read())
     key.update(_headers_digest().encode() + " ".join(ARCH + NVCC_FLAGS + extra).encode())
     stamp = key.hexdigest()
-    if not force and os.path.exists(LIB) and os.path.exists(stamp_path):
+    if not force and os.path.exists(lib) and os.path.exists(stamp_path):
         with open(stamp_path) as fh:
             if fh.read() == stamp:
-                return LIB
+                return lib
     workers = min(len(srcs), os.cpu_count() or 4)
     with cf.ThreadPoolExecutor(max_workers=workers) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra, verbose), srcs))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, extra, verbose, build_dir), srcs))
+    tmp = lib + ".tmp"
     cmd = [_nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp_path, "w") as fh:
         fh.write(stamp)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

@@ -108,6 +108,7 @@ struct Params {
   int64_t N;
   int nb;
   int64_t n_items;
+  int64_t rows_total;    // B*H*N rows of every tensor
   float sl2;             // scale * log2(e)
   float out_scale;       // scale for dQ and dK, 1 for dV
   const float* lse2;     // LSE * log2(e), [B*H*N]
@@ -219,7 +220,8 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
       if (len <= 0) continue;
       const int64_t bh = item / nb;
       const int i = item % nb;
-      const int32_t ya = (int32_t)(bh * p.N + (int64_t)i * BT);
+      int32_t ya = (int32_t)(bh * p.N + (int64_t)i * BT);
+      if (!dcheck(ya >= 0 && ya + BT <= p.rows_total, p.d_status)) ya = 0;
       if (!wait_warp(bar(A_EMPTY), (a_fill & 1u) ^ 1u, g)) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(bar(A_FULL), kHasDP ? 2 * kTile : kTile);
@@ -235,7 +237,8 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
       bool ok = true;
       for (int e = 0; e < len; ++e) {
         const int32_t c = p.idx[e0 + e];
-        const int64_t yc64 = bh * p.N + (int64_t)c * BT;
+        int64_t yc64 = bh * p.N + (int64_t)c * BT;
+        if (!dcheck(yc64 >= 0 && yc64 + BT <= p.rows_total, p.d_status)) yc64 = 0;   // flagged; counts kept
         const int32_t yc = (int32_t)yc64;
         const uint32_t st = c_fill % kNS;
         if (!(ok = wait_warp(bar(C_EMPTY + st), ((c_fill / kNS) & 1u) ^ 1u, g))) break;
@@ -474,7 +477,8 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
       const int64_t item = ent.x;
       const int64_t bh = item / nb;
       const int i = (int)(item % nb);
-      const int64_t row = bh * p.N + (int64_t)i * BT + threadIdx.x;
+      int64_t row = bh * p.N + (int64_t)i * BT + threadIdx.x;
+      if (!dcheck(row >= 0 && row < p.rows_total, p.d_status)) row = 0;
       uint4* orow = reinterpret_cast<uint4*>(p.out + row * D);
       uint4* orow2 = MODE == 3 ? reinterpret_cast<uint4*>(p.out2 + row * D) : nullptr;
       const int len = ent.y;
@@ -627,7 +631,7 @@ sparsp_status_t launch_attn_bwd_tc(const Dims& s, int mode, const __nv_bfloat16*
   if (!make_tmap_bf16_rows(&tq, q, rows, D, BT) || !make_tmap_bf16_rows(&tk, k, rows, D, BT) ||
       !make_tmap_bf16_rows(&tv, v, rows, D, BT) || !make_tmap_bf16_rows(&tdo, dout, rows, D, BT))
     return SPARSP_ERR_CUDA;
-  Params prm{ptr, idx, s.N, s.nb, s.rows(), scale * 1.4426950408889634f, mode == 2 ? 1.0f : scale,
+  Params prm{ptr, idx, s.N, s.nb, s.rows(), (int64_t)rows, scale * 1.4426950408889634f, mode == 2 ? 1.0f : scale,
              lse2, delta, out, out2, 1.0f, items, counter, prof, d_status};
   if (mode == 0) return go<0>(s, tq, tdo, tk, tv, prm, st);
   if (mode == 1) return go<1>(s, tk, tv, tq, tdo, prm, st);

@@ -146,6 +146,7 @@ struct Params {
   int nb;
   int nbp;           // items per head: nb, or ceil(nb/2) pairs of 64-token blocks
   int64_t n_items;
+  int64_t rows_total;   // B*H*N rows of Q, K, V, O and LSE
   float scale_log2;
   __nv_bfloat16* o;
   float* lse;
@@ -335,7 +336,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       if (len <= 0) continue;
       const int64_t bh = item / nbp;
       const int i0 = PAIR ? 2 * (item % nbp) : item % nb;   // first query block of the item
-      const int32_t yq = (int32_t)(bh * p.N + (int64_t)i0 * BT);
+      int32_t yq = (int32_t)(bh * p.N + (int64_t)i0 * BT);
+      if (!dcheck(yq >= 0 && yq < p.rows_total, p.d_status)) yq = 0;
       if (!wait_warp(bar(Q_EMPTY), (q_fill & 1u) ^ 1u, g)) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(bar(Q_FULL), C::kQTile);
@@ -355,8 +357,10 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         } else {
           j1 = p.col_idx[e0 + e];
         }
-        const int32_t yk1 = (int32_t)(bh * p.N + (int64_t)j1 * BT);
-        const int32_t yk2 = (int32_t)(bh * p.N + (int64_t)j2 * BT);
+        int32_t yk1 = (int32_t)(bh * p.N + (int64_t)j1 * BT);
+        int32_t yk2 = (int32_t)(bh * p.N + (int64_t)j2 * BT);
+        if (!dcheck(yk1 >= 0 && yk1 + BT <= p.rows_total && yk2 >= 0 && yk2 + BT <= p.rows_total, p.d_status))
+          yk1 = yk2 = 0;   // keep the transaction counts; the result is flagged
         const uint32_t ks = k_fill % C::NK;
         if (!(ok = wait_warp(bar(K_EMPTY + ks), ((k_fill / C::NK) & 1u) ^ 1u, g))) break;
         if (lane == 0) {
@@ -538,7 +542,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       const int i = PAIR ? 2 * (int)(item % nbp) + half : (int)(item % nb);
       const int o = PAIR ? (r & 63) : r;
       const int64_t row = bh * p.N + (int64_t)i * BT + o;
-      const bool stores = o < BT && i < nb && !((badbits >> half) & 1);
+      bool stores = o < BT && i < nb && !((badbits >> half) & 1);
       int64_t orow_idx = row;
       if (p.raster && stores) {
         const int tbc = p.tb * p.tc;
@@ -549,6 +553,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         orow_idx = ((bh / p.H) * p.N + n) * p.H + bh % p.H;
       }
       // this group stores columns [32*grp, 32*grp + 32) of the row
+      if (stores) stores = dcheck(row < p.rows_total && orow_idx >= 0 && orow_idx < p.rows_total, p.d_status);
       uint4* orow = reinterpret_cast<uint4*>(p.o + orow_idx * D) + grp * 4;
       if (len == 0) {
         if (stores) {
@@ -704,7 +709,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         const int o = PAIR ? (int)(threadIdx.x & 63) : (int)threadIdx.x;       // its token in the block
         const int64_t row = bh * p.N + (int64_t)i * BT + o;
         // rows past the block (or past the last block of a pair) are computed, never stored
-        const bool stores = o < BT && i < nb && !((badbits >> half) & 1);
+        bool stores = o < BT && i < nb && !((badbits >> half) & 1);
         int64_t orow_idx = row;
         if (p.raster && stores) {
           // tile i = (bt, by, bx) block-raster; token o = (it, iy, ix) raster inside the tile
@@ -715,6 +720,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                             (int64_t)bx * p.tc + ix;
           orow_idx = ((bh / p.H) * p.N + n) * p.H + bh % p.H;
         }
+        if (stores) stores = dcheck(row < p.rows_total && orow_idx >= 0 && orow_idx < p.rows_total, p.d_status);
         uint4* orow = reinterpret_cast<uint4*>(p.o + orow_idx * D);
         if (len == 0) {
           if (stores) {
@@ -895,7 +901,7 @@ sparsp_status_t launch_attn_fwd_tc(const Dims& s, const __nv_bfloat16* q, const 
   // 64-token blocks: items are pairs of query blocks, ordered by the caller
   // over the pair rows (attn_fwd_tc_items)
   const int nbp = attn_fwd_tc_items_per_head(s);
-  Params prm{row_ptr, col_idx, s.N, s.nb, nbp, (int64_t)s.B * s.H * nbp, scale * 1.4426950408889634f, o, lse,
+  Params prm{row_ptr, col_idx, s.N, s.nb, nbp, (int64_t)s.B * s.H * nbp, (int64_t)rows, scale * 1.4426950408889634f, o, lse,
              raster ? 1 : 0, s.H, s.Y, s.X, s.ta, s.tb, s.tc, s.nY, s.nX, items, counter, prof, d_status};
   if (s.Bt == 128 && s.d == 128) return go_fwd<128, 128>(s, tq, tk, tv, prm, st);
   if (s.Bt == 128 && s.d == 64) return go_fwd<128, 64>(s, tq, tk, tv, prm, st);

@@ -41,6 +41,20 @@ __device__ __forceinline__ void report(int32_t* st, int32_t code) {
   if (st != nullptr) atomicCAS(st, 0, code);
 }
 
+// Debug builds (compiled with -DSPARSP_DEBUG, see build.py) also check the
+// addresses a kernel derives from its own arithmetic - TMA coordinates, output
+// rows, list and CSR write positions - and report SPARSP_ERR_DATA instead of
+// using one out of range. Release builds check what comes from the caller and
+// compile these checks away.
+#ifdef SPARSP_DEBUG
+__device__ __forceinline__ bool dcheck(bool ok, int32_t* st) {
+  if (!ok) report(st, SPARSP_ERR_DATA);
+  return ok;
+}
+#else
+__device__ __forceinline__ bool dcheck(bool, int32_t*) { return true; }
+#endif
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -108,7 +108,7 @@ bitmap_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ c
 
 __global__ void __launch_bounds__(256)
 list_kernel(const uint32_t* __restrict__ bitmap, const int32_t* __restrict__ dem_ptr, int nparts,
-            int W, int32_t* __restrict__ dem_idx) {
+            int W, int32_t* __restrict__ dem_idx, int32_t* d_status) {
   const int lane = threadIdx.x & 31;
   const int part = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (part >= nparts) return;
@@ -124,11 +124,13 @@ list_kernel(const uint32_t* __restrict__ bitmap, const int32_t* __restrict__ dem
     if (lane >= off) incl += o;
   }
   int pos = dem_ptr[part] + incl - cnt;
+  const int end = dem_ptr[part + 1];
   for (int w = w0; w < w1; ++w) {
     uint32_t word = bm[w];
     while (word) {
       const int bit = __ffs(word) - 1;
-      dem_idx[pos++] = w * 32 + bit;
+      if (dcheck(pos < end, d_status)) dem_idx[pos] = w * 32 + bit;
+      ++pos;
       word &= word - 1;
     }
   }
@@ -145,11 +147,18 @@ constexpr int kGatherThreads = 128;
 
 __global__ void __launch_bounds__(kGatherThreads, 8)
 gather_kernel(const int32_t* __restrict__ dem_ptr, const int32_t* __restrict__ dem_idx, int nparts,
-              int P, int64_t N, int Bt, int vec_per_row, const uint4* __restrict__ k,
+              int P, int64_t N, int Bt, int nb, int vec_per_row, const uint4* __restrict__ k,
               const uint4* __restrict__ v, uint4* __restrict__ kg, uint4* __restrict__ vg,
               int64_t cap, int32_t* d_status) {
-  const int64_t total = dem_ptr[nparts];
+  // the lists may come from the caller (sparsp_kv_gather): a total beyond what
+  // nparts partitions can demand, or an index outside [0, nb), is reported
+  // and never used as an address
+  int64_t total = dem_ptr[nparts];
   const int64_t slot = blockIdx.x;
+  if (total < 0 || total > (int64_t)nparts * nb) {
+    if (slot == 0 && threadIdx.x == 0) report(d_status, SPARSP_ERR_DATA);
+    total = 0;
+  }
   if (slot == 0 && total > cap && threadIdx.x == 0) report(d_status, SPARSP_ERR_CAPACITY);
   if (slot >= total || slot >= cap) return;
   int lo = 0, hi = nparts - 1;   // last part with dem_ptr[part] <= slot
@@ -159,6 +168,10 @@ gather_kernel(const int32_t* __restrict__ dem_ptr, const int32_t* __restrict__ d
   }
   const int bh = lo / P;
   const int j = dem_idx[slot];
+  if (j < 0 || j >= nb) {
+    if (threadIdx.x == 0) report(d_status, SPARSP_ERR_DATA);
+    return;
+  }
   const int64_t nvec = (int64_t)Bt * vec_per_row;
   const uint4* ks = k + ((int64_t)bh * N + (int64_t)j * Bt) * vec_per_row;
   const uint4* vs = v + ((int64_t)bh * N + (int64_t)j * Bt) * vec_per_row;
@@ -220,7 +233,7 @@ sparsp_status_t launch_kv_demand(const Dims& s, int P, const int32_t* row_ptr,
   SPARSP_LAUNCH_CHECK();
   sparsp_status_t r = launch_scan_counts(dem_ptr, nparts, st);
   if (r != SPARSP_OK) return r;
-  list_kernel<<<(nparts + 7) / 8, 256, 0, st>>>(bitmap, dem_ptr, nparts, W, dem_idx);
+  list_kernel<<<(nparts + 7) / 8, 256, 0, st>>>(bitmap, dem_ptr, nparts, W, dem_idx, d_status);
   SPARSP_LAUNCH_CHECK();
   if (kg != nullptr && vg != nullptr) return launch_kv_gather(s, P, dem_ptr, dem_idx, k, v, kg, vg, cap, d_status, st);
   return SPARSP_OK;
@@ -235,7 +248,7 @@ sparsp_status_t launch_kv_gather(const Dims& s, int P, const int32_t* dem_ptr, c
   int64_t grid = upper < cap ? upper : cap;
   if (grid < 1) grid = 1;
   const int vec_per_row = s.d * s.elem / 16;
-  gather_kernel<<<(unsigned)grid, kGatherThreads, 0, st>>>(dem_ptr, dem_idx, nparts, P, s.N, s.Bt, vec_per_row,
+  gather_kernel<<<(unsigned)grid, kGatherThreads, 0, st>>>(dem_ptr, dem_idx, nparts, P, s.N, s.Bt, s.nb, vec_per_row,
                                                  (const uint4*)k, (const uint4*)v, (uint4*)kg, (uint4*)vg, cap,
                                                  d_status);
   SPARSP_LAUNCH_CHECK();

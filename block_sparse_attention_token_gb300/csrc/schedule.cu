@@ -169,7 +169,7 @@ csr_transpose_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restr
       const int32_t jj = col_idx[e];
       if (jj >= 0 && jj < nb) {
         const int32_t pos = atomicAdd(&cursor[jj], 1);   // distinct jj within a row
-        row_idx[pos] = i;
+        if (dcheck(pos >= e0 && pos < e1, d_status)) row_idx[pos] = i;
       }
     }
     __syncthreads();

@@ -411,7 +411,7 @@ count_row_kernel(const float* __restrict__ S, int nb, int NP, double top_p, int 
 
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
 fill_kernel(const float* __restrict__ S, int64_t rows, int nb, const int32_t* __restrict__ row_ptr,
-            const uint64_t* __restrict__ thr, int32_t* __restrict__ col_idx) {
+            const uint64_t* __restrict__ thr, int32_t* __restrict__ col_idx, int32_t* d_status) {
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   if (row >= rows) return;
@@ -426,7 +426,10 @@ fill_kernel(const float* __restrict__ S, int64_t rows, int nb, const int32_t* __
     bool keep = false;
     if (j < nb) keep = make_key(srow[j], j) <= tk;
     const uint32_t ball = __ballot_sync(0xffffffffu, keep);
-    if (keep) col_idx[base + written + __popc(ball & ((1u << lane) - 1u))] = j;
+    if (keep) {
+      const int32_t pos = written + __popc(ball & ((1u << lane) - 1u));
+      if (dcheck(pos < cnt, d_status)) col_idx[base + pos] = j;
+    }
     written += __popc(ball);
   }
 }
@@ -469,7 +472,7 @@ sparsp_status_t launch_select(const Dims& s, const float* scores, float top_p, i
   sparsp_status_t r = launch_scan_counts(row_ptr, rows, st);
   if (r != SPARSP_OK) return r;
   const int64_t ctas = (rows + kWarpsPerCta - 1) / kWarpsPerCta;
-  fill_kernel<<<(unsigned)ctas, kWarpsPerCta * 32, 0, st>>>(scores, rows, nb, row_ptr, thr, col_idx);
+  fill_kernel<<<(unsigned)ctas, kWarpsPerCta * 32, 0, st>>>(scores, rows, nb, row_ptr, thr, col_idx, d_status);
   SPARSP_LAUNCH_CHECK();
   return SPARSP_OK;
 }

@@ -264,7 +264,8 @@ SPARSP_API sparsp_status_t sparsp_kv_demand(const sparsp_shape_t* shape, int32_t
  * dem_idx, k, v, kg, vg, gather_cap_blocks and results as the gather there:
  * slot s < min(dem_ptr[B*H*P], gather_cap_blocks) of kg / vg receives the K / V
  * tile dem_idx[s] of its partition's head; a total above gather_cap_blocks
- * sets SPARSP_ERR_CAPACITY. It only reads k, v, dem_ptr and dem_idx and uses no
+ * sets SPARSP_ERR_CAPACITY. A total above B*H*P*nb or an index outside
+ * [0, nb) sets SPARSP_ERR_DATA and is not used. It only reads k, v, dem_ptr and dem_idx and uses no
  * shared memory, so it can run on a second stream beside the attention kernel
  * (which holds almost all of each SM's shared memory); the lists need a small
  * amount of it and do not fit there.

@@ -1,6 +1,7 @@
 """GPU parity of every step against the oracle, element by element, on
 workloads the oracle finishes in seconds (several tiles, ragged item counts,
 both tile sizes, both head dimensions, fp32 and bf16), plus edge cases."""
+import dataclasses
 import math
 import os
 
@@ -162,6 +163,37 @@ def test_select_nan_row_is_empty_and_reported():
     good = np.delete(np.arange(16), [4, 11])
     ref = orc.select(S[good], 0.9, 2)
     assert np.array_equal(np.diff(rp)[good], np.diff(ref.row_ptr))
+
+
+def test_kv_gather_rejects_bad_lists():
+    """Lists handed to sparsp_kv_gather by the caller: an index outside
+    [0, nb) or a total beyond B*H*P*nb is reported (SPARSP_ERR_DATA) and never
+    used as an address; the valid slots are still copied."""
+    wl, data, shape = _setup("r128")
+    ch = OracleChain(wl, data)
+    g = ch.g
+    k, v = dev(ch.kb, wl), dev(ch.vb, wl)
+    good = sp.kv_demand(shape, wl.P, i32(ch.sel.row_ptr), i32(ch.sel.col_idx))
+    torch.cuda.synchronize()
+    total = int(good.dem_ptr[-1].item())
+    dem_idx = good.dem_idx.clone()
+    dem_idx[1] = g.nb + 7                      # out of range
+    dem_idx[2] = -1
+    out = dataclasses.replace(good, kg=torch.zeros((total, g.Bt, g.d), dtype=k.dtype, device="cuda"),
+                              vg=torch.zeros((total, g.Bt, g.d), dtype=k.dtype, device="cuda"), dem_idx=dem_idx)
+    st = status_word()
+    sp.kv_gather(shape, wl.P, out, k, v, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == sp.DATA
+    j0 = int(dem_idx[0].item())
+    assert torch.equal(out.kg[0], k[0, 0, j0 * g.Bt:(j0 + 1) * g.Bt])   # slot 0: partition 0 of head 0
+    assert (out.kg[1] == 0).all() and (out.kg[2] == 0).all()
+    bad_ptr = good.dem_ptr.clone()
+    bad_ptr[-1] = shape.B * shape.H * wl.P * g.nb + 1
+    st2 = status_word()
+    sp.kv_gather(shape, wl.P, dataclasses.replace(out, dem_ptr=bad_ptr, dem_idx=good.dem_idx), k, v, status=st2)
+    torch.cuda.synchronize()
+    assert st2.item() == sp.DATA
 
 
 @pytest.mark.parametrize("name", list(SMALL))
