@@ -155,10 +155,11 @@ __device__ __forceinline__ uint32_t search_start(uint32_t umin, int hb) {
 }
 
 // Top-p cutoff m_p from e_j held in row.ev; *near when a prefix sum around the
-// crossing lies within 1e-6 of Z of the target.
+// crossing lies within 1e-6 of Z of the target. *tstar: the score bits of the
+// m_p-th block; *gt_out: the number of blocks above them.
 template <int E>
 __device__ __forceinline__ int topp_count(const WarpRow<E>& row, uint32_t umin, uint32_t umax, double top_p,
-                                          bool* near) {
+                                          bool* near, uint32_t* tstar, int* gt_out) {
   const uint64_t Zq = row.massq(0u, true);
   const double Z = (double)Zq, target = top_p * Z, band = 1e-6 * Z;
   const float target32 = (float)(top_p * (double)row.mass32(0u));
@@ -198,6 +199,8 @@ __device__ __forceinline__ int topp_count(const WarpRow<E>& row, uint32_t umin, 
     ++k;
   }
   *near = fabs((double)cq - target) < band || fabs((double)cq_prev - target) < band;
+  *tstar = t;
+  *gt_out = gtc;
   return min(row.nb, gtc + k);
 }
 
@@ -237,6 +240,8 @@ count_kernel(const float* __restrict__ S, int64_t rows, int nb, double top_p, in
   umin = __reduce_min_sync(0xffffffffu, umin);
   umax = __reduce_max_sync(0xffffffffu, umax);
   int m_p;
+  uint32_t tp = 0u;   // Top-p: score bits of the m_p-th block and the count above them
+  int gtp = 0;
   if (top_p <= 0.0) {
     m_p = 0;
   } else if (top_p >= 1.0) {
@@ -247,7 +252,7 @@ count_kernel(const float* __restrict__ S, int64_t rows, int nb, double top_p, in
     for (int e = 0; e < E; ++e)
       if (row.valid(e)) row.ev[e] = expf(from_ordered(row.u[e]) - smax);
     bool near = false;
-    m_p = topp_count<E>(row, umin, umax, top_p, &near);
+    m_p = topp_count<E>(row, umin, umax, top_p, &near, &tp, &gtp);
     // e_j is defined as the float32 rounding of exp(S_j - max). expf is within
     // 2 ulp of the exact value, which moves any of these sums (and Z) by at
     // most 3e-7 of Z; only a row whose crossing lies that close to p can decide
@@ -256,18 +261,23 @@ count_kernel(const float* __restrict__ S, int64_t rows, int nb, double top_p, in
 #pragma unroll
       for (int e = 0; e < E; ++e)
         if (row.valid(e)) row.ev[e] = __double2float_rn(exp((double)(from_ordered(row.u[e]) - smax)));
-      m_p = topp_count<E>(row, umin, umax, top_p, &near);
+      m_p = topp_count<E>(row, umin, umax, top_p, &near, &tp, &gtp);
     }
   }
   const int m = min(nb, max(m_p, max(k_floor, 1)));
-  // the m-th block in (score descending, index ascending) order
-  const int hb = search_top_bit(umin, umax);
-  uint32_t t = search_start(umin, hb);
-  for (int bit = hb; bit >= 0; --bit) {
-    const uint32_t cand = t | (1u << bit);
-    if (row.count_ge(cand) >= m) t = cand;
+  // the m-th block in (score descending, index ascending) order: the Top-p
+  // search has found it already unless the floor raised the count
+  uint32_t t = tp;
+  int gt = gtp;
+  if (m != m_p) {
+    const int hb = search_top_bit(umin, umax);
+    t = search_start(umin, hb);
+    for (int bit = hb; bit >= 0; --bit) {
+      const uint32_t cand = t | (1u << bit);
+      if (row.count_ge(cand) >= m) t = cand;
+    }
+    gt = t == 0xffffffffu ? 0 : row.count_ge(t + 1u);
   }
-  const int gt = t == 0xffffffffu ? 0 : row.count_ge(t + 1u);
   const int j = row.kth_tie(t, m - gt);
   if (lane == 0) {
     counts[r] = m;
