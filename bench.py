@@ -344,6 +344,50 @@ class Run:
         return float(busy.max() / busy.mean()) if len(busy) else None
 
 
+def end_to_end(sp, run, steps, work, world=1, barrier=None, replicas=None) -> dict:
+    """The same steps through sp.HostPipeline: every step copies its inputs in
+    from pinned host memory and its outputs (O; and dQ, dK, dV with a
+    backward) back, overlapped with the neighbouring steps' kernels. The timed
+    window includes the first step's uncovered input copy and the last step's
+    output copy."""
+    import torch
+    wl, pipe, host_in, kw = run.wl, run.pipe, run.host_in, run.kw
+    tdt = run.shape.torch_dtype
+    host_out = torch.empty(pipe.o.shape, dtype=tdt).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    if wl.backward:
+        host_grads = [torch.empty(pipe.o.shape, dtype=tdt).pin_memory() for _ in range(3)]
+        d2h += 3 * host_out.numel() * host_out.element_size()
+    hp = sp.HostPipeline(pipe)
+    if wl.backward:
+        def e2e_step():
+            hp.train_step(host_in["q"], host_in["k"], host_in["v"], host_in["do"], host_out, *host_grads, **kw)
+    else:
+        def e2e_step():
+            hp.step(host_in["q"], host_in["k"], host_in["v"], host_out, **kw)
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    if barrier is not None:
+        barrier()
+    stream = run.stream
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    stream.wait_stream(hp.d2h)         # the last result has reached the host
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    if replicas is not None:
+        ms = replicas.max_over_ranks(ms)
+    rate = (replicas.whole_job_rate(work, ms, world) if replicas is not None else work / (ms * 1e-3)) / 1e12
+    return {"value": rate, "unit": "TFLOP/s", "ms_per_step": ms, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "copies": "overlapped with neighbouring steps (HostPipeline)"}
+
+
 def workload_summary(sp, name, args, pk) -> dict:
     """One of the other seeded workloads, in the default configuration: its own
     short timed run (3 warm-ups, min(K, 10) steps), no CPU baseline."""
@@ -379,6 +423,11 @@ def workload_summary(sp, name, args, pk) -> dict:
     out["stages_ms"] = {k: round(v, 5) for k, v in st.items()}
     if wl.skew:
         out["attn_sm_imbalance"] = run.sm_imbalance()
+    if not args.no_e2e:
+        e = end_to_end(sp, run, min(args.steps, 10), f_step)
+        out["e2e_ms_per_step"] = e["ms_per_step"]
+        out["e2e_tflops"] = e["value"]
+        out["e2e_copies_gb_per_step"] = [round(e["h2d_bytes_per_step"] / 1e9, 3), round(e["d2h_bytes_per_step"] / 1e9, 3)]
     del run
     torch.cuda.empty_cache()
     return out
@@ -490,6 +539,11 @@ def main():
                     ("serial" if default_overlap else "overlapped") + "_hbm_stages":
                         hbm_fractions(other_stages, other_bytes, pk["hbm_gbs"])}
 
+    # ---- end to end through the public API: pinned host -> device, step, O -> pinned host
+    # (right after the device-timed steps, before the dense context line's heavy kernels)
+    tdt = shape.torch_dtype
+    e2e = None if args.no_e2e else end_to_end(sp, run, args.steps, f_step, world, barrier, replicas)
+
     # ---- context only: dense attention (PyTorch SDPA) over the same tensors
     BH = shape.B * shape.H
     dense = None
@@ -511,44 +565,6 @@ def main():
                  "kind": "torch SDPA, dense, same Q/K/V (a library baseline of unknown tuning: context only)"}
     except Exception as exc:   # context only: never fails the bench
         dense = {"unavailable": str(exc)[:120]}
-
-    # ---- end to end through the public API: pinned host -> device, step, O -> pinned host
-    tdt = shape.torch_dtype
-    e2e = None
-    if not args.no_e2e:
-        host_in, kw = run.host_in, run.kw
-        host_out = torch.empty(pipe.o.shape, dtype=tdt).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-        d2h = host_out.numel() * host_out.element_size()
-        if wl.backward:
-            host_grads = [torch.empty(pipe.o.shape, dtype=tdt).pin_memory() for _ in range(3)]
-            d2h += 3 * host_out.numel() * host_out.element_size()
-
-        hp = sp.HostPipeline(pipe)
-        if wl.backward:
-            def e2e_step():
-                hp.train_step(host_in["q"], host_in["k"], host_in["v"], host_in["do"], host_out, *host_grads, **kw)
-        else:
-            def e2e_step():
-                hp.step(host_in["q"], host_in["k"], host_in["v"], host_out, **kw)
-
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        stream.wait_stream(hp.d2h)         # the last result has reached the host
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / args.steps
-        e2e_ms = replicas.max_over_ranks(e2e_ms)
-        e2e = {"value": replicas.whole_job_rate(f_step, e2e_ms, world) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "copies": "overlapped with neighbouring steps (HostPipeline)"}
 
     imbalance = run.sm_imbalance()
 
