@@ -428,11 +428,13 @@ def attn_fwd(shape: Shape, q, k, v, row_ptr, col_idx, scale: float = 0.0, o=None
 
 def attn_bwd(shape: Shape, q, k, v, o, lse, dout, row_ptr, col_idx, scale: float = 0.0, dq=None, dk=None,
              dv=None, ws=None, flags: int = 0, prof=None, status=None, stream=None):
-    """Returns (dQ, dK, dV), blocked [B,H,N,d] bf16."""
+    """Returns (dQ, dK, dV), blocked [B,H,N,d] bf16; raster [B,N,H,d] with OUT_RASTER
+    in flags (o is then the raster O of attn_fwd with OUT_RASTER)."""
     dev = q.device
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    dims = (shape.B, shape.N, shape.H, shape.d) if flags & OUT_RASTER else tuple(q.shape)
+    dq = torch.empty(dims, dtype=q.dtype, device=dev) if dq is None else dq
+    dk = torch.empty(dims, dtype=k.dtype, device=dev) if dk is None else dk
+    dv = torch.empty(dims, dtype=v.dtype, device=dev) if dv is None else dv
     if ws is None:
         ws = _empty(attn_workspace_size(shape, True), dev)
     _check("sparsp_attn_bwd", lib().sparsp_attn_bwd(

@@ -529,7 +529,9 @@ sparsp_status_t sparsp_attn_bwd(const sparsp_shape_t* shape, const void* q, cons
   const bool flat = (flags & SPARSP_SCHED_FLAT) != 0;
   typedef const __nv_bfloat16* cb;
   const bool tc = !(flags & SPARSP_KERNEL_PORTABLE) && attn_bwd_tc_supported(s);
-  r = launch_bwd_rowdot(s, (cb)o, (cb)dout, w.delta, lse, tc ? w.lse2 : nullptr, st);
+  const bool raster = (flags & SPARSP_OUT_RASTER) != 0;
+  if (raster && !tc) return SPARSP_ERR_UNSUPPORTED;   // only the tcgen05 kernels write raster rows
+  r = launch_bwd_rowdot(s, (cb)o, (cb)dout, w.delta, lse, tc ? w.lse2 : nullptr, raster, st);
   if (r != SPARSP_OK) return r;
   r = launch_csr_transpose(s, row_ptr, col_idx, w.col_ptr, w.row_idx, d_status, st);
   if (r != SPARSP_OK) return r;
@@ -537,20 +539,22 @@ sparsp_status_t sparsp_attn_bwd(const sparsp_shape_t* shape, const void* q, cons
   if (r != SPARSP_OK) return r;
   if (tc) {
     r = launch_attn_bwd_tc(s, 0, (cb)q, (cb)k, (cb)v, (cb)dout, w.lse2, w.delta, row_ptr, col_idx, scale,
-                           (__nv_bfloat16*)dq, nullptr, w.items, w.counter, prof, d_status, st);
+                           (__nv_bfloat16*)dq, nullptr, w.items, w.counter, prof, d_status, raster, st);
     if (r != SPARSP_OK) return r;
     r = launch_lpt(s, w.col_ptr, flat, w.items2, w.counter + 1, w.hist, st);
     if (r != SPARSP_OK) return r;
     if (!(flags & SPARSP_BWD_SPLIT_KV))
       return launch_attn_bwd_tc(s, 3, (cb)q, (cb)k, (cb)v, (cb)dout, w.lse2, w.delta, w.col_ptr, w.row_idx,
                                 scale, (__nv_bfloat16*)dk, (__nv_bfloat16*)dv, w.items2, w.counter + 1, prof,
-                                d_status, st);
+                                d_status, raster, st);
     r = launch_attn_bwd_tc(s, 1, (cb)q, (cb)k, (cb)v, (cb)dout, w.lse2, w.delta, w.col_ptr, w.row_idx,
-                           scale, (__nv_bfloat16*)dk, nullptr, w.items2, w.counter + 1, prof, d_status, st);
+                           scale, (__nv_bfloat16*)dk, nullptr, w.items2, w.counter + 1, prof, d_status, raster,
+                           st);
     if (r != SPARSP_OK) return r;
     if (cudaMemsetAsync(w.counter + 2, 0, sizeof(int32_t), st) != cudaSuccess) return SPARSP_ERR_CUDA;
     return launch_attn_bwd_tc(s, 2, (cb)q, (cb)k, (cb)v, (cb)dout, w.lse2, w.delta, w.col_ptr, w.row_idx,
-                              scale, (__nv_bfloat16*)dv, nullptr, w.items2, w.counter + 2, prof, d_status, st);
+                              scale, (__nv_bfloat16*)dv, nullptr, w.items2, w.counter + 2, prof, d_status, raster,
+                              st);
   }
   r = launch_attn_bwd_dq(s, (cb)q, (cb)k, (cb)v, (cb)dout, lse, w.delta, row_ptr, col_idx, scale,
                          (__nv_bfloat16*)dq, w.items, w.counter, prof, d_status, st);

@@ -1,8 +1,9 @@
 // Step 5b: block-sparse attention backward (bf16 in, fp32 accumulate), with
 // the selection held fixed.
 //
-//  rowdot_kernel - D = rowsum(dO * O) per query token (fp32), and optionally
-//                  LSE * log2(e) for the tcgen05 backward.
+//  rowdot_kernel - D = rowsum(dO * O) per query token (fp32; O read from block
+//                  or raster order), and optionally LSE * log2(e) for the
+//                  tcgen05 backward.
 //  dq_kernel     - one work item per query block (CSR row): for each selected
 //                  key block, recompute P = exp2(S*log2e*scale - LSE*log2e),
 //                  dP = dO V^T, dS = P (dP - D), dQ += dS K. dQ stays in
@@ -26,15 +27,18 @@ constexpr float kLog2e = 1.4426950408889634f;
 __global__ void __launch_bounds__(256)
 rowdot_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
               int64_t rows, int d, float* __restrict__ delta, const float* __restrict__ lse,
-              float* __restrict__ lse2) {
+              float* __restrict__ lse2, int Bt, int o_raster, RasterMap rm) {
   // 8 threads per row (d <= 128: 16 bf16 each) -> 32 rows per CTA
   const int64_t row = (int64_t)blockIdx.x * 32 + (threadIdx.x >> 3);
   const int sub = threadIdx.x & 7;
   float acc = 0.f;
   if (row < rows) {
+    // the block-order row's O row: the same, or its raster row
+    const int64_t rem = row % rm.N;
+    const int64_t orow = o_raster ? rm.row(row / rm.N, (int)(rem / Bt), (int)(rem % Bt)) : row;
     const int per = d / 8;   // elements per thread: 8 or 16
     for (int c = sub * per; c < (sub + 1) * per; c += 8) {
-      const uint4 a = *reinterpret_cast<const uint4*>(o + row * d + c);
+      const uint4 a = *reinterpret_cast<const uint4*>(o + orow * d + c);
       const uint4 b = *reinterpret_cast<const uint4*>(dout + row * d + c);
       const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
       const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
@@ -395,9 +399,11 @@ sparsp_status_t persistent_grid(const Dims& s, K kern, int threads, int smem, in
 }  // namespace
 
 sparsp_status_t launch_bwd_rowdot(const Dims& s, const __nv_bfloat16* o, const __nv_bfloat16* dout,
-                                  float* delta, const float* lse, float* lse2, cudaStream_t st) {
+                                  float* delta, const float* lse, float* lse2, bool o_raster,
+                                  cudaStream_t st) {
   const int64_t rows = (int64_t)s.B * s.H * s.N;
-  rowdot_kernel<<<(unsigned)((rows + 31) / 32), 256, 0, st>>>(o, dout, rows, s.d, delta, lse, lse2);
+  rowdot_kernel<<<(unsigned)((rows + 31) / 32), 256, 0, st>>>(o, dout, rows, s.d, delta, lse, lse2, s.Bt,
+                                                               o_raster ? 1 : 0, raster_map(s));
   SPARSP_LAUNCH_CHECK();
   return SPARSP_OK;
 }

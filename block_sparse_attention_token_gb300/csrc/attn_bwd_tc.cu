@@ -29,7 +29,8 @@
 // and the dK/dV kernels recompute S (and dP) instead of sharing it so that
 // each fits TMEM. Modes 0-2 are laid out as above; mode 3 as described with it.
 // Sums are taken in a fixed order (no atomics), so results are bitwise
-// reproducible.
+// reproducible. The gradient rows go to block order, or straight to their
+// raster rows (the layout of the inverse reorder) when asked.
 //
 // One persistent CTA per SM, 7 warps (the forward kernel's structure):
 //   warp 4     producer: pulls items longest-first, validates the block list,
@@ -120,6 +121,8 @@ struct Params {
   int32_t* counter;
   uint64_t* prof;
   int32_t* d_status;
+  int raster;            // outputs in raster order at rm.row(bh, block, token); else block order
+  RasterMap rm;
 };
 
 template <int MODE>
@@ -479,8 +482,10 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
       const int i = (int)(item % nb);
       int64_t row = bh * p.N + (int64_t)i * BT + threadIdx.x;
       if (!dcheck(row >= 0 && row < p.rows_total, p.d_status)) row = 0;
-      uint4* orow = reinterpret_cast<uint4*>(p.out + row * D);
-      uint4* orow2 = MODE == 3 ? reinterpret_cast<uint4*>(p.out2 + row * D) : nullptr;
+      int64_t orow_idx = p.raster ? p.rm.row(bh, i, threadIdx.x) : row;
+      if (!dcheck(orow_idx >= 0 && orow_idx < p.rows_total, p.d_status)) orow_idx = 0;
+      uint4* orow = reinterpret_cast<uint4*>(p.out + orow_idx * D);
+      uint4* orow2 = MODE == 3 ? reinterpret_cast<uint4*>(p.out2 + orow_idx * D) : nullptr;
       const int len = ent.y;
       if (len == 0) {
 #pragma unroll
@@ -625,14 +630,14 @@ sparsp_status_t launch_attn_bwd_tc(const Dims& s, int mode, const __nv_bfloat16*
                                    const float* delta, const int32_t* ptr, const int32_t* idx,
                                    float scale, __nv_bfloat16* out, __nv_bfloat16* out2,
                                    const int32_t* items, int32_t* counter, uint64_t* prof, int32_t* d_status,
-                                   cudaStream_t st) {
+                                   bool raster, cudaStream_t st) {
   const uint64_t rows = (uint64_t)s.B * s.H * s.N;
   CUtensorMap tq, tk, tv, tdo;
   if (!make_tmap_bf16_rows(&tq, q, rows, D, BT) || !make_tmap_bf16_rows(&tk, k, rows, D, BT) ||
       !make_tmap_bf16_rows(&tv, v, rows, D, BT) || !make_tmap_bf16_rows(&tdo, dout, rows, D, BT))
     return SPARSP_ERR_CUDA;
   Params prm{ptr, idx, s.N, s.nb, s.rows(), (int64_t)rows, scale * 1.4426950408889634f, mode == 2 ? 1.0f : scale,
-             lse2, delta, out, out2, 1.0f, items, counter, prof, d_status};
+             lse2, delta, out, out2, 1.0f, items, counter, prof, d_status, raster ? 1 : 0, raster_map(s)};
   if (mode == 0) return go<0>(s, tq, tdo, tk, tv, prm, st);
   if (mode == 1) return go<1>(s, tk, tv, tq, tdo, prm, st);
   if (mode == 3) return go<3>(s, tk, tv, tq, tdo, prm, st);

@@ -150,9 +150,10 @@ struct Params {
   float scale_log2;
   __nv_bfloat16* o;
   float* lse;
-  // raster output: O row (b, h, token) at ((b*N + n)*H + h)*d with n the token's
-  // raster index (t slowest, x fastest); otherwise block order like Q
-  int raster, H, Y, X, ta, tb, tc, nY, nX;
+  // raster output: O rows at rm.row(bh, block, token) (the layout of the inverse
+  // reorder); otherwise block order like Q
+  int raster;
+  RasterMap rm;
   const int32_t* items;
   int32_t* counter;
   uint64_t* prof;
@@ -544,14 +545,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       const int64_t row = bh * p.N + (int64_t)i * BT + o;
       bool stores = o < BT && i < nb && !((badbits >> half) & 1);
       int64_t orow_idx = row;
-      if (p.raster && stores) {
-        const int tbc = p.tb * p.tc;
-        const int bx = i % p.nX, by = (i / p.nX) % p.nY, bt = i / (p.nX * p.nY);
-        const int it = o / tbc, iy = (o - it * tbc) / p.tc, ix = o - it * tbc - iy * p.tc;
-        const int64_t n = ((int64_t)bt * p.ta + it) * p.Y * p.X + ((int64_t)by * p.tb + iy) * p.X +
-                          (int64_t)bx * p.tc + ix;
-        orow_idx = ((bh / p.H) * p.N + n) * p.H + bh % p.H;
-      }
+      if (p.raster && stores) orow_idx = p.rm.row(bh, i, o);
       // this group stores columns [32*grp, 32*grp + 32) of the row
       if (stores) stores = dcheck(row < p.rows_total && orow_idx >= 0 && orow_idx < p.rows_total, p.d_status);
       uint4* orow = reinterpret_cast<uint4*>(p.o + orow_idx * D) + grp * 4;
@@ -711,15 +705,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         // rows past the block (or past the last block of a pair) are computed, never stored
         bool stores = o < BT && i < nb && !((badbits >> half) & 1);
         int64_t orow_idx = row;
-        if (p.raster && stores) {
-          // tile i = (bt, by, bx) block-raster; token o = (it, iy, ix) raster inside the tile
-          const int tbc = p.tb * p.tc;
-          const int bx = i % p.nX, by = (i / p.nX) % p.nY, bt = i / (p.nX * p.nY);
-          const int it = o / tbc, iy = (o - it * tbc) / p.tc, ix = o - it * tbc - iy * p.tc;
-          const int64_t n = ((int64_t)bt * p.ta + it) * p.Y * p.X + ((int64_t)by * p.tb + iy) * p.X +
-                            (int64_t)bx * p.tc + ix;
-          orow_idx = ((bh / p.H) * p.N + n) * p.H + bh % p.H;
-        }
+        if (p.raster && stores) orow_idx = p.rm.row(bh, i, o);
         if (stores) stores = dcheck(row < p.rows_total && orow_idx >= 0 && orow_idx < p.rows_total, p.d_status);
         uint4* orow = reinterpret_cast<uint4*>(p.o + orow_idx * D);
         if (len == 0) {
@@ -902,7 +888,7 @@ sparsp_status_t launch_attn_fwd_tc(const Dims& s, const __nv_bfloat16* q, const 
   // over the pair rows (attn_fwd_tc_items)
   const int nbp = attn_fwd_tc_items_per_head(s);
   Params prm{row_ptr, col_idx, s.N, s.nb, nbp, (int64_t)s.B * s.H * nbp, (int64_t)rows, scale * 1.4426950408889634f, o, lse,
-             raster ? 1 : 0, s.H, s.Y, s.X, s.ta, s.tb, s.tc, s.nY, s.nX, items, counter, prof, d_status};
+             raster ? 1 : 0, raster_map(s), items, counter, prof, d_status};
   if (s.Bt == 128 && s.d == 128) return go_fwd<128, 128>(s, tq, tk, tv, prm, st);
   if (s.Bt == 128 && s.d == 64) return go_fwd<128, 64>(s, tq, tk, tv, prm, st);
   if (s.Bt == 64 && s.d == 128) return go_fwd<64, 128>(s, tq, tk, tv, prm, st);

@@ -28,6 +28,25 @@ struct Dims {
   int64_t rows() const { return (int64_t)B * H * nb; }  // CSR rows = work items
 };
 
+// Where token o of tile i of head bh (b = bh / H, h = bh % H) sits in a
+// raster [B, N, H, d] tensor: tile i = (bt, by, bx) in tile-raster order, token
+// o = (it, iy, ix) in raster order inside the tile; the position is
+// n = (bt*ta + it)*Y*X + (by*tb + iy)*X + bx*tc + ix and the row (b*N + n)*H + h.
+// This is the map of sparsp_reorder, for kernels that read or write raster rows
+// themselves.
+struct RasterMap {
+  int64_t N;
+  int H, Y, X, ta, tb, tc, nY, nX;
+  __device__ __forceinline__ int64_t row(int64_t bh, int i, int o) const {
+    const int tbc = tb * tc;
+    const int bx = i % nX, by = (i / nX) % nY, bt = i / (nX * nY);
+    const int it = o / tbc, iy = (o - it * tbc) / tc, ix = o - it * tbc - iy * tc;
+    const int64_t n = ((int64_t)bt * ta + it) * Y * X + ((int64_t)by * tb + iy) * X + (int64_t)bx * tc + ix;
+    return ((bh / H) * N + n) * H + bh % H;
+  }
+};
+inline RasterMap raster_map(const Dims& s) { return RasterMap{s.N, s.H, s.Y, s.X, s.ta, s.tb, s.tc, s.nY, s.nX}; }
+
 // A persistent kernel's grid: `g` CTAs, at most one per work item and at most
 // the caller's cap (SPARSP_GRID_CAP), never fewer than one.
 inline int64_t cap_grid(const Dims& s, int64_t g, int64_t n_items) {
@@ -169,8 +188,10 @@ sparsp_status_t launch_attn_fwd_tc(const Dims& s, const __nv_bfloat16* q, const 
                                    uint64_t* prof, int32_t* d_status, cudaStream_t st);
 
 // Attention backward pieces.
+// D = rowsum(dO * O) per block-order row (o in raster order when o_raster)
 sparsp_status_t launch_bwd_rowdot(const Dims& s, const __nv_bfloat16* o, const __nv_bfloat16* dout,
-                                  float* delta, const float* lse, float* lse2, cudaStream_t st);
+                                  float* delta, const float* lse, float* lse2, bool o_raster,
+                                  cudaStream_t st);
 // tcgen05 backward (bf16, Bt = d = 128). mode 0: dQ over the CSR rows;
 // mode 1: dK, mode 2: dV, mode 3: dK (out) and dV (out2) over the transposed
 // CSR. `lse2` = LSE * log2(e).
@@ -181,7 +202,7 @@ sparsp_status_t launch_attn_bwd_tc(const Dims& s, int mode, const __nv_bfloat16*
                                    const float* delta, const int32_t* ptr, const int32_t* idx,
                                    float scale, __nv_bfloat16* out, __nv_bfloat16* out2,
                                    const int32_t* items, int32_t* counter, uint64_t* prof, int32_t* d_status,
-                                   cudaStream_t st);
+                                   bool raster, cudaStream_t st);
 sparsp_status_t launch_attn_bwd_dq(const Dims& s, const __nv_bfloat16* q, const __nv_bfloat16* k,
                                    const __nv_bfloat16* v, const __nv_bfloat16* dout,
                                    const float* lse, const float* delta, const int32_t* row_ptr,

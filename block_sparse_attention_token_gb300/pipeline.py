@@ -4,9 +4,11 @@ forward(): reorder Q, K, V into tiles -> block scores -> Top-p/Top-k selection
 -> (optional) head balancing over P virtual ranks and slack-aware augmentation
 of the CSR -> (optional) dependency-aware placement of blocks on the P
 partitions -> KV demand of P partitions (+ gather) -> block-sparse attention
--> O back to raster order. backward(): dO into tiles -> attention backward -> dQ, dK, dV
-back to raster order. Every step is one or more libsparsp kernels on the
-current stream, except that by default the KV demand gather runs on a side
+-> O in raster order (written there by attention itself where the tcgen05
+kernel runs, else by an inverse reorder). backward(): dO into tiles ->
+attention backward -> dQ, dK, dV in raster order (likewise). Every step is one
+or more libsparsp kernels on the current stream, except that by default the
+KV demand gather runs on a side
 stream beside attention (the caller's stream waits for both); nothing here
 allocates after construction.
 """
@@ -41,10 +43,11 @@ class Pipeline:
 
     def kernels_per_backward(self) -> int:
         """reorder dO, rowdot, CSR transpose, schedule, dQ, schedule, dK + dV (one
-        kernel, two with BWD_SPLIT_KV), 3 inverse reorders."""
+        kernel, two with BWD_SPLIT_KV), 3 inverse reorders (none when the
+        backward writes raster gradients)."""
         lpt = 2 if self.flags & 1 else 1
         kv = 2 if self.flags & 4 else 1
-        return 1 + 1 + 1 + lpt + 1 + lpt + kv + 3
+        return 1 + 1 + 1 + lpt + 1 + lpt + kv + (0 if self.raster_out else 3)
 
     def __init__(self, shape: Shape, estimator: str, top_p: float, k_floor: int, P: int, rank: int = 16,
                  gather: bool = True, flags: int = 0, backward: bool = False, device="cuda",
@@ -67,7 +70,7 @@ class Pipeline:
         dt = s.torch_dtype
         dev = torch.device(device)
         blocked = (s.B, s.H, s.N, s.d)
-        self.qb, self.kb, self.vb, self.ob = (torch.empty(blocked, dtype=dt, device=dev) for _ in range(4))
+        self.qb, self.kb, self.vb = (torch.empty(blocked, dtype=dt, device=dev) for _ in range(3))
         self.o = torch.empty((s.B, s.N, s.H, s.d), dtype=dt, device=dev)
         self.lse = torch.empty((s.B, s.H, s.N), dtype=torch.float32, device=dev)
         self.scores = torch.empty((s.B, s.H, s.nb, s.nb), dtype=torch.float32, device=dev)
@@ -100,13 +103,16 @@ class Pipeline:
             self.gwq, self.gwk = (torch.empty((s.H, s.d, rank), dtype=torch.float32, device=dev) for _ in range(2))
             self.ws_pred = torch.empty(max(lib().sparsp_predictor_workspace_size(ctypes.byref(s), rank), 16),
                                        dtype=torch.uint8, device=dev)
-        # forward-only steps on the tcgen05 kernel take O straight into raster order (the
-        # backward needs it in block order)
-        # (64-token blocks with d = 128 beyond 1,024 blocks run the portable kernel,
-        # which writes block order only)
-        self.raster_out = (not backward and s.torch_dtype == torch.bfloat16 and not (flags & 2)
-                           and s.Bt in (64, 128) and s.d in (64, 128)
-                           and not (s.Bt == 64 and s.d == 128 and s.nb > 1024))
+        # the tcgen05 forward takes O straight into raster order (64-token blocks with
+        # d = 128 beyond 1,024 blocks run the portable kernel, which writes block
+        # order only); with a backward, only where the tcgen05 backward (Bt = d = 128)
+        # also reads raster O and writes raster dQ, dK, dV
+        fwd_raster = (s.torch_dtype == torch.bfloat16 and not (flags & 2) and s.Bt in (64, 128)
+                      and s.d in (64, 128) and not (s.Bt == 64 and s.d == 128 and s.nb > 1024))
+        self.raster_out = fwd_raster and (not backward or (s.Bt == 128 and s.d == 128))
+        self._o_fwd = None   # the buffer forward() last wrote O to (read by backward() when raster)
+        # block-order O (and gradients) only where attention does not write raster rows
+        self.ob = None if self.raster_out else torch.empty(blocked, dtype=dt, device=dev)
         self.overlap_demand = overlap_demand
         if overlap_demand:
             lo, hi = torch.cuda.Stream.priority_range()   # least, greatest
@@ -136,7 +142,9 @@ class Pipeline:
         self.prof = torch.zeros(PROF_SLOTS, dtype=torch.int64, device=dev)
         if backward:
             self.dob = torch.empty(blocked, dtype=dt, device=dev)
-            self.dqb, self.dkb, self.dvb = (torch.empty(blocked, dtype=dt, device=dev) for _ in range(3))
+            self.dqb = self.dkb = self.dvb = None
+            if not self.raster_out:
+                self.dqb, self.dkb, self.dvb = (torch.empty(blocked, dtype=dt, device=dev) for _ in range(3))
             self.dq, self.dk, self.dv = (torch.empty((s.B, s.N, s.H, s.d), dtype=dt, device=dev)
                                          for _ in range(3))
 
@@ -218,19 +226,30 @@ class Pipeline:
         if not self.raster_out:
             reorder(s, self.ob, o, inverse=True)
             mark("reorder_out")
+        self._o_fwd = o
         return o, self.lse
 
     def backward(self, dout, prof: bool = False, mark=None, outs=None):
-        """outs: optional raster (dQ, dK, dV) output buffers (default: self.dq, self.dk, self.dv)."""
+        """outs: optional raster (dQ, dK, dV) output buffers (default: self.dq, self.dk, self.dv).
+        With raster_out the backward reads O from the buffer the last forward()
+        wrote it to, which must still hold it, and writes the gradients' raster
+        rows itself."""
         s = self.shape
         mark = mark or (lambda name: None)
         reorder(s, dout, self.dob)
         mark("reorder_dout")
         rp, ci = self.csr
+        dq, dk, dv = (self.dq, self.dk, self.dv) if outs is None else outs
+        if self.raster_out:
+            if self._o_fwd is None:
+                raise RuntimeError("backward() needs a forward() first")
+            attn_bwd(s, self.qb, self.kb, self.vb, self._o_fwd, self.lse, self.dob, rp, ci, 0.0, dq, dk, dv,
+                     self.ws_attn, self.flags | OUT_RASTER, self.prof if prof else None, self.status)
+            mark("attn_bwd")
+            return dq, dk, dv
         attn_bwd(s, self.qb, self.kb, self.vb, self.ob, self.lse, self.dob, rp, ci, 0.0,
                  self.dqb, self.dkb, self.dvb, self.ws_attn, self.flags, self.prof if prof else None, self.status)
         mark("attn_bwd")
-        dq, dk, dv = (self.dq, self.dk, self.dv) if outs is None else outs
         reorder(s, self.dqb, dq, inverse=True)
         reorder(s, self.dkb, dk, inverse=True)
         reorder(s, self.dvb, dv, inverse=True)

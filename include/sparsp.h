@@ -104,7 +104,11 @@ enum {
    * order. Only the tcgen05 kernel (bf16 on sm_103a, Bt and d in {64, 128},
    * nb <= 1024 when Bt = 64 and d = 128, without SPARSP_KERNEL_PORTABLE) does
    * this; elsewhere the call returns SPARSP_ERR_UNSUPPORTED before enqueuing
-   * anything. */
+   * anything.
+   * Backward: o is read in raster order (as the forward wrote it with this
+   * option) and dq, dk, dv are written in raster order; q, k, v, dout and lse
+   * stay in block order (the kernels read them as tiles). Only the tcgen05
+   * backward (Bt = d = 128) does this; elsewhere SPARSP_ERR_UNSUPPORTED. */
   SPARSP_OUT_RASTER = 1u << 3
 };
 /* Attention kernels: at most n persistent CTAs (1 <= n <= 4095) instead of
@@ -417,7 +421,8 @@ SPARSP_API sparsp_status_t sparsp_attn_fwd(const sparsp_shape_t* shape, const vo
  * Gradients of sum(dO * O) with O from sparsp_attn_fwd (its o and lse):
  *   D = rowsum(dO * O); P = exp(scale QK^T - LSE) on the selected blocks;
  *   dV = P^T dO; dS = P * (dO V^T - D); dQ = scale dS K; dK = scale dS^T Q.
- * bf16 only. dq, dk, dv: blocked [B,H,N,d] bf16. dQ is accumulated per query
+ * bf16 only. dq, dk, dv: blocked [B,H,N,d] bf16 (raster [B,N,H,d], and o
+ * raster too, with SPARSP_OUT_RASTER). dQ is accumulated per query
  * block over its CSR row and dK/dV per key block over the transposed CSR, so
  * the result is deterministic (no atomics on values). On tcgen05 one kernel
  * computes dQ and one both dK and dV (two with SPARSP_BWD_SPLIT_KV).

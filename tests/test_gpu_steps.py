@@ -800,6 +800,38 @@ def test_attn_bwd(name):
     compare_values(host(dv3), dV, wl, "dV (two kernels)")
 
 
+@pytest.mark.parametrize("split", [False, True])
+@pytest.mark.parametrize("name", ["r128", "wave", "r64", "r128d64"])
+def test_attn_bwd_raster_output(name, split):
+    """With OUT_RASTER the backward reads the raster O the forward wrote and
+    writes dQ, dK, dV straight into raster order: bit for bit the inverse
+    reorder of the block-ordered gradients. Shapes without the tcgen05
+    backward refuse the flag before enqueuing anything."""
+    wl, data, shape = _setup(name)
+    ch = OracleChain(wl, data)
+    dob = orc.reorder(synth.round_bf16(np.random.default_rng(wl.seed + 101).standard_normal(
+        data["q"].shape, dtype=np.float32)), ch.g)
+    q, k, v, do = dev(ch.qb, wl), dev(ch.kb, wl), dev(ch.vb, wl), dev(dob, wl)
+    rp, ci = i32(ch.sel.row_ptr), i32(ch.sel.col_idx)
+    st = status_word()
+    extra = sp.BWD_SPLIT_KV if split else 0
+    o, lse = sp.attn_fwd(shape, q, k, v, rp, ci, status=st)
+    if shape.Bt != 128 or shape.d != 128:
+        o_r = sp.reorder(shape, o, inverse=True)
+        with pytest.raises(sp.SparspError):
+            sp.attn_bwd(shape, q, k, v, o_r, lse, do, rp, ci, flags=sp.OUT_RASTER | extra)
+        return
+    o_r, lse_r = sp.attn_fwd(shape, q, k, v, rp, ci, flags=sp.OUT_RASTER, status=st)
+    grads = sp.attn_bwd(shape, q, k, v, o, lse, do, rp, ci, flags=extra, status=st)
+    raster = sp.attn_bwd(shape, q, k, v, o_r, lse_r, do, rp, ci, flags=sp.OUT_RASTER | extra, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    for a, b, what in zip(grads, raster, ("dQ", "dK", "dV")):
+        assert torch.equal(sp.reorder(shape, a, inverse=True), b), f"{what} in raster order differs"
+    with pytest.raises(sp.SparspError):
+        sp.attn_bwd(shape, q, k, v, o_r, lse_r, do, rp, ci, flags=sp.OUT_RASTER | sp.KERNEL_PORTABLE)
+
+
 @pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("name", ["tiny", "medium", "r128", "wave"])
 def test_pipeline_end_to_end(name, fused):
