@@ -1,13 +1,15 @@
 // Step 3: Top-p routing with a Top-k floor, compacted into a per-head CSR.
 //
 // Three launches, no atomics on data, deterministic:
-//  1. count_kernel  - one warp per row (one CTA per row beyond 1,024 blocks,
-//     count_row_kernel): bitonic sort of 64-bit keys
-//     (score descending as an order-preserving integer, then block index) held
-//     in registers and exchanged with shuffles; e_j = exp(S_j - max) rounded
-//     to fp32 (expf, or the correctly rounded value for rows whose Top-p
-//     crossing lies within 1e-6 of p); Z and the prefix masses in fp64;
-//     m = min(nb, max(m_p, k_floor, 1)).
+//  1. count_kernel  - one warp per row, without sorting: bitwise searches over
+//     the order-preserving score bits find the Top-p cutoff and the m-th
+//     block in the order (score descending, block index ascending); beyond
+//     1,024 blocks one CTA per row (count_row_kernel) sorts the 64-bit keys
+//     (score bits, then index) with a bitonic network in shared memory.
+//     e_j = exp(S_j - max) rounded to fp32 (expf, or the correctly rounded
+//     value for rows whose Top-p crossing lies within 1e-6 of p); Z and the
+//     prefix masses as exact 64-bit fixed-point sums (float64 in the
+//     CTA-per-row kernel); m = min(nb, max(m_p, k_floor, 1)).
 //     Writes m into row_ptr[row] and the key of the m-th kept block into ws.
 //  2. scan          - exclusive scan of the counts -> row_ptr.
 //  3. fill_kernel   - one warp per row: block j is kept iff its key <= the
@@ -59,7 +61,8 @@ __device__ __forceinline__ float key_score(uint64_t key) {
 //  - the m-th block (m = min(nb, max(m_p, k_floor, 1))): the largest t with
 //    #(u >= t) >= m, then the (m - #(u > t))-th of its ties by index.
 // e_j = expf(s_j - max) in fp32 (correctly rounded instead for a row whose
-// crossing lies within 1e-6 of p). The t* search runs on fp32 sums; t* and
+// crossing lies within 1e-6 of p). The t* search runs on coarse integer sums
+// (e_j truncated to 21-24 fraction bits, one warp reduction per step); t* and
 // the tie count are then decided on exact sums of e_j in 64-bit fixed point
 // (resolution 2^-52, each term truncated by less than that: for nb <= 1024
 // the sums lie within 4e-13 of Z of float64 sums of the same values in any
@@ -79,8 +82,12 @@ __device__ __forceinline__ uint64_t to_fix(float e) {
 
 template <int E>
 struct WarpRow {
+  // the steering sums: e_j (<= 1) in units of 2^-kSteerBits, truncated, so that
+  // the sum of all 32*E of them fits 31 bits and one integer warp reduction adds them
+  static constexpr int kSteerBits = E <= 2 ? 24 : (E <= 8 ? 23 : (E <= 16 ? 22 : 21));
   uint32_t u[E];
   float ev[E];
+  uint32_t es[E];   // e_j * 2^kSteerBits, truncated
   int nb, lane;
 
   __device__ __forceinline__ bool valid(int e) const { return e * 32 + lane < nb; }
@@ -92,15 +99,17 @@ struct WarpRow {
     for (int e = 0; e < E; ++e) c += (valid(e) && u[e] >= t) ? 1 : 0;
     return (int)__reduce_add_sync(0xffffffffu, (unsigned)c);
   }
-  // fp32 mass of the blocks with u >= t (warp total; only steers the search)
-  __device__ __forceinline__ float mass32(uint32_t t) const {
-    float m = 0.f;
+  // coarse mass of the blocks with u >= t (warp total, in units of 2^-kSteerBits;
+  // only steers the search)
+  __device__ __forceinline__ uint32_t mass_steer(uint32_t t) const {
+    uint32_t m = 0u;
 #pragma unroll
-    for (int e = 0; e < E; ++e)
-      if (valid(e) && u[e] >= t) m += ev[e];
+    for (int e = 0; e < E; ++e) m += u[e] >= t ? es[e] : 0u;   // es = 0 past nb
+    return __reduce_add_sync(0xffffffffu, m);
+  }
+  __device__ __forceinline__ void set_steer() {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m += __shfl_xor_sync(0xffffffffu, m, off);
-    return m;
+    for (int e = 0; e < E; ++e) es[e] = valid(e) ? (uint32_t)(ev[e] * (float)(1u << kSteerBits)) : 0u;
   }
   // exact fixed-point mass of the blocks with u >= t (ge) or u > t (!ge)
   __device__ __forceinline__ uint64_t massq(uint32_t t, bool ge) const {
@@ -161,22 +170,27 @@ template <int E>
 __device__ __forceinline__ int topp_count(const WarpRow<E>& row, uint32_t umin, uint32_t umax, double top_p,
                                           bool* near, uint32_t* tstar, int* gt_out) {
   const uint64_t Zq = row.massq(0u, true);
+  // the target p*Z and its 1e-6*Z band in the same fixed point, once per row
+  // (float64 is slow on this GPU: every comparison below is on integers). For
+  // an integer sum x, x >= p*Z exactly when x >= ceil(p*Z).
   const double Z = (double)Zq, target = top_p * Z, band = 1e-6 * Z;
-  const float target32 = (float)(top_p * (double)row.mass32(0u));
+  const uint64_t Tq = (uint64_t)ceil(target);
+  const uint64_t near_lo = (uint64_t)fmax(floor(target - band), 0.0), near_hi = (uint64_t)ceil(target + band);
+  const uint32_t target_s = (uint32_t)((float)top_p * (float)row.mass_steer(0u));
   const int hb = search_top_bit(umin, umax);
   uint32_t t = search_start(umin, hb);
   for (int bit = hb; bit >= 0; --bit) {
     const uint32_t cand = t | (1u << bit);
-    if (row.mass32(cand) >= target32) t = cand;
+    if (row.mass_steer(cand) >= target_s) t = cand;
   }
   // exact: M(t) >= target > M(> t), with t a score of the row
   uint64_t ge = 0ull, gt = 0ull;
   for (int step = 0; step <= 2 * row.nb; ++step) {
     ge = row.massq(t, true);
     gt = row.massq(t, false);
-    if ((double)ge < target) {
+    if (ge < Tq) {
       t = row.below(t);          // exists: M(umin) = Z >= target
-    } else if ((double)gt >= target) {
+    } else if (gt >= Tq) {
       t = row.above(t);          // exists: M(> umax) = 0 < target
     } else {
       break;
@@ -193,19 +207,22 @@ __device__ __forceinline__ int topp_count(const WarpRow<E>& row, uint32_t umin, 
   const uint64_t etq = to_fix(et);
   uint64_t cq = gt + etq, cq_prev = gt;
   int k = 1;
-  while ((double)cq < target && k < eq) {
+  while (cq < Tq && k < eq) {
     cq_prev = cq;
     cq += etq;
     ++k;
   }
-  *near = fabs((double)cq - target) < band || fabs((double)cq_prev - target) < band;
+  *near = (cq > near_lo && cq < near_hi) || (cq_prev > near_lo && cq_prev < near_hi);
   *tstar = t;
   *gt_out = gtc;
   return min(row.nb, gtc + k);
 }
 
+// Up to 512 blocks a row: registers capped for four CTAs (32 warps) per SM,
+// so that a whole wave of rows hides the search's reduction latencies
+// (measured faster than 80-128 registers at two or three CTAs).
 template <int E>   // blocks per lane; nb <= 32*E
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
+__global__ void __launch_bounds__(kWarpsPerCta * 32, E <= 16 ? 4 : 1)
 count_kernel(const float* __restrict__ S, int64_t rows, int nb, double top_p, int k_floor,
              int32_t* __restrict__ counts, uint64_t* __restrict__ thr, int32_t* d_status) {
   const int lane = threadIdx.x & 31;
@@ -251,6 +268,7 @@ count_kernel(const float* __restrict__ S, int64_t rows, int nb, double top_p, in
 #pragma unroll
     for (int e = 0; e < E; ++e)
       if (row.valid(e)) row.ev[e] = expf(from_ordered(row.u[e]) - smax);
+    row.set_steer();
     bool near = false;
     m_p = topp_count<E>(row, umin, umax, top_p, &near, &tp, &gtp);
     // e_j is defined as the float32 rounding of exp(S_j - max). expf is within
@@ -261,6 +279,7 @@ count_kernel(const float* __restrict__ S, int64_t rows, int nb, double top_p, in
 #pragma unroll
       for (int e = 0; e < E; ++e)
         if (row.valid(e)) row.ev[e] = __double2float_rn(exp((double)(from_ordered(row.u[e]) - smax)));
+      row.set_steer();
       m_p = topp_count<E>(row, umin, umax, top_p, &near, &tp, &gtp);
     }
   }
