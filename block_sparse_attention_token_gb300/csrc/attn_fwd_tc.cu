@@ -13,10 +13,13 @@
 // selections differ ("Dynamic Sparsity in Large-Scale Video DiT Training",
 // "How DSV works": queries grouped so that one key set serves several).
 //
-// One persistent CTA per SM; for d = 128, 7 warps (4 softmax warps, then the
-// producer, the S issuer and the PV issuer), for d = 64, 11 warps (8 softmax
-// warps in two groups, one per 64-column half of a stage, each with its own
-// running max, sum and O accumulator, combined once per item; see Cfg::SPLIT):
+// Persistent CTAs: one per SM with 7 warps (4 softmax warps, then the
+// producer, the S issuer and the PV issuer) for d = 128; one per SM with 11
+// warps (8 softmax warps in two groups, one per 64-column half of a stage,
+// each with its own running max, sum and O accumulator, combined once per
+// item; see Cfg::SPLIT) for 128-token blocks with d = 64; two per SM, each with
+// 7 warps and half of the TMEM and shared memory (one S and one P buffer; see
+// Cfg::DUO), for 64-token blocks with d = 64:
 //   producer: pulls items longest-first through an atomic counter,
 //              validates the CSR row(s), publishes the item in a shared-memory
 //              ring (for pairs with the two rows as bitmaps), and TMA-loads the
@@ -44,8 +47,9 @@
 //              memory, LSE = (m + log2 l) ln 2 (O = 0, LSE = -inf for a row
 //              that attended to nothing). A warp's 32 rows belong to one query
 //              block, so the masks of a pair are warp-uniform.
-// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256,384) (d = 64: O_a
-// [256,320) and O_b [320,384)), P0 [384,448), P1 [448,512). Every mbarrier wait is bounded (2 s); on expiry the CTA sets
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256,384) (SPLIT: O_a
+// [256,320) and O_b [320,384)), P0 [384,448), P1 [448,512); DUO (256 columns
+// per CTA): S [0,128), O [128,192), P [192,256). Every mbarrier wait is bounded (2 s); on expiry the CTA sets
 // SPARSP_ERR_TIMEOUT, all roles leave their loops, copies and MMAs in flight
 // are drained with a second bounded wait, and TMEM is released.
 #include "tc_helpers.cuh"
@@ -55,8 +59,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kMaxStages = 6, kNI = 4;   // K / V ring depth <= kMaxStages (Cfg::NK)
-constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+constexpr int kMaxStages = 6, kNI = 4;   // K / V ring depth <= kMaxStages (Cfg::NK); item ring <= kNI
 enum Bar {
   Q_FULL = 0, Q_EMPTY, K_FULL, K_EMPTY = K_FULL + kMaxStages, V_FULL = K_EMPTY + kMaxStages,
   V_EMPTY = V_FULL + kMaxStages, S_FULL = V_EMPTY + kMaxStages, S_FREE = S_FULL + 2, P_FULL = S_FREE + 2, PV_DONE = P_FULL + 2, O_FULL = PV_DONE + 2,
@@ -72,18 +75,30 @@ template <int BT_, int D_>
 struct Cfg {
   static constexpr int BT = BT_, D = D_, QR = 128, KR = 128;
   static constexpr bool PAIR = BT == 64;
-  // d = 64: two softmax warpgroups, one per 64-column half of a stage, each
-  // with its own running max, sum and O accumulator (TMEM O_a [256,320),
-  // O_b [320,384)), combined once per item. Two softmax warps per SM
-  // sub-partition hide each other's latencies.
-  static constexpr bool SPLIT = D == 64;
+  // 64-token blocks with d = 64: two CTAs per SM, each with half of the TMEM
+  // (one S buffer [0,128), O [128,192), one P buffer [192,256)) and half of
+  // the shared memory (3 K and 2 V stages), so that one CTA's softmax runs
+  // while the other's MMAs keep the tensor pipe busy. A softmax row goes in
+  // two passes over 64-column halves (the maximum, then the exponentials) to
+  // fit the registers two CTAs leave a thread.
+  static constexpr bool DUO = BT == 64 && D == 64;
+  // 128-token blocks with d = 64: two softmax warpgroups, one per 64-column
+  // half of a stage, each with its own running max, sum and O accumulator
+  // (TMEM O_a [256,320), O_b [320,384)), combined once per item. Two softmax
+  // warps per SM sub-partition hide each other's latencies.
+  static constexpr bool SPLIT = D == 64 && !DUO;
   static constexpr int NSM = SPLIT ? 8 : 4;               // softmax warps
   static constexpr int THREADS = 32 * (NSM + 3);           // + producer, S issuer, PV issuer
   static constexpr int W_PROD = NSM, W_S = NSM + 1, W_PV = NSM + 2;
   // K and V ring stages: 3 fit beside a d = 128 query tile; with d = 64 the
   // tiles are half the size and 6 stages keep more L2 loads in flight (a stage
   // then takes half the tensor time, so the same latency needs twice the depth)
-  static constexpr int NK = D == 64 ? 6 : 3, NV = NK;
+  static constexpr int NK = DUO ? 3 : (D == 64 ? 6 : 3), NV = DUO ? 2 : NK;
+  static constexpr int NSB = DUO ? 1 : 2, NPB = DUO ? 1 : 2;   // S and P buffers in TMEM
+  static constexpr int NI = DUO ? 2 : kNI;                      // item ring slots
+  static constexpr int kMinCtas = DUO ? 2 : 1;                  // CTAs per SM
+  static constexpr uint32_t kColS = 0, kColO = DUO ? 128 : 256, kColP = DUO ? 192 : 384;
+  static constexpr uint32_t kTmemCols = DUO ? 256 : 512;
   // bitmap words of one CSR row in the item ring (pairs): up to kMaxBlocks
   // blocks, except for d = 128 whose tiles leave room for 1,024 blocks only
   // (larger shapes run the portable kernel, see attn_fwd_tc_supported)
@@ -93,13 +108,13 @@ struct Cfg {
   static constexpr uint32_t kQTile = kQBox * NBOX, kKTile = kKBox * NBOX;
   static constexpr uint32_t kOffK = kQTile, kOffV = kOffK + NK * kKTile, kOffBar = kOffV + NV * kKTile;
   static constexpr uint32_t kOffRing = kOffBar + 8 * NBAR;
-  static constexpr uint32_t kOffBits = kOffRing + 16 * kNI;
-  static constexpr uint32_t kBitsBytes = PAIR ? kNI * 2 * MAXW * 4 : 0;
+  static constexpr uint32_t kOffBits = kOffRing + 16 * NI;
+  static constexpr uint32_t kBitsBytes = PAIR ? NI * 2 * MAXW * 4 : 0;
   static constexpr uint32_t kOffStat = kOffBits + kBitsBytes;   // [2 parities][2 groups][128 rows] (m, l)
   static constexpr uint32_t kStatBytes = SPLIT ? 2 * 2 * 128 * 8 : 0;
   static constexpr uint32_t kOffMisc = kOffStat + kStatBytes;
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
-  static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert(kSmemBytes <= (DUO ? 115712u : 232448u), "shared memory");
 };
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
@@ -212,7 +227,7 @@ __device__ __forceinline__ bool row_bitmap(const Params& p, int64_t r, uint32_t*
 }
 
 template <int BT, int D>
-__global__ void __launch_bounds__(Cfg<BT, D>::THREADS, 1)
+__global__ void __launch_bounds__(Cfg<BT, D>::THREADS, Cfg<BT, D>::kMinCtas)
 attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -225,7 +240,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   auto bar = [&](int idx) -> uint32_t { return base + C::kOffBar + 8u * (uint32_t)idx; };
   // ring entry: x = item, y = stages (-1: skip, -2: end), z = bad-row bits (pairs)
   volatile int4* ring = reinterpret_cast<volatile int4*>(gbase + C::kOffRing);
-  uint32_t* bits = reinterpret_cast<uint32_t*>(gbase + C::kOffBits);   // [kNI][2][C::MAXW] (pairs)
+  uint32_t* bits = reinterpret_cast<uint32_t*>(gbase + C::kOffBits);   // [C::NI][2][C::MAXW] (pairs)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + C::kOffMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -268,7 +283,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     prefetch_tmap(&tv);
   }
   if (warp == C::W_S) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
   fence_before();
@@ -285,8 +300,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       int32_t slot = 0;
       if (lane == 0) slot = atomicAdd(p.counter, 1);
       slot = __shfl_sync(0xffffffffu, slot, 0);
-      const int ri = (int)(it_fill % kNI);
-      if (!wait_warp(bar(I_EMPTY + ri), ((it_fill / kNI) & 1u) ^ 1u, g)) break;
+      const int ri = (int)(it_fill % C::NI);
+      if (!wait_warp(bar(I_EMPTY + ri), ((it_fill / C::NI) & 1u) ^ 1u, g)) break;
       uint32_t* bmA = bits + ri * 2 * C::MAXW;
       uint32_t* bmB = bmA + C::MAXW;
       int32_t item = -1, len = -2, badbits = 0;
@@ -403,8 +418,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     uint32_t it_use = 0, q_use = 0, k_use = 0, s_issue = 0;
     bool issued_any = false;
     for (;;) {
-      const int ri = (int)(it_use % kNI);
-      if (!wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
+      const int ri = (int)(it_use % C::NI);
+      if (!wait_warp(bar(I_FULL + ri), (it_use / C::NI) & 1u, g)) break;
       const int len = ring[ri].y;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
@@ -415,8 +430,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       ++q_use;
       bool ok = true;
       for (int e = 0; e < len; ++e) {
-        const uint32_t b = s_issue & 1u, ks = k_use % C::NK;
-        if (!(ok = wait_warp(bar(S_FREE + b), ((s_issue >> 1) & 1u) ^ 1u, g))) break;
+        const uint32_t b = s_issue % C::NSB, ks = k_use % C::NK;
+        if (!(ok = wait_warp(bar(S_FREE + b), ((s_issue / C::NSB) & 1u) ^ 1u, g))) break;
         if (!(ok = wait_warp(bar(K_FULL + ks), (k_use / C::NK) & 1u, g))) break;
         fence_after();
         const uint32_t kb = sK + ks * C::kKTile;
@@ -426,7 +441,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             // k-step kk: 16 columns = 32 bytes into the row, in box kk / 4
             const uint32_t offq = (uint32_t)(kk >> 2) * C::kQBox + (uint32_t)(kk & 3) * 32u;
             const uint32_t offk = (uint32_t)(kk >> 2) * C::kKBox + (uint32_t)(kk & 3) * 32u;
-            mma_ss(tmem + kColS + b * 128u, smem_desc(sQ + offq, 16, 1024, kSwizzle128B),
+            mma_ss(tmem + C::kColS + b * 128u, smem_desc(sQ + offq, 16, 1024, kSwizzle128B),
                    smem_desc(kb + offk, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
           }
           commit(bar(S_FULL + b));
@@ -452,8 +467,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     uint32_t it_use = 0, v_use = 0, pv = 0, o_items = 0;
     bool issued_any = false;
     for (;;) {
-      const int ri = (int)(it_use % kNI);
-      if (!wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
+      const int ri = (int)(it_use % C::NI);
+      if (!wait_warp(bar(I_FULL + ri), (it_use / C::NI) & 1u, g)) break;
       const int len = ring[ri].y;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
@@ -462,9 +477,9 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       if (len <= 0) continue;
       bool ok = true;
       for (int e = 0; e < len; ++e) {
-        const uint32_t b = pv & 1u, vs = v_use % C::NV;
+        const uint32_t b = pv % C::NPB, vs = v_use % C::NV;
         if (!(ok = wait_warp(bar(V_FULL + vs), (v_use / C::NV) & 1u, g))) break;
-        if (!(ok = wait_warp(bar(P_FULL + b), (pv >> 1) & 1u, g))) break;
+        if (!(ok = wait_warp(bar(P_FULL + b), (pv / C::NPB) & 1u, g))) break;
         if (e == 0 && !(ok = wait_warp(bar(O_EMPTY), (o_items & 1u) ^ 1u, g))) break;
         fence_after();
         const uint32_t vb = sV + vs * C::kKTile;
@@ -475,13 +490,13 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             for (int hg = 0; hg < 2; ++hg)
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                mma_ts(tmem + kColO + (uint32_t)hg * 64u, tmem + kColP + b * 64u + (uint32_t)hg * 32u + (uint32_t)kk * 8u,
+                mma_ts(tmem + C::kColO + (uint32_t)hg * 64u, tmem + C::kColP + b * 64u + (uint32_t)hg * 32u + (uint32_t)kk * 8u,
                        smem_desc(vb + (uint32_t)(hg * 4 + kk) * 2048u, C::kKBox, 1024, kSwizzle128B), idO,
                        (e > 0 || kk > 0) ? 1u : 0u);
           } else {
 #pragma unroll
             for (int kk = 0; kk < C::KR / 16; ++kk)
-              mma_ts(tmem + kColO, tmem + kColP + b * 64u + (uint32_t)kk * 8u,
+              mma_ts(tmem + C::kColO, tmem + C::kColP + b * 64u + (uint32_t)kk * 8u,
                      smem_desc(vb + (uint32_t)kk * 2048u, C::kKBox, 1024, kSwizzle128B), idO,
                      (e > 0 || kk > 0) ? 1u : 0u);
           }
@@ -520,8 +535,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     float2* stat = reinterpret_cast<float2*>(gbase + C::kOffStat);   // [parity][group][row]
     bool ok = true;
     for (;;) {
-      const int ri = (int)(it_use % kNI);
-      if (!wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
+      const int ri = (int)(it_use % C::NI);
+      if (!wait_warp(bar(I_FULL + ri), (it_use / C::NI) & 1u, g)) break;
       const int64_t item = ring[ri].x;
       const int len = ring[ri].y;
       const int badbits = ring[ri].z;
@@ -570,12 +585,12 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           const int j = grp == 0 ? j1 : j2;
           has = j >= 0 && bit_of(mine, j);
         }
-        const uint32_t b = s_use & 1u;
-        if (!(ok = wait_warp(bar(S_FULL + b), (s_use >> 1) & 1u, g))) break;
+        const uint32_t b = s_use % C::NSB;
+        if (!(ok = wait_warp(bar(S_FULL + b), (s_use / C::NSB) & 1u, g))) break;
         fence_after();
         uint32_t sv[64];
-        float cm0 = tmem_ld32_max(t_row + kColS + b * 128u + (uint32_t)grp * 64u, sv);
-        float cm1 = tmem_ld32_max(t_row + kColS + b * 128u + (uint32_t)grp * 64u + 32u, sv + 32);
+        float cm0 = tmem_ld32_max(t_row + C::kColS + b * 128u + (uint32_t)grp * 64u, sv);
+        float cm1 = tmem_ld32_max(t_row + C::kColS + b * 128u + (uint32_t)grp * 64u + 32u, sv + 32);
         wait_ld();
         fence_before();
         mbar_arrive(bar(S_FREE + b));
@@ -587,13 +602,13 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         } else if (__any_sync(0xffffffffu, m_new > m + kRescaleThreshold)) {
           // O_grp must not change under the PV of block g-1
           const uint64_t gp = blocks_done + e - 1;
-          if (!(ok = wait_warp(bar(PV_DONE + (uint32_t)(gp & 1u)), (uint32_t)((gp >> 1) & 1u), g))) break;
+          if (!(ok = wait_warp(bar(PV_DONE + (uint32_t)(gp % C::NPB)), (uint32_t)((gp / C::NPB) & 1u), g))) break;
           fence_after();
           const float f = ex2f(m - m_new);
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t ov[32];
-            const uint32_t a = t_row + kColO + (uint32_t)grp * 64u + c * 32u;
+            const uint32_t a = t_row + C::kColO + (uint32_t)grp * 64u + c * 32u;
             tmem_ld32(a, ov);
             wait_ld();
 #pragma unroll
@@ -623,11 +638,11 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
         // P buffer b was last read by the PV of block g-2
         const uint64_t gb = blocks_done + e;
-        if (gb >= 2) {
-          if (!(ok = wait_warp(bar(PV_DONE + b), (uint32_t)(((gb - 2) >> 1) & 1u), g))) break;
+        if (gb >= (uint64_t)C::NPB) {
+          if (!(ok = wait_warp(bar(PV_DONE + b), (uint32_t)(((gb - C::NPB) / C::NPB) & 1u), g))) break;
           fence_after();
         }
-        tmem_st32(t_row + kColP + b * 64u + (uint32_t)grp * 32u, pk);
+        tmem_st32(t_row + C::kColP + b * 64u + (uint32_t)grp * 32u, pk);
         wait_st();
         fence_before();
         mbar_arrive(bar(P_FULL + b));
@@ -651,8 +666,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       const float inv = L > 0.f ? 1.0f / L : 0.f;
       const float a0 = f0 * inv, a1 = f1 * inv;
       uint32_t oa[32], ob[32];
-      tmem_ld32(t_row + kColO + (uint32_t)grp * 32u, oa);
-      tmem_ld32(t_row + kColO + 64u + (uint32_t)grp * 32u, ob);
+      tmem_ld32(t_row + C::kColO + (uint32_t)grp * 32u, oa);
+      tmem_ld32(t_row + C::kColO + 64u + (uint32_t)grp * 32u, ob);
       wait_ld();
       fence_before();
       mbar_arrive(bar(O_EMPTY));
@@ -678,8 +693,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       const int half = PAIR ? (int)(threadIdx.x >> 6) : 0;
       bool ok = true;
       for (;;) {
-        const int ri = (int)(it_use % kNI);
-        if (!wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
+        const int ri = (int)(it_use % C::NI);
+        if (!wait_warp(bar(I_FULL + ri), (it_use / C::NI) & 1u, g)) break;
         const int64_t item = ring[ri].x;
         const int len = ring[ri].y;
         const int badbits = ring[ri].z;
@@ -729,14 +744,99 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             has1 = bit_of(mine, j1);
             has2 = j2 >= 0 && bit_of(mine, j2);
           }
-          const uint32_t b = s_use & 1u;
-          if (!(ok = wait_warp(bar(S_FULL + b), (s_use >> 1) & 1u, g))) break;
+          const uint32_t b = s_use % C::NSB;
+          if (!(ok = wait_warp(bar(S_FULL + b), (s_use / C::NSB) & 1u, g))) break;
           fence_after();
+          if constexpr (C::DUO) {
+            const uint64_t gb = blocks_done + e;
+            const uint32_t sbase = t_row + C::kColS;
+            float rs[8];
+  #pragma unroll
+            for (int u = 0; u < 8; ++u) rs[u] = 0.f;
+            // P (one buffer) was last read by the PV of block g-1, and O must not change
+            // under it either: waited for before the first P store or O rescale
+            bool pv_waited = gb == 0;
+            // pass 1: the maximum of the selected 32-column chunks (the loaded values are
+            // dropped; this pass also covers the time the PV of block g-1 takes)
+            float mx = -INFINITY;
+  #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (q < 2 ? has1 : has2) {
+                uint32_t tmp[32];
+                const float cq = tmem_ld32_max(sbase + 32u * q, tmp);
+                wait_ld();
+                mx = fmaxf(mx, cq);
+              }
+            }
+            const float m_new = fmaxf(m, mx * sl2);
+            if (e == 0) {
+              m = m_new;
+            } else if (__any_sync(0xffffffffu, m_new > m + kRescaleThreshold)) {
+              if (!pv_waited) {
+                pv_waited = true;
+                if (!(ok = wait_warp(bar(PV_DONE), (uint32_t)((gb - 1) & 1u), g))) break;
+                fence_after();
+              }
+              const float f = ex2f(m - m_new);
+  #pragma unroll
+              for (int c = 0; c < D / 32; ++c) {
+                uint32_t ov[32];
+                tmem_ld32(t_row + C::kColO + c * 32u, ov);
+                wait_ld();
+  #pragma unroll
+                for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * f);
+                tmem_st32(t_row + C::kColO + c * 32u, ov);
+              }
+              wait_st();
+              l *= f;
+              m = m_new;
+            }
+            // pass 2: the exponentials, 32 columns at a time; S is free once its last
+            // chunk is loaded
+  #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const bool act = q < 2 ? has1 : has2;
+              uint32_t sv[32];
+              if (act) {
+                tmem_ld32(sbase + 32u * q, sv);
+                wait_ld();
+              }
+              if (q == 3) {
+                fence_before();
+                mbar_arrive(bar(S_FREE));
+              }
+              uint32_t pk[16];
+              if (act) {
+  #pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                  const float p0 = ex2f(fmaf(__uint_as_float(sv[2 * c]), sl2, -m));
+                  const float p1 = ex2f(fmaf(__uint_as_float(sv[2 * c + 1]), sl2, -m));
+                  rs[c & 7] += p0 + p1;
+                  pk[c] = pack2(p0, p1);
+                }
+              } else {
+  #pragma unroll
+                for (int c = 0; c < 16; ++c) pk[c] = 0u;
+              }
+              if (!pv_waited) {
+                pv_waited = true;
+                if (!(ok = wait_warp(bar(PV_DONE), (uint32_t)((gb - 1) & 1u), g))) break;
+                fence_after();
+              }
+              tmem_st16(t_row + C::kColP + 16u * q, pk);
+            }
+            if (!ok) break;
+            ++s_use;
+            l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+            wait_st();
+            fence_before();
+            mbar_arrive(bar(P_FULL));
+          } else {
           uint32_t s[C::KR];
           float cm[C::KR / 32];   // the maximum of each 32-column load (exact, as any order of max)
   #pragma unroll
           for (int c = 0; c < C::KR / 32; ++c)
-            cm[c] = tmem_ld32_max(t_row + kColS + b * 128u + c * 32u, s + 32 * c);
+            cm[c] = tmem_ld32_max(t_row + C::kColS + b * 128u + c * 32u, s + 32 * c);
           wait_ld();
           fence_before();
           mbar_arrive(bar(S_FREE + b));
@@ -752,17 +852,17 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           } else if (__any_sync(0xffffffffu, m_new > m + kRescaleThreshold)) {
             // O must not change under the PV of block g-1 (g = global block index)
             const uint64_t gp = blocks_done + e - 1;
-            if (!(ok = wait_warp(bar(PV_DONE + (uint32_t)(gp & 1u)), (uint32_t)((gp >> 1) & 1u), g))) break;
+            if (!(ok = wait_warp(bar(PV_DONE + (uint32_t)(gp % C::NPB)), (uint32_t)((gp / C::NPB) & 1u), g))) break;
             fence_after();
             const float f = ex2f(m - m_new);
   #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
               uint32_t ov[32];
-              tmem_ld32(t_row + kColO + c * 32u, ov);
+              tmem_ld32(t_row + C::kColO + c * 32u, ov);
               wait_ld();
   #pragma unroll
               for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * f);
-              tmem_st32(t_row + kColO + c * 32u, ov);
+              tmem_st32(t_row + C::kColO + c * 32u, ov);
             }
             wait_st();
             l *= f;
@@ -792,15 +892,16 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
           // P buffer b was last read by the PV of block g-2
           const uint64_t gb = blocks_done + e;
-          if (gb >= 2) {
-            if (!(ok = wait_warp(bar(PV_DONE + b), (uint32_t)(((gb - 2) >> 1) & 1u), g))) break;
+          if (gb >= (uint64_t)C::NPB) {
+            if (!(ok = wait_warp(bar(PV_DONE + b), (uint32_t)(((gb - C::NPB) / C::NPB) & 1u), g))) break;
             fence_after();
           }
   #pragma unroll
-          for (int c = 0; c < C::KR / 64; ++c) tmem_st32(t_row + kColP + b * 64u + 32u * c, pk + 32 * c);
+          for (int c = 0; c < C::KR / 64; ++c) tmem_st32(t_row + C::kColP + b * 64u + 32u * c, pk + 32 * c);
           wait_st();
           fence_before();
           mbar_arrive(bar(P_FULL + b));
+          }
         }
         if (PAIR) release();
         if (!ok) break;
@@ -813,7 +914,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
-          tmem_ld32(t_row + kColO + c * 32u, ov);
+          tmem_ld32(t_row + C::kColO + c * 32u, ov);
           wait_ld();
           if (!stores) continue;
           uint32_t w[16];
@@ -833,7 +934,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   fence_before();
   __syncthreads();
   fence_after();
-  if (warp == C::W_S) tmem_dealloc(tmem, 512);
+  if (warp == C::W_S) tmem_dealloc(tmem, C::kTmemCols);
   if (p.prof != nullptr && threadIdx.x == 0)
     atomicAdd((unsigned long long*)&p.prof[smid() % SPARSP_PROF_SLOTS],
               (unsigned long long)(globaltimer_ns() - t_start));
@@ -862,9 +963,12 @@ sparsp_status_t go_fwd(const Dims& s, const CUtensorMap& tq, const CUtensorMap& 
   auto kern = attn_fwd_tc_kernel<BT, D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes) != cudaSuccess)
     return SPARSP_ERR_CUDA;
+  // all of the SM's memory as shared memory: one CTA of ~225 KB, or two of ~100 KB
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+    return SPARSP_ERR_CUDA;
   const int sms = device_sm_count();
   if (sms <= 0) return SPARSP_ERR_CUDA;
-  const int64_t grid = cap_grid(s, sms, prm.n_items);
+  const int64_t grid = cap_grid(s, (int64_t)sms * C::kMinCtas, prm.n_items);
   kern<<<(unsigned)grid, C::THREADS, C::kSmemBytes, st>>>(tq, tk, tv, prm);
   SPARSP_LAUNCH_CHECK();
   return SPARSP_OK;
