@@ -105,8 +105,11 @@ lpt_place_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict_
   if (bh == 0 && threadIdx.x == 0 && counter != nullptr) *counter = 0;
 }
 
-// CSR -> CSC per head. Rows are visited in order, one row per step, so each
-// key block's list of query blocks comes out ascending.
+constexpr int kBitmapMaxBlocks = 1024;
+
+// CSR -> CSC per head beyond kBitmapMaxBlocks blocks. Rows are visited in
+// order, one row per step, so each key block's list of query blocks comes out
+// ascending.
 __global__ void __launch_bounds__(kThreads)
 csr_transpose_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ col_idx,
                      int BH, int nb, int32_t* __restrict__ col_ptr, int32_t* __restrict__ row_idx,
@@ -176,6 +179,86 @@ csr_transpose_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restr
   }
 }
 
+// Up to kBitmapMaxBlocks blocks: the head's CSR as a row-major bitmap in
+// shared memory ([nb][ceil(nb/32)] words); thread j then walks column j down
+// the rows and writes its list in ascending row order. A row listing an index
+// twice, or one outside [0, nb), sets SPARSP_ERR_DATA.
+
+__global__ void __launch_bounds__(kThreads)
+csr_transpose_bitmap_kernel(const int32_t* __restrict__ row_ptr, const int32_t* __restrict__ col_idx,
+                            int BH, int nb, int32_t* __restrict__ col_ptr, int32_t* __restrict__ row_idx,
+                            int32_t* d_status) {
+  extern __shared__ uint32_t bm[];   // [nb][W]
+  __shared__ int32_t cnt[kBitmapMaxBlocks];
+  __shared__ int32_t warp_tot[32];
+  const int bh = blockIdx.x;
+  const int64_t r0 = (int64_t)bh * nb;
+  const int W = (nb + 31) >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  for (int w = threadIdx.x; w < nb * W; w += blockDim.x) bm[w] = 0u;
+  for (int j = threadIdx.x; j < nb; j += blockDim.x) cnt[j] = 0;
+  __syncthreads();
+  // one warp per row: its bits and the column counts
+  for (int i = warp; i < nb; i += nwarps) {
+    const int32_t a = row_ptr[r0 + i], b = row_ptr[r0 + i + 1];
+    bool bad = b < a;
+    for (int32_t e = a + lane; e < b && !bad; e += 32) {
+      const int32_t j = col_idx[e];
+      if (j < 0 || j >= nb) {
+        bad = true;
+      } else {
+        atomicOr(&bm[i * W + (j >> 5)], 1u << (j & 31));
+        atomicAdd(&cnt[j], 1);
+      }
+    }
+    __syncwarp();
+    int c = 0;
+    for (int w = lane; w < W; w += 32) c += __popc(bm[i * W + w]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+    if (__any_sync(0xffffffffu, bad) || (b >= a && c != b - a)) {
+      if (lane == 0) report(d_status, SPARSP_ERR_DATA);
+    }
+  }
+  __syncthreads();
+  // exclusive scan of the counts (one entry per thread: nb <= blockDim)
+  const int32_t e0 = row_ptr[r0];
+  const int j = threadIdx.x;
+  const int32_t v = j < nb ? cnt[j] : 0;
+  int32_t incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t t = lane < nwarps ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t o = __shfl_up_sync(0xffffffffu, t, off);
+      if (lane >= off) t += o;
+    }
+    warp_tot[lane] = t;
+  }
+  __syncthreads();
+  int32_t pos = e0 + (warp > 0 ? warp_tot[warp - 1] : 0) + incl - v;
+  if (j < nb) col_ptr[r0 + j] = pos;
+  if (bh == BH - 1 && threadIdx.x == 0) col_ptr[(int64_t)BH * nb] = row_ptr[(int64_t)BH * nb];
+  // column j, down the rows
+  if (j < nb) {
+    const int32_t end = pos + v;
+    const uint32_t bit = 1u << (j & 31);
+    const uint32_t* col = bm + (j >> 5);
+    for (int i = 0; i < nb; ++i)
+      if (col[i * W] & bit) {
+        if (dcheck(pos < end, d_status)) row_idx[pos] = i;
+        ++pos;
+      }
+  }
+}
+
 }  // namespace
 
 // Histogram space for costs up to 2*nb (the pair items of 64-token blocks cost
@@ -230,6 +313,16 @@ sparsp_status_t launch_csr_transpose(const Dims& s, const int32_t* row_ptr, cons
                                      int32_t* col_ptr, int32_t* row_idx, int32_t* d_status,
                                      cudaStream_t st) {
   const int BH = s.B * s.H;
+  if (s.nb <= kBitmapMaxBlocks) {
+    const size_t smem = (size_t)s.nb * ((s.nb + 31) / 32) * sizeof(uint32_t);   // up to 128 KB
+    if (cudaFuncSetAttribute(csr_transpose_bitmap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return SPARSP_ERR_CUDA;
+    csr_transpose_bitmap_kernel<<<BH, kThreads, smem, st>>>(row_ptr, col_idx, BH, s.nb, col_ptr, row_idx,
+                                                            d_status);
+    SPARSP_LAUNCH_CHECK();
+    return SPARSP_OK;
+  }
   csr_transpose_kernel<<<BH, kThreads, 0, st>>>(row_ptr, col_idx, BH, s.nb, col_ptr, row_idx,
                                                 d_status);
   SPARSP_LAUNCH_CHECK();

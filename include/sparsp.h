@@ -439,6 +439,8 @@ SPARSP_API sparsp_status_t sparsp_attn_bwd(const sparsp_shape_t* shape, const vo
  * Transpose of the per-head CSR (used by the backward): for each key block j
  * of head (b,h), the query blocks that selected it, ascending.
  * col_ptr int32 [B*H*nb+1]; row_idx int32 (capacity = nnz of the CSR).
+ * An index outside [0, nb) sets SPARSP_ERR_DATA (the entry is left out); up
+ * to 1,024 blocks so does a row that lists a block twice.
  */
 SPARSP_API sparsp_status_t sparsp_csr_transpose(const sparsp_shape_t* shape, const int32_t* row_ptr,
                                      const int32_t* col_idx, int32_t* col_ptr, int32_t* row_idx,
