@@ -148,25 +148,33 @@ class Pipeline:
             self.dq, self.dk, self.dv = (torch.empty((s.B, s.N, s.H, s.d), dtype=dt, device=dev)
                                          for _ in range(3))
 
-    def forward(self, q, k, v, wq=None, wk=None, prof: bool = False, mark=None, out=None):
+    def forward(self, q, k, v, wq=None, wk=None, prof: bool = False, mark=None, out=None, before=None):
         """mark: optional callable(stage_name, stream=None) invoked after each
         stage is enqueued (used to record CUDA events; stream None is the
         current stream). With overlap_demand the overlapped stages are marked on
         their own streams, each preceded by a "<stage>:begin" mark, and the
         region they share by "overlap". out: optional raster output buffer
-        (default: self.o)."""
+        (default: self.o). before: optional callable(name) invoked just before
+        input "q", "k" or "v" is first read (e.g. to wait for its copy)."""
         s = self.shape
         mark = mark or (lambda name, stream=None: None)
+        before = before or (lambda name: None)
         if self.fused:   # the tile means come out of the reorder pass itself
+            before("q")
             reorder_pool(s, q, self.qb, self.qmeans)
+            before("k")
             reorder_pool(s, k, self.kb, self.kmeans)
+            before("v")
             reorder(s, v, self.vb)
             mark("reorder")
             block_scores_pooled(s, self.qmeans, self.kmeans, self.est, wq, wk, self.rank, out=self.scores,
                                 ws=self.ws_pooled)
         else:
+            before("q")
             reorder(s, q, self.qb)
+            before("k")
             reorder(s, k, self.kb)
+            before("v")
             reorder(s, v, self.vb)
             mark("reorder")
             block_scores(s, self.qb, self.kb, self.est, wq, wk, self.rank, out=self.scores, ws=self.ws_scores)
@@ -229,13 +237,16 @@ class Pipeline:
         self._o_fwd = o
         return o, self.lse
 
-    def backward(self, dout, prof: bool = False, mark=None, outs=None):
-        """outs: optional raster (dQ, dK, dV) output buffers (default: self.dq, self.dk, self.dv).
+    def backward(self, dout, prof: bool = False, mark=None, outs=None, before=None):
+        """outs: optional raster (dQ, dK, dV) output buffers (default: self.dq, self.dk, self.dv);
+        before: optional callable("do") invoked just before dout is first read.
         With raster_out the backward reads O from the buffer the last forward()
         wrote it to, which must still hold it, and writes the gradients' raster
         rows itself."""
         s = self.shape
         mark = mark or (lambda name: None)
+        if before is not None:   # e.g. to wait for dout's copy
+            before("do")
         reorder(s, dout, self.dob)
         mark("reorder_dout")
         rp, ci = self.csr

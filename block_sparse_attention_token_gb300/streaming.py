@@ -6,8 +6,10 @@ HostPipeline.train_step() does the same for a forward + backward step (Q, K, V
 and dO in; O, dQ, dK and dV out). The device input and output buffers are
 double-buffered and the copies run on their own streams, so the host-to-device
 copy of step n+1 and the device-to-host copy of step n-1 overlap the kernels
-of step n. Every step still copies its own inputs in and its own results out;
-events order each buffer's reuse.
+of step n; each input has its own copy event, so a step's kernels start on an
+input as soon as it has landed, and in a training step O goes back while the
+backward runs. Every step still copies its own inputs in and its own results
+out; events order each buffer's reuse.
 """
 from __future__ import annotations
 
@@ -28,30 +30,40 @@ class HostPipeline:
         self.d2h = torch.cuda.Stream()
         cur = torch.cuda.current_stream()
         mk = lambda: [torch.cuda.Event() for _ in range(2)]
-        self.in_ready, self.in_free, self.out_ready, self.out_free = mk(), mk(), mk(), mk()
-        for evs in (self.in_ready, self.in_free, self.out_ready, self.out_free):
+        self.in_free, self.out_ready, self.out_free = mk(), mk(), mk()
+        # one event per input copy, so that a step's kernels start on each input as soon as
+        # it has landed rather than after all of them
+        self.in_ready = [{x: torch.cuda.Event() for x in ("q", "k", "v", "do")} for _ in range(2)]
+        self.o_ready = mk()
+        for evs in (self.in_free, self.out_ready, self.out_free, self.o_ready):
             for e in evs:
                 e.record(cur)
         self.n = 0
         self.t_inp = self.t_out = None
 
+    def _copy_in(self, b, dsts, srcs, names):
+        """Host-to-device copies of step buffers b on the copy stream, one event each."""
+        with torch.cuda.stream(self.h2d):
+            self.h2d.wait_event(self.in_free[b])          # step n-2 has consumed these buffers
+            for dst, src, x in zip(dsts, srcs, names):
+                dst.copy_(src, non_blocking=True)
+                self.in_ready[b][x].record(self.h2d)
+
+    def _waiter(self, b, cur):
+        return lambda name: cur.wait_event(self.in_ready[b][name])
+
     def step(self, hq, hk, hv, ho, wq=None, wk=None):
         """One forward step: pinned host q, k, v (raster) in, pinned host O out."""
         b = self.n & 1
         cur = torch.cuda.current_stream()
-        with torch.cuda.stream(self.h2d):
-            self.h2d.wait_event(self.in_free[b])          # step n-2 has consumed these buffers
-            for dst, src in zip(self.inp[b], (hq, hk, hv)):
-                dst.copy_(src, non_blocking=True)
-            self.in_ready[b].record(self.h2d)
-        cur.wait_event(self.in_ready[b])
+        self._copy_in(b, self.inp[b], (hq, hk, hv), ("q", "k", "v"))
         cur.wait_event(self.out_free[b])                   # step n-2's O has left the device
 
         def mark(name, stream=None):
             if name == "reorder":                          # raster inputs are no longer read
                 self.in_free[b].record(cur)
 
-        self.pipe.forward(*self.inp[b], wq=wq, wk=wk, mark=mark, out=self.out[b])
+        self.pipe.forward(*self.inp[b], wq=wq, wk=wk, mark=mark, out=self.out[b], before=self._waiter(b, cur))
         self.out_ready[b].record(cur)
         with torch.cuda.stream(self.d2h):
             self.d2h.wait_event(self.out_ready[b])
@@ -71,12 +83,7 @@ class HostPipeline:
             self.t_inp, self.t_out = mk(4), mk(4)
         b = self.n & 1
         cur = torch.cuda.current_stream()
-        with torch.cuda.stream(self.h2d):
-            self.h2d.wait_event(self.in_free[b])          # step n-2 has consumed these buffers
-            for dst, src in zip(self.t_inp[b], (hq, hk, hv, hdo)):
-                dst.copy_(src, non_blocking=True)
-            self.in_ready[b].record(self.h2d)
-        cur.wait_event(self.in_ready[b])
+        self._copy_in(b, self.t_inp[b], (hq, hk, hv, hdo), ("q", "k", "v", "do"))
         cur.wait_event(self.out_free[b])                   # step n-2's results have left the device
 
         def mark(name, stream=None):
@@ -85,12 +92,18 @@ class HostPipeline:
 
         q, k, v, do = self.t_inp[b]
         o, dq, dk, dv = self.t_out[b]
-        self.pipe.forward(q, k, v, wq=wq, wk=wk, out=o)
-        self.pipe.backward(do, mark=mark, outs=(dq, dk, dv))
+        waiter = self._waiter(b, cur)
+        self.pipe.forward(q, k, v, wq=wq, wk=wk, out=o, before=waiter)
+        # O goes back while the backward runs (the backward only reads it)
+        self.o_ready[b].record(cur)
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(self.o_ready[b])
+            ho.copy_(o, non_blocking=True)
+        self.pipe.backward(do, mark=mark, outs=(dq, dk, dv), before=waiter)
         self.out_ready[b].record(cur)
         with torch.cuda.stream(self.d2h):
             self.d2h.wait_event(self.out_ready[b])
-            for dst, src in zip((ho, hdq, hdk, hdv), self.t_out[b]):
+            for dst, src in zip((hdq, hdk, hdv), (dq, dk, dv)):
                 dst.copy_(src, non_blocking=True)
             self.out_free[b].record(self.d2h)
         self.n += 1
