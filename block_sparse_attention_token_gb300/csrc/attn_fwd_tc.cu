@@ -18,8 +18,10 @@
 // warps (8 softmax warps in two groups, one per 64-column half of a stage,
 // each with its own running max, sum and O accumulator, combined once per
 // item; see Cfg::SPLIT) for 128-token blocks with d = 64; two per SM, each with
-// 7 warps and half of the TMEM and shared memory (one S and one P buffer; see
-// Cfg::DUO), for 64-token blocks with d = 64:
+// 8 warps (4 softmax warps, the producer, one warp issuing both GEMM streams,
+// two idle warps that only give their registers to the softmax warpgroup) and
+// half of the TMEM and shared memory (one S and one P buffer; see Cfg::DUO),
+// for 64-token blocks with d = 64:
 //   producer: pulls items longest-first through an atomic counter,
 //              validates the CSR row(s), publishes the item in a shared-memory
 //              ring (for pairs with the two rows as bitmaps), and TMA-loads the
@@ -78,9 +80,10 @@ struct Cfg {
   // 64-token blocks with d = 64: two CTAs per SM, each with half of the TMEM
   // (one S buffer [0,128), O [128,192), one P buffer [192,256)) and half of
   // the shared memory (3 K and 2 V stages), so that one CTA's softmax runs
-  // while the other's MMAs keep the tensor pipe busy. A softmax row goes in
-  // two passes over 64-column halves (the maximum, then the exponentials) to
-  // fit the registers two CTAs leave a thread.
+  // while the other's MMAs keep the tensor pipe busy. The softmax warps hold
+  // a whole 128-column S row in registers (one pass per stage, S released as
+  // soon as it is loaded) with the 200 registers the register split below
+  // gives them.
   static constexpr bool DUO = BT == 64 && D == 64;
   // 128-token blocks with d = 64: two softmax warpgroups, one per 64-column
   // half of a stage, each with its own running max, sum and O accumulator
@@ -88,8 +91,21 @@ struct Cfg {
   // warps per SM sub-partition hide each other's latencies.
   static constexpr bool SPLIT = D == 64 && !DUO;
   static constexpr int NSM = SPLIT ? 8 : 4;               // softmax warps
-  static constexpr int THREADS = 32 * (NSM + 3);           // + producer, S issuer, PV issuer
-  static constexpr int W_PROD = NSM, W_S = NSM + 1, W_PV = NSM + 2;
+  // MMA issuer warps: S and PV each get their own, except with DUO, where one
+  // warp issues both streams so that two CTAs of 6 warps leave a thread 168
+  // registers (a whole 128-column S row held in registers: one pass per stage)
+  static constexpr int NIS = DUO ? 1 : 2;
+  // DUO: two idle warps complete the second warpgroup (producer, issuer), so
+  // that the softmax warpgroup can take registers from it (setmaxnreg works
+  // on whole warpgroups): two CTAs of 8 warps launch at 128 registers a
+  // thread; the softmax warps rise to 200 and the other four drop to 56
+  // (4 x 32 x 200 + 4 x 32 x 56 = 256 x 128)
+  static constexpr int NIDLE = DUO ? 2 : 0;
+  static constexpr int THREADS = 32 * (NSM + 1 + NIS + NIDLE);   // + producer, issuer(s), idle
+  static constexpr int W_PROD = NSM, W_S = NSM + 1, W_PV = NSM + NIS;
+  static constexpr uint32_t kRegSoftmax = 200, kRegAux = 56;
+  static_assert(!DUO || (THREADS == 256 && NSM == 4 && 128 * (kRegSoftmax + kRegAux) == 256 * 128),
+                "register split of the two warpgroups");
   // K and V ring stages: 3 fit beside a d = 128 query tile; with d = 64 the
   // tiles are half the size and 6 stages keep more L2 loads in flight (a stage
   // then takes half the tensor time, so the same latency needs twice the depth)
@@ -269,7 +285,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     mbar_init(bar(O_EMPTY), 32 * C::NSM);
     for (int r = 0; r < kNI; ++r) {
       mbar_init(bar(I_FULL + r), 1);
-      mbar_init(bar(I_EMPTY + r), C::NSM + 2);
+      mbar_init(bar(I_EMPTY + r), C::NSM + C::NIS);
     }
     mbar_init(bar(TEAR), 1);
     mbar_init(bar(TEAR_PV), 1);
@@ -293,6 +309,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   const Guard g{abort_flag, p.d_status, kWaitNs};
   const int nb = p.nb, nbp = p.nbp;
 
+  if (warp >= C::NSM) {
+  if constexpr (C::DUO) regs_decrease<C::kRegAux>();   // the whole second warpgroup
   if (warp == C::W_PROD) {
     // ------------------------------------------------------------ producer
     uint32_t it_fill = 0, q_fill = 0, k_fill = 0, v_fill = 0;
@@ -412,6 +430,82 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       for (uint32_t s = 0; s < C::NV; ++s)
         if (v_fill > s) wait_raw(bar(V_FULL + s), ((v_fill - 1 - s) / C::NV) & 1u, kDrainNs);
     }
+  } else if (C::DUO && warp == C::W_S) {
+    // ------------------------------------------------------------ S and PV from one warp (DUO)
+    // Per item: S(0), then S(e) before PV(e-1) for e = 1 .. len-1, then PV(len-1).
+    // S(e) waits for the softmax to have loaded S(e-1) (one S buffer) and PV(e-1)
+    // for P(e-1); the softmax releases S(e-1) before it writes P(e-1), so neither
+    // wait holds back the other stream, and S(e) runs under the softmax of e-1.
+    constexpr uint32_t idS = idesc_bf16(128, C::KR, 0, 0);
+    constexpr uint32_t idO = idesc_bf16(128, D, 0, 1);
+    uint32_t it_use = 0, q_use = 0, k_use = 0, v_use = 0, s_issue = 0, pv = 0, o_items = 0;
+    bool issued_any = false, ok = true;
+    for (;;) {
+      const int ri = (int)(it_use % C::NI);
+      if (!(ok = wait_warp(bar(I_FULL + ri), (it_use / C::NI) & 1u, g))) break;
+      const int len = ring[ri].y;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
+      ++it_use;
+      if (len == -2) break;
+      if (len <= 0) continue;
+      if (!(ok = wait_warp(bar(Q_FULL), q_use & 1u, g))) break;
+      ++q_use;
+      for (int e = 0; e <= len && ok; ++e) {
+        if (e < len) {
+          const uint32_t ks = k_use % C::NK;
+          if (!(ok = wait_warp(bar(S_FREE), (s_issue & 1u) ^ 1u, g))) break;
+          if (!(ok = wait_warp(bar(K_FULL + ks), (k_use / C::NK) & 1u, g))) break;
+          fence_after();
+          const uint32_t kb = sK + ks * C::kKTile;
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t offq = (uint32_t)(kk >> 2) * C::kQBox + (uint32_t)(kk & 3) * 32u;
+              const uint32_t offk = (uint32_t)(kk >> 2) * C::kKBox + (uint32_t)(kk & 3) * 32u;
+              mma_ss(tmem + C::kColS, smem_desc(sQ + offq, 16, 1024, kSwizzle128B),
+                     smem_desc(kb + offk, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
+            }
+            commit(bar(S_FULL));
+            commit(bar(K_EMPTY + ks));
+            if (e + 1 == len) commit(bar(Q_EMPTY));
+          }
+          __syncwarp();
+          ++s_issue;
+          ++k_use;
+          issued_any = true;
+        }
+        if (e == 0) continue;
+        // O += P(e-1) V(e-1)
+        const uint32_t vs = v_use % C::NV;
+        if (!(ok = wait_warp(bar(V_FULL + vs), (v_use / C::NV) & 1u, g))) break;
+        if (!(ok = wait_warp(bar(P_FULL), pv & 1u, g))) break;
+        if (e == 1 && !(ok = wait_warp(bar(O_EMPTY), (o_items & 1u) ^ 1u, g))) break;
+        fence_after();
+        const uint32_t vb = sV + vs * C::kKTile;
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < C::KR / 16; ++kk)
+            mma_ts(tmem + C::kColO, tmem + C::kColP + (uint32_t)kk * 8u,
+                   smem_desc(vb + (uint32_t)kk * 2048u, C::kKBox, 1024, kSwizzle128B), idO,
+                   (e > 1 || kk > 0) ? 1u : 0u);
+          commit(bar(V_EMPTY + vs));
+          commit(bar(PV_DONE));
+          if (e == len) commit(bar(O_FULL));
+        }
+        __syncwarp();
+        ++v_use;
+        ++pv;
+      }
+      if (!ok) break;
+      ++o_items;
+    }
+    if (*abort_flag && issued_any) {
+      if (elect_one()) commit(bar(TEAR));
+      __syncwarp();
+      wait_raw(bar(TEAR), 0, kDrainNs);
+    }
+    __syncwarp();
   } else if (warp == C::W_S) {
     // ------------------------------------------------------------ S = Q K^T issuer
     constexpr uint32_t idS = idesc_bf16(128, C::KR, 0, 0);
@@ -518,7 +612,9 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       wait_raw(bar(TEAR_PV), 0, kDrainNs);
     }
     __syncwarp();
+  }
   } else {
+    if constexpr (C::DUO) regs_increase<C::kRegSoftmax>();
     if constexpr (C::SPLIT) {
     // ------------------------------------------------------------ softmax + epilogue, d = 64
     // Warp w: lanes (rows) 32*(w & 3) .. +31 of the tile, columns [64g, 64g + 64)
@@ -747,91 +843,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           const uint32_t b = s_use % C::NSB;
           if (!(ok = wait_warp(bar(S_FULL + b), (s_use / C::NSB) & 1u, g))) break;
           fence_after();
-          if constexpr (C::DUO) {
-            const uint64_t gb = blocks_done + e;
-            const uint32_t sbase = t_row + C::kColS;
-            float rs[8];
-  #pragma unroll
-            for (int u = 0; u < 8; ++u) rs[u] = 0.f;
-            // P (one buffer) was last read by the PV of block g-1, and O must not change
-            // under it either: waited for before the first P store or O rescale
-            bool pv_waited = gb == 0;
-            // pass 1: the maximum of the selected 32-column chunks (the loaded values are
-            // dropped; this pass also covers the time the PV of block g-1 takes)
-            float mx = -INFINITY;
-  #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              if (q < 2 ? has1 : has2) {
-                uint32_t tmp[32];
-                const float cq = tmem_ld32_max(sbase + 32u * q, tmp);
-                wait_ld();
-                mx = fmaxf(mx, cq);
-              }
-            }
-            const float m_new = fmaxf(m, mx * sl2);
-            if (e == 0) {
-              m = m_new;
-            } else if (__any_sync(0xffffffffu, m_new > m + kRescaleThreshold)) {
-              if (!pv_waited) {
-                pv_waited = true;
-                if (!(ok = wait_warp(bar(PV_DONE), (uint32_t)((gb - 1) & 1u), g))) break;
-                fence_after();
-              }
-              const float f = ex2f(m - m_new);
-  #pragma unroll
-              for (int c = 0; c < D / 32; ++c) {
-                uint32_t ov[32];
-                tmem_ld32(t_row + C::kColO + c * 32u, ov);
-                wait_ld();
-  #pragma unroll
-                for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * f);
-                tmem_st32(t_row + C::kColO + c * 32u, ov);
-              }
-              wait_st();
-              l *= f;
-              m = m_new;
-            }
-            // pass 2: the exponentials, 32 columns at a time; S is free once its last
-            // chunk is loaded
-  #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const bool act = q < 2 ? has1 : has2;
-              uint32_t sv[32];
-              if (act) {
-                tmem_ld32(sbase + 32u * q, sv);
-                wait_ld();
-              }
-              if (q == 3) {
-                fence_before();
-                mbar_arrive(bar(S_FREE));
-              }
-              uint32_t pk[16];
-              if (act) {
-  #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                  const float p0 = ex2f(fmaf(__uint_as_float(sv[2 * c]), sl2, -m));
-                  const float p1 = ex2f(fmaf(__uint_as_float(sv[2 * c + 1]), sl2, -m));
-                  rs[c & 7] += p0 + p1;
-                  pk[c] = pack2(p0, p1);
-                }
-              } else {
-  #pragma unroll
-                for (int c = 0; c < 16; ++c) pk[c] = 0u;
-              }
-              if (!pv_waited) {
-                pv_waited = true;
-                if (!(ok = wait_warp(bar(PV_DONE), (uint32_t)((gb - 1) & 1u), g))) break;
-                fence_after();
-              }
-              tmem_st16(t_row + C::kColP + 16u * q, pk);
-            }
-            if (!ok) break;
-            ++s_use;
-            l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
-            wait_st();
-            fence_before();
-            mbar_arrive(bar(P_FULL));
-          } else {
+          {
           uint32_t s[C::KR];
           float cm[C::KR / 32];   // the maximum of each 32-column load (exact, as any order of max)
   #pragma unroll
@@ -847,25 +859,15 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   #pragma unroll
           for (int c = 1; c < C::KR / 32; ++c) mx = fmaxf(mx, cm[c]);
           const float m_new = fmaxf(m, mx * sl2);
+          // a rescale of O (by f) is applied after P is written, when the S row is
+          // no longer held in registers
+          bool resc = false;
+          float f = 1.f;
           if (e == 0) {
             m = m_new;
           } else if (__any_sync(0xffffffffu, m_new > m + kRescaleThreshold)) {
-            // O must not change under the PV of block g-1 (g = global block index)
-            const uint64_t gp = blocks_done + e - 1;
-            if (!(ok = wait_warp(bar(PV_DONE + (uint32_t)(gp % C::NPB)), (uint32_t)((gp / C::NPB) & 1u), g))) break;
-            fence_after();
-            const float f = ex2f(m - m_new);
-  #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t ov[32];
-              tmem_ld32(t_row + C::kColO + c * 32u, ov);
-              wait_ld();
-  #pragma unroll
-              for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * f);
-              tmem_st32(t_row + C::kColO + c * 32u, ov);
-            }
-            wait_st();
-            l *= f;
+            resc = true;
+            f = ex2f(m - m_new);
             m = m_new;
           }
           uint32_t pk[C::KR / 2];
@@ -889,8 +891,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
               for (int c = 32 * hh; c < 32 * hh + 32; ++c) pk[c] = 0u;
             }
           }
-          l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
-          // P buffer b was last read by the PV of block g-2
+          // P buffer b was last read by the PV of block g - NPB
           const uint64_t gb = blocks_done + e;
           if (gb >= (uint64_t)C::NPB) {
             if (!(ok = wait_warp(bar(PV_DONE + b), (uint32_t)(((gb - C::NPB) / C::NPB) & 1u), g))) break;
@@ -898,6 +899,23 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           }
   #pragma unroll
           for (int c = 0; c < C::KR / 64; ++c) tmem_st32(t_row + C::kColP + b * 64u + 32u * c, pk + 32 * c);
+          if (resc) {
+            // O must not change under the PV of block g-1 (g = global block index)
+            const uint64_t gp = gb - 1;
+            if (!(ok = wait_warp(bar(PV_DONE + (uint32_t)(gp % C::NPB)), (uint32_t)((gp / C::NPB) & 1u), g))) break;
+            fence_after();
+  #pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t ov[32];
+              tmem_ld32(t_row + C::kColO + c * 32u, ov);
+              wait_ld();
+  #pragma unroll
+              for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * f);
+              tmem_st32(t_row + C::kColO + c * 32u, ov);
+            }
+            l *= f;
+          }
+          l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
           wait_st();
           fence_before();
           mbar_arrive(bar(P_FULL + b));

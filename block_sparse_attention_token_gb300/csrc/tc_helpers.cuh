@@ -114,6 +114,21 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
                : "memory");
 }
 
+// Per-warpgroup register budget (setmaxnreg): every warp of a warpgroup runs
+// the same one. The budgets of a block's warpgroups must add up to no more
+// than the registers the block was launched with (threads x registers per
+// thread at launch), or an increase waits for registers that never come.
+template <uint32_t R>
+__device__ __forceinline__ void regs_increase() {
+  static_assert(R % 8 == 0 && R >= 24 && R <= 256, "setmaxnreg count");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(R));
+}
+template <uint32_t R>
+__device__ __forceinline__ void regs_decrease() {
+  static_assert(R % 8 == 0 && R >= 24 && R <= 256, "setmaxnreg count");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(R));
+}
+
 // True in exactly one active lane of the warp (tcgen05 ops are issued by one
 // thread while the whole warp keeps its control flow and values uniform).
 __device__ __forceinline__ bool elect_one() {
