@@ -126,7 +126,13 @@ struct Cfg {
   static constexpr uint32_t kOffRing = kOffBar + 8 * NBAR;
   static constexpr uint32_t kOffBits = kOffRing + 16 * NI;
   static constexpr uint32_t kBitsBytes = PAIR ? NI * 2 * MAXW * 4 : 0;
-  static constexpr uint32_t kOffStat = kOffBits + kBitsBytes;   // [2 parities][2 groups][128 rows] (m, l)
+  // DUO: per item slot, one byte per block of the union of the pair's rows in
+  // ascending order (byte 2s + t: block t of stage s; bit 0 = the first row
+  // selected it, bit 1 = the second), written by the producer with the item so
+  // that the softmax warps read a stage's masks with one shared-memory load
+  static constexpr uint32_t kMaskBytes = DUO ? 32 * MAXW : 0;
+  static constexpr uint32_t kOffMask = kOffBits + kBitsBytes;
+  static constexpr uint32_t kOffStat = kOffMask + NI * kMaskBytes;   // [2 parities][2 groups][128 rows] (m, l)
   static constexpr uint32_t kStatBytes = SPLIT ? 2 * 2 * 128 * 8 : 0;
   static constexpr uint32_t kOffMisc = kOffStat + kStatBytes;
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
@@ -257,6 +263,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   // ring entry: x = item, y = stages (-1: skip, -2: end), z = bad-row bits (pairs)
   volatile int4* ring = reinterpret_cast<volatile int4*>(gbase + C::kOffRing);
   uint32_t* bits = reinterpret_cast<uint32_t*>(gbase + C::kOffBits);   // [C::NI][2][C::MAXW] (pairs)
+  uint8_t* masks = gbase + C::kOffMask;                                 // [C::NI][C::kMaskBytes] (DUO)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + C::kOffMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -340,6 +347,31 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1) u += __shfl_xor_sync(0xffffffffu, u, off);
           len = (badbits == 3) ? -1 : (u + 1) / 2;   // stages of two key blocks
+          if constexpr (C::DUO) {
+            // the stage masks: the union's set bits ranked by a warp prefix sum
+            uint8_t* mk = masks + ri * C::kMaskBytes;
+            int base_rank = 0;
+            for (int w0 = 0; w0 < words; w0 += 32) {
+              const int w = w0 + lane;
+              const uint32_t a = w < words ? bmA[w] : 0u, bb = w < words ? bmB[w] : 0u;
+              uint32_t un = a | bb;
+              const int c = __popc(un);
+              int incl = c;
+#pragma unroll
+              for (int off = 1; off < 32; off <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += t;
+              }
+              int rk = base_rank + incl - c;
+              while (un != 0u) {
+                const int bit = __ffs(un) - 1;
+                un &= un - 1u;
+                mk[rk++] = (uint8_t)(((a >> bit) & 1u) | (((bb >> bit) & 1u) << 1));
+              }
+              base_rank += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if ((u & 1) && lane == 0) mk[u] = 0;   // a lone last block has no partner
+          }
         } else {
           const int32_t a = p.row_ptr[item], b = p.row_ptr[item + 1];
           bool bad = (b < a) || (b - a > nb);
@@ -830,12 +862,17 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         }
         const uint32_t* bmA = bits + ri * 2 * C::MAXW;
         const uint32_t* mine = bmA + half * C::MAXW;
-        UnionWalk walk(bmA, bmA + C::MAXW, PAIR ? words : 0);
+        UnionWalk walk(bmA, bmA + C::MAXW, PAIR && !C::DUO ? words : 0);
+        const uint16_t* mk = reinterpret_cast<const uint16_t*>(masks + ri * C::kMaskBytes);
         float m = -INFINITY, l = 0.f;
         for (int e = 0; e < len; ++e) {
           // which halves of this stage's 128 columns this row attends to (warp-uniform)
           bool has1 = true, has2 = true;
-          if constexpr (PAIR) {
+          if constexpr (C::DUO) {
+            const uint32_t st = mk[e];
+            has1 = (st >> half) & 1u;
+            has2 = (st >> (8 + half)) & 1u;
+          } else if constexpr (PAIR) {
             const int j1 = walk.next(), j2 = walk.next();
             has1 = bit_of(mine, j1);
             has2 = j2 >= 0 && bit_of(mine, j2);
