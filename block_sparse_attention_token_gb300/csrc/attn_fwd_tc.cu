@@ -14,14 +14,11 @@
 // "How DSV works": queries grouped so that one key set serves several).
 //
 // Persistent CTAs: one per SM with 7 warps (4 softmax warps, then the
-// producer, the S issuer and the PV issuer) for d = 128; one per SM with 11
-// warps (8 softmax warps in two groups, one per 64-column half of a stage,
-// each with its own running max, sum and O accumulator, combined once per
-// item; see Cfg::SPLIT) for 128-token blocks with d = 64; two per SM, each with
-// 8 warps (4 softmax warps, the producer, one warp issuing both GEMM streams,
-// two idle warps that only give their registers to the softmax warpgroup) and
-// half of the TMEM and shared memory (one S and one P buffer; see Cfg::DUO),
-// for 64-token blocks with d = 64:
+// producer, the S issuer and the PV issuer) for d = 128; two per SM for d = 64,
+// each with 8 warps (4 softmax warps, the producer, one warp issuing both GEMM
+// streams, two idle warps that only give their registers to the softmax
+// warpgroup) and half of the TMEM and shared memory (one S and one P buffer;
+// see Cfg::DUO):
 //   producer: pulls items longest-first through an atomic counter,
 //              validates the CSR row(s), publishes the item in a shared-memory
 //              ring (for pairs with the two rows as bitmaps), and TMA-loads the
@@ -32,10 +29,10 @@
 //              K=16 per instruction, both operands K-major from shared memory).
 //   PV issuer: O += P V (A = P read from TMEM as packed bf16,
 //              B = V MN-major from shared memory).
-//              The two GEMM streams are issued by different warps so that a
-//              wait in one (for P, or for a free S buffer) never holds back the
-//              other; each warp runs uniformly and one elected lane issues
-//              tcgen05.mma / tcgen05.commit.
+//              With d = 128 the two GEMM streams are issued by different warps
+//              so that a wait in one (for P, or for a free S buffer) never
+//              holds back the other; each warp runs uniformly and one elected
+//              lane issues tcgen05.mma / tcgen05.commit.
 //   softmax and epilogue: thread t owns query row t = TMEM lane t.
 //              It reads its S row from TMEM with the sm_103 load-with-maximum
 //              (tcgen05.ld.red: each 32-column load also returns the maximum of
@@ -49,9 +46,9 @@
 //              memory, LSE = (m + log2 l) ln 2 (O = 0, LSE = -inf for a row
 //              that attended to nothing). A warp's 32 rows belong to one query
 //              block, so the masks of a pair are warp-uniform.
-// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256,384) (SPLIT: O_a
-// [256,320) and O_b [320,384)), P0 [384,448), P1 [448,512); DUO (256 columns
-// per CTA): S [0,128), O [128,192), P [192,256). Every mbarrier wait is bounded (2 s); on expiry the CTA sets
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O [256,384), P0 [384,448),
+// P1 [448,512); DUO (256 columns per CTA): S [0,128), O [128,192),
+// P [192,256). Every mbarrier wait is bounded (2 s); on expiry the CTA sets
 // SPARSP_ERR_TIMEOUT, all roles leave their loops, copies and MMAs in flight
 // are drained with a second bounded wait, and TMEM is released.
 #include "tc_helpers.cuh"
@@ -66,7 +63,7 @@ enum Bar {
   Q_FULL = 0, Q_EMPTY, K_FULL, K_EMPTY = K_FULL + kMaxStages, V_FULL = K_EMPTY + kMaxStages,
   V_EMPTY = V_FULL + kMaxStages, S_FULL = V_EMPTY + kMaxStages, S_FREE = S_FULL + 2, P_FULL = S_FREE + 2, PV_DONE = P_FULL + 2, O_FULL = PV_DONE + 2,
   O_EMPTY,
-  I_FULL, I_EMPTY = I_FULL + kNI, TEAR = I_EMPTY + kNI, TEAR_PV, STAT, NBAR
+  I_FULL, I_EMPTY = I_FULL + kNI, TEAR = I_EMPTY + kNI, TEAR_PV, NBAR
 };
 // Tile geometry for blocks of BT tokens and head dimension D. The query tile
 // and a key/value stage are 128 rows each: one block, or two 64-token blocks
@@ -77,23 +74,18 @@ template <int BT_, int D_>
 struct Cfg {
   static constexpr int BT = BT_, D = D_, QR = 128, KR = 128;
   static constexpr bool PAIR = BT == 64;
-  // 64-token blocks with d = 64: two CTAs per SM, each with half of the TMEM
+  // d = 64 (64- or 128-token blocks): two CTAs per SM, each with half of the TMEM
   // (one S buffer [0,128), O [128,192), one P buffer [192,256)) and half of
   // the shared memory (3 K and 2 V stages), so that one CTA's softmax runs
   // while the other's MMAs keep the tensor pipe busy. The softmax warps hold
   // a whole 128-column S row in registers (one pass per stage, S released as
   // soon as it is loaded) with the 200 registers the register split below
   // gives them.
-  static constexpr bool DUO = BT == 64 && D == 64;
-  // 128-token blocks with d = 64: two softmax warpgroups, one per 64-column
-  // half of a stage, each with its own running max, sum and O accumulator
-  // (TMEM O_a [256,320), O_b [320,384)), combined once per item. Two softmax
-  // warps per SM sub-partition hide each other's latencies.
-  static constexpr bool SPLIT = D == 64 && !DUO;
-  static constexpr int NSM = SPLIT ? 8 : 4;               // softmax warps
-  // MMA issuer warps: S and PV each get their own, except with DUO, where one
-  // warp issues both streams so that two CTAs of 6 warps leave a thread 168
-  // registers (a whole 128-column S row held in registers: one pass per stage)
+  static constexpr bool DUO = D == 64;
+  static constexpr int NSM = 4;                           // softmax warps
+  // MMA issuer warps: S and PV each get their own with d = 128; with DUO one
+  // warp issues both streams (the softmax releases S(e-1) before it writes
+  // P(e-1), so S(e) then PV(e-1) in one warp never wait on each other)
   static constexpr int NIS = DUO ? 1 : 2;
   // DUO: two idle warps complete the second warpgroup (producer, issuer), so
   // that the softmax warpgroup can take registers from it (setmaxnreg works
@@ -106,10 +98,9 @@ struct Cfg {
   static constexpr uint32_t kRegSoftmax = 200, kRegAux = 56;
   static_assert(!DUO || (THREADS == 256 && NSM == 4 && 128 * (kRegSoftmax + kRegAux) == 256 * 128),
                 "register split of the two warpgroups");
-  // K and V ring stages: 3 fit beside a d = 128 query tile; with d = 64 the
-  // tiles are half the size and 6 stages keep more L2 loads in flight (a stage
-  // then takes half the tensor time, so the same latency needs twice the depth)
-  static constexpr int NK = DUO ? 3 : (D == 64 ? 6 : 3), NV = DUO ? 2 : NK;
+  // K and V ring stages: 3 of each fit beside a d = 128 query tile; a DUO CTA
+  // has half of the SM's shared memory for tiles of half the size: 3 K and 2 V
+  static constexpr int NK = 3, NV = DUO ? 2 : 3;
   static constexpr int NSB = DUO ? 1 : 2, NPB = DUO ? 1 : 2;   // S and P buffers in TMEM
   static constexpr int NI = DUO ? 2 : kNI;                      // item ring slots
   static constexpr int kMinCtas = DUO ? 2 : 1;                  // CTAs per SM
@@ -130,11 +121,9 @@ struct Cfg {
   // ascending order (byte 2s + t: block t of stage s; bit 0 = the first row
   // selected it, bit 1 = the second), written by the producer with the item so
   // that the softmax warps read a stage's masks with one shared-memory load
-  static constexpr uint32_t kMaskBytes = DUO ? 32 * MAXW : 0;
+  static constexpr uint32_t kMaskBytes = DUO && PAIR ? 32 * MAXW : 0;
   static constexpr uint32_t kOffMask = kOffBits + kBitsBytes;
-  static constexpr uint32_t kOffStat = kOffMask + NI * kMaskBytes;   // [2 parities][2 groups][128 rows] (m, l)
-  static constexpr uint32_t kStatBytes = SPLIT ? 2 * 2 * 128 * 8 : 0;
-  static constexpr uint32_t kOffMisc = kOffStat + kStatBytes;
+  static constexpr uint32_t kOffMisc = kOffMask + NI * kMaskBytes;
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
   static_assert(kSmemBytes <= (DUO ? 115712u : 232448u), "shared memory");
 };
@@ -296,7 +285,6 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     }
     mbar_init(bar(TEAR), 1);
     mbar_init(bar(TEAR_PV), 1);
-    mbar_init(bar(STAT), 32 * C::NSM);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -610,22 +598,11 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         fence_after();
         const uint32_t vb = sV + vs * C::kKTile;
         if (elect_one()) {
-          if constexpr (C::SPLIT) {
-            // O_g += P_g V[64g, 64g + 64): the keys of half g into accumulator g
 #pragma unroll
-            for (int hg = 0; hg < 2; ++hg)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_ts(tmem + C::kColO + (uint32_t)hg * 64u, tmem + C::kColP + b * 64u + (uint32_t)hg * 32u + (uint32_t)kk * 8u,
-                       smem_desc(vb + (uint32_t)(hg * 4 + kk) * 2048u, C::kKBox, 1024, kSwizzle128B), idO,
-                       (e > 0 || kk > 0) ? 1u : 0u);
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < C::KR / 16; ++kk)
-              mma_ts(tmem + C::kColO, tmem + C::kColP + b * 64u + (uint32_t)kk * 8u,
-                     smem_desc(vb + (uint32_t)kk * 2048u, C::kKBox, 1024, kSwizzle128B), idO,
-                     (e > 0 || kk > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < C::KR / 16; ++kk)
+            mma_ts(tmem + C::kColO, tmem + C::kColP + b * 64u + (uint32_t)kk * 8u,
+                   smem_desc(vb + (uint32_t)kk * 2048u, C::kKBox, 1024, kSwizzle128B), idO,
+                   (e > 0 || kk > 0) ? 1u : 0u);
           commit(bar(V_EMPTY + vs));
           commit(bar(PV_DONE + b));
           if (e + 1 == len) commit(bar(O_FULL));
@@ -647,170 +624,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   }
   } else {
     if constexpr (C::DUO) regs_increase<C::kRegSoftmax>();
-    if constexpr (C::SPLIT) {
-    // ------------------------------------------------------------ softmax + epilogue, d = 64
-    // Warp w: lanes (rows) 32*(w & 3) .. +31 of the tile, columns [64g, 64g + 64)
-    // of every stage with g = w >> 2: group g owns one half of the stage's keys
-    // (one key block of a pair), with its own max m, sum l and accumulator O_g.
-    const int grp = warp >> 2;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t t_row = tmem + lane_base;
-    const int r = (warp & 3) * 32 + lane;   // tile row = TMEM lane
-    uint32_t it_use = 0, s_use = 0, o_items = 0;
-    uint64_t blocks_done = 0;
-    const float sl2 = p.scale_log2;
-    const int half = PAIR ? (r >> 6) : 0;   // with pairs: the row's query block within the pair
-    float2* stat = reinterpret_cast<float2*>(gbase + C::kOffStat);   // [parity][group][row]
-    bool ok = true;
-    for (;;) {
-      const int ri = (int)(it_use % C::NI);
-      if (!wait_warp(bar(I_FULL + ri), (it_use / C::NI) & 1u, g)) break;
-      const int64_t item = ring[ri].x;
-      const int len = ring[ri].y;
-      const int badbits = ring[ri].z;
-      __syncwarp();
-      auto release = [&]() {
-        if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
-      };
-      if (!PAIR) release();
-      ++it_use;
-      if (len == -2) {
-        if (PAIR) release();
-        break;
-      }
-      if (len == -1) {
-        if (PAIR) release();
-        continue;
-      }
-      const int64_t bh = item / nbp;
-      const int i = PAIR ? 2 * (int)(item % nbp) + half : (int)(item % nb);
-      const int o = PAIR ? (r & 63) : r;
-      const int64_t row = bh * p.N + (int64_t)i * BT + o;
-      bool stores = o < BT && i < nb && !((badbits >> half) & 1);
-      int64_t orow_idx = row;
-      if (p.raster && stores) orow_idx = p.rm.row(bh, i, o);
-      // this group stores columns [32*grp, 32*grp + 32) of the row
-      if (stores) stores = dcheck(row < p.rows_total && orow_idx >= 0 && orow_idx < p.rows_total, p.d_status);
-      uint4* orow = reinterpret_cast<uint4*>(p.o + orow_idx * D) + grp * 4;
-      if (len == 0) {
-        if (stores) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) orow[c] = make_uint4(0, 0, 0, 0);
-          if (grp == 0) p.lse[row] = -INFINITY;
-        }
-        if (PAIR) release();
-        continue;
-      }
-      const uint32_t* bmA = bits + ri * 2 * C::MAXW;
-      const uint32_t* mine = bmA + half * C::MAXW;
-      UnionWalk walk(bmA, bmA + C::MAXW, PAIR ? words : 0);
-      float m = -INFINITY, l = 0.f;
-      for (int e = 0; e < len; ++e) {
-        // does this row attend to this group's key block of the stage (warp-uniform)
-        bool has = true;
-        if constexpr (PAIR) {
-          const int j1 = walk.next(), j2 = walk.next();
-          const int j = grp == 0 ? j1 : j2;
-          has = j >= 0 && bit_of(mine, j);
-        }
-        const uint32_t b = s_use % C::NSB;
-        if (!(ok = wait_warp(bar(S_FULL + b), (s_use / C::NSB) & 1u, g))) break;
-        fence_after();
-        uint32_t sv[64];
-        float cm0 = tmem_ld32_max(t_row + C::kColS + b * 128u + (uint32_t)grp * 64u, sv);
-        float cm1 = tmem_ld32_max(t_row + C::kColS + b * 128u + (uint32_t)grp * 64u + 32u, sv + 32);
-        wait_ld();
-        fence_before();
-        mbar_arrive(bar(S_FREE + b));
-        ++s_use;
-        if (!has) cm0 = cm1 = -INFINITY;
-        const float m_new = fmaxf(m, fmaxf(cm0, cm1) * sl2);
-        if (e == 0) {
-          m = m_new;
-        } else if (__any_sync(0xffffffffu, m_new > m + kRescaleThreshold)) {
-          // O_grp must not change under the PV of block g-1
-          const uint64_t gp = blocks_done + e - 1;
-          if (!(ok = wait_warp(bar(PV_DONE + (uint32_t)(gp % C::NPB)), (uint32_t)((gp / C::NPB) & 1u), g))) break;
-          fence_after();
-          const float f = ex2f(m - m_new);
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t ov[32];
-            const uint32_t a = t_row + C::kColO + (uint32_t)grp * 64u + c * 32u;
-            tmem_ld32(a, ov);
-            wait_ld();
-#pragma unroll
-            for (int x = 0; x < 32; ++x) ov[x] = __float_as_uint(__uint_as_float(ov[x]) * f);
-            tmem_st32(a, ov);
-          }
-          wait_st();
-          l *= f;
-          m = m_new;
-        }
-        uint32_t pk[32];
-        float rs[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) rs[u] = 0.f;
-        if (has) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float p0 = ex2f(fmaf(__uint_as_float(sv[2 * c]), sl2, -m));
-            const float p1 = ex2f(fmaf(__uint_as_float(sv[2 * c + 1]), sl2, -m));
-            rs[c & 7] += p0 + p1;
-            pk[c] = pack2(p0, p1);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) pk[c] = 0u;
-        }
-        l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
-        // P buffer b was last read by the PV of block g-2
-        const uint64_t gb = blocks_done + e;
-        if (gb >= (uint64_t)C::NPB) {
-          if (!(ok = wait_warp(bar(PV_DONE + b), (uint32_t)(((gb - C::NPB) / C::NPB) & 1u), g))) break;
-          fence_after();
-        }
-        tmem_st32(t_row + C::kColP + b * 64u + (uint32_t)grp * 32u, pk);
-        wait_st();
-        fence_before();
-        mbar_arrive(bar(P_FULL + b));
-      }
-      if (PAIR) release();
-      if (!ok) break;
-      blocks_done += (uint64_t)len;
-      if (!(ok = wait_warp(bar(O_FULL), o_items & 1u, g))) break;
-      fence_after();
-      // combine the two groups' partial softmax sums: exchange (m, l) per row
-      const uint32_t par = o_items & 1u;
-      stat[(par * 2 + grp) * 128 + r] = make_float2(m, l);
-      mbar_arrive(bar(STAT));
-      if (!(ok = wait_warp(bar(STAT), par, g))) break;
-      const float2 st0 = stat[(par * 2 + 0) * 128 + r], st1 = stat[(par * 2 + 1) * 128 + r];
-      ++o_items;
-      const float M = fmaxf(st0.x, st1.x);
-      const float f0 = st0.y > 0.f ? ex2f(st0.x - M) : 0.f;
-      const float f1 = st1.y > 0.f ? ex2f(st1.x - M) : 0.f;
-      const float L = st0.y * f0 + st1.y * f1;
-      const float inv = L > 0.f ? 1.0f / L : 0.f;
-      const float a0 = f0 * inv, a1 = f1 * inv;
-      uint32_t oa[32], ob[32];
-      tmem_ld32(t_row + C::kColO + (uint32_t)grp * 32u, oa);
-      tmem_ld32(t_row + C::kColO + 64u + (uint32_t)grp * 32u, ob);
-      wait_ld();
-      fence_before();
-      mbar_arrive(bar(O_EMPTY));
-      if (stores) {
-        uint32_t w[16];
-#pragma unroll
-        for (int x = 0; x < 16; ++x)
-          w[x] = pack2(fmaf(__uint_as_float(oa[2 * x]), a0, __uint_as_float(ob[2 * x]) * a1),
-                       fmaf(__uint_as_float(oa[2 * x + 1]), a0, __uint_as_float(ob[2 * x + 1]) * a1));
-#pragma unroll
-        for (int x = 0; x < 4; ++x) orow[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
-        if (grp == 0) p.lse[row] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
-      }
-    }
-    } else {
+    {
     // ------------------------------------------------------------ softmax + epilogue
       const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
       const uint32_t t_row = tmem + lane_base;
@@ -868,7 +682,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         for (int e = 0; e < len; ++e) {
           // which halves of this stage's 128 columns this row attends to (warp-uniform)
           bool has1 = true, has2 = true;
-          if constexpr (C::DUO) {
+          if constexpr (C::DUO && PAIR) {
             const uint32_t st = mk[e];
             has1 = (st >> half) & 1u;
             has2 = (st >> (8 + half)) & 1u;

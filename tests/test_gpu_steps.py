@@ -674,7 +674,7 @@ def test_attn_fwd_raster_output(name):
 
 
 @pytest.mark.parametrize("portable", [False, True])
-@pytest.mark.parametrize("name", ["r128", "tiny", "r64", "medium", "r64odd"])
+@pytest.mark.parametrize("name", ["r128", "tiny", "r64", "medium", "r64odd", "r128d64"])
 def test_attn_fwd_empty_and_bad_rows(name, portable):
     wl, data, shape = _setup(name)
     ch = OracleChain(wl, data)
