@@ -76,10 +76,10 @@ L2_BYTES = 129e6          # GB300 L2; a stage whose bytes fit was fed from L2, n
 EXTRA_WORKLOADS = ("skewed", "training", "medium", "tiny")
 
 # DRAM bytes (read + write) per launch of the tcgen05 forward kernel, from an ncu capture of the
-# Wan-layer shape with 8 of its 40 heads (237.2 MB: Q, K, V read once, O written), scaled by the
+# Wan-layer shape with 8 of its 40 heads (237.3 MB: Q, K, V read once, O written), scaled by the
 # heads a full launch processes; the traffic grows with the heads, each head's tiles being
 # independent. The algorithmic bytes are Q + K + V + O + LSE = 1,263 MB.
-ATTN_TRAFFIC = {"wan14b-layer-30k-bf16": 237.2e6 * 40 / 8}
+ATTN_TRAFFIC = {"wan14b-layer-30k-bf16": 237.3e6 * 40 / 8}
 
 
 def attn_flops(nnz: int, wl) -> float:
