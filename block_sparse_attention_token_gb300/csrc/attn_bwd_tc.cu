@@ -1,4 +1,4 @@
-// Step 5b, bf16, Bt = d = 128 on sm_103a: block-sparse attention backward on
+// Step 5b, bf16, Bt = 128 and d = 64 or 128 on sm_103a: block-sparse attention backward on
 // the tcgen05 tensor cores, as persistent kernels of one template: mode 0 and
 // mode 3 by default, modes 0, 1 and 2 when dK and dV are asked for apart.
 //
@@ -8,11 +8,12 @@
 //                S^T = K_j Q_c^T, dP^T = V_j dO_c^T, dS^T = P^T (dP^T - D), dK += dS^T Q_c.
 //   mode 2 (dV): item = key block j, as mode 1.  S^T = K_j Q_c^T, dV += P^T dO_c.
 //   mode 3 (dK and dV): modes 1 and 2 in one pass, both accumulators in TMEM
-//                [256,384) and [384,512); P^T is written over S^T and dS^T over
-//                dP^T, and the row tiles K_j, V_j stay in shared memory (no
-//                TMEM left for them), so S^T and dP^T take both operands from
-//                shared memory; the row tiles are released by an MMA commit
-//                after the item's last S^T / dP^T.
+//                (dK [256,256+d), dV [256+d,256+2d)); P^T is written over S^T and
+//                dS^T over dP^T. With d = 128 the row tiles K_j, V_j stay in
+//                shared memory (no TMEM left for them), so S^T and dP^T take
+//                both operands from shared memory and the row tiles are
+//                released by an MMA commit after the item's last S^T / dP^T;
+//                with d = 64 they fit in TMEM as in the other modes.
 // with P = exp2(S * scale*log2e - LSE*log2e) from the forward's LSE (no online
 // maximum is needed), D = rowsum(dO * O), and dQ, dK scaled by `scale` at the
 // end. Each column block is processed in two halves of 64 columns, double
@@ -20,14 +21,16 @@
 // tensor pipe computes the next half's S and dP and the previous half's
 // accumulate: half buffer b holds S_b [128b, 128b+64) and dP_b
 // [128b+64, 128b+128), and the half's bf16 operand X (P or dS) is written over
-// the first 32 columns of S_b; the fp32 accumulator is [256,384); the item's
-// row tiles A1 [384,448) and A2 [448,512) sit in TMEM as packed bf16, so every
+// the first 32 columns of S_b; the fp32 accumulator is [256,256+d); the item's
+// row tiles A1 [384,384+d/2) and A2 [384+d/2,384+d) sit in TMEM as packed bf16, so every
 // MMA takes A from TMEM and only B from shared memory (a 128x64x16 MMA with
 // both operands in shared memory is bound by shared-memory bandwidth at 62% of
 // the tensor rate; with A in TMEM it runs at the full rate). A half buffer is
 // free again once the accumulate MMA that read its X has completed. The dQ
 // and the dK/dV kernels recompute S (and dP) instead of sharing it so that
-// each fits TMEM. Modes 0-2 are laid out as above; mode 3 as described with it.
+// each fits TMEM. Modes 0-2 (and mode 3 with d = 64) are laid out as above;
+// mode 3 with d = 128 as described with it. With d = 64 the column tiles are
+// half the size and the ring holds 4 of them instead of 2.
 // Sums are taken in a fixed order (no atomics), so results are bitwise
 // reproducible. The gradient rows go to block order, or straight to their
 // raster rows (the layout of the inverse reorder) when asked.
@@ -61,27 +64,39 @@ namespace {
 
 using namespace tc;
 
-constexpr int BT = 128, D = 128;
-constexpr int kNS = 2, kNI = 4;
-constexpr uint32_t kTile = BT * D * 2;        // 32 KB
-constexpr uint32_t kHalfTile = BT * 64 * 2;   // one 64-column swizzled box
+constexpr int BT = 128;
+constexpr int kMaxNS = 4, kNI = 4;
+constexpr uint32_t kBox = BT * 64 * 2;        // one 64-column swizzled box of a 128-row tile
 constexpr uint32_t kStats = 1024;             // LSE*log2e [128] + D [128] of a column block
 constexpr int kThreads = 224;
-constexpr uint32_t kColAcc = 256, kColA1 = 384, kColA2 = 448;
-constexpr uint32_t kColAcc2 = 384;   // mode 3: the dV accumulator (A1, A2 stay in shared memory)
 constexpr int HB = 64;   // columns of a half block
-constexpr uint32_t kOffA2 = kTile, kOffStage = 2 * kTile;
-constexpr uint32_t kStageBytes = 2 * kTile + kStats;   // a multiple of 1024: tiles stay aligned
-constexpr uint32_t kOffBar = kOffStage + kNS * kStageBytes;
 enum Bar {
-  A_FULL = 0, A_EMPTY, AT_FULL, C_FULL, C_EMPTY = C_FULL + kNS, SD_FULL = C_EMPTY + kNS,
+  A_FULL = 0, A_EMPTY, AT_FULL, C_FULL, C_EMPTY = C_FULL + kMaxNS, SD_FULL = C_EMPTY + kMaxNS,
   X_FULL = SD_FULL + 2,
   X_DONE = X_FULL + 2, ACC_FULL = X_DONE + 2, ACC_EMPTY, I_FULL, I_EMPTY = I_FULL + kNI,
   TEAR = I_EMPTY + kNI, TEAR2, NBAR
 };
-constexpr uint32_t kOffRing = kOffBar + 8 * NBAR;
-constexpr uint32_t kOffMisc = kOffRing + 8 * kNI;
-constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
+// Tile geometry, shared-memory layout and TMEM map for head dimension D
+// (64 or 128): row and column tiles are 128 x D (D / 64 boxes of 64 columns);
+// TMEM holds the two half buffers [0,256), the accumulator(s) from 256
+// (mode 3: dK [256, 256+D), dV [256+D, 256+2D)) and, where the row tiles live
+// in TMEM, A1 [384, 384+D/2) and A2 [384+D/2, 384+D) as packed bf16.
+template <int D_>
+struct BCfg {
+  static constexpr int D = D_;
+  static constexpr int NBOX = D / 64;
+  static constexpr uint32_t kTile = BT * D * 2;
+  static constexpr int kNS = D == 64 ? 4 : 2;   // column-tile stages
+  static constexpr uint32_t kColAcc = 256, kColAcc2 = 256 + D;
+  static constexpr uint32_t kColA1 = 384, kColA2 = 384 + D / 2;
+  static constexpr uint32_t kOffA2 = kTile, kOffStage = 2 * kTile;
+  static constexpr uint32_t kStageBytes = 2 * kTile + kStats;   // a multiple of 1024: tiles stay aligned
+  static constexpr uint32_t kOffBar = kOffStage + kNS * kStageBytes;
+  static constexpr uint32_t kOffRing = kOffBar + 8 * NBAR;
+  static constexpr uint32_t kOffMisc = kOffRing + 8 * kNI;
+  static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
+  static_assert(kNS <= kMaxNS && kSmemBytes <= 232448u, "shared memory");
+};
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
 
@@ -125,28 +140,34 @@ struct Params {
   RasterMap rm;
 };
 
-template <int MODE>
+template <int MODE, int D>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constant__ CUtensorMap ta2,
                    const __grid_constant__ CUtensorMap tb1, const __grid_constant__ CUtensorMap tb2,
                    const Params p) {
+  using C = BCfg<D>;
   constexpr bool kHasDP = MODE != 2;
+  // the item's row tiles as the A operand in TMEM; mode 3 with d = 128 has no
+  // TMEM left beside its two accumulators and reads them from shared memory
+  constexpr bool kRowsInTmem = MODE != 3 || D == 64;
+  constexpr uint32_t kTile = C::kTile, kStageBytes = C::kStageBytes;
+  constexpr int kNS = C::kNS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t sA1 = base, sA2 = base + kOffA2;
-  auto stage = [&](uint32_t st) -> uint32_t { return base + kOffStage + st * kStageBytes; };
-  auto bar = [&](int idx) -> uint32_t { return base + kOffBar + 8u * (uint32_t)idx; };
-  volatile int2* ring = reinterpret_cast<volatile int2*>(gbase + kOffRing);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kOffMisc);
-  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + kOffMisc + 4);
+  const uint32_t sA1 = base, sA2 = base + C::kOffA2;
+  auto stage = [&](uint32_t st) -> uint32_t { return base + C::kOffStage + st * kStageBytes; };
+  auto bar = [&](int idx) -> uint32_t { return base + C::kOffBar + 8u * (uint32_t)idx; };
+  volatile int2* ring = reinterpret_cast<volatile int2*>(gbase + C::kOffRing);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + C::kOffMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t t_start = globaltimer_ns();
 
   if (threadIdx.x == 0) {
     mbar_init(bar(A_FULL), 1);
-    mbar_init(bar(A_EMPTY), MODE == 3 ? 1 : 128);   // mode 3: an MMA commit
+    mbar_init(bar(A_EMPTY), kRowsInTmem ? 128 : 1);   // else an MMA commit
     mbar_init(bar(AT_FULL), 128);
     for (int s = 0; s < kNS; ++s) {
       mbar_init(bar(C_FULL + s), 1);
@@ -228,11 +249,10 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
       if (!wait_warp(bar(A_EMPTY), (a_fill & 1u) ^ 1u, g)) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(bar(A_FULL), kHasDP ? 2 * kTile : kTile);
-        tma_load_2d(sA1, &ta1, bar(A_FULL), 0, ya);
-        tma_load_2d(sA1 + kHalfTile, &ta1, bar(A_FULL), 64, ya);
-        if (kHasDP) {
-          tma_load_2d(sA2, &ta2, bar(A_FULL), 0, ya);
-          tma_load_2d(sA2 + kHalfTile, &ta2, bar(A_FULL), 64, ya);
+#pragma unroll
+        for (int h = 0; h < C::NBOX; ++h) {
+          tma_load_2d(sA1 + h * kBox, &ta1, bar(A_FULL), 64 * h, ya);
+          if (kHasDP) tma_load_2d(sA2 + h * kBox, &ta2, bar(A_FULL), 64 * h, ya);
         }
       }
       ++a_fill;
@@ -248,10 +268,11 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
         if (lane == 0) {
           const uint32_t sb = stage(st);
           mbar_arrive_expect_tx(bar(C_FULL + st), 2 * kTile + (MODE != 0 ? kStats : 0u));
-          tma_load_2d(sb, &tb1, bar(C_FULL + st), 0, yc);
-          tma_load_2d(sb + kHalfTile, &tb1, bar(C_FULL + st), 64, yc);
-          tma_load_2d(sb + kTile, &tb2, bar(C_FULL + st), 0, yc);
-          tma_load_2d(sb + kTile + kHalfTile, &tb2, bar(C_FULL + st), 64, yc);
+#pragma unroll
+          for (int h = 0; h < C::NBOX; ++h) {
+            tma_load_2d(sb + h * kBox, &tb1, bar(C_FULL + st), 64 * h, yc);
+            tma_load_2d(sb + kTile + h * kBox, &tb2, bar(C_FULL + st), 64 * h, yc);
+          }
           if (MODE != 0) {
             bulk_load(sb + 2 * kTile, p.lse2 + yc64, 512, bar(C_FULL + st));
             bulk_load(sb + 2 * kTile + 512, p.delta + yc64, 512, bar(C_FULL + st));
@@ -281,8 +302,8 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
       if (ent.y == -2) break;
       if (ent.y <= 0) continue;
       const int len = ent.y;
-      // the item's row tiles: in TMEM (modes 0-2), in shared memory (mode 3)
-      if (!wait_warp(bar(MODE == 3 ? A_FULL : AT_FULL), a_use & 1u, g)) break;
+      // the item's row tiles: in TMEM, or in shared memory (mode 3 with d = 128)
+      if (!wait_warp(bar(kRowsInTmem ? AT_FULL : A_FULL), a_use & 1u, g)) break;
       ++a_use;
       fence_after();
       bool ok = true;
@@ -297,17 +318,17 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
           fence_after();
           // rows [64h, 64h+64) of the column tile: 64 rows x 128 B = 8 KB into each box
           const uint32_t rows_h = (uint32_t)h * (HB * 128u);
-          if constexpr (MODE == 3) {
+          if constexpr (!kRowsInTmem) {
             if (elect_one()) {
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
+                const uint32_t off = (uint32_t)(kk >> 2) * kBox + (uint32_t)(kk & 3) * 32u;
                 mma_ss(tmem + 128u * b, smem_desc(sA1 + off, 16, 1024, kSwizzle128B),
                        smem_desc(sb + rows_h + off, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
               }
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
+                const uint32_t off = (uint32_t)(kk >> 2) * kBox + (uint32_t)(kk & 3) * 32u;
                 mma_ss(tmem + 128u * b + HB, smem_desc(sA2 + off, 16, 1024, kSwizzle128B),
                        smem_desc(sb + kTile + rows_h + off, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
               }
@@ -316,15 +337,15 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
           } else if (elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
-              mma_ts(tmem + 128u * b, tmem + kColA1 + (uint32_t)kk * 8u,
+              const uint32_t off = (uint32_t)(kk >> 2) * kBox + (uint32_t)(kk & 3) * 32u;
+              mma_ts(tmem + 128u * b, tmem + C::kColA1 + (uint32_t)kk * 8u,
                      smem_desc(sb + rows_h + off, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
             }
             if (kHasDP) {
 #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (uint32_t)(kk >> 2) * kHalfTile + (uint32_t)(kk & 3) * 32u;
-                mma_ts(tmem + 128u * b + HB, tmem + kColA2 + (uint32_t)kk * 8u,
+                const uint32_t off = (uint32_t)(kk >> 2) * kBox + (uint32_t)(kk & 3) * 32u;
+                mma_ts(tmem + 128u * b + HB, tmem + C::kColA2 + (uint32_t)kk * 8u,
                        smem_desc(sb + kTile + rows_h + off, 16, 1024, kSwizzle128B), idS, kk > 0 ? 1u : 0u);
               }
             }
@@ -337,7 +358,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
         ++c_use;
       }
       if (!ok) break;
-      if (MODE == 3) {   // the row tiles are free once this item's S^T and dP^T are done
+      if (!kRowsInTmem) {   // the row tiles are free once this item's S^T and dP^T are done
         if (elect_one()) commit(bar(A_EMPTY));
         __syncwarp();
       }
@@ -350,7 +371,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
     __syncwarp();
   } else if (warp == 6) {
     // ------------------------------------------------------------ accumulate issuer
-    constexpr uint32_t idAcc = idesc_bf16(128, 128, 0, 1);
+    constexpr uint32_t idAcc = idesc_bf16(128, D, 0, 1);
     // the column tile the accumulator multiplies: K_c / Q_c (B1) or dO_c (B2)
     constexpr uint32_t kB3 = MODE == 2 ? kTile : 0u;
     uint32_t it_use = 0, c_use = 0, hg = 0, acc_items = 0;
@@ -381,19 +402,19 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
               const uint32_t bq = stage(st), bdo = stage(st) + kTile;
 #pragma unroll
               for (int kk = 0; kk < HB / 16; ++kk)   // dV += P^T dO_c
-                mma_ts(tmem + kColAcc2, tmem + 128u * b + (uint32_t)kk * 8u,
-                       smem_desc(bdo + (uint32_t)(4 * h + kk) * 2048u, 16384, 1024, kSwizzle128B), idAcc,
+                mma_ts(tmem + C::kColAcc2, tmem + 128u * b + (uint32_t)kk * 8u,
+                       smem_desc(bdo + (uint32_t)(4 * h + kk) * 2048u, kBox, 1024, kSwizzle128B), idAcc,
                        acc | (kk > 0 ? 1u : 0u));
 #pragma unroll
               for (int kk = 0; kk < HB / 16; ++kk)   // dK += dS^T Q_c
-                mma_ts(tmem + kColAcc, tmem + 128u * b + HB + (uint32_t)kk * 8u,
-                       smem_desc(bq + (uint32_t)(4 * h + kk) * 2048u, 16384, 1024, kSwizzle128B), idAcc,
+                mma_ts(tmem + C::kColAcc, tmem + 128u * b + HB + (uint32_t)kk * 8u,
+                       smem_desc(bq + (uint32_t)(4 * h + kk) * 2048u, kBox, 1024, kSwizzle128B), idAcc,
                        acc | (kk > 0 ? 1u : 0u));
             } else {
 #pragma unroll
               for (int kk = 0; kk < HB / 16; ++kk)
-                mma_ts(tmem + kColAcc, tmem + 128u * b + (uint32_t)kk * 8u,
-                       smem_desc(b3 + (uint32_t)(4 * h + kk) * 2048u, 16384, 1024, kSwizzle128B), idAcc,
+                mma_ts(tmem + C::kColAcc, tmem + 128u * b + (uint32_t)kk * 8u,
+                       smem_desc(b3 + (uint32_t)(4 * h + kk) * 2048u, kBox, 1024, kSwizzle128B), idAcc,
                        acc | (kk > 0 ? 1u : 0u));
             }
             commit(bar(X_DONE + b));
@@ -426,7 +447,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
     // one accumulator (128 columns at col) -> bf16 output row
     auto acc_out = [&](uint32_t col, float scale, uint4* orow) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(t_row + col + c * 32u, o);
         wait_ld();
@@ -443,30 +464,30 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
       if (!wait_warp(bar(ACC_FULL), acc_items & 1u, g)) return false;
       ++acc_items;
       fence_after();
-      acc_out(kColAcc, p.out_scale, orow);
-      if (MODE == 3) acc_out(kColAcc2, p.out_scale2, orow2);
+      acc_out(C::kColAcc, p.out_scale, orow);
+      if (MODE == 3) acc_out(C::kColAcc2, p.out_scale2, orow2);
       fence_before();
       mbar_arrive(bar(ACC_EMPTY));
       return true;
     };
-    // this thread's row of a 128x128 row tile (two 64-column boxes, 128-byte
-    // swizzle: 16-byte chunk c of row t sits at chunk c ^ (t & 7)) -> 64 TMEM columns
+    // this thread's row of a 128xD row tile (D/64 boxes of 64 columns, 128-byte
+    // swizzle: 16-byte chunk c of row t sits at chunk c ^ (t & 7)) -> D/2 TMEM columns
     auto row_to_tmem = [&](uint32_t tile_off, uint32_t col) {
       const int t = threadIdx.x;
-      uint32_t w[64];
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+      for (int h = 0; h < C::NBOX; ++h) {
+        uint32_t w[32];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(gbase + tile_off + (uint32_t)h * kHalfTile +
+          const uint4 v = *reinterpret_cast<const uint4*>(gbase + tile_off + (uint32_t)h * kBox +
                                                           (uint32_t)t * 128u + (uint32_t)((c ^ (t & 7)) * 16));
-          w[32 * h + 4 * c] = v.x;
-          w[32 * h + 4 * c + 1] = v.y;
-          w[32 * h + 4 * c + 2] = v.z;
-          w[32 * h + 4 * c + 3] = v.w;
+          w[4 * c] = v.x;
+          w[4 * c + 1] = v.y;
+          w[4 * c + 2] = v.z;
+          w[4 * c + 3] = v.w;
         }
-      tmem_st32(t_row + col, w);
-      tmem_st32(t_row + col + 32u, w + 32);
+        tmem_st32(t_row + col + 32u * h, w);
+      }
     };
     for (;;) {
       const int ri = (int)(it_use % kNI);
@@ -495,14 +516,14 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
           for (int c = 0; c < D / 8; ++c) orow2[c] = make_uint4(0, 0, 0, 0);
         continue;
       }
-      if (MODE != 3) {
+      if (kRowsInTmem) {
         // the item's row tiles -> TMEM; the A region is free because every S/dP
         // MMA of the previous item has completed (this thread consumed their SD_FULL)
         if (!(ok = wait_warp(bar(A_FULL), a_use & 1u, g))) break;
         ++a_use;
         fence_after();
-        row_to_tmem(0u, kColA1);
-        if (kHasDP) row_to_tmem(kOffA2, kColA2);
+        row_to_tmem(0u, C::kColA1);
+        if (kHasDP) row_to_tmem(C::kOffA2, C::kColA2);
         wait_st();
         fence_before();
         mbar_arrive(bar(A_EMPTY));   // the shared-memory tiles can take the next item's
@@ -518,7 +539,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
       const float own_d = MODE == 0 ? p.delta[row] : 0.f;
       for (int e = 0; e < len && ok; ++e) {
         const uint32_t st = c_use % kNS;
-        const float4* stats = reinterpret_cast<const float4*>(gbase + kOffStage + st * kStageBytes + 2 * kTile);
+        const float4* stats = reinterpret_cast<const float4*>(gbase + C::kOffStage + st * kStageBytes + 2 * kTile);
         for (int h = 0; h < 2; ++h) {
           const uint32_t b = hg & 1u;
           if (!(ok = wait_warp(bar(SD_FULL + b), (hg >> 1) & 1u, g))) break;
@@ -606,10 +627,11 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
               (unsigned long long)(globaltimer_ns() - t_start));
 }
 
-template <int MODE>
+template <int MODE, int D>
 sparsp_status_t go(const Dims& s, const CUtensorMap& a1, const CUtensorMap& a2, const CUtensorMap& b1,
                    const CUtensorMap& b2, const Params& prm, cudaStream_t st) {
-  auto kern = attn_bwd_tc_kernel<MODE>;
+  auto kern = attn_bwd_tc_kernel<MODE, D>;
+  constexpr uint32_t kSmemBytes = BCfg<D>::kSmemBytes;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
     return SPARSP_ERR_CUDA;
   const int sms = device_sm_count();
@@ -622,7 +644,22 @@ sparsp_status_t go(const Dims& s, const CUtensorMap& a1, const CUtensorMap& a2, 
 
 }  // namespace
 
-bool attn_bwd_tc_supported(const Dims& s) { return s.Bt == 128 && s.d == 128 && attn_fwd_tc_supported(s); }
+bool attn_bwd_tc_supported(const Dims& s) {
+  return s.Bt == 128 && (s.d == 128 || s.d == 64) && attn_fwd_tc_supported(s);
+}
+
+namespace {
+
+template <int D>
+sparsp_status_t launch_d(int mode, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, const Dims& s, const Params& prm, cudaStream_t st) {
+  if (mode == 0) return go<0, D>(s, tq, tdo, tk, tv, prm, st);
+  if (mode == 1) return go<1, D>(s, tk, tv, tq, tdo, prm, st);
+  if (mode == 3) return go<3, D>(s, tk, tv, tq, tdo, prm, st);
+  return go<2, D>(s, tk, tk, tq, tdo, prm, st);
+}
+
+}  // namespace
 
 sparsp_status_t launch_attn_bwd_tc(const Dims& s, int mode, const __nv_bfloat16* q,
                                    const __nv_bfloat16* k, const __nv_bfloat16* v,
@@ -633,15 +670,14 @@ sparsp_status_t launch_attn_bwd_tc(const Dims& s, int mode, const __nv_bfloat16*
                                    bool raster, cudaStream_t st) {
   const uint64_t rows = (uint64_t)s.B * s.H * s.N;
   CUtensorMap tq, tk, tv, tdo;
-  if (!make_tmap_bf16_rows(&tq, q, rows, D, BT) || !make_tmap_bf16_rows(&tk, k, rows, D, BT) ||
-      !make_tmap_bf16_rows(&tv, v, rows, D, BT) || !make_tmap_bf16_rows(&tdo, dout, rows, D, BT))
+  const uint64_t d = (uint64_t)s.d;
+  if (!make_tmap_bf16_rows(&tq, q, rows, d, BT) || !make_tmap_bf16_rows(&tk, k, rows, d, BT) ||
+      !make_tmap_bf16_rows(&tv, v, rows, d, BT) || !make_tmap_bf16_rows(&tdo, dout, rows, d, BT))
     return SPARSP_ERR_CUDA;
   Params prm{ptr, idx, s.N, s.nb, s.rows(), (int64_t)rows, scale * 1.4426950408889634f, mode == 2 ? 1.0f : scale,
              lse2, delta, out, out2, 1.0f, items, counter, prof, d_status, raster ? 1 : 0, raster_map(s)};
-  if (mode == 0) return go<0>(s, tq, tdo, tk, tv, prm, st);
-  if (mode == 1) return go<1>(s, tk, tv, tq, tdo, prm, st);
-  if (mode == 3) return go<3>(s, tk, tv, tq, tdo, prm, st);
-  return go<2>(s, tk, tk, tq, tdo, prm, st);
+  if (s.d == 64) return launch_d<64>(mode, tq, tk, tv, tdo, s, prm, st);
+  return launch_d<128>(mode, tq, tk, tv, tdo, s, prm, st);
 }
 
 }  // namespace sparsp

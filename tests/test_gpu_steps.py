@@ -816,7 +816,7 @@ def test_attn_bwd_raster_output(name, split):
     st = status_word()
     extra = sp.BWD_SPLIT_KV if split else 0
     o, lse = sp.attn_fwd(shape, q, k, v, rp, ci, status=st)
-    if shape.Bt != 128 or shape.d != 128:
+    if shape.Bt != 128:
         o_r = sp.reorder(shape, o, inverse=True)
         with pytest.raises(sp.SparspError):
             sp.attn_bwd(shape, q, k, v, o_r, lse, do, rp, ci, flags=sp.OUT_RASTER | extra)
