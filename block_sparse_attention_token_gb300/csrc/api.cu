@@ -535,13 +535,30 @@ sparsp_status_t sparsp_attn_bwd(const sparsp_shape_t* shape, const void* q, cons
   if (r != SPARSP_OK) return r;
   r = launch_csr_transpose(s, row_ptr, col_idx, w.col_ptr, w.row_idx, d_status, st);
   if (r != SPARSP_OK) return r;
-  r = launch_lpt(s, row_ptr, flat, w.items, w.counter, w.hist, st);
+  // the tcgen05 kernels' items with 64-token blocks are pairs of blocks, each
+  // costing the sum of its two lists (CSR rows for dQ, CSC columns for dK/dV)
+  const bool pairs = tc && attn_bwd_tc_items_per_head(s) != s.nb;
+  Dims sp = s;
+  sp.nb = pairs ? attn_bwd_tc_items_per_head(s) : s.nb;
+  if (pairs) {
+    r = launch_pair_ptr(s, row_ptr, w.pair_ptr, st);
+    if (r != SPARSP_OK) return r;
+    r = launch_lpt(sp, w.pair_ptr, flat, w.items, w.counter, w.hist, st, 2 * s.nb);
+  } else {
+    r = launch_lpt(s, row_ptr, flat, w.items, w.counter, w.hist, st);
+  }
   if (r != SPARSP_OK) return r;
   if (tc) {
     r = launch_attn_bwd_tc(s, 0, (cb)q, (cb)k, (cb)v, (cb)dout, w.lse2, w.delta, row_ptr, col_idx, scale,
                            (__nv_bfloat16*)dq, nullptr, w.items, w.counter, prof, d_status, raster, st);
     if (r != SPARSP_OK) return r;
-    r = launch_lpt(s, w.col_ptr, flat, w.items2, w.counter + 1, w.hist, st);
+    if (pairs) {   // pair_ptr is free again: the dQ kernel reads only its item list
+      r = launch_pair_ptr(s, w.col_ptr, w.pair_ptr, st);
+      if (r != SPARSP_OK) return r;
+      r = launch_lpt(sp, w.pair_ptr, flat, w.items2, w.counter + 1, w.hist, st, 2 * s.nb);
+    } else {
+      r = launch_lpt(s, w.col_ptr, flat, w.items2, w.counter + 1, w.hist, st);
+    }
     if (r != SPARSP_OK) return r;
     if (!(flags & SPARSP_BWD_SPLIT_KV))
       return launch_attn_bwd_tc(s, 3, (cb)q, (cb)k, (cb)v, (cb)dout, w.lse2, w.delta, w.col_ptr, w.row_idx,

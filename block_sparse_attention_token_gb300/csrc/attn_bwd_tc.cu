@@ -57,6 +57,7 @@
 // Every mbarrier wait is bounded (2 s): on expiry the CTA reports
 // SPARSP_ERR_TIMEOUT, all roles leave, in-flight copies and MMAs are drained
 // with a second bounded wait and TMEM is released.
+#include "pairs.cuh"
 #include "tc_helpers.cuh"
 
 namespace sparsp {
@@ -64,9 +65,9 @@ namespace {
 
 using namespace tc;
 
-constexpr int BT = 128;
+constexpr int TR = 128;   // rows of a row or column tile (the MMA's M; one block, or a pair of 64-token blocks)
 constexpr int kMaxNS = 4, kNI = 4;
-constexpr uint32_t kBox = BT * 64 * 2;        // one 64-column swizzled box of a 128-row tile
+constexpr uint32_t kBox = TR * 64 * 2;        // one 64-column swizzled box of a 128-row tile
 constexpr uint32_t kStats = 1024;             // LSE*log2e [128] + D [128] of a column block
 constexpr int kThreads = 224;
 constexpr int HB = 64;   // columns of a half block
@@ -81,19 +82,31 @@ enum Bar {
 // TMEM holds the two half buffers [0,256), the accumulator(s) from 256
 // (mode 3: dK [256, 256+D), dV [256+D, 256+2D)) and, where the row tiles live
 // in TMEM, A1 [384, 384+D/2) and A2 [384+D/2, 384+D) as packed bf16.
-template <int D_>
+//
+// With 64-token blocks (PAIR) an item is a pair of neighbouring blocks (2p,
+// 2p + 1: 128 contiguous rows) processed over the union of their two lists,
+// two blocks per column stage (the two halves); each item slot holds the two
+// lists as bitmaps and one byte per union block saying which of the two rows
+// selected it, so that the row warps mask a half for a row block that did not.
+template <int D_, int BTB_>
 struct BCfg {
-  static constexpr int D = D_;
+  static constexpr int D = D_, BTB = BTB_;
+  static constexpr bool PAIR = BTB == 64;
   static constexpr int NBOX = D / 64;
-  static constexpr uint32_t kTile = BT * D * 2;
+  static constexpr uint32_t kTile = TR * D * 2;
   static constexpr int kNS = D == 64 ? 4 : 2;   // column-tile stages
   static constexpr uint32_t kColAcc = 256, kColAcc2 = 256 + D;
   static constexpr uint32_t kColA1 = 384, kColA2 = 384 + D / 2;
   static constexpr uint32_t kOffA2 = kTile, kOffStage = 2 * kTile;
   static constexpr uint32_t kStageBytes = 2 * kTile + kStats;   // a multiple of 1024: tiles stay aligned
   static constexpr uint32_t kOffBar = kOffStage + kNS * kStageBytes;
-  static constexpr uint32_t kOffRing = kOffBar + 8 * NBAR;
-  static constexpr uint32_t kOffMisc = kOffRing + 8 * kNI;
+  static constexpr uint32_t kOffRing = kOffBar + 8 * NBAR;   // [kNI] int4: item, stages, bad-list bits
+  // pairs: bitmap words of one list (up to 1,024 blocks with d = 128, kMaxBlocks with d = 64)
+  static constexpr int MAXW = PAIR ? (D == 64 ? kMaxBlocks / 32 : 32) : 0;
+  static constexpr uint32_t kOffBits = kOffRing + 16 * kNI;   // [kNI][2][MAXW]
+  static constexpr uint32_t kMaskBytes = 32 * MAXW;           // per slot: one byte per union block (+1)
+  static constexpr uint32_t kOffMask = kOffBits + kNI * 2 * MAXW * 4;
+  static constexpr uint32_t kOffMisc = kOffMask + kNI * (kMaskBytes + (PAIR ? 16 : 0));
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
   static_assert(kNS <= kMaxNS && kSmemBytes <= 232448u, "shared memory");
 };
@@ -123,6 +136,7 @@ struct Params {
   const int32_t* idx;    // CSR col_idx or CSC row_idx
   int64_t N;
   int nb;
+  int nbp;               // items per head: nb, or ceil(nb / 2) pairs of 64-token blocks
   int64_t n_items;
   int64_t rows_total;    // B*H*N rows of every tensor
   float sl2;             // scale * log2(e)
@@ -140,12 +154,13 @@ struct Params {
   RasterMap rm;
 };
 
-template <int MODE, int D>
+template <int MODE, int D, int BTB>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constant__ CUtensorMap ta2,
                    const __grid_constant__ CUtensorMap tb1, const __grid_constant__ CUtensorMap tb2,
                    const Params p) {
-  using C = BCfg<D>;
+  using C = BCfg<D, BTB>;
+  constexpr bool PAIR = C::PAIR;
   constexpr bool kHasDP = MODE != 2;
   // the item's row tiles as the A operand in TMEM; mode 3 with d = 128 has no
   // TMEM left beside its two accumulators and reads them from shared memory
@@ -159,7 +174,9 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
   const uint32_t sA1 = base, sA2 = base + C::kOffA2;
   auto stage = [&](uint32_t st) -> uint32_t { return base + C::kOffStage + st * kStageBytes; };
   auto bar = [&](int idx) -> uint32_t { return base + C::kOffBar + 8u * (uint32_t)idx; };
-  volatile int2* ring = reinterpret_cast<volatile int2*>(gbase + C::kOffRing);
+  volatile int4* ring = reinterpret_cast<volatile int4*>(gbase + C::kOffRing);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(gbase + C::kOffBits);   // pairs: [kNI][2][MAXW]
+  uint8_t* masks = gbase + C::kOffMask;                                 // pairs: [kNI][kMaskBytes + 16]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + C::kOffMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -204,7 +221,8 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
   fence_after();
   const uint32_t tmem = *tmem_slot;
   const Guard g{abort_flag, p.d_status, kWaitNs};
-  const int nb = p.nb;
+  const int nb = p.nb, nbp = p.nbp;
+  const int words = (nb + 31) >> 5;
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
@@ -213,39 +231,59 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
       int32_t slot = 0;
       if (lane == 0) slot = atomicAdd(p.counter, 1);
       slot = __shfl_sync(0xffffffffu, slot, 0);
-      int32_t item = -1, len = -2;
+      const int ri = (int)(it_fill % kNI);
+      // the slot's bitmaps and masks stay in use until the row warps release it
+      if (!wait_warp(bar(I_EMPTY + ri), ((it_fill / kNI) & 1u) ^ 1u, g)) break;
+      uint32_t* bmA = bits + ri * 2 * C::MAXW;
+      uint32_t* bmB = bmA + C::MAXW;
+      int32_t item = -1, len = -2, badbits = 0;
       if (slot < p.n_items) {
         item = p.items[slot];
-        const int32_t a = p.ptr[item], b = p.ptr[item + 1];
-        bool bad = (b < a) || (b - a > nb);
-        if (!bad)
-          for (int32_t e = a + lane; e < b; e += 32) {
-            const int32_t j = p.idx[e];
-            if (j < 0 || j >= nb) bad = true;
-          }
-        bad = __any_sync(0xffffffffu, bad);
-        if (bad) {
-          if (lane == 0) report(p.d_status, SPARSP_ERR_DATA);
-          len = -1;
+        if constexpr (PAIR) {
+          // the pair's two lists as bitmaps; a bad list counts as empty
+          const int64_t bh = item / nbp;
+          const int iA = 2 * (item % nbp);
+          for (int w = lane; w < 2 * C::MAXW; w += 32) bmA[w] = 0u;
+          __syncwarp();
+          const bool okA = list_bitmap(p.ptr, p.idx, nb, bh * nb + iA, bmA, words, lane);
+          const bool okB = iA + 1 < nb ? list_bitmap(p.ptr, p.idx, nb, bh * nb + iA + 1, bmB, words, lane) : true;
+          badbits = (okA ? 0 : 1) | (okB ? 0 : 2);
+          if (badbits && lane == 0) report(p.d_status, SPARSP_ERR_DATA);
+          const int u = union_count(bmA, bmB, words, lane);
+          len = (badbits == 3) ? -1 : (u + 1) / 2;   // stages of two blocks
+          union_masks(bmA, bmB, words, u, lane, masks + ri * (C::kMaskBytes + 16));
         } else {
-          len = b - a;
+          const int32_t a = p.ptr[item], b = p.ptr[item + 1];
+          bool bad = (b < a) || (b - a > nb);
+          if (!bad)
+            for (int32_t e = a + lane; e < b; e += 32) {
+              const int32_t j = p.idx[e];
+              if (j < 0 || j >= nb) bad = true;
+            }
+          bad = __any_sync(0xffffffffu, bad);
+          if (bad) {
+            if (lane == 0) report(p.d_status, SPARSP_ERR_DATA);
+            len = -1;
+          } else {
+            len = b - a;
+          }
         }
       }
-      const int ri = (int)(it_fill % kNI);
-      if (!wait_warp(bar(I_EMPTY + ri), ((it_fill / kNI) & 1u) ^ 1u, g)) break;
+      __syncwarp();
       if (lane == 0) {
         ring[ri].x = item;
         ring[ri].y = len;
+        ring[ri].z = badbits;
         mbar_arrive(bar(I_FULL + ri));
       }
       __syncwarp();
       ++it_fill;
       if (len == -2) break;
       if (len <= 0) continue;
-      const int64_t bh = item / nb;
-      const int i = item % nb;
-      int32_t ya = (int32_t)(bh * p.N + (int64_t)i * BT);
-      if (!dcheck(ya >= 0 && ya + BT <= p.rows_total, p.d_status)) ya = 0;
+      const int64_t bh = item / nbp;
+      const int i0 = PAIR ? 2 * (item % nbp) : item % nb;   // the item's (first) row block
+      int32_t ya = (int32_t)(bh * p.N + (int64_t)i0 * BTB);
+      if (!dcheck(ya >= 0 && ya < p.rows_total, p.d_status)) ya = 0;
       if (!wait_warp(bar(A_EMPTY), (a_fill & 1u) ^ 1u, g)) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(bar(A_FULL), kHasDP ? 2 * kTile : kTile);
@@ -256,13 +294,24 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
         }
       }
       ++a_fill;
-      const int32_t e0 = p.ptr[item];
+      const int32_t e0 = PAIR ? 0 : p.ptr[item];
+      UnionWalk walk(bmA, bmB, PAIR ? words : 0);
       bool ok = true;
       for (int e = 0; e < len; ++e) {
-        const int32_t c = p.idx[e0 + e];
-        int64_t yc64 = bh * p.N + (int64_t)c * BT;
-        if (!dcheck(yc64 >= 0 && yc64 + BT <= p.rows_total, p.d_status)) yc64 = 0;   // flagged; counts kept
-        const int32_t yc = (int32_t)yc64;
+        // the stage's column block(s): one block, or the next two of the pair's union
+        int32_t c1, c2 = 0;
+        if constexpr (PAIR) {
+          c1 = walk.next();
+          c2 = walk.next();
+          if (c2 < 0) c2 = c1;   // a lone last block: loaded twice, its second half masked
+        } else {
+          c1 = p.idx[e0 + e];
+        }
+        int64_t yc64 = bh * p.N + (int64_t)c1 * BTB, yc64b = bh * p.N + (int64_t)c2 * BTB;
+        if (!dcheck(yc64 >= 0 && yc64 + BTB <= p.rows_total && yc64b >= 0 && yc64b + BTB <= p.rows_total,
+                    p.d_status))
+          yc64 = yc64b = 0;   // flagged; counts kept
+        const int32_t yc = (int32_t)yc64, ycb = (int32_t)yc64b;
         const uint32_t st = c_fill % kNS;
         if (!(ok = wait_warp(bar(C_EMPTY + st), ((c_fill / kNS) & 1u) ^ 1u, g))) break;
         if (lane == 0) {
@@ -272,10 +321,21 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
           for (int h = 0; h < C::NBOX; ++h) {
             tma_load_2d(sb + h * kBox, &tb1, bar(C_FULL + st), 64 * h, yc);
             tma_load_2d(sb + kTile + h * kBox, &tb2, bar(C_FULL + st), 64 * h, yc);
+            if (PAIR) {   // the second block's 64 rows, 8 KB into each box
+              tma_load_2d(sb + h * kBox + kBox / 2, &tb1, bar(C_FULL + st), 64 * h, ycb);
+              tma_load_2d(sb + kTile + h * kBox + kBox / 2, &tb2, bar(C_FULL + st), 64 * h, ycb);
+            }
           }
           if (MODE != 0) {
-            bulk_load(sb + 2 * kTile, p.lse2 + yc64, 512, bar(C_FULL + st));
-            bulk_load(sb + 2 * kTile + 512, p.delta + yc64, 512, bar(C_FULL + st));
+            if (PAIR) {   // LSE*log2e and D of the two blocks' rows, side by side
+              bulk_load(sb + 2 * kTile, p.lse2 + yc64, 256, bar(C_FULL + st));
+              bulk_load(sb + 2 * kTile + 256, p.lse2 + yc64b, 256, bar(C_FULL + st));
+              bulk_load(sb + 2 * kTile + 512, p.delta + yc64, 256, bar(C_FULL + st));
+              bulk_load(sb + 2 * kTile + 768, p.delta + yc64b, 256, bar(C_FULL + st));
+            } else {
+              bulk_load(sb + 2 * kTile, p.lse2 + yc64, 512, bar(C_FULL + st));
+              bulk_load(sb + 2 * kTile + 512, p.delta + yc64, 512, bar(C_FULL + st));
+            }
           }
         }
         ++c_fill;
@@ -295,7 +355,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
     for (;;) {
       const int ri = (int)(it_use % kNI);
       if (!wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
-      const int2 ent = make_int2(ring[ri].x, ring[ri].y);
+      const int4 ent = make_int4(ring[ri].x, ring[ri].y, ring[ri].z, 0);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
       ++it_use;
@@ -379,7 +439,7 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
     for (;;) {
       const int ri = (int)(it_use % kNI);
       if (!wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g)) break;
-      const int2 ent = make_int2(ring[ri].x, ring[ri].y);
+      const int4 ent = make_int4(ring[ri].x, ring[ri].y, ring[ri].z, 0);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
       ++it_use;
@@ -443,9 +503,10 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
     uint32_t it_use = 0, c_use = 0, hg = 0, acc_items = 0, a_use = 0;
     uint4* pending = nullptr;    // output row of the previous item, written once its accumulator is full
     uint4* pending2 = nullptr;   // mode 3: its dV row
+    bool has_pending = false, pend_store = false;   // pairs: a row of a missing or bad block is not stored
     bool ok = true;
-    // one accumulator (128 columns at col) -> bf16 output row
-    auto acc_out = [&](uint32_t col, float scale, uint4* orow) {
+    // one accumulator (d columns at col) -> bf16 output row (the TMEM loads run in every lane)
+    auto acc_out = [&](uint32_t col, float scale, uint4* orow, bool store) {
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -455,17 +516,18 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
 #pragma unroll
         for (int x = 0; x < 16; ++x)
           w[x] = pack2(__uint_as_float(o[2 * x]) * scale, __uint_as_float(o[2 * x + 1]) * scale);
+        if (store)
 #pragma unroll
-        for (int x = 0; x < 4; ++x) orow[c * 4 + x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+          for (int x = 0; x < 4; ++x) orow[c * 4 + x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
       }
     };
     // accumulator(s) -> output row(s); frees the accumulators for the next item
-    auto epilogue = [&](uint4* orow, uint4* orow2) -> bool {
+    auto epilogue = [&](uint4* orow, uint4* orow2, bool store) -> bool {
       if (!wait_warp(bar(ACC_FULL), acc_items & 1u, g)) return false;
       ++acc_items;
       fence_after();
-      acc_out(C::kColAcc, p.out_scale, orow);
-      if (MODE == 3) acc_out(C::kColAcc2, p.out_scale2, orow2);
+      acc_out(C::kColAcc, p.out_scale, orow, store);
+      if (MODE == 3) acc_out(C::kColAcc2, p.out_scale2, orow2, store);
       fence_before();
       mbar_arrive(bar(ACC_EMPTY));
       return true;
@@ -492,28 +554,45 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
     for (;;) {
       const int ri = (int)(it_use % kNI);
       if (!(ok = wait_warp(bar(I_FULL + ri), (it_use / kNI) & 1u, g))) break;
-      const int2 ent = make_int2(ring[ri].x, ring[ri].y);
+      const int4 ent = make_int4(ring[ri].x, ring[ri].y, ring[ri].z, 0);
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
+      // pairs read the slot's masks until the item ends; release it then
+      auto release = [&]() {
+        if (lane == 0) mbar_arrive(bar(I_EMPTY + ri));
+      };
+      if (!PAIR) release();
       ++it_use;
-      if (ent.y == -2) break;
-      if (ent.y == -1) continue;
+      if (ent.y == -2) {
+        if (PAIR) release();
+        break;
+      }
+      if (ent.y == -1) {
+        if (PAIR) release();
+        continue;
+      }
       const int64_t item = ent.x;
-      const int64_t bh = item / nb;
-      const int i = (int)(item % nb);
-      int64_t row = bh * p.N + (int64_t)i * BT + threadIdx.x;
-      if (!dcheck(row >= 0 && row < p.rows_total, p.d_status)) row = 0;
-      int64_t orow_idx = p.raster ? p.rm.row(bh, i, threadIdx.x) : row;
+      // with pairs, rows 0-63 are block 2p and rows 64-127 block 2p + 1
+      const int half = PAIR ? (int)(threadIdx.x >> 6) : 0;
+      const int64_t bh = item / nbp;
+      const int i = PAIR ? 2 * (int)(item % nbp) + half : (int)(item % nb);   // this thread's row block
+      const int o = PAIR ? (int)(threadIdx.x & 63) : (int)threadIdx.x;       // its token in the block
+      const bool exists = !PAIR || (i < nb && !((ent.z >> half) & 1));      // warp-uniform
+      int64_t row = bh * p.N + (int64_t)i * BTB + o;
+      if (!exists || !dcheck(row >= 0 && row < p.rows_total, p.d_status)) row = 0;
+      int64_t orow_idx = p.raster && exists ? p.rm.row(bh, i, o) : row;
       if (!dcheck(orow_idx >= 0 && orow_idx < p.rows_total, p.d_status)) orow_idx = 0;
       uint4* orow = reinterpret_cast<uint4*>(p.out + orow_idx * D);
       uint4* orow2 = MODE == 3 ? reinterpret_cast<uint4*>(p.out2 + orow_idx * D) : nullptr;
       const int len = ent.y;
       if (len == 0) {
+        if (exists) {
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
-        if (MODE == 3)
+          for (int c = 0; c < D / 8; ++c) orow[c] = make_uint4(0, 0, 0, 0);
+          if (MODE == 3)
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) orow2[c] = make_uint4(0, 0, 0, 0);
+            for (int c = 0; c < D / 8; ++c) orow2[c] = make_uint4(0, 0, 0, 0);
+        }
+        if (PAIR) release();
         continue;
       }
       if (kRowsInTmem) {
@@ -530,16 +609,18 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
         mbar_arrive(bar(AT_FULL));   // the S issuer may start this item
       }
       // the previous item's output, while this item's first S and dP run
-      if (pending != nullptr) {
-        if (!(ok = epilogue(pending, pending2))) break;
-        pending = pending2 = nullptr;
+      if (has_pending) {
+        if (!(ok = epilogue(pending, pending2, pend_store))) break;
+        has_pending = false;
       }
       // mode 0: this thread's query row has one LSE and one D
-      const float own_l2 = MODE == 0 ? p.lse2[row] : 0.f;
-      const float own_d = MODE == 0 ? p.delta[row] : 0.f;
+      const float own_l2 = MODE == 0 && exists ? p.lse2[row] : 0.f;
+      const float own_d = MODE == 0 && exists ? p.delta[row] : 0.f;
+      const uint16_t* mk = reinterpret_cast<const uint16_t*>(masks + ri * (C::kMaskBytes + 16));
       for (int e = 0; e < len && ok; ++e) {
         const uint32_t st = c_use % kNS;
         const float4* stats = reinterpret_cast<const float4*>(gbase + C::kOffStage + st * kStageBytes + 2 * kTile);
+        const uint32_t msk = PAIR ? (uint32_t)mk[e] : 0xffffu;   // byte h: which rows selected block h
         for (int h = 0; h < 2; ++h) {
           const uint32_t b = hg & 1u;
           if (!(ok = wait_warp(bar(SD_FULL + b), (hg >> 1) & 1u, g))) break;
@@ -552,10 +633,16 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
             tmem_ld32(t_row + 128u * b + HB + 32u, dv + 32);
           }
           wait_ld();
+          // pairs: a row block that did not select this half's block (or does not
+          // exist) gets X = 0 there (warp-uniform)
+          const bool has = !PAIR || (exists && ((msk >> (8 * h + half)) & 1u));
           uint32_t xk[HB / 2];
           if constexpr (MODE == 3) {
             // P^T over S^T; dS^T = P^T (dP^T - D) over dP^T (both already in registers)
             uint32_t xd[HB / 2];
+#pragma unroll
+            for (int x = 0; x < HB / 2; ++x) xk[x] = xd[x] = 0u;
+            if (has)
 #pragma unroll
             for (int x4 = 0; x4 < HB / 4; ++x4) {
               const float4 L = stats[16 * h + x4];
@@ -579,6 +666,9 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
             fence_before();
             mbar_arrive(bar(X_FULL + b));
           } else {
+#pragma unroll
+            for (int x = 0; x < HB / 2; ++x) xk[x] = 0u;
+            if (has)
 #pragma unroll
             for (int x4 = 0; x4 < HB / 4; ++x4) {
               float l2[4], dd[4];
@@ -612,10 +702,13 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
         ++c_use;
       }
       if (!ok) break;
+      if (PAIR) release();
       pending = orow;
       pending2 = orow2;
+      has_pending = true;
+      pend_store = exists;
     }
-    if (ok && pending != nullptr) epilogue(pending, pending2);
+    if (ok && has_pending) epilogue(pending, pending2, pend_store);
   }
 
   fence_before();
@@ -627,16 +720,16 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
               (unsigned long long)(globaltimer_ns() - t_start));
 }
 
-template <int MODE, int D>
+template <int MODE, int D, int BTB>
 sparsp_status_t go(const Dims& s, const CUtensorMap& a1, const CUtensorMap& a2, const CUtensorMap& b1,
                    const CUtensorMap& b2, const Params& prm, cudaStream_t st) {
-  auto kern = attn_bwd_tc_kernel<MODE, D>;
-  constexpr uint32_t kSmemBytes = BCfg<D>::kSmemBytes;
+  auto kern = attn_bwd_tc_kernel<MODE, D, BTB>;
+  constexpr uint32_t kSmemBytes = BCfg<D, BTB>::kSmemBytes;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
     return SPARSP_ERR_CUDA;
   const int sms = device_sm_count();
   if (sms <= 0) return SPARSP_ERR_CUDA;
-  const int64_t grid = cap_grid(s, sms, s.rows());
+  const int64_t grid = cap_grid(s, sms, prm.n_items);
   kern<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(a1, a2, b1, b2, prm);
   SPARSP_LAUNCH_CHECK();
   return SPARSP_OK;
@@ -645,18 +738,29 @@ sparsp_status_t go(const Dims& s, const CUtensorMap& a1, const CUtensorMap& a2, 
 }  // namespace
 
 bool attn_bwd_tc_supported(const Dims& s) {
-  return s.Bt == 128 && (s.d == 128 || s.d == 64) && attn_fwd_tc_supported(s);
+  if (s.d != 128 && s.d != 64) return false;
+  // 64-token blocks run as pairs; an item slot holds the pair's two lists as bitmaps
+  if (s.Bt == 64 && s.nb > 32 * (s.d == 64 ? BCfg<64, 64>::MAXW : BCfg<128, 64>::MAXW)) return false;
+  return (s.Bt == 128 || s.Bt == 64) && attn_fwd_tc_supported(s);
 }
+
+int attn_bwd_tc_items_per_head(const Dims& s) { return s.Bt == 64 ? (s.nb + 1) / 2 : s.nb; }
 
 namespace {
 
-template <int D>
-sparsp_status_t launch_d(int mode, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& tdo, const Dims& s, const Params& prm, cudaStream_t st) {
-  if (mode == 0) return go<0, D>(s, tq, tdo, tk, tv, prm, st);
-  if (mode == 1) return go<1, D>(s, tk, tv, tq, tdo, prm, st);
-  if (mode == 3) return go<3, D>(s, tk, tv, tq, tdo, prm, st);
-  return go<2, D>(s, tk, tk, tq, tdo, prm, st);
+// Tensor maps: the item's row tiles (A) are 128-row boxes, the column tiles
+// (B) boxes of one block (two per stage with 64-token blocks).
+struct Maps {
+  CUtensorMap q, k, v, dout;   // 128-row boxes
+  CUtensorMap qb, kb, vb, dob;  // one block per box
+};
+
+template <int D, int BTB>
+sparsp_status_t launch_d(int mode, const Maps& m, const Dims& s, const Params& prm, cudaStream_t st) {
+  if (mode == 0) return go<0, D, BTB>(s, m.q, m.dout, m.kb, m.vb, prm, st);
+  if (mode == 1) return go<1, D, BTB>(s, m.k, m.v, m.qb, m.dob, prm, st);
+  if (mode == 3) return go<3, D, BTB>(s, m.k, m.v, m.qb, m.dob, prm, st);
+  return go<2, D, BTB>(s, m.k, m.k, m.qb, m.dob, prm, st);
 }
 
 }  // namespace
@@ -669,15 +773,26 @@ sparsp_status_t launch_attn_bwd_tc(const Dims& s, int mode, const __nv_bfloat16*
                                    const int32_t* items, int32_t* counter, uint64_t* prof, int32_t* d_status,
                                    bool raster, cudaStream_t st) {
   const uint64_t rows = (uint64_t)s.B * s.H * s.N;
-  CUtensorMap tq, tk, tv, tdo;
   const uint64_t d = (uint64_t)s.d;
-  if (!make_tmap_bf16_rows(&tq, q, rows, d, BT) || !make_tmap_bf16_rows(&tk, k, rows, d, BT) ||
-      !make_tmap_bf16_rows(&tv, v, rows, d, BT) || !make_tmap_bf16_rows(&tdo, dout, rows, d, BT))
+  const uint32_t bt = (uint32_t)s.Bt;
+  Maps m;
+  if (!make_tmap_bf16_rows(&m.q, q, rows, d, TR) || !make_tmap_bf16_rows(&m.k, k, rows, d, TR) ||
+      !make_tmap_bf16_rows(&m.v, v, rows, d, TR) || !make_tmap_bf16_rows(&m.dout, dout, rows, d, TR) ||
+      !make_tmap_bf16_rows(&m.qb, q, rows, d, bt) || !make_tmap_bf16_rows(&m.kb, k, rows, d, bt) ||
+      !make_tmap_bf16_rows(&m.vb, v, rows, d, bt) || !make_tmap_bf16_rows(&m.dob, dout, rows, d, bt))
     return SPARSP_ERR_CUDA;
-  Params prm{ptr, idx, s.N, s.nb, s.rows(), (int64_t)rows, scale * 1.4426950408889634f, mode == 2 ? 1.0f : scale,
-             lse2, delta, out, out2, 1.0f, items, counter, prof, d_status, raster ? 1 : 0, raster_map(s)};
-  if (s.d == 64) return launch_d<64>(mode, tq, tk, tv, tdo, s, prm, st);
-  return launch_d<128>(mode, tq, tk, tv, tdo, s, prm, st);
+  // 64-token blocks: items are pairs of blocks, ordered by the caller over the
+  // pairs' lists (attn_bwd_tc_items_per_head per head)
+  const int nbp = attn_bwd_tc_items_per_head(s);
+  Params prm{ptr, idx, s.N, s.nb, nbp, (int64_t)s.B * s.H * nbp, (int64_t)rows, scale * 1.4426950408889634f,
+             mode == 2 ? 1.0f : scale, lse2, delta, out, out2, 1.0f, items, counter, prof, d_status,
+             raster ? 1 : 0, raster_map(s)};
+  if (s.Bt == 64) {
+    if (s.d == 64) return launch_d<64, 64>(mode, m, s, prm, st);
+    return launch_d<128, 64>(mode, m, s, prm, st);
+  }
+  if (s.d == 64) return launch_d<64, 128>(mode, m, s, prm, st);
+  return launch_d<128, 128>(mode, m, s, prm, st);
 }
 
 }  // namespace sparsp

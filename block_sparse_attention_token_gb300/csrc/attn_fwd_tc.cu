@@ -51,6 +51,7 @@
 // P [192,256). Every mbarrier wait is bounded (2 s); on expiry the CTA sets
 // SPARSP_ERR_TIMEOUT, all roles leave their loops, copies and MMAs in flight
 // are drained with a second bounded wait, and TMEM is released.
+#include "pairs.cuh"
 #include "tc_helpers.cuh"
 
 namespace sparsp {
@@ -186,57 +187,6 @@ struct Params {
   int32_t* d_status;
 };
 
-// Walk over the set bits of (a | b) in ascending order, two at a time: the
-// key blocks of the stages of a pair item. The same walk runs in the producer
-// and in every softmax warp (uniformly), so they agree on each stage's blocks.
-struct UnionWalk {
-  const uint32_t* a;
-  const uint32_t* b;
-  int words, w;
-  uint32_t cur;
-  __device__ __forceinline__ UnionWalk(const uint32_t* a_, const uint32_t* b_, int words_)
-      : a(a_), b(b_), words(words_), w(0), cur(words_ > 0 ? (a_[0] | b_[0]) : 0u) {}
-  __device__ __forceinline__ int next() {
-    while (cur == 0u) {
-      if (++w >= words) return -1;
-      cur = a[w] | b[w];
-    }
-    const int j = w * 32 + __ffs(cur) - 1;
-    cur &= cur - 1u;
-    return j;
-  }
-};
-
-__device__ __forceinline__ bool bit_of(const uint32_t* m, int j) { return (m[j >> 5] >> (j & 31)) & 1u; }
-
-// Validates CSR row r (length <= nb, indices in [0, nb), no index twice) and
-// writes its bitmap (words zeroed before). Warp-collective; returns false for
-// a bad row, whose bitmap is then cleared.
-__device__ __forceinline__ bool row_bitmap(const Params& p, int64_t r, uint32_t* bm, int words, int lane) {
-  const int32_t a = p.row_ptr[r], b = p.row_ptr[r + 1];
-  bool bad = (b < a) || (b - a > p.nb);
-  if (!bad)
-    for (int32_t e = a + lane; e < b; e += 32) {
-      const int32_t j = p.col_idx[e];
-      if (j < 0 || j >= p.nb) bad = true;
-      else atomicOr(&bm[j >> 5], 1u << (j & 31));
-    }
-  bad = __any_sync(0xffffffffu, bad);
-  __syncwarp();
-  if (!bad) {
-    int cnt = 0;
-    for (int w = lane; w < words; w += 32) cnt += __popc(bm[w]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
-    bad = cnt != b - a;   // an index listed twice
-  }
-  if (bad) {
-    for (int w = lane; w < words; w += 32) bm[w] = 0u;
-    __syncwarp();
-  }
-  return !bad;
-}
-
 template <int BT, int D>
 __global__ void __launch_bounds__(Cfg<BT, D>::THREADS, Cfg<BT, D>::kMinCtas)
 attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -326,39 +276,15 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           const int iA = 2 * (item % nbp);
           for (int w = lane; w < 2 * C::MAXW; w += 32) bmA[w] = 0u;
           __syncwarp();
-          const bool okA = row_bitmap(p, bh * nb + iA, bmA, words, lane);
-          const bool okB = iA + 1 < nb ? row_bitmap(p, bh * nb + iA + 1, bmB, words, lane) : true;
+          const bool okA = list_bitmap(p.row_ptr, p.col_idx, nb, bh * nb + iA, bmA, words, lane);
+          const bool okB = iA + 1 < nb ? list_bitmap(p.row_ptr, p.col_idx, nb, bh * nb + iA + 1, bmB, words, lane)
+                                       : true;
           badbits = (okA ? 0 : 1) | (okB ? 0 : 2);
           if (badbits && lane == 0) report(p.d_status, SPARSP_ERR_DATA);
-          int u = 0;
-          for (int w = lane; w < words; w += 32) u += __popc(bmA[w] | bmB[w]);
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) u += __shfl_xor_sync(0xffffffffu, u, off);
+          const int u = union_count(bmA, bmB, words, lane);
           len = (badbits == 3) ? -1 : (u + 1) / 2;   // stages of two key blocks
           if constexpr (C::DUO) {
-            // the stage masks: the union's set bits ranked by a warp prefix sum
-            uint8_t* mk = masks + ri * C::kMaskBytes;
-            int base_rank = 0;
-            for (int w0 = 0; w0 < words; w0 += 32) {
-              const int w = w0 + lane;
-              const uint32_t a = w < words ? bmA[w] : 0u, bb = w < words ? bmB[w] : 0u;
-              uint32_t un = a | bb;
-              const int c = __popc(un);
-              int incl = c;
-#pragma unroll
-              for (int off = 1; off < 32; off <<= 1) {
-                const int t = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += t;
-              }
-              int rk = base_rank + incl - c;
-              while (un != 0u) {
-                const int bit = __ffs(un) - 1;
-                un &= un - 1u;
-                mk[rk++] = (uint8_t)(((a >> bit) & 1u) | (((bb >> bit) & 1u) << 1));
-              }
-              base_rank += __shfl_sync(0xffffffffu, incl, 31);
-            }
-            if ((u & 1) && lane == 0) mk[u] = 0;   // a lone last block has no partner
+            union_masks(bmA, bmB, words, u, lane, masks + ri * C::kMaskBytes);
           }
         } else {
           const int32_t a = p.row_ptr[item], b = p.row_ptr[item + 1];

@@ -195,6 +195,9 @@ sparsp_status_t launch_bwd_rowdot(const Dims& s, const __nv_bfloat16* o, const _
 // tcgen05 backward (bf16, Bt = d = 128). mode 0: dQ over the CSR rows;
 // mode 1: dK, mode 2: dV, mode 3: dK (out) and dV (out2) over the transposed
 // CSR. `lse2` = LSE * log2(e).
+// Work items per head of the tcgen05 backward: nb, or ceil(nb/2) pairs of
+// 64-token blocks (pair p = blocks 2p and 2p+1 of a CSR row / CSC column list).
+int attn_bwd_tc_items_per_head(const Dims& s);
 bool attn_bwd_tc_supported(const Dims& s);
 sparsp_status_t launch_attn_bwd_tc(const Dims& s, int mode, const __nv_bfloat16* q,
                                    const __nv_bfloat16* k, const __nv_bfloat16* v,

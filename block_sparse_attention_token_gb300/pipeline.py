@@ -105,11 +105,11 @@ class Pipeline:
                                        dtype=torch.uint8, device=dev)
         # the tcgen05 forward takes O straight into raster order (64-token blocks with
         # d = 128 beyond 1,024 blocks run the portable kernel, which writes block
-        # order only); with a backward, only where the tcgen05 backward (Bt = 128,
-        # d = 64 or 128) also reads raster O and writes raster dQ, dK, dV
+        # order only); the tcgen05 backward (the same shapes) also reads raster O
+        # and writes raster dQ, dK, dV
         fwd_raster = (s.torch_dtype == torch.bfloat16 and not (flags & 2) and s.Bt in (64, 128)
                       and s.d in (64, 128) and not (s.Bt == 64 and s.d == 128 and s.nb > 1024))
-        self.raster_out = fwd_raster and (not backward or s.Bt == 128)
+        self.raster_out = fwd_raster
         self._o_fwd = None   # the buffer forward() last wrote O to (read by backward() when raster)
         # block-order O (and gradients) only where attention does not write raster rows
         self.ob = None if self.raster_out else torch.empty(blocked, dtype=dt, device=dev)

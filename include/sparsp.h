@@ -108,7 +108,7 @@ enum {
    * Backward: o is read in raster order (as the forward wrote it with this
    * option) and dq, dk, dv are written in raster order; q, k, v, dout and lse
    * stay in block order (the kernels read them as tiles). Only the tcgen05
-   * backward (Bt = 128, d = 64 or 128) does this; elsewhere
+   * backward (the tcgen05 forward's shapes) does this; elsewhere
    * SPARSP_ERR_UNSUPPORTED. */
   SPARSP_OUT_RASTER = 1u << 3
 };
@@ -425,10 +425,12 @@ SPARSP_API sparsp_status_t sparsp_attn_fwd(const sparsp_shape_t* shape, const vo
  * bf16 only. dq, dk, dv: blocked [B,H,N,d] bf16 (raster [B,N,H,d], and o
  * raster too, with SPARSP_OUT_RASTER). dQ is accumulated per query
  * block over its CSR row and dK/dV per key block over the transposed CSR, so
- * the result is deterministic (no atomics on values). On tcgen05 (Bt = 128,
- * d = 64 or 128, without SPARSP_KERNEL_PORTABLE) one kernel computes dQ and
- * one both dK and dV (two with SPARSP_BWD_SPLIT_KV); other shapes run the
- * portable mma.sync kernels.
+ * the result is deterministic (no atomics on values). On tcgen05 (bf16, Bt
+ * and d in {64, 128}, nb <= 1024 when Bt = 64 and d = 128, without
+ * SPARSP_KERNEL_PORTABLE) one kernel computes dQ and one both dK and dV (two
+ * with SPARSP_BWD_SPLIT_KV), 64-token blocks as pairs of neighbouring blocks
+ * over the union of their two lists; other shapes run the portable mma.sync
+ * kernels.
  * ws: at least sparsp_attn_workspace_size(shape, 1) bytes.
  */
 SPARSP_API sparsp_status_t sparsp_attn_bwd(const sparsp_shape_t* shape, const void* q, const void* k,

@@ -801,12 +801,12 @@ def test_attn_bwd(name):
 
 
 @pytest.mark.parametrize("split", [False, True])
-@pytest.mark.parametrize("name", ["r128", "wave", "r64", "r128d64"])
+@pytest.mark.parametrize("name", ["r128", "wave", "r64", "r128d64", "medium", "r64odd"])
 def test_attn_bwd_raster_output(name, split):
     """With OUT_RASTER the backward reads the raster O the forward wrote and
     writes dQ, dK, dV straight into raster order: bit for bit the inverse
-    reorder of the block-ordered gradients. Shapes without the tcgen05
-    backward refuse the flag before enqueuing anything."""
+    reorder of the block-ordered gradients. The portable kernels refuse the
+    flag before enqueuing anything."""
     wl, data, shape = _setup(name)
     ch = OracleChain(wl, data)
     dob = orc.reorder(synth.round_bf16(np.random.default_rng(wl.seed + 101).standard_normal(
@@ -816,11 +816,6 @@ def test_attn_bwd_raster_output(name, split):
     st = status_word()
     extra = sp.BWD_SPLIT_KV if split else 0
     o, lse = sp.attn_fwd(shape, q, k, v, rp, ci, status=st)
-    if shape.Bt != 128:
-        o_r = sp.reorder(shape, o, inverse=True)
-        with pytest.raises(sp.SparspError):
-            sp.attn_bwd(shape, q, k, v, o_r, lse, do, rp, ci, flags=sp.OUT_RASTER | extra)
-        return
     o_r, lse_r = sp.attn_fwd(shape, q, k, v, rp, ci, flags=sp.OUT_RASTER, status=st)
     grads = sp.attn_bwd(shape, q, k, v, o, lse, do, rp, ci, flags=extra, status=st)
     raster = sp.attn_bwd(shape, q, k, v, o_r, lse_r, do, rp, ci, flags=sp.OUT_RASTER | extra, status=st)
