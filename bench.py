@@ -316,6 +316,24 @@ class Run:
         side = ("attn_fwd", "kv_gather") if self.pipe.overlap_demand else ()
         return start.elapsed_time(end) / steps, stage_times(marks, side, lambda a, b: a.elapsed_time(b), steps)
 
+    def graph_ms(self, steps):
+        """The same step captured as one CUDA graph (Pipeline.capture) and
+        replayed: ms per step, with the host's per-kernel launches gone."""
+        torch = self.torch
+        graphed = self.pipe.capture(self.dev_in["q"], self.dev_in["k"], self.dev_in["v"],
+                                    dout=self.dout if self.wl.backward else None, **self.kw)
+        for _ in range(3):
+            graphed.replay()
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(self.stream)
+        for _ in range(steps):
+            graphed.replay()
+        end.record(self.stream)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) / steps
+
     def attn_alone_ms(self, calls=5):
         """The forward attention kernel with nothing beside it (in the step it
         may share its SMs with the KV gather)."""
@@ -423,6 +441,9 @@ def workload_summary(sp, name, args, pk) -> dict:
     out["stages_ms"] = {k: round(v, 5) for k, v in st.items()}
     if wl.skew:
         out["attn_sm_imbalance"] = run.sm_imbalance()
+    gms = run.graph_ms(min(args.steps, 10))
+    out["graph_ms_per_step"] = gms
+    out["graph_tflops"] = f_step / (gms * 1e-3) / 1e12
     if not args.no_e2e:
         e = end_to_end(sp, run, min(args.steps, 10), f_step)
         out["e2e_ms_per_step"] = e["ms_per_step"]

@@ -467,5 +467,5 @@ def default_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
 
 
-from .pipeline import Pipeline  # noqa: E402,F401
+from .pipeline import GraphedStep, Pipeline  # noqa: E402,F401
 from .streaming import HostPipeline  # noqa: E402,F401

@@ -10,7 +10,9 @@ attention backward -> dQ, dK, dV in raster order (likewise). Every step is one
 or more libsparsp kernels on the current stream, except that by default the
 KV demand gather runs on a side
 stream beside attention (the caller's stream waits for both); nothing here
-allocates after construction.
+allocates after construction. capture() records forward() (and, with a
+backward, forward() + backward()) as one CUDA graph, for shapes where the
+host's launches, not the kernels, set the pace.
 """
 from __future__ import annotations
 
@@ -266,3 +268,45 @@ class Pipeline:
         reorder(s, self.dvb, dv, inverse=True)
         mark("reorder_grads")
         return dq, dk, dv
+
+    def capture(self, q, k, v, wq=None, wk=None, dout=None) -> "GraphedStep":
+        """A CUDA graph of one step on these device buffers: forward(q, k, v),
+        and backward(dout) too when dout is given. replay() reruns the whole
+        step with one launch on whatever the buffers hold at that moment (the
+        caller refills them in place) and returns what the step returns. The
+        step runs once eagerly on a side stream first, as graph capture wants;
+        the buffers stay bound to the graph. The captured step runs the KV
+        demand gather before attention on one stream: a graph does not keep the
+        side streams' priorities, without which the gather beside attention
+        takes the SMs attention needs."""
+        def step():
+            out = self.forward(q, k, v, wq=wq, wk=wk)
+            return out if dout is None else out + self.backward(dout)
+        overlap, self.overlap_demand = self.overlap_demand, False
+        try:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                step()
+            torch.cuda.current_stream().wait_stream(side)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                outs = step()
+        finally:
+            self.overlap_demand = overlap
+        return GraphedStep(graph, outs)
+
+
+class GraphedStep:
+    """A captured Pipeline step (Pipeline.capture)."""
+
+    def __init__(self, graph, outs):
+        self.graph = graph
+        self.outs = outs
+
+    def replay(self):
+        """Runs the step on the current stream; returns the step's outputs
+        (O, LSE[, dQ, dK, dV]) in the buffers the capture bound."""
+        self.graph.replay()
+        return self.outs
+
