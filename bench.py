@@ -477,12 +477,21 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="skip the other seeded workloads")
     ap.add_argument("--heads", type=int, default=0, help="override the head count (smaller profiling case)")
+    ap.add_argument("--head-dim", type=int, default=0, choices=[0, 64, 128],
+                    help="override the head dimension (profiling the d = 64 kernels on a workload's shape)")
+    ap.add_argument("--tile-frames", type=int, default=0, choices=[0, 1, 2],
+                    help="override the tile's frame count (1: 64-token blocks on a 2x8x8 workload)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     wl = synth.WORKLOADS[args.workload]
-    if args.heads:
+    if args.heads or args.head_dim or args.tile_frames:
         import dataclasses
-        wl = dataclasses.replace(wl, H=args.heads, name=f"{wl.name}-h{args.heads}")
+        if args.heads:
+            wl = dataclasses.replace(wl, H=args.heads, name=f"{wl.name}-h{args.heads}")
+        if args.head_dim:
+            wl = dataclasses.replace(wl, d=args.head_dim, name=f"{wl.name}-d{args.head_dim}")
+        if args.tile_frames:
+            wl = dataclasses.replace(wl, ta=args.tile_frames, name=f"{wl.name}-ta{args.tile_frames}")
     if args.impl == "reference":
         return run_reference(args, wl)
 
