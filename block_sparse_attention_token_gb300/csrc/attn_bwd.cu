@@ -31,11 +31,19 @@ rowdot_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restri
   // 8 threads per row (d <= 128: 16 bf16 each) -> 32 rows per CTA
   const int64_t row = (int64_t)blockIdx.x * 32 + (threadIdx.x >> 3);
   const int sub = threadIdx.x & 7;
+  // the block-order row's O row: the same, or its raster row (the index
+  // arithmetic once per row, by the row's first thread)
+  int64_t orow = row;
+  if (o_raster) {
+    int64_t r = 0;
+    if (sub == 0 && row < rows) {
+      const int64_t rem = row % rm.N;
+      r = rm.row(row / rm.N, (int)(rem / Bt), (int)(rem % Bt));
+    }
+    orow = __shfl_sync(0xffffffffu, r, (threadIdx.x & 31) & ~7);
+  }
   float acc = 0.f;
   if (row < rows) {
-    // the block-order row's O row: the same, or its raster row
-    const int64_t rem = row % rm.N;
-    const int64_t orow = o_raster ? rm.row(row / rm.N, (int)(rem / Bt), (int)(rem % Bt)) : row;
     const int per = d / 8;   // elements per thread: 8 or 16
     for (int c = sub * per; c < (sub + 1) * per; c += 8) {
       const uint4 a = *reinterpret_cast<const uint4*>(o + orow * d + c);
