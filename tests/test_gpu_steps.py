@@ -767,6 +767,34 @@ def test_attn_fwd_pair_rejects_a_repeated_index():
     compare_values(on[0, 0, 3 * g.Bt:4 * g.Bt], O[0, 0, 3 * g.Bt:4 * g.Bt], wl, "O of the partner row")
 
 
+def test_attn_bwd_pair_rejects_a_repeated_index():
+    """The dQ kernel with 64-token blocks (pairs) reports a CSR row that lists a
+    key block twice (SPARSP_ERR_DATA), leaves that row block's dQ unwritten and
+    still computes its partner's."""
+    wl, data, shape = _setup("r64odd")
+    ch = OracleChain(wl, data)
+    g = ch.g
+    q, k, v = dev(ch.qb, wl), dev(ch.kb, wl), dev(ch.vb, wl)
+    rp, ci = i32(ch.sel.row_ptr), i32(ch.sel.col_idx)
+    o, lse = sp.attn_fwd(shape, q, k, v, rp, ci)
+    rows = [ch.sel.col_idx[ch.sel.row_ptr[r]:ch.sel.row_ptr[r + 1]].copy() for r in range(g.B * g.H * g.nb)]
+    rows[2] = np.concatenate([rows[2], rows[2][:1]])            # row 2 repeats its first block
+    rp2 = np.concatenate([[0], np.cumsum([len(x) for x in rows])]).astype(np.int32)
+    ci2 = np.concatenate(rows).astype(np.int32)
+    dob = orc.reorder(synth.round_bf16(np.random.default_rng(wl.seed + 9).standard_normal(
+        data["q"].shape, dtype=np.float32)), g)
+    st = status_word()
+    dq = torch.full_like(q, 7.0)
+    sp.attn_bwd(shape, q, k, v, o, lse, dev(dob, wl), i32(rp2), i32(ci2), dq=dq, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == sp.DATA
+    dqn = host(dq)
+    assert (dqn[0, 0, 2 * g.Bt:3 * g.Bt] == 7.0).all()
+    dQ, _, _ = orc.attn_bwd(ch.qb, ch.kb, ch.vb, dob, ch.sel.row_ptr, ch.sel.col_idx, g.Bt, ch.scale,
+                            q_blocks={(0, 0, 3)}, k_blocks=set())
+    compare_values(dqn[0, 0, 3 * g.Bt:4 * g.Bt], dQ[0, 0, 3 * g.Bt:4 * g.Bt], wl, "dQ of the partner row")
+
+
 @pytest.mark.parametrize("name", BWD)
 def test_attn_bwd(name):
     wl, data, shape = _setup(name)
