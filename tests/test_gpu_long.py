@@ -1,8 +1,10 @@
 """Long sequences: 2,048 and 4,096 blocks per head (up to 524,288 tokens in
 128-token blocks, the sequence lengths of "Dynamic Sparsity in Large-Scale
-Video DiT Training", summary). The steps run in the pipeline's launch
-configuration; cheap outputs are compared in full with the oracle, attention
-values and gradients on sampled blocks the oracle computes one by one."""
+Video DiT Training", summary), and 1,024-block heads for the d = 64 and the
+64-token-block (paired) tcgen05 kernels, forward and backward. The steps run
+in the pipeline's launch configuration; cheap outputs are compared in full
+with the oracle, attention values and gradients on sampled blocks the oracle
+computes one by one."""
 import numpy as np
 import pytest
 import torch
@@ -25,6 +27,12 @@ LONG = {
     # 4,096 blocks (524,288 tokens), one head, Top-k 10%
     "long4k": W("long-524k-bf16", 1, 1, 128, 128, 64, 64, 2, 8, 8, "bf16", "mean", 0.0, 410, 8, 8,
                 False, False, 43),
+    # 128-token blocks, d = 64: 1,024 blocks (131,072 tokens), Top-k 10%, with a backward
+    "long1k-d64": W("long-131k-bt128-d64-bf16", 1, 2, 64, 32, 64, 64, 2, 8, 8, "bf16", "mean", 0.0, 103, 8, 8,
+                    False, True, 44),
+    # 64-token blocks (pairs), d = 128: 1,024 blocks of 1x8x8 (65,536 tokens), Top-k 10%, with a backward
+    "long1k-bt64": W("long-65k-bt64-bf16", 1, 2, 128, 16, 64, 64, 1, 8, 8, "bf16", "mean", 0.0, 103, 8, 8,
+                     False, True, 45),
 }
 
 
@@ -52,7 +60,7 @@ def run(request):
 
 
 def test_long_reorder_scores_and_status(run):
-    assert run.shape.nb in (2048, 4096)
+    assert run.shape.nb in (1024, 2048, 4096)
     assert run.pipe.status.item() == 0
     assert np.array_equal(host(run.pipe.qb), run.ch.qb)
     S = run.ch.S64
