@@ -103,7 +103,7 @@ struct Cfg {
   // has half of the SM's shared memory for tiles of half the size: 3 K and 2 V
   static constexpr int NK = 3, NV = DUO ? 2 : 3;
   static constexpr int NSB = DUO ? 1 : 2, NPB = DUO ? 1 : 2;   // S and P buffers in TMEM
-  static constexpr int NI = DUO ? 2 : kNI;                      // item ring slots
+  static constexpr int NI = DUO || PAIR ? 2 : kNI;              // item ring slots
   static constexpr int kMinCtas = DUO ? 2 : 1;                  // CTAs per SM
   static constexpr uint32_t kColS = 0, kColO = DUO ? 128 : 256, kColP = DUO ? 192 : 384;
   static constexpr uint32_t kTmemCols = DUO ? 256 : 512;
@@ -118,13 +118,16 @@ struct Cfg {
   static constexpr uint32_t kOffRing = kOffBar + 8 * NBAR;
   static constexpr uint32_t kOffBits = kOffRing + 16 * NI;
   static constexpr uint32_t kBitsBytes = PAIR ? NI * 2 * MAXW * 4 : 0;
-  // DUO: per item slot, one byte per block of the union of the pair's rows in
-  // ascending order (byte 2s + t: block t of stage s; bit 0 = the first row
-  // selected it, bit 1 = the second), written by the producer with the item so
-  // that the softmax warps read a stage's masks with one shared-memory load
-  static constexpr uint32_t kMaskBytes = DUO && PAIR ? 32 * MAXW : 0;
+  // pairs: per item slot, which of the pair's two rows selected each block of
+  // the union of their rows (ascending), written by the producer with the item
+  // so that the softmax warps read a stage's masks with one shared-memory load:
+  // one byte per block with DUO (bytes 2s, 2s + 1: stage s; bit 0 = the first
+  // row, bit 1 = the second), two bits per block where shared memory is short
+  // (d = 128: stage s is nibble s)
+  static constexpr bool MASK_BYTES = DUO;
+  static constexpr uint32_t kMaskWords = !PAIR ? 0 : (MASK_BYTES ? 8 * MAXW + 4 : 2 * MAXW + 1);
   static constexpr uint32_t kOffMask = kOffBits + kBitsBytes;
-  static constexpr uint32_t kOffMisc = kOffMask + NI * kMaskBytes;
+  static constexpr uint32_t kOffMisc = kOffMask + NI * kMaskWords * 4;
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
   static_assert(kSmemBytes <= (DUO ? 115712u : 232448u), "shared memory");
 };
@@ -202,7 +205,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   // ring entry: x = item, y = stages (-1: skip, -2: end), z = bad-row bits (pairs)
   volatile int4* ring = reinterpret_cast<volatile int4*>(gbase + C::kOffRing);
   uint32_t* bits = reinterpret_cast<uint32_t*>(gbase + C::kOffBits);   // [C::NI][2][C::MAXW] (pairs)
-  uint8_t* masks = gbase + C::kOffMask;                                 // [C::NI][C::kMaskBytes] (DUO)
+  uint32_t* masks = reinterpret_cast<uint32_t*>(gbase + C::kOffMask);   // [C::NI][C::kMaskWords] (pairs)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + C::kOffMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -283,9 +286,10 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           if (badbits && lane == 0) report(p.d_status, SPARSP_ERR_DATA);
           const int u = union_count(bmA, bmB, words, lane);
           len = (badbits == 3) ? -1 : (u + 1) / 2;   // stages of two key blocks
-          if constexpr (C::DUO) {
-            union_masks(bmA, bmB, words, u, lane, masks + ri * C::kMaskBytes);
-          }
+          if constexpr (C::MASK_BYTES)
+            union_masks(bmA, bmB, words, u, lane, reinterpret_cast<uint8_t*>(masks + ri * C::kMaskWords));
+          else
+            union_masks2(bmA, bmB, words, u, lane, masks + ri * C::kMaskWords);
         } else {
           const int32_t a = p.row_ptr[item], b = p.row_ptr[item + 1];
           bool bad = (b < a) || (b - a > nb);
@@ -600,22 +604,19 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           if (PAIR) release();
           continue;
         }
-        const uint32_t* bmA = bits + ri * 2 * C::MAXW;
-        const uint32_t* mine = bmA + half * C::MAXW;
-        UnionWalk walk(bmA, bmA + C::MAXW, PAIR && !C::DUO ? words : 0);
-        const uint16_t* mk = reinterpret_cast<const uint16_t*>(masks + ri * C::kMaskBytes);
+        const uint32_t* mk = masks + ri * C::kMaskWords;
         float m = -INFINITY, l = 0.f;
         for (int e = 0; e < len; ++e) {
           // which halves of this stage's 128 columns this row attends to (warp-uniform)
           bool has1 = true, has2 = true;
-          if constexpr (C::DUO && PAIR) {
-            const uint32_t st = mk[e];
+          if constexpr (PAIR && C::MASK_BYTES) {
+            const uint32_t st = reinterpret_cast<const uint16_t*>(mk)[e];   // bytes 2e, 2e + 1
             has1 = (st >> half) & 1u;
             has2 = (st >> (8 + half)) & 1u;
           } else if constexpr (PAIR) {
-            const int j1 = walk.next(), j2 = walk.next();
-            has1 = bit_of(mine, j1);
-            has2 = j2 >= 0 && bit_of(mine, j2);
+            const uint32_t nib = mk[e >> 3] >> (4 * (e & 7));   // stage e's two blocks, two rows
+            has1 = (nib >> half) & 1u;
+            has2 = (nib >> (2 + half)) & 1u;
           }
           const uint32_t b = s_use % C::NSB;
           if (!(ok = wait_warp(bar(S_FULL + b), (s_use / C::NSB) & 1u, g))) break;

@@ -100,5 +100,50 @@ __device__ __forceinline__ void union_masks(const uint32_t* a, const uint32_t* b
   if ((u & 1) && lane == 0) mk[u] = 0;
 }
 
+// The same masks at two bits per union block (bit 2r: a has the block of
+// rank r; bit 2r + 1: b has it), so that stage s (ranks 2s, 2s + 1) is nibble
+// s of mk. Warp-collective; mk holds at least (2u + 31) / 32 + 1 words, which
+// are cleared first (ranks of one word can come from different lanes).
+__device__ __forceinline__ void union_masks2(const uint32_t* a, const uint32_t* b, int words, int u, int lane,
+                                             uint32_t* mk) {
+  const int nw = (2 * u + 31) / 32 + 1;
+  for (int w = lane; w < nw; w += 32) mk[w] = 0u;
+  __syncwarp();
+  int base_rank = 0;
+  for (int w0 = 0; w0 < words; w0 += 32) {
+    const int w = w0 + lane;
+    const uint32_t x = w < words ? a[w] : 0u, y = w < words ? b[w] : 0u;
+    uint32_t un = x | y;
+    const int c = __popc(un);
+    int incl = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += t;
+    }
+    // this word's c codes (ranks rk0 .. rk0 + c - 1) as 64 bits in registers,
+    // then OR-ed into the at most three mask words they straddle
+    const int rk0 = base_rank + incl - c;
+    uint32_t lo = 0u, hi = 0u;
+    for (int n = 0; un != 0u; ++n) {
+      const int bit = __ffs(un) - 1;
+      un &= un - 1u;
+      const uint32_t code = ((x >> bit) & 1u) | (((y >> bit) & 1u) << 1);
+      if (n < 16) lo |= code << (2 * n);
+      else hi |= code << (2 * (n - 16));
+    }
+    if (c > 0) {
+      const int wd = rk0 >> 4, sh = 2 * (rk0 & 15);
+      atomicOr(&mk[wd], lo << sh);
+      const uint32_t m1 = (sh ? lo >> (32 - sh) : 0u) | (hi << sh);
+      const uint32_t m2 = sh ? hi >> (32 - sh) : 0u;
+      if (m1) atomicOr(&mk[wd + 1], m1);
+      if (m2) atomicOr(&mk[wd + 2], m2);
+    }
+    base_rank += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  __syncwarp();
+}
+
 }  // namespace tc
 }  // namespace sparsp
