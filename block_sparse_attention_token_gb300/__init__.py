@@ -29,6 +29,7 @@ SCHED_FLAT = 1
 KERNEL_PORTABLE = 2
 BWD_SPLIT_KV = 4
 OUT_RASTER = 8
+IN_RASTER = 16
 GRID_CAP_SHIFT = 16
 
 
@@ -414,8 +415,8 @@ def attn_fwd(shape: Shape, q, k, v, row_ptr, col_idx, scale: float = 0.0, o=None
     """Returns (O blocked [B,H,N,d], or raster [B,N,H,d] with OUT_RASTER; LSE [B,H,N] fp32)."""
     dev = q.device
     if o is None:
-        o = (torch.empty((shape.B, shape.N, shape.H, shape.d), dtype=q.dtype, device=dev)
-             if flags & OUT_RASTER else torch.empty_like(q))
+        o = torch.empty((shape.B, shape.N, shape.H, shape.d) if flags & OUT_RASTER else
+                        (shape.B, shape.H, shape.N, shape.d), dtype=q.dtype, device=dev)
     if lse is None:
         lse = torch.empty((shape.B, shape.H, shape.N), dtype=torch.float32, device=dev)
     if ws is None:

@@ -53,7 +53,7 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Every attention option bit; a call ignores the ones that do not concern it.
 constexpr uint32_t kKnownFlags = SPARSP_SCHED_FLAT | SPARSP_KERNEL_PORTABLE | SPARSP_BWD_SPLIT_KV |
-                                 SPARSP_OUT_RASTER | SPARSP_GRID_CAP_MASK;
+                                 SPARSP_OUT_RASTER | SPARSP_IN_RASTER | SPARSP_GRID_CAP_MASK;
 
 // Attention workspace layout: items, counter(s), then backward extras.
 struct AttnWs {
@@ -467,7 +467,8 @@ sparsp_status_t sparsp_attn_fwd(const sparsp_shape_t* shape, const void* q, cons
   if (scale <= 0.f) scale = 1.0f / sqrtf((float)s.d);
   const bool tc = s.dtype != SPARSP_F32 && !(flags & SPARSP_KERNEL_PORTABLE) && attn_fwd_tc_supported(s);
   const bool raster = (flags & SPARSP_OUT_RASTER) != 0;
-  if (raster && !tc) return SPARSP_ERR_UNSUPPORTED;   // only the tcgen05 kernel writes raster rows
+  const bool in_raster = (flags & SPARSP_IN_RASTER) != 0;
+  if ((raster || in_raster) && !tc) return SPARSP_ERR_UNSUPPORTED;   // only the tcgen05 kernel reads or writes raster rows
   cudaStream_t st = (cudaStream_t)stream;
   const bool flat = (flags & SPARSP_SCHED_FLAT) != 0;
   if (tc && attn_fwd_tc_items_per_head(s) != s.nb) {
@@ -489,7 +490,7 @@ sparsp_status_t sparsp_attn_fwd(const sparsp_shape_t* shape, const void* q, cons
   if (tc)
     return launch_attn_fwd_tc(s, (const __nv_bfloat16*)q, (const __nv_bfloat16*)k,
                               (const __nv_bfloat16*)v, row_ptr, col_idx, scale,
-                              (__nv_bfloat16*)o, lse, raster, w.items, w.counter, prof, d_status, st);
+                              (__nv_bfloat16*)o, lse, raster, in_raster, w.items, w.counter, prof, d_status, st);
   return launch_attn_fwd_mma(s, (const __nv_bfloat16*)q, (const __nv_bfloat16*)k,
                              (const __nv_bfloat16*)v, row_ptr, col_idx, scale, (__nv_bfloat16*)o,
                              lse, w.items, w.counter, prof, d_status, st);
@@ -507,6 +508,7 @@ sparsp_status_t sparsp_attn_bwd(const sparsp_shape_t* shape, const void* q, cons
   if (s.dtype != SPARSP_BF16) return SPARSP_ERR_UNSUPPORTED;
   if (isnan(scale) || isinf(scale)) return SPARSP_ERR_INVALID_ARG;
   if (flags & ~kKnownFlags) return SPARSP_ERR_INVALID_ARG;
+  if (flags & SPARSP_IN_RASTER) return SPARSP_ERR_UNSUPPORTED;   // the backward reads block-ordered tiles
   s.max_ctas = (int)((flags & SPARSP_GRID_CAP_MASK) >> SPARSP_GRID_CAP_SHIFT);
   CHECK_PTR(q);
   CHECK_PTR(k);

@@ -184,6 +184,9 @@ struct Params {
   // reorder); otherwise block order like Q
   int raster;
   RasterMap rm;
+  // raster input: Q, K, V read from [B, N, H, d] through 5-D maps, one block per box
+  int in_raster;
+  RasterBox rbox;
   const int32_t* items;
   int32_t* counter;
   uint64_t* prof;
@@ -326,7 +329,18 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       if (lane == 0) {
         mbar_arrive_expect_tx(bar(Q_FULL), C::kQTile);
 #pragma unroll
-        for (int h = 0; h < C::NBOX; ++h) tma_load_2d(sQ + h * C::kQBox, &tq, bar(Q_FULL), 64 * h, yq);
+        for (int h = 0; h < C::NBOX; ++h) {
+          if (p.in_raster) {   // the item's block(s), one 5-D box each
+            const int4 c = p.rbox.at(bh, i0);
+            tma_load_5d(sQ + h * C::kQBox, &tq, bar(Q_FULL), 64 * h, c.x, c.y, c.z, c.w);
+            if (PAIR) {   // a head's last pair of an odd nb loads its first block twice (never stored)
+              const int4 c2 = p.rbox.at(bh, i0 + 1 < nb ? i0 + 1 : i0);
+              tma_load_5d(sQ + h * C::kQBox + C::kHalfBox, &tq, bar(Q_FULL), 64 * h, c2.x, c2.y, c2.z, c2.w);
+            }
+          } else {
+            tma_load_2d(sQ + h * C::kQBox, &tq, bar(Q_FULL), 64 * h, yq);
+          }
+        }
       }
       ++q_fill;
       const int32_t e0 = PAIR ? 0 : p.row_ptr[item];
@@ -352,8 +366,17 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 #pragma unroll
           for (int h = 0; h < C::NBOX; ++h) {
             const uint32_t dst = sK + ks * C::kKTile + h * C::kKBox;
-            tma_load_2d(dst, &tk, bar(K_FULL + ks), 64 * h, yk1);
-            if (PAIR) tma_load_2d(dst + C::kHalfBox, &tk, bar(K_FULL + ks), 64 * h, yk2);
+            if (p.in_raster) {
+              const int4 c1 = p.rbox.at(bh, j1);
+              tma_load_5d(dst, &tk, bar(K_FULL + ks), 64 * h, c1.x, c1.y, c1.z, c1.w);
+              if (PAIR) {
+                const int4 c2 = p.rbox.at(bh, j2);
+                tma_load_5d(dst + C::kHalfBox, &tk, bar(K_FULL + ks), 64 * h, c2.x, c2.y, c2.z, c2.w);
+              }
+            } else {
+              tma_load_2d(dst, &tk, bar(K_FULL + ks), 64 * h, yk1);
+              if (PAIR) tma_load_2d(dst + C::kHalfBox, &tk, bar(K_FULL + ks), 64 * h, yk2);
+            }
           }
         }
         ++k_fill;
@@ -364,8 +387,17 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 #pragma unroll
           for (int h = 0; h < C::NBOX; ++h) {
             const uint32_t dst = sV + vs * C::kKTile + h * C::kKBox;
-            tma_load_2d(dst, &tv, bar(V_FULL + vs), 64 * h, yk1);
-            if (PAIR) tma_load_2d(dst + C::kHalfBox, &tv, bar(V_FULL + vs), 64 * h, yk2);
+            if (p.in_raster) {
+              const int4 c1 = p.rbox.at(bh, j1);
+              tma_load_5d(dst, &tv, bar(V_FULL + vs), 64 * h, c1.x, c1.y, c1.z, c1.w);
+              if (PAIR) {
+                const int4 c2 = p.rbox.at(bh, j2);
+                tma_load_5d(dst + C::kHalfBox, &tv, bar(V_FULL + vs), 64 * h, c2.x, c2.y, c2.z, c2.w);
+              }
+            } else {
+              tma_load_2d(dst, &tv, bar(V_FULL + vs), 64 * h, yk1);
+              if (PAIR) tma_load_2d(dst + C::kHalfBox, &tv, bar(V_FULL + vs), 64 * h, yk2);
+            }
           }
         }
         ++v_fill;
@@ -775,20 +807,24 @@ sparsp_status_t go_fwd(const Dims& s, const CUtensorMap& tq, const CUtensorMap& 
 sparsp_status_t launch_attn_fwd_tc(const Dims& s, const __nv_bfloat16* q, const __nv_bfloat16* k,
                                    const __nv_bfloat16* v, const int32_t* row_ptr,
                                    const int32_t* col_idx, float scale, __nv_bfloat16* o,
-                                   float* lse, bool raster, const int32_t* items, int32_t* counter,
-                                   uint64_t* prof, int32_t* d_status, cudaStream_t st) {
+                                   float* lse, bool raster, bool in_raster, const int32_t* items,
+                                   int32_t* counter, uint64_t* prof, int32_t* d_status, cudaStream_t st) {
   const uint64_t rows = (uint64_t)s.B * s.H * s.N;
   CUtensorMap tq, tk, tv;
-  // Q boxes are 128 rows (the MMA's M) whatever the block size; K and V boxes one block
-  if (!make_tmap_bf16_rows(&tq, q, rows, (uint64_t)s.d, 128) ||
-      !make_tmap_bf16_rows(&tk, k, rows, (uint64_t)s.d, (uint32_t)s.Bt) ||
-      !make_tmap_bf16_rows(&tv, v, rows, (uint64_t)s.d, (uint32_t)s.Bt))
+  if (in_raster) {
+    // raster inputs: one block per 5-D box (two boxes for a pair's query tile)
+    if (!make_tmap_bf16_raster(&tq, q, s) || !make_tmap_bf16_raster(&tk, k, s) || !make_tmap_bf16_raster(&tv, v, s))
+      return SPARSP_ERR_CUDA;
+  } else if (!make_tmap_bf16_rows(&tq, q, rows, (uint64_t)s.d, 128) ||   // Q boxes: the MMA's 128 rows
+             !make_tmap_bf16_rows(&tk, k, rows, (uint64_t)s.d, (uint32_t)s.Bt) ||   // K, V: one block
+             !make_tmap_bf16_rows(&tv, v, rows, (uint64_t)s.d, (uint32_t)s.Bt)) {
     return SPARSP_ERR_CUDA;
+  }
   // 64-token blocks: items are pairs of query blocks, ordered by the caller
   // over the pair rows (attn_fwd_tc_items)
   const int nbp = attn_fwd_tc_items_per_head(s);
   Params prm{row_ptr, col_idx, s.N, s.nb, nbp, (int64_t)s.B * s.H * nbp, (int64_t)rows, scale * 1.4426950408889634f, o, lse,
-             raster ? 1 : 0, raster_map(s), items, counter, prof, d_status};
+             raster ? 1 : 0, raster_map(s), in_raster ? 1 : 0, raster_box(s), items, counter, prof, d_status};
   if (s.Bt == 128 && s.d == 128) return go_fwd<128, 128>(s, tq, tk, tv, prm, st);
   if (s.Bt == 128 && s.d == 64) return go_fwd<128, 64>(s, tq, tk, tv, prm, st);
   if (s.Bt == 64 && s.d == 128) return go_fwd<64, 128>(s, tq, tk, tv, prm, st);

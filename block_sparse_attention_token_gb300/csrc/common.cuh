@@ -184,8 +184,8 @@ int attn_fwd_tc_items_per_head(const Dims& s);
 sparsp_status_t launch_attn_fwd_tc(const Dims& s, const __nv_bfloat16* q, const __nv_bfloat16* k,
                                    const __nv_bfloat16* v, const int32_t* row_ptr,
                                    const int32_t* col_idx, float scale, __nv_bfloat16* o,
-                                   float* lse, bool raster, const int32_t* items, int32_t* counter,
-                                   uint64_t* prof, int32_t* d_status, cudaStream_t st);
+                                   float* lse, bool raster, bool in_raster, const int32_t* items,
+                                   int32_t* counter, uint64_t* prof, int32_t* d_status, cudaStream_t st);
 
 // Attention backward pieces.
 // D = rowsum(dO * O) per block-order row (o in raster order when o_raster)

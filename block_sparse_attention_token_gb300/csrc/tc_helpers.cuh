@@ -86,6 +86,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// A 5-D box (a raster tile: columns, head, x, y, frame; see make_tmap_bf16_raster).
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                            int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], "
+      "[%2];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
+
 // 1-D bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16),
 // completing on an mbarrier's transaction count.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -246,5 +256,21 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 // 64 x box_rows box and 128-byte swizzle. Returns false on failure.
 bool make_tmap_bf16_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                          uint32_t box_rows);
+
+// Host side: tensor map of a raster [B, N, H, d] bf16 tensor (N = T*Y*X) as 5-D
+// (column, head, x, y, b*T + t) with a box of 64 columns x one head x one tile
+// (tc x tb x ta tokens): one block's 64-column box, its rows in block order
+// (frame, row, column of the tile), 128-byte swizzle. Returns false on failure.
+bool make_tmap_bf16_raster(CUtensorMap* map, const void* base, const Dims& s);
+
+// Box origin of block j of head bh in a raster map: (head, x, y, frame).
+struct RasterBox {
+  int H, T, nY, nX, ta, tb, tc;
+  __device__ __forceinline__ int4 at(int64_t bh, int j) const {
+    const int bx = j % nX, by = (j / nX) % nY, bt = j / (nX * nY);
+    return make_int4((int)(bh % H), bx * tc, by * tb, (int)(bh / H) * T + bt * ta);
+  }
+};
+inline RasterBox raster_box(const Dims& s) { return RasterBox{s.H, s.T, s.nY, s.nX, s.ta, s.tb, s.tc}; }
 
 }  // namespace sparsp

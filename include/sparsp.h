@@ -110,7 +110,13 @@ enum {
    * stay in block order (the kernels read them as tiles). Only the tcgen05
    * backward (the tcgen05 forward's shapes) does this; elsewhere
    * SPARSP_ERR_UNSUPPORTED. */
-  SPARSP_OUT_RASTER = 1u << 3
+  SPARSP_OUT_RASTER = 1u << 3,
+  /* Forward: q, k, v are read in raster order [B, N, H, d] (the layout
+   * sparsp_reorder takes) instead of block order: the kernel loads each block
+   * as one 5-D tile (column, head, x, y, frame), so no reorder pass is needed.
+   * Results are bitwise those of the block-ordered inputs. Only the tcgen05
+   * kernel does this; elsewhere SPARSP_ERR_UNSUPPORTED. */
+  SPARSP_IN_RASTER = 1u << 4
 };
 /* Attention kernels: at most n persistent CTAs (1 <= n <= 4095) instead of
  * one per SM (times the kernel's occupancy), encoded in bits 16..27 of the

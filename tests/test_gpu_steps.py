@@ -673,6 +673,28 @@ def test_attn_fwd_raster_output(name):
         sp.attn_fwd(shape, q, k, v, rp, ci, flags=sp.OUT_RASTER | sp.KERNEL_PORTABLE)
 
 
+@pytest.mark.parametrize("out_raster", [False, True])
+@pytest.mark.parametrize("name", ["medium", "r128", "r64", "r128d64", "wave", "r64odd"])
+def test_attn_fwd_raster_input(name, out_raster):
+    """With IN_RASTER the kernel reads Q, K, V in raster order [B, N, H, d]
+    (each block one 5-D TMA box) and gives bit for bit what it gives on the
+    block-ordered tensors; the portable kernels refuse the flag."""
+    wl, data, shape = _setup(name)
+    ch = OracleChain(wl, data)
+    rp, ci = i32(ch.sel.row_ptr), i32(ch.sel.col_idx)
+    qb, kb, vb = dev(ch.qb, wl), dev(ch.kb, wl), dev(ch.vb, wl)
+    qr, kr, vr = (dev(data[x], wl) for x in ("q", "k", "v"))
+    extra = sp.OUT_RASTER if out_raster else 0
+    st = status_word()
+    o1, l1 = sp.attn_fwd(shape, qb, kb, vb, rp, ci, flags=extra, status=st)
+    o2, l2 = sp.attn_fwd(shape, qr, kr, vr, rp, ci, flags=extra | sp.IN_RASTER, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    with pytest.raises(sp.SparspError):
+        sp.attn_fwd(shape, qr, kr, vr, rp, ci, flags=sp.IN_RASTER | sp.KERNEL_PORTABLE)
+
+
 @pytest.mark.parametrize("portable", [False, True])
 @pytest.mark.parametrize("name", ["r128", "tiny", "r64", "medium", "r64odd", "r128d64"])
 def test_attn_fwd_empty_and_bad_rows(name, portable):
