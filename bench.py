@@ -263,7 +263,8 @@ class Run:
         self.pipe = sp.Pipeline(self.shape, wl.estimator, wl.top_p, wl.k_floor, wl.P, backward=wl.backward,
                                 flags=flags, fused_estimation=not args.unfused, placement=args.placement,
                                 migrations=wl.P if args.augment else None, augment=args.augment,
-                                overlap_demand=overlap)
+                                overlap_demand=overlap,
+                                raster_inputs=getattr(args, "raster_inputs", False) and not wl.backward)
         tdt = self.shape.torch_dtype
         self.host_in = {x: torch.from_numpy(self.data[x]).to(tdt).pin_memory() for x in ("q", "k", "v")}
         self.dev_in = {x: self.host_in[x].cuda() for x in self.host_in}
@@ -341,12 +342,14 @@ class Run:
         rp, ci = pipe.csr
         flags = pipe.flags | (sp.OUT_RASTER if pipe.raster_out else 0)
         o = pipe.o if pipe.raster_out else pipe.ob
+        q, k, v = pipe.qb, pipe.kb, pipe.vb
+        if pipe.raster_in:
+            q, k, v, flags = self.dev_in["q"], self.dev_in["k"], self.dev_in["v"], flags | sp.IN_RASTER
         b0 = torch.cuda.Event(enable_timing=True)
         b1 = torch.cuda.Event(enable_timing=True)
         b0.record(self.stream)
         for _ in range(calls):
-            sp.attn_fwd(self.shape, pipe.qb, pipe.kb, pipe.vb, rp, ci, 0.0, o, pipe.lse, pipe.ws_attn, flags,
-                        None, pipe.status)
+            sp.attn_fwd(self.shape, q, k, v, rp, ci, 0.0, o, pipe.lse, pipe.ws_attn, flags, None, pipe.status)
         b1.record(self.stream)
         torch.cuda.synchronize()
         return b0.elapsed_time(b1) / calls
@@ -473,6 +476,8 @@ def main():
     ap.add_argument("--serial-demand", action="store_true",
                     help="time the step with the KV demand stage before attention on one stream (default: the "
                          "gather beside attention on a side stream)")
+    ap.add_argument("--raster-inputs", action="store_true",
+                    help="forward-only steps: no reorder pass; pooling, the gather and attention read raster Q, K, V")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="skip the other seeded workloads")

@@ -101,6 +101,7 @@ _SIG = {
     "sparsp_kv_demand": (_I32, [_P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int64, _P, _P,
                                 _P]),
     "sparsp_kv_gather": (_I32, [_P, _I32, _P, _P, _P, _P, _P, _P, ctypes.c_int64, _P, _P]),
+    "sparsp_kv_gather_raster": (_I32, [_P, _I32, _P, _P, _P, _P, _P, _P, ctypes.c_int64, _P, _P]),
     "sparsp_placement_workspace_size": (ctypes.c_size_t, [_P]),
     "sparsp_placement": (_I32, [_P, _I32, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
     "sparsp_balance_heads": (_I32, [_P, _I32, _I32, _P, _P, _P, _P, _P]),
@@ -210,6 +211,15 @@ def reorder_pool(shape: Shape, x: torch.Tensor, out: torch.Tensor | None = None,
     return out, means
 
 
+def pool_means(shape: Shape, x: torch.Tensor, means: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The fp32 tile means [B, H, nb, d] of raster x alone (no reordered copy)."""
+    if means is None:
+        means = torch.empty((shape.B, shape.H, shape.nb, shape.d), dtype=torch.float32, device=x.device)
+    _check("sparsp_reorder_pool", lib().sparsp_reorder_pool(_sref(shape), _ptr(x), None, _ptr(means),
+                                                            _stream(stream)))
+    return means
+
+
 def block_scores_pooled(shape: Shape, qmeans, kmeans, estimator=EST_MEAN, wq=None, wk=None, rank=16, out=None,
                         ws=None, stream=None) -> torch.Tensor:
     if out is None:
@@ -283,14 +293,15 @@ def kv_demand(shape: Shape, P: int, row_ptr, col_idx, k=None, v=None, gather_cap
 
 
 def kv_gather(shape: Shape, P: int, dem: DemandOut, k, v, gather_cap: int | None = None, status=None,
-              stream=None) -> DemandOut:
+              stream=None, raster: bool = False) -> DemandOut:
     """The gather of kv_demand alone, into dem.kg / dem.vg, from the lists
     (dem.dem_ptr, dem.dem_idx) of an earlier kv_demand call; it can run on a
-    second stream beside attention."""
+    second stream beside attention. raster: k and v in raster order [B, N, H, d]."""
     if dem.kg is None or dem.vg is None:
         raise ValueError("kv_gather needs DemandOut with kg and vg buffers")
     cap = dem.kg.shape[0] if gather_cap is None else gather_cap
-    _check("sparsp_kv_gather", lib().sparsp_kv_gather(
+    name = "sparsp_kv_gather_raster" if raster else "sparsp_kv_gather"
+    _check(name, getattr(lib(), name)(
         _sref(shape), int(P), _ptr(dem.dem_ptr), _ptr(dem.dem_idx), _ptr(k), _ptr(v), _ptr(dem.kg), _ptr(dem.vg),
         int(cap), _ptr(status), _stream(stream)))
     return dem

@@ -139,12 +139,12 @@ sparsp_status_t sparsp_reorder_pool(const sparsp_shape_t* shape, const void* in,
   sparsp_status_t r = check_shape(shape, &s);
   if (r != SPARSP_OK) return r;
   CHECK_PTR(in);
-  CHECK_PTR(out);
+  CHECK_OPT_PTR(out);
   CHECK_PTR(means);
   const size_t bytes = (size_t)s.B * s.H * s.N * s.d * s.elem;
   const uint8_t* a = (const uint8_t*)in;
   const uint8_t* b = (const uint8_t*)out;
-  if (a < b + bytes && b < a + bytes) return SPARSP_ERR_INVALID_ARG;   // overlap
+  if (b != nullptr && a < b + bytes && b < a + bytes) return SPARSP_ERR_INVALID_ARG;   // overlap
   return launch_reorder(s, in, out, false, (cudaStream_t)stream, means);
 }
 
@@ -299,6 +299,26 @@ sparsp_status_t sparsp_kv_gather(const sparsp_shape_t* shape, int32_t P, const i
   if (gather_cap_blocks < 0) return SPARSP_ERR_INVALID_ARG;
   return launch_kv_gather(s, P, dem_ptr, dem_idx, k, v, kg, vg, gather_cap_blocks, d_status,
                           (cudaStream_t)stream);
+}
+
+sparsp_status_t sparsp_kv_gather_raster(const sparsp_shape_t* shape, int32_t P, const int32_t* dem_ptr,
+                                        const int32_t* dem_idx, const void* k, const void* v, void* kg, void* vg,
+                                        int64_t gather_cap_blocks, int32_t* d_status, sparsp_stream_t stream) {
+  Dims s;
+  sparsp_status_t r = check_shape(shape, &s);
+  if (r != SPARSP_OK) return r;
+  if (P < 1 || P > s.nb) return SPARSP_ERR_SHAPE;
+  if ((int64_t)s.B * s.H * P * s.nb > INT32_MAX) return SPARSP_ERR_UNSUPPORTED;   // int32 list offsets
+  CHECK_PTR(dem_ptr);
+  CHECK_PTR(dem_idx);
+  CHECK_PTR(k);
+  CHECK_PTR(v);
+  CHECK_PTR(kg);
+  CHECK_PTR(vg);
+  CHECK_OPT_PTR(d_status);
+  if (gather_cap_blocks < 0) return SPARSP_ERR_INVALID_ARG;
+  return launch_kv_gather_raster(s, P, dem_ptr, dem_idx, k, v, kg, vg, gather_cap_blocks, d_status,
+                                 (cudaStream_t)stream);
 }
 
 size_t sparsp_placement_workspace_size(const sparsp_shape_t* shape) {

@@ -130,6 +130,10 @@ sparsp_status_t launch_kv_demand(const Dims& s, int P, const int32_t* row_ptr,
 sparsp_status_t launch_kv_gather(const Dims& s, int P, const int32_t* dem_ptr, const int32_t* dem_idx,
                                  const void* k, const void* v, void* kg, void* vg, int64_t cap, int32_t* d_status,
                                  cudaStream_t st);
+// the same gather from raster k, v [B, N, H, d]
+sparsp_status_t launch_kv_gather_raster(const Dims& s, int P, const int32_t* dem_ptr, const int32_t* dem_idx,
+                                        const void* k, const void* v, void* kg, void* vg, int64_t cap,
+                                        int32_t* d_status, cudaStream_t st);
 
 size_t placement_ws(const Dims& s);
 sparsp_status_t launch_placement(const Dims& s, const int32_t* row_ptr, const int32_t* col_idx, int P,

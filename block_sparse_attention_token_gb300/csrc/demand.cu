@@ -216,6 +216,62 @@ gather_kernel(const int32_t* __restrict__ dem_ptr, const int32_t* __restrict__ d
   }
 }
 
+// The gather from raster K and V ([B, N, H, d]): the same slots and lists,
+// each tile's token rows read at their raster addresses. Tile sides are powers
+// of two (64- or 128-token tiles), so a token's offset inside its tile comes
+// from shifts: token o = (it, iy, ix) sits (it*Y + iy)*X + ix raster tokens
+// after the tile's first. Each thread copies 4 consecutive vectors (64 bytes)
+// of one row per step, so that four threads cover a 256-byte row.
+__global__ void __launch_bounds__(kGatherThreads, 8)
+gather_raster_kernel(const int32_t* __restrict__ dem_ptr, const int32_t* __restrict__ dem_idx, int nparts,
+                     int P, int64_t N, int H, int Y, int X, int ta, int tb, int tc, int nY, int nX, int Bt, int nb,
+                     int vec_per_row, int l_tbc, int l_tc, const uint4* __restrict__ k,
+                     const uint4* __restrict__ v, uint4* __restrict__ kg, uint4* __restrict__ vg, int64_t cap,
+                     int32_t* d_status) {
+  int64_t total = dem_ptr[nparts];
+  const int64_t slot = blockIdx.x;
+  if (total < 0 || total > (int64_t)nparts * nb) {
+    if (slot == 0 && threadIdx.x == 0) report(d_status, SPARSP_ERR_DATA);
+    total = 0;
+  }
+  if (slot == 0 && total > cap && threadIdx.x == 0) report(d_status, SPARSP_ERR_CAPACITY);
+  if (slot >= total || slot >= cap) return;
+  int lo = 0, hi = nparts - 1;   // last part with dem_ptr[part] <= slot
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (dem_ptr[mid] <= slot) lo = mid; else hi = mid - 1;
+  }
+  const int bh = lo / P;
+  const int j = dem_idx[slot];
+  if (j < 0 || j >= nb) {
+    if (threadIdx.x == 0) report(d_status, SPARSP_ERR_DATA);
+    return;
+  }
+  const int bx = j % nX, by = (j / nX) % nY, bt = j / (nX * nY);
+  const int64_t n0 = ((int64_t)bt * ta * Y + (int64_t)by * tb) * X + (int64_t)bx * tc;   // the tile's first token
+  const int64_t rowbase = ((int64_t)(bh / H) * N + n0) * H + bh % H;
+  const int64_t yx = (int64_t)Y * X;
+  const int64_t nvec = (int64_t)Bt * vec_per_row;
+  uint4* kd = kg + slot * nvec;
+  uint4* vd = vg + slot * nvec;
+  for (int64_t e = 4 * (int64_t)threadIdx.x; e < nvec; e += 4 * kGatherThreads) {
+    const int o = (int)(e / vec_per_row), col = (int)(e % vec_per_row);
+    const int64_t off = (int64_t)(o >> l_tbc) * yx + (int64_t)((o >> l_tc) & (tb - 1)) * X + (o & (tc - 1));
+    const int64_t src = (rowbase + off * H) * vec_per_row + col;
+    uint4 a[4], b[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      a[u] = k[src + u];
+      b[u] = v[src + u];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      __stcs(kd + e + u, a[u]);
+      __stcs(vd + e + u, b[u]);
+    }
+  }
+}
+
 }  // namespace
 
 sparsp_status_t launch_kv_demand(const Dims& s, int P, const int32_t* row_ptr,
@@ -251,6 +307,23 @@ sparsp_status_t launch_kv_gather(const Dims& s, int P, const int32_t* dem_ptr, c
   gather_kernel<<<(unsigned)grid, kGatherThreads, 0, st>>>(dem_ptr, dem_idx, nparts, P, s.N, s.Bt, s.nb, vec_per_row,
                                                  (const uint4*)k, (const uint4*)v, (uint4*)kg, (uint4*)vg, cap,
                                                  d_status);
+  SPARSP_LAUNCH_CHECK();
+  return SPARSP_OK;
+}
+
+sparsp_status_t launch_kv_gather_raster(const Dims& s, int P, const int32_t* dem_ptr, const int32_t* dem_idx,
+                                        const void* k, const void* v, void* kg, void* vg, int64_t cap,
+                                        int32_t* d_status, cudaStream_t st) {
+  const int nparts = s.B * s.H * P;
+  const int64_t upper = (int64_t)nparts * s.nb;
+  int64_t grid = upper < cap ? upper : cap;
+  if (grid < 1) grid = 1;
+  const int vec_per_row = s.d * s.elem / 16;
+  // tile sides are powers of two (64 or 128 tokens)
+  const int l_tc = __builtin_ctz((unsigned)s.tc), l_tbc = __builtin_ctz((unsigned)(s.tb * s.tc));
+  gather_raster_kernel<<<(unsigned)grid, kGatherThreads, 0, st>>>(
+      dem_ptr, dem_idx, nparts, P, s.N, s.H, s.Y, s.X, s.ta, s.tb, s.tc, s.nY, s.nX, s.Bt, s.nb, vec_per_row, l_tbc,
+      l_tc, (const uint4*)k, (const uint4*)v, (uint4*)kg, (uint4*)vg, cap, d_status);
   SPARSP_LAUNCH_CHECK();
   return SPARSP_OK;
 }

@@ -56,9 +56,10 @@ reorder_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, int H, int
       buf[u] = __ldcs(in + src);
     }
   }
+  if (out != nullptr)   // null: the tile means alone (a pooling read of raster input)
 #pragma unroll
-  for (int u = 0; u < kPer; ++u)
-    if (dst_off[u] >= 0) __stcs(out + dst_off[u], buf[u]);
+    for (int u = 0; u < kPer; ++u)
+      if (dst_off[u] >= 0) __stcs(out + dst_off[u], buf[u]);
   if (POOL) {
     __shared__ float part[kThreads][9];
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};

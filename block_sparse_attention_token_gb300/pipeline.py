@@ -24,7 +24,7 @@ from . import (EST_LOWRANK, EST_MEAN, PROF_SLOTS, Shape, attn_bwd, attn_fwd, att
                augment_workspace_size, balance_heads, Balance, predictor_fit,
                block_scores, block_scores_pooled, block_scores_workspace_size, kv_demand, kv_gather, lib, placement,
                placement_workspace_size, reorder, reorder_pool, select, select_workspace_size, DemandOut,
-               OUT_RASTER)
+               OUT_RASTER, IN_RASTER, pool_means)
 
 
 class Pipeline:
@@ -54,7 +54,8 @@ class Pipeline:
     def __init__(self, shape: Shape, estimator: str, top_p: float, k_floor: int, P: int, rank: int = 16,
                  gather: bool = True, flags: int = 0, backward: bool = False, device="cuda",
                  fused_estimation: bool = True, placement: bool = False, migrations: int | None = None,
-                 augment: bool = False, predictor_lr: float | None = None, overlap_demand: bool = True):
+                 augment: bool = False, predictor_lr: float | None = None, overlap_demand: bool = True,
+                 raster_inputs: bool = False):
         """overlap_demand: after the KV demand lists (bitmap, offsets, indices),
         run the demand gather on a low-priority side stream while attention runs
         on a high-priority one; the two only read the same K/V, and the
@@ -64,7 +65,12 @@ class Pipeline:
         extra blocks (on the balanced ranks, or the contiguous head split);
         attention then runs on the augmented CSR. predictor_lr: with the
         low-rank estimator, after the scores are taken, one fitting step of the
-        predictor weights (updated in place) against the real block scores."""
+        predictor weights (updated in place) against the real block scores.
+        raster_inputs (forward-only, tcgen05 shapes, fused estimation): no
+        reorder pass; the tile means come from a pooling read of raster Q and
+        K, and the demand gather and attention read the raster tensors
+        themselves (each block one 5-D TMA box), so forward()'s inputs stay
+        in use until attention and the gather have finished."""
         self.shape, self.top_p, self.k_floor, self.P, self.rank, self.flags = shape, top_p, k_floor, P, rank, flags
         self.est = EST_LOWRANK if estimator == "lowrank" else EST_MEAN
         self.fused = fused_estimation
@@ -72,7 +78,10 @@ class Pipeline:
         dt = s.torch_dtype
         dev = torch.device(device)
         blocked = (s.B, s.H, s.N, s.d)
-        self.qb, self.kb, self.vb = (torch.empty(blocked, dtype=dt, device=dev) for _ in range(3))
+        self.raster_in = raster_inputs
+        self.qb = self.kb = self.vb = None
+        if not raster_inputs:
+            self.qb, self.kb, self.vb = (torch.empty(blocked, dtype=dt, device=dev) for _ in range(3))
         self.o = torch.empty((s.B, s.N, s.H, s.d), dtype=dt, device=dev)
         self.lse = torch.empty((s.B, s.H, s.N), dtype=torch.float32, device=dev)
         self.scores = torch.empty((s.B, s.H, s.nb, s.nb), dtype=torch.float32, device=dev)
@@ -112,6 +121,11 @@ class Pipeline:
         fwd_raster = (s.torch_dtype == torch.bfloat16 and not (flags & 2) and s.Bt in (64, 128)
                       and s.d in (64, 128) and not (s.Bt == 64 and s.d == 128 and s.nb > 1024))
         self.raster_out = fwd_raster
+        if raster_inputs and (backward or not fwd_raster or not fused_estimation):
+            raise ValueError("raster inputs need a forward-only step on the tcgen05 kernel with fused estimation")
+        # the stage after which forward()'s raster inputs are no longer read
+        self.inputs_read_mark = ("overlap" if overlap_demand and gather else "attn_fwd") if raster_inputs \
+            else "reorder"
         self._o_fwd = None   # the buffer forward() last wrote O to (read by backward() when raster)
         # block-order O (and gradients) only where attention does not write raster rows
         self.ob = None if self.raster_out else torch.empty(blocked, dtype=dt, device=dev)
@@ -161,7 +175,15 @@ class Pipeline:
         s = self.shape
         mark = mark or (lambda name, stream=None: None)
         before = before or (lambda name: None)
-        if self.fused:   # the tile means come out of the reorder pass itself
+        if self.raster_in:   # the tile means alone: attention and the gather read the raster tensors
+            before("q")
+            pool_means(s, q, self.qmeans)
+            before("k")
+            pool_means(s, k, self.kmeans)
+            mark("reorder")
+            block_scores_pooled(s, self.qmeans, self.kmeans, self.est, wq, wk, self.rank, out=self.scores,
+                                ws=self.ws_pooled)
+        elif self.fused:   # the tile means come out of the reorder pass itself
             before("q")
             reorder_pool(s, q, self.qb, self.qmeans)
             before("k")
@@ -202,6 +224,11 @@ class Pipeline:
         o = self.o if out is None else out
         # attention output: raster O directly, or block order and an inverse reorder
         o_attn, aflags = (o, self.flags | OUT_RASTER) if self.raster_out else (self.ob, self.flags)
+        if self.raster_in:
+            before("v")
+            aq, ak, av, aflags = q, k, v, aflags | IN_RASTER
+        else:
+            aq, ak, av = self.qb, self.kb, self.vb
         if self.overlap_demand and self.demand.kg is not None:
             # the lists (bitmap, offsets, indices) first, on this stream: they need a
             # little shared memory, which attention leaves none of; then the gather
@@ -217,20 +244,26 @@ class Pipeline:
             lo.wait_event(self._selected)
             with torch.cuda.stream(hi):   # enqueued first: the persistent CTAs take their SMs first
                 mark("attn_fwd:begin", hi)
-                attn_fwd(s, self.qb, self.kb, self.vb, rp, ci, 0.0, o_attn, self.lse, self.ws_attn,
+                attn_fwd(s, aq, ak, av, rp, ci, 0.0, o_attn, self.lse, self.ws_attn,
                          aflags, self.prof if prof else None, self.status, stream=hi)
                 mark("attn_fwd", hi)
             with torch.cuda.stream(lo):
                 mark("kv_gather:begin", lo)
-                kv_gather(s, self.P, self.demand, self.kb, self.vb, status=self.status, stream=lo)
+                kv_gather(s, self.P, self.demand, ak, av, status=self.status, stream=lo, raster=self.raster_in)
                 mark("kv_gather", lo)
             main.wait_stream(hi)
             main.wait_stream(lo)
             mark("overlap")
         else:
-            kv_demand(s, self.P, rp, ci, self.kb, self.vb, out=self.demand, status=self.status, owner=self.owner)
+            if self.raster_in and self.demand.kg is not None:
+                lists = dataclasses.replace(self.demand, kg=None, vg=None)
+                kv_demand(s, self.P, rp, ci, out=lists, status=self.status, owner=self.owner)
+                kv_gather(s, self.P, self.demand, ak, av, status=self.status, raster=True)
+            else:
+                kv_demand(s, self.P, rp, ci, self.kb, self.vb, out=self.demand, status=self.status,
+                          owner=self.owner)
             mark("kv_demand")
-            attn_fwd(s, self.qb, self.kb, self.vb, rp, ci, 0.0, o_attn, self.lse, self.ws_attn,
+            attn_fwd(s, aq, ak, av, rp, ci, 0.0, o_attn, self.lse, self.ws_attn,
                      aflags, self.prof if prof else None, self.status)
             mark("attn_fwd")
         if not self.raster_out:

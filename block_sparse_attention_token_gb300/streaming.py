@@ -60,7 +60,7 @@ class HostPipeline:
         cur.wait_event(self.out_free[b])                   # step n-2's O has left the device
 
         def mark(name, stream=None):
-            if name == "reorder":                          # raster inputs are no longer read
+            if name == self.pipe.inputs_read_mark:         # raster inputs are no longer read
                 self.in_free[b].record(cur)
 
         self.pipe.forward(*self.inp[b], wq=wq, wk=wk, mark=mark, out=self.out[b], before=self._waiter(b, cur))

@@ -181,7 +181,9 @@ SPARSP_API sparsp_status_t sparsp_block_scores(const sparsp_shape_t* shape, int3
  * passes that already touch Q and K). sparsp_reorder_pool is the forward
  * sparsp_reorder of one tensor that also writes the fp32 mean of every tile
  * to `means` [B, H, nb, d] from the same read (a fixed summation order), so
- * the block scores need no second pass over Q and K.
+ * the block scores need no second pass over Q and K. out may be NULL: the
+ * means alone (for attention that reads raster input itself,
+ * SPARSP_IN_RASTER).
  * sparsp_block_scores_pooled: the scores of sparsp_block_scores from those
  * means (estimator MEAN: q_mean . k_mean; LOWRANK: (q_mean Wq)(k_mean Wk)^T);
  * ws is used by LOWRANK only (sparsp_block_scores_pooled_workspace_size(),
@@ -284,6 +286,13 @@ SPARSP_API sparsp_status_t sparsp_kv_demand(const sparsp_shape_t* shape, int32_t
 SPARSP_API sparsp_status_t sparsp_kv_gather(const sparsp_shape_t* shape, int32_t P, const int32_t* dem_ptr,
                                  const int32_t* dem_idx, const void* k, const void* v, void* kg, void* vg,
                                  int64_t gather_cap_blocks, int32_t* d_status, sparsp_stream_t stream);
+/* The same gather with k and v in raster order [B, N, H, d] (the layout
+ * sparsp_reorder takes): every tile's token rows are read at their raster
+ * addresses; the results equal those of sparsp_kv_gather on the reordered
+ * tensors. */
+SPARSP_API sparsp_status_t sparsp_kv_gather_raster(const sparsp_shape_t* shape, int32_t P, const int32_t* dem_ptr,
+                                        const int32_t* dem_idx, const void* k, const void* v, void* kg, void* vg,
+                                        int64_t gather_cap_blocks, int32_t* d_status, sparsp_stream_t stream);
 
 /*
  * Step 4b - Dependency-Aware Placement ("SparSP: Exploiting Communication

@@ -673,6 +673,59 @@ def test_attn_fwd_raster_output(name):
         sp.attn_fwd(shape, q, k, v, rp, ci, flags=sp.OUT_RASTER | sp.KERNEL_PORTABLE)
 
 
+@pytest.mark.parametrize("overlap", [True, False])
+@pytest.mark.parametrize("name", ["medium", "r128", "r64odd"])
+def test_pipeline_raster_inputs(name, overlap):
+    """A forward-only step that reads the raster inputs itself (no reorder
+    pass) gives the block-ordered step's O, LSE, CSR and gathered tiles, bit
+    for bit, also through HostPipeline from pinned host memory."""
+    wl, data, shape = _setup(name)
+    args = [dev(data[x], wl) for x in ("q", "k", "v")]
+    plain = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P, overlap_demand=overlap)
+    direct = sp.Pipeline(shape, wl.estimator, wl.top_p, wl.k_floor, wl.P, overlap_demand=overlap,
+                         raster_inputs=True)
+    o1, l1 = [t.clone() for t in plain.forward(*args)]
+    o2, l2 = [t.clone() for t in direct.forward(*args)]
+    torch.cuda.synchronize()
+    assert plain.status.item() == 0 and direct.status.item() == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(plain.row_ptr, direct.row_ptr)
+    total = int(plain.demand.dem_ptr[-1].item())
+    assert torch.equal(plain.demand.kg[:total], direct.demand.kg[:total])
+    assert torch.equal(plain.demand.vg[:total], direct.demand.vg[:total])
+    hp = sp.HostPipeline(direct)
+    hin = [t.cpu().pin_memory() for t in args]
+    ho = torch.empty(o1.shape, dtype=o1.dtype).pin_memory()
+    for _ in range(3):
+        hp.step(*hin, ho)
+    hp.synchronize()
+    torch.cuda.synchronize()
+    assert torch.equal(ho.cuda(), o1)
+
+
+@pytest.mark.parametrize("name", ["tiny", "medium", "r128", "r64odd"])
+def test_raster_pooling_and_gather(name):
+    """Tile means from a pooling read of raster input (no reordered copy)
+    equal those of the fused reorder, and the demand gather from raster K, V
+    equals the gather from the block-ordered tensors, bit for bit."""
+    wl, data, shape = _setup(name)
+    ch = OracleChain(wl, data)
+    x = dev(data["q"], wl)
+    _, m1 = sp.reorder_pool(shape, x)
+    m2 = sp.pool_means(shape, x)
+    rp, ci = i32(ch.sel.row_ptr), i32(ch.sel.col_idx)
+    st = status_word()
+    blocked = sp.kv_demand(shape, wl.P, rp, ci, dev(ch.kb, wl), dev(ch.vb, wl), status=st)
+    raster = dataclasses.replace(blocked, kg=torch.full_like(blocked.kg, 3), vg=torch.full_like(blocked.vg, 3))
+    sp.kv_gather(shape, wl.P, raster, dev(data["k"], wl), dev(data["v"], wl), status=st, raster=True)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(m1, m2)
+    total = int(blocked.dem_ptr[-1].item())
+    assert total > 0
+    assert torch.equal(blocked.kg[:total], raster.kg[:total]) and torch.equal(blocked.vg[:total], raster.vg[:total])
+
+
 @pytest.mark.parametrize("out_raster", [False, True])
 @pytest.mark.parametrize("name", ["medium", "r128", "r64", "r128d64", "wave", "r64odd"])
 def test_attn_fwd_raster_input(name, out_raster):
