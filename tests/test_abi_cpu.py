@@ -131,6 +131,14 @@ def test_call_validation_codes(lib):
     assert lib.sparsp_kv_gather(S, 2, None, FAKE, FAKE, FAKE, FAKE, FAKE, 4, None, None) == sp.INVALID_ARG
     assert lib.sparsp_kv_gather(S, 2, *g, -1, None, None) == sp.INVALID_ARG
     assert lib.sparsp_kv_gather(S, 2, FAKE, FAKE + 4, FAKE, FAKE, FAKE, FAKE, 4, None, None) == sp.ALIGN
+    # the same checks for the gather from raster K and V
+    assert lib.sparsp_kv_gather_raster(S, 0, *g, 4, None, None) == sp.SHAPE
+    assert lib.sparsp_kv_gather_raster(S, 2, FAKE, FAKE, FAKE, FAKE, FAKE, None, 4, None, None) == sp.INVALID_ARG
+    assert lib.sparsp_kv_gather_raster(S, 2, *g, -1, None, None) == sp.INVALID_ARG
+    assert lib.sparsp_kv_gather_raster(S, 2, FAKE, FAKE, FAKE + 4, FAKE, FAKE, FAKE, 4, None, None) == sp.ALIGN
+    # pooling: the reordered copy is optional, the means are not; a copy over its input is refused
+    assert lib.sparsp_reorder_pool(S, FAKE, FAKE, None, None) == sp.INVALID_ARG
+    assert lib.sparsp_reorder_pool(S, FAKE, FAKE, FAKE, None) == sp.INVALID_ARG
     # placement: P out of range, missing owner, small workspace
     need = lib.sparsp_placement_workspace_size(S)
     assert need == s.B * s.nb * s.nb * 4
@@ -199,6 +207,11 @@ def test_call_validation_codes(lib):
                                None, None, None) == sp.UNSUPPORTED
     assert lib.sparsp_attn_bwd(ctypes.byref(s32), *((FAKE,) * 8), f(0.0), FAKE, FAKE, FAKE, FAKE, 1 << 30, 0,
                                None, None, None) == sp.UNSUPPORTED
+    # raster inputs: the tcgen05 forward only (no GPU here, so not even that); never the backward
+    assert lib.sparsp_attn_fwd(S, *p7, f(0.0), FAKE, FAKE, FAKE, 1 << 30, sp.IN_RASTER | sp.KERNEL_PORTABLE,
+                               None, None, None) == sp.UNSUPPORTED
+    assert lib.sparsp_attn_bwd(S, *((FAKE,) * 8), f(0.0), FAKE, FAKE, FAKE, FAKE, 1 << 30, sp.IN_RASTER, None,
+                               None, None) == sp.UNSUPPORTED
     assert lib.sparsp_attn_bwd(S, *((FAKE,) * 8), f(0.0), FAKE, FAKE, FAKE, FAKE, 8, 0, None, None,
                                None) == sp.WORKSPACE
     assert lib.sparsp_lpt_schedule(S, FAKE, sp.SCHED_FLAT, FAKE, FAKE, 4, None) == sp.WORKSPACE
