@@ -650,10 +650,14 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
               const float l2[4] = {L.x, L.y, L.z, L.w}, dd[4] = {Dv.x, Dv.y, Dv.z, Dv.w};
               float pr[4], ds[4];
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
+              for (int u = 0; u < 4; u += 2) {   // column pairs: each lane rounds as the scalar form
                 const int x = 4 * x4 + u;
-                pr[u] = ex2f(fmaf(__uint_as_float(sv[x]), sl2, -l2[u]));
-                ds[u] = pr[u] * (__uint_as_float(dv[x]) - dd[u]);
+                float e0, e1, t0, t1;
+                fma_x2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1]), sl2, -l2[u], -l2[u + 1], e0, e1);
+                pr[u] = ex2f(e0);
+                pr[u + 1] = ex2f(e1);
+                sub_x2(__uint_as_float(dv[x]), __uint_as_float(dv[x + 1]), dd[u], dd[u + 1], t0, t1);
+                mul_x2(pr[u], pr[u + 1], t0, t1, ds[u], ds[u + 1]);
               }
               xk[2 * x4] = pack2(pr[0], pr[1]);
               xk[2 * x4 + 1] = pack2(pr[2], pr[3]);
@@ -683,10 +687,19 @@ attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap ta1, const __grid_constan
               }
               float v[4];
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
+              for (int u = 0; u < 4; u += 2) {   // column pairs: each lane rounds as the scalar form
                 const int x = 4 * x4 + u;
-                const float pr = ex2f(fmaf(__uint_as_float(sv[x]), sl2, -l2[u]));
-                v[u] = kHasDP ? pr * (__uint_as_float(dv[x]) - dd[u]) : pr;
+                float e0, e1;
+                fma_x2(__uint_as_float(sv[x]), __uint_as_float(sv[x + 1]), sl2, -l2[u], -l2[u + 1], e0, e1);
+                const float p0 = ex2f(e0), p1 = ex2f(e1);
+                if (kHasDP) {
+                  float t0, t1;
+                  sub_x2(__uint_as_float(dv[x]), __uint_as_float(dv[x + 1]), dd[u], dd[u + 1], t0, t1);
+                  mul_x2(p0, p1, t0, t1, v[u], v[u + 1]);
+                } else {
+                  v[u] = p0;
+                  v[u + 1] = p1;
+                }
               }
               xk[2 * x4] = pack2(v[0], v[1]);
               xk[2 * x4 + 1] = pack2(v[2], v[3]);

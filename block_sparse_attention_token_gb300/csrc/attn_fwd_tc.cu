@@ -164,19 +164,6 @@ __device__ __forceinline__ float tmem_ld32_max(uint32_t taddr, uint32_t* r) {
   return m;
 }
 
-// Two fp32 lanes at once (sm_100 family): d = a * b + c and d = a + b, each
-// lane rounded exactly as the scalar instruction.
-__device__ __forceinline__ void fma_x2(float a0, float a1, float b, float c, float& d0, float& d1) {
-  asm("{\n.reg .b64 ra, rb, rc, rd;\nmov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %4};\nmov.b64 rc, {%5, %5};\n"
-      "fma.rn.f32x2 rd, ra, rb, rc;\nmov.b64 {%0, %1}, rd;\n}\n"
-      : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b), "f"(c));
-}
-__device__ __forceinline__ void add_x2(float& d0, float& d1, float a0, float a1) {
-  asm("{\n.reg .b64 ra, rd;\nmov.b64 rd, {%0, %1};\nmov.b64 ra, {%2, %3};\n"
-      "add.rn.f32x2 rd, rd, ra;\nmov.b64 {%0, %1}, rd;\n}\n"
-      : "+f"(d0), "+f"(d1) : "f"(a0), "f"(a1));
-}
-
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

@@ -139,6 +139,36 @@ __device__ __forceinline__ void regs_decrease() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(R));
 }
 
+// ---------------------------------------------------------------- fp32 pairs
+// Two fp32 lanes per instruction (sm_100 family), each lane rounded exactly as
+// the scalar instruction: d = a * b + c (b, c shared or per lane), d = a + b,
+// d = a - b, d = a * b.
+__device__ __forceinline__ void fma_x2(float a0, float a1, float b, float c, float& d0, float& d1) {
+  asm("{\n.reg .b64 ra, rb, rc, rd;\nmov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %4};\nmov.b64 rc, {%5, %5};\n"
+      "fma.rn.f32x2 rd, ra, rb, rc;\nmov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+__device__ __forceinline__ void fma_x2(float a0, float a1, float b, float c0, float c1, float& d0, float& d1) {
+  asm("{\n.reg .b64 ra, rb, rc, rd;\nmov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %4};\nmov.b64 rc, {%5, %6};\n"
+      "fma.rn.f32x2 rd, ra, rb, rc;\nmov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add_x2(float& d0, float& d1, float a0, float a1) {
+  asm("{\n.reg .b64 ra, rd;\nmov.b64 rd, {%0, %1};\nmov.b64 ra, {%2, %3};\n"
+      "add.rn.f32x2 rd, rd, ra;\nmov.b64 {%0, %1}, rd;\n}\n"
+      : "+f"(d0), "+f"(d1) : "f"(a0), "f"(a1));
+}
+__device__ __forceinline__ void sub_x2(float a0, float a1, float b0, float b1, float& d0, float& d1) {
+  asm("{\n.reg .b64 ra, rb, rd;\nmov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %5};\n"
+      "sub.rn.f32x2 rd, ra, rb;\nmov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void mul_x2(float a0, float a1, float b0, float b1, float& d0, float& d1) {
+  asm("{\n.reg .b64 ra, rb, rd;\nmov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %5};\n"
+      "mul.rn.f32x2 rd, ra, rb;\nmov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d0), "=f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // True in exactly one active lane of the warp (tcgen05 ops are issued by one
 // thread while the whole warp keeps its control flow and values uniform).
 __device__ __forceinline__ bool elect_one() {
