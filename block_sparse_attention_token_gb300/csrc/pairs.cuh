@@ -30,8 +30,6 @@ struct UnionWalk {
   }
 };
 
-__device__ __forceinline__ bool bit_of(const uint32_t* m, int j) { return (m[j >> 5] >> (j & 31)) & 1u; }
-
 // Validates list r of a CSR-like structure (length <= nb, indices in [0, nb),
 // no index twice) and writes its bitmap (words zeroed before). Warp-collective;
 // returns false for a bad list, whose bitmap is then cleared.
