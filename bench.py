@@ -73,6 +73,8 @@ def peaks():
 
 
 L2_BYTES = 129e6          # GB300 L2; a stage whose bytes fit was fed from L2, not HBM
+# fp32 FFMA peak, derived (not measured): 152 SMs x 128 fp32 lanes x 2 flop per FMA x 2,070 MHz
+FP32_FFMA_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 EXTRA_WORKLOADS = ("skewed", "training", "medium", "tiny")
 
 # DRAM bytes (read + write) per launch of the tcgen05 forward kernel, from an ncu capture of the
@@ -432,7 +434,9 @@ def workload_summary(sp, name, args, pk) -> dict:
         out["attn_fwd_frac_of_burst"] = out["attn_fwd_tflops"] / peak
         out["attn_fwd_alone_frac_of_burst"] = out["attn_fwd_alone_tflops"] / peak
     else:
-        out["attn_fwd_bound"] = "fp32 FFMA kernel (no tensor-core peak applies)"
+        out["attn_fwd_bound"] = "alu (fp32 FFMA kernel; peak derived: 152 SMs x 128 lanes x 2 x 2,070 MHz)"
+        out["attn_fwd_frac_of_fp32_peak"] = out["attn_fwd_tflops"] / FP32_FFMA_TFLOPS
+        out["attn_fwd_alone_frac_of_fp32_peak"] = out["attn_fwd_alone_tflops"] / FP32_FFMA_TFLOPS
     if wl.backward:
         fb = bwd_flops(run.nnz, wl)
         out["attn_bwd_ms"] = st["attn_bwd"]
@@ -546,13 +550,19 @@ def main():
     value = replicas.whole_job_rate(f_step, ms_step, world) / 1e12
     attn_ms = stage_ms["attn_fwd"]
     achieved = f_fwd / (attn_ms * 1e-3) / 1e12
-    peak = pk["bf16_tflops"]
-    roofline = {"bound": "tensor", "kernel": "attn_fwd", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "peak_kind": f"bf16 burst ({pk['source']}; the kernel runs at full clock "
-                                                      f"inside a sub-second timed region)",
-                "frac_of_sustained": achieved / pk["bf16_tflops_sustained"],
-                "traffic": ATTN_TRAFFIC.get(wl.name) if not args.portable else None,
-                "work": f"4*nnz*Bt^2*d = {f_fwd:.4g} flop per launch (nnz={nnz})"}
+    if wl.dtype == "bf16":
+        peak = pk["bf16_tflops"]
+        roofline = {"bound": "tensor", "kernel": "attn_fwd", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "peak_kind": f"bf16 burst ({pk['source']}; the kernel runs at full "
+                                                          f"clock inside a sub-second timed region)",
+                    "frac_of_sustained": achieved / pk["bf16_tflops_sustained"]}
+    else:
+        peak = FP32_FFMA_TFLOPS
+        roofline = {"bound": "alu", "kernel": "attn_fwd", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak,
+                    "peak_kind": "fp32 FFMA, derived: 152 SMs x 128 lanes x 2 flop x 2,070 MHz"}
+    roofline.update({"traffic": ATTN_TRAFFIC.get(wl.name) if not args.portable else None,
+                     "work": f"4*nnz*Bt^2*d = {f_fwd:.4g} flop per launch (nnz={nnz})"})
     if wl.backward:
         roofline["bwd_achieved"] = bwd_flops(nnz, wl) / (stage_ms["attn_bwd"] * 1e-3) / 1e12
         roofline["bwd_frac"] = roofline["bwd_achieved"] / peak
