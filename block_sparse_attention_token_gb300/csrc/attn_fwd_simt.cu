@@ -2,17 +2,18 @@
 // (no TF32), for workloads whose tolerance is 1e-4.
 //
 // Persistent CTAs of 256 threads pull work items from the longest-first list;
-// an item is 32 query rows of a query block (the Bt/32 items of one block are
-// consecutive, so their CTAs share the K and V tiles in L2). Warp g takes the
-// keys [g Bt/8, (g+1) Bt/8) of every selected key block and lane r query
-// row r, with its own online softmax in base 2 (maximum, sum and a d-float
-// accumulator in registers) eight keys at a time; every shared-memory read is
-// 16 bytes, and the K and V reads are broadcasts (one address per warp). The
-// K and V tiles of a key block are one contiguous bulk copy each, completing
-// on an mbarrier, two blocks in flight where both fit in shared memory. At the
-// end of the item the eight partial states of each row are combined through
-// shared memory (the usual merge of softmax partials: scale each by
-// 2^(m_g - M) and add), each thread finishing d/8 of its row's columns.
+// an item is 16 query rows of a query block (the Bt/16 items of one block are
+// consecutive, so their CTAs share the K and V tiles in L2). Thread (g, r)
+// takes the keys [g Bt/16, (g+1) Bt/16) of every selected key block for
+// query row r, with its own online softmax in base 2 (maximum, sum and a
+// d-float accumulator in registers) up to eight keys at a time; every
+// shared-memory read is 16 bytes, and a warp's K and V reads go to two
+// addresses (its two key groups). The K and V tiles of a key block are one
+// contiguous bulk copy each, completing on an mbarrier, two blocks in flight
+// where both fit in shared memory. At the end of the item the sixteen partial
+// states of each row are combined through shared memory (the usual merge of
+// softmax partials: scale each by 2^(m_g - M) and add), each thread finishing
+// d/16 of its row's columns.
 #include "common.cuh"
 #include "tc_helpers.cuh"
 
@@ -25,10 +26,9 @@ using tc::mbar_arrive_expect_tx;
 using tc::mbar_init;
 using tc::mbar_try_wait;
 
-constexpr int kChunk = 8;
 constexpr int kThreads = 256;
-constexpr int kRows = 32;                        // query rows per item (one per lane)
-constexpr int kGroups = kThreads / kRows;        // key groups (one per warp)
+constexpr int kRows = 16;                        // query rows per item
+constexpr int kGroups = kThreads / kRows;        // key groups, two per warp
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
 
@@ -61,6 +61,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, uint64
 template <int D, int BT>
 struct F32Cfg {
   static constexpr int KS = BT / kGroups;     // keys of a block per thread
+  static constexpr int KC = KS < 8 ? KS : 8;  // keys per online-softmax update
   static constexpr int DP = D + 4;            // padded row stride (floats), 16-byte aligned
   static constexpr int kTile = BT * D;        // floats of one K (or V) tile
   static constexpr int NST = 2 * kTile <= 16384 ? 2 : 1;   // K+V stages in flight
@@ -68,7 +69,7 @@ struct F32Cfg {
   static constexpr int kMerge = kThreads * DP;
   static constexpr int kRegion = kTiles > kMerge ? kTiles : kMerge;   // tiles, then the merge
   static constexpr size_t kSmemBytes = (size_t)(kRegion + kRows * DP + 2 * kThreads) * sizeof(float);
-  static_assert(KS % kChunk == 0 && D % (4 * kGroups) == 0 && BT % kRows == 0, "layout");
+  static_assert(KS % KC == 0 && D % (4 * kGroups) == 0 && BT % kRows == 0 && kRows * 2 == 32, "layout");
   static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
@@ -83,14 +84,14 @@ attn_fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
   using C = F32Cfg<D, BT>;
   constexpr int RG = BT / kRows;         // items per query block
   extern __shared__ __align__(16) float smem[];
-  float* mrg = smem;                     // [8][32][DP] accumulators, over the tiles after the last block
-  float* qs = smem + C::kRegion;         // [32][DP]
-  float* ml = qs + kRows * C::DP;        // [8][32] maxima, then [8][32] sums
+  float* mrg = smem;                     // [16][16][DP] accumulators, over the tiles after the last block
+  float* qs = smem + C::kRegion;         // [16][DP]
+  float* ml = qs + kRows * C::DP;        // [16][16] maxima, then [16][16] sums
   __shared__ __align__(8) uint64_t full[2];
   __shared__ int32_t item_s;
   const uint64_t t_start = globaltimer_ns();
   const int t = threadIdx.x;
-  const int g = t / kRows, r = t % kRows;   // g is the warp
+  const int g = t / kRows, r = t % kRows;   // warp w holds key groups 2w and 2w + 1
   if (t == 0) {
     mbar_init(tc::smem_u32(&full[0]), 1);
     mbar_init(tc::smem_u32(&full[1]), 1);
@@ -149,6 +150,7 @@ attn_fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
       const float* vs = ks + C::kTile;
       const bool ok = wait_phase(tc::smem_u32(&full[b % C::NST]), (b / C::NST) & 1u, kWaitNs);
       if (ok) {
+        constexpr int kChunk = C::KC;
         for (int kb = g * C::KS; kb < (g + 1) * C::KS; kb += kChunk) {
           const float4* kr = reinterpret_cast<const float4*>(ks + kb * D);
           const float4* vr = reinterpret_cast<const float4*>(vs + kb * D);
@@ -217,9 +219,9 @@ attn_fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
       }
     }
     nblk += (uint32_t)len;
-    // combine the eight partial states of each row; thread (g, r) then
-    // finishes columns [g D/8, (g+1) D/8) of row r (no copy is in flight: the
-    // tiles' last reads passed the block barrier above)
+    // combine the sixteen partial states of each row; thread (g, r) then
+    // finishes columns [g D/16, (g+1) D/16) of row r (no copy is in flight:
+    // the tiles' last reads passed the block barrier above)
     {
       float* dst = mrg + (g * kRows + r) * C::DP;
 #pragma unroll
@@ -281,7 +283,7 @@ sparsp_status_t go(const Dims& s, const float* q, const float* k, const float* v
     return SPARSP_ERR_CUDA;
   const int sms = device_sm_count();
   if (sms <= 0) return SPARSP_ERR_CUDA;
-  const int64_t n_items = s.rows();   // query blocks; each is Bt / 32 work items
+  const int64_t n_items = s.rows();   // query blocks; each is Bt / 16 work items
   int per_sm = 1;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
   if (per_sm < 1) per_sm = 1;
